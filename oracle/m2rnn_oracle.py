@@ -1,0 +1,127 @@
+"""Float64 CPU oracle for the M2RNN forward scan and its backward-through-time.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path imports this module:
+only the test-suite, the smoke check of the package entry module and the
+CPU-baseline leg of the benchmark call it.  It shares no code with the CUDA
+library; both consume the same seeded inputs (float64 values of the stored
+bf16/fp32 data).
+
+Source: reading notes on "M2RNN: Non-Linear RNNs with Matrix-Valued States for
+Scalable Language Modeling" (Mishra, Tan, Stoica, Gonzalez, Dao;
+arXiv:2603.14360v2), section 2.1 (the paper's Eq. 10-12) for the forward and
+section 2.7 (the notes' chain-rule correction of the paper's Algorithm 2) for
+the backward.
+
+Notation (per batch element b and head n, from H_0 = 0):
+    Z_t = tanh(H_{t-1} W + k_t v_t^T)            (Eq. 10)
+    H_t = f_t H_{t-1} + (1 - f_t) Z_t            (Eq. 11)
+    y_t = H_t^T q_t + w_r * v_t                  (Eq. 12)
+H, Z are K x V; W is V x V and multiplies from the right, so
+(H W)_{ij} = sum_m H_{im} W_{mj}; q_t, k_t have K entries, v_t and w_r have V;
+f_t is a scalar.  Array layouts: q, k [B,T,N,K]; v [B,T,N,V]; f [B,T,N];
+W [N,V,V]; w_r [N,V]; y, dy [B,T,N,V]; H_T, dH_T [B,N,K,V].
+
+Every function is a plain loop over t, vectorised over (b, n) with numpy
+matmul/einsum; there is no blocking, fusion or reordering beyond the equations.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def _as64(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+def forward(q, k, v, f, W, w_r, return_states: bool = False):
+    """M2RNN forward scan (Eq. 10-12) from H_0 = 0.
+
+    Returns (y [B,T,N,V], H_T [B,N,K,V]); with ``return_states`` also the
+    stacked H_t and Z_t, shape [T+1,B,N,K,V] (index 0 holds H_0 = 0) and
+    [T,B,N,K,V] (index t-1 holds Z_t).
+    """
+    q, k, v, f, W, w_r = map(_as64, (q, k, v, f, W, w_r))
+    B, T, N, K = q.shape
+    V = v.shape[-1]
+    H = np.zeros((B, N, K, V))
+    y = np.empty((B, T, N, V))
+    if return_states:
+        Hs = np.empty((T + 1, B, N, K, V))
+        Zs = np.empty((T, B, N, K, V))
+        Hs[0] = H
+    for t in range(T):
+        kt, vt, qt = k[:, t], v[:, t], q[:, t]           # [B,N,K], [B,N,V], [B,N,K]
+        ft = f[:, t][:, :, None, None]                    # [B,N,1,1]
+        # Eq. 10: transform the old state by W (right multiplication), add the
+        # rank-1 write k_t v_t^T, squash elementwise.
+        A = np.matmul(H, W[None]) + kt[..., :, None] * vt[..., None, :]
+        Z = np.tanh(A)
+        # Eq. 11: gate blend between the retained and the candidate state.
+        H = ft * H + (1.0 - ft) * Z
+        # Eq. 12: read out along the K rows with q_t, plus the value residual.
+        y[:, t] = np.einsum("bnkv,bnk->bnv", H, qt) + w_r[None] * vt
+        if return_states:
+            Hs[t + 1] = H
+            Zs[t] = Z
+    if return_states:
+        return y, H, Hs, Zs
+    return y, H
+
+
+def backward(q, k, v, f, W, w_r, dy, dH_T=None):
+    """Gradients of L = sum(dy * y) + <dH_T, H_T> with respect to every input.
+
+    Follows the chain rule for Eq. 10-12 as derived in section 2.7 of the
+    reading notes, with u_t the upstream gradient of the readout H_t^T q_t
+    (equal to dy_t, since the value residual w_r*v_t enters y_t additively)
+    and C_t the state gradient flowing back from steps after t (C_T = dH_T):
+        R_t     = C_t + q_t u_t^T
+        D_t     = ((1 - f_t) R_t) * (1 - Z_t * Z_t)
+        C_{t-1} = f_t R_t + D_t W^T
+        dq_t = H_t u_t          dk_t = D_t v_t
+        dv_t = D_t^T k_t + w_r * u_t
+        df_t = <R_t, H_{t-1} - Z_t>_F
+        dW   = sum over b, t of H_{t-1}^T D_t
+        dw_r = sum over b, t of u_t * v_t
+    The value-residual terms (w_r * u_t in dv, and dw_r) are the direct-path
+    contributions that the notes tell the reader to restore.
+
+    Returns a dict with dq, dk [B,T,N,K]; dv [B,T,N,V]; df [B,T,N];
+    dW [N,V,V]; dw_r [N,V]; all float64.
+    """
+    q, k, v, f, W, w_r, dy = map(_as64, (q, k, v, f, W, w_r, dy))
+    B, T, N, K = q.shape
+    V = v.shape[-1]
+    _, _, Hs, Zs = forward(q, k, v, f, W, w_r, return_states=True)
+    C = np.zeros((B, N, K, V)) if dH_T is None else _as64(dH_T).copy()
+    dq = np.empty((B, T, N, K))
+    dk = np.empty((B, T, N, K))
+    dv = np.empty((B, T, N, V))
+    df = np.empty((B, T, N))
+    dW = np.zeros((N, V, V))
+    dw_r = np.zeros((N, V))
+    Wt = np.swapaxes(W, -1, -2)[None]                      # [1,N,V,V] = W^T
+    for t in range(T - 1, -1, -1):
+        u = dy[:, t]                                        # [B,N,V]
+        qt, kt, vt = q[:, t], k[:, t], v[:, t]
+        ft = f[:, t][:, :, None, None]
+        H_prev, H_t, Z = Hs[t], Hs[t + 1], Zs[t]
+        R = C + qt[..., :, None] * u[..., None, :]
+        D = ((1.0 - ft) * R) * (1.0 - Z * Z)
+        dq[:, t] = np.einsum("bnkv,bnv->bnk", H_t, u)
+        dk[:, t] = np.einsum("bnkv,bnv->bnk", D, vt)
+        dv[:, t] = np.einsum("bnkv,bnk->bnv", D, kt) + w_r[None] * u
+        df[:, t] = np.einsum("bnkv,bnkv->bn", R, H_prev - Z)
+        dW += np.einsum("bnkm,bnkj->nmj", H_prev, D)
+        dw_r += np.einsum("bnv,bnv->nv", u, vt)
+        C = ft * R + np.matmul(D, Wt)
+    return dict(dq=dq, dk=dk, dv=dv, df=df, dW=dW, dw_r=dw_r)
+
+
+def loss(q, k, v, f, W, w_r, dy, dH_T=None):
+    """Scalar L = sum(dy * y) + <dH_T, H_T>, the function ``backward`` differentiates."""
+    y, H_T = forward(q, k, v, f, W, w_r)
+    val = float(np.sum(_as64(dy) * y))
+    if dH_T is not None:
+        val += float(np.sum(_as64(dH_T) * H_T))
+    return val
