@@ -1,0 +1,147 @@
+/*
+ * m2rnn.h -- C ABI of the GB300 M2RNN scan library (libm2rnn.so).
+ *
+ * The operation is the matrix-state non-linear recurrence of "M2RNN:
+ * Non-Linear RNNs with Matrix-Valued States for Scalable Language Modeling"
+ * (reading notes, section 2.1, the paper's Eq. 10-12), per batch element b
+ * and head n, from H_0 = 0:
+ *
+ *     Z_t = tanh(H_{t-1} W + k_t v_t^T)          H, Z: K x V;  W: V x V
+ *     H_t = f_t H_{t-1} + (1 - f_t) Z_t          f_t: scalar in [0, 1]
+ *     y_t = H_t^T q_t + w_r (*) v_t              q_t, k_t: K;  v_t, w_r, y_t: V
+ *
+ * and its backward-through-time (notes section 2.7, the chain-rule
+ * correction of the paper's Algorithm 2; see m2rnn_backward).
+ *
+ * Conventions shared by every entry point
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller, dense and
+ *    row-major in the layout given, 16-byte aligned.  The library allocates
+ *    no memory; all scratch comes from the caller's workspace.
+ *  - Layouts: q, k [B,T,N,K]; v [B,T,N,V]; f [B,T,N]; W [N,V,V] with
+ *    W[n][m][j] the coefficient from state column m to column j (so
+ *    (H W)_{ij} = sum_m H_{im} W_{mj}); w_r [N,V]; y, dy [B,T,N,V];
+ *    H_T, dH_T [B,N,K,V]; checkpoints [B,N,n_ckpt,K,V] (see below).
+ *  - q, k, v, f, W and w_r all have the element type `dtype`.  Every output,
+ *    the upstream gradients and the state are float32.
+ *  - Calls are asynchronous and ordered on `cuda_stream` (a cudaStream_t;
+ *    NULL = legacy default stream).  The return value reports argument
+ *    errors, unsupported shapes and launch/CUDA errors.  Errors that only the
+ *    device can see (a bounded wait that gave up, a failed bounds check) are
+ *    recorded in the workspace status block and reported by
+ *    m2rnn_sync_status.
+ *  - Supported shapes: B, T, N >= 1; K, V in [1, 128].  bf16 inputs with
+ *    V in {64, 128} and K a multiple of 16 (and at most 128) run on the
+ *    tensor-core (tcgen05) kernels; every other supported shape runs on the
+ *    fp32 CUDA-core kernels.  Nothing runs on the host CPU.
+ */
+#ifndef M2RNN_H_
+#define M2RNN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  M2RNN_OK = 0,
+  M2RNN_ERR_INVALID_ARG = -1, /* NULL/misaligned pointer, bad size or flag  */
+  M2RNN_ERR_UNSUPPORTED = -2, /* shape/dtype outside the supported set      */
+  M2RNN_ERR_WORKSPACE = -3,   /* workspace NULL or smaller than required    */
+  M2RNN_ERR_CUDA = -4,        /* a CUDA runtime/driver call failed          */
+  M2RNN_ERR_TIMEOUT = -5,     /* device: a bounded wait gave up             */
+  M2RNN_ERR_DEVICE = -6       /* device: an internal check failed           */
+} m2rnn_status;
+
+typedef enum { M2RNN_F32 = 0, M2RNN_BF16 = 1 } m2rnn_dtype;
+
+/* Library version, as MAJOR*10000 + MINOR*100 + PATCH. */
+int m2rnn_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* m2rnn_status_string(int status);
+
+/* Number of stored checkpoints for T steps taken every `ckpt_every` steps:
+ * (T - 1) / ckpt_every.  Checkpoint c (0-based) holds the fp32 state
+ * H_{(c+1) * ckpt_every}, i.e. the state at the start of chunk c+1; chunk 0
+ * starts from H_0 = 0, which is never stored.  Returns -1 on bad arguments. */
+int64_t m2rnn_checkpoint_count(int64_t T, int ckpt_every);
+
+/* Bytes of device workspace m2rnn_forward needs (at least the 256-byte
+ * status block).  0 on bad arguments. */
+size_t m2rnn_forward_workspace_size(int64_t B, int64_t T, int64_t N, int64_t K,
+                                    int64_t V, m2rnn_dtype dtype);
+
+/* Bytes of device workspace m2rnn_backward needs.  `have_ckpt` != 0 means the
+ * caller will pass the forward's checkpoints; otherwise the workspace also
+ * holds the checkpoints the backward recomputes.  0 on bad arguments. */
+size_t m2rnn_backward_workspace_size(int64_t B, int64_t T, int64_t N, int64_t K,
+                                     int64_t V, m2rnn_dtype dtype, int ckpt_every,
+                                     int have_ckpt);
+
+/*
+ * Forward scan (Eq. 10-12 from H_0 = 0).
+ *   in : q, k, v, f, W, w_r      (dtype, layouts above)
+ *   out: y   [B,T,N,V] fp32      (required)
+ *        H_T [B,N,K,V] fp32      (may be NULL)
+ *        ckpt [B,N,n_ckpt,K,V] fp32, n_ckpt = m2rnn_checkpoint_count(T,
+ *             ckpt_every)        (may be NULL; ckpt_every is ignored then)
+ *   workspace: >= m2rnn_forward_workspace_size(...) bytes of device memory,
+ *        16-byte aligned; its status block is cleared by this call.
+ * Outputs are overwritten.  Inputs are not modified.  Concurrent calls that
+ * share a workspace race on its status block.
+ */
+int m2rnn_forward(const void* q, const void* k, const void* v, const void* f,
+                  const void* W, const void* w_r, float* y, float* H_T,
+                  float* ckpt, int ckpt_every, int64_t B, int64_t T, int64_t N,
+                  int64_t K, int64_t V, m2rnn_dtype dtype, void* workspace,
+                  size_t workspace_bytes, void* cuda_stream);
+
+/*
+ * Backward through time: gradients of L = sum(dy * y) + <dH_T, H_T> with
+ * respect to every input (notes section 2.7, with the value-residual terms
+ * restored):  u_t = dy_t,  C_T = dH_T,
+ *     R_t = C_t + q_t u_t^T
+ *     D_t = ((1 - f_t) R_t) (*) (1 - Z_t (*) Z_t)
+ *     C_{t-1} = f_t R_t + D_t W^T
+ *     dq_t = H_t u_t        dk_t = D_t v_t        dv_t = D_t^T k_t + w_r (*) u_t
+ *     df_t = <R_t, H_{t-1} - Z_t>_F
+ *     dW[n] = sum_{b,t} H_{t-1}^T D_t      dw_r[n] = sum_{b,t} u_t (*) v_t
+ *   in : q, k, v, f, W, w_r (dtype); dy [B,T,N,V] fp32 (required);
+ *        dH_T [B,N,K,V] fp32 (may be NULL = zero);
+ *        ckpt: the forward's checkpoints for the same ckpt_every (may be NULL:
+ *        they are recomputed into the workspace).
+ *   out: dq, dk [B,T,N,K]; dv [B,T,N,V]; df [B,T,N]; dW [N,V,V]; dw_r [N,V];
+ *        all fp32, all required, overwritten (not accumulated).
+ *   ckpt_every: chunk length of the recompute, 1 <= ckpt_every <= 4096.
+ *   workspace: >= m2rnn_backward_workspace_size(...) bytes.
+ * dW and dw_r are reduced over b in a fixed order: results are bitwise
+ * reproducible run to run.
+ */
+int m2rnn_backward(const void* q, const void* k, const void* v, const void* f,
+                   const void* W, const void* w_r, const float* dy,
+                   const float* dH_T, const float* ckpt, int ckpt_every,
+                   float* dq, float* dk, float* dv, float* df, float* dW,
+                   float* dw_r, int64_t B, int64_t T, int64_t N, int64_t K,
+                   int64_t V, m2rnn_dtype dtype, void* workspace,
+                   size_t workspace_bytes, void* cuda_stream);
+
+/*
+ * Synchronises `cuda_stream`, then reads and clears the workspace status
+ * block that the last call on this workspace wrote.  Returns M2RNN_OK,
+ * M2RNN_ERR_TIMEOUT or M2RNN_ERR_DEVICE; `detail` (may be NULL) receives an
+ * implementation-defined location code of the first device error.
+ */
+int m2rnn_sync_status(void* workspace, void* cuda_stream, uint32_t* detail);
+
+/* Which kernel family a call with these arguments would run:
+ * 1 = tensor-core (tcgen05) kernels, 0 = fp32 CUDA-core kernels,
+ * negative = the status the call would return. */
+int m2rnn_path(int64_t K, int64_t V, m2rnn_dtype dtype);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* M2RNN_H_ */

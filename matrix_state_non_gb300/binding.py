@@ -1,0 +1,247 @@
+"""Thin ctypes binding of libm2rnn.so (include/m2rnn.h).
+
+The ``m2rnn_*`` functions mirror the C ABI one to one (raw device pointers and
+sizes).  ``forward`` / ``backward`` are torch conveniences on top: they take
+contiguous CUDA tensors, allocate outputs and the workspace with torch (device
+memory and streams are all torch is used for) and call the C ABI on the
+current stream.  Every step of both scans runs in the library's CUDA kernels;
+there is no CPU path.  Loading fails loudly when the library is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libm2rnn.so")
+
+M2RNN_OK = 0
+M2RNN_ERR_INVALID_ARG = -1
+M2RNN_ERR_UNSUPPORTED = -2
+M2RNN_ERR_WORKSPACE = -3
+M2RNN_ERR_CUDA = -4
+M2RNN_ERR_TIMEOUT = -5
+M2RNN_ERR_DEVICE = -6
+M2RNN_F32 = 0
+M2RNN_BF16 = 1
+
+EXPORTS = (
+    "m2rnn_version", "m2rnn_status_string", "m2rnn_checkpoint_count", "m2rnn_path",
+    "m2rnn_forward_workspace_size", "m2rnn_backward_workspace_size", "m2rnn_forward",
+    "m2rnn_backward", "m2rnn_sync_status",
+)
+
+_lib = None
+
+
+class M2RNNError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+def load() -> ctypes.CDLL:
+    """Load libm2rnn.so (built in-tree); raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build it with `python -m matrix_state_non_gb300.build` "
+            "(there is no fallback implementation)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i64, ci, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    lib.m2rnn_version.restype = ci
+    lib.m2rnn_version.argtypes = []
+    lib.m2rnn_status_string.restype = ctypes.c_char_p
+    lib.m2rnn_status_string.argtypes = [ci]
+    lib.m2rnn_checkpoint_count.restype = i64
+    lib.m2rnn_checkpoint_count.argtypes = [i64, ci]
+    lib.m2rnn_path.restype = ci
+    lib.m2rnn_path.argtypes = [i64, i64, ci]
+    lib.m2rnn_forward_workspace_size.restype = sz
+    lib.m2rnn_forward_workspace_size.argtypes = [i64, i64, i64, i64, i64, ci]
+    lib.m2rnn_backward_workspace_size.restype = sz
+    lib.m2rnn_backward_workspace_size.argtypes = [i64, i64, i64, i64, i64, ci, ci, ci]
+    lib.m2rnn_forward.restype = ci
+    lib.m2rnn_forward.argtypes = [vp] * 9 + [ci] + [i64] * 5 + [ci, vp, sz, vp]
+    lib.m2rnn_backward.restype = ci
+    lib.m2rnn_backward.argtypes = [vp] * 9 + [ci] + [vp] * 6 + [i64] * 5 + [ci, vp, sz, vp]
+    lib.m2rnn_sync_status.restype = ci
+    lib.m2rnn_sync_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+    _lib = lib
+    return lib
+
+
+# ---------------------------------------------------------------------------
+# One-to-one wrappers of the C ABI (integers are device addresses).
+# ---------------------------------------------------------------------------
+def m2rnn_version() -> int:
+    return load().m2rnn_version()
+
+
+def status_string(status: int) -> str:
+    return load().m2rnn_status_string(status).decode()
+
+
+m2rnn_status_string = status_string
+
+
+def m2rnn_checkpoint_count(T: int, ckpt_every: int) -> int:
+    return load().m2rnn_checkpoint_count(T, ckpt_every)
+
+
+def m2rnn_path(K: int, V: int, dtype: int) -> int:
+    return load().m2rnn_path(K, V, dtype)
+
+
+def m2rnn_forward_workspace_size(B, T, N, K, V, dtype) -> int:
+    return load().m2rnn_forward_workspace_size(B, T, N, K, V, dtype)
+
+
+def m2rnn_backward_workspace_size(B, T, N, K, V, dtype, ckpt_every, have_ckpt) -> int:
+    return load().m2rnn_backward_workspace_size(B, T, N, K, V, dtype, ckpt_every, int(bool(have_ckpt)))
+
+
+def m2rnn_forward(q, k, v, f, W, w_r, y, H_T, ckpt, ckpt_every, B, T, N, K, V, dtype,
+                  workspace, workspace_bytes, stream) -> int:
+    return load().m2rnn_forward(q, k, v, f, W, w_r, y, H_T, ckpt, ckpt_every, B, T, N, K, V,
+                                dtype, workspace, workspace_bytes, stream)
+
+
+def m2rnn_backward(q, k, v, f, W, w_r, dy, dH_T, ckpt, ckpt_every, dq, dk, dv, df, dW, dw_r,
+                   B, T, N, K, V, dtype, workspace, workspace_bytes, stream) -> int:
+    return load().m2rnn_backward(q, k, v, f, W, w_r, dy, dH_T, ckpt, ckpt_every, dq, dk, dv,
+                                 df, dW, dw_r, B, T, N, K, V, dtype, workspace,
+                                 workspace_bytes, stream)
+
+
+def m2rnn_sync_status(workspace, stream):
+    """Returns (status, detail)."""
+    d = ctypes.c_uint32(0)
+    st = load().m2rnn_sync_status(workspace, stream, ctypes.byref(d))
+    return st, d.value
+
+
+# ---------------------------------------------------------------------------
+# torch conveniences
+# ---------------------------------------------------------------------------
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return M2RNN_BF16
+    if t.dtype == torch.float32:
+        return M2RNN_F32
+    raise TypeError(f"unsupported input dtype {t.dtype}")
+
+
+def _check(st: int, what: str):
+    if st != M2RNN_OK:
+        raise M2RNNError(st, what)
+
+
+def _stream_handle(stream) -> int:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _shapes(q, v):
+    B, T, N, K = q.shape
+    V = v.shape[-1]
+    return B, T, N, K, V
+
+
+def forward(q, k, v, f, W, w_r, *, want_state: bool = True, ckpt_every: int = 0,
+            out=None, workspace=None, stream=None):
+    """Forward scan on the GPU.  Returns dict(y, H_T[, ckpt]).
+
+    ``ckpt_every`` > 0 also writes the checkpoints the backward can reuse.
+    ``out`` may hold preallocated y / H_T / ckpt tensors.
+    """
+    import torch
+    B, T, N, K, V = _shapes(q, v)
+    dt = _dtype_code(q)
+    dev = q.device
+    out = dict(out or {})
+    y = out.get("y")
+    if y is None:
+        y = torch.empty((B, T, N, V), device=dev, dtype=torch.float32)
+    H_T = out.get("H_T")
+    if H_T is None and want_state:
+        H_T = torch.empty((B, N, K, V), device=dev, dtype=torch.float32)
+    ckpt = out.get("ckpt")
+    if ckpt is None and ckpt_every > 0:
+        nck = m2rnn_checkpoint_count(T, ckpt_every)
+        ckpt = torch.empty((B, N, max(nck, 0), K, V), device=dev, dtype=torch.float32)
+    ws_bytes = m2rnn_forward_workspace_size(B, T, N, K, V, dt)
+    if ws_bytes == 0:
+        raise M2RNNError(M2RNN_ERR_INVALID_ARG, "m2rnn_forward_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
+    st = m2rnn_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(f), _ptr(W), _ptr(w_r), _ptr(y),
+                       _ptr(H_T), _ptr(ckpt), ckpt_every if ckpt is not None else 0,
+                       B, T, N, K, V, dt, _ptr(workspace), workspace.numel(),
+                       _stream_handle(stream))
+    _check(st, "m2rnn_forward")
+    res = dict(y=y, H_T=H_T, workspace=workspace)
+    if ckpt is not None:
+        res["ckpt"] = ckpt
+    return res
+
+
+def backward(q, k, v, f, W, w_r, dy, *, dH_T=None, ckpt=None, ckpt_every: int = 64,
+             out=None, workspace=None, stream=None):
+    """Backward scan on the GPU.  Returns dict(dq, dk, dv, df, dW, dw_r)."""
+    import torch
+    B, T, N, K, V = _shapes(q, v)
+    dt = _dtype_code(q)
+    dev = q.device
+    out = dict(out or {})
+
+    def _get(name, shape):
+        t = out.get(name)
+        return t if t is not None else torch.empty(shape, device=dev, dtype=torch.float32)
+
+    dq = _get("dq", (B, T, N, K))
+    dk = _get("dk", (B, T, N, K))
+    dv = _get("dv", (B, T, N, V))
+    df = _get("df", (B, T, N))
+    dW = _get("dW", (N, V, V))
+    dw_r = _get("dw_r", (N, V))
+    ws_bytes = m2rnn_backward_workspace_size(B, T, N, K, V, dt, ckpt_every, ckpt is not None)
+    if ws_bytes == 0:
+        raise M2RNNError(M2RNN_ERR_INVALID_ARG, "m2rnn_backward_workspace_size")
+    if workspace is None or workspace.numel() < ws_bytes:
+        workspace = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
+    st = m2rnn_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(f), _ptr(W), _ptr(w_r), _ptr(dy),
+                        _ptr(dH_T), _ptr(ckpt), ckpt_every, _ptr(dq), _ptr(dk), _ptr(dv),
+                        _ptr(df), _ptr(dW), _ptr(dw_r), B, T, N, K, V, dt, _ptr(workspace),
+                        workspace.numel(), _stream_handle(stream))
+    _check(st, "m2rnn_backward")
+    return dict(dq=dq, dk=dk, dv=dv, df=df, dW=dW, dw_r=dw_r, workspace=workspace)
+
+
+def sync_status(workspace, stream=None):
+    st, detail = m2rnn_sync_status(workspace.data_ptr(), _stream_handle(stream))
+    return st, detail
+
+
+def to_device(inp, device="cuda"):
+    """Upload an ``inputs.M2RNNInputs`` batch: bf16 bit patterns become
+    torch.bfloat16 tensors, float32 stays float32."""
+    import numpy as np
+    import torch
+    res = {}
+    for name, arr in inp.store.items():
+        if arr.dtype == np.uint16:
+            t = torch.from_numpy(arr.view(np.int16).copy()).view(torch.bfloat16)
+        else:
+            t = torch.from_numpy(np.ascontiguousarray(arr))
+        res[name] = t.to(device).contiguous()
+    return res

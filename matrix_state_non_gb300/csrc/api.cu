@@ -1,0 +1,212 @@
+// C-ABI entry points of libm2rnn.so (declared in include/m2rnn.h): argument
+// validation, workspace carving and kernel dispatch.  Every step of both
+// scans runs in this library's CUDA kernels; nothing runs on the host CPU.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <cstring>
+
+#include "internal.h"
+
+using namespace m2rnn;
+
+namespace {
+
+constexpr size_t kStatusBytes = sizeof(StatusBlock);
+constexpr int kMaxDim = 128;
+constexpr int kMaxCkptEvery = 4096;
+
+inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool dims_ok(int64_t B, int64_t T, int64_t N, int64_t K, int64_t V) {
+  if (B < 1 || T < 1 || N < 1 || K < 1 || V < 1) return false;
+  if (B > INT_MAX / 8 || T > INT_MAX || N > INT_MAX / 8) return false;
+  if (B * N > INT_MAX / 8) return false;
+  return true;
+}
+
+bool dtype_ok(int dt) { return dt == M2RNN_F32 || dt == M2RNN_BF16; }
+
+// Which family runs: 1 = tcgen05, 0 = SIMT fp32, <0 = error.
+int choose_path(int64_t K, int64_t V, int dt) {
+  if (!dtype_ok(dt)) return M2RNN_ERR_INVALID_ARG;
+  if (K < 1 || V < 1) return M2RNN_ERR_INVALID_ARG;
+  if (K > kMaxDim || V > kMaxDim) return M2RNN_ERR_UNSUPPORTED;
+  if (dt == M2RNN_BF16 && tc_forward_supported(static_cast<int>(K), static_cast<int>(V))) return 1;
+  return 0;
+}
+
+struct BwdLayout {
+  size_t ckpt_off, dwp_off, dwrp_off, scratch_off, total;
+};
+
+BwdLayout bwd_layout(int64_t B, int64_t T, int64_t N, int64_t K, int64_t V, int dt, int C,
+                     bool have_ckpt) {
+  BwdLayout l{};
+  const int path = choose_path(K, V, dt);
+  const int64_t nck = (T - 1) / C;
+  size_t off = kStatusBytes;
+  l.ckpt_off = off;
+  if (!have_ckpt) off = align256(off + sizeof(float) * static_cast<size_t>(B * N * nck * K * V));
+  const int parts = (path == 1 && tc_backward_supported(static_cast<int>(K), static_cast<int>(V)))
+                        ? tc_backward_parts(static_cast<int>(K), static_cast<int>(V))
+                        : 1;
+  l.dwp_off = off;
+  off = align256(off + sizeof(float) * static_cast<size_t>(B * N * parts * V * V));
+  l.dwrp_off = off;
+  off = align256(off + sizeof(float) * static_cast<size_t>(B * N * V));
+  l.scratch_off = off;
+  if (path == 1 && tc_backward_supported(static_cast<int>(K), static_cast<int>(V)))
+    off = align256(off + tc_backward_scratch_bytes(static_cast<int>(B), static_cast<int>(N),
+                                                   static_cast<int>(K), static_cast<int>(V), C));
+  else
+    off = align256(off + simt_backward_scratch_bytes(static_cast<int>(B), static_cast<int>(N),
+                                                     static_cast<int>(K), static_cast<int>(V), C));
+  l.total = off;
+  return l;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int m2rnn_version(void) { return 10000; }
+
+const char* m2rnn_status_string(int status) {
+  switch (status) {
+    case M2RNN_OK: return "ok";
+    case M2RNN_ERR_INVALID_ARG: return "invalid argument";
+    case M2RNN_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case M2RNN_ERR_WORKSPACE: return "workspace missing or too small";
+    case M2RNN_ERR_CUDA: return "CUDA error";
+    case M2RNN_ERR_TIMEOUT: return "device wait timed out";
+    case M2RNN_ERR_DEVICE: return "device-side check failed";
+    default: return "unknown status";
+  }
+}
+
+int64_t m2rnn_checkpoint_count(int64_t T, int ckpt_every) {
+  if (T < 1 || ckpt_every < 1) return -1;
+  return (T - 1) / ckpt_every;
+}
+
+int m2rnn_path(int64_t K, int64_t V, m2rnn_dtype dtype) { return choose_path(K, V, dtype); }
+
+size_t m2rnn_forward_workspace_size(int64_t B, int64_t T, int64_t N, int64_t K, int64_t V,
+                                    m2rnn_dtype dtype) {
+  if (!dims_ok(B, T, N, K, V) || choose_path(K, V, dtype) < 0) return 0;
+  return kStatusBytes;
+}
+
+size_t m2rnn_backward_workspace_size(int64_t B, int64_t T, int64_t N, int64_t K, int64_t V,
+                                     m2rnn_dtype dtype, int ckpt_every, int have_ckpt) {
+  if (!dims_ok(B, T, N, K, V) || choose_path(K, V, dtype) < 0) return 0;
+  if (ckpt_every < 1 || ckpt_every > kMaxCkptEvery) return 0;
+  return bwd_layout(B, T, N, K, V, dtype, ckpt_every, have_ckpt != 0).total;
+}
+
+int m2rnn_forward(const void* q, const void* k, const void* v, const void* f, const void* W,
+                  const void* w_r, float* y, float* H_T, float* ckpt, int ckpt_every, int64_t B,
+                  int64_t T, int64_t N, int64_t K, int64_t V, m2rnn_dtype dtype, void* workspace,
+                  size_t workspace_bytes, void* cuda_stream) {
+  if (!dtype_ok(dtype) || !dims_ok(B, T, N, K, V)) return M2RNN_ERR_INVALID_ARG;
+  const int path = choose_path(K, V, dtype);
+  if (path < 0) return path;
+  const void* req[] = {q, k, v, f, W, w_r, y};
+  for (const void* p : req)
+    if (p == nullptr || !aligned16(p)) return M2RNN_ERR_INVALID_ARG;
+  if ((H_T && !aligned16(H_T)) || (ckpt && !aligned16(ckpt))) return M2RNN_ERR_INVALID_ARG;
+  if (ckpt && (ckpt_every < 1 || ckpt_every > kMaxCkptEvery)) return M2RNN_ERR_INVALID_ARG;
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < kStatusBytes)
+    return M2RNN_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  StatusBlock* status = static_cast<StatusBlock*>(workspace);
+  cudaError_t e = cudaMemsetAsync(status, 0, kStatusBytes, s);
+  if (e != cudaSuccess) return M2RNN_ERR_CUDA;
+  FwdArgs a{};
+  a.q = q; a.k = k; a.v = v; a.f = f; a.W = W; a.w_r = w_r;
+  a.y = y; a.H_T = H_T; a.ckpt = ckpt;
+  a.ckpt_every = ckpt ? ckpt_every : 1;
+  a.n_ckpt = ckpt ? (T - 1) / ckpt_every : 0;
+  a.B = static_cast<int>(B); a.T = static_cast<int>(T); a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K); a.V = static_cast<int>(V);
+  a.dtype = dtype;
+  a.status = status;
+  e = (path == 1) ? launch_tc_forward(a, s) : launch_simt_forward(a, s);
+  return cuda_status(e);
+}
+
+int m2rnn_backward(const void* q, const void* k, const void* v, const void* f, const void* W,
+                   const void* w_r, const float* dy, const float* dH_T, const float* ckpt,
+                   int ckpt_every, float* dq, float* dk, float* dv, float* df, float* dW,
+                   float* dw_r, int64_t B, int64_t T, int64_t N, int64_t K, int64_t V,
+                   m2rnn_dtype dtype, void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  if (!dtype_ok(dtype) || !dims_ok(B, T, N, K, V)) return M2RNN_ERR_INVALID_ARG;
+  const int path = choose_path(K, V, dtype);
+  if (path < 0) return path;
+  if (ckpt_every < 1 || ckpt_every > kMaxCkptEvery) return M2RNN_ERR_INVALID_ARG;
+  const void* req[] = {q, k, v, f, W, w_r, dy, dq, dk, dv, df, dW, dw_r};
+  for (const void* p : req)
+    if (p == nullptr || !aligned16(p)) return M2RNN_ERR_INVALID_ARG;
+  if ((dH_T && !aligned16(dH_T)) || (ckpt && !aligned16(ckpt))) return M2RNN_ERR_INVALID_ARG;
+  const BwdLayout l = bwd_layout(B, T, N, K, V, dtype, ckpt_every, ckpt != nullptr);
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < l.total)
+    return M2RNN_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  StatusBlock* status = reinterpret_cast<StatusBlock*>(ws);
+  cudaError_t e = cudaMemsetAsync(status, 0, kStatusBytes, s);
+  if (e != cudaSuccess) return M2RNN_ERR_CUDA;
+  const int64_t nck = (T - 1) / ckpt_every;
+  float* ck = const_cast<float*>(ckpt);
+  if (ck == nullptr) {
+    ck = reinterpret_cast<float*>(ws + l.ckpt_off);
+    if (nck > 0) {
+      // Checkpoint pass: the forward without the readout.
+      FwdArgs fa{};
+      fa.q = q; fa.k = k; fa.v = v; fa.f = f; fa.W = W; fa.w_r = w_r;
+      fa.y = nullptr; fa.H_T = nullptr; fa.ckpt = ck;
+      fa.ckpt_every = ckpt_every; fa.n_ckpt = nck;
+      fa.B = static_cast<int>(B); fa.T = static_cast<int>(T); fa.N = static_cast<int>(N);
+      fa.K = static_cast<int>(K); fa.V = static_cast<int>(V);
+      fa.dtype = dtype; fa.status = status;
+      e = (path == 1) ? launch_tc_forward(fa, s) : launch_simt_forward(fa, s);
+      if (e != cudaSuccess) return M2RNN_ERR_CUDA;
+    }
+  }
+  BwdArgs a{};
+  a.q = q; a.k = k; a.v = v; a.f = f; a.W = W; a.w_r = w_r;
+  a.dy = dy; a.dH_T = dH_T; a.ckpt = ck; a.ckpt_every = ckpt_every; a.n_ckpt = nck;
+  a.dq = dq; a.dk = dk; a.dv = dv; a.df = df; a.dW = dW; a.dw_r = dw_r;
+  a.B = static_cast<int>(B); a.T = static_cast<int>(T); a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K); a.V = static_cast<int>(V);
+  a.dtype = dtype; a.status = status;
+  a.dW_part = reinterpret_cast<float*>(ws + l.dwp_off);
+  a.dwr_part = reinterpret_cast<float*>(ws + l.dwrp_off);
+  a.scratch = reinterpret_cast<float*>(ws + l.scratch_off);
+  const bool tc = path == 1 && tc_backward_supported(a.K, a.V);
+  a.parts = tc ? tc_backward_parts(a.K, a.V) : 1;
+  e = tc ? launch_tc_backward(a, s) : launch_simt_backward(a, s);
+  if (e != cudaSuccess) return M2RNN_ERR_CUDA;
+  return cuda_status(launch_reduce_partials(a, s));
+}
+
+int m2rnn_sync_status(void* workspace, void* cuda_stream, uint32_t* detail) {
+  if (workspace == nullptr || !aligned16(workspace)) return M2RNN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  StatusBlock host{};
+  if (cudaMemcpyAsync(&host, workspace, 8, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return M2RNN_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return M2RNN_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, 8, s) != cudaSuccess) return M2RNN_ERR_CUDA;
+  if (detail) *detail = host.detail;
+  if (host.code == 0) return M2RNN_OK;
+  return host.code == kStatusTimeout ? M2RNN_ERR_TIMEOUT : M2RNN_ERR_DEVICE;
+}
+
+}  // extern "C"

@@ -1,0 +1,75 @@
+// Internal launcher interface shared by the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/m2rnn.h"
+#include "status.cuh"
+
+namespace m2rnn {
+
+// Everything a forward launch needs, already validated by the C-ABI layer.
+struct FwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* f;
+  const void* W;
+  const void* w_r;
+  float* y;      // may be null (checkpoint-only pass)
+  float* H_T;    // may be null
+  float* ckpt;   // may be null
+  int ckpt_every;
+  int64_t n_ckpt;
+  int B, T, N, K, V;
+  m2rnn_dtype dtype;
+  StatusBlock* status;
+};
+
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* f;
+  const void* W;
+  const void* w_r;
+  const float* dy;
+  const float* dH_T;  // may be null
+  const float* ckpt;  // never null here (recomputed by the caller layer if needed)
+  int ckpt_every;
+  int64_t n_ckpt;
+  float* dq;
+  float* dk;
+  float* dv;
+  float* df;
+  float* dW;
+  float* dw_r;
+  int B, T, N, K, V;
+  m2rnn_dtype dtype;
+  StatusBlock* status;
+  // Scratch carved from the workspace by the C-ABI layer.
+  float* dW_part;    // [B*N*parts][V][V]
+  float* dwr_part;   // [B*N][V]
+  float* scratch;    // kernel-specific (SIMT: per-chain chunk states)
+  int parts;         // dW partials per chain
+};
+
+// fp32 CUDA-core kernels (any K, V in [1, 128]).
+cudaError_t launch_simt_forward(const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_simt_backward(const BwdArgs& a, cudaStream_t s);
+size_t simt_backward_scratch_bytes(int B, int N, int K, int V, int ckpt_every);
+
+// Fixed-order sum of per-chain partials over b (and parts): dW, dw_r.
+cudaError_t launch_reduce_partials(const BwdArgs& a, cudaStream_t s);
+
+// tcgen05 tensor-core kernels (bf16 inputs).
+bool tc_forward_supported(int K, int V);
+cudaError_t launch_tc_forward(const FwdArgs& a, cudaStream_t s);
+bool tc_backward_supported(int K, int V);
+int tc_backward_parts(int K, int V);
+size_t tc_backward_scratch_bytes(int B, int N, int K, int V, int ckpt_every);
+cudaError_t launch_tc_backward(const BwdArgs& a, cudaStream_t s);
+
+}  // namespace m2rnn

@@ -1,0 +1,519 @@
+// tcgen05 forward scan of the M2RNN recurrence for bf16 inputs, fp32 state.
+//
+// Recurrence (reading notes on "M2RNN: Non-Linear RNNs with Matrix-Valued
+// States for Scalable Language Modeling", section 2.1, Eq. 10-12):
+//   Z_t = tanh(H_{t-1} W + k_t v_t^T),  H_t = f_t H_{t-1} + (1-f_t) Z_t,
+//   y_t = H_t^T q_t + w_r * v_t.
+//
+// Work split.  Key rows never mix (notes section 1.2): every row of H is its
+// own vector recurrence sharing W.  A chain (b, n) is therefore split into R
+// row blocks of G*NR rows, one CTA each, the R CTAs of a chain forming one
+// thread-block cluster; only the readout y_t sums over rows, and that sum
+// crosses CTAs through distributed shared memory, off the serial chain.
+//
+// Per step, per group of NR rows (one warpgroup), the transform runs on the
+// tensor core in transposed form
+//     D^T [V x NR] = W^T [V x V] * H_{t-1}^T [V x NR]      (M = 128, N = NR, K = V)
+// with A = W^T staged once (stacked 128/V times to fill M = 128, so the V = 64
+// case keeps all four TMEM lane quadrants busy), B = bf16(H_{t-1}) rewritten
+// every step, D in TMEM.  TMEM lane L holds value column j = L mod V, so each
+// thread owns a column j and ROWS rows of the state in fp32 registers: the
+// rank-1 add, tanh, gate blend and the readout over its rows are all
+// thread-local.  The bf16 copy of H_t goes back to shared memory as the next
+// MMA's B operand (MN-major: the thread's ROWS values are 16-byte runs).
+//
+// Warp roles: warps 0..4G-1 = G epilogue warpgroups (group g issues its own
+// MMAs from one elected thread); warp 4G = TMA producer for q/k/v tiles of
+// S = 32 steps (f through plain loads); warp 4G+1 = readout reducer, which
+// sums the per-group/per-CTA partial readouts of a tile, adds w_r * v and
+// stores y.  Every wait is bounded (see ptx.cuh).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace m2rnn {
+namespace {
+
+constexpr int kS = 32;   // steps per input tile (one f value per producer lane)
+constexpr int kYS = 2;   // readout partial stages
+
+template <int V_, int ROWS_>
+struct FwdCfg {
+  static constexpr int V = V_;
+  static constexpr int ROWS = ROWS_;            // state rows per thread
+  static constexpr int COPIES = 128 / V;        // W^T stacked to fill M = 128
+  static constexpr int NR = ROWS * COPIES;      // rows per group = MMA N
+  static constexpr int NS = (V == 64) ? 4 : 3;  // input pipeline stages
+  static constexpr int KSTEPS = V / 16;         // MMAs per step (K = 16 each)
+  static constexpr uint32_t A_BYTES = 128u * V * 2u;
+  static constexpr uint32_t B_BYTES = NR * V * 2u;
+  static constexpr uint32_t SBO = V * 16u;  // next 8 rows (A) / next 8 columns (B)
+  static constexpr uint32_t LBO = 128u;     // next 8 K-elements
+  static_assert(ROWS % 8 == 0, "rows per thread come in 16-byte runs");
+  static_assert(NR % 16 == 0 && NR <= 256, "MMA N for M = 128");
+};
+
+struct TcFwdParams {
+  FwdArgs a;
+  int G, R, NRtot;
+  int ntiles;
+  uint32_t tmem_cols;
+  uint32_t b_off, stage_off, stage_bytes, q_off, k_off, v_off, f_off;
+  uint32_t y_off, bar_off, misc_off;
+  uint32_t tx_bytes;
+};
+
+__device__ __forceinline__ void unpack8_bf16(const uint4 w, float (&o)[8]) {
+  o[0] = __uint_as_float(w.x << 16);
+  o[1] = __uint_as_float(w.x & 0xFFFF0000u);
+  o[2] = __uint_as_float(w.y << 16);
+  o[3] = __uint_as_float(w.y & 0xFFFF0000u);
+  o[4] = __uint_as_float(w.z << 16);
+  o[5] = __uint_as_float(w.z & 0xFFFF0000u);
+  o[6] = __uint_as_float(w.w << 16);
+  o[7] = __uint_as_float(w.w & 0xFFFF0000u);
+}
+
+template <class C>
+__device__ __forceinline__ void issue_step_mma(uint32_t d_tmem, uint32_t a_base, uint32_t b_base,
+                                               uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < C::KSTEPS; ++kk) {
+    // K slice kk covers K-blocks 2kk and 2kk+1 (LBO apart) in both operands.
+    const uint64_t ad = smem_desc_noswizzle(a_base + kk * 2 * C::LBO, C::LBO, C::SBO);
+    const uint64_t bd = smem_desc_noswizzle(b_base + kk * 2 * C::LBO, C::LBO, C::SBO);
+    tc_mma_f16_ss(d_tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+template <int V, int ROWS>
+__global__ void __launch_bounds__(320, 1)
+    tc_forward_kernel(const __grid_constant__ TcFwdParams p, const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v) {
+  using C = FwdCfg<V, ROWS>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // Align the working base to 1 KB (the launch reserves the slack).
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int G = p.G, R = p.R, NRtot = p.NRtot;
+  const int T = p.a.T, N = p.a.N;
+  const int cta_rank = static_cast<int>(blockIdx.x) % R;
+  const int chain = static_cast<int>(blockIdx.x) / R;
+  const int b = chain / N, n = chain % N;
+  const int ntiles = p.ntiles;
+  const bool do_y = p.a.y != nullptr;
+  const int slots = G * C::COPIES;
+  StatusBlock* status = p.a.status;
+
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + p.b_off;
+  uint8_t* sStage = smem + p.stage_off;
+  float* sY = reinterpret_cast<float*>(smem + p.y_off);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.bar_off);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::NS;
+  uint64_t* dfull = bars + 2 * C::NS;
+  uint64_t* hready = dfull + G;
+  uint64_t* yfull = hready + G;
+  uint64_t* ypeer = yfull + kYS;
+  uint64_t* yempty = ypeer + kYS;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + p.misc_off);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.misc_off + 4);
+
+  // ---------------- set-up ----------------
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NS; ++i) {
+      mbar_init(smem_u32(&full[i]), 32);
+      mbar_init(smem_u32(&empty[i]), 4 * G);
+    }
+    for (int g = 0; g < G; ++g) {
+      mbar_init(smem_u32(&dfull[g]), 1);
+      mbar_init(smem_u32(&hready[g]), 4);
+    }
+    for (int i = 0; i < kYS; ++i) {
+      mbar_init(smem_u32(&yfull[i]), 4 * G);
+      mbar_init(smem_u32(&ypeer[i]), R);
+      mbar_init(smem_u32(&yempty[i]), R);
+    }
+    *abort_flag = 0;
+    fence_mbar_init_cluster();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
+    tmem_relinquish();
+  }
+  {
+    // A = [W^T; W^T; ...] (K-major, interleaved core matrices): A[row][m] = W[m][row mod V].
+    const uint16_t* W = static_cast<const uint16_t*>(p.a.W) + static_cast<int64_t>(n) * V * V;
+    for (int e = threadIdx.x; e < V * V; e += blockDim.x) {
+      const int m = e / V, j = e % V;
+      const uint16_t w = W[e];
+#pragma unroll
+      for (int c = 0; c < C::COPIES; ++c) {
+        const int row = c * V + j;
+        const uint32_t off = (row / 8) * C::SBO + (m / 8) * C::LBO + (row % 8) * 16 + (m % 8) * 2;
+        *reinterpret_cast<uint16_t*>(sA + off) = w;
+      }
+    }
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    for (uint32_t e = threadIdx.x * 16; e < static_cast<uint32_t>(G) * C::B_BYTES; e += blockDim.x * 16)
+      *reinterpret_cast<uint4*>(sB + e) = zero;  // H_0 = 0
+  }
+  fence_proxy_async_smem();
+  tc_fence_before_sync();
+  cluster_sync_all();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t idesc = idesc_bf16_f32(128, C::NR, /*a_mn_major=*/false, /*b_mn_major=*/true);
+  const uint32_t a_base = smem_u32(sA);
+
+  if (warp < 4 * G) {
+    // ---------------- epilogue warpgroups ----------------
+    const int g = warp / 4, wq = warp % 4;
+    const int L = 32 * wq + lane;
+    const int j = L % V, c = L / V;  // c is uniform within a warp
+    const int row_in_cta = g * C::NR + c * ROWS;
+    const int64_t row_global = static_cast<int64_t>(cta_rank) * NRtot + row_in_cta;
+    const uint32_t b_base = smem_u32(sB + g * C::B_BYTES);
+    const uint32_t dbar = smem_u32(&dfull[g]);
+    const uint32_t hbar = smem_u32(&hready[g]);
+    const uint32_t d_tmem = tmem_base + g * C::NR;
+    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * wq) << 16) + g * C::NR + c * ROWS;
+    uint8_t* bslot = sB + g * C::B_BYTES + ((c * ROWS) / 8) * C::SBO + (j / 8) * C::LBO + (j % 8) * 16;
+    const bool issuer = (wq == 0 && lane == 0);
+    if (issuer) {  // step 0's transform: H_0 W = 0 (keeps the loop uniform)
+      issue_step_mma<C>(d_tmem, a_base, b_base, idesc);
+      tc_commit(dbar);
+    }
+    float h[ROWS];
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) h[r] = 0.f;
+    uint32_t dphase = 0, hphase = 0;
+    bool ok = true;
+    for (int tile = 0; tile < ntiles && ok; ++tile) {
+      const int st = tile % C::NS;
+      if (!mbar_wait(smem_u32(&full[st]), (tile / C::NS) & 1, abort_flag, status, kWhereFwdFull)) {
+        ok = false;
+        break;
+      }
+      const int ys = tile % kYS;
+      if (do_y && tile >= kYS &&
+          !mbar_wait<true>(smem_u32(&yempty[ys]), ((tile / kYS) - 1) & 1, abort_flag, status,
+                           kWhereFwdYEmpty)) {
+        ok = false;
+        break;
+      }
+      const uint8_t* stage = sStage + st * p.stage_bytes;
+      const uint16_t* qs = reinterpret_cast<const uint16_t*>(stage + p.q_off);
+      const uint16_t* ks = reinterpret_cast<const uint16_t*>(stage + p.k_off);
+      const uint16_t* vs = reinterpret_cast<const uint16_t*>(stage + p.v_off);
+      const float* fs = reinterpret_cast<const float*>(stage + p.f_off);
+      float* yp = sY + ys * (kS * slots * V);
+      const int nsteps = min(kS, T - tile * kS);
+      for (int s = 0; s < nsteps; ++s) {
+        const int t = tile * kS + s;
+        const float vj = bf16_bits_to_f32(vs[s * V + j]);
+        const float omf = 1.f - fs[s];
+        if (!mbar_wait(dbar, dphase, abort_flag, status, kWhereFwdD)) {
+          ok = false;
+          break;
+        }
+        dphase ^= 1u;
+        tc_fence_after_sync();
+        uint32_t acc[ROWS];
+        tmem_ld_32x32b<ROWS>(taddr, acc);
+        tmem_ld_wait();
+        tmem_ld_fence_regs(acc);
+        const uint16_t* kr = ks + s * NRtot + row_in_cta;
+#pragma unroll
+        for (int r0 = 0; r0 < ROWS; r0 += 8) {
+          float kf[8];
+          unpack8_bf16(*reinterpret_cast<const uint4*>(kr + r0), kf);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float x = fmaf(kf[u], vj, __uint_as_float(acc[r0 + u]));  // (H W)_ij + k_i v_j
+            const float z = tanh_fast(x);                                   // Eq. 10
+            h[r0 + u] = fmaf(omf, z - h[r0 + u], h[r0 + u]);                // Eq. 11
+          }
+          uint4 pk;
+          pk.x = pack_bf16x2(h[r0 + 0], h[r0 + 1]);
+          pk.y = pack_bf16x2(h[r0 + 2], h[r0 + 3]);
+          pk.z = pack_bf16x2(h[r0 + 4], h[r0 + 5]);
+          pk.w = pack_bf16x2(h[r0 + 6], h[r0 + 7]);
+          *reinterpret_cast<uint4*>(bslot + (r0 / 8) * C::SBO) = pk;
+        }
+        // Hand bf16(H_t) to the tensor core: make the generic-proxy stores
+        // visible to the async proxy, then one arrival per warp; the group's
+        // issuing thread waits for all four (a bounded wait, unlike bar.sync).
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(hbar);
+        if (issuer && t + 1 < T) {
+          if (!mbar_wait(hbar, hphase, abort_flag, status, kWhereFwdH)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          issue_step_mma<C>(d_tmem, a_base, b_base, idesc);
+          tc_commit(dbar);
+        }
+        hphase ^= 1u;
+        // ---- off the serial chain ----
+        if (do_y) {
+          const uint16_t* qr = qs + s * NRtot + row_in_cta;
+          float ya = 0.f;
+#pragma unroll
+          for (int r0 = 0; r0 < ROWS; r0 += 8) {
+            float qf[8];
+            unpack8_bf16(*reinterpret_cast<const uint4*>(qr + r0), qf);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) ya = fmaf(qf[u], h[r0 + u], ya);  // Eq. 12, this thread's rows
+          }
+          yp[(s * slots + g * C::COPIES + c) * V + j] = ya;
+        }
+        if (p.a.ckpt != nullptr && (t + 1) % p.a.ckpt_every == 0 && t + 1 < T) {
+          float* dst = p.a.ckpt +
+                       ((static_cast<int64_t>(chain) * p.a.n_ckpt + (t + 1) / p.a.ckpt_every - 1) *
+                            p.a.K +
+                        row_global) *
+                           V +
+                       j;
+#pragma unroll
+          for (int r = 0; r < ROWS; ++r) dst[static_cast<int64_t>(r) * V] = h[r];
+        }
+      }
+      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&empty[st]));
+        if (do_y) mbar_arrive(smem_u32(&yfull[ys]));
+      }
+    }
+    if (ok && p.a.H_T != nullptr) {
+      float* dst = p.a.H_T + (static_cast<int64_t>(chain) * p.a.K + row_global) * V + j;
+#pragma unroll
+      for (int r = 0; r < ROWS; ++r) dst[static_cast<int64_t>(r) * V] = h[r];
+    }
+    if (!ok) *abort_flag = 1;
+  } else if (warp == 4 * G) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+    }
+    const uint16_t* fg = static_cast<const uint16_t*>(p.a.f);
+    int issued = 0;
+    bool ok = true;
+    for (int tile = 0; tile < ntiles; ++tile) {
+      const int st = tile % C::NS;
+      if (tile >= C::NS &&
+          !mbar_wait(smem_u32(&empty[st]), ((tile / C::NS) - 1) & 1, abort_flag, status, kWhereFwdEmpty)) {
+        ok = false;
+        break;
+      }
+      const int t0 = tile * kS;
+      uint8_t* stage = sStage + st * p.stage_bytes;
+      float fv = 0.f;
+      if (t0 + lane < T) fv = bf16_bits_to_f32(fg[(static_cast<int64_t>(b) * T + t0 + lane) * N + n]);
+      reinterpret_cast<float*>(stage + p.f_off)[lane] = fv;
+      __syncwarp();
+      const uint32_t fb = smem_u32(&full[st]);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(fb, p.tx_bytes);
+        tma_load_4d(smem_u32(stage + p.q_off), &tm_q, fb, cta_rank * NRtot, n, t0, b);
+        tma_load_4d(smem_u32(stage + p.k_off), &tm_k, fb, cta_rank * NRtot, n, t0, b);
+        tma_load_4d(smem_u32(stage + p.v_off), &tm_v, fb, 0, n, t0, b);
+      } else {
+        mbar_arrive(fb);
+      }
+      issued = tile + 1;
+    }
+    if (!ok) {  // let every issued copy land before the CTA can exit
+      for (int tile = std::max(0, issued - C::NS); tile < issued; ++tile) {
+        volatile int never = 0;
+        mbar_wait(smem_u32(&full[tile % C::NS]), (tile / C::NS) & 1, &never, nullptr, kWhereFwdDrain);
+      }
+    }
+  } else if (do_y) {
+    // ---------------- readout reducer ----------------
+    const uint16_t* vg = static_cast<const uint16_t*>(p.a.v);
+    const uint16_t* wr = static_cast<const uint16_t*>(p.a.w_r) + static_cast<int64_t>(n) * V;
+    float wrl[V / 32];
+#pragma unroll
+    for (int u = 0; u < V / 32; ++u) wrl[u] = bf16_bits_to_f32(wr[lane + 32 * u]);
+    bool ok = true;
+    int done = 0;
+    for (int tile = 0; tile < ntiles; ++tile) {
+      const int ys = tile % kYS;
+      const uint32_t par = (tile / kYS) & 1;
+      if (!mbar_wait(smem_u32(&yfull[ys]), par, abort_flag, status, kWhereFwdYFull)) {
+        ok = false;
+        break;
+      }
+      fence_acq_rel_cluster();
+      if (lane < R) mbar_arrive_cluster(mapa_shared(smem_u32(&ypeer[ys]), lane));
+      if (!mbar_wait<true>(smem_u32(&ypeer[ys]), par, abort_flag, status, kWhereFwdYPeer)) {
+        ok = false;
+        break;
+      }
+      const int t0 = tile * kS;
+      const int nsteps = min(kS, T - t0);
+      const uint32_t ybase = smem_u32(sY + ys * (kS * slots * V));
+      for (int s = cta_rank; s < nsteps; s += R) {
+        const int64_t row = (static_cast<int64_t>(b) * T + t0 + s) * N + n;
+#pragma unroll
+        for (int u = 0; u < V / 32; ++u) {
+          const int jj = lane + 32 * u;
+          float acc = 0.f;
+          for (int pr = 0; pr < R; ++pr) {  // fixed order: CTAs, then slots
+            const uint32_t rb = mapa_shared(ybase, pr);
+            for (int sl = 0; sl < slots; ++sl)
+              acc += ld_shared_cluster_f32(rb + static_cast<uint32_t>(((s * slots + sl) * V + jj) * 4));
+          }
+          const float vv = bf16_bits_to_f32(vg[row * V + jj]);
+          p.a.y[row * V + jj] = fmaf(wrl[u], vv, acc);  // + w_r * v_t
+        }
+      }
+      fence_acq_rel_cluster();
+      __syncwarp();
+      if (lane < R) mbar_arrive_cluster(mapa_shared(smem_u32(&yempty[ys]), lane));
+      done = tile + 1;
+    }
+    // Do not let this CTA exit while a peer may still read its partials.
+    for (int tile = std::max(0, done - kYS); tile < done; ++tile) {
+      if (!mbar_wait<true>(smem_u32(&yempty[tile % kYS]), (tile / kYS) & 1, abort_flag, status,
+                           kWhereFwdExit))
+        break;
+    }
+    if (!ok) *abort_flag = 1;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, p.tmem_cols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 4-D bf16 tensor map over [B][T][N][X] (innermost X), box {bx, 1, by, 1}.
+bool make_map_btnx(CUtensorMap* m, const void* base, int B, int T, int N, int X, int bx, int by) {
+  auto enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(X), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(X) * 2, static_cast<cuuint64_t>(N) * X * 2,
+                           static_cast<cuuint64_t>(T) * N * X * 2};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(bx), 1, static_cast<cuuint32_t>(by), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+template <int V, int ROWS>
+cudaError_t launch_cfg(const FwdArgs& a, int G, int R, cudaStream_t stream) {
+  using C = FwdCfg<V, ROWS>;
+  TcFwdParams p{};
+  p.a = a;
+  p.G = G;
+  p.R = R;
+  p.NRtot = G * C::NR;
+  p.ntiles = (a.T + kS - 1) / kS;
+  uint32_t cols = 32;
+  while (cols < static_cast<uint32_t>(G * C::NR)) cols *= 2;
+  p.tmem_cols = cols;
+  p.b_off = C::A_BYTES;
+  p.stage_off = align_up(p.b_off + G * C::B_BYTES, 128);
+  p.q_off = 0;
+  p.k_off = align_up(p.q_off + kS * p.NRtot * 2, 128);
+  p.v_off = align_up(p.k_off + kS * p.NRtot * 2, 128);
+  p.f_off = align_up(p.v_off + kS * V * 2, 128);
+  p.stage_bytes = align_up(p.f_off + kS * 4, 128);
+  p.y_off = p.stage_off + C::NS * p.stage_bytes;
+  const uint32_t slots = G * C::COPIES;
+  p.bar_off = align_up(p.y_off + kYS * kS * slots * V * 4, 8);
+  p.misc_off = p.bar_off + (2 * C::NS + 2 * G + 3 * kYS) * 8;
+  uint32_t smem = align_up(p.misc_off + 16, 128) + 1024;
+  // One CTA per SM: the per-step latency, not throughput, bounds this kernel,
+  // so CTAs must not share an SM's special-function and tensor units.
+  smem = std::max<uint32_t>(smem, 120 * 1024);
+  p.tx_bytes = 2 * kS * p.NRtot * 2 + kS * V * 2;
+
+  CUtensorMap mq, mk, mv;
+  if (!make_map_btnx(&mq, a.q, a.B, a.T, a.N, a.K, p.NRtot, kS) ||
+      !make_map_btnx(&mk, a.k, a.B, a.T, a.N, a.K, p.NRtot, kS) ||
+      !make_map_btnx(&mv, a.v, a.B, a.T, a.N, V, V, kS))
+    return cudaErrorInvalidValue;
+
+  auto kern = tc_forward_kernel<V, ROWS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  if (R > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.B * a.N * R));
+  cfg.blockDim = dim3(static_cast<unsigned>((4 * G + 2) * 32));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(R);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, p, mq, mk, mv);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_forward_supported(int K, int V) {
+  if (V == 64) return K >= 16 && K <= 128 && K % 16 == 0;
+  if (V == 128) return K == 32 || K == 64 || K == 128;
+  return false;
+}
+
+cudaError_t launch_tc_forward(const FwdArgs& a, cudaStream_t s) {
+  if (a.V == 64) return launch_cfg<64, 8>(a, /*G=*/1, /*R=*/a.K / 16, s);
+  if (a.V == 128) {
+    // Two warpgroups ping-pong on the tensor core, each with half the rows.
+    if (a.K == 128) return launch_cfg<128, 64>(a, 2, 1, s);
+    if (a.K == 64) return launch_cfg<128, 32>(a, 2, 1, s);
+    if (a.K == 32) return launch_cfg<128, 16>(a, 2, 1, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace m2rnn
