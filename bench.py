@@ -1,0 +1,520 @@
+#!/usr/bin/env python
+"""Benchmark of the M2RNN forward + backward-through-time scans on GB300.
+
+One step = one pass of the whole hot path over one batch of seeded synthetic
+input: the forward scan (writing the per-chunk checkpoints) followed by the
+backward scan that reuses them, for the bf16 forward+backward workload
+B=4, heads=8, T=4096, K=V=64.  ``value`` is tokens*heads/s (B*T*heads per
+step / device time) with inputs resident in HBM; ``e2e`` is the same through
+the C ABI with host buffers (pinned host->device copies of the inputs and
+device->host copies of every result inside the timed region).  The forward-
+only workloads (T=2048 K=V=64, T=4096 K=V=128, T=16384 K=V=64) are timed too
+and reported under ``forward``.
+
+``--impl reference`` times the float64 CPU oracle on the same workload
+(a bounded sample per step) instead.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+Under torchrun every rank runs its own full batch (independent chains, no
+data-path collective: weak scaling); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import os
+
+_CORES = os.cpu_count() or 1
+os.environ.setdefault("OPENBLAS_NUM_THREADS", str(_CORES))
+os.environ.setdefault("OMP_NUM_THREADS", str(_CORES))
+
+import argparse  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import threading  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from matrix_state_non_gb300.inputs import WORKLOADS, make_workload  # noqa: E402
+
+METRIC = "M²RNN scan tokens·heads/s (fwd, fwd+bwd) and % of tensor/HBM roofline, 1 GB300"
+UNIT = "tokens*heads/s"
+MAIN = "fwdbwd_bf16_k64"
+FWD_EXTRA = ("fwd_bf16_k64", "fwd_bf16_k128", "fwd_bf16_16k")
+IN_NAMES = ("q", "k", "v", "f", "W", "w_r")
+GRADS = ("dq", "dk", "dv", "df", "dW", "dw_r")
+CKPT_EVERY = 64
+FLUSH_BYTES = 256 << 20  # larger than the 129 MB L2
+
+
+# ---------------------------------------------------------------------------
+# Shared helpers
+# ---------------------------------------------------------------------------
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return dict(hbm_gbs=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(hbm_gbs=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+def units(w):
+    return w["B"] * w["T"] * w["N"]
+
+
+def fwd_flops(w):
+    return 2.0 * w["K"] * w["V"] ** 2 * units(w)
+
+
+def bwd_flops(w):
+    return 4.0 * w["K"] * w["V"] ** 2 * units(w)
+
+
+def io_bytes_fwd(w, s_in=2):
+    K, V = w["K"], w["V"]
+    return units(w) * ((2 * K + V + 1) * s_in + 4 * V)
+
+
+def io_bytes_bwd(w, s_in=2, ckpt_every=CKPT_EVERY):
+    K, V = w["K"], w["V"]
+    per_unit = (2 * K + V + 1) * s_in + 4 * V + 4 * (2 * K + V + 1)
+    ck = 4.0 * K * V * units(w) / ckpt_every
+    return units(w) * per_unit + ck
+
+
+def source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "matrix_state_non_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(name.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(f"{kernel}@{workload}")
+    if not ent or ent.get("source_hash") != source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# Distributed plumbing (torchrun): barrier + max over ranks
+# ---------------------------------------------------------------------------
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as td
+            backend = "nccl" if _cuda_ok() else "gloo"
+            td.init_process_group(backend=backend)
+            self.pg = td
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        dev = "cuda" if _cuda_ok() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def _cuda_ok():
+    import torch
+    return torch.cuda.is_available()
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the float64 CPU oracle on a bounded sample of the workload
+# ---------------------------------------------------------------------------
+def run_reference(args, dist):
+    if dist.rank != 0:
+        return None
+    from oracle import backward as oracle_backward
+    from oracle import forward as oracle_forward
+    w = WORKLOADS[MAIN]
+    t_sample = 256  # timesteps of every chain per step: a few seconds of CPU work
+    inp = make_workload(MAIN)
+    ex = inp.exact
+    sl = slice(0, t_sample)
+    a = [ex["q"][:, sl], ex["k"][:, sl], ex["v"][:, sl], ex["f"][:, sl], ex["W"], ex["w_r"]]
+    dy = ex["dy"][:, sl]
+
+    def step():
+        oracle_forward(*a)
+        oracle_backward(*a, dy)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    n_units = w["B"] * w["N"] * t_sample
+    val = n_units / dt
+    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", _CORES))
+    sample = (f"all {w['B']}x{w['N']} chains, first {t_sample} of {w['T']} steps, "
+              "forward + backward (float64 numpy oracle)")
+    return {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOADS[MAIN]["desc"], "B": w["B"], "T": w["T"], "heads": w["N"],
+                   "K": w["K"], "V": w["V"], "parallelism": "cpu"},
+        "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def cpu_baseline_sample():
+    """The oracle as it stands on a bounded sample of the main workload."""
+    from oracle import backward as oracle_backward
+    from oracle import forward as oracle_forward
+    w = WORKLOADS[MAIN]
+    t_sample = 512
+    inp = make_workload(MAIN)
+    ex = inp.exact
+    sl = slice(0, t_sample)
+    a = [ex["q"][:, sl], ex["k"][:, sl], ex["v"][:, sl], ex["f"][:, sl], ex["W"], ex["w_r"]]
+    t0 = time.perf_counter()
+    oracle_forward(*a)
+    oracle_backward(*a, ex["dy"][:, sl])
+    dt = time.perf_counter() - t0
+    n_units = w["B"] * w["N"] * t_sample
+    return {"value": n_units / dt, "unit": UNIT,
+            "cores": int(os.environ.get("OPENBLAS_NUM_THREADS", _CORES)), "kind": "oracle",
+            "sample": (f"all {w['B']}x{w['N']} chains, first {t_sample} of {w['T']} steps, "
+                       f"forward + backward, {dt:.1f} s of float64 numpy")}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_gpu(args, dist):
+    import torch
+
+    from matrix_state_non_gb300 import binding
+
+    torch.cuda.set_device(dist.local)
+    dev = torch.device("cuda", dist.local)
+    binding.load()
+    pk = peaks()
+    w = WORKLOADS[MAIN]
+    inp = make_workload(MAIN)
+    d = binding.to_device(inp, dev)
+    B, T, N, K, V = w["B"], w["T"], w["N"], w["K"], w["V"]
+    stream = torch.cuda.current_stream(dev)
+    # Preallocated outputs and workspaces.
+    fwd_out = binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=CKPT_EVERY)
+    bwd_out = binding.backward(*(d[n] for n in IN_NAMES), d["dy"], ckpt=fwd_out["ckpt"],
+                               ckpt_every=CKPT_EVERY)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def step(timing=None):
+        if timing is not None:
+            timing[0].record(stream)
+        binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=CKPT_EVERY, out=fwd_out,
+                        workspace=fwd_out["workspace"])
+        if timing is not None:
+            timing[1].record(stream)
+        binding.backward(*(d[n] for n in IN_NAMES), d["dy"], ckpt=fwd_out["ckpt"],
+                         ckpt_every=CKPT_EVERY, out=bwd_out, workspace=bwd_out["workspace"])
+        if timing is not None:
+            timing[2].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    st, detail = binding.sync_status(bwd_out["workspace"])
+    if st != binding.M2RNN_OK:
+        raise RuntimeError(f"device status {binding.status_string(st)} at {detail}")
+
+    sampler = ClockSampler(torch.cuda.current_device()) if dist.rank == 0 else None
+    timings = [(ev(), ev(), ev()) for _ in range(args.steps)]
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    for i in range(args.steps):
+        flush.zero_()  # L2 flush between timed steps (outside the events)
+        step(timings[i])
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop() if sampler else None
+    dist.barrier()
+    fwd_ms = [a.elapsed_time(b) for a, b, _ in timings]
+    bwd_ms = [b.elapsed_time(c) for _, b, c in timings]
+    step_ms_local = sum(f + b for f, b in zip(fwd_ms, bwd_ms)) / args.steps
+    step_ms = dist.max(step_ms_local)
+    value = dist.world * units(w) / (step_ms * 1e-3)
+
+    # e2e: host buffers through the C ABI, copies inside the timed region.
+    host_in = {n: torch.empty_like(d[n], device="cpu").pin_memory() for n in list(IN_NAMES) + ["dy"]}
+    for n in host_in:
+        host_in[n].copy_(d[n].cpu())
+    outs_dev = [fwd_out["y"]] + [bwd_out[g] for g in GRADS]
+    host_out = [torch.empty_like(t, device="cpu").pin_memory() for t in outs_dev]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def e2e_step():
+        for n, t in host_in.items():
+            d[n].copy_(t, non_blocking=True)
+        step()
+        for hd, dd in zip(host_out, outs_dev):
+            hd.copy_(dd, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    e_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = ev(), ev()
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        e_ms.append((a, b))
+    torch.cuda.synchronize(dev)
+    e2e_local = sum(a.elapsed_time(b) for a, b in e_ms) / args.steps
+    e2e_ms = dist.max(e2e_local)
+    e2e_val = dist.world * units(w) / (e2e_ms * 1e-3)
+
+    # Roofline of the dominant kernel in the step.
+    f_avg = sum(fwd_ms) / len(fwd_ms)
+    b_avg = sum(bwd_ms) / len(bwd_ms)
+    peak = pk["bf16_sustained"]
+    if b_avg >= f_avg:
+        kname, kflops, kms = "m2rnn_backward", bwd_flops(w), b_avg
+    else:
+        kname, kflops, kms = "m2rnn_forward", fwd_flops(w), f_avg
+    achieved = kflops / (kms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": profiled_traffic(kname, MAIN),
+                "kernel": kname, "peak_source": f"{pk['source']} bf16 sustained",
+                "kernel_ms": kms, "ns_per_step_per_chain": kms * 1e6 / T,
+                "hbm_frac": (io_bytes_bwd(w) if kname == "m2rnn_backward" else io_bytes_fwd(w))
+                / (kms * 1e-3) / (pk["hbm_gbs"] * 1e9)}
+
+    # Forward-only workloads.
+    fwd_extra = {}
+    if not args.no_extra:
+        for name in FWD_EXTRA:
+            fwd_extra[name] = time_forward(name, binding, dev, stream, flush, pk, dist,
+                                           reps=max(3, args.steps // 2))
+    cpu = cpu_baseline_sample() if (dist.rank == 0 and not args.no_cpu) else None
+    launches_per_step = 3  # forward scan, backward scan, partial-sum reduction
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w["desc"], "B": B, "T": T, "heads": N, "K": K, "V": V,
+                   "state": "fp32", "ckpt_every": CKPT_EVERY,
+                   "l2": "flushed between timed steps (256 MiB write outside the events)",
+                   "parallelism": f"replicas x{dist.world} (independent chains, no collective)"},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "clocks": clocks,
+        "gpu_launches": launches_per_step * args.steps,
+        "step_breakdown_ms": {"forward": f_avg, "backward": b_avg},
+        "forward": fwd_extra,
+        "kernels": {"forward": binding.m2rnn_path(K, V, binding.M2RNN_BF16) == 1 and "tcgen05" or "simt"},
+    }
+    return line
+
+
+def time_forward(name, binding, dev, stream, flush, pk, dist, reps=5):
+    import torch
+    w = WORKLOADS[name]
+    inp = make_workload(name)
+    d = binding.to_device(inp, dev)
+    out = binding.forward(*(d[n] for n in IN_NAMES))
+    for _ in range(3):
+        binding.forward(*(d[n] for n in IN_NAMES), out=out, workspace=out["workspace"])
+    torch.cuda.synchronize(dev)
+    ms = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        binding.forward(*(d[n] for n in IN_NAMES), out=out, workspace=out["workspace"])
+        b.record(stream)
+        ms.append((a, b))
+    torch.cuda.synchronize(dev)
+    st, detail = binding.sync_status(out["workspace"])
+    if st != binding.M2RNN_OK:
+        raise RuntimeError(f"{name}: device status {binding.status_string(st)} at {detail}")
+    t = dist.max(sum(a.elapsed_time(b) for a, b in ms) / reps)
+    fl = fwd_flops(w)
+    by = io_bytes_fwd(w)
+    t_tensor = fl / (pk["bf16"] * 1e12)
+    t_hbm = by / (pk["hbm_gbs"] * 1e9)
+    del d, out
+    return {"workload": w["desc"], "ms": t, "value": dist.world * units(w) / (t * 1e-3), "unit": UNIT,
+            "ns_per_step_per_chain": t * 1e6 / w["T"],
+            "roofline_ms": max(t_tensor, t_hbm) * 1e3,
+            "roofline_frac": max(t_tensor, t_hbm) / (t * 1e-3),
+            "bound": "tensor" if t_tensor >= t_hbm else "hbm",
+            "tensor_tflops": fl / (t * 1e-3) / 1e12,
+            "peak_source": f"{pk['source']} bf16 burst / hbm copy"}
+
+
+def run_only(args, dist):
+    """One workload, no extras: warm-up launches, then --steps launches."""
+    import torch
+
+    from matrix_state_non_gb300 import binding
+    torch.cuda.set_device(dist.local)
+    dev = torch.device("cuda", dist.local)
+    w = WORKLOADS[args.only]
+    inp = make_workload(args.only)
+    d = binding.to_device(inp, dev)
+    ck = CKPT_EVERY if w["backward"] else 0
+    out = binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=ck)
+    bout = None
+
+    def step():
+        nonlocal bout
+        binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=ck, out=out, workspace=out["workspace"])
+        if w["backward"]:
+            bout = binding.backward(*(d[n] for n in IN_NAMES), d["dy"], ckpt=out["ckpt"],
+                                    ckpt_every=ck, out=bout, workspace=None if bout is None
+                                    else bout["workspace"])
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize(dev)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    st, detail = binding.sync_status(out["workspace"])
+    return {"only": args.only, "host_ms_per_step": dt * 1e3, "status": binding.status_string(st),
+            "detail": detail}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
+    ap.add_argument("--no-extra", action="store_true", help="skip the forward-only workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--only", choices=sorted(WORKLOADS), default=None,
+                    help="run just this workload (forward, or forward+backward) --steps times "
+                         "after --warmup; for profiler captures")
+    args = ap.parse_args()
+    dist = Dist()
+    try:
+        if args.only:
+            line = run_only(args, dist)
+        elif args.impl == "reference":
+            line = run_reference(args, dist)
+        else:
+            line = run_gpu(args, dist)
+        if dist.rank == 0 and line is not None:
+            print(json.dumps(line), flush=True)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

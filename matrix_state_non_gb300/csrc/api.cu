@@ -5,6 +5,7 @@
 
 #include <climits>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 
 #include "internal.h"
@@ -30,13 +31,61 @@ bool dims_ok(int64_t B, int64_t T, int64_t N, int64_t K, int64_t V) {
 
 bool dtype_ok(int dt) { return dt == M2RNN_F32 || dt == M2RNN_BF16; }
 
-// Which family runs: 1 = tcgen05, 0 = SIMT fp32, <0 = error.
+constexpr int kPathSimt = 0, kPathTc = 1, kPathMma = 2;
+constexpr int kMmaMaxChunk = 128;  // chunk buffers of the warp-MMA backward
+
+// Kernel family override for tests and benchmarks: M2RNN_KERNEL = auto |
+// tcgen05 | mma | simt.  A family that does not support the shape falls back
+// to the automatic choice.
+int kernel_override() {
+  const char* e = std::getenv("M2RNN_KERNEL");
+  if (e == nullptr || std::strcmp(e, "auto") == 0) return -1;
+  if (std::strcmp(e, "tcgen05") == 0) return kPathTc;
+  if (std::strcmp(e, "mma") == 0) return kPathMma;
+  if (std::strcmp(e, "simt") == 0) return kPathSimt;
+  return -1;
+}
+
+// Which family runs the forward: 2 = warp-MMA, 1 = tcgen05, 0 = SIMT fp32, <0 = error.
 int choose_path(int64_t K, int64_t V, int dt) {
   if (!dtype_ok(dt)) return M2RNN_ERR_INVALID_ARG;
   if (K < 1 || V < 1) return M2RNN_ERR_INVALID_ARG;
   if (K > kMaxDim || V > kMaxDim) return M2RNN_ERR_UNSUPPORTED;
-  if (dt == M2RNN_BF16 && tc_forward_supported(static_cast<int>(K), static_cast<int>(V))) return 1;
-  return 0;
+  if (dt != M2RNN_BF16) return kPathSimt;
+  const int k = static_cast<int>(K), v = static_cast<int>(V);
+  const bool mma = mma_forward_supported(k, v), tc = tc_forward_supported(k, v);
+  switch (kernel_override()) {
+    case kPathTc: if (tc) return kPathTc; break;
+    case kPathMma: if (mma) return kPathMma; break;
+    case kPathSimt: return kPathSimt;
+    default: break;
+  }
+  if (mma) return kPathMma;  // latency-bound small state: ~16 rows per SM
+  if (tc) return kPathTc;    // wide heads: tensor throughput matters
+  return kPathSimt;
+}
+
+// Backward family (the tensor-core backwards cover fewer shapes and chunk
+// lengths than the forwards).
+int choose_bwd_path(int64_t K, int64_t V, int dt, int ckpt_every) {
+  const int path = choose_path(K, V, dt);
+  if (path < 0) return path;
+  const int k = static_cast<int>(K), v = static_cast<int>(V);
+  const bool mma = mma_backward_supported(k, v) && ckpt_every <= kMmaMaxChunk;
+  const bool tc = tc_backward_supported(k, v);
+  if (path == kPathMma && mma) return kPathMma;
+  if (path == kPathTc && tc) return kPathTc;
+  if (dt == M2RNN_BF16 && kernel_override() != kPathSimt) {
+    if (mma) return kPathMma;
+    if (tc) return kPathTc;
+  }
+  return kPathSimt;
+}
+
+cudaError_t launch_forward_path(int path, const FwdArgs& a, cudaStream_t s) {
+  if (path == kPathMma) return launch_mma_forward(a, s);
+  if (path == kPathTc) return launch_tc_forward(a, s);
+  return launch_simt_forward(a, s);
 }
 
 struct BwdLayout {
@@ -46,25 +95,25 @@ struct BwdLayout {
 BwdLayout bwd_layout(int64_t B, int64_t T, int64_t N, int64_t K, int64_t V, int dt, int C,
                      bool have_ckpt) {
   BwdLayout l{};
-  const int path = choose_path(K, V, dt);
+  const int path = choose_bwd_path(K, V, dt, C);
   const int64_t nck = (T - 1) / C;
+  const int b = static_cast<int>(B), nn = static_cast<int>(N), k = static_cast<int>(K),
+            v = static_cast<int>(V);
   size_t off = kStatusBytes;
   l.ckpt_off = off;
   if (!have_ckpt) off = align256(off + sizeof(float) * static_cast<size_t>(B * N * nck * K * V));
-  const int parts = (path == 1 && tc_backward_supported(static_cast<int>(K), static_cast<int>(V)))
-                        ? tc_backward_parts(static_cast<int>(K), static_cast<int>(V))
-                        : 1;
+  const int parts = (path == kPathSimt) ? 1 : (path == kPathMma ? k / 16 : tc_backward_parts(k, v));
   l.dwp_off = off;
   off = align256(off + sizeof(float) * static_cast<size_t>(B * N * parts * V * V));
   l.dwrp_off = off;
   off = align256(off + sizeof(float) * static_cast<size_t>(B * N * V));
   l.scratch_off = off;
-  if (path == 1 && tc_backward_supported(static_cast<int>(K), static_cast<int>(V)))
-    off = align256(off + tc_backward_scratch_bytes(static_cast<int>(B), static_cast<int>(N),
-                                                   static_cast<int>(K), static_cast<int>(V), C));
+  if (path == kPathMma)
+    off = align256(off + mma_backward_scratch_bytes(b, nn, k, v, C));
+  else if (path == kPathTc)
+    off = align256(off + tc_backward_scratch_bytes(b, nn, k, v, C));
   else
-    off = align256(off + simt_backward_scratch_bytes(static_cast<int>(B), static_cast<int>(N),
-                                                     static_cast<int>(K), static_cast<int>(V), C));
+    off = align256(off + simt_backward_scratch_bytes(b, nn, k, v, C));
   l.total = off;
   return l;
 }
@@ -137,7 +186,7 @@ int m2rnn_forward(const void* q, const void* k, const void* v, const void* f, co
   a.K = static_cast<int>(K); a.V = static_cast<int>(V);
   a.dtype = dtype;
   a.status = status;
-  e = (path == 1) ? launch_tc_forward(a, s) : launch_simt_forward(a, s);
+  e = launch_forward_path(path, a, s);
   return cuda_status(e);
 }
 
@@ -149,6 +198,7 @@ int m2rnn_backward(const void* q, const void* k, const void* v, const void* f, c
   if (!dtype_ok(dtype) || !dims_ok(B, T, N, K, V)) return M2RNN_ERR_INVALID_ARG;
   const int path = choose_path(K, V, dtype);
   if (path < 0) return path;
+  const int bpath = choose_bwd_path(K, V, dtype, ckpt_every);
   if (ckpt_every < 1 || ckpt_every > kMaxCkptEvery) return M2RNN_ERR_INVALID_ARG;
   const void* req[] = {q, k, v, f, W, w_r, dy, dq, dk, dv, df, dW, dw_r};
   for (const void* p : req)
@@ -175,7 +225,7 @@ int m2rnn_backward(const void* q, const void* k, const void* v, const void* f, c
       fa.B = static_cast<int>(B); fa.T = static_cast<int>(T); fa.N = static_cast<int>(N);
       fa.K = static_cast<int>(K); fa.V = static_cast<int>(V);
       fa.dtype = dtype; fa.status = status;
-      e = (path == 1) ? launch_tc_forward(fa, s) : launch_simt_forward(fa, s);
+      e = launch_forward_path(path, fa, s);
       if (e != cudaSuccess) return M2RNN_ERR_CUDA;
     }
   }
@@ -189,9 +239,13 @@ int m2rnn_backward(const void* q, const void* k, const void* v, const void* f, c
   a.dW_part = reinterpret_cast<float*>(ws + l.dwp_off);
   a.dwr_part = reinterpret_cast<float*>(ws + l.dwrp_off);
   a.scratch = reinterpret_cast<float*>(ws + l.scratch_off);
-  const bool tc = path == 1 && tc_backward_supported(a.K, a.V);
-  a.parts = tc ? tc_backward_parts(a.K, a.V) : 1;
-  e = tc ? launch_tc_backward(a, s) : launch_simt_backward(a, s);
+  a.parts = (bpath == kPathSimt) ? 1 : (bpath == kPathMma ? a.K / 16 : tc_backward_parts(a.K, a.V));
+  if (bpath == kPathMma)
+    e = launch_mma_backward(a, s);
+  else if (bpath == kPathTc)
+    e = launch_tc_backward(a, s);
+  else
+    e = launch_simt_backward(a, s);
   if (e != cudaSuccess) return M2RNN_ERR_CUDA;
   return cuda_status(launch_reduce_partials(a, s));
 }

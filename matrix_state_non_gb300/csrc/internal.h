@@ -64,6 +64,13 @@ size_t simt_backward_scratch_bytes(int B, int N, int K, int V, int ckpt_every);
 // Fixed-order sum of per-chain partials over b (and parts): dW, dw_r.
 cudaError_t launch_reduce_partials(const BwdArgs& a, cudaStream_t s);
 
+// Register-resident warp-MMA kernels (bf16 inputs, V = 64).
+bool mma_forward_supported(int K, int V);
+cudaError_t launch_mma_forward(const FwdArgs& a, cudaStream_t s);
+bool mma_backward_supported(int K, int V);
+size_t mma_backward_scratch_bytes(int B, int N, int K, int V, int ckpt_every);
+cudaError_t launch_mma_backward(const BwdArgs& a, cudaStream_t s);
+
 // tcgen05 tensor-core kernels (bf16 inputs).
 bool tc_forward_supported(int K, int V);
 cudaError_t launch_tc_forward(const FwdArgs& a, cudaStream_t s);

@@ -1,0 +1,604 @@
+// Register-resident backward-through-time for V = 64 value columns (bf16
+// inputs, fp32 state and gradients).
+//
+// Chain rule for Eq. 10-12 as derived in section 2.7 of the reading notes on
+// "M2RNN: Non-Linear RNNs with Matrix-Valued States for Scalable Language
+// Modeling" (the notes' correction of the paper's Algorithm 2), with the
+// value-residual terms restored; u_t = dy_t, C_T = dH_T:
+//   R_t = C_t + q_t u_t^T,  D_t = ((1-f_t) R_t) * (1 - Z_t * Z_t),
+//   C_{t-1} = f_t R_t + D_t W^T,
+//   dq_t = H_t u_t, dk_t = D_t v_t, dv_t = D_t^T k_t + w_r * u_t,
+//   df_t = <R_t, H_{t-1} - Z_t>,  dW += H_{t-1}^T D_t,  dw_r += u_t * v_t.
+//
+// Work split as in the forward: a chain's K rows in blocks of 16, one CTA per
+// block, the blocks of a chain in one cluster (only dv_t and df_t sum over
+// rows; dW is summed later over row blocks and batch in a fixed order).
+// Four compute warps own 16 value columns each.  The time axis runs over
+// chunks of C steps, last chunk first.  For each chunk the forward is rerun
+// from its checkpoint (section 2.6 of the notes describes the paper's
+// rerun-and-cache backward; here only one chunk is cached), each thread
+// caching its own Z_t and H_t values (fp32) in a thread-private scratch that
+// stays in L2; then the chunk is walked backwards.  Per reverse step the
+// serial chain is R -> D -> bf16(D) tile -> one named barrier -> 8 warp MMAs
+// seeded with f R -> C_{t-1}.  Off the chain: dW += H_{t-1}^T D as 8 more warp
+// MMAs per warp into register accumulators (H_{t-1}^T fragments by movmatrix,
+// D fragments by ldmatrix.trans), and the row/column reductions for dq, dk,
+// dv, df, written as per-step partials that a reducer warp sums (over warps,
+// and over the cluster's CTAs for dv, df) and stores.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "internal.h"
+#include "mma_common.cuh"
+
+namespace m2rnn {
+namespace {
+
+constexpr int kV = 64;
+constexpr int kRows = 16;
+constexpr int kPS = 32;      // reverse steps per partial tile
+constexpr int kPStages = 2;
+constexpr int kThreads = 192;
+constexpr int kMaxChunk = 128;
+constexpr int kSlotFloats = 4 * 16 + 4 * 16 + kV + 4;  // qpart, kpart, dvpart, dfpart
+
+struct MmaBwdParams {
+  BwdArgs a;
+  int R;
+  int nchunks;
+  int nptiles;
+  uint32_t htile_off, dtile_off, cbuf_off, cbuf_bytes, cq_off, ck_off, cv_off, cdy_off, cf_off;
+  uint32_t part_off, bar_off, misc_off;
+  uint32_t tx_bytes;
+};
+
+__device__ __forceinline__ float4 ldg_f4(const float* p) {
+  return *reinterpret_cast<const float4*>(p);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    mma_backward_kernel(const __grid_constant__ MmaBwdParams p, const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                        const __grid_constant__ CUtensorMap tm_dy) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const BwdArgs& A = p.a;
+  const int R = p.R, T = A.T, N = A.N, CL = A.ckpt_every;
+  const int cta_rank = static_cast<int>(blockIdx.x) % R;
+  const int chain = static_cast<int>(blockIdx.x) / R;
+  const int b = chain / N, n = chain % N;
+  StatusBlock* status = A.status;
+
+  float* sPart = reinterpret_cast<float*>(smem + p.part_off);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.bar_off);
+  uint64_t* cfull = bars;
+  uint64_t* cempty = cfull + 2;
+  uint64_t* pfull = cempty + 2;
+  uint64_t* ppeer = pfull + kPStages;
+  uint64_t* pempty = ppeer + kPStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.misc_off);
+  volatile int* cabort = reinterpret_cast<volatile int*>(smem + p.misc_off + 4);
+  const uint32_t htile0 = smem_u32(smem + p.htile_off);
+  const uint32_t dtile0 = smem_u32(smem + p.dtile_off);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&cfull[i]), 32);
+      mbar_init(smem_u32(&cempty[i]), 1);
+    }
+    for (int i = 0; i < kPStages; ++i) {
+      mbar_init(smem_u32(&pfull[i]), 1);
+      mbar_init(smem_u32(&ppeer[i]), R);
+      mbar_init(smem_u32(&pempty[i]), R);
+    }
+    *abort_flag = 0;
+    *cabort = 0;
+    fence_mbar_init_cluster();
+  }
+  cluster_sync_all();
+
+  if (warp < 4) {
+    // ======================= compute warps =======================
+    const int g = lane >> 2, qd = lane & 3, w = warp;
+    const int tid = threadIdx.x;
+    const int jcol0 = 16 * w + 2 * qd;           // this thread's columns: jcol0 + 8nt + {0,1}
+    const int64_t row_g = static_cast<int64_t>(cta_rank) * kRows + g;
+    const uint16_t* Wg = static_cast<const uint16_t*>(A.W) + static_cast<int64_t>(n) * kV * kV;
+    // Forward transform fragments: B[k][col] = W[k][16w + col].
+    uint32_t bw[2][4][2];
+    // Backward transform fragments: B[k = j][col = m] = W[16w + m][j] (D W^T).
+    uint32_t bt[2][4][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int col = 16 * w + 8 * nt + g;
+#pragma unroll
+      for (int kt = 0; kt < 4; ++kt) {
+        const int k0 = 16 * kt + 2 * qd;
+        bw[nt][kt][0] = static_cast<uint32_t>(Wg[k0 * kV + col]) |
+                        (static_cast<uint32_t>(Wg[(k0 + 1) * kV + col]) << 16);
+        bw[nt][kt][1] = static_cast<uint32_t>(Wg[(k0 + 8) * kV + col]) |
+                        (static_cast<uint32_t>(Wg[(k0 + 9) * kV + col]) << 16);
+        bt[nt][kt][0] = *reinterpret_cast<const uint32_t*>(Wg + col * kV + k0);
+        bt[nt][kt][1] = *reinterpret_cast<const uint32_t*>(Wg + col * kV + k0 + 8);
+      }
+    }
+    // State gradient C (C-fragment layout), initialised with dH_T.
+    float Cg[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      if (A.dH_T != nullptr) {
+        const float* src = A.dH_T + (static_cast<int64_t>(chain) * A.K + row_g) * kV + jcol0 + 8 * nt;
+        const float2 x0 = *reinterpret_cast<const float2*>(src);
+        const float2 x1 = *reinterpret_cast<const float2*>(src + 8 * kV);
+        Cg[nt][0] = x0.x; Cg[nt][1] = x0.y; Cg[nt][2] = x1.x; Cg[nt][3] = x1.y;
+      } else {
+        Cg[nt][0] = Cg[nt][1] = Cg[nt][2] = Cg[nt][3] = 0.f;
+      }
+    }
+    float dWacc[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) dWacc[i][0] = dWacc[i][1] = dWacc[i][2] = dWacc[i][3] = 0.f;
+    float dwr[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    // Thread-private chunk cache: H slots [CL+1][2 float4], Z slots [CL][2 float4].
+    float* scr = A.scratch + static_cast<int64_t>(blockIdx.x) * (4 * CL + 2) * 128 * 4;
+    auto hslot = [&](int sl) { return scr + (static_cast<int64_t>(sl) * 2 * 128 + tid) * 4; };
+    auto zslot = [&](int sl) { return scr + (static_cast<int64_t>(CL + 1 + sl) * 2 * 128 + tid) * 4; };
+
+    bool ok = true;
+    int rs = 0;                  // reverse steps done so far (processing order)
+    int pending_pfull = -1;      // partial tile whose last slot was written in the previous step
+    for (int ci = 0; ci < p.nchunks && ok; ++ci) {
+      const int c = p.nchunks - 1 - ci;
+      const int s0 = c * CL;
+      const int L = min(CL, T - s0);
+      const int cb = ci & 1;
+      bool mine = mbar_wait_timed(smem_u32(&cfull[cb]), (ci >> 1) & 1, status, kWhereBwdFull);
+      if (!mine) *cabort = 1;
+      named_bar_sync(1, 128);
+      if (*cabort) {
+        ok = false;
+        break;
+      }
+      const uint8_t* cbuf = smem + p.cbuf_off + cb * p.cbuf_bytes;
+      const uint16_t* cq = reinterpret_cast<const uint16_t*>(cbuf + p.cq_off);
+      const uint16_t* ck = reinterpret_cast<const uint16_t*>(cbuf + p.ck_off);
+      const uint16_t* cv = reinterpret_cast<const uint16_t*>(cbuf + p.cv_off);
+      const float* cdy = reinterpret_cast<const float*>(cbuf + p.cdy_off);
+      const float* cf = reinterpret_cast<const float*>(cbuf + p.cf_off);
+
+      // ---------- recompute the chunk's states (Eq. 10-11) ----------
+      float h[2][4];
+      if (c == 0) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) h[nt][0] = h[nt][1] = h[nt][2] = h[nt][3] = 0.f;
+      } else {
+        const float* src = A.ckpt + ((static_cast<int64_t>(chain) * A.n_ckpt + (c - 1)) * A.K + row_g) * kV + jcol0;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const float2 x0 = *reinterpret_cast<const float2*>(src + 8 * nt);
+          const float2 x1 = *reinterpret_cast<const float2*>(src + 8 * kV + 8 * nt);
+          h[nt][0] = x0.x; h[nt][1] = x0.y; h[nt][2] = x1.x; h[nt][3] = x1.y;
+        }
+      }
+      {
+        float* hs = hslot(0);
+        *reinterpret_cast<float4*>(hs) = make_float4(h[0][0], h[0][1], h[0][2], h[0][3]);
+        *reinterpret_cast<float4*>(hs + 128 * 4) = make_float4(h[1][0], h[1][1], h[1][2], h[1][3]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const int col = jcol0 + 8 * nt;
+          st_shared_b32(htile0 + tile_off(g, col), pack2_bf16(h[nt][0], h[nt][1]));
+          st_shared_b32(htile0 + tile_off(g + 8, col), pack2_bf16(h[nt][2], h[nt][3]));
+        }
+      }
+      named_bar_sync(1, 128);
+      for (int s = 0; s < L; ++s) {
+        const float k0 = bf16_bits_to_f32(ck[s * kRows + g]);
+        const float k1 = bf16_bits_to_f32(ck[s * kRows + g + 8]);
+        const float omf = 1.f - cf[s];
+        float acc[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const uint32_t vv = *reinterpret_cast<const uint32_t*>(cv + s * kV + jcol0 + 8 * nt);
+          const float v0 = bf16lo(vv), v1 = bf16hi(vv);
+          acc[nt][0] = k0 * v0;
+          acc[nt][1] = k0 * v1;
+          acc[nt][2] = k1 * v0;
+          acc[nt][3] = k1 * v1;
+        }
+        const uint32_t atile = htile0 + (s & 1) * 2048;
+        uint32_t af[4][4];
+#pragma unroll
+        for (int kt = 0; kt < 4; ++kt) ldmatrix_x4(af[kt], ldsm_addr_a(atile, kt, lane));
+#pragma unroll
+        for (int kt = 0; kt < 4; ++kt)
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) mma_bf16_16816(acc[nt], af[kt], bw[nt][kt][0], bw[nt][kt][1]);
+        const uint32_t otile = htile0 + ((s + 1) & 1) * 2048;
+        float z[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            z[nt][e] = tanh_fast(acc[nt][e]);
+            h[nt][e] = fmaf(omf, z[nt][e] - h[nt][e], h[nt][e]);
+          }
+          const int col = jcol0 + 8 * nt;
+          st_shared_b32(otile + tile_off(g, col), pack2_bf16(h[nt][0], h[nt][1]));
+          st_shared_b32(otile + tile_off(g + 8, col), pack2_bf16(h[nt][2], h[nt][3]));
+        }
+        float* zs = zslot(s);
+        *reinterpret_cast<float4*>(zs) = make_float4(z[0][0], z[0][1], z[0][2], z[0][3]);
+        *reinterpret_cast<float4*>(zs + 128 * 4) = make_float4(z[1][0], z[1][1], z[1][2], z[1][3]);
+        float* hs = hslot(s + 1);
+        *reinterpret_cast<float4*>(hs) = make_float4(h[0][0], h[0][1], h[0][2], h[0][3]);
+        *reinterpret_cast<float4*>(hs + 128 * 4) = make_float4(h[1][0], h[1][1], h[1][2], h[1][3]);
+        named_bar_sync(1, 128);
+      }
+
+      // ---------- reverse walk over the chunk ----------
+      // h holds H_t for the chunk's last step.  (Z_s, H_{s-1}) are prefetched
+      // two steps ahead through a two-deep register rotation.
+      float4 z1[2], h1[2], z2[2], h2[2];
+      auto load_slot = [&](int sl, float4 (&zz)[2], float4 (&hh)[2]) {
+        if (sl >= 0) {
+          const float* zs = zslot(sl);
+          const float* hs = hslot(sl);
+          zz[0] = ldg_f4(zs);
+          zz[1] = ldg_f4(zs + 128 * 4);
+          hh[0] = ldg_f4(hs);
+          hh[1] = ldg_f4(hs + 128 * 4);
+        }
+      };
+      load_slot(L - 1, z1, h1);
+      load_slot(L - 2, z2, h2);
+      for (int s = L - 1; s >= 0; --s, ++rs) {
+        const int ptile = rs / kPS, slot = rs % kPS, pst = ptile % kPStages;
+        if (slot == 0) {
+          // Partial tile ptile: wait until every CTA of the cluster has read
+          // what this stage held two tiles ago.
+          bool m2 = true;
+          if (ptile >= kPStages)
+            m2 = mbar_wait_timed<true>(smem_u32(&pempty[pst]), ((ptile / kPStages) - 1) & 1, status,
+                                       kWhereBwdPeerEmpty);
+          if (!m2) *cabort = 1;
+          named_bar_sync(1, 128);
+          if (*cabort) {
+            ok = false;
+            break;
+          }
+        }
+        // Step inputs.
+        const float q0 = bf16_bits_to_f32(cq[s * kRows + g]);
+        const float q1 = bf16_bits_to_f32(cq[s * kRows + g + 8]);
+        const float k0 = bf16_bits_to_f32(ck[s * kRows + g]);
+        const float k1 = bf16_bits_to_f32(ck[s * kRows + g + 8]);
+        const float ft = cf[s];
+        const float omf = 1.f - ft;
+        float u[2][2], vv[2][2];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const float2 uu = *reinterpret_cast<const float2*>(cdy + s * kV + jcol0 + 8 * nt);
+          u[nt][0] = uu.x;
+          u[nt][1] = uu.y;
+          const uint32_t vb = *reinterpret_cast<const uint32_t*>(cv + s * kV + jcol0 + 8 * nt);
+          vv[nt][0] = bf16lo(vb);
+          vv[nt][1] = bf16hi(vb);
+        }
+        float Z[2][4], Hp[2][4];
+        Z[0][0] = z1[0].x; Z[0][1] = z1[0].y; Z[0][2] = z1[0].z; Z[0][3] = z1[0].w;
+        Z[1][0] = z1[1].x; Z[1][1] = z1[1].y; Z[1][2] = z1[1].z; Z[1][3] = z1[1].w;
+        Hp[0][0] = h1[0].x; Hp[0][1] = h1[0].y; Hp[0][2] = h1[0].z; Hp[0][3] = h1[0].w;
+        Hp[1][0] = h1[1].x; Hp[1][1] = h1[1].y; Hp[1][2] = h1[1].z; Hp[1][3] = h1[1].w;
+        z1[0] = z2[0]; z1[1] = z2[1]; h1[0] = h2[0]; h1[1] = h2[1];
+        load_slot(s - 2, z2, h2);
+        // R = C + q u^T ; D = (1-f) R (1 - Z^2)
+        float Rv[2][4], Dv[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float qq = (e < 2) ? q0 : q1;
+            Rv[nt][e] = fmaf(qq, u[nt][e & 1], Cg[nt][e]);
+            const float zz = Z[nt][e];
+            Dv[nt][e] = omf * Rv[nt][e] * fmaf(-zz, zz, 1.f);
+          }
+        }
+        const uint32_t dt = dtile0 + (rs & 1) * 2048;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const int col = jcol0 + 8 * nt;
+          st_shared_b32(dt + tile_off(g, col), pack2_bf16(Dv[nt][0], Dv[nt][1]));
+          st_shared_b32(dt + tile_off(g + 8, col), pack2_bf16(Dv[nt][2], Dv[nt][3]));
+        }
+        named_bar_sync(1, 128);
+        if (pending_pfull >= 0 && threadIdx.x == 0) mbar_arrive(smem_u32(&pfull[pending_pfull % kPStages]));
+        pending_pfull = -1;
+        // Serial chain: C_{t-1} = f R + D W^T on the warp MMAs.
+        float acc[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[nt][e] = ft * Rv[nt][e];
+        uint32_t af[4][4];
+#pragma unroll
+        for (int kt = 0; kt < 4; ++kt) ldmatrix_x4(af[kt], ldsm_addr_a(dt, kt, lane));
+#pragma unroll
+        for (int kt = 0; kt < 4; ++kt)
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) mma_bf16_16816(acc[nt], af[kt], bt[nt][kt][0], bt[nt][kt][1]);
+        // Off the chain: dW[16w.., :] += H_{t-1}^T D.
+        {
+          uint32_t ha[4];
+          ha[0] = movmatrix_trans(pack2_bf16(Hp[0][0], Hp[0][1]));
+          ha[1] = movmatrix_trans(pack2_bf16(Hp[1][0], Hp[1][1]));
+          ha[2] = movmatrix_trans(pack2_bf16(Hp[0][2], Hp[0][3]));
+          ha[3] = movmatrix_trans(pack2_bf16(Hp[1][2], Hp[1][3]));
+#pragma unroll
+          for (int nt2 = 0; nt2 < 4; ++nt2) {
+            uint32_t bd[4];
+            ldmatrix_x4_trans(bd, ldsm_addr_b_trans(dt, nt2, lane));
+            mma_bf16_16816(dWacc[2 * nt2], ha, bd[0], bd[1]);
+            mma_bf16_16816(dWacc[2 * nt2 + 1], ha, bd[2], bd[3]);
+          }
+        }
+        // Off the chain: per-step partial reductions.
+        float* part = sPart + (pst * kPS + slot) * kSlotFloats;
+        {
+          float pq0 = 0.f, pq1 = 0.f, pk0 = 0.f, pk1 = 0.f, pf = 0.f;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              pq0 = fmaf(h[nt][e], u[nt][e], pq0);          // dq = H_t u
+              pq1 = fmaf(h[nt][e + 2], u[nt][e], pq1);
+              pk0 = fmaf(Dv[nt][e], vv[nt][e], pk0);        // dk = D v
+              pk1 = fmaf(Dv[nt][e + 2], vv[nt][e], pk1);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) pf = fmaf(Rv[nt][e], Hp[nt][e] - Z[nt][e], pf);  // <R, H_{t-1} - Z>
+          }
+#pragma unroll
+          for (int o = 1; o < 4; o <<= 1) {
+            pq0 += __shfl_xor_sync(0xffffffffu, pq0, o);
+            pq1 += __shfl_xor_sync(0xffffffffu, pq1, o);
+            pk0 += __shfl_xor_sync(0xffffffffu, pk0, o);
+            pk1 += __shfl_xor_sync(0xffffffffu, pk1, o);
+          }
+          if (qd == 0) {
+            part[w * 16 + g] = pq0;
+            part[w * 16 + g + 8] = pq1;
+            part[64 + w * 16 + g] = pk0;
+            part[64 + w * 16 + g + 8] = pk1;
+          }
+          // dv partial over this CTA's 16 rows: D^T k.
+          float pv[4];
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            pv[2 * nt + 0] = fmaf(Dv[nt][0], k0, Dv[nt][2] * k1);
+            pv[2 * nt + 1] = fmaf(Dv[nt][1], k0, Dv[nt][3] * k1);
+          }
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) pv[e] += __shfl_xor_sync(0xffffffffu, pv[e], o);
+            pf += __shfl_xor_sync(0xffffffffu, pf, o);
+          }
+          pf += __shfl_xor_sync(0xffffffffu, pf, 1);
+          pf += __shfl_xor_sync(0xffffffffu, pf, 2);
+          if (g == 0) {
+            *reinterpret_cast<float2*>(part + 128 + jcol0) = make_float2(pv[0], pv[1]);
+            *reinterpret_cast<float2*>(part + 128 + jcol0 + 8) = make_float2(pv[2], pv[3]);
+          }
+          if (lane == 0) part[192 + w] = pf;
+          if (cta_rank == 0 && g == 0) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+              dwr[nt][0] = fmaf(u[nt][0], vv[nt][0], dwr[nt][0]);
+              dwr[nt][1] = fmaf(u[nt][1], vv[nt][1], dwr[nt][1]);
+            }
+          }
+        }
+        if (slot == kPS - 1 || rs == T - 1) pending_pfull = ptile;
+        // C_{t-1}; H_{t-1} becomes the next step's H_t.
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            Cg[nt][e] = acc[nt][e];
+            h[nt][e] = Hp[nt][e];
+          }
+      }
+      if (!ok) break;
+      // The chunk buffer is free once every compute warp is past its last read.
+      named_bar_sync(1, 128);
+      if (threadIdx.x == 0) mbar_arrive(smem_u32(&cempty[cb]));
+    }
+    if (ok) {
+      named_bar_sync(1, 128);
+      if (pending_pfull >= 0 && threadIdx.x == 0) mbar_arrive(smem_u32(&pfull[pending_pfull % kPStages]));
+      // dW partial of this row block: rows m = 16w + g (+8), columns 8nt + 2qd (+1).
+      float* dwp = A.dW_part + static_cast<int64_t>(blockIdx.x) * kV * kV;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        const int col = 8 * nt + 2 * qd;
+        *reinterpret_cast<float2*>(dwp + (16 * w + g) * kV + col) = make_float2(dWacc[nt][0], dWacc[nt][1]);
+        *reinterpret_cast<float2*>(dwp + (16 * w + g + 8) * kV + col) = make_float2(dWacc[nt][2], dWacc[nt][3]);
+      }
+      if (cta_rank == 0 && g == 0) {
+        float* dst = A.dwr_part + static_cast<int64_t>(chain) * kV + jcol0;
+        *reinterpret_cast<float2*>(dst) = make_float2(dwr[0][0], dwr[0][1]);
+        *reinterpret_cast<float2*>(dst + 8) = make_float2(dwr[1][0], dwr[1][1]);
+      }
+    } else {
+      *abort_flag = 1;
+    }
+  } else if (warp == 4) {
+    // ======================= TMA producer (chunks, last first) =======================
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_dy);
+    }
+    const uint16_t* fg = static_cast<const uint16_t*>(A.f);
+    int issued = 0;
+    bool ok = true;
+    for (int ci = 0; ci < p.nchunks; ++ci) {
+      const int c = p.nchunks - 1 - ci;
+      const int cb = ci & 1;
+      if (ci >= 2 && !mbar_wait(smem_u32(&cempty[cb]), ((ci >> 1) - 1) & 1, abort_flag, status, kWhereBwdEmpty)) {
+        ok = false;
+        break;
+      }
+      const int t0 = c * CL;
+      uint8_t* cbuf = smem + p.cbuf_off + cb * p.cbuf_bytes;
+      float* cf = reinterpret_cast<float*>(cbuf + p.cf_off);
+      for (int s = lane; s < CL; s += 32) {
+        const int t = t0 + s;
+        cf[s] = (t < T) ? bf16_bits_to_f32(fg[(static_cast<int64_t>(b) * T + t) * N + n]) : 0.f;
+      }
+      __syncwarp();
+      const uint32_t fb = smem_u32(&cfull[cb]);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(fb, p.tx_bytes);
+        tma_load_4d(smem_u32(cbuf + p.cq_off), &tm_q, fb, cta_rank * kRows, n, t0, b);
+        tma_load_4d(smem_u32(cbuf + p.ck_off), &tm_k, fb, cta_rank * kRows, n, t0, b);
+        tma_load_4d(smem_u32(cbuf + p.cv_off), &tm_v, fb, 0, n, t0, b);
+        tma_load_4d(smem_u32(cbuf + p.cdy_off), &tm_dy, fb, 0, n, t0, b);
+      } else {
+        mbar_arrive(fb);
+      }
+      issued = ci + 1;
+    }
+    if (!ok) {
+      for (int ci = std::max(0, issued - 2); ci < issued; ++ci)
+        mbar_wait_timed(smem_u32(&cfull[ci & 1]), (ci >> 1) & 1, nullptr, kWhereBwdDrain);
+    }
+  } else {
+    // ======================= reducer: partial tiles -> dq, dk, dv, df =======================
+    const uint16_t* wr = static_cast<const uint16_t*>(A.w_r) + static_cast<int64_t>(n) * kV;
+    const float wr0 = bf16_bits_to_f32(wr[2 * lane]), wr1 = bf16_bits_to_f32(wr[2 * lane + 1]);
+    int done = 0;
+    for (int ptile = 0; ptile < p.nptiles; ++ptile) {
+      const int pst = ptile % kPStages;
+      const uint32_t par = (ptile / kPStages) & 1;
+      if (!mbar_wait(smem_u32(&pfull[pst]), par, abort_flag, status, kWhereBwdRec)) break;
+      fence_acq_rel_cluster();
+      if (lane < R) mbar_arrive_cluster(mapa_shared(smem_u32(&ppeer[pst]), lane));
+      if (!mbar_wait<true>(smem_u32(&ppeer[pst]), par, abort_flag, status, kWhereBwdPeer)) break;
+      const int rs0 = ptile * kPS;
+      const int nslots = min(kPS, T - rs0);
+      const float* base = sPart + pst * kPS * kSlotFloats;
+      // dq, dk: this CTA's 16 rows, summed over the four compute warps.
+      for (int slot = 0; slot < nslots; ++slot) {
+        const int t = T - 1 - (rs0 + slot);
+        const int64_t rowt = (static_cast<int64_t>(b) * T + t) * N + n;
+        const float* part = base + slot * kSlotFloats;
+        const int i = lane & 15;
+        const int off = (lane < 16) ? 0 : 64;
+        const float sum = ((part[off + i] + part[off + 16 + i]) + part[off + 32 + i]) + part[off + 48 + i];
+        float* dst = (lane < 16) ? A.dq : A.dk;
+        dst[rowt * A.K + cta_rank * kRows + i] = sum;
+      }
+      // dv, df: summed over the cluster's row blocks, in fixed order.
+      const uint32_t sbase = smem_u32(base);
+      for (int slot = cta_rank; slot < nslots; slot += R) {
+        const int t = T - 1 - (rs0 + slot);
+        const int64_t rowt = (static_cast<int64_t>(b) * T + t) * N + n;
+        float a0 = 0.f, a1 = 0.f, fsum = 0.f;
+        for (int pr = 0; pr < R; ++pr) {
+          const uint32_t ra = mapa_shared(sbase, pr) + static_cast<uint32_t>((slot * kSlotFloats + 128 + 2 * lane) * 4);
+          a0 += ld_shared_cluster_f32(ra);
+          a1 += ld_shared_cluster_f32(ra + 4);
+          if (lane < 4)
+            fsum += ld_shared_cluster_f32(mapa_shared(sbase, pr) +
+                                          static_cast<uint32_t>((slot * kSlotFloats + 192 + lane) * 4));
+        }
+        const float2 uu = *reinterpret_cast<const float2*>(A.dy + rowt * kV + 2 * lane);
+        *reinterpret_cast<float2*>(A.dv + rowt * kV + 2 * lane) = make_float2(fmaf(wr0, uu.x, a0), fmaf(wr1, uu.y, a1));
+        fsum += __shfl_xor_sync(0xffffffffu, fsum, 1);
+        fsum += __shfl_xor_sync(0xffffffffu, fsum, 2);
+        if (lane == 0) A.df[rowt] = fsum;
+      }
+      fence_acq_rel_cluster();
+      __syncwarp();
+      if (lane < R) mbar_arrive_cluster(mapa_shared(smem_u32(&pempty[pst]), lane));
+      done = ptile + 1;
+    }
+    for (int ptile = std::max(0, done - kPStages); ptile < done; ++ptile) {
+      if (!mbar_wait<true>(smem_u32(&pempty[ptile % kPStages]), (ptile / kPStages) & 1, abort_flag, status,
+                           kWhereBwdExit))
+        break;
+    }
+  }
+  __syncthreads();
+}
+
+inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+bool mma_backward_supported(int K, int V) { return V == kV && K % kRows == 0 && K >= kRows && K <= 128; }
+
+size_t mma_backward_scratch_bytes(int B, int N, int K, int V, int ckpt_every) {
+  (void)V;
+  const size_t ctas = static_cast<size_t>(B) * N * (K / kRows);
+  return ctas * (4 * static_cast<size_t>(ckpt_every) + 2) * 128 * 4 * sizeof(float);
+}
+
+cudaError_t launch_mma_backward(const BwdArgs& a, cudaStream_t stream) {
+  if (a.ckpt_every > kMaxChunk) return cudaErrorInvalidValue;
+  MmaBwdParams p{};
+  p.a = a;
+  p.R = a.K / kRows;
+  const int C = a.ckpt_every;
+  p.nchunks = (a.T + C - 1) / C;
+  p.nptiles = (a.T + kPS - 1) / kPS;
+  p.htile_off = 0;
+  p.dtile_off = 4096;
+  p.cbuf_off = 8192;
+  p.cq_off = 0;
+  p.ck_off = align_up(C * kRows * 2, 128);
+  p.cv_off = p.ck_off + align_up(C * kRows * 2, 128);
+  p.cdy_off = p.cv_off + align_up(C * kV * 2, 128);
+  p.cf_off = p.cdy_off + align_up(C * kV * 4, 128);
+  p.cbuf_bytes = align_up(p.cf_off + C * 4, 128);
+  p.part_off = p.cbuf_off + 2 * p.cbuf_bytes;
+  p.bar_off = p.part_off + kPStages * kPS * kSlotFloats * 4;
+  p.misc_off = p.bar_off + (4 + 3 * kPStages) * 8;
+  uint32_t smem = align_up(p.misc_off + 16, 128) + 1024;
+  smem = std::max<uint32_t>(smem, 120 * 1024);
+  p.tx_bytes = 2 * C * kRows * 2 + C * kV * 2 + C * kV * 4;
+
+  CUtensorMap mq, mk, mv, mdy;
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!make_tensor_map_btnx(&mq, a.q, bf, 2, a.B, a.T, a.N, a.K, kRows, C) ||
+      !make_tensor_map_btnx(&mk, a.k, bf, 2, a.B, a.T, a.N, a.K, kRows, C) ||
+      !make_tensor_map_btnx(&mv, a.v, bf, 2, a.B, a.T, a.N, kV, kV, C) ||
+      !make_tensor_map_btnx(&mdy, a.dy, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.B, a.T, a.N, kV, kV, C))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(mma_backward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.B * a.N * p.R));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(p.R);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, mma_backward_kernel, p, mq, mk, mv, mdy);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace m2rnn

@@ -1,0 +1,101 @@
+// Helpers for the register-resident warp-MMA scan kernels (V = 64 value
+// columns, 16 key rows per CTA): mma.sync m16n8k16 bf16 fragments, ldmatrix,
+// movmatrix, the XOR-swizzled 16 x 64 bf16 operand tile in shared memory,
+// and host-side TMA tensor-map construction.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace m2rnn {
+
+// D (16 x 8, fp32) += A (16 x 16, bf16, row) * B (16 x 8, bf16, col).
+// Fragment ownership, g = lane / 4, q = lane % 4:
+//   A: a0 = A[g][2q..2q+1], a1 = A[g+8][2q..], a2 = A[g][2q+8..], a3 = A[g+8][2q+8..]
+//   B: b0 = B[2q..2q+1][g], b1 = B[2q+8..2q+9][g]
+//   C/D: c0 = D[g][2q], c1 = D[g][2q+1], c2 = D[g+8][2q], c3 = D[g+8][2q+1]
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+// Transpose of an 8 x 8 bf16 tile held one b32 (two elements) per thread.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// A 16-row x 64-column bf16 tile, 128 bytes per row, 16-byte chunks XOR-
+// swizzled by (row mod 8) so that ldmatrix row fetches hit distinct banks.
+__device__ __forceinline__ uint32_t tile_off(int row, int col) {
+  return static_cast<uint32_t>(row * 128 + ((((col >> 3) ^ (row & 7)) & 7) << 4) + (col & 7) * 2);
+}
+
+// Address thread `lane` hands to ldmatrix.x4 for the 16 x 16 sub-tile at
+// column block kt (columns 16kt..16kt+15): matrices (rows 0-7, k 0-7),
+// (rows 8-15, k 0-7), (rows 0-7, k 8-15), (rows 8-15, k 8-15).
+__device__ __forceinline__ uint32_t ldsm_addr_a(uint32_t tile, int kt, int lane) {
+  const int mi = lane >> 3, r = lane & 7;
+  const int row = r + (mi & 1) * 8;
+  const int col = 16 * kt + (mi >> 1) * 8;
+  return tile + tile_off(row, col);
+}
+
+// Address for ldmatrix.x4.trans giving the B fragments (k = tile row, n =
+// tile column) of two adjacent n-tiles 16nt2..16nt2+15: matrices
+// (k 0-7, n 0-7), (k 8-15, n 0-7), (k 0-7, n 8-15), (k 8-15, n 8-15).
+__device__ __forceinline__ uint32_t ldsm_addr_b_trans(uint32_t tile, int nt2, int lane) {
+  const int mi = lane >> 3, r = lane & 7;
+  const int row = r + (mi & 1) * 8;
+  const int col = 16 * nt2 + (mi >> 1) * 8;
+  return tile + tile_off(row, col);
+}
+
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) { return pack_bf16x2(lo, hi); }
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Bounded wait without the CTA-wide abort flag: used by the compute warps,
+// which then agree on the outcome through a flag read after a named barrier.
+template <bool kClusterScope = false>
+__device__ __forceinline__ bool mbar_wait_timed(uint32_t bar, uint32_t parity, StatusBlock* status,
+                                                uint32_t where) {
+  volatile int never = 0;
+  return mbar_wait<kClusterScope>(bar, parity, &never, status, where);
+}
+
+// Host: 4-D bf16 / fp32 tensor map over [B][T][N][X] (X innermost), box
+// {bx, 1, by, 1}, no swizzle, zero fill out of bounds.
+bool make_tensor_map_btnx(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, int B,
+                          int T, int N, int X, int bx, int by);
+
+}  // namespace m2rnn

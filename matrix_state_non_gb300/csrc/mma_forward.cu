@@ -1,0 +1,372 @@
+// Register-resident forward scan for V = 64 value columns (bf16 inputs, fp32
+// state): the latency-optimised kernel for small-state, long-sequence work.
+//
+// Recurrence (reading notes on "M2RNN: Non-Linear RNNs with Matrix-Valued
+// States for Scalable Language Modeling", section 2.1, Eq. 10-12):
+//   Z_t = tanh(H_{t-1} W + k_t v_t^T),  H_t = f_t H_{t-1} + (1-f_t) Z_t,
+//   y_t = H_t^T q_t + w_r * v_t.
+//
+// Each chain (b, n) is split into K/16 row blocks (key rows never mix, notes
+// section 1.2), one CTA each; the CTAs of a chain form a cluster and sum the
+// readout through distributed shared memory, as in the tensor-memory kernel.
+// Inside a CTA four compute warps own 16 value columns each of the 16 x 64
+// state.  Per step a warp runs D = bf16(H_{t-1}) * W[:, its 16 columns] + k v^T
+// as eight m16n8k16 warp MMAs (W fragments live in registers for the whole
+// scan, the rank-1 write seeds the accumulator exactly), applies tanh and the
+// gate blend to its 8 fp32 state values per thread, and writes bf16(H_t) to a
+// swizzled shared tile that the four warps read back with ldmatrix after one
+// named barrier.  Nothing else sits on the serial chain: the readout of step
+// t-1 is reduced while the MMAs of step t are in flight.  This beats the
+// tcgen05 kernel when only ~16 rows share an SM: a dependent m16n8k16 takes
+// ~21 cycles, while a 4-instruction tcgen05 step costs several hundred cycles
+// from issue to completion (measured on GB300).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "internal.h"
+#include "mma_common.cuh"
+
+namespace m2rnn {
+namespace {
+
+constexpr int kV = 64;
+constexpr int kRows = 16;   // key rows per CTA
+constexpr int kS = 32;      // steps per input tile
+constexpr int kNS = 4;      // input stages
+constexpr int kYS = 2;      // readout partial stages
+constexpr int kThreads = 192;
+
+struct MmaFwdParams {
+  FwdArgs a;
+  int R;
+  int ntiles;
+  uint32_t abuf_off, stage_off, stage_bytes, q_off, k_off, v_off, f_off, y_off, bar_off, misc_off;
+  uint32_t tx_bytes;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    mma_forward_kernel(const __grid_constant__ MmaFwdParams p, const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int R = p.R;
+  const int T = p.a.T, N = p.a.N;
+  const int cta_rank = static_cast<int>(blockIdx.x) % R;
+  const int chain = static_cast<int>(blockIdx.x) / R;
+  const int b = chain / N, n = chain % N;
+  const int ntiles = p.ntiles;
+  const bool do_y = p.a.y != nullptr;
+  StatusBlock* status = p.a.status;
+
+  uint8_t* sStage = smem + p.stage_off;
+  float* sY = reinterpret_cast<float*>(smem + p.y_off);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.bar_off);
+  uint64_t* full = bars;
+  uint64_t* empty = full + kNS;
+  uint64_t* yfull = empty + kNS;
+  uint64_t* ypeer = yfull + kYS;
+  uint64_t* yempty = ypeer + kYS;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.misc_off);
+  volatile int* cabort = reinterpret_cast<volatile int*>(smem + p.misc_off + 4);
+  const uint32_t abuf0 = smem_u32(smem + p.abuf_off);  // two 2 KB bf16 tiles
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNS; ++i) {
+      mbar_init(smem_u32(&full[i]), 32);
+      mbar_init(smem_u32(&empty[i]), 1);
+    }
+    for (int i = 0; i < kYS; ++i) {
+      mbar_init(smem_u32(&yfull[i]), 1);
+      mbar_init(smem_u32(&ypeer[i]), R);
+      mbar_init(smem_u32(&yempty[i]), R);
+    }
+    *abort_flag = 0;
+    *cabort = 0;
+    fence_mbar_init_cluster();
+  }
+  for (int e = threadIdx.x; e < 2 * 2048 / 16; e += kThreads)
+    reinterpret_cast<uint4*>(smem + p.abuf_off)[e] = make_uint4(0, 0, 0, 0);  // H_0 = 0
+  cluster_sync_all();
+
+  if (warp < 4) {
+    // ---------------- compute warps ----------------
+    const int g = lane >> 2, qd = lane & 3;
+    const int w = warp;
+    // W fragments for this warp's 16 output columns: B[k][n] = W[k][16w + n].
+    const uint16_t* Wg = static_cast<const uint16_t*>(p.a.W) + static_cast<int64_t>(n) * kV * kV;
+    uint32_t bw[2][4][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int col = 16 * w + 8 * nt + g;
+#pragma unroll
+      for (int kt = 0; kt < 4; ++kt) {
+        const int k0 = 16 * kt + 2 * qd;
+        bw[nt][kt][0] = static_cast<uint32_t>(Wg[k0 * kV + col]) |
+                        (static_cast<uint32_t>(Wg[(k0 + 1) * kV + col]) << 16);
+        bw[nt][kt][1] = static_cast<uint32_t>(Wg[(k0 + 8) * kV + col]) |
+                        (static_cast<uint32_t>(Wg[(k0 + 9) * kV + col]) << 16);
+      }
+    }
+    // State: h[nt][0..3] = H[g][j], H[g][j+1], H[g+8][j], H[g+8][j+1], j = 16w + 8nt + 2qd.
+    float h[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) h[nt][c] = 0.f;
+    const int jcol0 = 16 * w + 2 * qd;
+    const int64_t row_g = static_cast<int64_t>(cta_rank) * kRows + g;
+    float q_prev0 = 0.f, q_prev1 = 0.f;
+    int ys_prev = 0, s_prev = 0;
+    bool have_prev = false;
+
+    auto readout = [&](float q0, float q1, int ys, int s) {
+      // y partial over this CTA's 16 rows for the warp's 16 columns.
+      float part[4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        part[2 * nt + 0] = fmaf(q0, h[nt][0], q1 * h[nt][2]);
+        part[2 * nt + 1] = fmaf(q0, h[nt][1], q1 * h[nt][3]);
+      }
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) part[u] += __shfl_xor_sync(0xffffffffu, part[u], o);
+      if (g == 0) {
+        float* dst = sY + (ys * kS + s) * kV + jcol0;
+        *reinterpret_cast<float2*>(dst) = make_float2(part[0], part[1]);
+        *reinterpret_cast<float2*>(dst + 8) = make_float2(part[2], part[3]);
+      }
+    };
+
+    bool ok = true;
+    for (int tile = 0; tile < ntiles; ++tile) {
+      const int st = tile % kNS;
+      const int ys = tile % kYS;
+      bool mine = mbar_wait_timed(smem_u32(&full[st]), (tile / kNS) & 1, status, kWhereFwdFull);
+      if (mine && do_y && tile >= kYS)
+        mine = mbar_wait_timed<true>(smem_u32(&yempty[ys]), ((tile / kYS) - 1) & 1, status, kWhereFwdYEmpty);
+      if (!mine) *cabort = 1;
+      named_bar_sync(1, 128);
+      if (*cabort) {  // every compute warp reads the flag after the same barrier
+        ok = false;
+        break;
+      }
+      const uint8_t* stage = sStage + st * p.stage_bytes;
+      const uint16_t* qs = reinterpret_cast<const uint16_t*>(stage + p.q_off);
+      const uint16_t* ks = reinterpret_cast<const uint16_t*>(stage + p.k_off);
+      const uint16_t* vs = reinterpret_cast<const uint16_t*>(stage + p.v_off);
+      const float* fs = reinterpret_cast<const float*>(stage + p.f_off);
+      const int nsteps = min(kS, T - tile * kS);
+      for (int s = 0; s < nsteps; ++s) {
+        const int t = tile * kS + s;
+        // Inputs of step t.
+        const float k0 = bf16_bits_to_f32(ks[s * kRows + g]);
+        const float k1 = bf16_bits_to_f32(ks[s * kRows + g + 8]);
+        const float omf = 1.f - fs[s];
+        float acc[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const uint32_t vv = *reinterpret_cast<const uint32_t*>(vs + s * kV + jcol0 + 8 * nt);
+          const float v0 = bf16lo(vv), v1 = bf16hi(vv);
+          acc[nt][0] = k0 * v0;  // exact: products of bf16 values fit in fp32
+          acc[nt][1] = k0 * v1;
+          acc[nt][2] = k1 * v0;
+          acc[nt][3] = k1 * v1;
+        }
+        // H_{t-1} (bf16) as the A operand.
+        const uint32_t atile = abuf0 + (t & 1) * 2048;
+        uint32_t af[4][4];
+#pragma unroll
+        for (int kt = 0; kt < 4; ++kt) ldmatrix_x4(af[kt], ldsm_addr_a(atile, kt, lane));
+#pragma unroll
+        for (int kt = 0; kt < 4; ++kt)
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) mma_bf16_16816(acc[nt], af[kt], bw[nt][kt][0], bw[nt][kt][1]);
+        // Off the chain, while the MMAs run: readout of step t-1 (h holds H_{t-1}).
+        if (do_y && have_prev) readout(q_prev0, q_prev1, ys_prev, s_prev);
+        // Eq. 10-11 on this thread's 8 state values; bf16(H_t) to the other tile.
+        const uint32_t otile = abuf0 + ((t + 1) & 1) * 2048;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float z = tanh_fast(acc[nt][c]);
+            h[nt][c] = fmaf(omf, z - h[nt][c], h[nt][c]);
+          }
+          const int col = jcol0 + 8 * nt;
+          st_shared_b32(otile + tile_off(g, col), pack2_bf16(h[nt][0], h[nt][1]));
+          st_shared_b32(otile + tile_off(g + 8, col), pack2_bf16(h[nt][2], h[nt][3]));
+        }
+        if (p.a.ckpt != nullptr && (t + 1) % p.a.ckpt_every == 0 && t + 1 < T) {
+          float* dst = p.a.ckpt +
+                       ((static_cast<int64_t>(chain) * p.a.n_ckpt + (t + 1) / p.a.ckpt_every - 1) * p.a.K +
+                        row_g) * kV + jcol0;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            *reinterpret_cast<float2*>(dst + 8 * nt) = make_float2(h[nt][0], h[nt][1]);
+            *reinterpret_cast<float2*>(dst + 8 * kV + 8 * nt) = make_float2(h[nt][2], h[nt][3]);
+          }
+        }
+        q_prev0 = bf16_bits_to_f32(qs[s * kRows + g]);
+        q_prev1 = bf16_bits_to_f32(qs[s * kRows + g + 8]);
+        const bool prev_was_tile_end = have_prev && s == 0;  // y of the last step of the previous tile
+        have_prev = true;
+        ys_prev = ys;
+        s_prev = s;
+        named_bar_sync(1, 128);
+        if (do_y && prev_was_tile_end && threadIdx.x == 0) mbar_arrive(smem_u32(&yfull[(tile + kYS - 1) % kYS]));
+      }
+      // Every compute warp is past its last read of this stage.
+      if (threadIdx.x == 0) mbar_arrive(smem_u32(&empty[st]));
+    }
+    if (ok) {
+      if (do_y && have_prev) {
+        readout(q_prev0, q_prev1, ys_prev, s_prev);
+        named_bar_sync(1, 128);
+        if (threadIdx.x == 0) mbar_arrive(smem_u32(&yfull[ys_prev]));
+      }
+      if (p.a.H_T != nullptr) {
+        float* dst = p.a.H_T + (static_cast<int64_t>(chain) * p.a.K + row_g) * kV + jcol0;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          *reinterpret_cast<float2*>(dst + 8 * nt) = make_float2(h[nt][0], h[nt][1]);
+          *reinterpret_cast<float2*>(dst + 8 * kV + 8 * nt) = make_float2(h[nt][2], h[nt][3]);
+        }
+      }
+    } else {
+      *abort_flag = 1;
+    }
+  } else if (warp == 4) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+    }
+    const uint16_t* fg = static_cast<const uint16_t*>(p.a.f);
+    int issued = 0;
+    bool ok = true;
+    for (int tile = 0; tile < ntiles; ++tile) {
+      const int st = tile % kNS;
+      if (tile >= kNS &&
+          !mbar_wait(smem_u32(&empty[st]), ((tile / kNS) - 1) & 1, abort_flag, status, kWhereFwdEmpty)) {
+        ok = false;
+        break;
+      }
+      const int t0 = tile * kS;
+      uint8_t* stage = sStage + st * p.stage_bytes;
+      float fv = 0.f;
+      if (t0 + lane < T) fv = bf16_bits_to_f32(fg[(static_cast<int64_t>(b) * T + t0 + lane) * N + n]);
+      reinterpret_cast<float*>(stage + p.f_off)[lane] = fv;
+      __syncwarp();
+      const uint32_t fb = smem_u32(&full[st]);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(fb, p.tx_bytes);
+        tma_load_4d(smem_u32(stage + p.q_off), &tm_q, fb, cta_rank * kRows, n, t0, b);
+        tma_load_4d(smem_u32(stage + p.k_off), &tm_k, fb, cta_rank * kRows, n, t0, b);
+        tma_load_4d(smem_u32(stage + p.v_off), &tm_v, fb, 0, n, t0, b);
+      } else {
+        mbar_arrive(fb);
+      }
+      issued = tile + 1;
+    }
+    if (!ok) {
+      for (int tile = std::max(0, issued - kNS); tile < issued; ++tile)
+        mbar_wait_timed(smem_u32(&full[tile % kNS]), (tile / kNS) & 1, nullptr, kWhereFwdDrain);
+    }
+  } else if (do_y) {
+    // ---------------- readout reducer (sum over the chain's row blocks) ----------------
+    const uint16_t* vg = static_cast<const uint16_t*>(p.a.v);
+    const uint16_t* wr = static_cast<const uint16_t*>(p.a.w_r) + static_cast<int64_t>(n) * kV;
+    const float wr0 = bf16_bits_to_f32(wr[2 * lane]), wr1 = bf16_bits_to_f32(wr[2 * lane + 1]);
+    int done = 0;
+    for (int tile = 0; tile < ntiles; ++tile) {
+      const int ys = tile % kYS;
+      const uint32_t par = (tile / kYS) & 1;
+      if (!mbar_wait(smem_u32(&yfull[ys]), par, abort_flag, status, kWhereFwdYFull)) break;
+      fence_acq_rel_cluster();
+      if (lane < R) mbar_arrive_cluster(mapa_shared(smem_u32(&ypeer[ys]), lane));
+      if (!mbar_wait<true>(smem_u32(&ypeer[ys]), par, abort_flag, status, kWhereFwdYPeer)) break;
+      const int t0 = tile * kS;
+      const int nsteps = min(kS, T - t0);
+      const uint32_t ybase = smem_u32(sY + ys * kS * kV);
+      for (int s = cta_rank; s < nsteps; s += R) {
+        const int64_t row = (static_cast<int64_t>(b) * T + t0 + s) * N + n;
+        float a0 = 0.f, a1 = 0.f;
+        for (int pr = 0; pr < R; ++pr) {  // fixed order over the chain's row blocks
+          const uint32_t ra = mapa_shared(ybase, pr) + static_cast<uint32_t>((s * kV + 2 * lane) * 4);
+          a0 += ld_shared_cluster_f32(ra);
+          a1 += ld_shared_cluster_f32(ra + 4);
+        }
+        const uint32_t vv = *reinterpret_cast<const uint32_t*>(vg + row * kV + 2 * lane);
+        *reinterpret_cast<float2*>(p.a.y + row * kV + 2 * lane) =
+            make_float2(fmaf(wr0, bf16lo(vv), a0), fmaf(wr1, bf16hi(vv), a1));
+      }
+      fence_acq_rel_cluster();
+      __syncwarp();
+      if (lane < R) mbar_arrive_cluster(mapa_shared(smem_u32(&yempty[ys]), lane));
+      done = tile + 1;
+    }
+    for (int tile = std::max(0, done - kYS); tile < done; ++tile) {
+      if (!mbar_wait<true>(smem_u32(&yempty[tile % kYS]), (tile / kYS) & 1, abort_flag, status, kWhereFwdExit))
+        break;
+    }
+  }
+  __syncthreads();
+}
+
+inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+bool mma_forward_supported(int K, int V) { return V == kV && K % kRows == 0 && K >= kRows && K <= 128; }
+
+cudaError_t launch_mma_forward(const FwdArgs& a, cudaStream_t stream) {
+  MmaFwdParams p{};
+  p.a = a;
+  p.R = a.K / kRows;
+  p.ntiles = (a.T + kS - 1) / kS;
+  p.abuf_off = 0;
+  p.stage_off = 4096;
+  p.q_off = 0;
+  p.k_off = align_up(kS * kRows * 2, 128);
+  p.v_off = p.k_off + align_up(kS * kRows * 2, 128);
+  p.f_off = p.v_off + align_up(kS * kV * 2, 128);
+  p.stage_bytes = align_up(p.f_off + kS * 4, 128);
+  p.y_off = p.stage_off + kNS * p.stage_bytes;
+  p.bar_off = p.y_off + kYS * kS * kV * 4;
+  p.misc_off = p.bar_off + (2 * kNS + 3 * kYS) * 8;
+  uint32_t smem = align_up(p.misc_off + 16, 128) + 1024;
+  smem = std::max<uint32_t>(smem, 120 * 1024);  // one CTA per SM
+  p.tx_bytes = 2 * kS * kRows * 2 + kS * kV * 2;
+
+  CUtensorMap mq, mk, mv;
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!make_tensor_map_btnx(&mq, a.q, bf, 2, a.B, a.T, a.N, a.K, kRows, kS) ||
+      !make_tensor_map_btnx(&mk, a.k, bf, 2, a.B, a.T, a.N, a.K, kRows, kS) ||
+      !make_tensor_map_btnx(&mv, a.v, bf, 2, a.B, a.T, a.N, kV, kV, kS))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(mma_forward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.B * a.N * p.R));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(p.R);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, mma_forward_kernel, p, mq, mk, mv);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace m2rnn

@@ -32,9 +32,9 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <mutex>
 
 #include "internal.h"
+#include "mma_common.cuh"
 #include "ptx.cuh"
 
 namespace m2rnn {
@@ -406,36 +406,6 @@ __global__ void __launch_bounds__(320, 1)
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
-
-// 4-D bf16 tensor map over [B][T][N][X] (innermost X), box {bx, 1, by, 1}.
-bool make_map_btnx(CUtensorMap* m, const void* base, int B, int T, int N, int X, int bx, int by) {
-  auto enc = get_encode_fn();
-  if (enc == nullptr) return false;
-  cuuint64_t dims[4] = {static_cast<cuuint64_t>(X), static_cast<cuuint64_t>(N),
-                        static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(B)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(X) * 2, static_cast<cuuint64_t>(N) * X * 2,
-                           static_cast<cuuint64_t>(T) * N * X * 2};
-  cuuint32_t box[4] = {static_cast<cuuint32_t>(bx), 1, static_cast<cuuint32_t>(by), 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
-                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
 template <int V, int ROWS>
@@ -468,9 +438,10 @@ cudaError_t launch_cfg(const FwdArgs& a, int G, int R, cudaStream_t stream) {
   p.tx_bytes = 2 * kS * p.NRtot * 2 + kS * V * 2;
 
   CUtensorMap mq, mk, mv;
-  if (!make_map_btnx(&mq, a.q, a.B, a.T, a.N, a.K, p.NRtot, kS) ||
-      !make_map_btnx(&mk, a.k, a.B, a.T, a.N, a.K, p.NRtot, kS) ||
-      !make_map_btnx(&mv, a.v, a.B, a.T, a.N, V, V, kS))
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!make_tensor_map_btnx(&mq, a.q, bf, 2, a.B, a.T, a.N, a.K, p.NRtot, kS) ||
+      !make_tensor_map_btnx(&mk, a.k, bf, 2, a.B, a.T, a.N, a.K, p.NRtot, kS) ||
+      !make_tensor_map_btnx(&mv, a.v, bf, 2, a.B, a.T, a.N, V, V, kS))
     return cudaErrorInvalidValue;
 
   auto kern = tc_forward_kernel<V, ROWS>;

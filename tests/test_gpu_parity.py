@@ -200,3 +200,47 @@ def test_backward_is_deterministic():
     b = gpu_backward(inp, ckpt_every=16)
     for name in a:
         assert np.array_equal(a[name], b[name]), name
+
+
+# ---------------------------------------------------------------------------
+# Every kernel family on the shapes they share (V = 64): the dispatcher picks
+# the warp-MMA kernels; M2RNN_KERNEL selects the others explicitly.
+# ---------------------------------------------------------------------------
+@pytest.fixture
+def kernel_family(request, monkeypatch):
+    monkeypatch.setenv("M2RNN_KERNEL", request.param)
+    return request.param
+
+
+@pytest.mark.parametrize("kernel_family", ["mma", "tcgen05", "simt"], indirect=True)
+@pytest.mark.parametrize("B,N,T,K,V", [(2, 3, 37, 64, 64), (1, 2, 70, 16, 64), (1, 1, 97, 128, 64),
+                                       (2, 1, 33, 48, 64), (1, 1, 1, 64, 64)])
+def test_forward_each_kernel_family(kernel_family, B, N, T, K, V):
+    from matrix_state_non_gb300 import binding
+    expect = {"mma": 2, "tcgen05": 1, "simt": 0}[kernel_family]
+    assert binding.m2rnn_path(K, V, binding.M2RNN_BF16) == expect
+    inp = make_inputs(B, N, T, K, V, "bf16", seed=T + K)
+    got = gpu_forward(inp, ckpt_every=16)
+    y_ref, H_ref, Hs, _ = oracle_forward(*oracle_args(inp), return_states=True)
+    check_forward(got, y_ref, H_ref, "bf16", label=(kernel_family, B, N, T, K, V))
+    for c in range((T - 1) // 16):
+        assert rel_fro(got["ckpt"][:, :, c], Hs[(c + 1) * 16]) <= 1e-2
+
+
+@pytest.mark.parametrize("kernel_family", ["mma", "simt"], indirect=True)
+@pytest.mark.parametrize("B,N,T,K,V,C", [(2, 2, 37, 64, 64, 16), (1, 1, 70, 32, 64, 64),
+                                         (1, 2, 129, 16, 64, 128), (1, 1, 5, 64, 64, 1)])
+def test_backward_each_kernel_family(kernel_family, B, N, T, K, V, C):
+    inp = make_inputs(B, N, T, K, V, "bf16", seed=T + C, with_dy=True)
+    dH = np.random.default_rng(4).standard_normal((B, N, K, V)).astype(np.float32)
+    got = gpu_backward(inp, dH_T=dH, ckpt_every=C)
+    ref = oracle_backward(*oracle_args(inp), inp.exact["dy"], dH.astype(np.float64))
+    check_grads(got, ref, "bf16", label=(kernel_family, B, N, T, K, V, C))
+
+
+def test_backward_long_chunk_falls_back():
+    """Chunks longer than the warp-MMA backward's buffers run on the CUDA cores."""
+    inp = make_inputs(1, 1, 300, 64, 64, "bf16", seed=21, with_dy=True)
+    got = gpu_backward(inp, ckpt_every=256)
+    ref = oracle_backward(*oracle_args(inp), inp.exact["dy"])
+    check_grads(got, ref, "bf16")
