@@ -135,6 +135,43 @@ int m2rnn_backward(const void* q, const void* k, const void* v, const void* f,
  */
 int m2rnn_sync_status(void* workspace, void* cuda_stream, uint32_t* detail);
 
+/*
+ * Backward scan for callers that cannot allocate device memory: the same
+ * gradients as m2rnn_backward, with every scratch buffer taken from an array
+ * of 32 MiB built into the library's device image instead of a caller
+ * workspace.  (No counterpart in the paper: this is a deployment variant.)
+ *
+ * Who needs it: code that must not or cannot call cudaMalloc -- e.g. a
+ * plug-in inside a framework that owns all device memory, or a path where an
+ * allocation would synchronise the device or fail.  Such a caller passes only
+ * inputs and outputs.
+ *
+ * Limits: bf16 inputs, V = 64, K a multiple of 16 (<= 128), 1 <= ckpt_every
+ * <= 128, and `ckpt` (the forward's checkpoints for this ckpt_every) is
+ * required whenever T > ckpt_every.  A problem whose scratch would exceed the
+ * built-in 32 MiB returns M2RNN_ERR_WORKSPACE; other shapes return
+ * M2RNN_ERR_UNSUPPORTED.  Nothing is allocated, on the host or the device.
+ *
+ * The first call on a device looks the array's device address up (with that
+ * device current); make that first call before any stream capture on the
+ * device.  Every GPU that loads the library holds the array until exit.  All
+ * calls share the array and it keeps the last call's contents (this call
+ * clears what must start at zero): calls that overlap on the GPU race and
+ * corrupt each other's results.
+ *
+ * sync != 0: synchronise `cuda_stream` and return the device-side status
+ * (M2RNN_ERR_TIMEOUT / M2RNN_ERR_DEVICE) of this call; sync == 0: return
+ * after queuing the work.
+ */
+int m2rnn_backward_noalloc(const void* q, const void* k, const void* v,
+                           const void* f, const void* W, const void* w_r,
+                           const float* dy, const float* dH_T,
+                           const float* ckpt, int ckpt_every, float* dq,
+                           float* dk, float* dv, float* df, float* dW,
+                           float* dw_r, int64_t B, int64_t T, int64_t N,
+                           int64_t K, int64_t V, m2rnn_dtype dtype, int sync,
+                           void* cuda_stream);
+
 /* Which kernel family a call with these arguments would run:
  * 1 = tensor-core (tcgen05) kernels, 0 = fp32 CUDA-core kernels,
  * negative = the status the call would return. */

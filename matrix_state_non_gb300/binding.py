@@ -245,3 +245,18 @@ def to_device(inp, device="cuda"):
             t = torch.from_numpy(np.ascontiguousarray(arr))
         res[name] = t.to(device).contiguous()
     return res
+
+
+def m2rnn_backward_noalloc(q, k, v, f, W, w_r, dy, dH_T, ckpt, ckpt_every, dq, dk, dv, df, dW,
+                           dw_r, B, T, N, K, V, dtype, sync, stream) -> int:
+    """The backward for callers that cannot allocate device memory: scratch
+    comes from an array built into the library (see include/m2rnn.h for the
+    limits).  Integers are device addresses, as for m2rnn_backward."""
+    lib = load()
+    fn = lib.m2rnn_backward_noalloc
+    if fn.argtypes is None:
+        vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        fn.restype = ci
+        fn.argtypes = [vp] * 9 + [ci] + [vp] * 6 + [i64] * 5 + [ci, ci, vp]
+    return fn(q, k, v, f, W, w_r, dy, dH_T, ckpt, ckpt_every, dq, dk, dv, df, dW, dw_r, B, T, N,
+              K, V, dtype, sync, stream)
