@@ -396,6 +396,18 @@ def run_gpu(args, dist):
         for name in FWD_EXTRA:
             fwd_extra[name] = time_forward(name, binding, dev, stream, flush, pk, dist,
                                            reps=max(3, args.steps // 2))
+        # The same long-context workload on the tcgen05 kernel, for comparison
+        # with the kernel the dispatcher picks.
+        prev = os.environ.get("M2RNN_KERNEL")
+        os.environ["M2RNN_KERNEL"] = "tcgen05"
+        try:
+            fwd_extra["fwd_bf16_16k@tcgen05"] = time_forward("fwd_bf16_16k", binding, dev, stream, flush,
+                                                             pk, dist, reps=3)
+        finally:
+            if prev is None:
+                os.environ.pop("M2RNN_KERNEL", None)
+            else:
+                os.environ["M2RNN_KERNEL"] = prev
     cpu = cpu_baseline_sample() if (dist.rank == 0 and not args.no_cpu) else None
     launches_per_step = 3  # forward scan, backward scan, partial-sum reduction
     line = {
@@ -414,7 +426,8 @@ def run_gpu(args, dist):
         "gpu_launches": launches_per_step * args.steps,
         "step_breakdown_ms": {"forward": f_avg, "backward": b_avg},
         "forward": fwd_extra,
-        "kernels": {"forward": binding.m2rnn_path(K, V, binding.M2RNN_BF16) == 1 and "tcgen05" or "simt"},
+        "kernels": {"forward": {0: "simt", 1: "tcgen05", 2: "warp-mma"}.get(
+            binding.m2rnn_path(K, V, binding.M2RNN_BF16), "?"), "backward": "warp-mma"},
     }
     return line
 
@@ -446,7 +459,9 @@ def time_forward(name, binding, dev, stream, flush, pk, dist, reps=5):
     t_tensor = fl / (pk["bf16"] * 1e12)
     t_hbm = by / (pk["hbm_gbs"] * 1e9)
     del d, out
-    return {"workload": w["desc"], "ms": t, "value": dist.world * units(w) / (t * 1e-3), "unit": UNIT,
+    kern = {0: "simt", 1: "tcgen05", 2: "warp-mma"}.get(
+        binding.m2rnn_path(w["K"], w["V"], binding.M2RNN_BF16), "?")
+    return {"workload": w["desc"], "kernel": kern, "ms": t, "value": dist.world * units(w) / (t * 1e-3), "unit": UNIT,
             "ns_per_step_per_chain": t * 1e6 / w["T"],
             "roofline_ms": max(t_tensor, t_hbm) * 1e3,
             "roofline_frac": max(t_tensor, t_hbm) / (t * 1e-3),
