@@ -147,7 +147,7 @@ int m2rnn_sync_status(void* workspace, void* cuda_stream, uint32_t* detail);
  * inputs and outputs.
  *
  * Limits: bf16 inputs, V = 64, K a multiple of 16 (<= 128), 1 <= ckpt_every
- * <= 128, and `ckpt` (the forward's checkpoints for this ckpt_every) is
+ * <= 32, and `ckpt` (the forward's checkpoints for this ckpt_every) is
  * required whenever T > ckpt_every.  A problem whose scratch would exceed the
  * built-in 32 MiB returns M2RNN_ERR_WORKSPACE; other shapes return
  * M2RNN_ERR_UNSUPPORTED.  Nothing is allocated, on the host or the device.

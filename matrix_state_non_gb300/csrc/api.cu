@@ -32,7 +32,6 @@ bool dims_ok(int64_t B, int64_t T, int64_t N, int64_t K, int64_t V) {
 bool dtype_ok(int dt) { return dt == M2RNN_F32 || dt == M2RNN_BF16; }
 
 constexpr int kPathSimt = 0, kPathTc = 1, kPathMma = 2;
-constexpr int kMmaMaxChunk = 128;  // chunk buffers of the warp-MMA backward
 
 // Kernel family override for tests and benchmarks: M2RNN_KERNEL = auto |
 // tcgen05 | mma | simt.  A family that does not support the shape falls back
@@ -71,7 +70,7 @@ int choose_bwd_path(int64_t K, int64_t V, int dt, int ckpt_every) {
   const int path = choose_path(K, V, dt);
   if (path < 0) return path;
   const int k = static_cast<int>(K), v = static_cast<int>(V);
-  const bool mma = mma_backward_supported(k, v) && ckpt_every <= kMmaMaxChunk;
+  const bool mma = mma_backward_supported(k, v) && ckpt_every <= mma_backward_max_chunk();
   const bool tc = tc_backward_supported(k, v);
   if (path == kPathMma && mma) return kPathMma;
   if (path == kPathTc && tc) return kPathTc;

@@ -14,11 +14,12 @@
 // block, the blocks of a chain in one cluster (only dv_t and df_t sum over
 // rows; dW is summed later over row blocks and batch in a fixed order).
 // Four compute warps own 16 value columns each.  The time axis runs over
-// chunks of C steps, last chunk first.  For each chunk the forward is rerun
-// from its checkpoint (section 2.6 of the notes describes the paper's
+// chunks of C <= 32 steps, last chunk first.  For each chunk the forward is
+// rerun from its checkpoint (section 2.6 of the notes describes the paper's
 // rerun-and-cache backward; here only one chunk is cached), each thread
-// caching its own Z_t and H_t values (fp32) in a thread-private scratch that
-// stays in L2; then the chunk is walked backwards.  Per reverse step the
+// caching its own Z_t and H_{t-1} values (fp32) in its own lane of tensor
+// memory (32 steps x 16 values fill the 512 columns), so the cache never
+// touches DRAM; then the chunk is walked backwards.  Per reverse step the
 // serial chain is R -> D -> bf16(D) tile -> one named barrier -> 8 warp MMAs
 // seeded with f R -> C_{t-1}.  Off the chain: dW += H_{t-1}^T D as 8 more warp
 // MMAs per warp into register accumulators (H_{t-1}^T fragments by movmatrix,
@@ -41,7 +42,7 @@ constexpr int kRows = 16;
 constexpr int kPS = 32;      // reverse steps per partial tile
 constexpr int kPStages = 2;
 constexpr int kThreads = 192;
-constexpr int kMaxChunk = 128;
+constexpr int kMaxChunk = 32;   // the chunk cache fills the 512 TMEM columns at 32 steps
 constexpr int kSlotFloats = 4 * 16 + 4 * 16 + kV + 4;  // qpart, kpart, dvpart, dfpart
 
 struct MmaBwdParams {
@@ -53,10 +54,6 @@ struct MmaBwdParams {
   uint32_t part_off, bar_off, misc_off;
   uint32_t tx_bytes;
 };
-
-__device__ __forceinline__ float4 ldg_f4(const float* p) {
-  return *reinterpret_cast<const float4*>(p);
-}
 
 __global__ void __launch_bounds__(kThreads, 1)
     mma_backward_kernel(const __grid_constant__ MmaBwdParams p, const __grid_constant__ CUtensorMap tm_q,
@@ -81,6 +78,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* pempty = ppeer + kPStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.misc_off);
   volatile int* cabort = reinterpret_cast<volatile int*>(smem + p.misc_off + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + p.misc_off + 8);
   const uint32_t htile0 = smem_u32(smem + p.htile_off);
   const uint32_t dtile0 = smem_u32(smem + p.dtile_off);
 
@@ -98,7 +96,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     *cabort = 0;
     fence_mbar_init_cluster();
   }
+  if (warp == 0) {  // the whole tensor memory: the per-thread chunk cache
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
   cluster_sync_all();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
 
   if (warp < 4) {
     // ======================= compute warps =======================
@@ -142,10 +147,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int i = 0; i < 8; ++i) dWacc[i][0] = dWacc[i][1] = dWacc[i][2] = dWacc[i][3] = 0.f;
     float dwr[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-    // Thread-private chunk cache: H slots [CL+1][2 float4], Z slots [CL][2 float4].
-    float* scr = A.scratch + static_cast<int64_t>(blockIdx.x) * (4 * CL + 2) * 128 * 4;
-    auto hslot = [&](int sl) { return scr + (static_cast<int64_t>(sl) * 2 * 128 + tid) * 4; };
-    auto zslot = [&](int sl) { return scr + (static_cast<int64_t>(CL + 1 + sl) * 2 * 128 + tid) * 4; };
+    // Thread-private chunk cache in tensor memory: this thread owns TMEM lane
+    // `tid` (warp w reads and writes lanes 32w..32w+31); slot s = columns
+    // 16s..16s+15 hold {Z_s (8 values), H_{s-1} (8 values)}.
+    (void)tid;
+    const uint32_t tcache = tmem_base + (static_cast<uint32_t>(32 * w) << 16);
 
     bool ok = true;
     int rs = 0;                  // reverse steps done so far (processing order)
@@ -184,9 +190,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       {
-        float* hs = hslot(0);
-        *reinterpret_cast<float4*>(hs) = make_float4(h[0][0], h[0][1], h[0][2], h[0][3]);
-        *reinterpret_cast<float4*>(hs + 128 * 4) = make_float4(h[1][0], h[1][1], h[1][2], h[1][3]);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           const int col = jcol0 + 8 * nt;
@@ -219,42 +222,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int nt = 0; nt < 2; ++nt) mma_bf16_16816(acc[nt], af[kt], bw[nt][kt][0], bw[nt][kt][1]);
         const uint32_t otile = htile0 + ((s + 1) & 1) * 2048;
         float z[2][4];
+        uint32_t cache[16];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             z[nt][e] = tanh_fast(acc[nt][e]);
+            cache[4 * nt + e] = __float_as_uint(z[nt][e]);
+            cache[8 + 4 * nt + e] = __float_as_uint(h[nt][e]);  // H_{s-1}
             h[nt][e] = fmaf(omf, z[nt][e] - h[nt][e], h[nt][e]);
           }
           const int col = jcol0 + 8 * nt;
           st_shared_b32(otile + tile_off(g, col), pack2_bf16(h[nt][0], h[nt][1]));
           st_shared_b32(otile + tile_off(g + 8, col), pack2_bf16(h[nt][2], h[nt][3]));
         }
-        float* zs = zslot(s);
-        *reinterpret_cast<float4*>(zs) = make_float4(z[0][0], z[0][1], z[0][2], z[0][3]);
-        *reinterpret_cast<float4*>(zs + 128 * 4) = make_float4(z[1][0], z[1][1], z[1][2], z[1][3]);
-        float* hs = hslot(s + 1);
-        *reinterpret_cast<float4*>(hs) = make_float4(h[0][0], h[0][1], h[0][2], h[0][3]);
-        *reinterpret_cast<float4*>(hs + 128 * 4) = make_float4(h[1][0], h[1][1], h[1][2], h[1][3]);
+        tmem_st_32x32b_x16(tcache + 16 * s, cache);
         named_bar_sync(1, 128);
       }
+      tmem_st_wait();
 
       // ---------- reverse walk over the chunk ----------
-      // h holds H_t for the chunk's last step.  (Z_s, H_{s-1}) are prefetched
-      // two steps ahead through a two-deep register rotation.
-      float4 z1[2], h1[2], z2[2], h2[2];
-      auto load_slot = [&](int sl, float4 (&zz)[2], float4 (&hh)[2]) {
-        if (sl >= 0) {
-          const float* zs = zslot(sl);
-          const float* hs = hslot(sl);
-          zz[0] = ldg_f4(zs);
-          zz[1] = ldg_f4(zs + 128 * 4);
-          hh[0] = ldg_f4(hs);
-          hh[1] = ldg_f4(hs + 128 * 4);
-        }
-      };
-      load_slot(L - 1, z1, h1);
-      load_slot(L - 2, z2, h2);
+      // h holds H_t for the chunk's last step.  The next slot's TMEM load is
+      // issued one step ahead and waited for at the top of the step.
+      uint32_t slot_regs[16];
+      tmem_ld_32x32b<16>(tcache + 16 * (L - 1), slot_regs);
       for (int s = L - 1; s >= 0; --s, ++rs) {
         const int ptile = rs / kPS, slot = rs % kPS, pst = ptile % kPStages;
         if (slot == 0) {
@@ -288,13 +279,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           vv[nt][0] = bf16lo(vb);
           vv[nt][1] = bf16hi(vb);
         }
+        tmem_ld_wait();
+        tmem_ld_fence_regs(slot_regs);
         float Z[2][4], Hp[2][4];
-        Z[0][0] = z1[0].x; Z[0][1] = z1[0].y; Z[0][2] = z1[0].z; Z[0][3] = z1[0].w;
-        Z[1][0] = z1[1].x; Z[1][1] = z1[1].y; Z[1][2] = z1[1].z; Z[1][3] = z1[1].w;
-        Hp[0][0] = h1[0].x; Hp[0][1] = h1[0].y; Hp[0][2] = h1[0].z; Hp[0][3] = h1[0].w;
-        Hp[1][0] = h1[1].x; Hp[1][1] = h1[1].y; Hp[1][2] = h1[1].z; Hp[1][3] = h1[1].w;
-        z1[0] = z2[0]; z1[1] = z2[1]; h1[0] = h2[0]; h1[1] = h2[1];
-        load_slot(s - 2, z2, h2);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            Z[nt][e] = __uint_as_float(slot_regs[4 * nt + e]);
+            Hp[nt][e] = __uint_as_float(slot_regs[8 + 4 * nt + e]);
+          }
+        if (s > 0) tmem_ld_32x32b<16>(tcache + 16 * (s - 1), slot_regs);
         // R = C + q u^T ; D = (1-f) R (1 - Z^2)
         float Rv[2][4], Dv[2][4];
 #pragma unroll
@@ -535,7 +530,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
     }
   }
+  tc_fence_before_sync();
   __syncthreads();
+  if (warp == 0) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, 512);
+  }
 }
 
 inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
@@ -544,11 +544,9 @@ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
 bool mma_backward_supported(int K, int V) { return V == kV && K % kRows == 0 && K >= kRows && K <= 128; }
 
-size_t mma_backward_scratch_bytes(int B, int N, int K, int V, int ckpt_every) {
-  (void)V;
-  const size_t ctas = static_cast<size_t>(B) * N * (K / kRows);
-  return ctas * (4 * static_cast<size_t>(ckpt_every) + 2) * 128 * 4 * sizeof(float);
-}
+size_t mma_backward_scratch_bytes(int, int, int, int, int) { return 0; }  // the cache is in TMEM
+
+int mma_backward_max_chunk() { return kMaxChunk; }
 
 cudaError_t launch_mma_backward(const BwdArgs& a, cudaStream_t stream) {
   if (a.ckpt_every > kMaxChunk) return cudaErrorInvalidValue;

@@ -15,8 +15,11 @@
 // scan, the rank-1 write seeds the accumulator exactly), applies tanh and the
 // gate blend to its 8 fp32 state values per thread, and writes bf16(H_t) to a
 // swizzled shared tile that the four warps read back with ldmatrix after one
-// named barrier.  Nothing else sits on the serial chain: the readout of step
-// t-1 is reduced while the MMAs of step t are in flight.  This beats the
+// named barrier.  The readout of step t-1 runs on the tensor core too, while
+// the step-t MMAs are in flight: y^T = q^T H_{t-1} as one m16n8k16 per column
+// tile with q replicated over the A rows and H_{t-1} (fp32, split into bf16
+// high and low parts, transposed into B fragments with movmatrix) as B, so the
+// sum over rows needs no shuffles.  This beats the
 // tcgen05 kernel when only ~16 rows share an SM: a dependent m16n8k16 takes
 // ~21 cycles, while a 4-instruction tcgen05 step costs several hundred cycles
 // from issue to completion (measured on GB300).
@@ -119,6 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int jcol0 = 16 * w + 2 * qd;
     const int64_t row_g = static_cast<int64_t>(cta_rank) * kRows + g;
     float q_prev0 = 0.f, q_prev1 = 0.f;
+    uint32_t q_prev_lo = 0u, q_prev_hi = 0u;
     int ys_prev = 0, s_prev = 0;
     bool have_prev = false;
 
@@ -181,12 +185,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t af[4][4];
 #pragma unroll
         for (int kt = 0; kt < 4; ++kt) ldmatrix_x4(af[kt], ldsm_addr_a(atile, kt, lane));
+        // Readout of step t-1 on the tensor core: y^T = q^T H_{t-1} as an
+        // m16n8k16 with q replicated over the 16 A rows and H_{t-1} (split
+        // into bf16 hi + lo parts) as B, transposed from the accumulator
+        // layout with movmatrix.
+        uint32_t rb[2][2][2];
+        float yd[2][4];
+        if (do_y && have_prev) {
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            const uint32_t hi0 = pack2_bf16(h[nt][0], h[nt][1]);
+            const uint32_t hi1 = pack2_bf16(h[nt][2], h[nt][3]);
+            const uint32_t lo0 = pack2_bf16(h[nt][0] - bf16lo(hi0), h[nt][1] - bf16hi(hi0));
+            const uint32_t lo1 = pack2_bf16(h[nt][2] - bf16lo(hi1), h[nt][3] - bf16hi(hi1));
+            rb[nt][0][0] = movmatrix_trans(hi0);
+            rb[nt][0][1] = movmatrix_trans(hi1);
+            rb[nt][1][0] = movmatrix_trans(lo0);
+            rb[nt][1][1] = movmatrix_trans(lo1);
+            yd[nt][0] = yd[nt][1] = yd[nt][2] = yd[nt][3] = 0.f;
+          }
+        }
 #pragma unroll
         for (int kt = 0; kt < 4; ++kt)
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) mma_bf16_16816(acc[nt], af[kt], bw[nt][kt][0], bw[nt][kt][1]);
-        // Off the chain, while the MMAs run: readout of step t-1 (h holds H_{t-1}).
-        if (do_y && have_prev) readout(q_prev0, q_prev1, ys_prev, s_prev);
+        if (do_y && have_prev) {
+          uint32_t qa[4];
+          qa[0] = qa[1] = q_prev_lo;
+          qa[2] = qa[3] = q_prev_hi;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            mma_bf16_16816(yd[nt], qa, rb[nt][0][0], rb[nt][0][1]);
+            mma_bf16_16816(yd[nt], qa, rb[nt][1][0], rb[nt][1][1]);
+          }
+        }
         // Eq. 10-11 on this thread's 8 state values; bf16(H_t) to the other tile.
         const uint32_t otile = abuf0 + ((t + 1) & 1) * 2048;
 #pragma unroll
@@ -210,8 +242,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<float2*>(dst + 8 * kV + 8 * nt) = make_float2(h[nt][2], h[nt][3]);
           }
         }
-        q_prev0 = bf16_bits_to_f32(qs[s * kRows + g]);
-        q_prev1 = bf16_bits_to_f32(qs[s * kRows + g + 8]);
+        if (do_y && have_prev && g == 0) {
+          float* dst = sY + (ys_prev * kS + s_prev) * kV + jcol0;
+          *reinterpret_cast<float2*>(dst) = make_float2(yd[0][0], yd[0][1]);
+          *reinterpret_cast<float2*>(dst + 8) = make_float2(yd[1][0], yd[1][1]);
+        }
+        q_prev_lo = *reinterpret_cast<const uint32_t*>(qs + s * kRows + 2 * qd);
+        q_prev_hi = *reinterpret_cast<const uint32_t*>(qs + s * kRows + 2 * qd + 8);
         const bool prev_was_tile_end = have_prev && s == 0;  // y of the last step of the previous tile
         have_prev = true;
         ys_prev = ys;
@@ -224,6 +261,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok) {
       if (do_y && have_prev) {
+        {
+          // q rows g and g+8 from the packed pairs held by lanes with qd = g/2 (and +8).
+          const uint32_t lo = __shfl_sync(0xffffffffu, q_prev_lo, (g >> 1));
+          const uint32_t hi = __shfl_sync(0xffffffffu, q_prev_hi, (g >> 1));
+          q_prev0 = (g & 1) ? bf16hi(lo) : bf16lo(lo);
+          q_prev1 = (g & 1) ? bf16hi(hi) : bf16lo(hi);
+        }
         readout(q_prev0, q_prev1, ys_prev, s_prev);
         named_bar_sync(1, 128);
         if (threadIdx.x == 0) mbar_arrive(smem_u32(&yfull[ys_prev]));
@@ -370,3 +414,4 @@ cudaError_t launch_mma_forward(const FwdArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace m2rnn
+

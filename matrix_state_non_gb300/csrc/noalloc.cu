@@ -31,7 +31,6 @@ namespace {
 
 constexpr size_t kStaticScratchBytes = size_t(32) << 20;  // 32 MiB
 constexpr int kMaxDevices = 64;
-constexpr int kMaxChunk = 128;  // chunk buffers of the warp-MMA backward
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kStaticScratchBytes];
 
@@ -70,7 +69,7 @@ extern "C" int m2rnn_backward_noalloc(const void* q, const void* k, const void* 
     return M2RNN_ERR_INVALID_ARG;
   if (dtype != M2RNN_BF16 || !mma_backward_supported(static_cast<int>(K), static_cast<int>(V)))
     return M2RNN_ERR_UNSUPPORTED;
-  if (ckpt_every < 1 || ckpt_every > kMaxChunk) return M2RNN_ERR_UNSUPPORTED;
+  if (ckpt_every < 1 || ckpt_every > mma_backward_max_chunk()) return M2RNN_ERR_UNSUPPORTED;
   const int64_t nck = (T - 1) / ckpt_every;
   if (nck > 0 && ckpt == nullptr) return M2RNN_ERR_INVALID_ARG;  // checkpoints must come from the forward
   const void* req[] = {q, k, v, f, W, w_r, dy, dq, dk, dv, df, dW, dw_r};

@@ -253,6 +253,17 @@ __device__ __forceinline__ void tmem_ld_32x32b<64>(uint32_t taddr, uint32_t (&r)
   tmem_ld_32x32b<32>(taddr + 32, hi);
 }
 
+// Store 32 data-path lanes x 32 bits x 16 columns: thread i of the warp
+// writes lane (quadrant base + i), columns [col, col + 16).
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
 // Registers written by tcgen05.ld are only valid after tcgen05.wait::ld.  The
 // empty volatile asm below makes every later use depend on a point after the
 // wait, so the compiler cannot hoist a use above it.
