@@ -27,6 +27,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdlib>
 
 #include "internal.h"
 #include "mma_common.cuh"
@@ -39,7 +40,10 @@ constexpr int kRows = 16;   // key rows per CTA
 constexpr int kS = 32;      // steps per input tile
 constexpr int kNS = 4;      // input stages
 constexpr int kYS = 2;      // readout partial stages
-constexpr int kThreads = 192;
+// Compute warps per CTA: 8 / NT, each owning 8*NT of the 64 value columns
+// (NT n-tiles of 8).  Plus one TMA producer warp and one readout-reducer warp.
+template <int NT>
+constexpr int kThreadsFor() { return (8 / NT + 2) * 32; }
 
 struct MmaFwdParams {
   FwdArgs a;
@@ -49,7 +53,8 @@ struct MmaFwdParams {
   uint32_t tx_bytes;
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <int NT>
+__global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
     mma_forward_kernel(const __grid_constant__ MmaFwdParams p, const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -63,6 +68,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntiles = p.ntiles;
   const bool do_y = p.a.y != nullptr;
   StatusBlock* status = p.a.status;
+  constexpr int CW = 8 / NT;        // compute warps
+  constexpr int NCOL = 8 * NT;      // value columns per compute warp
+  constexpr int CT = CW * 32;       // compute threads (named barrier 1)
 
   uint8_t* sStage = smem + p.stage_off;
   float* sY = reinterpret_cast<float*>(smem + p.y_off);
@@ -90,20 +98,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     *cabort = 0;
     fence_mbar_init_cluster();
   }
-  for (int e = threadIdx.x; e < 2 * 2048 / 16; e += kThreads)
+  for (int e = threadIdx.x; e < 2 * 2048 / 16; e += static_cast<int>(blockDim.x))
     reinterpret_cast<uint4*>(smem + p.abuf_off)[e] = make_uint4(0, 0, 0, 0);  // H_0 = 0
   cluster_sync_all();
 
-  if (warp < 4) {
+  if (warp < CW) {
     // ---------------- compute warps ----------------
     const int g = lane >> 2, qd = lane & 3;
     const int w = warp;
-    // W fragments for this warp's 16 output columns: B[k][n] = W[k][16w + n].
+    // W fragments for this warp's output columns: B[k][n] = W[k][NCOL w + n].
     const uint16_t* Wg = static_cast<const uint16_t*>(p.a.W) + static_cast<int64_t>(n) * kV * kV;
-    uint32_t bw[2][4][2];
+    uint32_t bw[NT][4][2];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      const int col = 16 * w + 8 * nt + g;
+    for (int nt = 0; nt < NT; ++nt) {
+      const int col = NCOL * w + 8 * nt + g;
 #pragma unroll
       for (int kt = 0; kt < 4; ++kt) {
         const int k0 = 16 * kt + 2 * qd;
@@ -113,35 +121,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                         (static_cast<uint32_t>(Wg[(k0 + 9) * kV + col]) << 16);
       }
     }
-    // State: h[nt][0..3] = H[g][j], H[g][j+1], H[g+8][j], H[g+8][j+1], j = 16w + 8nt + 2qd.
-    float h[2][4];
+    // State: h[nt][0..3] = H[g][j], H[g][j+1], H[g+8][j], H[g+8][j+1], j = NCOL w + 8nt + 2qd.
+    float h[NT][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int c = 0; c < 4; ++c) h[nt][c] = 0.f;
-    const int jcol0 = 16 * w + 2 * qd;
+    const int jcol0 = NCOL * w + 2 * qd;
     const int64_t row_g = static_cast<int64_t>(cta_rank) * kRows + g;
     float q_prev0 = 0.f, q_prev1 = 0.f;
     uint32_t q_prev_lo = 0u, q_prev_hi = 0u;
+    int ck_left = p.a.ckpt_every, ck_idx = 0;  // countdown to the next checkpoint (no division per step)
     int ys_prev = 0, s_prev = 0;
     bool have_prev = false;
 
     auto readout = [&](float q0, float q1, int ys, int s) {
-      // y partial over this CTA's 16 rows for the warp's 16 columns.
-      float part[4];
+      // y partial over this CTA's 16 rows for the warp's columns (last step only).
+      float part[2 * NT];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
+      for (int nt = 0; nt < NT; ++nt) {
         part[2 * nt + 0] = fmaf(q0, h[nt][0], q1 * h[nt][2]);
         part[2 * nt + 1] = fmaf(q0, h[nt][1], q1 * h[nt][3]);
       }
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1)
 #pragma unroll
-        for (int u = 0; u < 4; ++u) part[u] += __shfl_xor_sync(0xffffffffu, part[u], o);
+        for (int u = 0; u < 2 * NT; ++u) part[u] += __shfl_xor_sync(0xffffffffu, part[u], o);
       if (g == 0) {
         float* dst = sY + (ys * kS + s) * kV + jcol0;
-        *reinterpret_cast<float2*>(dst) = make_float2(part[0], part[1]);
-        *reinterpret_cast<float2*>(dst + 8) = make_float2(part[2], part[3]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          *reinterpret_cast<float2*>(dst + 8 * nt) = make_float2(part[2 * nt], part[2 * nt + 1]);
       }
     };
 
@@ -153,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (mine && do_y && tile >= kYS)
         mine = mbar_wait_timed<true>(smem_u32(&yempty[ys]), ((tile / kYS) - 1) & 1, status, kWhereFwdYEmpty);
       if (!mine) *cabort = 1;
-      named_bar_sync(1, 128);
+      named_bar_sync(1, CT);
       if (*cabort) {  // every compute warp reads the flag after the same barrier
         ok = false;
         break;
@@ -170,9 +180,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float k0 = bf16_bits_to_f32(ks[s * kRows + g]);
         const float k1 = bf16_bits_to_f32(ks[s * kRows + g + 8]);
         const float omf = 1.f - fs[s];
-        float acc[2][4];
+        float acc[NT][4];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int nt = 0; nt < NT; ++nt) {
           const uint32_t vv = *reinterpret_cast<const uint32_t*>(vs + s * kV + jcol0 + 8 * nt);
           const float v0 = bf16lo(vv), v1 = bf16hi(vv);
           acc[nt][0] = k0 * v0;  // exact: products of bf16 values fit in fp32
@@ -189,11 +199,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // m16n8k16 with q replicated over the 16 A rows and H_{t-1} (split
         // into bf16 hi + lo parts) as B, transposed from the accumulator
         // layout with movmatrix.
-        uint32_t rb[2][2][2];
-        float yd[2][4];
+        uint32_t rb[NT][2][2];
+        float yd[NT][4];
         if (do_y && have_prev) {
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
+          for (int nt = 0; nt < NT; ++nt) {
             const uint32_t hi0 = pack2_bf16(h[nt][0], h[nt][1]);
             const uint32_t hi1 = pack2_bf16(h[nt][2], h[nt][3]);
             const uint32_t lo0 = pack2_bf16(h[nt][0] - bf16lo(hi0), h[nt][1] - bf16hi(hi0));
@@ -208,13 +218,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kt = 0; kt < 4; ++kt)
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt) mma_bf16_16816(acc[nt], af[kt], bw[nt][kt][0], bw[nt][kt][1]);
+          for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[nt], af[kt], bw[nt][kt][0], bw[nt][kt][1]);
         if (do_y && have_prev) {
           uint32_t qa[4];
           qa[0] = qa[1] = q_prev_lo;
           qa[2] = qa[3] = q_prev_hi;
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
+          for (int nt = 0; nt < NT; ++nt) {
             mma_bf16_16816(yd[nt], qa, rb[nt][0][0], rb[nt][0][1]);
             mma_bf16_16816(yd[nt], qa, rb[nt][1][0], rb[nt][1][1]);
           }
@@ -222,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Eq. 10-11 on this thread's 8 state values; bf16(H_t) to the other tile.
         const uint32_t otile = abuf0 + ((t + 1) & 1) * 2048;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const float z = tanh_fast(acc[nt][c]);
@@ -232,20 +242,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           st_shared_b32(otile + tile_off(g, col), pack2_bf16(h[nt][0], h[nt][1]));
           st_shared_b32(otile + tile_off(g + 8, col), pack2_bf16(h[nt][2], h[nt][3]));
         }
-        if (p.a.ckpt != nullptr && (t + 1) % p.a.ckpt_every == 0 && t + 1 < T) {
+        if (p.a.ckpt != nullptr && --ck_left == 0) {  // H_{t+1} starts a chunk: checkpoint it
+          ck_left = p.a.ckpt_every;
+          ++ck_idx;
+        }
+        if (p.a.ckpt != nullptr && ck_left == p.a.ckpt_every && t + 1 < T) {
           float* dst = p.a.ckpt +
-                       ((static_cast<int64_t>(chain) * p.a.n_ckpt + (t + 1) / p.a.ckpt_every - 1) * p.a.K +
-                        row_g) * kV + jcol0;
+                       ((static_cast<int64_t>(chain) * p.a.n_ckpt + ck_idx - 1) * p.a.K + row_g) * kV + jcol0;
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
+          for (int nt = 0; nt < NT; ++nt) {
             *reinterpret_cast<float2*>(dst + 8 * nt) = make_float2(h[nt][0], h[nt][1]);
             *reinterpret_cast<float2*>(dst + 8 * kV + 8 * nt) = make_float2(h[nt][2], h[nt][3]);
           }
         }
         if (do_y && have_prev && g == 0) {
           float* dst = sY + (ys_prev * kS + s_prev) * kV + jcol0;
-          *reinterpret_cast<float2*>(dst) = make_float2(yd[0][0], yd[0][1]);
-          *reinterpret_cast<float2*>(dst + 8) = make_float2(yd[1][0], yd[1][1]);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            *reinterpret_cast<float2*>(dst + 8 * nt) = make_float2(yd[nt][0], yd[nt][1]);
         }
         q_prev_lo = *reinterpret_cast<const uint32_t*>(qs + s * kRows + 2 * qd);
         q_prev_hi = *reinterpret_cast<const uint32_t*>(qs + s * kRows + 2 * qd + 8);
@@ -253,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         have_prev = true;
         ys_prev = ys;
         s_prev = s;
-        named_bar_sync(1, 128);
+        named_bar_sync(1, CT);
         if (do_y && prev_was_tile_end && threadIdx.x == 0) mbar_arrive(smem_u32(&yfull[(tile + kYS - 1) % kYS]));
       }
       // Every compute warp is past its last read of this stage.
@@ -269,13 +283,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           q_prev1 = (g & 1) ? bf16hi(hi) : bf16lo(hi);
         }
         readout(q_prev0, q_prev1, ys_prev, s_prev);
-        named_bar_sync(1, 128);
+        named_bar_sync(1, CT);
         if (threadIdx.x == 0) mbar_arrive(smem_u32(&yfull[ys_prev]));
       }
       if (p.a.H_T != nullptr) {
         float* dst = p.a.H_T + (static_cast<int64_t>(chain) * p.a.K + row_g) * kV + jcol0;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int nt = 0; nt < NT; ++nt) {
           *reinterpret_cast<float2*>(dst + 8 * nt) = make_float2(h[nt][0], h[nt][1]);
           *reinterpret_cast<float2*>(dst + 8 * kV + 8 * nt) = make_float2(h[nt][2], h[nt][3]);
         }
@@ -283,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       *abort_flag = 1;
     }
-  } else if (warp == 4) {
+  } else if (warp == CW) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -321,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = std::max(0, issued - kNS); tile < issued; ++tile)
         mbar_wait_timed(smem_u32(&full[tile % kNS]), (tile / kNS) & 1, nullptr, kWhereFwdDrain);
     }
-  } else if (do_y) {
+  } else if (warp == CW + 1 && do_y) {
     // ---------------- readout reducer (sum over the chain's row blocks) ----------------
     const uint16_t* vg = static_cast<const uint16_t*>(p.a.v);
     const uint16_t* wr = static_cast<const uint16_t*>(p.a.w_r) + static_cast<int64_t>(n) * kV;
@@ -364,11 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-}  // namespace
-
-bool mma_forward_supported(int K, int V) { return V == kV && K % kRows == 0 && K >= kRows && K <= 128; }
-
-cudaError_t launch_mma_forward(const FwdArgs& a, cudaStream_t stream) {
+template <int NT>
+cudaError_t launch_nt(const FwdArgs& a, cudaStream_t stream) {
   MmaFwdParams p{};
   p.a = a;
   p.R = a.K / kRows;
@@ -393,12 +404,12 @@ cudaError_t launch_mma_forward(const FwdArgs& a, cudaStream_t stream) {
       !make_tensor_map_btnx(&mk, a.k, bf, 2, a.B, a.T, a.N, a.K, kRows, kS) ||
       !make_tensor_map_btnx(&mv, a.v, bf, 2, a.B, a.T, a.N, kV, kV, kS))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(mma_forward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(mma_forward_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(a.B * a.N * p.R));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kThreadsFor<NT>());
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -408,9 +419,21 @@ cudaError_t launch_mma_forward(const FwdArgs& a, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, mma_forward_kernel, p, mq, mk, mv);
+  e = cudaLaunchKernelEx(&cfg, mma_forward_kernel<NT>, p, mq, mk, mv);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+}  // namespace
+
+bool mma_forward_supported(int K, int V) { return V == kV && K % kRows == 0 && K >= kRows && K <= 128; }
+
+// Tuning knob M2RNN_MMA_NT = 1 | 2: value-column tiles per compute warp
+// (1: eight compute warps, two per SM sub-partition; 2: four compute warps).
+cudaError_t launch_mma_forward(const FwdArgs& a, cudaStream_t stream) {
+  const char* e = std::getenv("M2RNN_MMA_NT");
+  if (e != nullptr && e[0] == '1') return launch_nt<1>(a, stream);
+  return launch_nt<2>(a, stream);
 }
 
 }  // namespace m2rnn
