@@ -24,8 +24,9 @@
 // seeded with f R -> C_{t-1}.  Off the chain: dW += H_{t-1}^T D as 8 more warp
 // MMAs per warp into register accumulators (H_{t-1}^T fragments by movmatrix,
 // D fragments by ldmatrix.trans), and the row/column reductions for dq, dk,
-// dv, df, written as per-step partials that a reducer warp sums (over warps,
-// and over the cluster's CTAs for dv, df) and stores.
+// dv, df, also as warp MMAs against replicated vectors (no shuffle chains),
+// written as per-step partials that a reducer warp sums (over warps, and over
+// the cluster's CTAs for dv, df) and stores.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -43,7 +44,7 @@ constexpr int kPS = 32;      // reverse steps per partial tile
 constexpr int kPStages = 2;
 constexpr int kThreads = 192;
 constexpr int kMaxChunk = 32;   // the chunk cache fills the 512 TMEM columns at 32 steps
-constexpr int kSlotFloats = 4 * 16 + 4 * 16 + kV + 4;  // qpart, kpart, dvpart, dfpart
+constexpr int kSlotFloats = 4 * 16 + 4 * 16 + kV + 4 * 16;  // dq, dk row partials, dv, df row partials
 
 struct MmaBwdParams {
   BwdArgs a;
@@ -343,52 +344,66 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Off the chain: per-step partial reductions.
         float* part = sPart + (pst * kPS + slot) * kSlotFloats;
         {
-          float pq0 = 0.f, pq1 = 0.f, pk0 = 0.f, pk1 = 0.f, pf = 0.f;
+          // Reductions on the tensor core (m16n8k16, fp32 accumulate), fp32
+          // operands split into bf16 high + low parts (products of the parts
+          // lose nothing that matters at fp32 accuracy):
+          //   row sums     dq = H_t u, dk = D v, df rows = (R * (H_{t-1} - Z)) 1
+          //                (A straight from the accumulator-layout registers,
+          //                 B = the vector replicated over the 8 columns)
+          //   column sums  dv = k^T D (A = k replicated over the rows,
+          //                 B = D transposed with movmatrix)
+          auto hl = [](float x0, float x1, uint32_t& hi, uint32_t& lo) {
+            hi = pack2_bf16(x0, x1);
+            lo = pack2_bf16(x0 - bf16lo(hi), x1 - bf16hi(hi));
+          };
+          uint32_t Ah[4], Al[4], Dh[4], Dl[4], Eh[4], El[4];
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
+            float E[4];
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              pq0 = fmaf(h[nt][e], u[nt][e], pq0);          // dq = H_t u
-              pq1 = fmaf(h[nt][e + 2], u[nt][e], pq1);
-              pk0 = fmaf(Dv[nt][e], vv[nt][e], pk0);        // dk = D v
-              pk1 = fmaf(Dv[nt][e + 2], vv[nt][e], pk1);
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) pf = fmaf(Rv[nt][e], Hp[nt][e] - Z[nt][e], pf);  // <R, H_{t-1} - Z>
+            for (int e = 0; e < 4; ++e) E[e] = Rv[nt][e] * (Hp[nt][e] - Z[nt][e]);
+            hl(h[nt][0], h[nt][1], Ah[2 * nt], Al[2 * nt]);
+            hl(h[nt][2], h[nt][3], Ah[2 * nt + 1], Al[2 * nt + 1]);
+            hl(Dv[nt][0], Dv[nt][1], Dh[2 * nt], Dl[2 * nt]);
+            hl(Dv[nt][2], Dv[nt][3], Dh[2 * nt + 1], Dl[2 * nt + 1]);
+            hl(E[0], E[1], Eh[2 * nt], El[2 * nt]);
+            hl(E[2], E[3], Eh[2 * nt + 1], El[2 * nt + 1]);
           }
-#pragma unroll
-          for (int o = 1; o < 4; o <<= 1) {
-            pq0 += __shfl_xor_sync(0xffffffffu, pq0, o);
-            pq1 += __shfl_xor_sync(0xffffffffu, pq1, o);
-            pk0 += __shfl_xor_sync(0xffffffffu, pk0, o);
-            pk1 += __shfl_xor_sync(0xffffffffu, pk1, o);
-          }
-          if (qd == 0) {
-            part[w * 16 + g] = pq0;
-            part[w * 16 + g + 8] = pq1;
-            part[64 + w * 16 + g] = pk0;
-            part[64 + w * 16 + g + 8] = pk1;
-          }
-          // dv partial over this CTA's 16 rows: D^T k.
-          float pv[4];
+          uint32_t uh0, ul0, uh1, ul1;
+          hl(u[0][0], u[0][1], uh0, ul0);
+          hl(u[1][0], u[1][1], uh1, ul1);
+          const uint32_t vb0 = pack2_bf16(vv[0][0], vv[0][1]), vb1 = pack2_bf16(vv[1][0], vv[1][1]);  // exact
+          const uint32_t one2 = 0x3F803F80u;  // bf16 pair (1, 1)
+          float rq[4] = {0.f, 0.f, 0.f, 0.f}, rk[4] = {0.f, 0.f, 0.f, 0.f}, rf[4] = {0.f, 0.f, 0.f, 0.f};
+          mma_bf16_16816(rq, Ah, uh0, uh1);
+          mma_bf16_16816(rq, Al, uh0, uh1);
+          mma_bf16_16816(rq, Ah, ul0, ul1);
+          mma_bf16_16816(rk, Dh, vb0, vb1);
+          mma_bf16_16816(rk, Dl, vb0, vb1);
+          mma_bf16_16816(rf, Eh, one2, one2);
+          mma_bf16_16816(rf, El, one2, one2);
+          uint32_t ka[4];
+          ka[0] = ka[1] = *reinterpret_cast<const uint32_t*>(ck + s * kRows + 2 * qd);
+          ka[2] = ka[3] = *reinterpret_cast<const uint32_t*>(ck + s * kRows + 2 * qd + 8);
+          float rv[2][4];
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
-            pv[2 * nt + 0] = fmaf(Dv[nt][0], k0, Dv[nt][2] * k1);
-            pv[2 * nt + 1] = fmaf(Dv[nt][1], k0, Dv[nt][3] * k1);
+            rv[nt][0] = rv[nt][1] = rv[nt][2] = rv[nt][3] = 0.f;
+            mma_bf16_16816(rv[nt], ka, movmatrix_trans(Dh[2 * nt]), movmatrix_trans(Dh[2 * nt + 1]));
+            mma_bf16_16816(rv[nt], ka, movmatrix_trans(Dl[2 * nt]), movmatrix_trans(Dl[2 * nt + 1]));
           }
-#pragma unroll
-          for (int o = 4; o < 32; o <<= 1) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) pv[e] += __shfl_xor_sync(0xffffffffu, pv[e], o);
-            pf += __shfl_xor_sync(0xffffffffu, pf, o);
+          if (qd == 0) {  // column 0 of the row sums: rows g and g+8
+            part[w * 16 + g] = rq[0];
+            part[w * 16 + g + 8] = rq[2];
+            part[64 + w * 16 + g] = rk[0];
+            part[64 + w * 16 + g + 8] = rk[2];
+            part[192 + w * 16 + g] = rf[0];
+            part[192 + w * 16 + g + 8] = rf[2];
           }
-          pf += __shfl_xor_sync(0xffffffffu, pf, 1);
-          pf += __shfl_xor_sync(0xffffffffu, pf, 2);
-          if (g == 0) {
-            *reinterpret_cast<float2*>(part + 128 + jcol0) = make_float2(pv[0], pv[1]);
-            *reinterpret_cast<float2*>(part + 128 + jcol0 + 8) = make_float2(pv[2], pv[3]);
+          if (g == 0) {  // row 0 of the column sums
+            *reinterpret_cast<float2*>(part + 128 + jcol0) = make_float2(rv[0][0], rv[0][1]);
+            *reinterpret_cast<float2*>(part + 128 + jcol0 + 8) = make_float2(rv[1][0], rv[1][1]);
           }
-          if (lane == 0) part[192 + w] = pf;
           if (cta_rank == 0 && g == 0) {
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
@@ -505,18 +520,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = T - 1 - (rs0 + slot);
         const int64_t rowt = (static_cast<int64_t>(b) * T + t) * N + n;
         float a0 = 0.f, a1 = 0.f, fsum = 0.f;
-        for (int pr = 0; pr < R; ++pr) {
-          const uint32_t ra = mapa_shared(sbase, pr) + static_cast<uint32_t>((slot * kSlotFloats + 128 + 2 * lane) * 4);
-          a0 += ld_shared_cluster_f32(ra);
-          a1 += ld_shared_cluster_f32(ra + 4);
-          if (lane < 4)
-            fsum += ld_shared_cluster_f32(mapa_shared(sbase, pr) +
-                                          static_cast<uint32_t>((slot * kSlotFloats + 192 + lane) * 4));
+        for (int pr = 0; pr < R; ++pr) {  // fixed order over the chain's row blocks
+          const uint32_t pb = mapa_shared(sbase, pr) + static_cast<uint32_t>(slot * kSlotFloats * 4);
+          a0 += ld_shared_cluster_f32(pb + (128 + 2 * lane) * 4);
+          a1 += ld_shared_cluster_f32(pb + (128 + 2 * lane + 1) * 4);
+          fsum += ld_shared_cluster_f32(pb + (192 + 2 * lane) * 4) +
+                  ld_shared_cluster_f32(pb + (192 + 2 * lane + 1) * 4);
         }
         const float2 uu = *reinterpret_cast<const float2*>(A.dy + rowt * kV + 2 * lane);
         *reinterpret_cast<float2*>(A.dv + rowt * kV + 2 * lane) = make_float2(fmaf(wr0, uu.x, a0), fmaf(wr1, uu.y, a1));
-        fsum += __shfl_xor_sync(0xffffffffu, fsum, 1);
-        fsum += __shfl_xor_sync(0xffffffffu, fsum, 2);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) fsum += __shfl_xor_sync(0xffffffffu, fsum, o);  // fixed tree
         if (lane == 0) A.df[rowt] = fsum;
       }
       fence_acq_rel_cluster();

@@ -49,6 +49,7 @@ struct MmaFwdParams {
   FwdArgs a;
   int R;
   int ntiles;
+  int stall_tile;  // test hook: the producer never completes this tile (-1: off)
   uint32_t abuf_off, stage_off, stage_bytes, q_off, k_off, v_off, f_off, y_off, bar_off, misc_off;
   uint32_t tx_bytes;
 };
@@ -314,6 +315,10 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
         ok = false;
         break;
       }
+      if (tile == p.stall_tile) {  // failure-detection test: this stage never fills
+        issued = tile + 1;
+        continue;
+      }
       const int t0 = tile * kS;
       uint8_t* stage = sStage + st * p.stage_bytes;
       float fv = 0.f;
@@ -384,6 +389,13 @@ cudaError_t launch_nt(const FwdArgs& a, cudaStream_t stream) {
   p.a = a;
   p.R = a.K / kRows;
   p.ntiles = (a.T + kS - 1) / kS;
+  // Test hook for failure detection (single-CTA chains only, so no cluster
+  // peer is left waiting): M2RNN_TEST_STALL_TILE=n makes tile n never arrive;
+  // the consumers' bounded waits expire and the status block reports it.
+  p.stall_tile = -1;
+  if (const char* st = std::getenv("M2RNN_TEST_STALL_TILE")) {
+    if (p.R == 1) p.stall_tile = std::atoi(st);
+  }
   p.abuf_off = 0;
   p.stage_off = 4096;
   p.q_off = 0;

@@ -1,0 +1,121 @@
+"""C-ABI boundary checks that need no GPU: the library loads, exports every
+function include/m2rnn.h declares, and rejects bad arguments before touching
+the device (so these calls are safe on a host without a GPU)."""
+import os
+import re
+
+import pytest
+
+from matrix_state_non_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return binding.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "m2rnn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(m2rnn_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "m2rnn_forward" in names and "m2rnn_backward" in names
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_host_helpers(lib):
+    assert binding.m2rnn_version() >= 10000
+    assert binding.status_string(binding.M2RNN_ERR_WORKSPACE) == "workspace missing or too small"
+    assert binding.status_string(12345) == "unknown status"
+    assert binding.m2rnn_checkpoint_count(4096, 32) == 127
+    assert binding.m2rnn_checkpoint_count(64, 64) == 0
+    assert binding.m2rnn_checkpoint_count(0, 4) == -1
+    # kernel families: warp MMA for V=64 bf16, tcgen05 for V=128 bf16, fp32 CUDA cores otherwise
+    assert binding.m2rnn_path(64, 64, binding.M2RNN_BF16) == 2
+    assert binding.m2rnn_path(128, 128, binding.M2RNN_BF16) == 1
+    assert binding.m2rnn_path(16, 16, binding.M2RNN_F32) == 0
+    assert binding.m2rnn_path(200, 64, binding.M2RNN_BF16) == binding.M2RNN_ERR_UNSUPPORTED
+    assert binding.m2rnn_path(64, 64, 7) == binding.M2RNN_ERR_INVALID_ARG
+
+
+def test_workspace_sizes(lib):
+    assert binding.m2rnn_forward_workspace_size(2, 16384, 16, 64, 64, binding.M2RNN_BF16) == 256
+    assert binding.m2rnn_forward_workspace_size(0, 16, 1, 64, 64, binding.M2RNN_BF16) == 0
+    with_ck = binding.m2rnn_backward_workspace_size(4, 4096, 8, 64, 64, binding.M2RNN_BF16, 32, 1)
+    without = binding.m2rnn_backward_workspace_size(4, 4096, 8, 64, 64, binding.M2RNN_BF16, 32, 0)
+    assert without - with_ck >= 4 * 8 * 127 * 64 * 64 * 4  # the recomputed checkpoints
+    assert binding.m2rnn_backward_workspace_size(4, 4096, 8, 64, 64, binding.M2RNN_BF16, 0, 1) == 0
+    assert binding.m2rnn_backward_workspace_size(4, 4096, 8, 64, 64, binding.M2RNN_BF16, 5000, 1) == 0
+
+
+P = 1 << 20  # a 16-byte-aligned fake address: never dereferenced by these calls
+
+
+def fwd(**kw):
+    a = dict(q=P, k=P, v=P, f=P, W=P, w_r=P, y=P, H_T=None, ckpt=None, C=0, B=1, T=8, N=1, K=64, V=64,
+             dt=binding.M2RNN_BF16, ws=P, wsb=256, stream=None)
+    a.update(kw)
+    return binding.m2rnn_forward(a["q"], a["k"], a["v"], a["f"], a["W"], a["w_r"], a["y"], a["H_T"],
+                                 a["ckpt"], a["C"], a["B"], a["T"], a["N"], a["K"], a["V"], a["dt"],
+                                 a["ws"], a["wsb"], a["stream"])
+
+
+def test_forward_rejects_bad_arguments_without_a_device(lib):
+    assert fwd(q=None) == binding.M2RNN_ERR_INVALID_ARG
+    assert fwd(y=None) == binding.M2RNN_ERR_INVALID_ARG
+    assert fwd(k=P + 8) == binding.M2RNN_ERR_INVALID_ARG          # misaligned
+    assert fwd(H_T=P + 4) == binding.M2RNN_ERR_INVALID_ARG
+    assert fwd(B=0) == binding.M2RNN_ERR_INVALID_ARG
+    assert fwd(T=-3) == binding.M2RNN_ERR_INVALID_ARG
+    assert fwd(K=129) == binding.M2RNN_ERR_UNSUPPORTED
+    assert fwd(V=256) == binding.M2RNN_ERR_UNSUPPORTED
+    assert fwd(dt=9) == binding.M2RNN_ERR_INVALID_ARG
+    assert fwd(ckpt=P, C=0) == binding.M2RNN_ERR_INVALID_ARG
+    assert fwd(ws=None) == binding.M2RNN_ERR_WORKSPACE
+    assert fwd(wsb=128) == binding.M2RNN_ERR_WORKSPACE
+
+
+def bwd(**kw):
+    a = dict(dH=None, ckpt=None, C=32, dq=P, B=1, T=8, N=1, K=64, V=64, dt=binding.M2RNN_BF16, ws=P,
+             wsb=1 << 30)
+    a.update(kw)
+    return binding.m2rnn_backward(P, P, P, P, P, P, P, a["dH"], a["ckpt"], a["C"], a["dq"], P, P, P, P, P,
+                                  a["B"], a["T"], a["N"], a["K"], a["V"], a["dt"], a["ws"], a["wsb"], None)
+
+
+def test_backward_rejects_bad_arguments_without_a_device(lib):
+    assert bwd(dq=None) == binding.M2RNN_ERR_INVALID_ARG
+    assert bwd(dH=P + 2) == binding.M2RNN_ERR_INVALID_ARG
+    assert bwd(C=0) == binding.M2RNN_ERR_INVALID_ARG
+    assert bwd(C=4097) == binding.M2RNN_ERR_INVALID_ARG
+    assert bwd(K=0) == binding.M2RNN_ERR_INVALID_ARG
+    assert bwd(wsb=16) == binding.M2RNN_ERR_WORKSPACE
+    assert bwd(ws=None) == binding.M2RNN_ERR_WORKSPACE
+
+
+def test_noalloc_backward_rejects_unsupported_shapes_without_a_device(lib):
+    def call(**kw):
+        a = dict(C=32, B=1, T=64, N=1, K=64, V=64, dt=binding.M2RNN_BF16, ckpt=P)
+        a.update(kw)
+        return binding.m2rnn_backward_noalloc(P, P, P, P, P, P, P, None, a["ckpt"], a["C"], P, P, P, P, P, P,
+                                              a["B"], a["T"], a["N"], a["K"], a["V"], a["dt"], 0, None)
+    assert call(V=128) == binding.M2RNN_ERR_UNSUPPORTED
+    assert call(dt=binding.M2RNN_F32) == binding.M2RNN_ERR_UNSUPPORTED
+    assert call(C=33) == binding.M2RNN_ERR_UNSUPPORTED
+    assert call(ckpt=None) == binding.M2RNN_ERR_INVALID_ARG      # T > C needs the forward's checkpoints
+    assert call(B=4096, N=1024) == binding.M2RNN_ERR_WORKSPACE   # exceeds the built-in scratch
+
+
+def test_kernel_override_env(lib, monkeypatch):
+    monkeypatch.setenv("M2RNN_KERNEL", "tcgen05")
+    assert binding.m2rnn_path(64, 64, binding.M2RNN_BF16) == 1
+    monkeypatch.setenv("M2RNN_KERNEL", "simt")
+    assert binding.m2rnn_path(64, 64, binding.M2RNN_BF16) == 0
+    monkeypatch.setenv("M2RNN_KERNEL", "mma")
+    assert binding.m2rnn_path(128, 128, binding.M2RNN_BF16) == 1  # no warp-MMA kernel for V=128

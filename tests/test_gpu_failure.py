@@ -1,0 +1,36 @@
+"""Failure detection on the GPU without a GPU fault: a test hook withholds one
+input tile, the consumers' bounded waits expire (about 2 s), the kernel
+records a timeout in the workspace status block and returns, and the context
+stays usable for the next call."""
+import numpy as np
+import pytest
+
+from matrix_state_non_gb300.inputs import make_inputs
+from oracle import forward as oracle_forward
+from parity_util import check_forward, gpu_forward, oracle_args
+
+pytestmark = pytest.mark.gpu
+
+NAMES = ("q", "k", "v", "f", "W", "w_r")
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(monkeypatch):
+    import torch
+    from matrix_state_non_gb300 import binding
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA GPU required for -m gpu tests")
+    # K = 16 rows: one CTA per chain, no cluster peer left waiting.
+    inp = make_inputs(1, 1, 200, 16, 64, "bf16", seed=3)
+    d = binding.to_device(inp)
+    monkeypatch.setenv("M2RNN_TEST_STALL_TILE", "1")
+    out = binding.forward(*(d[n] for n in NAMES))
+    st, detail = binding.sync_status(out["workspace"])
+    assert st == binding.M2RNN_ERR_TIMEOUT, binding.status_string(st)
+    # The consumers (input tile), the producer (free stage) and the reducer
+    # (readout tile) all wait on the withheld tile; whichever gives up first
+    # is recorded: any forward-kernel wait site (codes 1xx).
+    assert detail // 100 == 1, detail
+    monkeypatch.delenv("M2RNN_TEST_STALL_TILE")
+    got = gpu_forward(inp)  # the same context keeps working
+    y_ref, H_ref = oracle_forward(*oracle_args(inp))
+    check_forward(got, y_ref, H_ref, "bf16")
