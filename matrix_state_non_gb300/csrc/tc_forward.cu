@@ -14,19 +14,22 @@
 // Per step, per group of NR rows (one warpgroup), the transform runs on the
 // tensor core in transposed form
 //     D^T [V x NR] = W^T [V x V] * H_{t-1}^T [V x NR]      (M = 128, N = NR, K = V)
-// with A = W^T staged once (stacked 128/V times to fill M = 128, so the V = 64
-// case keeps all four TMEM lane quadrants busy), B = bf16(H_{t-1}) rewritten
-// every step, D in TMEM.  TMEM lane L holds value column j = L mod V, so each
+// with A = W^T written to tensor memory once (stacked 128/V times to fill
+// M = 128, so the V = 64 case keeps all four TMEM lane quadrants busy), B =
+// bf16(H_{t-1}) rewritten in shared memory every step, D in TMEM.  TMEM lane L holds value column j = L mod V, so each
 // thread owns a column j and ROWS rows of the state in fp32 registers: the
 // rank-1 add, tanh, gate blend and the readout over its rows are all
 // thread-local.  The bf16 copy of H_t goes back to shared memory as the next
 // MMA's B operand (MN-major: the thread's ROWS values are 16-byte runs).
 //
-// Warp roles: warps 0..4G-1 = G epilogue warpgroups (group g issues its own
-// MMAs from one elected thread); warp 4G = TMA producer for q/k/v tiles of
-// S = 32 steps (f through plain loads); warp 4G+1 = readout reducer, which
-// sums the per-group/per-CTA partial readouts of a tile, adds w_r * v and
-// stores y.  Every wait is bounded (see ptx.cuh).
+// Warp roles: warps 0..4G-1 = G epilogue warpgroups; warp 4G = the MMA warp,
+// which issues every group's MMAs from one elected lane of a converged warp,
+// alternating between the groups so that one group's MMAs overlap the other
+// group's tanh work (issuing a step's MMAs costs a few hundred cycles, so it
+// must not sit inside an epilogue warp); warp 4G+1 = TMA producer for q/k/v
+// tiles of S = 32 steps (f through plain loads); warp 4G+2 = readout reducer,
+// which sums the per-group/per-CTA partial readouts of a tile, adds w_r * v
+// and stores y.  Every wait is bounded (see ptx.cuh).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -51,7 +54,6 @@ struct FwdCfg {
   static constexpr int NR = ROWS * COPIES;      // rows per group = MMA N
   static constexpr int NS = (V == 64) ? 4 : 3;  // input pipeline stages
   static constexpr int KSTEPS = V / 16;         // MMAs per step (K = 16 each)
-  static constexpr uint32_t A_BYTES = 128u * V * 2u;
   static constexpr uint32_t B_BYTES = NR * V * 2u;
   static constexpr uint32_t SBO = V * 16u;  // next 8 rows (A) / next 8 columns (B)
   static constexpr uint32_t LBO = 128u;     // next 8 K-elements
@@ -64,6 +66,7 @@ struct TcFwdParams {
   int G, R, NRtot;
   int ntiles;
   uint32_t tmem_cols;
+  uint32_t a_tcol;  // TMEM column of the A operand (W^T stacked)
   uint32_t b_off, stage_off, stage_bytes, q_off, k_off, v_off, f_off;
   uint32_t y_off, bar_off, misc_off;
   uint32_t tx_bytes;
@@ -80,20 +83,8 @@ __device__ __forceinline__ void unpack8_bf16(const uint4 w, float (&o)[8]) {
   o[7] = __uint_as_float(w.w & 0xFFFF0000u);
 }
 
-template <class C>
-__device__ __forceinline__ void issue_step_mma(uint32_t d_tmem, uint32_t a_base, uint32_t b_base,
-                                               uint32_t idesc) {
-#pragma unroll
-  for (int kk = 0; kk < C::KSTEPS; ++kk) {
-    // K slice kk covers K-blocks 2kk and 2kk+1 (LBO apart) in both operands.
-    const uint64_t ad = smem_desc_noswizzle(a_base + kk * 2 * C::LBO, C::LBO, C::SBO);
-    const uint64_t bd = smem_desc_noswizzle(b_base + kk * 2 * C::LBO, C::LBO, C::SBO);
-    tc_mma_f16_ss(d_tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
-  }
-}
-
 template <int V, int ROWS>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     tc_forward_kernel(const __grid_constant__ TcFwdParams p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v) {
@@ -112,7 +103,6 @@ __global__ void __launch_bounds__(320, 1)
   const int slots = G * C::COPIES;
   StatusBlock* status = p.a.status;
 
-  uint8_t* sA = smem;
   uint8_t* sB = smem + p.b_off;
   uint8_t* sStage = smem + p.stage_off;
   float* sY = reinterpret_cast<float*>(smem + p.y_off);
@@ -150,18 +140,6 @@ __global__ void __launch_bounds__(320, 1)
     tmem_relinquish();
   }
   {
-    // A = [W^T; W^T; ...] (K-major, interleaved core matrices): A[row][m] = W[m][row mod V].
-    const uint16_t* W = static_cast<const uint16_t*>(p.a.W) + static_cast<int64_t>(n) * V * V;
-    for (int e = threadIdx.x; e < V * V; e += blockDim.x) {
-      const int m = e / V, j = e % V;
-      const uint16_t w = W[e];
-#pragma unroll
-      for (int c = 0; c < C::COPIES; ++c) {
-        const int row = c * V + j;
-        const uint32_t off = (row / 8) * C::SBO + (m / 8) * C::LBO + (row % 8) * 16 + (m % 8) * 2;
-        *reinterpret_cast<uint16_t*>(sA + off) = w;
-      }
-    }
     const uint4 zero = make_uint4(0, 0, 0, 0);
     for (uint32_t e = threadIdx.x * 16; e < static_cast<uint32_t>(G) * C::B_BYTES; e += blockDim.x * 16)
       *reinterpret_cast<uint4*>(sB + e) = zero;  // H_0 = 0
@@ -172,7 +150,28 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t idesc = idesc_bf16_f32(128, C::NR, /*a_mn_major=*/false, /*b_mn_major=*/true);
-  const uint32_t a_base = smem_u32(sA);
+  const uint32_t a_tmem = tmem_base + p.a_tcol;
+  if (warp < 4) {
+    // A = [W^T; W^T; ...] in tensor memory (M = 128 lanes, K = V): lane L holds
+    // row L, i.e. A[L][m] = W[m][L mod V], two bf16 per 32-bit column.  Warp w
+    // writes lanes 32w..32w+31.
+    const uint16_t* Wg = static_cast<const uint16_t*>(p.a.W) + static_cast<int64_t>(n) * V * V;
+    const int jr = (32 * warp + lane) % V;
+#pragma unroll
+    for (int c0 = 0; c0 < V / 2; c0 += 32) {
+      uint32_t regs[32];
+#pragma unroll
+      for (int u = 0; u < 32; ++u) {
+        const int m = 2 * (c0 + u);
+        regs[u] = static_cast<uint32_t>(Wg[m * V + jr]) | (static_cast<uint32_t>(Wg[(m + 1) * V + jr]) << 16);
+      }
+      tmem_st_32x32b_x32(a_tmem + (static_cast<uint32_t>(32 * warp) << 16) + c0, regs);
+    }
+    tmem_st_wait();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
 
   if (warp < 4 * G) {
     // ---------------- epilogue warpgroups ----------------
@@ -181,21 +180,14 @@ __global__ void __launch_bounds__(320, 1)
     const int j = L % V, c = L / V;  // c is uniform within a warp
     const int row_in_cta = g * C::NR + c * ROWS;
     const int64_t row_global = static_cast<int64_t>(cta_rank) * NRtot + row_in_cta;
-    const uint32_t b_base = smem_u32(sB + g * C::B_BYTES);
     const uint32_t dbar = smem_u32(&dfull[g]);
     const uint32_t hbar = smem_u32(&hready[g]);
-    const uint32_t d_tmem = tmem_base + g * C::NR;
     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * wq) << 16) + g * C::NR + c * ROWS;
     uint8_t* bslot = sB + g * C::B_BYTES + ((c * ROWS) / 8) * C::SBO + (j / 8) * C::LBO + (j % 8) * 16;
-    const bool issuer = (wq == 0 && lane == 0);
-    if (issuer) {  // step 0's transform: H_0 W = 0 (keeps the loop uniform)
-      issue_step_mma<C>(d_tmem, a_base, b_base, idesc);
-      tc_commit(dbar);
-    }
     float h[ROWS];
 #pragma unroll
     for (int r = 0; r < ROWS; ++r) h[r] = 0.f;
-    uint32_t dphase = 0, hphase = 0;
+    uint32_t dphase = 0;
     bool ok = true;
     for (int tile = 0; tile < ntiles && ok; ++tile) {
       const int st = tile % C::NS;
@@ -250,22 +242,11 @@ __global__ void __launch_bounds__(320, 1)
           *reinterpret_cast<uint4*>(bslot + (r0 / 8) * C::SBO) = pk;
         }
         // Hand bf16(H_t) to the tensor core: make the generic-proxy stores
-        // visible to the async proxy, then one arrival per warp; the group's
-        // issuing thread waits for all four (a bounded wait, unlike bar.sync).
+        // visible to the async proxy, then one arrival per warp for the MMA warp.
         fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(hbar);
-        if (issuer && t + 1 < T) {
-          if (!mbar_wait(hbar, hphase, abort_flag, status, kWhereFwdH)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-          issue_step_mma<C>(d_tmem, a_base, b_base, idesc);
-          tc_commit(dbar);
-        }
-        hphase ^= 1u;
         // ---- off the serial chain ----
         if (do_y) {
           const uint16_t* qr = qs + s * NRtot + row_in_cta;
@@ -304,6 +285,38 @@ __global__ void __launch_bounds__(320, 1)
     }
     if (!ok) *abort_flag = 1;
   } else if (warp == 4 * G) {
+    // ---------------- MMA warp: one converged warp issues every group's MMAs ----------------
+    // Step t of group g needs bf16(H_{t-1}) from that group's epilogue (step
+    // 0 multiplies H_0 = 0); the groups alternate, so one group's MMAs run
+    // while the other group's epilogue uses the special-function units.
+    // B descriptor of group g, K slice kk: the start-address field (bits 0-13,
+    // in 16-byte units) advances by (g * B_BYTES + kk * 2 * LBO) / 16.
+    const uint64_t bdesc0 = smem_desc_noswizzle(smem_u32(sB), C::LBO, C::SBO);
+    uint32_t hph = 0u;  // bit g: phase of hready[g]
+    bool ok = true;
+    for (int t = 0; t < T && ok; ++t) {
+      for (int g = 0; g < G; ++g) {
+        if (t > 0) {
+          if (!mbar_wait(smem_u32(&hready[g]), (hph >> g) & 1u, abort_flag, status, kWhereFwdH)) {
+            ok = false;
+            break;
+          }
+          hph ^= 1u << g;
+        }
+        if (elect_one()) {
+          tc_fence_after_sync();
+          const uint64_t bg = bdesc0 + ((static_cast<uint32_t>(g) * C::B_BYTES) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < C::KSTEPS; ++kk)
+            tc_mma_f16_ts(tmem_base + g * C::NR, a_tmem + kk * 8, bg + ((kk * 2 * C::LBO) >> 4), idesc,
+                          kk > 0 ? 1u : 0u);
+          tc_commit(smem_u32(&dfull[g]));
+        }
+        __syncwarp();
+      }
+    }
+    if (!ok) *abort_flag = 1;
+  } else if (warp == 4 * G + 1) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -343,7 +356,7 @@ __global__ void __launch_bounds__(320, 1)
         mbar_wait(smem_u32(&full[tile % C::NS]), (tile / C::NS) & 1, &never, nullptr, kWhereFwdDrain);
       }
     }
-  } else if (do_y) {
+  } else if (warp == 4 * G + 2 && do_y) {
     // ---------------- readout reducer ----------------
     const uint16_t* vg = static_cast<const uint16_t*>(p.a.v);
     const uint16_t* wr = static_cast<const uint16_t*>(p.a.w_r) + static_cast<int64_t>(n) * V;
@@ -417,10 +430,12 @@ cudaError_t launch_cfg(const FwdArgs& a, int G, int R, cudaStream_t stream) {
   p.R = R;
   p.NRtot = G * C::NR;
   p.ntiles = (a.T + kS - 1) / kS;
+  // TMEM: D accumulators (G x NR columns) then A = W^T (V/2 columns).
+  p.a_tcol = align_up(static_cast<uint32_t>(G * C::NR), 32);
   uint32_t cols = 32;
-  while (cols < static_cast<uint32_t>(G * C::NR)) cols *= 2;
+  while (cols < p.a_tcol + V / 2) cols *= 2;
   p.tmem_cols = cols;
-  p.b_off = C::A_BYTES;
+  p.b_off = 0;
   p.stage_off = align_up(p.b_off + G * C::B_BYTES, 128);
   p.q_off = 0;
   p.k_off = align_up(p.q_off + kS * p.NRtot * 2, 128);
@@ -453,7 +468,7 @@ cudaError_t launch_cfg(const FwdArgs& a, int G, int R, cudaStream_t stream) {
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(a.B * a.N * R));
-  cfg.blockDim = dim3(static_cast<unsigned>((4 * G + 2) * 32));
+  cfg.blockDim = dim3(static_cast<unsigned>((4 * G + 3) * 32));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
