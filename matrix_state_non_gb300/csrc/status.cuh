@@ -24,7 +24,8 @@ constexpr uint32_t kWhereFwdFull = 101, kWhereFwdEmpty = 102, kWhereFwdD = 103,
                    kWhereFwdH = 109;
 constexpr uint32_t kWhereBwdFull = 201, kWhereBwdEmpty = 202, kWhereBwdD = 203,
                    kWhereBwdPeer = 204, kWhereBwdPeerEmpty = 205, kWhereBwdDrain = 206,
-                   kWhereBwdExit = 207, kWhereBwdRec = 208;
+                   kWhereBwdExit = 207, kWhereBwdRec = 208, kWhereBwdTFree = 209,
+                   kWhereBwdTReady = 210;
 
 __device__ __forceinline__ void report_device_error(StatusBlock* s, unsigned int code,
                                                     uint32_t where) {

@@ -184,7 +184,7 @@ def test_backward_full_size_sampled_head():
     name = "fwdbwd_bf16_k64"
     w = WORKLOADS[name]
     inp = make_workload(name)
-    got = gpu_backward(inp, ckpt_every=32, use_fwd_ckpt=True)
+    got = gpu_backward(inp, ckpt_every=16, use_fwd_ckpt=True)
     n = w["N"] - 1
     ref = oracle_backward(*oracle_args(inp, slice(None), slice(n, n + 1)),
                           inp.exact["dy"][:, :, n:n + 1])
@@ -230,7 +230,8 @@ def test_forward_each_kernel_family(kernel_family, B, N, T, K, V):
 @pytest.mark.parametrize("kernel_family", ["mma", "simt"], indirect=True)
 @pytest.mark.parametrize("B,N,T,K,V,C", [(2, 2, 37, 64, 64, 16), (1, 1, 70, 32, 64, 32),
                                          (1, 2, 129, 16, 64, 7), (1, 1, 5, 64, 64, 1),
-                                         (1, 1, 64, 128, 64, 32)])
+                                         (1, 1, 64, 128, 64, 32), (1, 1, 200, 64, 64, 16),
+                                         (2, 1, 90, 32, 64, 17)])
 def test_backward_each_kernel_family(kernel_family, B, N, T, K, V, C):
     inp = make_inputs(B, N, T, K, V, "bf16", seed=T + C, with_dy=True)
     dH = np.random.default_rng(4).standard_normal((B, N, K, V)).astype(np.float32)
