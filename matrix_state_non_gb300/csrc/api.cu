@@ -108,7 +108,7 @@ BwdLayout bwd_layout(int64_t B, int64_t T, int64_t N, int64_t K, int64_t V, int 
   off = align256(off + sizeof(float) * static_cast<size_t>(B * N * V));
   l.scratch_off = off;
   if (path == kPathMma)
-    off = align256(off + mma_backward_scratch_bytes(b, nn, k, v, C));
+    off = align256(off + mma_backward_scratch_bytes(b, static_cast<int>(T), nn, k, v, C));
   else if (path == kPathTc)
     off = align256(off + tc_backward_scratch_bytes(b, nn, k, v, C));
   else

@@ -68,7 +68,7 @@ cudaError_t launch_reduce_partials(const BwdArgs& a, cudaStream_t s);
 bool mma_forward_supported(int K, int V);
 cudaError_t launch_mma_forward(const FwdArgs& a, cudaStream_t s);
 bool mma_backward_supported(int K, int V);
-size_t mma_backward_scratch_bytes(int B, int N, int K, int V, int ckpt_every);
+size_t mma_backward_scratch_bytes(int B, int T, int N, int K, int V, int ckpt_every);
 int mma_backward_max_chunk();
 cudaError_t launch_mma_backward(const BwdArgs& a, cudaStream_t s);
 

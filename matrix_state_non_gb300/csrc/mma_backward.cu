@@ -11,26 +11,29 @@
 //   df_t = <R_t, H_{t-1} - Z_t>,  dW += H_{t-1}^T D_t,  dw_r += u_t * v_t.
 //
 // Work split as in the forward: a chain's K rows in blocks of 16, one CTA per
-// block, the blocks of a chain in one cluster (only dv_t and df_t sum over
-// rows; dW is summed later over row blocks and batch in a fixed order).
-// The time axis runs over chunks of C <= 32 steps, last chunk first.  For
-// each chunk the forward is rerun from its checkpoint (section 2.6 of the
+// block (rows never mix; only dv_t, df_t, dW and dw_r sum over rows, and
+// those are written as row-block partials and summed afterwards in a fixed
+// order).  The time axis runs over chunks of C <= 32 steps, last chunk first;
+// for each chunk the forward is rerun from its checkpoint (section 2.6 of the
 // notes describes the paper's rerun-and-cache backward; here only one or two
-// chunks are cached), each thread caching its own Z_t and H_{t-1} values
-// (fp32) in its own lane of tensor memory, so the cache never touches DRAM;
-// then the chunk is walked backwards.  The two jobs run on separate warps:
-// four recompute warps and four reverse warps, each owning 16 value columns,
-// paired on the SM's four schedulers so that one's latency hides the other's.
-// With C <= 16 two caches fit in the 512 TMEM columns and the recompute of
+// chunks are cached) and then walked backwards.  Three warpgroups, each warp
+// owning 16 value columns (or, for the gradient warps, 16 rows of dW):
+//   reverse warps   the serial chain only: R -> D -> bf16(D) tile -> one
+//                   named barrier -> 8 warp MMAs seeded with f R -> C_{t-1};
+//                   then they hand D (fp32 and bf16), E = R * (H_{t-1} - Z)
+//                   and bf16 H_{t-1} to the gradient warps through a ring of
+//                   shared-memory slots;
+//   recompute warps the forward rerun of the next chunk (Eq. 10-11), caching
+//                   each thread's Z_t and H_{t-1} values (fp32) in its own
+//                   lane of tensor memory, so the cache never touches DRAM;
+//                   also dq_t = H_t u_t, and the chunk loads (TMA);
+//   gradient warps  dW += H_{t-1}^T D_t (8 warp MMAs per warp per step into
+//                   register accumulators), dk_t, the row-block partials of
+//                   dv_t and df_t, and dw_r.
+// Warp w of each warpgroup runs on scheduler w, so the three interleave.  With
+// C <= 16 two chunk caches fit in the 512 TMEM columns and the recompute of
 // chunk c-1 overlaps the reverse walk of chunk c; with 16 < C <= 32 the two
-// alternate.  Per reverse step the serial chain is R -> D -> bf16(D) tile ->
-// one named barrier -> 8 warp MMAs seeded with f R -> C_{t-1}.  Off the
-// chain: dW += H_{t-1}^T D as 8 more warp MMAs per warp into register
-// accumulators (H_{t-1}^T fragments by movmatrix, D fragments by
-// ldmatrix.trans), and the row/column reductions for dq, dk, dv, df, also as
-// warp MMAs against replicated vectors (no shuffle chains), written as
-// per-step partials that a reducer warp sums (over warps, and over the
-// cluster's CTAs for dv, df) and stores.
+// alternate.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -44,30 +47,33 @@ namespace {
 
 constexpr int kV = 64;
 constexpr int kRows = 16;
-constexpr int kPS = 32;      // reverse steps per partial tile
-constexpr int kPStages = 2;
-// Three warpgroups: 4 reverse warps, 4 recompute warps (one also loads), and
-// the reducer warp with three idle ones.  The registers are rebalanced after
-// launch: the reverse warps carry the most live state.
-constexpr int kThreads = 384;
-constexpr int kLaunchRegs = 168;   // 65536 / 384, rounded down to the allocation unit of 8
-constexpr int kReverseRegs = 240, kRecomputeRegs = kLaunchRegs, kReducerRegs = 96;
-static_assert(kReverseRegs + kRecomputeRegs + kReducerRegs <= 3 * kLaunchRegs,
-              "warpgroup register budgets exceed the launch's");
-constexpr int kMaxChunk = 32;   // one chunk cache fills the 512 TMEM columns at 32 steps
+constexpr int kThreads = 384;     // reverse warps 0-3, recompute warps 4-7, gradient warps 8-11
+constexpr int kMaxChunk = 32;     // one chunk cache fills the 512 TMEM columns at 32 steps
 constexpr int kTwoBufChunk = 16;  // up to 16 steps two caches fit: the recompute runs a chunk ahead
-constexpr int kCBufs = 3;       // chunk input buffers: reverse, recompute, loading
-constexpr int kSlotFloats = 4 * 16 + 4 * 16 + kV + 4 * 16;  // dq, dk row partials, dv, df row partials
+constexpr int kCBufs = 4;         // chunk input buffers (reverse, gradient, recompute, loading)
+constexpr int kNX = 8;            // exchange ring slots, reverse -> gradient warps
+// Exchange slot (reverse -> gradient warps), one per time step:
+//   Dt  bf16 D tile (also the A operand of the reverse warps' chain MMAs)
+//   Ht  bf16 H_{t-1} tile
+//   Dv  per-thread sums of D k over the thread's two rows: [g][64 columns], rows padded to 72 floats
+//   Dk  per-thread sums of D v over the thread's four columns: [warp][qd][g][row g, g+8], groups padded to 18
+//   Df  per-thread sums of R (H_{t-1} - Z) over the thread's eight values: [128]
+// (strides chosen so that both the writers' and the readers' accesses are free of bank conflicts).
+constexpr int kDvStride = 72, kDkGroup = 18;
+constexpr uint32_t kXDt = 0, kXHt = 2048, kXDv = 4096, kXDk = kXDv + 8 * kDvStride * 4,
+                   kXDf = kXDk + 16 * kDkGroup * 4, kXSlotBytes = 8192;
+static_assert(kXDf + 128 * 4 <= kXSlotBytes, "exchange slot overflow");
 
 struct MmaBwdParams {
   BwdArgs a;
   int R;
   int nchunks;
-  int nptiles;
   int nbuf;  // TMEM cache buffers: 2 if ckpt_every <= kTwoBufChunk, else 1
-  uint32_t htile_off, dtile_off, cbuf_off, cbuf_bytes, cq_off, ck_off, cv_off, cdy_off, cf_off;
-  uint32_t hend_off, part_off, bar_off, misc_off;
+  uint32_t htile_off, cbuf_off, cbuf_bytes, cq_off, ck_off, cv_off, cdy_off, cf_off;
+  uint32_t xring_off, dqp_off, dwr_off, bar_off, misc_off;
   uint32_t tx_bytes;
+  float* dvp;  // [B*T*N][R][V]: row-block partials of D^T k
+  float* dfp;  // [B*T*N][R]:    row-block partials of df
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -84,34 +90,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = chain / N, n = chain % N;
   StatusBlock* status = A.status;
 
-  float* sPart = reinterpret_cast<float*>(smem + p.part_off);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.bar_off);
   uint64_t* cfull = bars;
-  uint64_t* tready = cfull + kCBufs;
+  uint64_t* cempty = cfull + kCBufs;
+  uint64_t* tready = cempty + kCBufs;
   uint64_t* tfree = tready + 2;
-  uint64_t* pfull = tfree + 2;
-  uint64_t* ppeer = pfull + kPStages;
-  uint64_t* pempty = ppeer + kPStages;
+  uint64_t* xfull = tfree + 2;
+  uint64_t* xempty = xfull + kNX;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.misc_off);
   volatile int* vabort = reinterpret_cast<volatile int*>(smem + p.misc_off + 4);
   volatile int* rabort = reinterpret_cast<volatile int*>(smem + p.misc_off + 8);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + p.misc_off + 12);
-  float* hend = reinterpret_cast<float*>(smem + p.hend_off);
+  volatile int* gabort = reinterpret_cast<volatile int*>(smem + p.misc_off + 12);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + p.misc_off + 16);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kCBufs; ++i) mbar_init(smem_u32(&cfull[i]), 32);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&tready[i]), 4);
-      mbar_init(smem_u32(&tfree[i]), 4);
+    // Warps arrive once each (lane 0 after __syncwarp), except the loading
+    // warp, whose lanes each publish a value of f.
+    for (int i = 0; i < kCBufs; ++i) {
+      mbar_init(smem_u32(&cfull[i]), 32);    // the loading warp's lanes (+ TMA bytes)
+      mbar_init(smem_u32(&cempty[i]), 4);    // the gradient warps
     }
-    for (int i = 0; i < kPStages; ++i) {
-      mbar_init(smem_u32(&pfull[i]), 1);
-      mbar_init(smem_u32(&ppeer[i]), R);
-      mbar_init(smem_u32(&pempty[i]), R);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&tready[i]), 4);    // one lane per recompute warp
+      mbar_init(smem_u32(&tfree[i]), 4);     // one lane per reverse warp
+    }
+    for (int i = 0; i < kNX; ++i) {
+      mbar_init(smem_u32(&xfull[i]), 4);     // the reverse warps
+      mbar_init(smem_u32(&xempty[i]), 4);    // the gradient warps
     }
     *abort_flag = 0;
     *vabort = 0;
     *rabort = 0;
+    *gabort = 0;
     fence_mbar_init_cluster();
   }
   if (warp == 0) {  // the whole tensor memory: the per-thread chunk caches
@@ -119,512 +129,498 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before_sync();
-  cluster_sync_all();
+  __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp < 8) {
-    // Warps 0-3 walk the chunks backwards, warps 4-7 recompute them; warp w
-    // and warp w + 4 share TMEM lanes 32(w % 4).. and the same fragment
-    // positions, so thread i of the reverse warp reads exactly what thread i
-    // of the recompute warp cached.
-    const int w = warp & 3;
-    const int g = lane >> 2, qd = lane & 3;
-    const int ctid = threadIdx.x & 127;
-    const int jcol0 = 16 * w + 2 * qd;           // this thread's columns: jcol0 + 8nt + {0,1}
-    const int64_t row_g = static_cast<int64_t>(cta_rank) * kRows + g;
-    const uint16_t* Wg = static_cast<const uint16_t*>(A.W) + static_cast<int64_t>(n) * kV * kV;
-    // Cache buffer tb of this thread: TMEM lane 32w + lane, slot s = columns
-    // 256 tb + 16 s .. + 15 holding {Z_s (8 values), H_{s-1} (8 values)}.
-    const uint32_t tcache = tmem_base + (static_cast<uint32_t>(32 * w) << 16);
-    const uint32_t htile0 = smem_u32(smem + p.htile_off);
-    const uint32_t dtile0 = smem_u32(smem + p.dtile_off);
+  // Warp w of every warpgroup owns value columns 16w..16w+15 (thread columns
+  // jcol0 + 8nt + {0,1}, rows g and g+8 of the CTA's block).  Reverse warp w
+  // and recompute warp w + 4 share TMEM lanes 32w.. and the same fragment
+  // positions, so each reverse thread reads exactly what its recompute
+  // partner cached: buffer tb, slot s = columns 256 tb + 16 s .. + 15 holding
+  // {Z_s (8 values), H_{s-1} (8 values)}.
+  const int w = warp & 3;
+  const int g = lane >> 2, qd = lane & 3;
+  const int ctid = threadIdx.x & 127;
+  const int jcol0 = 16 * w + 2 * qd;
+  const int64_t row_g = static_cast<int64_t>(cta_rank) * kRows + g;
+  const uint16_t* Wg = static_cast<const uint16_t*>(A.W) + static_cast<int64_t>(n) * kV * kV;
+  const uint32_t tcache = tmem_base + (static_cast<uint32_t>(32 * w) << 16);
+  const uint32_t xring0 = smem_u32(smem + p.xring_off);
 
-    if (warp >= 4) {
-      // ======================= recompute warps (Eq. 10-11) =======================
-      // Warp 4 also loads the chunk inputs, one chunk ahead of its own use:
-      // q, k, v, dy by TMA, f gathered by the lanes (its global-load latency
-      // hidden behind the chunk's recompute) and published at the chunk's end.
-      const bool loader = (warp == 4);
-      const uint16_t* fg = static_cast<const uint16_t*>(A.f);
-      auto issue_chunk = [&](int li) -> float {
-        const int t0 = (p.nchunks - 1 - li) * CL;
-        uint8_t* buf = smem + p.cbuf_off + (li % kCBufs) * p.cbuf_bytes;
-        const uint32_t fb = smem_u32(&cfull[li % kCBufs]);
-        if (lane == 0) {
-          mbar_expect_tx(fb, p.tx_bytes);
-          tma_load_4d(smem_u32(buf + p.cq_off), &tm_q, fb, cta_rank * kRows, n, t0, b);
-          tma_load_4d(smem_u32(buf + p.ck_off), &tm_k, fb, cta_rank * kRows, n, t0, b);
-          tma_load_4d(smem_u32(buf + p.cv_off), &tm_v, fb, 0, n, t0, b);
-          tma_load_4d(smem_u32(buf + p.cdy_off), &tm_dy, fb, 0, n, t0, b);
-        }
-        const int t = t0 + lane;
-        return (lane < CL && t < T) ? bf16_bits_to_f32(fg[(static_cast<int64_t>(b) * T + t) * N + n]) : 0.f;
-      };
-      auto publish_chunk = [&](int li, float fv) {
-        float* cfw = reinterpret_cast<float*>(smem + p.cbuf_off + (li % kCBufs) * p.cbuf_bytes + p.cf_off);
-        if (lane < CL) cfw[lane] = fv;
-        mbar_arrive(smem_u32(&cfull[li % kCBufs]));  // all 32 lanes: the phase's arrival count
-      };
-      if (loader) {
-        if (lane == 0) {
-          tma_prefetch_desc(&tm_q);
-          tma_prefetch_desc(&tm_k);
-          tma_prefetch_desc(&tm_v);
-          tma_prefetch_desc(&tm_dy);
-        }
-        publish_chunk(0, issue_chunk(0));
+  if (warp < 4) {
+    // ======================= reverse warps =======================
+    // Backward transform fragments: B[k = j][col = m] = W[16w + m][j] (D W^T).
+    uint32_t bt[2][4][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int col = 16 * w + 8 * nt + g;
+#pragma unroll
+      for (int kt = 0; kt < 4; ++kt) {
+        const int k0 = 16 * kt + 2 * qd;
+        bt[nt][kt][0] = *reinterpret_cast<const uint32_t*>(Wg + col * kV + k0);
+        bt[nt][kt][1] = *reinterpret_cast<const uint32_t*>(Wg + col * kV + k0 + 8);
       }
-      // Forward transform fragments: B[k][col] = W[k][16w + col].
-      uint32_t bw[2][4][2];
+    }
+    // State gradient C (C-fragment layout), initialised with dH_T.
+    float Cg[2][4];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const int col = 16 * w + 8 * nt + g;
-#pragma unroll
-        for (int kt = 0; kt < 4; ++kt) {
-          const int k0 = 16 * kt + 2 * qd;
-          bw[nt][kt][0] = static_cast<uint32_t>(Wg[k0 * kV + col]) |
-                          (static_cast<uint32_t>(Wg[(k0 + 1) * kV + col]) << 16);
-          bw[nt][kt][1] = static_cast<uint32_t>(Wg[(k0 + 8) * kV + col]) |
-                          (static_cast<uint32_t>(Wg[(k0 + 9) * kV + col]) << 16);
-        }
+    for (int nt = 0; nt < 2; ++nt) {
+      if (A.dH_T != nullptr) {
+        const float* src = A.dH_T + (static_cast<int64_t>(chain) * A.K + row_g) * kV + jcol0 + 8 * nt;
+        const float2 x0 = *reinterpret_cast<const float2*>(src);
+        const float2 x1 = *reinterpret_cast<const float2*>(src + 8 * kV);
+        Cg[nt][0] = x0.x; Cg[nt][1] = x0.y; Cg[nt][2] = x1.x; Cg[nt][3] = x1.y;
+      } else {
+        Cg[nt][0] = Cg[nt][1] = Cg[nt][2] = Cg[nt][3] = 0.f;
       }
-      bool ok = true;
-      int issued = 1;  // chunks whose loads have been issued
-      for (int ci = 0; ci < p.nchunks; ++ci) {
-        const int c = p.nchunks - 1 - ci;
-        const int L = min(CL, T - c * CL);
-        const int cb = ci % kCBufs, tb = ci % p.nbuf;
-        bool mine = mbar_wait_timed(smem_u32(&cfull[cb]), (ci / kCBufs) & 1, status, kWhereBwdFull);
-        // The cache buffer is free once the reverse warps have finished chunk
-        // ci - nbuf; then the input buffer of chunk ci + 1 (last used by chunk
-        // ci - 2) is free as well.
-        if (mine && ci >= p.nbuf)
-          mine = mbar_wait_timed(smem_u32(&tfree[tb]), ((ci / p.nbuf) - 1) & 1, status, kWhereBwdTFree);
-        if (!mine) *rabort = 1;
-        named_bar_sync(2, 128);
-        if (*rabort) {
-          ok = false;
-          break;
+    }
+    bool ok = true;
+    int rs = 0;          // reverse steps done (processing order)
+    int xs = 0;          // exchange slot of step rs
+    uint32_t xpar = 0;   // its phase parity, (rs / kNX) & 1
+    for (int ci = 0; ci < p.nchunks; ++ci) {
+      const int c = p.nchunks - 1 - ci;
+      const int L = min(CL, T - c * CL);
+      const int cb = ci % kCBufs, tb = ci % p.nbuf;
+      bool mine = mbar_wait_timed(smem_u32(&cfull[cb]), (ci / kCBufs) & 1, status, kWhereBwdFull);
+      if (mine)
+        mine = mbar_wait_timed(smem_u32(&tready[tb]), (ci / p.nbuf) & 1, status, kWhereBwdTReady);
+      if (!mine) *vabort = 1;
+      named_bar_sync(1, 128);
+      if (*vabort) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint8_t* cbuf = smem + p.cbuf_off + cb * p.cbuf_bytes;
+      const uint16_t* cq = reinterpret_cast<const uint16_t*>(cbuf + p.cq_off);
+      const uint16_t* ck = reinterpret_cast<const uint16_t*>(cbuf + p.ck_off);
+      const uint16_t* cv = reinterpret_cast<const uint16_t*>(cbuf + p.cv_off);
+      const float* cdy = reinterpret_cast<const float*>(cbuf + p.cdy_off);
+      const float* cf = reinterpret_cast<const float*>(cbuf + p.cf_off);
+      const uint32_t tbuf = tcache + 256 * tb;
+      // The next slot's TMEM load is issued one step ahead and waited for at
+      // the top of the step.
+      uint32_t slot_regs[16];
+      tmem_ld_32x32b<16>(tbuf + 16 * (L - 1), slot_regs);
+      for (int s = L - 1; s >= 0; --s, ++rs) {
+        // The slot is free once the gradient warps have consumed step rs - kNX.
+        // A give-up here is acted on at the next chunk boundary (the wait
+        // raised the CTA's abort flag, so the remaining waits end at once).
+        if (rs >= kNX &&
+            !mbar_wait(smem_u32(&xempty[xs]), xpar ^ 1u, abort_flag, status, kWhereBwdXEmpty))
+          *vabort = 1;
+        const uint32_t xb = xring0 + xs * kXSlotBytes;
+        float* xg = reinterpret_cast<float*>(smem + p.xring_off + xs * kXSlotBytes);
+        const float q0 = bf16_bits_to_f32(cq[s * kRows + g]);
+        const float q1 = bf16_bits_to_f32(cq[s * kRows + g + 8]);
+        const float ft = cf[s];
+        const float omf = 1.f - ft;
+        float u[2][2];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const float2 uu = *reinterpret_cast<const float2*>(cdy + s * kV + jcol0 + 8 * nt);
+          u[nt][0] = uu.x;
+          u[nt][1] = uu.y;
         }
-        tc_fence_after_sync();
-        const bool more = loader && ci + 1 < p.nchunks;
-        float fnext = 0.f;
-        if (more) fnext = issue_chunk(ci + 1);
-        const uint8_t* cbuf = smem + p.cbuf_off + cb * p.cbuf_bytes;
-        const uint16_t* ck = reinterpret_cast<const uint16_t*>(cbuf + p.ck_off);
-        const uint16_t* cv = reinterpret_cast<const uint16_t*>(cbuf + p.cv_off);
-        const float* cf = reinterpret_cast<const float*>(cbuf + p.cf_off);
-        const uint32_t tbuf = tcache + 256 * tb;
-        float h[2][4];
-        if (c == 0) {
+        tmem_ld_wait();
+        tmem_ld_fence_regs(slot_regs);
+        float Z[2][4], Hp[2][4];
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt) h[nt][0] = h[nt][1] = h[nt][2] = h[nt][3] = 0.f;
-        } else {
-          const float* src =
-              A.ckpt + ((static_cast<int64_t>(chain) * A.n_ckpt + (c - 1)) * A.K + row_g) * kV + jcol0;
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            const float2 x0 = *reinterpret_cast<const float2*>(src + 8 * nt);
-            const float2 x1 = *reinterpret_cast<const float2*>(src + 8 * kV + 8 * nt);
-            h[nt][0] = x0.x; h[nt][1] = x0.y; h[nt][2] = x1.x; h[nt][3] = x1.y;
+          for (int e = 0; e < 4; ++e) {
+            Z[nt][e] = __uint_as_float(slot_regs[4 * nt + e]);
+            Hp[nt][e] = __uint_as_float(slot_regs[8 + 4 * nt + e]);
+          }
+        if (s > 0) tmem_ld_32x32b<16>(tbuf + 16 * (s - 1), slot_regs);
+        // R = C + q u^T ; D = (1-f) R (1 - Z^2)
+        float Rv[2][4], Dv[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float qq = (e < 2) ? q0 : q1;
+            Rv[nt][e] = fmaf(qq, u[nt][e & 1], Cg[nt][e]);
+            const float zz = Z[nt][e];
+            Dv[nt][e] = omf * Rv[nt][e] * fmaf(-zz, zz, 1.f);
           }
         }
+        const uint32_t dt = xb + kXDt;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           const int col = jcol0 + 8 * nt;
-          st_shared_b32(htile0 + tile_off(g, col), pack2_bf16(h[nt][0], h[nt][1]));
-          st_shared_b32(htile0 + tile_off(g + 8, col), pack2_bf16(h[nt][2], h[nt][3]));
+          st_shared_b32(dt + tile_off(g, col), pack2_bf16(Dv[nt][0], Dv[nt][1]));
+          st_shared_b32(dt + tile_off(g + 8, col), pack2_bf16(Dv[nt][2], Dv[nt][3]));
+        }
+        named_bar_sync(1, 128);
+        // Serial chain: C_{t-1} = f R + D W^T on the warp MMAs.
+        float acc[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[nt][e] = ft * Rv[nt][e];
+        uint32_t af[4][4];
+#pragma unroll
+        for (int kt = 0; kt < 4; ++kt) ldmatrix_x4(af[kt], ldsm_addr_a(dt, kt, lane));
+#pragma unroll
+        for (int kt = 0; kt < 4; ++kt)
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) mma_bf16_16816(acc[nt], af[kt], bt[nt][kt][0], bt[nt][kt][1]);
+        // Off the chain: this thread's shares of dk, dv, df, and bf16 H_{t-1}
+        // for dW, handed to the gradient warps.
+        {
+          const float k0 = bf16_bits_to_f32(ck[s * kRows + g]);
+          const float k1 = bf16_bits_to_f32(ck[s * kRows + g + 8]);
+          float pk0 = 0.f, pk1 = 0.f, pe = 0.f;
+          float* xdv = xg + kXDv / 4;
+          const uint32_t ht = xb + kXHt;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            const int col = jcol0 + 8 * nt;
+            const uint32_t vb = *reinterpret_cast<const uint32_t*>(cv + s * kV + col);
+            const float v0 = bf16lo(vb), v1 = bf16hi(vb);
+            pk0 = fmaf(Dv[nt][0], v0, pk0);
+            pk0 = fmaf(Dv[nt][1], v1, pk0);
+            pk1 = fmaf(Dv[nt][2], v0, pk1);
+            pk1 = fmaf(Dv[nt][3], v1, pk1);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) pe = fmaf(Rv[nt][e], Hp[nt][e] - Z[nt][e], pe);
+            *reinterpret_cast<float2*>(xdv + g * kDvStride + col) =
+                make_float2(fmaf(Dv[nt][0], k0, Dv[nt][2] * k1), fmaf(Dv[nt][1], k0, Dv[nt][3] * k1));
+            st_shared_b32(ht + tile_off(g, col), pack2_bf16(Hp[nt][0], Hp[nt][1]));
+            st_shared_b32(ht + tile_off(g + 8, col), pack2_bf16(Hp[nt][2], Hp[nt][3]));
+          }
+          *reinterpret_cast<float2*>(xg + kXDk / 4 + (w * 4 + qd) * kDkGroup + 2 * g) = make_float2(pk0, pk1);
+          xg[kXDf / 4 + ctid] = pe;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&xfull[xs]));
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) Cg[nt][e] = acc[nt][e];
+        if (++xs == kNX) {
+          xs = 0;
+          xpar ^= 1u;
+        }
+      }
+      // Every slot of this cache buffer has been read (the last load was
+      // waited for at s = 0): the recompute may refill it.
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&tfree[tb]));
+    }
+    if (!ok) *abort_flag = 1;
+  } else if (warp < 8) {
+    // ======================= recompute warps (Eq. 10-11) =======================
+    // Forward transform fragments: B[k][col] = W[k][16w + col].
+    uint32_t bw[2][4][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int col = 16 * w + 8 * nt + g;
+#pragma unroll
+      for (int kt = 0; kt < 4; ++kt) {
+        const int k0 = 16 * kt + 2 * qd;
+        bw[nt][kt][0] = static_cast<uint32_t>(Wg[k0 * kV + col]) |
+                        (static_cast<uint32_t>(Wg[(k0 + 1) * kV + col]) << 16);
+        bw[nt][kt][1] = static_cast<uint32_t>(Wg[(k0 + 8) * kV + col]) |
+                        (static_cast<uint32_t>(Wg[(k0 + 9) * kV + col]) << 16);
+      }
+    }
+    const uint32_t htile0 = smem_u32(smem + p.htile_off);
+    float* dqp = reinterpret_cast<float*>(smem + p.dqp_off);  // [C][4 warps][4 qd][8 g][row g, g+8]
+    // Warp 4 also loads the chunk inputs, one chunk ahead of its own use:
+    // q, k, v, dy by TMA, f gathered by the lanes (its global-load latency
+    // hidden behind the chunk's recompute) and published at the chunk's end.
+    const bool loader = (warp == 4);
+    const uint16_t* fg = static_cast<const uint16_t*>(A.f);
+    auto issue_chunk = [&](int li) -> float {
+      const int t0 = (p.nchunks - 1 - li) * CL;
+      uint8_t* buf = smem + p.cbuf_off + (li % kCBufs) * p.cbuf_bytes;
+      const uint32_t fb = smem_u32(&cfull[li % kCBufs]);
+      if (lane == 0) {
+        mbar_expect_tx(fb, p.tx_bytes);
+        tma_load_4d(smem_u32(buf + p.cq_off), &tm_q, fb, cta_rank * kRows, n, t0, b);
+        tma_load_4d(smem_u32(buf + p.ck_off), &tm_k, fb, cta_rank * kRows, n, t0, b);
+        tma_load_4d(smem_u32(buf + p.cv_off), &tm_v, fb, 0, n, t0, b);
+        tma_load_4d(smem_u32(buf + p.cdy_off), &tm_dy, fb, 0, n, t0, b);
+      }
+      const int t = t0 + lane;
+      return (lane < CL && t < T) ? bf16_bits_to_f32(fg[(static_cast<int64_t>(b) * T + t) * N + n]) : 0.f;
+    };
+    auto publish_chunk = [&](int li, float fv) {
+      float* cfw = reinterpret_cast<float*>(smem + p.cbuf_off + (li % kCBufs) * p.cbuf_bytes + p.cf_off);
+      if (lane < CL) cfw[lane] = fv;
+      mbar_arrive(smem_u32(&cfull[li % kCBufs]));  // all 32 lanes: the phase's arrival count
+    };
+    if (loader) {
+      if (lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_dy);
+      }
+      publish_chunk(0, issue_chunk(0));
+    }
+    bool ok = true;
+    int issued = 1;  // chunks whose loads have been issued
+    for (int ci = 0; ci < p.nchunks; ++ci) {
+      const int c = p.nchunks - 1 - ci;
+      const int s0 = c * CL;
+      const int L = min(CL, T - s0);
+      const int cb = ci % kCBufs, tb = ci % p.nbuf;
+      bool mine = mbar_wait_timed(smem_u32(&cfull[cb]), (ci / kCBufs) & 1, status, kWhereBwdFull);
+      // The cache buffer is free once the reverse warps have finished chunk
+      // ci - nbuf.
+      if (mine && ci >= p.nbuf)
+        mine = mbar_wait_timed(smem_u32(&tfree[tb]), ((ci / p.nbuf) - 1) & 1, status, kWhereBwdTFree);
+      // The input buffer chunk ci + 1 will use last held chunk ci - 3: free
+      // once the gradient warps (the last to read it) are past it.
+      if (mine && ci >= 3 && ci + 1 < p.nchunks)
+        mine = mbar_wait_timed(smem_u32(&cempty[(ci + 1) % kCBufs]), ((ci - 3) / kCBufs) & 1, status,
+                               kWhereBwdCEmpty);
+      if (!mine) *rabort = 1;
+      named_bar_sync(2, 128);
+      if (*rabort) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const bool more = loader && ci + 1 < p.nchunks;
+      float fnext = 0.f;
+      if (more) fnext = issue_chunk(ci + 1);
+      const uint8_t* cbuf = smem + p.cbuf_off + cb * p.cbuf_bytes;
+      const uint16_t* ck = reinterpret_cast<const uint16_t*>(cbuf + p.ck_off);
+      const uint16_t* cv = reinterpret_cast<const uint16_t*>(cbuf + p.cv_off);
+      const float* cdy = reinterpret_cast<const float*>(cbuf + p.cdy_off);
+      const float* cf = reinterpret_cast<const float*>(cbuf + p.cf_off);
+      const uint32_t tbuf = tcache + 256 * tb;
+      float h[2][4];
+      if (c == 0) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) h[nt][0] = h[nt][1] = h[nt][2] = h[nt][3] = 0.f;
+      } else {
+        const float* src =
+            A.ckpt + ((static_cast<int64_t>(chain) * A.n_ckpt + (c - 1)) * A.K + row_g) * kV + jcol0;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const float2 x0 = *reinterpret_cast<const float2*>(src + 8 * nt);
+          const float2 x1 = *reinterpret_cast<const float2*>(src + 8 * kV + 8 * nt);
+          h[nt][0] = x0.x; h[nt][1] = x0.y; h[nt][2] = x1.x; h[nt][3] = x1.y;
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int col = jcol0 + 8 * nt;
+        st_shared_b32(htile0 + tile_off(g, col), pack2_bf16(h[nt][0], h[nt][1]));
+        st_shared_b32(htile0 + tile_off(g + 8, col), pack2_bf16(h[nt][2], h[nt][3]));
+      }
+      named_bar_sync(2, 128);
+      for (int s = 0; s < L; ++s) {
+        const float k0 = bf16_bits_to_f32(ck[s * kRows + g]);
+        const float k1 = bf16_bits_to_f32(ck[s * kRows + g + 8]);
+        const float omf = 1.f - cf[s];
+        float acc[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const uint32_t vv = *reinterpret_cast<const uint32_t*>(cv + s * kV + jcol0 + 8 * nt);
+          const float v0 = bf16lo(vv), v1 = bf16hi(vv);
+          acc[nt][0] = k0 * v0;
+          acc[nt][1] = k0 * v1;
+          acc[nt][2] = k1 * v0;
+          acc[nt][3] = k1 * v1;
+        }
+        const uint32_t atile = htile0 + (s & 1) * 2048;
+        uint32_t af[4][4];
+#pragma unroll
+        for (int kt = 0; kt < 4; ++kt) ldmatrix_x4(af[kt], ldsm_addr_a(atile, kt, lane));
+#pragma unroll
+        for (int kt = 0; kt < 4; ++kt)
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) mma_bf16_16816(acc[nt], af[kt], bw[nt][kt][0], bw[nt][kt][1]);
+        const uint32_t otile = htile0 + ((s + 1) & 1) * 2048;
+        uint32_t cache[16];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float z = tanh_fast(acc[nt][e]);
+            cache[4 * nt + e] = __float_as_uint(z);
+            cache[8 + 4 * nt + e] = __float_as_uint(h[nt][e]);  // H_{s-1}
+            h[nt][e] = fmaf(omf, z - h[nt][e], h[nt][e]);
+          }
+          const int col = jcol0 + 8 * nt;
+          st_shared_b32(otile + tile_off(g, col), pack2_bf16(h[nt][0], h[nt][1]));
+          st_shared_b32(otile + tile_off(g + 8, col), pack2_bf16(h[nt][2], h[nt][3]));
+        }
+        tmem_st_32x32b_x16(tbuf + 16 * s, cache);
+        // dq_t = H_t u_t: this thread's share (its four columns, rows g and
+        // g + 8); the sixteen shares of a row are summed at the chunk's end.
+        {
+          const float2 u0 = *reinterpret_cast<const float2*>(cdy + s * kV + jcol0);
+          const float2 u1 = *reinterpret_cast<const float2*>(cdy + s * kV + jcol0 + 8);
+          float p0 = h[0][0] * u0.x;
+          p0 = fmaf(h[0][1], u0.y, p0);
+          p0 = fmaf(h[1][0], u1.x, p0);
+          p0 = fmaf(h[1][1], u1.y, p0);
+          float p1 = h[0][2] * u0.x;
+          p1 = fmaf(h[0][3], u0.y, p1);
+          p1 = fmaf(h[1][2], u1.x, p1);
+          p1 = fmaf(h[1][3], u1.y, p1);
+          *reinterpret_cast<float2*>(dqp + (s * 16 + w * 4 + qd) * kRows + 2 * g) = make_float2(p0, p1);
         }
         named_bar_sync(2, 128);
-        for (int s = 0; s < L; ++s) {
-          const float k0 = bf16_bits_to_f32(ck[s * kRows + g]);
-          const float k1 = bf16_bits_to_f32(ck[s * kRows + g + 8]);
-          const float omf = 1.f - cf[s];
-          float acc[2][4];
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            const uint32_t vv = *reinterpret_cast<const uint32_t*>(cv + s * kV + jcol0 + 8 * nt);
-            const float v0 = bf16lo(vv), v1 = bf16hi(vv);
-            acc[nt][0] = k0 * v0;
-            acc[nt][1] = k0 * v1;
-            acc[nt][2] = k1 * v0;
-            acc[nt][3] = k1 * v1;
-          }
-          const uint32_t atile = htile0 + (s & 1) * 2048;
-          uint32_t af[4][4];
-#pragma unroll
-          for (int kt = 0; kt < 4; ++kt) ldmatrix_x4(af[kt], ldsm_addr_a(atile, kt, lane));
-#pragma unroll
-          for (int kt = 0; kt < 4; ++kt)
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) mma_bf16_16816(acc[nt], af[kt], bw[nt][kt][0], bw[nt][kt][1]);
-          const uint32_t otile = htile0 + ((s + 1) & 1) * 2048;
-          uint32_t cache[16];
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float z = tanh_fast(acc[nt][e]);
-              cache[4 * nt + e] = __float_as_uint(z);
-              cache[8 + 4 * nt + e] = __float_as_uint(h[nt][e]);  // H_{s-1}
-              h[nt][e] = fmaf(omf, z - h[nt][e], h[nt][e]);
-            }
-            const int col = jcol0 + 8 * nt;
-            st_shared_b32(otile + tile_off(g, col), pack2_bf16(h[nt][0], h[nt][1]));
-            st_shared_b32(otile + tile_off(g + 8, col), pack2_bf16(h[nt][2], h[nt][3]));
-          }
-          tmem_st_32x32b_x16(tbuf + 16 * s, cache);
-          named_bar_sync(2, 128);
-        }
-        tmem_st_wait();
-        if (more) publish_chunk(ci + 1, fnext);
-        // The chunk's final state, the reverse walk's first H_t.
-        float4* he = reinterpret_cast<float4*>(hend + (tb * 128 + ctid) * 8);
-        he[0] = make_float4(h[0][0], h[0][1], h[0][2], h[0][3]);
-        he[1] = make_float4(h[1][0], h[1][1], h[1][2], h[1][3]);
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&tready[tb]));
-        issued = ci + 2;
       }
-      if (!ok) {
-        *abort_flag = 1;
-        // No TMA copy may still be writing when the CTA exits.
-        if (loader)
-          for (int li = max(0, issued - 2); li < min(issued, p.nchunks); ++li)
-            mbar_wait_timed(smem_u32(&cfull[li % kCBufs]), (li / kCBufs) & 1, nullptr, kWhereBwdDrain);
+      tmem_st_wait();
+      if (more) publish_chunk(ci + 1, fnext);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&tready[tb]));
+      issued = ci + 2;
+      // dq rows of the chunk (the last step's barrier ordered every share):
+      // the sixteen shares of row r = g + 8 hi, warp by warp, in a fixed order.
+      for (int idx = ctid; idx < L * kRows; idx += 128) {
+        const int s = idx >> 4, r = idx & 15;
+        const float* pp = dqp + s * 16 * kRows + 2 * (r & 7) + (r >> 3);
+        float sum = 0.f;
+#pragma unroll
+        for (int sh = 0; sh < 16; ++sh) sum += pp[sh * kRows];
+        const int64_t rowt = (static_cast<int64_t>(b) * T + s0 + s) * N + n;
+        A.dq[rowt * A.K + cta_rank * kRows + r] = sum;
       }
-    } else {
-      // ======================= reverse warps =======================
-      warpgroup_reg_increase<kReverseRegs>();
-      // Backward transform fragments: B[k = j][col = m] = W[16w + m][j] (D W^T).
-      uint32_t bt[2][4][2];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const int col = 16 * w + 8 * nt + g;
-#pragma unroll
-        for (int kt = 0; kt < 4; ++kt) {
-          const int k0 = 16 * kt + 2 * qd;
-          bt[nt][kt][0] = *reinterpret_cast<const uint32_t*>(Wg + col * kV + k0);
-          bt[nt][kt][1] = *reinterpret_cast<const uint32_t*>(Wg + col * kV + k0 + 8);
-        }
-      }
-      // State gradient C (C-fragment layout), initialised with dH_T.
-      float Cg[2][4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        if (A.dH_T != nullptr) {
-          const float* src = A.dH_T + (static_cast<int64_t>(chain) * A.K + row_g) * kV + jcol0 + 8 * nt;
-          const float2 x0 = *reinterpret_cast<const float2*>(src);
-          const float2 x1 = *reinterpret_cast<const float2*>(src + 8 * kV);
-          Cg[nt][0] = x0.x; Cg[nt][1] = x0.y; Cg[nt][2] = x1.x; Cg[nt][3] = x1.y;
-        } else {
-          Cg[nt][0] = Cg[nt][1] = Cg[nt][2] = Cg[nt][3] = 0.f;
-        }
-      }
-      float dWacc[8][4];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) dWacc[i][0] = dWacc[i][1] = dWacc[i][2] = dWacc[i][3] = 0.f;
-      float dwr[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-
-      bool ok = true;
-      int rs = 0;                  // reverse steps done so far (processing order)
-      int pending_pfull = -1;      // partial tile whose last slot was written in the previous step
-      for (int ci = 0; ci < p.nchunks && ok; ++ci) {
-        const int c = p.nchunks - 1 - ci;
-        const int L = min(CL, T - c * CL);
-        const int cb = ci % kCBufs, tb = ci % p.nbuf;
-        bool mine = mbar_wait_timed(smem_u32(&cfull[cb]), (ci / kCBufs) & 1, status, kWhereBwdFull);
-        if (mine)
-          mine = mbar_wait_timed(smem_u32(&tready[tb]), (ci / p.nbuf) & 1, status, kWhereBwdTReady);
-        if (!mine) *vabort = 1;
-        named_bar_sync(1, 128);
-        if (*vabort) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        const uint8_t* cbuf = smem + p.cbuf_off + cb * p.cbuf_bytes;
-        const uint16_t* cq = reinterpret_cast<const uint16_t*>(cbuf + p.cq_off);
-        const uint16_t* ck = reinterpret_cast<const uint16_t*>(cbuf + p.ck_off);
-        const uint16_t* cv = reinterpret_cast<const uint16_t*>(cbuf + p.cv_off);
-        const float* cdy = reinterpret_cast<const float*>(cbuf + p.cdy_off);
-        const float* cf = reinterpret_cast<const float*>(cbuf + p.cf_off);
-        const uint32_t tbuf = tcache + 256 * tb;
-        // h = H_t for the chunk's last step; the next slot's TMEM load is
-        // issued one step ahead and waited for at the top of the step.
-        float h[2][4];
-        {
-          const float4* he = reinterpret_cast<const float4*>(hend + (tb * 128 + ctid) * 8);
-          const float4 a0 = he[0], a1 = he[1];
-          h[0][0] = a0.x; h[0][1] = a0.y; h[0][2] = a0.z; h[0][3] = a0.w;
-          h[1][0] = a1.x; h[1][1] = a1.y; h[1][2] = a1.z; h[1][3] = a1.w;
-        }
-        uint32_t slot_regs[16];
-        tmem_ld_32x32b<16>(tbuf + 16 * (L - 1), slot_regs);
-        for (int s = L - 1; s >= 0; --s, ++rs) {
-          const int ptile = rs / kPS, slot = rs % kPS, pst = ptile % kPStages;
-          if (slot == 0) {
-            // Partial tile ptile: wait until every CTA of the cluster has read
-            // what this stage held two tiles ago.
-            bool m2 = true;
-            if (ptile >= kPStages)
-              m2 = mbar_wait_timed<true>(smem_u32(&pempty[pst]), ((ptile / kPStages) - 1) & 1, status,
-                                         kWhereBwdPeerEmpty);
-            if (!m2) *vabort = 1;
-            named_bar_sync(1, 128);
-            if (*vabort) {
-              ok = false;
-              break;
-            }
-          }
-          // Step inputs.
-          const float q0 = bf16_bits_to_f32(cq[s * kRows + g]);
-          const float q1 = bf16_bits_to_f32(cq[s * kRows + g + 8]);
-          const float k0 = bf16_bits_to_f32(ck[s * kRows + g]);
-          const float k1 = bf16_bits_to_f32(ck[s * kRows + g + 8]);
-          const float ft = cf[s];
-          const float omf = 1.f - ft;
-          float u[2][2], vv[2][2];
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            const float2 uu = *reinterpret_cast<const float2*>(cdy + s * kV + jcol0 + 8 * nt);
-            u[nt][0] = uu.x;
-            u[nt][1] = uu.y;
-            const uint32_t vb = *reinterpret_cast<const uint32_t*>(cv + s * kV + jcol0 + 8 * nt);
-            vv[nt][0] = bf16lo(vb);
-            vv[nt][1] = bf16hi(vb);
-          }
-          tmem_ld_wait();
-          tmem_ld_fence_regs(slot_regs);
-          float Z[2][4], Hp[2][4];
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              Z[nt][e] = __uint_as_float(slot_regs[4 * nt + e]);
-              Hp[nt][e] = __uint_as_float(slot_regs[8 + 4 * nt + e]);
-            }
-          if (s > 0) tmem_ld_32x32b<16>(tbuf + 16 * (s - 1), slot_regs);
-          // R = C + q u^T ; D = (1-f) R (1 - Z^2)
-          float Rv[2][4], Dv[2][4];
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float qq = (e < 2) ? q0 : q1;
-              Rv[nt][e] = fmaf(qq, u[nt][e & 1], Cg[nt][e]);
-              const float zz = Z[nt][e];
-              Dv[nt][e] = omf * Rv[nt][e] * fmaf(-zz, zz, 1.f);
-            }
-          }
-          const uint32_t dt = dtile0 + (rs & 1) * 2048;
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            const int col = jcol0 + 8 * nt;
-            st_shared_b32(dt + tile_off(g, col), pack2_bf16(Dv[nt][0], Dv[nt][1]));
-            st_shared_b32(dt + tile_off(g + 8, col), pack2_bf16(Dv[nt][2], Dv[nt][3]));
-          }
-          named_bar_sync(1, 128);
-          if (pending_pfull >= 0 && threadIdx.x == 0) mbar_arrive(smem_u32(&pfull[pending_pfull % kPStages]));
-          pending_pfull = -1;
-          // Serial chain: C_{t-1} = f R + D W^T on the warp MMAs.
-          float acc[2][4];
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[nt][e] = ft * Rv[nt][e];
-          uint32_t af[4][4];
-#pragma unroll
-          for (int kt = 0; kt < 4; ++kt) ldmatrix_x4(af[kt], ldsm_addr_a(dt, kt, lane));
-#pragma unroll
-          for (int kt = 0; kt < 4; ++kt)
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) mma_bf16_16816(acc[nt], af[kt], bt[nt][kt][0], bt[nt][kt][1]);
-          // Off the chain: dW[16w.., :] += H_{t-1}^T D.
-          {
-            uint32_t ha[4];
-            ha[0] = movmatrix_trans(pack2_bf16(Hp[0][0], Hp[0][1]));
-            ha[1] = movmatrix_trans(pack2_bf16(Hp[1][0], Hp[1][1]));
-            ha[2] = movmatrix_trans(pack2_bf16(Hp[0][2], Hp[0][3]));
-            ha[3] = movmatrix_trans(pack2_bf16(Hp[1][2], Hp[1][3]));
-#pragma unroll
-            for (int nt2 = 0; nt2 < 4; ++nt2) {
-              uint32_t bd[4];
-              ldmatrix_x4_trans(bd, ldsm_addr_b_trans(dt, nt2, lane));
-              mma_bf16_16816(dWacc[2 * nt2], ha, bd[0], bd[1]);
-              mma_bf16_16816(dWacc[2 * nt2 + 1], ha, bd[2], bd[3]);
-            }
-          }
-          // Off the chain: per-step partial reductions.
-          float* part = sPart + (pst * kPS + slot) * kSlotFloats;
-          {
-            // Reductions on the tensor core (m16n8k16, fp32 accumulate), fp32
-            // operands split into bf16 high + low parts (products of the parts
-            // lose nothing that matters at fp32 accuracy):
-            //   row sums     dq = H_t u, dk = D v, df rows = (R * (H_{t-1} - Z)) 1
-            //                (A straight from the accumulator-layout registers,
-            //                 B = the vector replicated over the 8 columns)
-            //   column sums  dv = k^T D (A = k replicated over the rows,
-            //                 B = D transposed with movmatrix)
-            auto hl = [](float x0, float x1, uint32_t& hi, uint32_t& lo) {
-              hi = pack2_bf16(x0, x1);
-              lo = pack2_bf16(x0 - bf16lo(hi), x1 - bf16hi(hi));
-            };
-            uint32_t Ah[4], Al[4], Dh[4], Dl[4], Eh[4], El[4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-              float E[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) E[e] = Rv[nt][e] * (Hp[nt][e] - Z[nt][e]);
-              hl(h[nt][0], h[nt][1], Ah[2 * nt], Al[2 * nt]);
-              hl(h[nt][2], h[nt][3], Ah[2 * nt + 1], Al[2 * nt + 1]);
-              hl(Dv[nt][0], Dv[nt][1], Dh[2 * nt], Dl[2 * nt]);
-              hl(Dv[nt][2], Dv[nt][3], Dh[2 * nt + 1], Dl[2 * nt + 1]);
-              hl(E[0], E[1], Eh[2 * nt], El[2 * nt]);
-              hl(E[2], E[3], Eh[2 * nt + 1], El[2 * nt + 1]);
-            }
-            uint32_t uh0, ul0, uh1, ul1;
-            hl(u[0][0], u[0][1], uh0, ul0);
-            hl(u[1][0], u[1][1], uh1, ul1);
-            const uint32_t vb0 = pack2_bf16(vv[0][0], vv[0][1]), vb1 = pack2_bf16(vv[1][0], vv[1][1]);  // exact
-            const uint32_t one2 = 0x3F803F80u;  // bf16 pair (1, 1)
-            float rq[4] = {0.f, 0.f, 0.f, 0.f}, rk[4] = {0.f, 0.f, 0.f, 0.f}, rf[4] = {0.f, 0.f, 0.f, 0.f};
-            mma_bf16_16816(rq, Ah, uh0, uh1);
-            mma_bf16_16816(rq, Al, uh0, uh1);
-            mma_bf16_16816(rq, Ah, ul0, ul1);
-            mma_bf16_16816(rk, Dh, vb0, vb1);
-            mma_bf16_16816(rk, Dl, vb0, vb1);
-            mma_bf16_16816(rf, Eh, one2, one2);
-            mma_bf16_16816(rf, El, one2, one2);
-            uint32_t ka[4];
-            ka[0] = ka[1] = *reinterpret_cast<const uint32_t*>(ck + s * kRows + 2 * qd);
-            ka[2] = ka[3] = *reinterpret_cast<const uint32_t*>(ck + s * kRows + 2 * qd + 8);
-            float rv[2][4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-              rv[nt][0] = rv[nt][1] = rv[nt][2] = rv[nt][3] = 0.f;
-              mma_bf16_16816(rv[nt], ka, movmatrix_trans(Dh[2 * nt]), movmatrix_trans(Dh[2 * nt + 1]));
-              mma_bf16_16816(rv[nt], ka, movmatrix_trans(Dl[2 * nt]), movmatrix_trans(Dl[2 * nt + 1]));
-            }
-            if (qd == 0) {  // column 0 of the row sums: rows g and g+8
-              part[w * 16 + g] = rq[0];
-              part[w * 16 + g + 8] = rq[2];
-              part[64 + w * 16 + g] = rk[0];
-              part[64 + w * 16 + g + 8] = rk[2];
-              part[192 + w * 16 + g] = rf[0];
-              part[192 + w * 16 + g + 8] = rf[2];
-            }
-            if (g == 0) {  // row 0 of the column sums
-              *reinterpret_cast<float2*>(part + 128 + jcol0) = make_float2(rv[0][0], rv[0][1]);
-              *reinterpret_cast<float2*>(part + 128 + jcol0 + 8) = make_float2(rv[1][0], rv[1][1]);
-            }
-            if (cta_rank == 0 && g == 0) {
-#pragma unroll
-              for (int nt = 0; nt < 2; ++nt) {
-                dwr[nt][0] = fmaf(u[nt][0], vv[nt][0], dwr[nt][0]);
-                dwr[nt][1] = fmaf(u[nt][1], vv[nt][1], dwr[nt][1]);
-              }
-            }
-          }
-          if (slot == kPS - 1 || rs == T - 1) pending_pfull = ptile;
-          // C_{t-1}; H_{t-1} becomes the next step's H_t.
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              Cg[nt][e] = acc[nt][e];
-              h[nt][e] = Hp[nt][e];
-            }
-        }
-        if (!ok) break;
-        // Every slot of this cache buffer has been read (the last load was
-        // waited for at s = 0): the recompute may refill it.
-        tc_fence_before_sync();
-        __syncwarp();
-        // This also frees the chunk's input buffer (the reverse warps read it last).
-        if (lane == 0) mbar_arrive(smem_u32(&tfree[tb]));
-      }
-      if (ok) {
-        named_bar_sync(1, 128);
-        if (pending_pfull >= 0 && threadIdx.x == 0) mbar_arrive(smem_u32(&pfull[pending_pfull % kPStages]));
-        // dW partial of this row block: rows m = 16w + g (+8), columns 8nt + 2qd (+1).
-        float* dwp = A.dW_part + static_cast<int64_t>(blockIdx.x) * kV * kV;
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-          const int col = 8 * nt + 2 * qd;
-          *reinterpret_cast<float2*>(dwp + (16 * w + g) * kV + col) = make_float2(dWacc[nt][0], dWacc[nt][1]);
-          *reinterpret_cast<float2*>(dwp + (16 * w + g + 8) * kV + col) = make_float2(dWacc[nt][2], dWacc[nt][3]);
-        }
-        if (cta_rank == 0 && g == 0) {
-          float* dst = A.dwr_part + static_cast<int64_t>(chain) * kV + jcol0;
-          *reinterpret_cast<float2*>(dst) = make_float2(dwr[0][0], dwr[0][1]);
-          *reinterpret_cast<float2*>(dst + 8) = make_float2(dwr[1][0], dwr[1][1]);
-        }
-      } else {
-        *abort_flag = 1;
-      }
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      // No TMA copy may still be writing when the CTA exits.
+      if (loader)
+        for (int li = max(0, issued - 2); li < min(issued, p.nchunks); ++li)
+          mbar_wait_timed(smem_u32(&cfull[li % kCBufs]), (li / kCBufs) & 1, nullptr, kWhereBwdDrain);
     }
   } else {
-    // The whole third warpgroup gives registers back at one instruction;
-    // warps 9-11 then idle until the end.
-    warpgroup_reg_decrease<kReducerRegs>();
-  }
-  if (warp == 8) {
-    // ======================= reducer: partial tiles -> dq, dk, dv, df =======================
-    const uint16_t* wr = static_cast<const uint16_t*>(A.w_r) + static_cast<int64_t>(n) * kV;
-    const float wr0 = bf16_bits_to_f32(wr[2 * lane]), wr1 = bf16_bits_to_f32(wr[2 * lane + 1]);
-    int done = 0;
-    for (int ptile = 0; ptile < p.nptiles; ++ptile) {
-      const int pst = ptile % kPStages;
-      const uint32_t par = (ptile / kPStages) & 1;
-      if (!mbar_wait(smem_u32(&pfull[pst]), par, abort_flag, status, kWhereBwdRec)) break;
-      fence_acq_rel_cluster();
-      if (lane < R) mbar_arrive_cluster(mapa_shared(smem_u32(&ppeer[pst]), lane));
-      if (!mbar_wait<true>(smem_u32(&ppeer[pst]), par, abort_flag, status, kWhereBwdPeer)) break;
-      const int rs0 = ptile * kPS;
-      const int nslots = min(kPS, T - rs0);
-      const float* base = sPart + pst * kPS * kSlotFloats;
-      // dq, dk: this CTA's 16 rows, summed over the four compute warps.
-      for (int slot = 0; slot < nslots; ++slot) {
-        const int t = T - 1 - (rs0 + slot);
-        const int64_t rowt = (static_cast<int64_t>(b) * T + t) * N + n;
-        const float* part = base + slot * kSlotFloats;
-        const int i = lane & 15;
-        const int off = (lane < 16) ? 0 : 64;
-        const float sum = ((part[off + i] + part[off + 16 + i]) + part[off + 32 + i]) + part[off + 48 + i];
-        float* dst = (lane < 16) ? A.dq : A.dk;
-        dst[rowt * A.K + cta_rank * kRows + i] = sum;
-      }
-      // dv, df: summed over the cluster's row blocks, in fixed order.
-      const uint32_t sbase = smem_u32(base);
-      for (int slot = cta_rank; slot < nslots; slot += R) {
-        const int t = T - 1 - (rs0 + slot);
-        const int64_t rowt = (static_cast<int64_t>(b) * T + t) * N + n;
-        float a0 = 0.f, a1 = 0.f, fsum = 0.f;
-        for (int pr = 0; pr < R; ++pr) {  // fixed order over the chain's row blocks
-          const uint32_t pb = mapa_shared(sbase, pr) + static_cast<uint32_t>(slot * kSlotFloats * 4);
-          a0 += ld_shared_cluster_f32(pb + (128 + 2 * lane) * 4);
-          a1 += ld_shared_cluster_f32(pb + (128 + 2 * lane + 1) * 4);
-          fsum += ld_shared_cluster_f32(pb + (192 + 2 * lane) * 4) +
-                  ld_shared_cluster_f32(pb + (192 + 2 * lane + 1) * 4);
-        }
-        const float2 uu = *reinterpret_cast<const float2*>(A.dy + rowt * kV + 2 * lane);
-        *reinterpret_cast<float2*>(A.dv + rowt * kV + 2 * lane) = make_float2(fmaf(wr0, uu.x, a0), fmaf(wr1, uu.y, a1));
+    // ======================= gradient warps =======================
+    // Warp w: dW rows 16w..16w+15 (A = H_{t-1}^T from the bf16 H tile, B = D
+    // from the bf16 D tile); every fourth step (rs % 4 == w) also the row and
+    // column sums of that step.
+    float dWacc[8][4];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) fsum += __shfl_xor_sync(0xffffffffu, fsum, o);  // fixed tree
-        if (lane == 0) A.df[rowt] = fsum;
-      }
-      fence_acq_rel_cluster();
-      __syncwarp();
-      if (lane < R) mbar_arrive_cluster(mapa_shared(smem_u32(&pempty[pst]), lane));
-      done = ptile + 1;
-    }
-    for (int ptile = std::max(0, done - kPStages); ptile < done; ++ptile) {
-      if (!mbar_wait<true>(smem_u32(&pempty[ptile % kPStages]), (ptile / kPStages) & 1, abort_flag, status,
-                           kWhereBwdExit))
+    for (int i = 0; i < 8; ++i) dWacc[i][0] = dWacc[i][1] = dWacc[i][2] = dWacc[i][3] = 0.f;
+    float dwr0 = 0.f, dwr1 = 0.f;  // dw_r columns 2 lane, 2 lane + 1 (row block 0 only)
+    const int r16 = lane & 15, hh = lane >> 4;
+    bool ok = true;
+    int rs = 0, xs = 0;
+    uint32_t xpar = 0;
+    for (int ci = 0; ci < p.nchunks; ++ci) {
+      const int c = p.nchunks - 1 - ci;
+      const int s0 = c * CL;
+      const int L = min(CL, T - s0);
+      const int cb = ci % kCBufs;
+      const bool mine = mbar_wait_timed(smem_u32(&cfull[cb]), (ci / kCBufs) & 1, status, kWhereBwdFull);
+      if (!mine) *gabort = 1;
+      named_bar_sync(3, 128);
+      if (*gabort) {
+        ok = false;
         break;
+      }
+      const uint8_t* cbuf = smem + p.cbuf_off + cb * p.cbuf_bytes;
+      const uint16_t* cv = reinterpret_cast<const uint16_t*>(cbuf + p.cv_off);
+      const float* cdy = reinterpret_cast<const float*>(cbuf + p.cdy_off);
+      for (int s = L - 1; s >= 0; --s, ++rs) {
+        // A give-up is acted on at the next chunk boundary.
+        if (!mbar_wait(smem_u32(&xfull[xs]), xpar, abort_flag, status, kWhereBwdXFull)) *gabort = 1;
+        const uint32_t xb = xring0 + xs * kXSlotBytes;
+        const float* xg = reinterpret_cast<const float*>(smem + p.xring_off + xs * kXSlotBytes);
+        {
+          uint32_t ta[4];
+          ldmatrix_x4_trans(ta, ldsm_addr_b_trans(xb + kXHt, w, lane));
+          const uint32_t a[4] = {ta[0], ta[2], ta[1], ta[3]};
+#pragma unroll
+          for (int nt2 = 0; nt2 < 4; ++nt2) {
+            uint32_t bd[4];
+            ldmatrix_x4_trans(bd, ldsm_addr_b_trans(xb + kXDt, nt2, lane));
+            mma_bf16_16816(dWacc[2 * nt2], a, bd[0], bd[1]);
+            mma_bf16_16816(dWacc[2 * nt2 + 1], a, bd[2], bd[3]);
+          }
+        }
+        if ((rs & 3) == w) {
+          const int64_t rowt = (static_cast<int64_t>(b) * T + s0 + s) * N + n;
+          // dk_t = D_t v_t: lane -> row r16 = g + 8 hi; warps 2 hh, 2 hh + 1 and
+          // their four qd shares, then the two halves (fixed order).
+          {
+            const int gg = r16 & 7, hi = r16 >> 3;
+            const float* xk = xg + kXDk / 4 + 2 * gg + hi;
+            float pk = 0.f;
+#pragma unroll
+            for (int ww = 0; ww < 2; ++ww)
+#pragma unroll
+              for (int qq = 0; qq < 4; ++qq) pk += xk[((2 * hh + ww) * 4 + qq) * kDkGroup];
+            pk += __shfl_xor_sync(0xffffffffu, pk, 16);
+            if (lane < 16) A.dk[rowt * A.K + cta_rank * kRows + r16] = pk;
+          }
+          // Row-block partial of D_t^T k_t: lane -> columns 2 lane, 2 lane + 1.
+          {
+            const float* xdv = xg + kXDv / 4 + 2 * lane;
+            float2 a2 = *reinterpret_cast<const float2*>(xdv);
+#pragma unroll
+            for (int gg = 1; gg < 8; ++gg) {
+              const float2 x = *reinterpret_cast<const float2*>(xdv + gg * kDvStride);
+              a2.x += x.x;
+              a2.y += x.y;
+            }
+            *reinterpret_cast<float2*>(p.dvp + (rowt * R + cta_rank) * kV + 2 * lane) = a2;
+          }
+          // Row-block partial of df_t = <R_t, H_{t-1} - Z_t>.
+          {
+            const float4 e4 = *reinterpret_cast<const float4*>(xg + kXDf / 4 + 4 * lane);
+            float pf = (e4.x + e4.y) + (e4.z + e4.w);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) pf += __shfl_xor_sync(0xffffffffu, pf, o);  // fixed tree
+            if (lane == 0) p.dfp[rowt * R + cta_rank] = pf;
+          }
+          if (cta_rank == 0) {  // dw_r += u_t * v_t, once per chain
+            const float2 uu = *reinterpret_cast<const float2*>(cdy + s * kV + 2 * lane);
+            const uint32_t vb = *reinterpret_cast<const uint32_t*>(cv + s * kV + 2 * lane);
+            dwr0 = fmaf(uu.x, bf16lo(vb), dwr0);
+            dwr1 = fmaf(uu.y, bf16hi(vb), dwr1);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&xempty[xs]));
+        if (++xs == kNX) {
+          xs = 0;
+          xpar ^= 1u;
+        }
+      }
+      // The gradient warps are the last readers of the chunk's inputs.
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&cempty[cb]));
+    }
+    if (ok) {
+      // dW partial of this row block: rows m = 16w + g (+8), columns 8nt + 2qd (+1).
+      float* dwp = A.dW_part + static_cast<int64_t>(blockIdx.x) * kV * kV;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        const int col = 8 * nt + 2 * qd;
+        *reinterpret_cast<float2*>(dwp + (16 * w + g) * kV + col) = make_float2(dWacc[nt][0], dWacc[nt][1]);
+        *reinterpret_cast<float2*>(dwp + (16 * w + g + 8) * kV + col) = make_float2(dWacc[nt][2], dWacc[nt][3]);
+      }
+      // dw_r: the four warps' step subsets, summed in a fixed order.
+      float* sd = reinterpret_cast<float*>(smem + p.dwr_off);
+      *reinterpret_cast<float2*>(sd + w * kV + 2 * lane) = make_float2(dwr0, dwr1);
+      named_bar_sync(3, 128);
+      if (cta_rank == 0 && w == 0) {
+        float2 acc2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int ww = 0; ww < 4; ++ww) {
+          const float2 x = *reinterpret_cast<const float2*>(sd + ww * kV + 2 * lane);
+          acc2.x += x.x;
+          acc2.y += x.y;
+        }
+        *reinterpret_cast<float2*>(A.dwr_part + static_cast<int64_t>(chain) * kV + 2 * lane) = acc2;
+      }
+    } else {
+      *abort_flag = 1;
     }
   }
   tc_fence_before_sync();
@@ -635,13 +631,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// dv = sum over the chain's row blocks of D^T k (fixed order) + w_r * dy;
+// df = sum over the row blocks.  One warp per (b, t, n).
+__global__ void __launch_bounds__(256) mma_backward_rows_kernel(const float* __restrict__ dvp,
+                                                                const float* __restrict__ dfp,
+                                                                const float* __restrict__ dy,
+                                                                const uint16_t* __restrict__ w_r,
+                                                                float* __restrict__ dv, float* __restrict__ df,
+                                                                int64_t rows, int N, int R) {
+  const int lane = threadIdx.x & 31;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; row < rows;
+       row += stride) {
+    const int n = static_cast<int>(row % N);
+    float a0 = 0.f, a1 = 0.f;
+    for (int pr = 0; pr < R; ++pr) {
+      const float2 x = *reinterpret_cast<const float2*>(dvp + (row * R + pr) * kV + 2 * lane);
+      a0 += x.x;
+      a1 += x.y;
+    }
+    const float2 u = *reinterpret_cast<const float2*>(dy + row * kV + 2 * lane);
+    const uint32_t wb = *reinterpret_cast<const uint32_t*>(w_r + static_cast<int64_t>(n) * kV + 2 * lane);
+    *reinterpret_cast<float2*>(dv + row * kV + 2 * lane) = make_float2(fmaf(bf16lo(wb), u.x, a0), fmaf(bf16hi(wb), u.y, a1));
+    if (lane == 0) {
+      float sf = 0.f;
+      for (int pr = 0; pr < R; ++pr) sf += dfp[row * R + pr];
+      df[row] = sf;
+    }
+  }
+}
+
 inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 }  // namespace
 
 bool mma_backward_supported(int K, int V) { return V == kV && K % kRows == 0 && K >= kRows && K <= 128; }
 
-size_t mma_backward_scratch_bytes(int, int, int, int, int) { return 0; }  // the cache is in TMEM
+size_t mma_backward_scratch_bytes(int B, int T, int N, int K, int, int) {
+  const size_t rows = static_cast<size_t>(B) * T * N, R = static_cast<size_t>(K / kRows);
+  return align256(sizeof(float) * rows * R * kV) + align256(sizeof(float) * rows * R);
+}
 
 int mma_backward_max_chunk() { return kMaxChunk; }
 
@@ -652,24 +682,26 @@ cudaError_t launch_mma_backward(const BwdArgs& a, cudaStream_t stream) {
   p.R = a.K / kRows;
   const int C = a.ckpt_every;
   p.nchunks = (a.T + C - 1) / C;
-  p.nptiles = (a.T + kPS - 1) / kPS;
+  p.nbuf = (C <= kTwoBufChunk) ? 2 : 1;
   p.htile_off = 0;
-  p.dtile_off = 4096;
-  p.cbuf_off = 8192;
+  p.cbuf_off = 4096;
   p.cq_off = 0;
   p.ck_off = align_up(C * kRows * 2, 128);
   p.cv_off = p.ck_off + align_up(C * kRows * 2, 128);
   p.cdy_off = p.cv_off + align_up(C * kV * 2, 128);
   p.cf_off = p.cdy_off + align_up(C * kV * 4, 128);
   p.cbuf_bytes = align_up(p.cf_off + C * 4, 128);
-  p.nbuf = (C <= kTwoBufChunk) ? 2 : 1;
-  p.hend_off = p.cbuf_off + kCBufs * p.cbuf_bytes;
-  p.part_off = p.hend_off + 2 * 128 * 8 * 4;
-  p.bar_off = p.part_off + kPStages * kPS * kSlotFloats * 4;
-  p.misc_off = p.bar_off + (kCBufs + 4 + 3 * kPStages) * 8;
-  uint32_t smem = align_up(p.misc_off + 16, 128) + 1024;
-  smem = std::max<uint32_t>(smem, 120 * 1024);
+  p.xring_off = align_up(p.cbuf_off + kCBufs * p.cbuf_bytes, 1024);
+  p.dqp_off = p.xring_off + kNX * kXSlotBytes;
+  p.dwr_off = p.dqp_off + kMaxChunk * 16 * kRows * 4;
+  p.bar_off = p.dwr_off + 4 * kV * 4;
+  p.misc_off = p.bar_off + (2 * kCBufs + 4 + 2 * kNX) * 8;
+  const uint32_t smem = align_up(p.misc_off + 32, 128) + 1024;
   p.tx_bytes = 2 * C * kRows * 2 + C * kV * 2 + C * kV * 4;
+  const size_t rows = static_cast<size_t>(a.B) * a.T * a.N;
+  p.dvp = a.scratch;
+  p.dfp = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(a.scratch) +
+                                   align256(sizeof(float) * rows * p.R * kV));
 
   CUtensorMap mq, mk, mv, mdy;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -678,30 +710,15 @@ cudaError_t launch_mma_backward(const BwdArgs& a, cudaStream_t stream) {
       !make_tensor_map_btnx(&mv, a.v, bf, 2, a.B, a.T, a.N, kV, kV, C) ||
       !make_tensor_map_btnx(&mdy, a.dy, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.B, a.T, a.N, kV, kV, C))
     return cudaErrorInvalidValue;
-  // The warpgroups' register budgets must fit in what the launch holds, or
-  // the reverse warps' increase would wait forever: check the built kernel.
-  cudaFuncAttributes fa{};
-  cudaError_t e = cudaFuncGetAttributes(&fa, mma_backward_kernel);
+  cudaError_t e = cudaFuncSetAttribute(mma_backward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  if (kReverseRegs + kRecomputeRegs + kReducerRegs > 3 * fa.numRegs || fa.numRegs > kLaunchRegs)
-    return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(mma_backward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem));
+  mma_backward_kernel<<<static_cast<unsigned>(a.B * a.N * p.R), kThreads, smem, stream>>>(p, mq, mk, mv, mdy);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(a.B * a.N * p.R));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(p.R);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, mma_backward_kernel, p, mq, mk, mv, mdy);
-  if (e != cudaSuccess) return e;
+  const int blocks = static_cast<int>(std::min<size_t>((rows + 7) / 8, 152 * 16));
+  mma_backward_rows_kernel<<<blocks, 256, 0, stream>>>(p.dvp, p.dfp, a.dy, static_cast<const uint16_t*>(a.w_r),
+                                                       a.dv, a.df, static_cast<int64_t>(rows), a.N, p.R);
   return cudaGetLastError();
 }
 

@@ -81,9 +81,9 @@ extern "C" int m2rnn_backward_noalloc(const void* q, const void* k, const void* 
   const size_t status_bytes = sizeof(StatusBlock);
   const size_t dwp_bytes = round256(sizeof(float) * static_cast<size_t>(B * N * parts) * V * V);
   const size_t dwr_bytes = round256(sizeof(float) * static_cast<size_t>(B * N) * V);
-  const size_t scr_bytes = round256(mma_backward_scratch_bytes(static_cast<int>(B), static_cast<int>(N),
-                                                               static_cast<int>(K), static_cast<int>(V),
-                                                               ckpt_every));
+  const size_t scr_bytes = round256(mma_backward_scratch_bytes(static_cast<int>(B), static_cast<int>(T),
+                                                               static_cast<int>(N), static_cast<int>(K),
+                                                               static_cast<int>(V), ckpt_every));
   if (status_bytes + dwp_bytes + dwr_bytes + scr_bytes > kStaticScratchBytes)
     return M2RNN_ERR_WORKSPACE;  // the problem needs more scratch than the built-in array holds
 

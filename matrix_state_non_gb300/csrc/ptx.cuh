@@ -57,19 +57,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
-// Per-thread register budget of the executing warpgroup (all four warps of
-// the warpgroup execute the same instruction).  The increase waits until the
-// CTA's other warpgroups have released enough registers: the launch must hold
-// at least the sum of every warpgroup's budget.
-template <uint32_t kRegs>
-__device__ __forceinline__ void warpgroup_reg_increase() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kRegs));
-}
-template <uint32_t kRegs>
-__device__ __forceinline__ void warpgroup_reg_decrease() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegs));
-}
-
 // Raise the expected transaction bytes of the current phase without arriving.
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");

@@ -22,10 +22,9 @@ constexpr uint32_t kWhereFwdFull = 101, kWhereFwdEmpty = 102, kWhereFwdD = 103,
                    kWhereFwdYFull = 104, kWhereFwdYPeer = 105, kWhereFwdYEmpty = 106,
                    kWhereFwdDrain = 107, kWhereFwdExit = 108,
                    kWhereFwdH = 109;
-constexpr uint32_t kWhereBwdFull = 201, kWhereBwdEmpty = 202, kWhereBwdD = 203,
-                   kWhereBwdPeer = 204, kWhereBwdPeerEmpty = 205, kWhereBwdDrain = 206,
-                   kWhereBwdExit = 207, kWhereBwdRec = 208, kWhereBwdTFree = 209,
-                   kWhereBwdTReady = 210;
+constexpr uint32_t kWhereBwdFull = 201, kWhereBwdCEmpty = 202, kWhereBwdTReady = 203,
+                   kWhereBwdTFree = 204, kWhereBwdXFull = 205, kWhereBwdXEmpty = 206,
+                   kWhereBwdDrain = 207;
 
 __device__ __forceinline__ void report_device_error(StatusBlock* s, unsigned int code,
                                                     uint32_t where) {
