@@ -30,9 +30,11 @@
  *    recorded in the workspace status block and reported by
  *    m2rnn_sync_status.
  *  - Supported shapes: B, T, N >= 1; K, V in [1, 128].  bf16 inputs with
- *    V in {64, 128} and K a multiple of 16 (and at most 128) run on the
- *    tensor-core (tcgen05) kernels; every other supported shape runs on the
- *    fp32 CUDA-core kernels.  Nothing runs on the host CPU.
+ *    K a multiple of 16 (and at most 128) run on tensor-core kernels: V = 64
+ *    on the warp-MMA scans (the backward for ckpt_every <= 28, its dW on
+ *    tcgen05), V = 128 (forward, K in {32, 64, 128}) on tcgen05.  Every
+ *    other supported shape runs on the fp32 CUDA-core kernels.  Nothing runs
+ *    on the host CPU.
  */
 #ifndef M2RNN_H_
 #define M2RNN_H_
@@ -147,7 +149,7 @@ int m2rnn_sync_status(void* workspace, void* cuda_stream, uint32_t* detail);
  * inputs and outputs.
  *
  * Limits: bf16 inputs, V = 64, K a multiple of 16 (<= 128), 1 <= ckpt_every
- * <= 32, and `ckpt` (the forward's checkpoints for this ckpt_every) is
+ * <= 28, and `ckpt` (the forward's checkpoints for this ckpt_every) is
  * required whenever T > ckpt_every.  A problem whose scratch would exceed the
  * built-in 32 MiB returns M2RNN_ERR_WORKSPACE; other shapes return
  * M2RNN_ERR_UNSUPPORTED.  Nothing is allocated, on the host or the device.

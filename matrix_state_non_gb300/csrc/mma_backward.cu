@@ -13,27 +13,27 @@
 // Work split as in the forward: a chain's K rows in blocks of 16, one CTA per
 // block (rows never mix; only dv_t, df_t, dW and dw_r sum over rows, and
 // those are written as row-block partials and summed afterwards in a fixed
-// order).  The time axis runs over chunks of C <= 32 steps, last chunk first;
+// order).  The time axis runs over chunks of C <= 28 steps, last chunk first;
 // for each chunk the forward is rerun from its checkpoint (section 2.6 of the
 // notes describes the paper's rerun-and-cache backward; here only one or two
-// chunks are cached) and then walked backwards.  Three warpgroups, each warp
-// owning 16 value columns (or, for the gradient warps, 16 rows of dW):
-//   reverse warps   the serial chain only: R -> D -> bf16(D) tile -> one
-//                   named barrier -> 8 warp MMAs seeded with f R -> C_{t-1};
-//                   then they hand D (fp32 and bf16), E = R * (H_{t-1} - Z)
-//                   and bf16 H_{t-1} to the gradient warps through a ring of
-//                   shared-memory slots;
-//   recompute warps the forward rerun of the next chunk (Eq. 10-11), caching
-//                   each thread's Z_t and H_{t-1} values (fp32) in its own
-//                   lane of tensor memory, so the cache never touches DRAM;
-//                   also dq_t = H_t u_t, and the chunk loads (TMA);
-//   gradient warps  dW += H_{t-1}^T D_t (8 warp MMAs per warp per step into
-//                   register accumulators), dk_t, the row-block partials of
-//                   dv_t and df_t, and dw_r.
-// Warp w of each warpgroup runs on scheduler w, so the three interleave.  With
-// C <= 16 two chunk caches fit in the 512 TMEM columns and the recompute of
-// chunk c-1 overlaps the reverse walk of chunk c; with 16 < C <= 32 the two
-// alternate.
+// chunks are cached) and then walked backwards.  Three warpgroups:
+//   reverse warps   (each owning 16 value columns) the serial chain only:
+//                   R -> D -> bf16(D) tile -> one named barrier -> 8 warp MMAs
+//                   seeded with f R -> C_{t-1}; then their shares of dk, dv,
+//                   df and the bf16 D and H_{t-1} tiles go to the gradient
+//                   warps through a ring of shared-memory slots;
+//   recompute warps (each owning 16 value columns) the forward rerun of the
+//                   next chunk (Eq. 10-11), caching each thread's Z_t and
+//                   H_{t-1} values (fp32) in its own lane of tensor memory, so
+//                   the cache never touches DRAM; also dq_t = H_t u_t and the
+//                   chunk loads (TMA);
+//   gradient warps  dW += H_{t-1}^T D_t as one tcgen05 MMA per step into a
+//                   tensor-memory accumulator, and the fixed-order sums of
+//                   the dk, dv, df shares and dw_r.
+// Warp w of each warpgroup runs on scheduler w, so the three interleave.  The
+// chunk caches take 16 TMEM columns per step and the dW accumulator 64: with
+// C <= 14 two caches fit and the recompute of chunk c-1 overlaps the reverse
+// walk of chunk c; with 14 < C <= 28 the two alternate.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -48,21 +48,40 @@ namespace {
 constexpr int kV = 64;
 constexpr int kRows = 16;
 constexpr int kThreads = 384;     // reverse warps 0-3, recompute warps 4-7, gradient warps 8-11
-constexpr int kMaxChunk = 32;     // one chunk cache fills the 512 TMEM columns at 32 steps
-constexpr int kTwoBufChunk = 16;  // up to 16 steps two caches fit: the recompute runs a chunk ahead
+// Tensor memory: columns [0, 448) hold the chunk caches (16 columns per step),
+// columns [448, 512) the dW accumulator.
+constexpr int kDWCol = 448;
+constexpr int kMaxChunk = kDWCol / 16;     // 28: one chunk cache
+constexpr int kTwoBufChunk = kDWCol / 32;  // 14: two caches, the recompute runs a chunk ahead
 constexpr int kCBufs = 4;         // chunk input buffers (reverse, gradient, recompute, loading)
 constexpr int kNX = 8;            // exchange ring slots, reverse -> gradient warps
 // Exchange slot (reverse -> gradient warps), one per time step:
-//   Dt  bf16 D tile (also the A operand of the reverse warps' chain MMAs)
-//   Ht  bf16 H_{t-1} tile
+//   Dt  bf16 D tile: A operand of the reverse warps' chain MMAs (ldmatrix) and
+//       B operand of the dW MMA (tcgen05)
+//   Ht  bf16 H_{t-1} tile, followed by 2 KB of zeros: A operand of the dW MMA,
+//       H_{t-1}^T padded from 64 to 128 rows
 //   Dv  per-thread sums of D k over the thread's two rows: [g][64 columns], rows padded to 72 floats
 //   Dk  per-thread sums of D v over the thread's four columns: [warp][qd][g][row g, g+8], groups padded to 18
 //   Df  per-thread sums of R (H_{t-1} - Z) over the thread's eight values: [128]
 // (strides chosen so that both the writers' and the readers' accesses are free of bank conflicts).
+// Both bf16 tiles use the canonical no-swizzle core-matrix layout: the 8 x 8
+// block (rows 8i.., columns 8j..) is 128 contiguous bytes at 256 j + 128 i, so
+// as tcgen05 operands (MN-major, the columns contiguous) the core matrices
+// advance by 128 bytes along K (the 16 rows) and 256 bytes along M / N.
 constexpr int kDvStride = 72, kDkGroup = 18;
-constexpr uint32_t kXDt = 0, kXHt = 2048, kXDv = 4096, kXDk = kXDv + 8 * kDvStride * 4,
-                   kXDf = kXDk + 16 * kDkGroup * 4, kXSlotBytes = 8192;
+constexpr uint32_t kXDt = 0, kXHt = 2048, kXZero = 4096, kXDv = 6144, kXDk = kXDv + 8 * kDvStride * 4,
+                   kXDf = kXDk + 16 * kDkGroup * 4, kXSlotBytes = 10240;
 static_assert(kXDf + 128 * 4 <= kXSlotBytes, "exchange slot overflow");
+
+__device__ __forceinline__ uint32_t cm_off(int row, int col) {
+  return static_cast<uint32_t>((col >> 3) * 256 + (row >> 3) * 128 + (row & 7) * 16 + (col & 7) * 2);
+}
+// ldmatrix.x4 address for the A fragments of k-tile kt (columns 16kt..16kt+15)
+// of a core-matrix tile: matrices (rows 0-7 | 8-15) x (columns 16kt.. | 16kt+8..).
+__device__ __forceinline__ uint32_t cm_ldsm_a(uint32_t tile, int kt, int lane) {
+  const int mi = lane >> 3;
+  return tile + cm_off((lane & 7) + (mi & 1) * 8, 16 * kt + (mi >> 1) * 8);
+}
 
 struct MmaBwdParams {
   BwdArgs a;
@@ -97,6 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tfree = tready + 2;
   uint64_t* xfull = tfree + 2;
   uint64_t* xempty = xfull + kNX;
+  uint64_t* dwdone = xempty + kNX;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.misc_off);
   volatile int* vabort = reinterpret_cast<volatile int*>(smem + p.misc_off + 4);
   volatile int* rabort = reinterpret_cast<volatile int*>(smem + p.misc_off + 8);
@@ -116,18 +136,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kNX; ++i) {
       mbar_init(smem_u32(&xfull[i]), 4);     // the reverse warps
-      mbar_init(smem_u32(&xempty[i]), 4);    // the gradient warps
+      mbar_init(smem_u32(&xempty[i]), 2);    // the dW MMA's commit + the step's duty warp
     }
+    mbar_init(smem_u32(dwdone), 1);          // every dW MMA complete
     *abort_flag = 0;
     *vabort = 0;
     *rabort = 0;
     *gabort = 0;
     fence_mbar_init_cluster();
   }
-  if (warp == 0) {  // the whole tensor memory: the per-thread chunk caches
+  if (warp == 0) {  // the whole tensor memory: chunk caches and the dW accumulator
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
+  // The zero halves of the dW MMA's A operand, written once.
+  for (uint32_t i = threadIdx.x; i < kNX * 128u; i += kThreads) {
+    const uint32_t slot = i >> 7, part = i & 127u;
+    *reinterpret_cast<uint4*>(smem + p.xring_off + slot * kXSlotBytes + kXZero + part * 16) =
+        make_uint4(0u, 0u, 0u, 0u);
+  }
+  fence_proxy_async_smem();
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -137,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // jcol0 + 8nt + {0,1}, rows g and g+8 of the CTA's block).  Reverse warp w
   // and recompute warp w + 4 share TMEM lanes 32w.. and the same fragment
   // positions, so each reverse thread reads exactly what its recompute
-  // partner cached: buffer tb, slot s = columns 256 tb + 16 s .. + 15 holding
+  // partner cached: buffer tb, slot s = columns 16 (C tb + s) .. + 15 holding
   // {Z_s (8 values), H_{s-1} (8 values)}.
   const int w = warp & 3;
   const int g = lane >> 2, qd = lane & 3;
@@ -150,16 +178,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
     // ======================= reverse warps =======================
-    // Backward transform fragments: B[k = j][col = m] = W[16w + m][j] (D W^T).
+    // Backward transform fragments: B[k = j][col = m] = W[16w + m][j] (D W^T),
+    // k-tiles in the order w, w+1, w+2, w+3 (mod 4): the first is this warp's
+    // own 16 columns of D, whose A fragments it already holds.
     uint32_t bt[2][4][2];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       const int col = 16 * w + 8 * nt + g;
 #pragma unroll
-      for (int kt = 0; kt < 4; ++kt) {
-        const int k0 = 16 * kt + 2 * qd;
-        bt[nt][kt][0] = *reinterpret_cast<const uint32_t*>(Wg + col * kV + k0);
-        bt[nt][kt][1] = *reinterpret_cast<const uint32_t*>(Wg + col * kV + k0 + 8);
+      for (int i = 0; i < 4; ++i) {
+        const int k0 = 16 * ((w + i) & 3) + 2 * qd;
+        bt[nt][i][0] = *reinterpret_cast<const uint32_t*>(Wg + col * kV + k0);
+        bt[nt][i][1] = *reinterpret_cast<const uint32_t*>(Wg + col * kV + k0 + 8);
       }
     }
     // State gradient C (C-fragment layout), initialised with dH_T.
@@ -199,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint16_t* cv = reinterpret_cast<const uint16_t*>(cbuf + p.cv_off);
       const float* cdy = reinterpret_cast<const float*>(cbuf + p.cdy_off);
       const float* cf = reinterpret_cast<const float*>(cbuf + p.cf_off);
-      const uint32_t tbuf = tcache + 256 * tb;
+      const uint32_t tbuf = tcache + 16 * CL * tb;
       // The next slot's TMEM load is issued one step ahead and waited for at
       // the top of the step.
       uint32_t slot_regs[16];
@@ -247,27 +277,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             Dv[nt][e] = omf * Rv[nt][e] * fmaf(-zz, zz, 1.f);
           }
         }
+        // Serial chain: C_{t-1} = f R + D W^T on the warp MMAs.  bf16(D) of
+        // this warp's columns is its own k-tile (the accumulator layout of
+        // two n-tiles is the A layout of one k-tile): those two MMAs run
+        // while the other three k-tiles load from the tile.
         const uint32_t dt = xb + kXDt;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const int col = jcol0 + 8 * nt;
-          st_shared_b32(dt + tile_off(g, col), pack2_bf16(Dv[nt][0], Dv[nt][1]));
-          st_shared_b32(dt + tile_off(g + 8, col), pack2_bf16(Dv[nt][2], Dv[nt][3]));
-        }
+        uint32_t aown[4];
+        aown[0] = pack2_bf16(Dv[0][0], Dv[0][1]);
+        aown[1] = pack2_bf16(Dv[0][2], Dv[0][3]);
+        aown[2] = pack2_bf16(Dv[1][0], Dv[1][1]);
+        aown[3] = pack2_bf16(Dv[1][2], Dv[1][3]);
+        st_shared_b32(dt + cm_off(g, jcol0), aown[0]);
+        st_shared_b32(dt + cm_off(g + 8, jcol0), aown[1]);
+        st_shared_b32(dt + cm_off(g, jcol0 + 8), aown[2]);
+        st_shared_b32(dt + cm_off(g + 8, jcol0 + 8), aown[3]);
         named_bar_sync(1, 128);
-        // Serial chain: C_{t-1} = f R + D W^T on the warp MMAs.
+        uint32_t af[3][4];
+#pragma unroll
+        for (int i = 0; i < 3; ++i) ldmatrix_x4(af[i], cm_ldsm_a(dt, (w + 1 + i) & 3, lane));
         float acc[2][4];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[nt][e] = ft * Rv[nt][e];
-        uint32_t af[4][4];
+          mma_bf16_16816(acc[nt], aown, bt[nt][0][0], bt[nt][0][1]);
+        }
 #pragma unroll
-        for (int kt = 0; kt < 4; ++kt) ldmatrix_x4(af[kt], ldsm_addr_a(dt, kt, lane));
+        for (int i = 0; i < 3; ++i)
 #pragma unroll
-        for (int kt = 0; kt < 4; ++kt)
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) mma_bf16_16816(acc[nt], af[kt], bt[nt][kt][0], bt[nt][kt][1]);
+          for (int nt = 0; nt < 2; ++nt) mma_bf16_16816(acc[nt], af[i], bt[nt][i + 1][0], bt[nt][i + 1][1]);
         // Off the chain: this thread's shares of dk, dv, df, and bf16 H_{t-1}
         // for dW, handed to the gradient warps.
         {
@@ -289,12 +327,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 4; ++e) pe = fmaf(Rv[nt][e], Hp[nt][e] - Z[nt][e], pe);
             *reinterpret_cast<float2*>(xdv + g * kDvStride + col) =
                 make_float2(fmaf(Dv[nt][0], k0, Dv[nt][2] * k1), fmaf(Dv[nt][1], k0, Dv[nt][3] * k1));
-            st_shared_b32(ht + tile_off(g, col), pack2_bf16(Hp[nt][0], Hp[nt][1]));
-            st_shared_b32(ht + tile_off(g + 8, col), pack2_bf16(Hp[nt][2], Hp[nt][3]));
+            st_shared_b32(ht + cm_off(g, col), pack2_bf16(Hp[nt][0], Hp[nt][1]));
+            st_shared_b32(ht + cm_off(g + 8, col), pack2_bf16(Hp[nt][2], Hp[nt][3]));
           }
           *reinterpret_cast<float2*>(xg + kXDk / 4 + (w * 4 + qd) * kDkGroup + 2 * g) = make_float2(pk0, pk1);
           xg[kXDf / 4 + ctid] = pe;
         }
+        fence_proxy_async_smem();  // the tiles are read by the tensor core
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&xfull[xs]));
 #pragma unroll
@@ -315,14 +354,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) *abort_flag = 1;
   } else if (warp < 8) {
     // ======================= recompute warps (Eq. 10-11) =======================
-    // Forward transform fragments: B[k][col] = W[k][16w + col].
+    // Forward transform fragments: B[k][col] = W[k][16w + col], k-tiles in
+    // the order w, w+1, w+2, w+3 (mod 4): the first is this warp's own 16
+    // columns of H, whose A fragments it holds in registers.
     uint32_t bw[2][4][2];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       const int col = 16 * w + 8 * nt + g;
 #pragma unroll
       for (int kt = 0; kt < 4; ++kt) {
-        const int k0 = 16 * kt + 2 * qd;
+        const int k0 = 16 * ((w + kt) & 3) + 2 * qd;
         bw[nt][kt][0] = static_cast<uint32_t>(Wg[k0 * kV + col]) |
                         (static_cast<uint32_t>(Wg[(k0 + 1) * kV + col]) << 16);
         bw[nt][kt][1] = static_cast<uint32_t>(Wg[(k0 + 8) * kV + col]) |
@@ -331,6 +372,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const uint32_t htile0 = smem_u32(smem + p.htile_off);
     float* dqp = reinterpret_cast<float*>(smem + p.dqp_off);  // [C][4 warps][4 qd][8 g][row g, g+8]
+    // Start state of a chunk: the checkpoint (zero for chunk 0).  The next
+    // chunk's is loaded a chunk ahead, so its latency stays off the path.
+    auto load_start = [&](int cc, float (&hs)[2][4]) {
+      if (cc == 0) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) hs[nt][0] = hs[nt][1] = hs[nt][2] = hs[nt][3] = 0.f;
+      } else {
+        const float* src =
+            A.ckpt + ((static_cast<int64_t>(chain) * A.n_ckpt + (cc - 1)) * A.K + row_g) * kV + jcol0;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const float2 x0 = *reinterpret_cast<const float2*>(src + 8 * nt);
+          const float2 x1 = *reinterpret_cast<const float2*>(src + 8 * kV + 8 * nt);
+          hs[nt][0] = x0.x; hs[nt][1] = x0.y; hs[nt][2] = x1.x; hs[nt][3] = x1.y;
+        }
+      }
+    };
+    float hnext[2][4];
+    load_start(p.nchunks - 1, hnext);
     // Warp 4 also loads the chunk inputs, one chunk ahead of its own use:
     // q, k, v, dy by TMA, f gathered by the lanes (its global-load latency
     // hidden behind the chunk's recompute) and published at the chunk's end.
@@ -396,33 +456,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint16_t* cv = reinterpret_cast<const uint16_t*>(cbuf + p.cv_off);
       const float* cdy = reinterpret_cast<const float*>(cbuf + p.cdy_off);
       const float* cf = reinterpret_cast<const float*>(cbuf + p.cf_off);
-      const uint32_t tbuf = tcache + 256 * tb;
+      const uint32_t tbuf = tcache + 16 * CL * tb;
       float h[2][4];
-      if (c == 0) {
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) h[nt][0] = h[nt][1] = h[nt][2] = h[nt][3] = 0.f;
-      } else {
-        const float* src =
-            A.ckpt + ((static_cast<int64_t>(chain) * A.n_ckpt + (c - 1)) * A.K + row_g) * kV + jcol0;
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const float2 x0 = *reinterpret_cast<const float2*>(src + 8 * nt);
-          const float2 x1 = *reinterpret_cast<const float2*>(src + 8 * kV + 8 * nt);
-          h[nt][0] = x0.x; h[nt][1] = x0.y; h[nt][2] = x1.x; h[nt][3] = x1.y;
-        }
-      }
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const int col = jcol0 + 8 * nt;
-        st_shared_b32(htile0 + tile_off(g, col), pack2_bf16(h[nt][0], h[nt][1]));
-        st_shared_b32(htile0 + tile_off(g + 8, col), pack2_bf16(h[nt][2], h[nt][3]));
-      }
-      named_bar_sync(2, 128);
-      for (int s = 0; s < L; ++s) {
+        for (int e = 0; e < 4; ++e) h[nt][e] = hnext[nt][e];
+      if (c > 0) load_start(c - 1, hnext);
+      // Step s: acc = k_s v_s^T + H_{s-1} W with H_{s-1}'s own k-tile taken
+      // from registers (while the other three load from the bf16 tile).
+      uint32_t hown[4];
+      hown[0] = pack2_bf16(h[0][0], h[0][1]);
+      hown[1] = pack2_bf16(h[0][2], h[0][3]);
+      hown[2] = pack2_bf16(h[1][0], h[1][1]);
+      hown[3] = pack2_bf16(h[1][2], h[1][3]);
+      st_shared_b32(htile0 + tile_off(g, jcol0), hown[0]);
+      st_shared_b32(htile0 + tile_off(g + 8, jcol0), hown[1]);
+      st_shared_b32(htile0 + tile_off(g, jcol0 + 8), hown[2]);
+      st_shared_b32(htile0 + tile_off(g + 8, jcol0 + 8), hown[3]);
+      float acc[2][4];
+      auto start_step = [&](int s) {
         const float k0 = bf16_bits_to_f32(ck[s * kRows + g]);
         const float k1 = bf16_bits_to_f32(ck[s * kRows + g + 8]);
-        const float omf = 1.f - cf[s];
-        float acc[2][4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           const uint32_t vv = *reinterpret_cast<const uint32_t*>(cv + s * kV + jcol0 + 8 * nt);
@@ -431,19 +486,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc[nt][1] = k0 * v1;
           acc[nt][2] = k1 * v0;
           acc[nt][3] = k1 * v1;
+          mma_bf16_16816(acc[nt], hown, bw[nt][0][0], bw[nt][0][1]);
         }
+      };
+      named_bar_sync(2, 128);
+      for (int s = 0; s < L; ++s) {
+        const float omf = 1.f - cf[s];
         const uint32_t atile = htile0 + (s & 1) * 2048;
-        uint32_t af[4][4];
+        uint32_t af[3][4];
 #pragma unroll
-        for (int kt = 0; kt < 4; ++kt) ldmatrix_x4(af[kt], ldsm_addr_a(atile, kt, lane));
+        for (int i = 0; i < 3; ++i) ldmatrix_x4(af[i], ldsm_addr_a(atile, (w + 1 + i) & 3, lane));
+        start_step(s);
 #pragma unroll
-        for (int kt = 0; kt < 4; ++kt)
+        for (int i = 0; i < 3; ++i)
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt) mma_bf16_16816(acc[nt], af[kt], bw[nt][kt][0], bw[nt][kt][1]);
+          for (int nt = 0; nt < 2; ++nt) mma_bf16_16816(acc[nt], af[i], bw[nt][i + 1][0], bw[nt][i + 1][1]);
         const uint32_t otile = htile0 + ((s + 1) & 1) * 2048;
         uint32_t cache[16];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float z = tanh_fast(acc[nt][e]);
@@ -451,10 +512,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             cache[8 + 4 * nt + e] = __float_as_uint(h[nt][e]);  // H_{s-1}
             h[nt][e] = fmaf(omf, z - h[nt][e], h[nt][e]);
           }
-          const int col = jcol0 + 8 * nt;
-          st_shared_b32(otile + tile_off(g, col), pack2_bf16(h[nt][0], h[nt][1]));
-          st_shared_b32(otile + tile_off(g + 8, col), pack2_bf16(h[nt][2], h[nt][3]));
-        }
+        hown[0] = pack2_bf16(h[0][0], h[0][1]);
+        hown[1] = pack2_bf16(h[0][2], h[0][3]);
+        hown[2] = pack2_bf16(h[1][0], h[1][1]);
+        hown[3] = pack2_bf16(h[1][2], h[1][3]);
+        st_shared_b32(otile + tile_off(g, jcol0), hown[0]);
+        st_shared_b32(otile + tile_off(g + 8, jcol0), hown[1]);
+        st_shared_b32(otile + tile_off(g, jcol0 + 8), hown[2]);
+        st_shared_b32(otile + tile_off(g + 8, jcol0 + 8), hown[3]);
         tmem_st_32x32b_x16(tbuf + 16 * s, cache);
         // dq_t = H_t u_t: this thread's share (its four columns, rows g and
         // g + 8); the sixteen shares of a row are summed at the chunk's end.
@@ -482,12 +547,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // dq rows of the chunk (the last step's barrier ordered every share):
       // the sixteen shares of row r = g + 8 hi, warp by warp, in a fixed order.
       for (int idx = ctid; idx < L * kRows; idx += 128) {
-        const int s = idx >> 4, r = idx & 15;
-        const float* pp = dqp + s * 16 * kRows + 2 * (r & 7) + (r >> 3);
+        const int sp = idx >> 4, r = idx & 15;
+        const float* pp = dqp + sp * 16 * kRows + 2 * (r & 7) + (r >> 3);
         float sum = 0.f;
 #pragma unroll
         for (int sh = 0; sh < 16; ++sh) sum += pp[sh * kRows];
-        const int64_t rowt = (static_cast<int64_t>(b) * T + s0 + s) * N + n;
+        const int64_t rowt = (static_cast<int64_t>(b) * T + s0 + sp) * N + n;
         A.dq[rowt * A.K + cta_rank * kRows + r] = sum;
       }
     }
@@ -500,14 +565,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ======================= gradient warps =======================
-    // Warp w: dW rows 16w..16w+15 (A = H_{t-1}^T from the bf16 H tile, B = D
-    // from the bf16 D tile); every fourth step (rs % 4 == w) also the row and
-    // column sums of that step.
-    float dWacc[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) dWacc[i][0] = dWacc[i][1] = dWacc[i][2] = dWacc[i][3] = 0.f;
+    // Warp 8 issues the step's dW MMA (one elected lane, tcgen05, the
+    // accumulator in TMEM columns 448..511):
+    //   dW (+)= [H_{t-1}^T ; 0] (128 x 16) * D (16 x 64),
+    // committed to the slot's empty barrier.  Every fourth step (rs % 4 == w)
+    // warp 8 + w also sums that step's dk, dv and df shares.
     float dwr0 = 0.f, dwr1 = 0.f;  // dw_r columns 2 lane, 2 lane + 1 (row block 0 only)
     const int r16 = lane & 15, hh = lane >> 4;
+    const uint32_t idesc = idesc_bf16_f32(128, kV, /*a_mn_major=*/true, /*b_mn_major=*/true);
+    const uint32_t dw_tmem = tmem_base + kDWCol;
     bool ok = true;
     int rs = 0, xs = 0;
     uint32_t xpar = 0;
@@ -527,23 +593,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint16_t* cv = reinterpret_cast<const uint16_t*>(cbuf + p.cv_off);
       const float* cdy = reinterpret_cast<const float*>(cbuf + p.cdy_off);
       for (int s = L - 1; s >= 0; --s, ++rs) {
-        // A give-up is acted on at the next chunk boundary.
-        if (!mbar_wait(smem_u32(&xfull[xs]), xpar, abort_flag, status, kWhereBwdXFull)) *gabort = 1;
+        const bool duty = (rs & 3) == w;
         const uint32_t xb = xring0 + xs * kXSlotBytes;
         const float* xg = reinterpret_cast<const float*>(smem + p.xring_off + xs * kXSlotBytes);
-        {
-          uint32_t ta[4];
-          ldmatrix_x4_trans(ta, ldsm_addr_b_trans(xb + kXHt, w, lane));
-          const uint32_t a[4] = {ta[0], ta[2], ta[1], ta[3]};
-#pragma unroll
-          for (int nt2 = 0; nt2 < 4; ++nt2) {
-            uint32_t bd[4];
-            ldmatrix_x4_trans(bd, ldsm_addr_b_trans(xb + kXDt, nt2, lane));
-            mma_bf16_16816(dWacc[2 * nt2], a, bd[0], bd[1]);
-            mma_bf16_16816(dWacc[2 * nt2 + 1], a, bd[2], bd[3]);
+        // A give-up is acted on at the next chunk boundary.
+        if ((w == 0 || duty) && !mbar_wait(smem_u32(&xfull[xs]), xpar, abort_flag, status, kWhereBwdXFull))
+          *gabort = 1;
+        if (w == 0) {
+          tc_fence_after_sync();
+          if (elect_one()) {
+            tc_mma_f16_ss(dw_tmem, smem_desc_noswizzle(xb + kXHt, 128, 256),
+                          smem_desc_noswizzle(xb + kXDt, 128, 256), idesc, rs > 0 ? 1u : 0u);
+            tc_commit(smem_u32(&xempty[xs]));  // arrives once the MMA has read the slot
           }
+          __syncwarp();
         }
-        if ((rs & 3) == w) {
+        if (duty) {
           const int64_t rowt = (static_cast<int64_t>(b) * T + s0 + s) * N + n;
           // dk_t = D_t v_t: lane -> row r16 = g + 8 hi; warps 2 hh, 2 hh + 1 and
           // their four qd shares, then the two halves (fixed order).
@@ -584,9 +649,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             dwr0 = fmaf(uu.x, bf16lo(vb), dwr0);
             dwr1 = fmaf(uu.y, bf16hi(vb), dwr1);
           }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&xempty[xs]));
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&xempty[xs]));
         if (++xs == kNX) {
           xs = 0;
           xpar ^= 1u;
@@ -596,14 +661,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&cempty[cb]));
     }
+    // No dW MMA may still be running when tensor memory is released.
+    if (w == 0 && rs > 0) {
+      if (elect_one()) tc_commit(smem_u32(dwdone));
+      __syncwarp();
+    }
     if (ok) {
-      // dW partial of this row block: rows m = 16w + g (+8), columns 8nt + 2qd (+1).
-      float* dwp = A.dW_part + static_cast<int64_t>(blockIdx.x) * kV * kV;
+      // dW partial of this row block from TMEM: accumulator row m = lane 32w + lane
+      // (rows 64..127 are the zero padding), column n = 448 + n.
+      if (w < 2) {
+        if (!mbar_wait_timed(smem_u32(dwdone), 0, status, kWhereBwdDW)) *gabort = 1;
+        tc_fence_after_sync();
+        float* dwp = A.dW_part + static_cast<int64_t>(blockIdx.x) * kV * kV + (32 * w + lane) * kV;
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        const int col = 8 * nt + 2 * qd;
-        *reinterpret_cast<float2*>(dwp + (16 * w + g) * kV + col) = make_float2(dWacc[nt][0], dWacc[nt][1]);
-        *reinterpret_cast<float2*>(dwp + (16 * w + g + 8) * kV + col) = make_float2(dWacc[nt][2], dWacc[nt][3]);
+        for (int half = 0; half < 2; ++half) {
+          uint32_t r[32];
+          tmem_ld_32x32b<32>(tmem_base + (static_cast<uint32_t>(32 * w) << 16) + kDWCol + 32 * half, r);
+          tmem_ld_wait();
+          tmem_ld_fence_regs(r);
+#pragma unroll
+          for (int c4 = 0; c4 < 32; c4 += 4)
+            *reinterpret_cast<float4*>(dwp + 32 * half + c4) =
+                make_float4(__uint_as_float(r[c4]), __uint_as_float(r[c4 + 1]), __uint_as_float(r[c4 + 2]),
+                            __uint_as_float(r[c4 + 3]));
+        }
       }
       // dw_r: the four warps' step subsets, summed in a fixed order.
       float* sd = reinterpret_cast<float*>(smem + p.dwr_off);
@@ -621,6 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {
       *abort_flag = 1;
+      if (w == 0 && rs > 0) mbar_wait_timed(smem_u32(dwdone), 0, nullptr, kWhereBwdDW);
     }
   }
   tc_fence_before_sync();
@@ -695,7 +777,7 @@ cudaError_t launch_mma_backward(const BwdArgs& a, cudaStream_t stream) {
   p.dqp_off = p.xring_off + kNX * kXSlotBytes;
   p.dwr_off = p.dqp_off + kMaxChunk * 16 * kRows * 4;
   p.bar_off = p.dwr_off + 4 * kV * 4;
-  p.misc_off = p.bar_off + (2 * kCBufs + 4 + 2 * kNX) * 8;
+  p.misc_off = p.bar_off + (2 * kCBufs + 4 + 2 * kNX + 1) * 8;
   const uint32_t smem = align_up(p.misc_off + 32, 128) + 1024;
   p.tx_bytes = 2 * C * kRows * 2 + C * kV * 2 + C * kV * 4;
   const size_t rows = static_cast<size_t>(a.B) * a.T * a.N;

@@ -50,6 +50,6 @@ def test_backward_noalloc_matches_workspace_entry_point():
 def test_backward_noalloc_rejects_oversized_problem():
     from matrix_state_non_gb300 import binding
     # 1024 chains of 128 rows need 128 MiB of dW partials, more than the built-in scratch.
-    st = binding.m2rnn_backward_noalloc(*([16] * 9), 32, *([16] * 6), 16, 1024, 64, 128, 64,
+    st = binding.m2rnn_backward_noalloc(*([16] * 9), 16, *([16] * 6), 16, 1024, 64, 128, 64,
                                         binding.M2RNN_BF16, 0, None)
     assert st == binding.M2RNN_ERR_WORKSPACE
