@@ -108,6 +108,9 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
     const int g = lane >> 2, qd = lane & 3;
     const int w = warp;
     // W fragments for this warp's output columns: B[k][n] = W[k][NCOL w + n].
+    // With NT = 2 a warp's 16 columns of H are one k-tile, whose A fragments
+    // it holds in registers: the k-tiles are stored in the order w, w+1,
+    // w+2, w+3 (mod 4) so that the first is its own.
     const uint16_t* Wg = static_cast<const uint16_t*>(p.a.W) + static_cast<int64_t>(n) * kV * kV;
     uint32_t bw[NT][4][2];
 #pragma unroll
@@ -115,7 +118,7 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
       const int col = NCOL * w + 8 * nt + g;
 #pragma unroll
       for (int kt = 0; kt < 4; ++kt) {
-        const int k0 = 16 * kt + 2 * qd;
+        const int k0 = 16 * (NT == 2 ? ((w + kt) & 3) : kt) + 2 * qd;
         bw[nt][kt][0] = static_cast<uint32_t>(Wg[k0 * kV + col]) |
                         (static_cast<uint32_t>(Wg[(k0 + 1) * kV + col]) << 16);
         bw[nt][kt][1] = static_cast<uint32_t>(Wg[(k0 + 8) * kV + col]) |
@@ -132,6 +135,7 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
     const int64_t row_g = static_cast<int64_t>(cta_rank) * kRows + g;
     float q_prev0 = 0.f, q_prev1 = 0.f;
     uint32_t q_prev_lo = 0u, q_prev_hi = 0u;
+    uint32_t hown[4] = {0u, 0u, 0u, 0u};  // bf16 H_{t-1} of the warp's own k-tile (NT = 2), A layout
     int ck_left = p.a.ckpt_every, ck_idx = 0;  // countdown to the next checkpoint (no division per step)
     int ys_prev = 0, s_prev = 0;
     bool have_prev = false;
@@ -191,11 +195,19 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
           acc[nt][2] = k1 * v0;
           acc[nt][3] = k1 * v1;
         }
-        // H_{t-1} (bf16) as the A operand.
+        // H_{t-1} (bf16) as the A operand (NT = 2: the own k-tile from
+        // registers, issued while the other three load).
         const uint32_t atile = abuf0 + (t & 1) * 2048;
         uint32_t af[4][4];
+        if constexpr (NT == 2) {
 #pragma unroll
-        for (int kt = 0; kt < 4; ++kt) ldmatrix_x4(af[kt], ldsm_addr_a(atile, kt, lane));
+          for (int i = 1; i < 4; ++i) ldmatrix_x4(af[i], ldsm_addr_a(atile, (w + i) & 3, lane));
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[nt], hown, bw[nt][0][0], bw[nt][0][1]);
+        } else {
+#pragma unroll
+          for (int kt = 0; kt < 4; ++kt) ldmatrix_x4(af[kt], ldsm_addr_a(atile, kt, lane));
+        }
         // Readout of step t-1 on the tensor core: y^T = q^T H_{t-1} as an
         // m16n8k16 with q replicated over the 16 A rows and H_{t-1} (split
         // into bf16 hi + lo parts) as B, transposed from the accumulator
@@ -217,7 +229,7 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
           }
         }
 #pragma unroll
-        for (int kt = 0; kt < 4; ++kt)
+        for (int kt = (NT == 2 ? 1 : 0); kt < 4; ++kt)
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[nt], af[kt], bw[nt][kt][0], bw[nt][kt][1]);
         if (do_y && have_prev) {
@@ -240,8 +252,13 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
             h[nt][c] = fmaf(omf, z - h[nt][c], h[nt][c]);
           }
           const int col = jcol0 + 8 * nt;
-          st_shared_b32(otile + tile_off(g, col), pack2_bf16(h[nt][0], h[nt][1]));
-          st_shared_b32(otile + tile_off(g + 8, col), pack2_bf16(h[nt][2], h[nt][3]));
+          const uint32_t p0 = pack2_bf16(h[nt][0], h[nt][1]), p1 = pack2_bf16(h[nt][2], h[nt][3]);
+          if constexpr (NT == 2) {
+            hown[2 * nt] = p0;
+            hown[2 * nt + 1] = p1;
+          }
+          st_shared_b32(otile + tile_off(g, col), p0);
+          st_shared_b32(otile + tile_off(g + 8, col), p1);
         }
         if (p.a.ckpt != nullptr && --ck_left == 0) {  // H_{t+1} starts a chunk: checkpoint it
           ck_left = p.a.ckpt_every;
