@@ -12,14 +12,16 @@ arXiv:2603.14360v2), section 2.1 (the paper's Eq. 10-12) for the forward and
 section 2.7 (the notes' chain-rule correction of the paper's Algorithm 2) for
 the backward.
 
-Notation (per batch element b and head n, from H_0 = 0):
+Notation (per batch element b and head n, from H_0 = 0 unless an initial
+state H_0 is given; the pages' fixed-size recurrent state is what lets a long
+sequence be run in pieces, the state of one piece starting the next):
     Z_t = tanh(H_{t-1} W + k_t v_t^T)            (Eq. 10)
     H_t = f_t H_{t-1} + (1 - f_t) Z_t            (Eq. 11)
     y_t = H_t^T q_t + w_r * v_t                  (Eq. 12)
 H, Z are K x V; W is V x V and multiplies from the right, so
 (H W)_{ij} = sum_m H_{im} W_{mj}; q_t, k_t have K entries, v_t and w_r have V;
 f_t is a scalar.  Array layouts: q, k [B,T,N,K]; v [B,T,N,V]; f [B,T,N];
-W [N,V,V]; w_r [N,V]; y, dy [B,T,N,V]; H_T, dH_T [B,N,K,V].
+W [N,V,V]; w_r [N,V]; y, dy [B,T,N,V]; H_0, dH_0, H_T, dH_T [B,N,K,V].
 
 Every function is a plain loop over t, vectorised over (b, n) with numpy
 matmul/einsum; there is no blocking, fusion or reordering beyond the equations.
@@ -33,17 +35,17 @@ def _as64(x):
     return np.asarray(x, dtype=np.float64)
 
 
-def forward(q, k, v, f, W, w_r, return_states: bool = False):
-    """M2RNN forward scan (Eq. 10-12) from H_0 = 0.
+def forward(q, k, v, f, W, w_r, return_states: bool = False, H_0=None):
+    """M2RNN forward scan (Eq. 10-12) from H_0 (zero if None).
 
     Returns (y [B,T,N,V], H_T [B,N,K,V]); with ``return_states`` also the
-    stacked H_t and Z_t, shape [T+1,B,N,K,V] (index 0 holds H_0 = 0) and
+    stacked H_t and Z_t, shape [T+1,B,N,K,V] (index 0 holds H_0) and
     [T,B,N,K,V] (index t-1 holds Z_t).
     """
     q, k, v, f, W, w_r = map(_as64, (q, k, v, f, W, w_r))
     B, T, N, K = q.shape
     V = v.shape[-1]
-    H = np.zeros((B, N, K, V))
+    H = np.zeros((B, N, K, V)) if H_0 is None else _as64(H_0).copy()
     y = np.empty((B, T, N, V))
     if return_states:
         Hs = np.empty((T + 1, B, N, K, V))
@@ -68,8 +70,9 @@ def forward(q, k, v, f, W, w_r, return_states: bool = False):
     return y, H
 
 
-def backward(q, k, v, f, W, w_r, dy, dH_T=None):
-    """Gradients of L = sum(dy * y) + <dH_T, H_T> with respect to every input.
+def backward(q, k, v, f, W, w_r, dy, dH_T=None, H_0=None):
+    """Gradients of L = sum(dy * y) + <dH_T, H_T> with respect to every input
+    (and to the initial state H_0, zero if None).
 
     Follows the chain rule for Eq. 10-12 as derived in section 2.7 of the
     reading notes, with u_t the upstream gradient of the readout H_t^T q_t
@@ -86,13 +89,16 @@ def backward(q, k, v, f, W, w_r, dy, dH_T=None):
     The value-residual terms (w_r * u_t in dv, and dw_r) are the direct-path
     contributions that the notes tell the reader to restore.
 
+    The state gradient left after step 1, C_0, is dH_0 = dL/dH_0 (the same
+    recursion carried one step further back).
+
     Returns a dict with dq, dk [B,T,N,K]; dv [B,T,N,V]; df [B,T,N];
-    dW [N,V,V]; dw_r [N,V]; all float64.
+    dW [N,V,V]; dw_r [N,V]; dH_0 [B,N,K,V]; all float64.
     """
     q, k, v, f, W, w_r, dy = map(_as64, (q, k, v, f, W, w_r, dy))
     B, T, N, K = q.shape
     V = v.shape[-1]
-    _, _, Hs, Zs = forward(q, k, v, f, W, w_r, return_states=True)
+    _, _, Hs, Zs = forward(q, k, v, f, W, w_r, return_states=True, H_0=H_0)
     C = np.zeros((B, N, K, V)) if dH_T is None else _as64(dH_T).copy()
     dq = np.empty((B, T, N, K))
     dk = np.empty((B, T, N, K))
@@ -115,12 +121,12 @@ def backward(q, k, v, f, W, w_r, dy, dH_T=None):
         dW += np.einsum("bnkm,bnkj->nmj", H_prev, D)
         dw_r += np.einsum("bnv,bnv->nv", u, vt)
         C = ft * R + np.matmul(D, Wt)
-    return dict(dq=dq, dk=dk, dv=dv, df=df, dW=dW, dw_r=dw_r)
+    return dict(dq=dq, dk=dk, dv=dv, df=df, dW=dW, dw_r=dw_r, dH_0=C)
 
 
-def loss(q, k, v, f, W, w_r, dy, dH_T=None):
+def loss(q, k, v, f, W, w_r, dy, dH_T=None, H_0=None):
     """Scalar L = sum(dy * y) + <dH_T, H_T>, the function ``backward`` differentiates."""
-    y, H_T = forward(q, k, v, f, W, w_r)
+    y, H_T = forward(q, k, v, f, W, w_r, H_0=H_0)
     val = float(np.sum(_as64(dy) * y))
     if dH_T is not None:
         val += float(np.sum(_as64(dH_T) * H_T))

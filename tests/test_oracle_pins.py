@@ -216,14 +216,14 @@ def test_backward_matches_central_finite_differences(B, N, T, K, V, with_dH):
         np.testing.assert_allclose(g[name], fd[name], rtol=2e-7, atol=2e-8, err_msg=name)
 
 
-def _torch_forward(q, k, v, f, W, w_r):
+def _torch_forward(q, k, v, f, W, w_r, H_0=None):
     """An independent restatement of Eq. 10-12 in torch, written with explicit
     per-row loops over the key index so it shares no structure with the
     vectorised oracle."""
     B, T, N, K = q.shape
     ys = []
-    H = [[[torch.zeros(v.shape[-1], dtype=torch.float64) for _ in range(K)]
-          for _ in range(N)] for _ in range(B)]
+    H = [[[torch.zeros(v.shape[-1], dtype=torch.float64) if H_0 is None else H_0[b, n, i]
+           for i in range(K)] for n in range(N)] for b in range(B)]
     for t in range(T):
         yt_b = []
         for b in range(B):
@@ -352,3 +352,115 @@ def test_planted_mistakes_fail_a_pin(mode):
     least one forward pin, while the oracle itself passes them all."""
     assert _pins_pass(forward)
     assert not _pins_pass(_mutant_forward(mode))
+
+
+# --------------------------------------------------------------------------
+# Initial state H_0 and its gradient (running a sequence in pieces)
+# --------------------------------------------------------------------------
+
+def test_forward_pieces_compose_exactly():
+    """The state is the whole memory: the forward over [0, T) equals the
+    forward over [0, T1) followed by the forward over [T1, T) started from
+    the first piece's final state (the same float64 operations in the same
+    order, so bit for bit)."""
+    args = _rand(B=2, N=2, T=11, K=4, V=3, seed=51)
+    y, H_T = forward(*args)
+    for T1 in (1, 4, 10):
+        a1 = [a[:, :T1] if a.ndim >= 3 else a for a in args[:4]] + list(args[4:])
+        a2 = [a[:, T1:] if a.ndim >= 3 else a for a in args[:4]] + list(args[4:])
+        y1, H1 = forward(*a1)
+        y2, H2 = forward(*a2, H_0=H1)
+        np.testing.assert_array_equal(np.concatenate([y1, y2], axis=1), y)
+        np.testing.assert_array_equal(H2, H_T)
+
+
+def test_backward_pieces_compose():
+    """Backward in two pieces: the later piece (started from H_{T1}, with the
+    upstream dH_T) returns dH_0, which is the upstream state gradient of the
+    earlier piece; per-step gradients concatenate and dW, dw_r add up to the
+    single-pass result."""
+    args = _rand(B=2, N=2, T=9, K=3, V=4, seed=52)
+    rng = np.random.default_rng(8)
+    dy = rng.standard_normal((2, 9, 2, 4))
+    dH_T = rng.standard_normal((2, 2, 3, 4))
+    H_0 = 0.5 * rng.standard_normal((2, 2, 3, 4))
+    g = backward(*args, dy, dH_T, H_0=H_0)
+    T1 = 4
+    a1 = [a[:, :T1] if a.ndim >= 3 else a for a in args[:4]] + list(args[4:])
+    a2 = [a[:, T1:] if a.ndim >= 3 else a for a in args[:4]] + list(args[4:])
+    _, H1 = forward(*a1, H_0=H_0)
+    g2 = backward(*a2, dy[:, T1:], dH_T, H_0=H1)
+    g1 = backward(*a1, dy[:, :T1], g2["dH_0"], H_0=H_0)
+    for name in ("dq", "dk", "dv", "df"):
+        np.testing.assert_allclose(np.concatenate([g1[name], g2[name]], axis=1), g[name], rtol=1e-12, atol=1e-13)
+    for name in ("dW", "dw_r"):
+        np.testing.assert_allclose(g1[name] + g2[name], g[name], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(g1["dH_0"], g["dH_0"], rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("B,N,T,K,V", [(1, 1, 1, 2, 3), (1, 1, 4, 3, 2), (2, 2, 3, 2, 3)])
+def test_initial_state_gradient_matches_finite_differences(B, N, T, K, V):
+    """Brute force on H_0: central differences of L over every element of H_0,
+    and the other inputs' gradients stay right with a non-zero H_0."""
+    args = list(_rand(B, N, T, K, V, seed=200 + T + K))
+    rng = np.random.default_rng(11)
+    dy = rng.standard_normal((B, T, N, V))
+    dH_T = rng.standard_normal((B, N, K, V))
+    H_0 = rng.standard_normal((B, N, K, V))
+    g = backward(*args, dy, dH_T, H_0=H_0)
+    eps = 1e-6
+    fd = np.zeros_like(H_0)
+    it = np.nditer(H_0, flags=["multi_index"])
+    for _ in it:
+        mi = it.multi_index
+        hp, hm = H_0.copy(), H_0.copy()
+        hp[mi] += eps
+        hm[mi] -= eps
+        fd[mi] = (loss(*args, dy, dH_T, H_0=hp) - loss(*args, dy, dH_T, H_0=hm)) / (2 * eps)
+    np.testing.assert_allclose(g["dH_0"], fd, rtol=2e-7, atol=2e-8)
+    x = args[4]  # W, whose gradient runs through H_{t-1} and so sees H_0
+    fdw = np.zeros_like(x)
+    it = np.nditer(x, flags=["multi_index"])
+    for _ in it:
+        mi = it.multi_index
+        xp = [a.copy() for a in args]
+        xm = [a.copy() for a in args]
+        xp[4][mi] += eps
+        xm[4][mi] -= eps
+        fdw[mi] = (loss(*xp, dy, dH_T, H_0=H_0) - loss(*xm, dy, dH_T, H_0=H_0)) / (2 * eps)
+    np.testing.assert_allclose(g["dW"], fdw, rtol=2e-7, atol=2e-8)
+
+
+def test_initial_state_forget_one_closed_form():
+    """f = 1 from a non-zero H_0: the state never moves (H_t = H_0), so
+    y_t = H_0^T q_t + w_r v_t; D = 0, C_{t-1} = R_t, hence
+    dH_0 = dH_T + sum_t q_t u_t^T, dq_t = H_0 u_t, dW = 0."""
+    q, k, v, f, W, w_r = _rand(B=2, N=2, T=5, K=3, V=4, seed=53)
+    f = np.ones_like(f)
+    rng = np.random.default_rng(12)
+    H_0 = rng.standard_normal((2, 2, 3, 4))
+    dy = rng.standard_normal(v.shape)
+    dH_T = rng.standard_normal((2, 2, 3, 4))
+    y, H_T = forward(q, k, v, f, W, w_r, H_0=H_0)
+    np.testing.assert_array_equal(H_T, H_0)
+    np.testing.assert_allclose(y, np.einsum("bnkv,btnk->btnv", H_0, q) + w_r[None, None] * v, rtol=1e-13)
+    g = backward(q, k, v, f, W, w_r, dy, dH_T, H_0=H_0)
+    np.testing.assert_allclose(g["dH_0"], dH_T + np.einsum("btnk,btnv->bnkv", q, dy), rtol=1e-13)
+    np.testing.assert_allclose(g["dq"], np.einsum("bnkv,btnv->btnk", H_0, dy), rtol=1e-13)
+    assert np.all(g["dW"] == 0)
+
+
+def test_initial_state_gradient_matches_torch_autograd():
+    """torch.autograd through the independently written forward, H_0 a leaf."""
+    args = _rand(B=1, N=2, T=5, K=3, V=4, seed=54)
+    rng = np.random.default_rng(13)
+    H_0 = rng.standard_normal((1, 2, 3, 4))
+    dy = rng.standard_normal((1, 5, 2, 4))
+    dH_T = rng.standard_normal((1, 2, 3, 4))
+    ts = [torch.tensor(a) for a in args]
+    h0 = torch.tensor(H_0, requires_grad=True)
+    y, H_T = _torch_forward(*ts, H_0=h0)
+    L = (y * torch.from_numpy(dy)).sum() + (H_T * torch.from_numpy(dH_T)).sum()
+    L.backward()
+    g = backward(*args, dy, dH_T, H_0=H_0)
+    np.testing.assert_allclose(g["dH_0"], h0.grad.numpy(), rtol=1e-10, atol=1e-12)
