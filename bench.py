@@ -408,8 +408,9 @@ def run_gpu(args, dist):
                 os.environ.pop("M2RNN_KERNEL", None)
             else:
                 os.environ["M2RNN_KERNEL"] = prev
+        fwd_extra["decode_bf16_k64"] = time_decode(binding, dev, stream, dist)
     cpu = cpu_baseline_sample() if (dist.rank == 0 and not args.no_cpu) else None
-    launches_per_step = 3  # forward scan, backward scan, partial-sum reduction
+    launches_per_step = 4  # forward scan, backward scan, dv/df row sums, dW/dw_r partial sums
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": step_ms, "higher_is_better": True,
@@ -468,6 +469,38 @@ def time_forward(name, binding, dev, stream, flush, pk, dist, reps=5):
             "bound": "tensor" if t_tensor >= t_hbm else "hbm",
             "tensor_tflops": fl / (t * 1e-3) / 1e12,
             "peak_source": f"{pk['source']} bf16 burst / hbm copy"}
+
+
+def time_decode(binding, dev, stream, dist, steps=64):
+    """One-token decoding (m2rnn_decode_step): the B x heads states of the
+    forward+backward workload advanced one step per call, `steps` calls in a
+    row, the state updated in place."""
+    import torch
+    w = WORKLOADS[MAIN]
+    inp = make_workload(MAIN)
+    d = binding.to_device(inp, dev)
+    B, N, K, V = w["B"], w["N"], w["K"], w["V"]
+    toks = [[d[n][:, t].contiguous() for n in ("q", "k", "v", "f")] for t in range(steps)]
+    H = torch.zeros((B, N, K, V), device=dev, dtype=torch.float32)
+    y = torch.empty((B, N, V), device=dev, dtype=torch.float32)
+    ws = torch.empty(binding.m2rnn_forward_workspace_size(B, 1, N, K, V, binding.M2RNN_BF16),
+                     device=dev, dtype=torch.uint8)
+    for t in range(8):
+        binding.decode_step(H, *toks[t], d["W"], d["w_r"], y=y, workspace=ws)
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for t in range(steps):
+        binding.decode_step(H, *toks[t], d["W"], d["w_r"], y=y, workspace=ws)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    st, detail = binding.sync_status(ws)
+    if st != binding.M2RNN_OK:
+        raise RuntimeError(f"decode: device status {binding.status_string(st)} at {detail}")
+    us = dist.max(a.elapsed_time(b) * 1e3 / steps)
+    return {"workload": f"bf16 decode, {B}x{N} states of {K}x{V}, one token per call, {steps} calls",
+            "kernel": "warp-mma (T = 1)", "us_per_step": us,
+            "value": dist.world * B * N / (us * 1e-6), "unit": UNIT, "launches_per_step": 1}
 
 
 def run_only(args, dist):

@@ -130,6 +130,54 @@ int m2rnn_backward(const void* q, const void* k, const void* v, const void* f,
                    size_t workspace_bytes, void* cuda_stream);
 
 /*
+ * Forward scan from a given initial state: as m2rnn_forward, with
+ *   H_0 [B,N,K,V] fp32 (may be NULL = zero): the state before step 1.
+ * With H_T set to the final state of one call, the next call over the
+ * following steps continues the same sequence (the fixed-size recurrent
+ * state of the reading notes, section 2.6): a sequence can run in pieces.
+ * H_0 may equal H_T (each state element is read before it is overwritten).
+ */
+int m2rnn_forward_state(const void* q, const void* k, const void* v,
+                        const void* f, const void* W, const void* w_r,
+                        const float* H_0, float* y, float* H_T, float* ckpt,
+                        int ckpt_every, int64_t B, int64_t T, int64_t N,
+                        int64_t K, int64_t V, m2rnn_dtype dtype,
+                        void* workspace, size_t workspace_bytes,
+                        void* cuda_stream);
+
+/*
+ * Backward through time from a given initial state: as m2rnn_backward, with
+ *   H_0  [B,N,K,V] fp32 (may be NULL = zero): the forward's initial state;
+ *   dH_0 [B,N,K,V] fp32 (may be NULL): receives dL/dH_0, the state gradient
+ *        carried one step past t = 1 (C_0 in the recursion above).
+ * When a sequence runs in pieces, dH_0 of a later piece is the dH_T of the
+ * piece before it.  `ckpt`, if given, must come from m2rnn_forward_state
+ * with the same H_0.
+ */
+int m2rnn_backward_state(const void* q, const void* k, const void* v,
+                         const void* f, const void* W, const void* w_r,
+                         const float* H_0, const float* dy, const float* dH_T,
+                         const float* ckpt, int ckpt_every, float* dq,
+                         float* dk, float* dv, float* df, float* dW,
+                         float* dw_r, float* dH_0, int64_t B, int64_t T,
+                         int64_t N, int64_t K, int64_t V, m2rnn_dtype dtype,
+                         void* workspace, size_t workspace_bytes,
+                         void* cuda_stream);
+
+/*
+ * One decoding step for a batch of states (serving: one new token per
+ * (b, head)): H [B,N,K,V] fp32 is updated in place to H_t from H_{t-1}, and
+ * y [B,N,V] fp32 receives y_t.  q, k [B,N,K]; v [B,N,V]; f [B,N]; W, w_r as
+ * above.  Same kernels as m2rnn_forward_state with T = 1; the workspace is
+ * m2rnn_forward_workspace_size(B, 1, N, K, V, dtype) bytes.
+ */
+int m2rnn_decode_step(float* H, const void* q, const void* k, const void* v,
+                      const void* f, const void* W, const void* w_r, float* y,
+                      int64_t B, int64_t N, int64_t K, int64_t V,
+                      m2rnn_dtype dtype, void* workspace,
+                      size_t workspace_bytes, void* cuda_stream);
+
+/*
  * Synchronises `cuda_stream`, then reads and clears the workspace status
  * block that the last call on this workspace wrote.  Returns M2RNN_OK,
  * M2RNN_ERR_TIMEOUT or M2RNN_ERR_DEVICE; `detail` (may be NULL) receives an

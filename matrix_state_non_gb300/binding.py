@@ -29,7 +29,8 @@ M2RNN_BF16 = 1
 EXPORTS = (
     "m2rnn_version", "m2rnn_status_string", "m2rnn_checkpoint_count", "m2rnn_path",
     "m2rnn_forward_workspace_size", "m2rnn_backward_workspace_size", "m2rnn_forward",
-    "m2rnn_backward", "m2rnn_sync_status",
+    "m2rnn_backward", "m2rnn_sync_status", "m2rnn_forward_state", "m2rnn_backward_state",
+    "m2rnn_decode_step",
 )
 
 _lib = None
@@ -70,6 +71,12 @@ def load() -> ctypes.CDLL:
     lib.m2rnn_backward.argtypes = [vp] * 9 + [ci] + [vp] * 6 + [i64] * 5 + [ci, vp, sz, vp]
     lib.m2rnn_sync_status.restype = ci
     lib.m2rnn_sync_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.m2rnn_forward_state.restype = ci
+    lib.m2rnn_forward_state.argtypes = [vp] * 10 + [ci] + [i64] * 5 + [ci, vp, sz, vp]
+    lib.m2rnn_backward_state.restype = ci
+    lib.m2rnn_backward_state.argtypes = [vp] * 10 + [ci] + [vp] * 7 + [i64] * 5 + [ci, vp, sz, vp]
+    lib.m2rnn_decode_step.restype = ci
+    lib.m2rnn_decode_step.argtypes = [vp] * 8 + [i64] * 4 + [ci, vp, sz, vp]
     _lib = lib
     return lib
 
@@ -117,6 +124,25 @@ def m2rnn_backward(q, k, v, f, W, w_r, dy, dH_T, ckpt, ckpt_every, dq, dk, dv, d
                                  workspace_bytes, stream)
 
 
+def m2rnn_forward_state(q, k, v, f, W, w_r, H_0, y, H_T, ckpt, ckpt_every, B, T, N, K, V, dtype,
+                        workspace, workspace_bytes, stream) -> int:
+    return load().m2rnn_forward_state(q, k, v, f, W, w_r, H_0, y, H_T, ckpt, ckpt_every, B, T, N, K,
+                                      V, dtype, workspace, workspace_bytes, stream)
+
+
+def m2rnn_backward_state(q, k, v, f, W, w_r, H_0, dy, dH_T, ckpt, ckpt_every, dq, dk, dv, df, dW,
+                         dw_r, dH_0, B, T, N, K, V, dtype, workspace, workspace_bytes, stream) -> int:
+    return load().m2rnn_backward_state(q, k, v, f, W, w_r, H_0, dy, dH_T, ckpt, ckpt_every, dq, dk,
+                                       dv, df, dW, dw_r, dH_0, B, T, N, K, V, dtype, workspace,
+                                       workspace_bytes, stream)
+
+
+def m2rnn_decode_step(H, q, k, v, f, W, w_r, y, B, N, K, V, dtype, workspace, workspace_bytes,
+                      stream) -> int:
+    return load().m2rnn_decode_step(H, q, k, v, f, W, w_r, y, B, N, K, V, dtype, workspace,
+                                    workspace_bytes, stream)
+
+
 def m2rnn_sync_status(workspace, stream):
     """Returns (status, detail)."""
     d = ctypes.c_uint32(0)
@@ -157,9 +183,10 @@ def _shapes(q, v):
     return B, T, N, K, V
 
 
-def forward(q, k, v, f, W, w_r, *, want_state: bool = True, ckpt_every: int = 0,
+def forward(q, k, v, f, W, w_r, *, H_0=None, want_state: bool = True, ckpt_every: int = 0,
             out=None, workspace=None, stream=None):
-    """Forward scan on the GPU.  Returns dict(y, H_T[, ckpt]).
+    """Forward scan on the GPU from ``H_0`` (fp32 [B,N,K,V]; None = zero).
+    Returns dict(y, H_T[, ckpt]).
 
     ``ckpt_every`` > 0 also writes the checkpoints the backward can reuse.
     ``out`` may hold preallocated y / H_T / ckpt tensors.
@@ -184,20 +211,23 @@ def forward(q, k, v, f, W, w_r, *, want_state: bool = True, ckpt_every: int = 0,
         raise M2RNNError(M2RNN_ERR_INVALID_ARG, "m2rnn_forward_workspace_size")
     if workspace is None:
         workspace = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
-    st = m2rnn_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(f), _ptr(W), _ptr(w_r), _ptr(y),
-                       _ptr(H_T), _ptr(ckpt), ckpt_every if ckpt is not None else 0,
-                       B, T, N, K, V, dt, _ptr(workspace), workspace.numel(),
-                       _stream_handle(stream))
-    _check(st, "m2rnn_forward")
+    st = m2rnn_forward_state(_ptr(q), _ptr(k), _ptr(v), _ptr(f), _ptr(W), _ptr(w_r), _ptr(H_0),
+                             _ptr(y), _ptr(H_T), _ptr(ckpt), ckpt_every if ckpt is not None else 0,
+                             B, T, N, K, V, dt, _ptr(workspace), workspace.numel(),
+                             _stream_handle(stream))
+    _check(st, "m2rnn_forward_state")
     res = dict(y=y, H_T=H_T, workspace=workspace)
     if ckpt is not None:
         res["ckpt"] = ckpt
     return res
 
 
-def backward(q, k, v, f, W, w_r, dy, *, dH_T=None, ckpt=None, ckpt_every: int = 64,
-             out=None, workspace=None, stream=None):
-    """Backward scan on the GPU.  Returns dict(dq, dk, dv, df, dW, dw_r)."""
+def backward(q, k, v, f, W, w_r, dy, *, dH_T=None, H_0=None, want_dH0: bool = False, ckpt=None,
+             ckpt_every: int = 14, out=None, workspace=None, stream=None):
+    """Backward scan on the GPU.  Returns dict(dq, dk, dv, df, dW, dw_r[, dH_0]).
+
+    ``H_0`` is the forward's initial state (None = zero); ``ckpt``, if given,
+    must come from a forward with the same ``H_0``."""
     import torch
     B, T, N, K, V = _shapes(q, v)
     dt = _dtype_code(q)
@@ -214,17 +244,41 @@ def backward(q, k, v, f, W, w_r, dy, *, dH_T=None, ckpt=None, ckpt_every: int = 
     df = _get("df", (B, T, N))
     dW = _get("dW", (N, V, V))
     dw_r = _get("dw_r", (N, V))
+    dH_0 = _get("dH_0", (B, N, K, V)) if want_dH0 else None
     ws_bytes = m2rnn_backward_workspace_size(B, T, N, K, V, dt, ckpt_every, ckpt is not None)
     if ws_bytes == 0:
         raise M2RNNError(M2RNN_ERR_INVALID_ARG, "m2rnn_backward_workspace_size")
     if workspace is None or workspace.numel() < ws_bytes:
         workspace = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
-    st = m2rnn_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(f), _ptr(W), _ptr(w_r), _ptr(dy),
-                        _ptr(dH_T), _ptr(ckpt), ckpt_every, _ptr(dq), _ptr(dk), _ptr(dv),
-                        _ptr(df), _ptr(dW), _ptr(dw_r), B, T, N, K, V, dt, _ptr(workspace),
-                        workspace.numel(), _stream_handle(stream))
-    _check(st, "m2rnn_backward")
-    return dict(dq=dq, dk=dk, dv=dv, df=df, dW=dW, dw_r=dw_r, workspace=workspace)
+    st = m2rnn_backward_state(_ptr(q), _ptr(k), _ptr(v), _ptr(f), _ptr(W), _ptr(w_r), _ptr(H_0),
+                              _ptr(dy), _ptr(dH_T), _ptr(ckpt), ckpt_every, _ptr(dq), _ptr(dk),
+                              _ptr(dv), _ptr(df), _ptr(dW), _ptr(dw_r), _ptr(dH_0), B, T, N, K, V,
+                              dt, _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    _check(st, "m2rnn_backward_state")
+    res = dict(dq=dq, dk=dk, dv=dv, df=df, dW=dW, dw_r=dw_r, workspace=workspace)
+    if dH_0 is not None:
+        res["dH_0"] = dH_0
+    return res
+
+
+def decode_step(H, q, k, v, f, W, w_r, *, y=None, workspace=None, stream=None):
+    """One decoding step on the GPU: ``H`` (fp32 [B,N,K,V], contiguous) is
+    updated in place; q, k [B,N,K], v [B,N,V], f [B,N].  Returns y [B,N,V]."""
+    import torch
+    B, N, K = q.shape
+    V = v.shape[-1]
+    dt = _dtype_code(q)
+    if y is None:
+        y = torch.empty((B, N, V), device=q.device, dtype=torch.float32)
+    ws_bytes = m2rnn_forward_workspace_size(B, 1, N, K, V, dt)
+    if ws_bytes == 0:
+        raise M2RNNError(M2RNN_ERR_INVALID_ARG, "m2rnn_forward_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, device=q.device, dtype=torch.uint8)
+    st = m2rnn_decode_step(_ptr(H), _ptr(q), _ptr(k), _ptr(v), _ptr(f), _ptr(W), _ptr(w_r), _ptr(y),
+                           B, N, K, V, dt, _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    _check(st, "m2rnn_decode_step")
+    return y
 
 
 def sync_status(workspace, stream=None):

@@ -158,17 +158,18 @@ size_t m2rnn_backward_workspace_size(int64_t B, int64_t T, int64_t N, int64_t K,
   return bwd_layout(B, T, N, K, V, dtype, ckpt_every, have_ckpt != 0).total;
 }
 
-int m2rnn_forward(const void* q, const void* k, const void* v, const void* f, const void* W,
-                  const void* w_r, float* y, float* H_T, float* ckpt, int ckpt_every, int64_t B,
-                  int64_t T, int64_t N, int64_t K, int64_t V, m2rnn_dtype dtype, void* workspace,
-                  size_t workspace_bytes, void* cuda_stream) {
+int m2rnn_forward_state(const void* q, const void* k, const void* v, const void* f, const void* W,
+                        const void* w_r, const float* H_0, float* y, float* H_T, float* ckpt,
+                        int ckpt_every, int64_t B, int64_t T, int64_t N, int64_t K, int64_t V,
+                        m2rnn_dtype dtype, void* workspace, size_t workspace_bytes, void* cuda_stream) {
   if (!dtype_ok(dtype) || !dims_ok(B, T, N, K, V)) return M2RNN_ERR_INVALID_ARG;
   const int path = choose_path(K, V, dtype);
   if (path < 0) return path;
   const void* req[] = {q, k, v, f, W, w_r, y};
   for (const void* p : req)
     if (p == nullptr || !aligned16(p)) return M2RNN_ERR_INVALID_ARG;
-  if ((H_T && !aligned16(H_T)) || (ckpt && !aligned16(ckpt))) return M2RNN_ERR_INVALID_ARG;
+  if ((H_T && !aligned16(H_T)) || (ckpt && !aligned16(ckpt)) || (H_0 && !aligned16(H_0)))
+    return M2RNN_ERR_INVALID_ARG;
   if (ckpt && (ckpt_every < 1 || ckpt_every > kMaxCkptEvery)) return M2RNN_ERR_INVALID_ARG;
   if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < kStatusBytes)
     return M2RNN_ERR_WORKSPACE;
@@ -178,7 +179,7 @@ int m2rnn_forward(const void* q, const void* k, const void* v, const void* f, co
   if (e != cudaSuccess) return M2RNN_ERR_CUDA;
   FwdArgs a{};
   a.q = q; a.k = k; a.v = v; a.f = f; a.W = W; a.w_r = w_r;
-  a.y = y; a.H_T = H_T; a.ckpt = ckpt;
+  a.H0 = H_0; a.y = y; a.H_T = H_T; a.ckpt = ckpt;
   a.ckpt_every = ckpt ? ckpt_every : 1;
   a.n_ckpt = ckpt ? (T - 1) / ckpt_every : 0;
   a.B = static_cast<int>(B); a.T = static_cast<int>(T); a.N = static_cast<int>(N);
@@ -189,11 +190,31 @@ int m2rnn_forward(const void* q, const void* k, const void* v, const void* f, co
   return cuda_status(e);
 }
 
-int m2rnn_backward(const void* q, const void* k, const void* v, const void* f, const void* W,
-                   const void* w_r, const float* dy, const float* dH_T, const float* ckpt,
-                   int ckpt_every, float* dq, float* dk, float* dv, float* df, float* dW,
-                   float* dw_r, int64_t B, int64_t T, int64_t N, int64_t K, int64_t V,
-                   m2rnn_dtype dtype, void* workspace, size_t workspace_bytes, void* cuda_stream) {
+int m2rnn_forward(const void* q, const void* k, const void* v, const void* f, const void* W,
+                  const void* w_r, float* y, float* H_T, float* ckpt, int ckpt_every, int64_t B,
+                  int64_t T, int64_t N, int64_t K, int64_t V, m2rnn_dtype dtype, void* workspace,
+                  size_t workspace_bytes, void* cuda_stream) {
+  return m2rnn_forward_state(q, k, v, f, W, w_r, nullptr, y, H_T, ckpt, ckpt_every, B, T, N, K, V,
+                             dtype, workspace, workspace_bytes, cuda_stream);
+}
+
+int m2rnn_decode_step(float* H, const void* q, const void* k, const void* v, const void* f,
+                      const void* W, const void* w_r, float* y, int64_t B, int64_t N, int64_t K,
+                      int64_t V, m2rnn_dtype dtype, void* workspace, size_t workspace_bytes,
+                      void* cuda_stream) {
+  if (H == nullptr) return M2RNN_ERR_INVALID_ARG;
+  // One step from H to H: every kernel reads a state element before the same
+  // thread block overwrites it.
+  return m2rnn_forward_state(q, k, v, f, W, w_r, H, y, H, nullptr, 0, B, 1, N, K, V, dtype,
+                             workspace, workspace_bytes, cuda_stream);
+}
+
+int m2rnn_backward_state(const void* q, const void* k, const void* v, const void* f,
+                         const void* W, const void* w_r, const float* H_0, const float* dy,
+                         const float* dH_T, const float* ckpt, int ckpt_every, float* dq,
+                         float* dk, float* dv, float* df, float* dW, float* dw_r, float* dH_0,
+                         int64_t B, int64_t T, int64_t N, int64_t K, int64_t V, m2rnn_dtype dtype,
+                         void* workspace, size_t workspace_bytes, void* cuda_stream) {
   if (!dtype_ok(dtype) || !dims_ok(B, T, N, K, V)) return M2RNN_ERR_INVALID_ARG;
   const int path = choose_path(K, V, dtype);
   if (path < 0) return path;
@@ -202,7 +223,9 @@ int m2rnn_backward(const void* q, const void* k, const void* v, const void* f, c
   const void* req[] = {q, k, v, f, W, w_r, dy, dq, dk, dv, df, dW, dw_r};
   for (const void* p : req)
     if (p == nullptr || !aligned16(p)) return M2RNN_ERR_INVALID_ARG;
-  if ((dH_T && !aligned16(dH_T)) || (ckpt && !aligned16(ckpt))) return M2RNN_ERR_INVALID_ARG;
+  if ((dH_T && !aligned16(dH_T)) || (ckpt && !aligned16(ckpt)) || (H_0 && !aligned16(H_0)) ||
+      (dH_0 && !aligned16(dH_0)))
+    return M2RNN_ERR_INVALID_ARG;
   const BwdLayout l = bwd_layout(B, T, N, K, V, dtype, ckpt_every, ckpt != nullptr);
   if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < l.total)
     return M2RNN_ERR_WORKSPACE;
@@ -219,7 +242,7 @@ int m2rnn_backward(const void* q, const void* k, const void* v, const void* f, c
       // Checkpoint pass: the forward without the readout.
       FwdArgs fa{};
       fa.q = q; fa.k = k; fa.v = v; fa.f = f; fa.W = W; fa.w_r = w_r;
-      fa.y = nullptr; fa.H_T = nullptr; fa.ckpt = ck;
+      fa.H0 = H_0; fa.y = nullptr; fa.H_T = nullptr; fa.ckpt = ck;
       fa.ckpt_every = ckpt_every; fa.n_ckpt = nck;
       fa.B = static_cast<int>(B); fa.T = static_cast<int>(T); fa.N = static_cast<int>(N);
       fa.K = static_cast<int>(K); fa.V = static_cast<int>(V);
@@ -230,8 +253,8 @@ int m2rnn_backward(const void* q, const void* k, const void* v, const void* f, c
   }
   BwdArgs a{};
   a.q = q; a.k = k; a.v = v; a.f = f; a.W = W; a.w_r = w_r;
-  a.dy = dy; a.dH_T = dH_T; a.ckpt = ck; a.ckpt_every = ckpt_every; a.n_ckpt = nck;
-  a.dq = dq; a.dk = dk; a.dv = dv; a.df = df; a.dW = dW; a.dw_r = dw_r;
+  a.dy = dy; a.dH_T = dH_T; a.H0 = H_0; a.ckpt = ck; a.ckpt_every = ckpt_every; a.n_ckpt = nck;
+  a.dq = dq; a.dk = dk; a.dv = dv; a.df = df; a.dW = dW; a.dw_r = dw_r; a.dH0 = dH_0;
   a.B = static_cast<int>(B); a.T = static_cast<int>(T); a.N = static_cast<int>(N);
   a.K = static_cast<int>(K); a.V = static_cast<int>(V);
   a.dtype = dtype; a.status = status;
@@ -247,6 +270,16 @@ int m2rnn_backward(const void* q, const void* k, const void* v, const void* f, c
     e = launch_simt_backward(a, s);
   if (e != cudaSuccess) return M2RNN_ERR_CUDA;
   return cuda_status(launch_reduce_partials(a, s));
+}
+
+int m2rnn_backward(const void* q, const void* k, const void* v, const void* f, const void* W,
+                   const void* w_r, const float* dy, const float* dH_T, const float* ckpt,
+                   int ckpt_every, float* dq, float* dk, float* dv, float* df, float* dW,
+                   float* dw_r, int64_t B, int64_t T, int64_t N, int64_t K, int64_t V,
+                   m2rnn_dtype dtype, void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  return m2rnn_backward_state(q, k, v, f, W, w_r, nullptr, dy, dH_T, ckpt, ckpt_every, dq, dk, dv,
+                              df, dW, dw_r, nullptr, B, T, N, K, V, dtype, workspace,
+                              workspace_bytes, cuda_stream);
 }
 
 int m2rnn_sync_status(void* workspace, void* cuda_stream, uint32_t* detail) {

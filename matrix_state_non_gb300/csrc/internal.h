@@ -18,6 +18,7 @@ struct FwdArgs {
   const void* f;
   const void* W;
   const void* w_r;
+  const float* H0;  // initial state [B,N,K,V] fp32; null = zero
   float* y;      // may be null (checkpoint-only pass)
   float* H_T;    // may be null
   float* ckpt;   // may be null
@@ -37,6 +38,8 @@ struct BwdArgs {
   const void* w_r;
   const float* dy;
   const float* dH_T;  // may be null
+  const float* H0;    // initial state; null = zero
+  float* dH0;         // gradient of the initial state; may be null
   const float* ckpt;  // never null here (recomputed by the caller layer if needed)
   int ckpt_every;
   int64_t n_ckpt;

@@ -351,6 +351,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&tfree[tb]));
     }
+    if (ok && A.dH0 != nullptr) {  // C_0, the state gradient left after step 1
+      float* dst = A.dH0 + (static_cast<int64_t>(chain) * A.K + row_g) * kV + jcol0;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        *reinterpret_cast<float2*>(dst + 8 * nt) = make_float2(Cg[nt][0], Cg[nt][1]);
+        *reinterpret_cast<float2*>(dst + 8 * kV + 8 * nt) = make_float2(Cg[nt][2], Cg[nt][3]);
+      }
+    }
     if (!ok) *abort_flag = 1;
   } else if (warp < 8) {
     // ======================= recompute warps (Eq. 10-11) =======================
@@ -372,15 +380,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const uint32_t htile0 = smem_u32(smem + p.htile_off);
     float* dqp = reinterpret_cast<float*>(smem + p.dqp_off);  // [C][4 warps][4 qd][8 g][row g, g+8]
-    // Start state of a chunk: the checkpoint (zero for chunk 0).  The next
+    // Start state of a chunk: the checkpoint (H_0, zero if not given, for
+    // chunk 0).  The next
     // chunk's is loaded a chunk ahead, so its latency stays off the path.
     auto load_start = [&](int cc, float (&hs)[2][4]) {
-      if (cc == 0) {
+      if (cc == 0 && A.H0 == nullptr) {
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) hs[nt][0] = hs[nt][1] = hs[nt][2] = hs[nt][3] = 0.f;
       } else {
         const float* src =
-            A.ckpt + ((static_cast<int64_t>(chain) * A.n_ckpt + (cc - 1)) * A.K + row_g) * kV + jcol0;
+            (cc == 0 ? A.H0 + (static_cast<int64_t>(chain) * A.K + row_g) * kV
+                     : A.ckpt + ((static_cast<int64_t>(chain) * A.n_ckpt + (cc - 1)) * A.K + row_g) * kV) +
+            jcol0;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           const float2 x0 = *reinterpret_cast<const float2*>(src + 8 * nt);

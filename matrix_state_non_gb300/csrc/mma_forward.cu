@@ -136,6 +136,24 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
     float q_prev0 = 0.f, q_prev1 = 0.f;
     uint32_t q_prev_lo = 0u, q_prev_hi = 0u;
     uint32_t hown[4] = {0u, 0u, 0u, 0u};  // bf16 H_{t-1} of the warp's own k-tile (NT = 2), A layout
+    if (p.a.H0 != nullptr) {
+      // Start from the given state: fp32 into the registers, bf16 into the
+      // operand tile of step 0 (ordered by the first tile's barrier).
+      const float* src = p.a.H0 + (static_cast<int64_t>(chain) * p.a.K + row_g) * kV + jcol0;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const float2 x0 = *reinterpret_cast<const float2*>(src + 8 * nt);
+        const float2 x1 = *reinterpret_cast<const float2*>(src + 8 * kV + 8 * nt);
+        h[nt][0] = x0.x; h[nt][1] = x0.y; h[nt][2] = x1.x; h[nt][3] = x1.y;
+        const uint32_t p0 = pack2_bf16(h[nt][0], h[nt][1]), p1 = pack2_bf16(h[nt][2], h[nt][3]);
+        st_shared_b32(abuf0 + tile_off(g, jcol0 + 8 * nt), p0);
+        st_shared_b32(abuf0 + tile_off(g + 8, jcol0 + 8 * nt), p1);
+        if constexpr (NT == 2) {
+          hown[2 * nt] = p0;
+          hown[2 * nt + 1] = p1;
+        }
+      }
+    }
     int ck_left = p.a.ckpt_every, ck_idx = 0;  // countdown to the next checkpoint (no division per step)
     int ys_prev = 0, s_prev = 0;
     bool have_prev = false;

@@ -51,7 +51,7 @@ __global__ void __launch_bounds__(kThreads) simt_forward_kernel(FwdArgs a) {
   const Tin* w_r = static_cast<const Tin*>(a.w_r) + static_cast<int64_t>(n) * V;
 
   for (int e = threadIdx.x; e < V * V; e += kThreads) Ws[e] = ld_in(W, e);
-  for (int e = threadIdx.x; e < KV; e += kThreads) Ha[e] = 0.f;
+  for (int e = threadIdx.x; e < KV; e += kThreads) Ha[e] = a.H0 ? a.H0[static_cast<int64_t>(chain) * KV + e] : 0.f;
   __syncthreads();
   float* Hc = Ha;
   float* Hn = Hb;
@@ -153,8 +153,8 @@ __global__ void __launch_bounds__(kThreads) simt_backward_kernel(BwdArgs a) {
     const int s0 = c * CL;
     const int L = min(CL, T - s0);
     // ---- recompute the chunk's states ----
-    const float* Hstart =
-        (c == 0) ? nullptr : a.ckpt + (static_cast<int64_t>(chain) * a.n_ckpt + (c - 1)) * KV;
+    const float* Hstart = (c == 0) ? (a.H0 ? a.H0 + static_cast<int64_t>(chain) * KV : nullptr)
+                                   : a.ckpt + (static_cast<int64_t>(chain) * a.n_ckpt + (c - 1)) * KV;
     for (int e = threadIdx.x; e < KV; e += kThreads) {
       const float h = Hstart ? Hstart[e] : 0.f;
       Dm[e] = h;
@@ -240,6 +240,8 @@ __global__ void __launch_bounds__(kThreads) simt_backward_kernel(BwdArgs a) {
       __syncthreads();
     }
   }
+  if (a.dH0 != nullptr)  // C_0, the state gradient left after step 1
+    for (int e = threadIdx.x; e < KV; e += kThreads) a.dH0[static_cast<int64_t>(chain) * KV + e] = Cm[e];
 }
 
 // dW[n] = sum_b sum_p part[b][n][p], dw_r[n] = sum_b wpart[b][n], fixed order.

@@ -139,10 +139,28 @@ __global__ void __launch_bounds__(352, 1)
     tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
     tmem_relinquish();
   }
-  {
+  if (p.a.H0 == nullptr) {
     const uint4 zero = make_uint4(0, 0, 0, 0);
     for (uint32_t e = threadIdx.x * 16; e < static_cast<uint32_t>(G) * C::B_BYTES; e += blockDim.x * 16)
       *reinterpret_cast<uint4*>(sB + e) = zero;  // H_0 = 0
+  } else if (warp < 4 * G) {
+    // bf16(H_0) as step 0's B operand: each epilogue thread writes the rows
+    // and column it owns (the same mapping as below; together they cover
+    // every element of each group's tile).
+    const int g = warp / 4, L = 32 * (warp % 4) + lane;
+    const int j = L % V, c = L / V;
+    const int64_t row_global = static_cast<int64_t>(cta_rank) * NRtot + g * C::NR + c * ROWS;
+    const float* src = p.a.H0 + (static_cast<int64_t>(chain) * p.a.K + row_global) * V + j;
+    uint8_t* bslot = sB + g * C::B_BYTES + ((c * ROWS) / 8) * C::SBO + (j / 8) * C::LBO + (j % 8) * 16;
+#pragma unroll
+    for (int r0 = 0; r0 < ROWS; r0 += 8) {
+      uint4 pk;
+      pk.x = pack_bf16x2(src[(r0 + 0) * V], src[(r0 + 1) * V]);
+      pk.y = pack_bf16x2(src[(r0 + 2) * V], src[(r0 + 3) * V]);
+      pk.z = pack_bf16x2(src[(r0 + 4) * V], src[(r0 + 5) * V]);
+      pk.w = pack_bf16x2(src[(r0 + 6) * V], src[(r0 + 7) * V]);
+      *reinterpret_cast<uint4*>(bslot + (r0 / 8) * C::SBO) = pk;
+    }
   }
   fence_proxy_async_smem();
   tc_fence_before_sync();
@@ -186,7 +204,8 @@ __global__ void __launch_bounds__(352, 1)
     uint8_t* bslot = sB + g * C::B_BYTES + ((c * ROWS) / 8) * C::SBO + (j / 8) * C::LBO + (j % 8) * 16;
     float h[ROWS];
 #pragma unroll
-    for (int r = 0; r < ROWS; ++r) h[r] = 0.f;
+    for (int r = 0; r < ROWS; ++r)
+      h[r] = p.a.H0 ? p.a.H0[(static_cast<int64_t>(chain) * p.a.K + row_global + r) * V + j] : 0.f;
     uint32_t dphase = 0;
     bool ok = true;
     for (int tile = 0; tile < ntiles && ok; ++tile) {

@@ -26,11 +26,16 @@ def max_abs(x, ref):
     return float(np.max(np.abs(np.asarray(x, np.float64) - np.asarray(ref, np.float64)))) if np.size(ref) else 0.0
 
 
-def gpu_forward(inp, ckpt_every=0):
+def _cuda_f32(x):
+    import torch
+    return None if x is None else torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).cuda()
+
+
+def gpu_forward(inp, ckpt_every=0, H_0=None):
     import torch
     from matrix_state_non_gb300 import binding
     d = binding.to_device(inp)
-    out = binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=ckpt_every)
+    out = binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=ckpt_every, H_0=_cuda_f32(H_0))
     st, detail = binding.sync_status(out["workspace"])
     assert st == binding.M2RNN_OK, (binding.status_string(st), detail)
     torch.cuda.synchronize()
@@ -40,20 +45,21 @@ def gpu_forward(inp, ckpt_every=0):
     return res
 
 
-def gpu_backward(inp, dH_T=None, ckpt_every=16, use_fwd_ckpt=False):
+def gpu_backward(inp, dH_T=None, ckpt_every=16, use_fwd_ckpt=False, H_0=None, want_dH0=False):
     import torch
     from matrix_state_non_gb300 import binding
     d = binding.to_device(inp)
+    h0 = _cuda_f32(H_0)
     ckpt = None
     if use_fwd_ckpt:
-        ckpt = binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=ckpt_every)["ckpt"]
-    dH = None if dH_T is None else torch.from_numpy(np.ascontiguousarray(dH_T, dtype=np.float32)).cuda()
-    out = binding.backward(*(d[n] for n in IN_NAMES), d["dy"], dH_T=dH, ckpt=ckpt,
-                           ckpt_every=ckpt_every)
+        ckpt = binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=ckpt_every, H_0=h0)["ckpt"]
+    out = binding.backward(*(d[n] for n in IN_NAMES), d["dy"], dH_T=_cuda_f32(dH_T), H_0=h0,
+                           want_dH0=want_dH0, ckpt=ckpt, ckpt_every=ckpt_every)
     st, detail = binding.sync_status(out["workspace"])
     assert st == binding.M2RNN_OK, (binding.status_string(st), detail)
     torch.cuda.synchronize()
-    return {k: out[k].cpu().numpy() for k in GRAD_NAMES}
+    names = GRAD_NAMES + (("dH_0",) if want_dH0 else ())
+    return {k: out[k].cpu().numpy() for k in names}
 
 
 def oracle_args(inp, sl_b=slice(None), sl_n=slice(None)):
@@ -76,6 +82,6 @@ def check_forward(got, y_ref, H_ref, dtype, label=""):
 
 def check_grads(got, ref, dtype, label=""):
     tol = TOL_F32 if dtype == "f32" else TOL_BF16_REL
-    for name in GRAD_NAMES:
+    for name in GRAD_NAMES + (("dH_0",) if "dH_0" in got else ()):
         r = rel_fro(got[name], ref[name])
         assert r <= tol, (label, name, r)

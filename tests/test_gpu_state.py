@@ -1,0 +1,135 @@
+"""GPU parity for the stateful boundary: a scan started from a given state
+H_0, the gradient dH_0 of that state, sequences run in pieces, and one-step
+decoding (the fixed-size recurrent state of the reading notes, section 2.6).
+
+Every kernel family is compared element by element with the float64 oracle;
+the piece and decode tests compare the GPU with itself where the arithmetic
+is the same by construction.
+"""
+import numpy as np
+import pytest
+
+from matrix_state_non_gb300.inputs import make_inputs
+from oracle import backward as oracle_backward
+from oracle import forward as oracle_forward
+from parity_util import (IN_NAMES, TOL_BF16_REL, check_forward, check_grads, gpu_backward,
+                         gpu_forward, oracle_args, rel_fro)
+
+pytestmark = pytest.mark.gpu
+
+
+def _state(B, N, K, V, seed):
+    """A plausible state: the recurrence keeps H inside (-1, 1)."""
+    return np.random.default_rng(seed).uniform(-0.9, 0.9, (B, N, K, V)).astype(np.float32)
+
+
+@pytest.fixture
+def kernel_family(request, monkeypatch):
+    monkeypatch.setenv("M2RNN_KERNEL", request.param)
+    return request.param
+
+
+@pytest.mark.parametrize("kernel_family", ["mma", "tcgen05", "simt"], indirect=True)
+@pytest.mark.parametrize("B,N,T,K,V", [(2, 3, 37, 64, 64), (1, 1, 1, 64, 64), (1, 2, 70, 32, 64)])
+def test_forward_from_initial_state(kernel_family, B, N, T, K, V):
+    inp = make_inputs(B, N, T, K, V, "bf16", seed=300 + T)
+    H0 = _state(B, N, K, V, seed=T)
+    got = gpu_forward(inp, ckpt_every=16, H_0=H0)
+    y_ref, H_ref, Hs, _ = oracle_forward(*oracle_args(inp), return_states=True, H_0=H0.astype(np.float64))
+    check_forward(got, y_ref, H_ref, "bf16", label=(kernel_family, B, N, T, K, V))
+    for c in range((T - 1) // 16):
+        assert rel_fro(got["ckpt"][:, :, c], Hs[(c + 1) * 16]) <= 1e-2
+
+
+@pytest.mark.parametrize("B,N,T,K,V,dtype", [(1, 2, 45, 128, 128, "bf16"), (1, 2, 20, 16, 16, "f32")])
+def test_forward_from_initial_state_other_shapes(B, N, T, K, V, dtype):
+    inp = make_inputs(B, N, T, K, V, dtype, seed=310 + T)
+    H0 = _state(B, N, K, V, seed=T + 1)
+    got = gpu_forward(inp, H_0=H0)
+    y_ref, H_ref = oracle_forward(*oracle_args(inp), H_0=H0.astype(np.float64))
+    check_forward(got, y_ref, H_ref, dtype, label=(B, N, T, K, V, dtype))
+
+
+@pytest.mark.parametrize("kernel_family", ["mma", "simt"], indirect=True)
+@pytest.mark.parametrize("B,N,T,K,V,C,reuse", [(2, 2, 37, 64, 64, 14, False), (1, 1, 64, 32, 64, 14, True),
+                                               (1, 2, 29, 64, 64, 28, True), (1, 1, 1, 64, 64, 14, False)])
+def test_backward_from_initial_state(kernel_family, B, N, T, K, V, C, reuse):
+    inp = make_inputs(B, N, T, K, V, "bf16", seed=320 + T, with_dy=True)
+    H0 = _state(B, N, K, V, seed=T + 2)
+    dH = np.random.default_rng(5).standard_normal((B, N, K, V)).astype(np.float32)
+    got = gpu_backward(inp, dH_T=dH, ckpt_every=C, use_fwd_ckpt=reuse, H_0=H0, want_dH0=True)
+    ref = oracle_backward(*oracle_args(inp), inp.exact["dy"], dH.astype(np.float64), H_0=H0.astype(np.float64))
+    check_grads(got, ref, "bf16", label=(kernel_family, B, N, T, K, V, C))
+
+
+def test_backward_initial_state_f32():
+    inp = make_inputs(1, 2, 30, 16, 16, "f32", seed=330, with_dy=True)
+    H0 = _state(1, 2, 16, 16, seed=9)
+    got = gpu_backward(inp, ckpt_every=8, H_0=H0, want_dH0=True)
+    ref = oracle_backward(*oracle_args(inp), inp.exact["dy"], None, H_0=H0.astype(np.float64))
+    check_grads(got, ref, "f32")
+
+
+def _split(inp, T1):
+    import copy
+    a, b = copy.copy(inp), copy.copy(inp)
+    def cut(d, sl):
+        return {k: (x[:, sl] if k in ("q", "k", "v", "f", "dy") else x) for k, x in d.items()}
+    a.store, a.exact = cut(inp.store, slice(0, T1)), cut(inp.exact, slice(0, T1))
+    b.store, b.exact = cut(inp.store, slice(T1, None)), cut(inp.exact, slice(T1, None))
+    return a, b
+
+
+@pytest.mark.parametrize("kernel_family", ["mma", "tcgen05", "simt"], indirect=True)
+def test_forward_pieces_equal_one_pass(kernel_family):
+    """The state carried between calls is the fp32 state the kernel keeps, so
+    two calls over [0, T1) and [T1, T) reproduce one call's state bit for bit.
+    y agrees to fp32 rounding: a call reads out its last step by a different
+    (shuffle) summation than the in-scan readout."""
+    inp = make_inputs(2, 2, 50, 64, 64, "bf16", seed=340)
+    full = gpu_forward(inp)
+    a, b = _split(inp, 21)
+    ga = gpu_forward(a)
+    gb = gpu_forward(b, H_0=ga["H_T"])
+    np.testing.assert_allclose(np.concatenate([ga["y"], gb["y"]], axis=1), full["y"], rtol=0, atol=1e-5)
+    np.testing.assert_array_equal(gb["H_T"], full["H_T"])
+
+
+@pytest.mark.parametrize("kernel_family", ["mma", "simt"], indirect=True)
+def test_backward_pieces_compose(kernel_family):
+    """Backward in two pieces (dH_0 of the later piece feeds the earlier one)
+    agrees with one pass to within the bf16 tolerance."""
+    inp = make_inputs(1, 2, 60, 64, 64, "bf16", seed=350, with_dy=True)
+    full = gpu_backward(inp, ckpt_every=14, want_dH0=True)
+    a, b = _split(inp, 25)
+    H1 = gpu_forward(a)["H_T"]
+    gb = gpu_backward(b, ckpt_every=14, H_0=H1, want_dH0=True)
+    ga = gpu_backward(a, dH_T=gb["dH_0"], ckpt_every=14, want_dH0=True)
+    for name in ("dq", "dk", "dv", "df"):
+        assert rel_fro(np.concatenate([ga[name], gb[name]], axis=1), full[name]) <= TOL_BF16_REL, name
+    for name in ("dW", "dw_r"):
+        assert rel_fro(ga[name] + gb[name], full[name]) <= TOL_BF16_REL, name
+    assert rel_fro(ga["dH_0"], full["dH_0"]) <= TOL_BF16_REL
+
+
+@pytest.mark.parametrize("kernel_family", ["mma", "tcgen05", "simt"], indirect=True)
+def test_decode_steps_follow_the_scan(kernel_family):
+    """T single-step decodes from H_0 give the scan's y_t and final state."""
+    import torch
+    from matrix_state_non_gb300 import binding
+    B, N, T, K, V = 2, 4, 12, 64, 64
+    inp = make_inputs(B, N, T, K, V, "bf16", seed=360)
+    H0 = _state(B, N, K, V, seed=4)
+    full = gpu_forward(inp, H_0=H0)
+    d = binding.to_device(inp)
+    H = torch.from_numpy(H0).cuda()
+    ys = []
+    for t in range(T):
+        step = [d[n][:, t].contiguous() for n in ("q", "k", "v", "f")]
+        y = binding.decode_step(H, *step, d["W"], d["w_r"])
+        ys.append(y.cpu().numpy())
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(np.stack(ys, axis=1), full["y"], rtol=0, atol=1e-5)
+    np.testing.assert_allclose(H.cpu().numpy(), full["H_T"], rtol=0, atol=1e-5)
+    y_ref, H_ref = oracle_forward(*oracle_args(inp), H_0=H0.astype(np.float64))
+    check_forward({"y": np.stack(ys, axis=1), "H_T": H.cpu().numpy()}, y_ref, H_ref, "bf16")
