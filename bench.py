@@ -474,7 +474,9 @@ def time_forward(name, binding, dev, stream, flush, pk, dist, reps=5):
 def time_decode(binding, dev, stream, dist, steps=64):
     """One-token decoding (m2rnn_decode_step): the B x heads states of the
     forward+backward workload advanced one step per call, `steps` calls in a
-    row, the state updated in place."""
+    row, the state updated in place.  Timed twice: called eagerly from Python
+    (bound by the host call) and replayed as one CUDA graph of the `steps`
+    calls (the device time per step)."""
     import torch
     w = WORKLOADS[MAIN]
     inp = make_workload(MAIN)
@@ -485,21 +487,43 @@ def time_decode(binding, dev, stream, dist, steps=64):
     y = torch.empty((B, N, V), device=dev, dtype=torch.float32)
     ws = torch.empty(binding.m2rnn_forward_workspace_size(B, 1, N, K, V, binding.M2RNN_BF16),
                      device=dev, dtype=torch.uint8)
+
+    def run_all():
+        for t in range(steps):
+            binding.decode_step(H, *toks[t], d["W"], d["w_r"], y=y, workspace=ws)
+
     for t in range(8):
         binding.decode_step(H, *toks[t], d["W"], d["w_r"], y=y, workspace=ws)
     torch.cuda.synchronize(dev)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for t in range(steps):
-        binding.decode_step(H, *toks[t], d["W"], d["w_r"], y=y, workspace=ws)
+    run_all()
     b.record(stream)
     torch.cuda.synchronize(dev)
+    us_eager = dist.max(a.elapsed_time(b) * 1e3 / steps)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        run_all()  # warm the side stream before capture
+    torch.cuda.current_stream(dev).wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run_all()
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    reps = 5
+    a.record(stream)
+    for _ in range(reps):
+        graph.replay()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    us = dist.max(a.elapsed_time(b) * 1e3 / (reps * steps))
     st, detail = binding.sync_status(ws)
     if st != binding.M2RNN_OK:
         raise RuntimeError(f"decode: device status {binding.status_string(st)} at {detail}")
-    us = dist.max(a.elapsed_time(b) * 1e3 / steps)
     return {"workload": f"bf16 decode, {B}x{N} states of {K}x{V}, one token per call, {steps} calls",
-            "kernel": "warp-mma (T = 1)", "us_per_step": us,
+            "kernel": "decode kernel (warp MMA, state in registers)", "us_per_step": us,
+            "us_per_step_eager": us_eager, "timing": "CUDA graph of the calls (eager: Python call per step)",
             "value": dist.world * B * N / (us * 1e-6), "unit": UNIT, "launches_per_step": 1}
 
 

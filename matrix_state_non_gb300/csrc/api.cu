@@ -203,8 +203,18 @@ int m2rnn_decode_step(float* H, const void* q, const void* k, const void* v, con
                       int64_t V, m2rnn_dtype dtype, void* workspace, size_t workspace_bytes,
                       void* cuda_stream) {
   if (H == nullptr) return M2RNN_ERR_INVALID_ARG;
-  // One step from H to H: every kernel reads a state element before the same
-  // thread block overwrites it.
+  if (dtype_ok(dtype) && dims_ok(B, 1, N, K, V) && decode_kernel_supported(static_cast<int>(K), static_cast<int>(V), dtype) &&
+      kernel_override() < 0) {
+    const void* req[] = {H, q, k, v, f, W, w_r, y};
+    for (const void* p : req)
+      if (!aligned16(p)) return M2RNN_ERR_INVALID_ARG;
+    if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < kStatusBytes)
+      return M2RNN_ERR_WORKSPACE;
+    return cuda_status(launch_decode_step(H, q, k, v, f, W, w_r, y, static_cast<int>(B), static_cast<int>(N),
+                                          static_cast<int>(K), static_cast<cudaStream_t>(cuda_stream)));
+  }
+  // Otherwise the scan kernels with T = 1, from H to H: every kernel reads a
+  // state element before the same thread block overwrites it.
   return m2rnn_forward_state(q, k, v, f, W, w_r, H, y, H, nullptr, 0, B, 1, N, K, V, dtype,
                              workspace, workspace_bytes, cuda_stream);
 }

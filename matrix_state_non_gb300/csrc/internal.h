@@ -70,6 +70,12 @@ cudaError_t launch_reduce_partials(const BwdArgs& a, cudaStream_t s);
 // Register-resident warp-MMA kernels (bf16 inputs, V = 64).
 bool mma_forward_supported(int K, int V);
 cudaError_t launch_mma_forward(const FwdArgs& a, cudaStream_t s);
+// One decoding step (bf16, V = 64, K % 16 == 0, K <= 128), state in place.
+bool decode_kernel_supported(int K, int V, m2rnn_dtype dtype);
+cudaError_t launch_decode_step(float* H, const void* q, const void* k, const void* v, const void* f,
+                               const void* W, const void* w_r, float* y, int B, int N, int K,
+                               cudaStream_t stream);
+
 bool mma_backward_supported(int K, int V);
 size_t mma_backward_scratch_bytes(int B, int T, int N, int K, int V, int ckpt_every);
 int mma_backward_max_chunk();

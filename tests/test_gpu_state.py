@@ -112,12 +112,15 @@ def test_backward_pieces_compose(kernel_family):
     assert rel_fro(ga["dH_0"], full["dH_0"]) <= TOL_BF16_REL
 
 
-@pytest.mark.parametrize("kernel_family", ["mma", "tcgen05", "simt"], indirect=True)
-def test_decode_steps_follow_the_scan(kernel_family):
-    """T single-step decodes from H_0 give the scan's y_t and final state."""
+@pytest.mark.parametrize("kernel_family,K", [("auto", 64), ("auto", 16), ("auto", 128), ("mma", 64),
+                                            ("tcgen05", 64), ("simt", 64)], indirect=["kernel_family"])
+def test_decode_steps_follow_the_scan(kernel_family, K):
+    """T single-step decodes from H_0 give the scan's y_t and final state
+    ("auto": the dedicated decode kernel; a forced family: the scan kernels
+    with T = 1)."""
     import torch
     from matrix_state_non_gb300 import binding
-    B, N, T, K, V = 2, 4, 12, 64, 64
+    B, N, T, V = 2, 4, 12, 64
     inp = make_inputs(B, N, T, K, V, "bf16", seed=360)
     H0 = _state(B, N, K, V, seed=4)
     full = gpu_forward(inp, H_0=H0)
@@ -129,7 +132,13 @@ def test_decode_steps_follow_the_scan(kernel_family):
         y = binding.decode_step(H, *step, d["W"], d["w_r"])
         ys.append(y.cpu().numpy())
     torch.cuda.synchronize()
-    np.testing.assert_allclose(np.stack(ys, axis=1), full["y"], rtol=0, atol=1e-5)
-    np.testing.assert_allclose(H.cpu().numpy(), full["H_T"], rtol=0, atol=1e-5)
+    # The dedicated kernel sums the MMA k-tiles in another order than the scan,
+    # which can flip a bf16 rounding of the state operand (one bf16 ulp of a
+    # state element in (0.5, 1) is 2^-8): 2e-3 between the two GPU kernels;
+    # the same kernel with T = 1 agrees to 1e-5.  Correctness is the oracle
+    # check below.
+    tol = 2e-3 if kernel_family == "auto" else 1e-5
+    np.testing.assert_allclose(np.stack(ys, axis=1), full["y"], rtol=0, atol=tol)
+    np.testing.assert_allclose(H.cpu().numpy(), full["H_T"], rtol=0, atol=tol)
     y_ref, H_ref = oracle_forward(*oracle_args(inp), H_0=H0.astype(np.float64))
     check_forward({"y": np.stack(ys, axis=1), "H_T": H.cpu().numpy()}, y_ref, H_ref, "bf16")
