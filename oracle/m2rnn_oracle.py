@@ -23,6 +23,11 @@ H, Z are K x V; W is V x V and multiplies from the right, so
 f_t is a scalar.  Array layouts: q, k [B,T,N,K]; v [B,T,N,V]; f [B,T,N];
 W [N,V,V]; w_r [N,V]; y, dy [B,T,N,V]; H_0, dH_0, H_T, dH_T [B,N,K,V].
 
+Multi-value sharing (section 2.4 of the notes): q and k may have a head
+axis of length 1, [B,T,1,K], shared by every value head; each head keeps its
+own v, f, W, w_r and state.  Their gradients are then summed over the heads
+(section 2.7) and returned with the same [B,T,1,K] shape.
+
 Every function is a plain loop over t, vectorised over (b, n) with numpy
 matmul/einsum; there is no blocking, fusion or reordering beyond the equations.
 """
@@ -35,6 +40,17 @@ def _as64(x):
     return np.asarray(x, dtype=np.float64)
 
 
+def _heads(q, k, v):
+    """q, k broadcast to every value head (a shared q/k has a head axis of 1)."""
+    N = v.shape[2]
+    if q.shape[2] != N:
+        if q.shape[2] != 1 or k.shape[2] != 1:
+            raise ValueError("q/k need one head (shared) or as many heads as v")
+        q = np.broadcast_to(q, q.shape[:2] + (N,) + q.shape[3:])
+        k = np.broadcast_to(k, k.shape[:2] + (N,) + k.shape[3:])
+    return q, k
+
+
 def forward(q, k, v, f, W, w_r, return_states: bool = False, H_0=None):
     """M2RNN forward scan (Eq. 10-12) from H_0 (zero if None).
 
@@ -43,6 +59,7 @@ def forward(q, k, v, f, W, w_r, return_states: bool = False, H_0=None):
     [T,B,N,K,V] (index t-1 holds Z_t).
     """
     q, k, v, f, W, w_r = map(_as64, (q, k, v, f, W, w_r))
+    q, k = _heads(q, k, v)
     B, T, N, K = q.shape
     V = v.shape[-1]
     H = np.zeros((B, N, K, V)) if H_0 is None else _as64(H_0).copy()
@@ -92,10 +109,13 @@ def backward(q, k, v, f, W, w_r, dy, dH_T=None, H_0=None):
     The state gradient left after step 1, C_0, is dH_0 = dL/dH_0 (the same
     recursion carried one step further back).
 
-    Returns a dict with dq, dk [B,T,N,K]; dv [B,T,N,V]; df [B,T,N];
-    dW [N,V,V]; dw_r [N,V]; dH_0 [B,N,K,V]; all float64.
+    Returns a dict with dq, dk [B,T,N,K] ([B,T,1,K], summed over the heads,
+    when q and k are shared); dv [B,T,N,V]; df [B,T,N]; dW [N,V,V];
+    dw_r [N,V]; dH_0 [B,N,K,V]; all float64.
     """
     q, k, v, f, W, w_r, dy = map(_as64, (q, k, v, f, W, w_r, dy))
+    shared = q.shape[2] != v.shape[2]
+    q, k = _heads(q, k, v)
     B, T, N, K = q.shape
     V = v.shape[-1]
     _, _, Hs, Zs = forward(q, k, v, f, W, w_r, return_states=True, H_0=H_0)
@@ -121,6 +141,9 @@ def backward(q, k, v, f, W, w_r, dy, dH_T=None, H_0=None):
         dW += np.einsum("bnkm,bnkj->nmj", H_prev, D)
         dw_r += np.einsum("bnv,bnv->nv", u, vt)
         C = ft * R + np.matmul(D, Wt)
+    if shared:  # one q/k for every head: their gradients sum over the heads
+        dq = dq.sum(axis=2, keepdims=True)
+        dk = dk.sum(axis=2, keepdims=True)
     return dict(dq=dq, dk=dk, dv=dv, df=df, dW=dW, dw_r=dw_r, dH_0=C)
 
 

@@ -464,3 +464,55 @@ def test_initial_state_gradient_matches_torch_autograd():
     L.backward()
     g = backward(*args, dy, dH_T, H_0=H_0)
     np.testing.assert_allclose(g["dH_0"], h0.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# Multi-value heads: one q/k shared by every value head
+# --------------------------------------------------------------------------
+
+def _shared_qk(B=2, N=3, T=6, K=4, V=3, seed=60):
+    q, k, v, f, W, w_r = _rand(B, N, T, K, V, seed)
+    return q[:, :, :1].copy(), k[:, :, :1].copy(), v, f, W, w_r
+
+
+def test_shared_qk_equals_replicated_heads():
+    """A shared q/k is the multi-head case with the same q/k in every head
+    (section 2.4): the forward is identical, and the shared gradients are the
+    per-head gradients summed over heads (section 2.7)."""
+    q1, k1, v, f, W, w_r = _shared_qk()
+    N = v.shape[2]
+    qN, kN = np.repeat(q1, N, axis=2), np.repeat(k1, N, axis=2)
+    y1, H1 = forward(q1, k1, v, f, W, w_r)
+    yN, HN = forward(qN, kN, v, f, W, w_r)
+    np.testing.assert_array_equal(y1, yN)
+    np.testing.assert_array_equal(H1, HN)
+    rng = np.random.default_rng(14)
+    dy = rng.standard_normal(v.shape)
+    g1 = backward(q1, k1, v, f, W, w_r, dy)
+    gN = backward(qN, kN, v, f, W, w_r, dy)
+    assert g1["dq"].shape == q1.shape and g1["dk"].shape == k1.shape
+    np.testing.assert_allclose(g1["dq"], gN["dq"].sum(axis=2, keepdims=True), rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(g1["dk"], gN["dk"].sum(axis=2, keepdims=True), rtol=1e-13, atol=1e-15)
+    for name in ("dv", "df", "dW", "dw_r", "dH_0"):
+        np.testing.assert_array_equal(g1[name], gN[name])
+
+
+def test_shared_qk_gradient_matches_finite_differences():
+    """Brute force on the shared q and k (one key/query vector feeding every head)."""
+    q1, k1, v, f, W, w_r = _shared_qk(B=1, N=3, T=4, K=3, V=2, seed=61)
+    rng = np.random.default_rng(15)
+    dy = rng.standard_normal(v.shape)
+    args = [q1, k1, v, f, W, w_r]
+    g = backward(*args, dy)
+    eps = 1e-6
+    for idx, name in ((0, "dq"), (1, "dk")):
+        fd = np.zeros_like(args[idx])
+        it = np.nditer(args[idx], flags=["multi_index"])
+        for _ in it:
+            mi = it.multi_index
+            xp = [a.copy() for a in args]
+            xm = [a.copy() for a in args]
+            xp[idx][mi] += eps
+            xm[idx][mi] -= eps
+            fd[mi] = (loss(*xp, dy) - loss(*xm, dy)) / (2 * eps)
+        np.testing.assert_allclose(g[name], fd, rtol=2e-7, atol=2e-8, err_msg=name)
