@@ -130,8 +130,13 @@ int m2rnn_backward(const void* q, const void* k, const void* v, const void* f,
                    size_t workspace_bytes, void* cuda_stream);
 
 /*
- * Forward scan from a given initial state: as m2rnn_forward, with
- *   H_0 [B,N,K,V] fp32 (may be NULL = zero): the state before step 1.
+ * Forward scan from a given initial state, optionally with one q/k shared by
+ * every head: as m2rnn_forward, with
+ *   H_0 [B,N,K,V] fp32 (may be NULL = zero): the state before step 1;
+ *   qk_heads: N (q, k are [B,T,N,K], one per head) or 1 (q, k are
+ *        [B,T,1,K], shared by all N value heads: the multi-value heads of
+ *        the reading notes, section 2.4; each head keeps its own v, f, W,
+ *        w_r and state).  Anything else is M2RNN_ERR_INVALID_ARG.
  * With H_T set to the final state of one call, the next call over the
  * following steps continues the same sequence (the fixed-size recurrent
  * state of the reading notes, section 2.6): a sequence can run in pieces.
@@ -141,18 +146,28 @@ int m2rnn_forward_state(const void* q, const void* k, const void* v,
                         const void* f, const void* W, const void* w_r,
                         const float* H_0, float* y, float* H_T, float* ckpt,
                         int ckpt_every, int64_t B, int64_t T, int64_t N,
-                        int64_t K, int64_t V, m2rnn_dtype dtype,
-                        void* workspace, size_t workspace_bytes,
-                        void* cuda_stream);
+                        int64_t qk_heads, int64_t K, int64_t V,
+                        m2rnn_dtype dtype, void* workspace,
+                        size_t workspace_bytes, void* cuda_stream);
+
+/* Bytes of device workspace m2rnn_backward_state needs (a shared q/k,
+ * qk_heads = 1 with N > 1, adds room for the per-head dq, dk). */
+size_t m2rnn_backward_state_workspace_size(int64_t B, int64_t T, int64_t N,
+                                           int64_t qk_heads, int64_t K,
+                                           int64_t V, m2rnn_dtype dtype,
+                                           int ckpt_every, int have_ckpt);
 
 /*
  * Backward through time from a given initial state: as m2rnn_backward, with
  *   H_0  [B,N,K,V] fp32 (may be NULL = zero): the forward's initial state;
  *   dH_0 [B,N,K,V] fp32 (may be NULL): receives dL/dH_0, the state gradient
- *        carried one step past t = 1 (C_0 in the recursion above).
+ *        carried one step past t = 1 (C_0 in the recursion above);
+ *   qk_heads: as for m2rnn_forward_state.  With a shared q/k (1), dq and dk
+ *        are [B,T,1,K]: the per-head gradients summed over the heads in a
+ *        fixed order (notes section 2.7).
  * When a sequence runs in pieces, dH_0 of a later piece is the dH_T of the
  * piece before it.  `ckpt`, if given, must come from m2rnn_forward_state
- * with the same H_0.
+ * with the same H_0.  workspace: m2rnn_backward_state_workspace_size bytes.
  */
 int m2rnn_backward_state(const void* q, const void* k, const void* v,
                          const void* f, const void* W, const void* w_r,
@@ -160,21 +175,23 @@ int m2rnn_backward_state(const void* q, const void* k, const void* v,
                          const float* ckpt, int ckpt_every, float* dq,
                          float* dk, float* dv, float* df, float* dW,
                          float* dw_r, float* dH_0, int64_t B, int64_t T,
-                         int64_t N, int64_t K, int64_t V, m2rnn_dtype dtype,
-                         void* workspace, size_t workspace_bytes,
-                         void* cuda_stream);
+                         int64_t N, int64_t qk_heads, int64_t K, int64_t V,
+                         m2rnn_dtype dtype, void* workspace,
+                         size_t workspace_bytes, void* cuda_stream);
 
 /*
  * One decoding step for a batch of states (serving: one new token per
  * (b, head)): H [B,N,K,V] fp32 is updated in place to H_t from H_{t-1}, and
- * y [B,N,V] fp32 receives y_t.  q, k [B,N,K]; v [B,N,V]; f [B,N]; W, w_r as
- * above.  Same kernels as m2rnn_forward_state with T = 1; the workspace is
+ * y [B,N,V] fp32 receives y_t.  q, k [B,qk_heads,K]; v [B,N,V]; f [B,N];
+ * W, w_r as above; qk_heads as for m2rnn_forward_state.  bf16 with V = 64
+ * and K a multiple of 16 (<= 128) runs a dedicated kernel, other shapes the
+ * scan kernels with T = 1; the workspace is
  * m2rnn_forward_workspace_size(B, 1, N, K, V, dtype) bytes.
  */
 int m2rnn_decode_step(float* H, const void* q, const void* k, const void* v,
                       const void* f, const void* W, const void* w_r, float* y,
-                      int64_t B, int64_t N, int64_t K, int64_t V,
-                      m2rnn_dtype dtype, void* workspace,
+                      int64_t B, int64_t N, int64_t qk_heads, int64_t K,
+                      int64_t V, m2rnn_dtype dtype, void* workspace,
                       size_t workspace_bytes, void* cuda_stream);
 
 /*

@@ -30,7 +30,7 @@ EXPORTS = (
     "m2rnn_version", "m2rnn_status_string", "m2rnn_checkpoint_count", "m2rnn_path",
     "m2rnn_forward_workspace_size", "m2rnn_backward_workspace_size", "m2rnn_forward",
     "m2rnn_backward", "m2rnn_sync_status", "m2rnn_forward_state", "m2rnn_backward_state",
-    "m2rnn_decode_step",
+    "m2rnn_decode_step", "m2rnn_backward_state_workspace_size",
 )
 
 _lib = None
@@ -72,11 +72,13 @@ def load() -> ctypes.CDLL:
     lib.m2rnn_sync_status.restype = ci
     lib.m2rnn_sync_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.m2rnn_forward_state.restype = ci
-    lib.m2rnn_forward_state.argtypes = [vp] * 10 + [ci] + [i64] * 5 + [ci, vp, sz, vp]
+    lib.m2rnn_forward_state.argtypes = [vp] * 10 + [ci] + [i64] * 6 + [ci, vp, sz, vp]
     lib.m2rnn_backward_state.restype = ci
-    lib.m2rnn_backward_state.argtypes = [vp] * 10 + [ci] + [vp] * 7 + [i64] * 5 + [ci, vp, sz, vp]
+    lib.m2rnn_backward_state.argtypes = [vp] * 10 + [ci] + [vp] * 7 + [i64] * 6 + [ci, vp, sz, vp]
+    lib.m2rnn_backward_state_workspace_size.restype = sz
+    lib.m2rnn_backward_state_workspace_size.argtypes = [i64] * 6 + [ci, ci, ci]
     lib.m2rnn_decode_step.restype = ci
-    lib.m2rnn_decode_step.argtypes = [vp] * 8 + [i64] * 4 + [ci, vp, sz, vp]
+    lib.m2rnn_decode_step.argtypes = [vp] * 8 + [i64] * 5 + [ci, vp, sz, vp]
     _lib = lib
     return lib
 
@@ -124,22 +126,28 @@ def m2rnn_backward(q, k, v, f, W, w_r, dy, dH_T, ckpt, ckpt_every, dq, dk, dv, d
                                  workspace_bytes, stream)
 
 
-def m2rnn_forward_state(q, k, v, f, W, w_r, H_0, y, H_T, ckpt, ckpt_every, B, T, N, K, V, dtype,
-                        workspace, workspace_bytes, stream) -> int:
-    return load().m2rnn_forward_state(q, k, v, f, W, w_r, H_0, y, H_T, ckpt, ckpt_every, B, T, N, K,
-                                      V, dtype, workspace, workspace_bytes, stream)
+def m2rnn_forward_state(q, k, v, f, W, w_r, H_0, y, H_T, ckpt, ckpt_every, B, T, N, qk_heads, K, V,
+                        dtype, workspace, workspace_bytes, stream) -> int:
+    return load().m2rnn_forward_state(q, k, v, f, W, w_r, H_0, y, H_T, ckpt, ckpt_every, B, T, N,
+                                      qk_heads, K, V, dtype, workspace, workspace_bytes, stream)
+
+
+def m2rnn_backward_state_workspace_size(B, T, N, qk_heads, K, V, dtype, ckpt_every, have_ckpt) -> int:
+    return load().m2rnn_backward_state_workspace_size(B, T, N, qk_heads, K, V, dtype, ckpt_every,
+                                                      int(bool(have_ckpt)))
 
 
 def m2rnn_backward_state(q, k, v, f, W, w_r, H_0, dy, dH_T, ckpt, ckpt_every, dq, dk, dv, df, dW,
-                         dw_r, dH_0, B, T, N, K, V, dtype, workspace, workspace_bytes, stream) -> int:
+                         dw_r, dH_0, B, T, N, qk_heads, K, V, dtype, workspace, workspace_bytes,
+                         stream) -> int:
     return load().m2rnn_backward_state(q, k, v, f, W, w_r, H_0, dy, dH_T, ckpt, ckpt_every, dq, dk,
-                                       dv, df, dW, dw_r, dH_0, B, T, N, K, V, dtype, workspace,
-                                       workspace_bytes, stream)
+                                       dv, df, dW, dw_r, dH_0, B, T, N, qk_heads, K, V, dtype,
+                                       workspace, workspace_bytes, stream)
 
 
-def m2rnn_decode_step(H, q, k, v, f, W, w_r, y, B, N, K, V, dtype, workspace, workspace_bytes,
-                      stream) -> int:
-    return load().m2rnn_decode_step(H, q, k, v, f, W, w_r, y, B, N, K, V, dtype, workspace,
+def m2rnn_decode_step(H, q, k, v, f, W, w_r, y, B, N, qk_heads, K, V, dtype, workspace,
+                      workspace_bytes, stream) -> int:
+    return load().m2rnn_decode_step(H, q, k, v, f, W, w_r, y, B, N, qk_heads, K, V, dtype, workspace,
                                     workspace_bytes, stream)
 
 
@@ -178,9 +186,10 @@ def _stream_handle(stream) -> int:
 
 
 def _shapes(q, v):
-    B, T, N, K = q.shape
-    V = v.shape[-1]
-    return B, T, N, K, V
+    """(B, T, N, K, V, qk_heads): N from v; q, k carry 1 head when shared."""
+    B, T, _, K = q.shape
+    N, V = v.shape[2], v.shape[-1]
+    return B, T, N, K, V, q.shape[2]
 
 
 def forward(q, k, v, f, W, w_r, *, H_0=None, want_state: bool = True, ckpt_every: int = 0,
@@ -192,7 +201,7 @@ def forward(q, k, v, f, W, w_r, *, H_0=None, want_state: bool = True, ckpt_every
     ``out`` may hold preallocated y / H_T / ckpt tensors.
     """
     import torch
-    B, T, N, K, V = _shapes(q, v)
+    B, T, N, K, V, NQ = _shapes(q, v)
     dt = _dtype_code(q)
     dev = q.device
     out = dict(out or {})
@@ -213,7 +222,7 @@ def forward(q, k, v, f, W, w_r, *, H_0=None, want_state: bool = True, ckpt_every
         workspace = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
     st = m2rnn_forward_state(_ptr(q), _ptr(k), _ptr(v), _ptr(f), _ptr(W), _ptr(w_r), _ptr(H_0),
                              _ptr(y), _ptr(H_T), _ptr(ckpt), ckpt_every if ckpt is not None else 0,
-                             B, T, N, K, V, dt, _ptr(workspace), workspace.numel(),
+                             B, T, N, NQ, K, V, dt, _ptr(workspace), workspace.numel(),
                              _stream_handle(stream))
     _check(st, "m2rnn_forward_state")
     res = dict(y=y, H_T=H_T, workspace=workspace)
@@ -229,7 +238,7 @@ def backward(q, k, v, f, W, w_r, dy, *, dH_T=None, H_0=None, want_dH0: bool = Fa
     ``H_0`` is the forward's initial state (None = zero); ``ckpt``, if given,
     must come from a forward with the same ``H_0``."""
     import torch
-    B, T, N, K, V = _shapes(q, v)
+    B, T, N, K, V, NQ = _shapes(q, v)
     dt = _dtype_code(q)
     dev = q.device
     out = dict(out or {})
@@ -238,22 +247,22 @@ def backward(q, k, v, f, W, w_r, dy, *, dH_T=None, H_0=None, want_dH0: bool = Fa
         t = out.get(name)
         return t if t is not None else torch.empty(shape, device=dev, dtype=torch.float32)
 
-    dq = _get("dq", (B, T, N, K))
-    dk = _get("dk", (B, T, N, K))
+    dq = _get("dq", (B, T, NQ, K))
+    dk = _get("dk", (B, T, NQ, K))
     dv = _get("dv", (B, T, N, V))
     df = _get("df", (B, T, N))
     dW = _get("dW", (N, V, V))
     dw_r = _get("dw_r", (N, V))
     dH_0 = _get("dH_0", (B, N, K, V)) if want_dH0 else None
-    ws_bytes = m2rnn_backward_workspace_size(B, T, N, K, V, dt, ckpt_every, ckpt is not None)
+    ws_bytes = m2rnn_backward_state_workspace_size(B, T, N, NQ, K, V, dt, ckpt_every, ckpt is not None)
     if ws_bytes == 0:
-        raise M2RNNError(M2RNN_ERR_INVALID_ARG, "m2rnn_backward_workspace_size")
+        raise M2RNNError(M2RNN_ERR_INVALID_ARG, "m2rnn_backward_state_workspace_size")
     if workspace is None or workspace.numel() < ws_bytes:
         workspace = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
     st = m2rnn_backward_state(_ptr(q), _ptr(k), _ptr(v), _ptr(f), _ptr(W), _ptr(w_r), _ptr(H_0),
                               _ptr(dy), _ptr(dH_T), _ptr(ckpt), ckpt_every, _ptr(dq), _ptr(dk),
-                              _ptr(dv), _ptr(df), _ptr(dW), _ptr(dw_r), _ptr(dH_0), B, T, N, K, V,
-                              dt, _ptr(workspace), workspace.numel(), _stream_handle(stream))
+                              _ptr(dv), _ptr(df), _ptr(dW), _ptr(dw_r), _ptr(dH_0), B, T, N, NQ, K,
+                              V, dt, _ptr(workspace), workspace.numel(), _stream_handle(stream))
     _check(st, "m2rnn_backward_state")
     res = dict(dq=dq, dk=dk, dv=dv, df=df, dW=dW, dw_r=dw_r, workspace=workspace)
     if dH_0 is not None:
@@ -263,10 +272,11 @@ def backward(q, k, v, f, W, w_r, dy, *, dH_T=None, H_0=None, want_dH0: bool = Fa
 
 def decode_step(H, q, k, v, f, W, w_r, *, y=None, workspace=None, stream=None):
     """One decoding step on the GPU: ``H`` (fp32 [B,N,K,V], contiguous) is
-    updated in place; q, k [B,N,K], v [B,N,V], f [B,N].  Returns y [B,N,V]."""
+    updated in place; q, k [B,N,K] (or [B,1,K], shared by the heads),
+    v [B,N,V], f [B,N].  Returns y [B,N,V]."""
     import torch
-    B, N, K = q.shape
-    V = v.shape[-1]
+    B, NQ, K = q.shape
+    N, V = v.shape[1], v.shape[-1]
     dt = _dtype_code(q)
     if y is None:
         y = torch.empty((B, N, V), device=q.device, dtype=torch.float32)
@@ -276,7 +286,8 @@ def decode_step(H, q, k, v, f, W, w_r, *, y=None, workspace=None, stream=None):
     if workspace is None:
         workspace = torch.empty(ws_bytes, device=q.device, dtype=torch.uint8)
     st = m2rnn_decode_step(_ptr(H), _ptr(q), _ptr(k), _ptr(v), _ptr(f), _ptr(W), _ptr(w_r), _ptr(y),
-                           B, N, K, V, dt, _ptr(workspace), workspace.numel(), _stream_handle(stream))
+                           B, N, NQ, K, V, dt, _ptr(workspace), workspace.numel(),
+                           _stream_handle(stream))
     _check(st, "m2rnn_decode_step")
     return y
 

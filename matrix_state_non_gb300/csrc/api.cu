@@ -88,11 +88,13 @@ cudaError_t launch_forward_path(int path, const FwdArgs& a, cudaStream_t s) {
 }
 
 struct BwdLayout {
-  size_t ckpt_off, dwp_off, dwrp_off, scratch_off, total;
+  size_t ckpt_off, dwp_off, dwrp_off, scratch_off, qk_off, total;
 };
 
+// shared_qk: one q/k for every head; the per-head dq, dk go to the workspace
+// ([B,T,N,K] each) and are summed over heads into the caller's [B,T,1,K].
 BwdLayout bwd_layout(int64_t B, int64_t T, int64_t N, int64_t K, int64_t V, int dt, int C,
-                     bool have_ckpt) {
+                     bool have_ckpt, bool shared_qk = false) {
   BwdLayout l{};
   const int path = choose_bwd_path(K, V, dt, C);
   const int64_t nck = (T - 1) / C;
@@ -113,6 +115,8 @@ BwdLayout bwd_layout(int64_t B, int64_t T, int64_t N, int64_t K, int64_t V, int 
     off = align256(off + tc_backward_scratch_bytes(b, nn, k, v, C));
   else
     off = align256(off + simt_backward_scratch_bytes(b, nn, k, v, C));
+  l.qk_off = off;
+  if (shared_qk) off = align256(off + 2 * sizeof(float) * static_cast<size_t>(B * T * N * K));
   l.total = off;
   return l;
 }
@@ -158,11 +162,21 @@ size_t m2rnn_backward_workspace_size(int64_t B, int64_t T, int64_t N, int64_t K,
   return bwd_layout(B, T, N, K, V, dtype, ckpt_every, have_ckpt != 0).total;
 }
 
+size_t m2rnn_backward_state_workspace_size(int64_t B, int64_t T, int64_t N, int64_t qk_heads,
+                                           int64_t K, int64_t V, m2rnn_dtype dtype, int ckpt_every,
+                                           int have_ckpt) {
+  if (!dims_ok(B, T, N, K, V) || choose_path(K, V, dtype) < 0) return 0;
+  if (ckpt_every < 1 || ckpt_every > kMaxCkptEvery || (qk_heads != 1 && qk_heads != N)) return 0;
+  return bwd_layout(B, T, N, K, V, dtype, ckpt_every, have_ckpt != 0, qk_heads == 1 && N > 1).total;
+}
+
 int m2rnn_forward_state(const void* q, const void* k, const void* v, const void* f, const void* W,
                         const void* w_r, const float* H_0, float* y, float* H_T, float* ckpt,
-                        int ckpt_every, int64_t B, int64_t T, int64_t N, int64_t K, int64_t V,
-                        m2rnn_dtype dtype, void* workspace, size_t workspace_bytes, void* cuda_stream) {
+                        int ckpt_every, int64_t B, int64_t T, int64_t N, int64_t qk_heads, int64_t K,
+                        int64_t V, m2rnn_dtype dtype, void* workspace, size_t workspace_bytes,
+                        void* cuda_stream) {
   if (!dtype_ok(dtype) || !dims_ok(B, T, N, K, V)) return M2RNN_ERR_INVALID_ARG;
+  if (qk_heads != 1 && qk_heads != N) return M2RNN_ERR_INVALID_ARG;
   const int path = choose_path(K, V, dtype);
   if (path < 0) return path;
   const void* req[] = {q, k, v, f, W, w_r, y};
@@ -179,7 +193,7 @@ int m2rnn_forward_state(const void* q, const void* k, const void* v, const void*
   if (e != cudaSuccess) return M2RNN_ERR_CUDA;
   FwdArgs a{};
   a.q = q; a.k = k; a.v = v; a.f = f; a.W = W; a.w_r = w_r;
-  a.H0 = H_0; a.y = y; a.H_T = H_T; a.ckpt = ckpt;
+  a.H0 = H_0; a.qkN = static_cast<int>(qk_heads); a.y = y; a.H_T = H_T; a.ckpt = ckpt;
   a.ckpt_every = ckpt ? ckpt_every : 1;
   a.n_ckpt = ckpt ? (T - 1) / ckpt_every : 0;
   a.B = static_cast<int>(B); a.T = static_cast<int>(T); a.N = static_cast<int>(N);
@@ -194,15 +208,15 @@ int m2rnn_forward(const void* q, const void* k, const void* v, const void* f, co
                   const void* w_r, float* y, float* H_T, float* ckpt, int ckpt_every, int64_t B,
                   int64_t T, int64_t N, int64_t K, int64_t V, m2rnn_dtype dtype, void* workspace,
                   size_t workspace_bytes, void* cuda_stream) {
-  return m2rnn_forward_state(q, k, v, f, W, w_r, nullptr, y, H_T, ckpt, ckpt_every, B, T, N, K, V,
+  return m2rnn_forward_state(q, k, v, f, W, w_r, nullptr, y, H_T, ckpt, ckpt_every, B, T, N, N, K, V,
                              dtype, workspace, workspace_bytes, cuda_stream);
 }
 
 int m2rnn_decode_step(float* H, const void* q, const void* k, const void* v, const void* f,
-                      const void* W, const void* w_r, float* y, int64_t B, int64_t N, int64_t K,
-                      int64_t V, m2rnn_dtype dtype, void* workspace, size_t workspace_bytes,
+                      const void* W, const void* w_r, float* y, int64_t B, int64_t N, int64_t qk_heads,
+                      int64_t K, int64_t V, m2rnn_dtype dtype, void* workspace, size_t workspace_bytes,
                       void* cuda_stream) {
-  if (H == nullptr) return M2RNN_ERR_INVALID_ARG;
+  if (H == nullptr || (qk_heads != 1 && qk_heads != N)) return M2RNN_ERR_INVALID_ARG;
   if (dtype_ok(dtype) && dims_ok(B, 1, N, K, V) && decode_kernel_supported(static_cast<int>(K), static_cast<int>(V), dtype) &&
       kernel_override() < 0) {
     const void* req[] = {H, q, k, v, f, W, w_r, y};
@@ -211,11 +225,12 @@ int m2rnn_decode_step(float* H, const void* q, const void* k, const void* v, con
     if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < kStatusBytes)
       return M2RNN_ERR_WORKSPACE;
     return cuda_status(launch_decode_step(H, q, k, v, f, W, w_r, y, static_cast<int>(B), static_cast<int>(N),
-                                          static_cast<int>(K), static_cast<cudaStream_t>(cuda_stream)));
+                                          static_cast<int>(K), static_cast<int>(qk_heads),
+                                          static_cast<cudaStream_t>(cuda_stream)));
   }
   // Otherwise the scan kernels with T = 1, from H to H: every kernel reads a
   // state element before the same thread block overwrites it.
-  return m2rnn_forward_state(q, k, v, f, W, w_r, H, y, H, nullptr, 0, B, 1, N, K, V, dtype,
+  return m2rnn_forward_state(q, k, v, f, W, w_r, H, y, H, nullptr, 0, B, 1, N, qk_heads, K, V, dtype,
                              workspace, workspace_bytes, cuda_stream);
 }
 
@@ -223,9 +238,11 @@ int m2rnn_backward_state(const void* q, const void* k, const void* v, const void
                          const void* W, const void* w_r, const float* H_0, const float* dy,
                          const float* dH_T, const float* ckpt, int ckpt_every, float* dq,
                          float* dk, float* dv, float* df, float* dW, float* dw_r, float* dH_0,
-                         int64_t B, int64_t T, int64_t N, int64_t K, int64_t V, m2rnn_dtype dtype,
-                         void* workspace, size_t workspace_bytes, void* cuda_stream) {
+                         int64_t B, int64_t T, int64_t N, int64_t qk_heads, int64_t K, int64_t V,
+                         m2rnn_dtype dtype, void* workspace, size_t workspace_bytes, void* cuda_stream) {
   if (!dtype_ok(dtype) || !dims_ok(B, T, N, K, V)) return M2RNN_ERR_INVALID_ARG;
+  if (qk_heads != 1 && qk_heads != N) return M2RNN_ERR_INVALID_ARG;
+  const bool shared_qk = qk_heads == 1 && N > 1;
   const int path = choose_path(K, V, dtype);
   if (path < 0) return path;
   const int bpath = choose_bwd_path(K, V, dtype, ckpt_every);
@@ -236,7 +253,7 @@ int m2rnn_backward_state(const void* q, const void* k, const void* v, const void
   if ((dH_T && !aligned16(dH_T)) || (ckpt && !aligned16(ckpt)) || (H_0 && !aligned16(H_0)) ||
       (dH_0 && !aligned16(dH_0)))
     return M2RNN_ERR_INVALID_ARG;
-  const BwdLayout l = bwd_layout(B, T, N, K, V, dtype, ckpt_every, ckpt != nullptr);
+  const BwdLayout l = bwd_layout(B, T, N, K, V, dtype, ckpt_every, ckpt != nullptr, shared_qk);
   if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < l.total)
     return M2RNN_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
@@ -252,7 +269,7 @@ int m2rnn_backward_state(const void* q, const void* k, const void* v, const void
       // Checkpoint pass: the forward without the readout.
       FwdArgs fa{};
       fa.q = q; fa.k = k; fa.v = v; fa.f = f; fa.W = W; fa.w_r = w_r;
-      fa.H0 = H_0; fa.y = nullptr; fa.H_T = nullptr; fa.ckpt = ck;
+      fa.H0 = H_0; fa.qkN = static_cast<int>(qk_heads); fa.y = nullptr; fa.H_T = nullptr; fa.ckpt = ck;
       fa.ckpt_every = ckpt_every; fa.n_ckpt = nck;
       fa.B = static_cast<int>(B); fa.T = static_cast<int>(T); fa.N = static_cast<int>(N);
       fa.K = static_cast<int>(K); fa.V = static_cast<int>(V);
@@ -265,6 +282,13 @@ int m2rnn_backward_state(const void* q, const void* k, const void* v, const void
   a.q = q; a.k = k; a.v = v; a.f = f; a.W = W; a.w_r = w_r;
   a.dy = dy; a.dH_T = dH_T; a.H0 = H_0; a.ckpt = ck; a.ckpt_every = ckpt_every; a.n_ckpt = nck;
   a.dq = dq; a.dk = dk; a.dv = dv; a.df = df; a.dW = dW; a.dw_r = dw_r; a.dH0 = dH_0;
+  a.qkN = static_cast<int>(qk_heads);
+  float* dq_heads = reinterpret_cast<float*>(ws + l.qk_off);
+  float* dk_heads = dq_heads + B * T * N * K;
+  if (shared_qk) {  // per-head gradients first, summed over the heads below
+    a.dq = dq_heads;
+    a.dk = dk_heads;
+  }
   a.B = static_cast<int>(B); a.T = static_cast<int>(T); a.N = static_cast<int>(N);
   a.K = static_cast<int>(K); a.V = static_cast<int>(V);
   a.dtype = dtype; a.status = status;
@@ -279,6 +303,10 @@ int m2rnn_backward_state(const void* q, const void* k, const void* v, const void
   else
     e = launch_simt_backward(a, s);
   if (e != cudaSuccess) return M2RNN_ERR_CUDA;
+  if (shared_qk) {
+    e = launch_sum_qk_heads(dq_heads, dk_heads, dq, dk, B * T, static_cast<int>(N), static_cast<int>(K), s);
+    if (e != cudaSuccess) return M2RNN_ERR_CUDA;
+  }
   return cuda_status(launch_reduce_partials(a, s));
 }
 
@@ -288,7 +316,7 @@ int m2rnn_backward(const void* q, const void* k, const void* v, const void* f, c
                    float* dw_r, int64_t B, int64_t T, int64_t N, int64_t K, int64_t V,
                    m2rnn_dtype dtype, void* workspace, size_t workspace_bytes, void* cuda_stream) {
   return m2rnn_backward_state(q, k, v, f, W, w_r, nullptr, dy, dH_T, ckpt, ckpt_every, dq, dk, dv,
-                              df, dW, dw_r, nullptr, B, T, N, K, V, dtype, workspace,
+                              df, dW, dw_r, nullptr, B, T, N, N, K, V, dtype, workspace,
                               workspace_bytes, cuda_stream);
 }
 

@@ -29,7 +29,7 @@ constexpr int kMaxWarps = 8;  // K <= 128
 __global__ void __launch_bounds__(kMaxWarps * 32) decode_step_kernel(
     float* __restrict__ H, const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
     const uint16_t* __restrict__ v, const uint16_t* __restrict__ f, const uint16_t* __restrict__ W,
-    const uint16_t* __restrict__ w_r, float* __restrict__ y, int N, int K) {
+    const uint16_t* __restrict__ w_r, float* __restrict__ y, int N, int K, int qkN) {
   __shared__ float ypart[kMaxWarps][kV];
   __shared__ __align__(128) uint8_t wtile[4][2048];  // W as four 16 x 64 bf16 k-tiles (swizzled)
   const int chain = blockIdx.x, n = chain % N;
@@ -38,8 +38,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32) decode_step_kernel(
   const int nw = K / 16;
   const int64_t r0 = static_cast<int64_t>(chain) * K + 16 * warp;  // first state row of this warp
   const uint16_t* Wn = W + static_cast<int64_t>(n) * kV * kV;
-  const uint16_t* kc = k + static_cast<int64_t>(chain) * K;
-  const uint16_t* qc = q + static_cast<int64_t>(chain) * K;
+  const int64_t qkrow = static_cast<int64_t>(chain / N) * qk_heads(qkN, N) + qk_head(qkN, n);
+  const uint16_t* kc = k + qkrow * K;
+  const uint16_t* qc = q + qkrow * K;
   const uint16_t* vc = v + static_cast<int64_t>(chain) * kV;
   const float ft = bf16_bits_to_f32(f[chain]);
   const float omf = 1.f - ft;
@@ -125,11 +126,11 @@ bool decode_kernel_supported(int K, int V, m2rnn_dtype dtype) {
 }
 
 cudaError_t launch_decode_step(float* H, const void* q, const void* k, const void* v, const void* f,
-                               const void* W, const void* w_r, float* y, int B, int N, int K,
+                               const void* W, const void* w_r, float* y, int B, int N, int K, int qkN,
                                cudaStream_t stream) {
   decode_step_kernel<<<B * N, 32 * (K / 16), 0, stream>>>(
       H, static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v),
-      static_cast<const uint16_t*>(f), static_cast<const uint16_t*>(W), static_cast<const uint16_t*>(w_r), y, N, K);
+      static_cast<const uint16_t*>(f), static_cast<const uint16_t*>(W), static_cast<const uint16_t*>(w_r), y, N, K, qkN);
   return cudaGetLastError();
 }
 

@@ -19,6 +19,7 @@ struct FwdArgs {
   const void* W;
   const void* w_r;
   const float* H0;  // initial state [B,N,K,V] fp32; null = zero
+  int qkN;          // heads of q and k: 1 = one q/k shared by every head, else N
   float* y;      // may be null (checkpoint-only pass)
   float* H_T;    // may be null
   float* ckpt;   // may be null
@@ -40,6 +41,7 @@ struct BwdArgs {
   const float* dH_T;  // may be null
   const float* H0;    // initial state; null = zero
   float* dH0;         // gradient of the initial state; may be null
+  int qkN;            // heads of q and k (1 = shared); dq/dk are per head here either way
   const float* ckpt;  // never null here (recomputed by the caller layer if needed)
   int ckpt_every;
   int64_t n_ckpt;
@@ -70,11 +72,18 @@ cudaError_t launch_reduce_partials(const BwdArgs& a, cudaStream_t s);
 // Register-resident warp-MMA kernels (bf16 inputs, V = 64).
 bool mma_forward_supported(int K, int V);
 cudaError_t launch_mma_forward(const FwdArgs& a, cudaStream_t s);
+// Head of q/k that head n reads: 0 when one q/k is shared by every head.
+__host__ __device__ inline int qk_head(int qkN, int n) { return qkN == 1 ? 0 : n; }
+__host__ __device__ inline int qk_heads(int qkN, int N) { return qkN == 1 ? 1 : N; }
+
 // One decoding step (bf16, V = 64, K % 16 == 0, K <= 128), state in place.
 bool decode_kernel_supported(int K, int V, m2rnn_dtype dtype);
 cudaError_t launch_decode_step(float* H, const void* q, const void* k, const void* v, const void* f,
-                               const void* W, const void* w_r, float* y, int B, int N, int K,
+                               const void* W, const void* w_r, float* y, int B, int N, int K, int qkN,
                                cudaStream_t stream);
+// dq[b,t,0,:] = sum over heads n of dq_heads[b,t,n,:] (fixed order), same for dk.
+cudaError_t launch_sum_qk_heads(const float* dq_heads, const float* dk_heads, float* dq, float* dk,
+                                int64_t BT, int N, int K, cudaStream_t stream);
 
 bool mma_backward_supported(int K, int V);
 size_t mma_backward_scratch_bytes(int B, int T, int N, int K, int V, int ckpt_every);

@@ -413,8 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t fb = smem_u32(&cfull[li % kCBufs]);
       if (lane == 0) {
         mbar_expect_tx(fb, p.tx_bytes);
-        tma_load_4d(smem_u32(buf + p.cq_off), &tm_q, fb, cta_rank * kRows, n, t0, b);
-        tma_load_4d(smem_u32(buf + p.ck_off), &tm_k, fb, cta_rank * kRows, n, t0, b);
+        tma_load_4d(smem_u32(buf + p.cq_off), &tm_q, fb, cta_rank * kRows, qk_head(A.qkN, n), t0, b);
+        tma_load_4d(smem_u32(buf + p.ck_off), &tm_k, fb, cta_rank * kRows, qk_head(A.qkN, n), t0, b);
         tma_load_4d(smem_u32(buf + p.cv_off), &tm_v, fb, 0, n, t0, b);
         tma_load_4d(smem_u32(buf + p.cdy_off), &tm_dy, fb, 0, n, t0, b);
       }
@@ -798,8 +798,9 @@ cudaError_t launch_mma_backward(const BwdArgs& a, cudaStream_t stream) {
 
   CUtensorMap mq, mk, mv, mdy;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if (!make_tensor_map_btnx(&mq, a.q, bf, 2, a.B, a.T, a.N, a.K, kRows, C) ||
-      !make_tensor_map_btnx(&mk, a.k, bf, 2, a.B, a.T, a.N, a.K, kRows, C) ||
+  const int qN = qk_heads(a.qkN, a.N);
+  if (!make_tensor_map_btnx(&mq, a.q, bf, 2, a.B, a.T, qN, a.K, kRows, C) ||
+      !make_tensor_map_btnx(&mk, a.k, bf, 2, a.B, a.T, qN, a.K, kRows, C) ||
       !make_tensor_map_btnx(&mv, a.v, bf, 2, a.B, a.T, a.N, kV, kV, C) ||
       !make_tensor_map_btnx(&mdy, a.dy, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.B, a.T, a.N, kV, kV, C))
     return cudaErrorInvalidValue;

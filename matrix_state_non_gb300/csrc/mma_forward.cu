@@ -363,8 +363,8 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
       const uint32_t fb = smem_u32(&full[st]);
       if (lane == 0) {
         mbar_arrive_expect_tx(fb, p.tx_bytes);
-        tma_load_4d(smem_u32(stage + p.q_off), &tm_q, fb, cta_rank * kRows, n, t0, b);
-        tma_load_4d(smem_u32(stage + p.k_off), &tm_k, fb, cta_rank * kRows, n, t0, b);
+        tma_load_4d(smem_u32(stage + p.q_off), &tm_q, fb, cta_rank * kRows, qk_head(p.a.qkN, n), t0, b);
+        tma_load_4d(smem_u32(stage + p.k_off), &tm_k, fb, cta_rank * kRows, qk_head(p.a.qkN, n), t0, b);
         tma_load_4d(smem_u32(stage + p.v_off), &tm_v, fb, 0, n, t0, b);
       } else {
         mbar_arrive(fb);
@@ -447,8 +447,9 @@ cudaError_t launch_nt(const FwdArgs& a, cudaStream_t stream) {
 
   CUtensorMap mq, mk, mv;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if (!make_tensor_map_btnx(&mq, a.q, bf, 2, a.B, a.T, a.N, a.K, kRows, kS) ||
-      !make_tensor_map_btnx(&mk, a.k, bf, 2, a.B, a.T, a.N, a.K, kRows, kS) ||
+  const int qN = qk_heads(a.qkN, a.N);
+  if (!make_tensor_map_btnx(&mq, a.q, bf, 2, a.B, a.T, qN, a.K, kRows, kS) ||
+      !make_tensor_map_btnx(&mk, a.k, bf, 2, a.B, a.T, qN, a.K, kRows, kS) ||
       !make_tensor_map_btnx(&mv, a.v, bf, 2, a.B, a.T, a.N, kV, kV, kS))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(mma_forward_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -57,9 +57,10 @@ __global__ void __launch_bounds__(kThreads) simt_forward_kernel(FwdArgs a) {
   float* Hn = Hb;
   for (int t = 0; t < T; ++t) {
     const int64_t row = (static_cast<int64_t>(b) * T + t) * N + n;
+    const int64_t rowqk = (static_cast<int64_t>(b) * T + t) * qk_heads(a.qkN, N) + qk_head(a.qkN, n);
     for (int i = threadIdx.x; i < K; i += kThreads) {
-      ks[i] = ld_in(k, row * K + i);
-      qs[i] = ld_in(q, row * K + i);
+      ks[i] = ld_in(k, rowqk * K + i);
+      qs[i] = ld_in(q, rowqk * K + i);
     }
     for (int j = threadIdx.x; j < V; j += kThreads) vs[j] = ld_in(v, row * V + j);
     if (threadIdx.x == 0) fs[0] = ld_in(f, row);
@@ -163,7 +164,8 @@ __global__ void __launch_bounds__(kThreads) simt_backward_kernel(BwdArgs a) {
     __syncthreads();
     for (int s = 0; s < L; ++s) {
       const int64_t row = (static_cast<int64_t>(b) * T + s0 + s) * N + n;
-      for (int i = threadIdx.x; i < K; i += kThreads) ks[i] = ld_in(k, row * K + i);
+      const int64_t rowqk = (static_cast<int64_t>(b) * T + s0 + s) * qk_heads(a.qkN, N) + qk_head(a.qkN, n);
+      for (int i = threadIdx.x; i < K; i += kThreads) ks[i] = ld_in(k, rowqk * K + i);
       for (int j = threadIdx.x; j < V; j += kThreads) vs[j] = ld_in(v, row * V + j);
       if (threadIdx.x == 0) fs[0] = ld_in(f, row);
       __syncthreads();
@@ -184,9 +186,10 @@ __global__ void __launch_bounds__(kThreads) simt_backward_kernel(BwdArgs a) {
     // ---- reverse walk over the chunk ----
     for (int s = L - 1; s >= 0; --s) {
       const int64_t row = (static_cast<int64_t>(b) * T + s0 + s) * N + n;
+      const int64_t rowqk = (static_cast<int64_t>(b) * T + s0 + s) * qk_heads(a.qkN, N) + qk_head(a.qkN, n);
       for (int i = threadIdx.x; i < K; i += kThreads) {
-        ks[i] = ld_in(k, row * K + i);
-        qs[i] = ld_in(q, row * K + i);
+        ks[i] = ld_in(k, rowqk * K + i);
+        qs[i] = ld_in(q, rowqk * K + i);
       }
       for (int j = threadIdx.x; j < V; j += kThreads) {
         vs[j] = ld_in(v, row * V + j);
@@ -315,4 +318,32 @@ cudaError_t launch_reduce_partials(const BwdArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+}  // namespace m2rnn
+
+namespace m2rnn {
+namespace {
+__global__ void sum_qk_heads_kernel(const float* __restrict__ dqh, const float* __restrict__ dkh,
+                                    float* __restrict__ dq, float* __restrict__ dk, int64_t BT, int N, int K) {
+  const int64_t total = BT * K;
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t bt = e / K, i = e % K;
+    float sq = 0.f, sk = 0.f;
+    for (int n = 0; n < N; ++n) {  // fixed order over the heads
+      sq += dqh[(bt * N + n) * K + i];
+      sk += dkh[(bt * N + n) * K + i];
+    }
+    dq[e] = sq;
+    dk[e] = sk;
+  }
+}
+}  // namespace
+
+cudaError_t launch_sum_qk_heads(const float* dq_heads, const float* dk_heads, float* dq, float* dk,
+                                int64_t BT, int N, int K, cudaStream_t stream) {
+  const int64_t total = BT * K;
+  const int blocks = static_cast<int>(std::min<int64_t>((total + 255) / 256, 152 * 16));
+  sum_qk_heads_kernel<<<blocks, 256, 0, stream>>>(dq_heads, dk_heads, dq, dk, BT, N, K);
+  return cudaGetLastError();
+}
 }  // namespace m2rnn

@@ -361,8 +361,8 @@ __global__ void __launch_bounds__(352, 1)
       const uint32_t fb = smem_u32(&full[st]);
       if (lane == 0) {
         mbar_arrive_expect_tx(fb, p.tx_bytes);
-        tma_load_4d(smem_u32(stage + p.q_off), &tm_q, fb, cta_rank * NRtot, n, t0, b);
-        tma_load_4d(smem_u32(stage + p.k_off), &tm_k, fb, cta_rank * NRtot, n, t0, b);
+        tma_load_4d(smem_u32(stage + p.q_off), &tm_q, fb, cta_rank * NRtot, qk_head(p.a.qkN, n), t0, b);
+        tma_load_4d(smem_u32(stage + p.k_off), &tm_k, fb, cta_rank * NRtot, qk_head(p.a.qkN, n), t0, b);
         tma_load_4d(smem_u32(stage + p.v_off), &tm_v, fb, 0, n, t0, b);
       } else {
         mbar_arrive(fb);
@@ -473,8 +473,9 @@ cudaError_t launch_cfg(const FwdArgs& a, int G, int R, cudaStream_t stream) {
 
   CUtensorMap mq, mk, mv;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if (!make_tensor_map_btnx(&mq, a.q, bf, 2, a.B, a.T, a.N, a.K, p.NRtot, kS) ||
-      !make_tensor_map_btnx(&mk, a.k, bf, 2, a.B, a.T, a.N, a.K, p.NRtot, kS) ||
+  const int qN = qk_heads(a.qkN, a.N);
+  if (!make_tensor_map_btnx(&mq, a.q, bf, 2, a.B, a.T, qN, a.K, p.NRtot, kS) ||
+      !make_tensor_map_btnx(&mk, a.k, bf, 2, a.B, a.T, qN, a.K, p.NRtot, kS) ||
       !make_tensor_map_btnx(&mv, a.v, bf, 2, a.B, a.T, a.N, V, V, kS))
     return cudaErrorInvalidValue;
 

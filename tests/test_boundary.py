@@ -101,17 +101,24 @@ def test_backward_rejects_bad_arguments_without_a_device(lib):
 
 def test_state_entry_points_reject_bad_arguments_without_a_device(lib):
     # Misaligned initial state / state gradient, and a decode step without a state.
-    st = binding.m2rnn_forward_state(P, P, P, P, P, P, P + 4, P, None, None, 0, 1, 8, 1, 64, 64,
+    st = binding.m2rnn_forward_state(P, P, P, P, P, P, P + 4, P, None, None, 0, 1, 8, 1, 1, 64, 64,
                                      binding.M2RNN_BF16, P, 1 << 20, None)
     assert st == binding.M2RNN_ERR_INVALID_ARG
-    common = dict(B=1, T=8, N=1, K=64, V=64)
+    st = binding.m2rnn_forward_state(P, P, P, P, P, P, None, P, None, None, 0, 1, 8, 4, 2, 64, 64,
+                                     binding.M2RNN_BF16, P, 1 << 20, None)
+    assert st == binding.M2RNN_ERR_INVALID_ARG   # q/k heads must be 1 or N
+    assert binding.m2rnn_backward_state_workspace_size(1, 8, 4, 3, 64, 64, binding.M2RNN_BF16, 14, 1) == 0
+    shared = binding.m2rnn_backward_state_workspace_size(2, 8, 4, 1, 64, 64, binding.M2RNN_BF16, 14, 1)
+    per_head = binding.m2rnn_backward_state_workspace_size(2, 8, 4, 4, 64, 64, binding.M2RNN_BF16, 14, 1)
+    assert shared >= per_head + 2 * 4 * 2 * 8 * 4 * 64   # room for the per-head dq, dk
+    common = dict(B=1, T=8, N=1, QK=1, K=64, V=64)
     st = binding.m2rnn_backward_state(P, P, P, P, P, P, None, P, None, None, 14, P, P, P, P, P, P,
                                       P + 8, *common.values(), binding.M2RNN_BF16, P, 1 << 30, None)
     assert st == binding.M2RNN_ERR_INVALID_ARG
-    st = binding.m2rnn_decode_step(None, P, P, P, P, P, P, P, 1, 1, 64, 64, binding.M2RNN_BF16, P,
+    st = binding.m2rnn_decode_step(None, P, P, P, P, P, P, P, 1, 1, 1, 64, 64, binding.M2RNN_BF16, P,
                                    1 << 20, None)
     assert st == binding.M2RNN_ERR_INVALID_ARG
-    st = binding.m2rnn_decode_step(P, P, P, P, P, P, P, P, 1, 1, 64, 200, binding.M2RNN_BF16, P,
+    st = binding.m2rnn_decode_step(P, P, P, P, P, P, P, P, 1, 1, 1, 64, 200, binding.M2RNN_BF16, P,
                                    1 << 20, None)
     assert st == binding.M2RNN_ERR_UNSUPPORTED   # V above the supported 128
 

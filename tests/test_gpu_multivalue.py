@@ -1,0 +1,88 @@
+"""GPU parity for multi-value heads: one q/k shared by every value head
+(section 2.4 of the M2RNN reading notes; the paper's configuration uses
+K = 64, V = 16), with dq, dk summed over the heads (section 2.7).  Every
+kernel family against the float64 oracle."""
+import copy
+
+import numpy as np
+import pytest
+
+from matrix_state_non_gb300.inputs import make_inputs
+from oracle import backward as oracle_backward
+from oracle import forward as oracle_forward
+from parity_util import check_forward, check_grads, gpu_backward, gpu_forward, oracle_args
+
+pytestmark = pytest.mark.gpu
+
+
+def shared_inputs(B, N, T, K, V, dtype, seed, with_dy=False):
+    """Seeded inputs with q, k reduced to one head ([B,T,1,K])."""
+    inp = make_inputs(B, N, T, K, V, dtype, seed=seed, with_dy=with_dy)
+    out = copy.copy(inp)
+    out.store = dict(inp.store)
+    out.exact = dict(inp.exact)
+    for name in ("q", "k"):
+        out.store[name] = np.ascontiguousarray(inp.store[name][:, :, :1])
+        out.exact[name] = np.ascontiguousarray(inp.exact[name][:, :, :1])
+    return out
+
+
+@pytest.fixture
+def kernel_family(request, monkeypatch):
+    monkeypatch.setenv("M2RNN_KERNEL", request.param)
+    return request.param
+
+
+@pytest.mark.parametrize("kernel_family", ["mma", "tcgen05", "simt"], indirect=True)
+@pytest.mark.parametrize("B,N,T,K,V", [(2, 4, 37, 64, 64), (1, 3, 50, 32, 64)])
+def test_forward_shared_qk(kernel_family, B, N, T, K, V):
+    inp = shared_inputs(B, N, T, K, V, "bf16", seed=400 + T)
+    got = gpu_forward(inp, ckpt_every=16)
+    y_ref, H_ref = oracle_forward(*oracle_args(inp))
+    check_forward(got, y_ref, H_ref, "bf16", label=(kernel_family, B, N, T, K, V))
+
+
+@pytest.mark.parametrize("B,N,T,K,V,dtype", [(2, 8, 40, 64, 16, "bf16"), (1, 4, 30, 64, 16, "f32"),
+                                             (1, 2, 33, 128, 128, "bf16")])
+def test_forward_shared_qk_other_shapes(B, N, T, K, V, dtype):
+    """The paper's multi-value shape (K = 64, V = 16) and the wide heads."""
+    inp = shared_inputs(B, N, T, K, V, dtype, seed=410 + T)
+    got = gpu_forward(inp)
+    y_ref, H_ref = oracle_forward(*oracle_args(inp))
+    check_forward(got, y_ref, H_ref, dtype, label=(B, N, T, K, V, dtype))
+
+
+@pytest.mark.parametrize("kernel_family", ["mma", "simt"], indirect=True)
+@pytest.mark.parametrize("B,N,T,K,V,C", [(2, 4, 37, 64, 64, 14), (1, 3, 45, 32, 64, 28)])
+def test_backward_shared_qk(kernel_family, B, N, T, K, V, C):
+    inp = shared_inputs(B, N, T, K, V, "bf16", seed=420 + T, with_dy=True)
+    dH = np.random.default_rng(6).standard_normal((B, N, K, V)).astype(np.float32)
+    got = gpu_backward(inp, dH_T=dH, ckpt_every=C, use_fwd_ckpt=True)
+    ref = oracle_backward(*oracle_args(inp), inp.exact["dy"], dH.astype(np.float64))
+    assert got["dq"].shape == (B, T, 1, K) and got["dk"].shape == (B, T, 1, K)
+    check_grads(got, ref, "bf16", label=(kernel_family, B, N, T, K, V, C))
+
+
+@pytest.mark.parametrize("B,N,T,K,V,dtype", [(2, 8, 40, 64, 16, "bf16"), (1, 4, 30, 64, 16, "f32")])
+def test_backward_shared_qk_paper_shape(B, N, T, K, V, dtype):
+    inp = shared_inputs(B, N, T, K, V, dtype, seed=430 + T, with_dy=True)
+    got = gpu_backward(inp, ckpt_every=8)
+    ref = oracle_backward(*oracle_args(inp), inp.exact["dy"])
+    check_grads(got, ref, dtype, label=(B, N, T, K, V, dtype))
+
+
+@pytest.mark.parametrize("kernel_family", ["auto", "mma"], indirect=True)
+def test_decode_shared_qk(kernel_family):
+    import torch
+    from matrix_state_non_gb300 import binding
+    B, N, T, K, V = 2, 4, 10, 64, 64
+    inp = shared_inputs(B, N, T, K, V, "bf16", seed=440)
+    d = binding.to_device(inp)
+    H = torch.zeros((B, N, K, V), device="cuda", dtype=torch.float32)
+    ys = []
+    for t in range(T):
+        step = [d[n][:, t].contiguous() for n in ("q", "k", "v", "f")]
+        ys.append(binding.decode_step(H, *step, d["W"], d["w_r"]).cpu().numpy())
+    torch.cuda.synchronize()
+    y_ref, H_ref = oracle_forward(*oracle_args(inp))
+    check_forward({"y": np.stack(ys, axis=1), "H_T": H.cpu().numpy()}, y_ref, H_ref, "bf16")
