@@ -45,7 +45,7 @@ from matrix_state_non_gb300.inputs import WORKLOADS, make_workload  # noqa: E402
 METRIC = "M²RNN scan tokens·heads/s (fwd, fwd+bwd) and % of tensor/HBM roofline, 1 GB300"
 UNIT = "tokens*heads/s"
 MAIN = "fwdbwd_bf16_k64"
-FWD_EXTRA = ("fwd_bf16_k64", "fwd_bf16_k128", "fwd_bf16_16k")
+FWD_EXTRA = ("fwd_bf16_k64", "fwd_bf16_k128", "fwd_bf16_16k", "mv_bf16_k64v16")
 IN_NAMES = ("q", "k", "v", "f", "W", "w_r")
 GRADS = ("dq", "dk", "dv", "df", "dW", "dw_r")
 CKPT_EVERY = 14  # chunk length of the backward recompute (two chunk caches fit in TMEM)
@@ -79,14 +79,19 @@ def bwd_flops(w):
     return 4.0 * w["K"] * w["V"] ** 2 * units(w)
 
 
+def qk_share(w):
+    """Fraction of the q/k traffic per unit: 1/N when one q/k serves every head."""
+    return 1.0 / w["N"] if w.get("shared_qk") else 1.0
+
+
 def io_bytes_fwd(w, s_in=2):
     K, V = w["K"], w["V"]
-    return units(w) * ((2 * K + V + 1) * s_in + 4 * V)
+    return units(w) * ((2 * K * qk_share(w) + V + 1) * s_in + 4 * V)
 
 
 def io_bytes_bwd(w, s_in=2, ckpt_every=CKPT_EVERY):
     K, V = w["K"], w["V"]
-    per_unit = (2 * K + V + 1) * s_in + 4 * V + 4 * (2 * K + V + 1)
+    per_unit = (2 * K * qk_share(w) + V + 1) * s_in + 4 * V + 4 * (2 * K * qk_share(w) + V + 1)
     ck = 4.0 * K * V * units(w) / ckpt_every
     return units(w) * per_unit + ck
 
@@ -408,7 +413,18 @@ def run_gpu(args, dist):
                 os.environ.pop("M2RNN_KERNEL", None)
             else:
                 os.environ["M2RNN_KERNEL"] = prev
+        os.environ["M2RNN_KERNEL"] = "simt"  # the multi-value workload on the fp32 kernel, for comparison
+        try:
+            fwd_extra["mv_bf16_k64v16@simt"] = time_forward("mv_bf16_k64v16", binding, dev, stream, flush,
+                                                            pk, dist, reps=3)
+        finally:
+            if prev is None:
+                os.environ.pop("M2RNN_KERNEL", None)
+            else:
+                os.environ["M2RNN_KERNEL"] = prev
         fwd_extra["decode_bf16_k64"] = time_decode(binding, dev, stream, dist)
+        fwd_extra["mv_bf16_k64v16@fwd+bwd"] = time_fwdbwd("mv_bf16_k64v16", binding, dev, stream, flush, pk,
+                                                          dist)
     cpu = cpu_baseline_sample() if (dist.rank == 0 and not args.no_cpu) else None
     launches_per_step = 4  # forward scan, backward scan, dv/df row sums, dW/dw_r partial sums
     line = {
@@ -469,6 +485,49 @@ def time_forward(name, binding, dev, stream, flush, pk, dist, reps=5):
             "bound": "tensor" if t_tensor >= t_hbm else "hbm",
             "tensor_tflops": fl / (t * 1e-3) / 1e12,
             "peak_source": f"{pk['source']} bf16 burst / hbm copy"}
+
+
+def time_fwdbwd(name, binding, dev, stream, flush, pk, dist, reps=3):
+    """Forward (writing checkpoints) + backward of a training workload, per
+    step: the same protocol as the headline step, for another workload."""
+    import torch
+    w = WORKLOADS[name]
+    inp = make_workload(name)
+    d = binding.to_device(inp, dev)
+    fo = binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=CKPT_EVERY)
+    bo = binding.backward(*(d[n] for n in IN_NAMES), d["dy"], ckpt=fo["ckpt"], ckpt_every=CKPT_EVERY)
+
+    def step():
+        binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=CKPT_EVERY, out=fo, workspace=fo["workspace"])
+        binding.backward(*(d[n] for n in IN_NAMES), d["dy"], ckpt=fo["ckpt"], ckpt_every=CKPT_EVERY, out=bo,
+                         workspace=bo["workspace"])
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    ev = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        ev.append((a, b))
+    torch.cuda.synchronize(dev)
+    for out in (fo, bo):
+        st, detail = binding.sync_status(out["workspace"])
+        if st != binding.M2RNN_OK:
+            raise RuntimeError(f"{name}: device status {binding.status_string(st)} at {detail}")
+    t = dist.max(sum(a.elapsed_time(b) for a, b in ev) / reps)
+    fl = fwd_flops(w) + bwd_flops(w)
+    t_tensor = fl / (pk["bf16_sustained"] * 1e12)
+    t_hbm = (io_bytes_fwd(w) + io_bytes_bwd(w)) / (pk["hbm_gbs"] * 1e9)
+    del d, fo, bo
+    return {"workload": w["desc"], "kernel": "warp-mma (V = 16 register kernels)", "ms": t,
+            "value": dist.world * units(w) / (t * 1e-3), "unit": UNIT,
+            "ns_per_step_per_chain": t * 1e6 / w["T"],
+            "roofline_ms": max(t_tensor, t_hbm) * 1e3, "roofline_frac": max(t_tensor, t_hbm) / (t * 1e-3),
+            "bound": "tensor" if t_tensor >= t_hbm else "hbm"}
 
 
 def time_decode(binding, dev, stream, dist, steps=64):

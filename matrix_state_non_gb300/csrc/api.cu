@@ -70,7 +70,8 @@ int choose_bwd_path(int64_t K, int64_t V, int dt, int ckpt_every) {
   const int path = choose_path(K, V, dt);
   if (path < 0) return path;
   const int k = static_cast<int>(K), v = static_cast<int>(V);
-  const bool mma = mma_backward_supported(k, v) && ckpt_every <= mma_backward_max_chunk();
+  const bool mma = (v == 16) ? mv_backward_supported(k, v, ckpt_every)
+                             : mma_backward_supported(k, v) && ckpt_every <= mma_backward_max_chunk();
   const bool tc = tc_backward_supported(k, v);
   if (path == kPathMma && mma) return kPathMma;
   if (path == kPathTc && tc) return kPathTc;
@@ -226,6 +227,7 @@ int m2rnn_decode_step(float* H, const void* q, const void* k, const void* v, con
       return M2RNN_ERR_WORKSPACE;
     return cuda_status(launch_decode_step(H, q, k, v, f, W, w_r, y, static_cast<int>(B), static_cast<int>(N),
                                           static_cast<int>(K), static_cast<int>(qk_heads),
+                                          static_cast<StatusBlock*>(workspace),
                                           static_cast<cudaStream_t>(cuda_stream)));
   }
   // Otherwise the scan kernels with T = 1, from H to H: every kernel reads a

@@ -29,7 +29,13 @@ constexpr int kMaxWarps = 8;  // K <= 128
 __global__ void __launch_bounds__(kMaxWarps * 32) decode_step_kernel(
     float* __restrict__ H, const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
     const uint16_t* __restrict__ v, const uint16_t* __restrict__ f, const uint16_t* __restrict__ W,
-    const uint16_t* __restrict__ w_r, float* __restrict__ y, int N, int K, int qkN) {
+    const uint16_t* __restrict__ w_r, float* __restrict__ y, int N, int K, int qkN, StatusBlock* status) {
+  // Nothing in this kernel waits, so it has no device error to report: it
+  // only clears the caller's status block, as every call does.
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    status->code = 0u;
+    status->detail = 0u;
+  }
   __shared__ float ypart[kMaxWarps][kV];
   __shared__ __align__(128) uint8_t wtile[4][2048];  // W as four 16 x 64 bf16 k-tiles (swizzled)
   const int chain = blockIdx.x, n = chain % N;
@@ -127,10 +133,10 @@ bool decode_kernel_supported(int K, int V, m2rnn_dtype dtype) {
 
 cudaError_t launch_decode_step(float* H, const void* q, const void* k, const void* v, const void* f,
                                const void* W, const void* w_r, float* y, int B, int N, int K, int qkN,
-                               cudaStream_t stream) {
+                               StatusBlock* status, cudaStream_t stream) {
   decode_step_kernel<<<B * N, 32 * (K / 16), 0, stream>>>(
       H, static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v),
-      static_cast<const uint16_t*>(f), static_cast<const uint16_t*>(W), static_cast<const uint16_t*>(w_r), y, N, K, qkN);
+      static_cast<const uint16_t*>(f), static_cast<const uint16_t*>(W), static_cast<const uint16_t*>(w_r), y, N, K, qkN, status);
   return cudaGetLastError();
 }
 

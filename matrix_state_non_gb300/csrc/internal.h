@@ -80,10 +80,18 @@ __host__ __device__ inline int qk_heads(int qkN, int N) { return qkN == 1 ? 1 : 
 bool decode_kernel_supported(int K, int V, m2rnn_dtype dtype);
 cudaError_t launch_decode_step(float* H, const void* q, const void* k, const void* v, const void* f,
                                const void* W, const void* w_r, float* y, int B, int N, int K, int qkN,
-                               cudaStream_t stream);
+                               StatusBlock* status, cudaStream_t stream);
 // dq[b,t,0,:] = sum over heads n of dq_heads[b,t,n,:] (fixed order), same for dk.
 cudaError_t launch_sum_qk_heads(const float* dq_heads, const float* dk_heads, float* dq, float* dk,
                                 int64_t BT, int N, int K, cudaStream_t stream);
+
+// Register-resident forward for V = 16 (one warp per 16 key rows, no exchange).
+bool mv_forward_supported(int K, int V);
+cudaError_t launch_mv_forward(const FwdArgs& a, cudaStream_t s);
+
+// Register-resident backward for V = 16 (chunks of up to 32 steps, 16 with K > 64).
+bool mv_backward_supported(int K, int V, int ckpt_every);
+cudaError_t launch_mv_backward(const BwdArgs& a, cudaStream_t s);
 
 bool mma_backward_supported(int K, int V);
 size_t mma_backward_scratch_bytes(int B, int T, int N, int K, int V, int ckpt_every);

@@ -769,6 +769,7 @@ size_t mma_backward_scratch_bytes(int B, int T, int N, int K, int, int) {
 int mma_backward_max_chunk() { return kMaxChunk; }
 
 cudaError_t launch_mma_backward(const BwdArgs& a, cudaStream_t stream) {
+  if (a.V != kV) return launch_mv_backward(a, stream);  // V = 16: the register-resident kernel
   if (a.ckpt_every > kMaxChunk) return cudaErrorInvalidValue;
   MmaBwdParams p{};
   p.a = a;

@@ -474,11 +474,15 @@ cudaError_t launch_nt(const FwdArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
-bool mma_forward_supported(int K, int V) { return V == kV && K % kRows == 0 && K >= kRows && K <= 128; }
+// The warp-MMA family: V = 64 here, V = 16 in the register-resident kernel.
+bool mma_forward_supported(int K, int V) {
+  return (V == kV && K % kRows == 0 && K >= kRows && K <= 128) || mv_forward_supported(K, V);
+}
 
 // Tuning knob M2RNN_MMA_NT = 1 | 2: value-column tiles per compute warp
 // (1: eight compute warps, two per SM sub-partition; 2: four compute warps).
 cudaError_t launch_mma_forward(const FwdArgs& a, cudaStream_t stream) {
+  if (a.V != kV) return launch_mv_forward(a, stream);
   const char* e = std::getenv("M2RNN_MMA_NT");
   if (e != nullptr && e[0] == '1') return launch_nt<1>(a, stream);
   return launch_nt<2>(a, stream);

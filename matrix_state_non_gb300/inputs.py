@@ -33,6 +33,11 @@ WORKLOADS = {
                          desc="bf16 long-context forward B=2 heads=16 T=16384 K=64 V=64"),
     "fwdbwd_bf16_k64": dict(B=4, N=8, T=4096, K=64, V=64, dtype="bf16", backward=True, seed=4,
                             desc="bf16 forward+backward B=4 heads=8 T=4096 K=64 V=64"),
+    # Multi-value heads (the pages' K = 64, V = 16 per head, one q/k shared by
+    # every head) at the forward+backward workload's batch and length.
+    "mv_bf16_k64v16": dict(B=4, N=16, T=4096, K=64, V=16, dtype="bf16", backward=True, seed=5,
+                           shared_qk=True,
+                           desc="bf16 multi-value forward+backward B=4 heads=16 T=4096 K=64 V=16, shared q/k"),
 }
 
 
@@ -119,8 +124,13 @@ def make_inputs(B: int, N: int, T: int, K: int, V: int, dtype: str = "bf16",
 def make_workload(name: str, seed: Optional[int] = None) -> M2RNNInputs:
     """Inputs of one of the named workloads (seed defaults to the workload's own)."""
     w = WORKLOADS[name]
-    return make_inputs(w["B"], w["N"], w["T"], w["K"], w["V"], w["dtype"],
-                       seed=w["seed"] if seed is None else seed, with_dy=w["backward"])
+    inp = make_inputs(w["B"], w["N"], w["T"], w["K"], w["V"], w["dtype"],
+                      seed=w["seed"] if seed is None else seed, with_dy=w["backward"])
+    if w.get("shared_qk"):  # one q/k for every head: keep head 0 of the drawn q, k
+        for name_ in ("q", "k"):
+            inp.store[name_] = np.ascontiguousarray(inp.store[name_][:, :, :1])
+            inp.exact[name_] = np.ascontiguousarray(inp.exact[name_][:, :, :1])
+    return inp
 
 
 def from_exact(exact: dict, dtype: str) -> M2RNNInputs:

@@ -86,3 +86,37 @@ def test_decode_shared_qk(kernel_family):
     torch.cuda.synchronize()
     y_ref, H_ref = oracle_forward(*oracle_args(inp))
     check_forward({"y": np.stack(ys, axis=1), "H_T": H.cpu().numpy()}, y_ref, H_ref, "bf16")
+
+
+@pytest.mark.parametrize("shared", [True, False])
+@pytest.mark.parametrize("B,N,T,K", [(2, 4, 77, 64), (1, 3, 33, 16), (1, 2, 40, 128), (1, 1, 1, 64)])
+def test_forward_v16_register_kernel(shared, B, N, T, K):
+    """The V = 16 register-resident kernel (bf16): y, H_T and checkpoints
+    from a non-zero initial state, several tiles and a ragged last tile."""
+    V = 16
+    maker = shared_inputs if shared else (lambda *a, **kw: make_inputs(*a, **kw))
+    inp = maker(B, N, T, K, V, "bf16", seed=450 + T + K)
+    H0 = np.random.default_rng(T).uniform(-0.9, 0.9, (B, N, K, V)).astype(np.float32)
+    got = gpu_forward(inp, ckpt_every=8, H_0=H0)
+    y_ref, H_ref, Hs, _ = oracle_forward(*oracle_args(inp), return_states=True, H_0=H0.astype(np.float64))
+    check_forward(got, y_ref, H_ref, "bf16", label=(shared, B, N, T, K))
+    from parity_util import rel_fro
+    for c in range((T - 1) // 8):
+        assert rel_fro(got["ckpt"][:, :, c], Hs[(c + 1) * 8]) <= 1e-2
+
+
+@pytest.mark.parametrize("shared", [True, False])
+@pytest.mark.parametrize("B,N,T,K,C", [(2, 4, 45, 64, 8), (1, 3, 70, 16, 32), (1, 2, 33, 128, 16),
+                                       (1, 2, 5, 64, 1), (2, 2, 64, 32, 13)])
+def test_backward_v16_register_kernel(shared, B, N, T, K, C):
+    """The V = 16 register-resident backward (bf16): every gradient and dH_0
+    from a non-zero initial state, several chunks and a ragged first chunk."""
+    V = 16
+    maker = shared_inputs if shared else (lambda *a, **kw: make_inputs(*a, **kw))
+    inp = maker(B, N, T, K, V, "bf16", seed=460 + T + K + C, with_dy=True)
+    rng = np.random.default_rng(C)
+    H0 = rng.uniform(-0.9, 0.9, (B, N, K, V)).astype(np.float32)
+    dH = rng.standard_normal((B, N, K, V)).astype(np.float32)
+    got = gpu_backward(inp, dH_T=dH, ckpt_every=C, use_fwd_ckpt=(C % 2 == 0), H_0=H0, want_dH0=True)
+    ref = oracle_backward(*oracle_args(inp), inp.exact["dy"], dH.astype(np.float64), H_0=H0.astype(np.float64))
+    check_grads(got, ref, "bf16", label=(shared, B, N, T, K, C))
