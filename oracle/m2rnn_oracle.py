@@ -87,9 +87,15 @@ def forward(q, k, v, f, W, w_r, return_states: bool = False, H_0=None):
     return y, H
 
 
-def backward(q, k, v, f, W, w_r, dy, dH_T=None, H_0=None):
+def backward(q, k, v, f, W, w_r, dy, dH_T=None, H_0=None, state_grad_clip=None):
     """Gradients of L = sum(dy * y) + <dH_T, H_T> with respect to every input
     (and to the initial state H_0, zero if None).
+
+    ``state_grad_clip`` = c > 0 clips the recurrent state gradient at every
+    step of BPTT (section 2.3 of the notes: training clips the per-step state
+    gradient, separately from whole-model gradient clipping; the notes do not
+    say how): each newly formed C_{t-1} is clamped elementwise to [-c, c]
+    before it is used.  The results are then no longer the exact gradient.
 
     Follows the chain rule for Eq. 10-12 as derived in section 2.7 of the
     reading notes, with u_t the upstream gradient of the readout H_t^T q_t
@@ -141,6 +147,8 @@ def backward(q, k, v, f, W, w_r, dy, dH_T=None, H_0=None):
         dW += np.einsum("bnkm,bnkj->nmj", H_prev, D)
         dw_r += np.einsum("bnv,bnv->nv", u, vt)
         C = ft * R + np.matmul(D, Wt)
+        if state_grad_clip is not None and state_grad_clip > 0:
+            C = np.clip(C, -state_grad_clip, state_grad_clip)
     if shared:  # one q/k for every head: their gradients sum over the heads
         dq = dq.sum(axis=2, keepdims=True)
         dk = dk.sum(axis=2, keepdims=True)

@@ -516,3 +516,49 @@ def test_shared_qk_gradient_matches_finite_differences():
             xm[idx][mi] -= eps
             fd[mi] = (loss(*xp, dy) - loss(*xm, dy)) / (2 * eps)
         np.testing.assert_allclose(g[name], fd, rtol=2e-7, atol=2e-8, err_msg=name)
+
+
+# --------------------------------------------------------------------------
+# Per-step clipping of the recurrent state gradient (not an exact gradient)
+# --------------------------------------------------------------------------
+
+def test_state_grad_clip_large_is_exact_gradient():
+    args = _rand(B=2, N=2, T=7, K=3, V=4, seed=70)
+    dy = np.random.default_rng(16).standard_normal((2, 7, 2, 4))
+    g0 = backward(*args, dy)
+    g1 = backward(*args, dy, state_grad_clip=1e30)
+    for name in g0:
+        np.testing.assert_array_equal(g0[name], g1[name])
+
+
+def test_state_grad_clip_forget_one_by_hand():
+    """f = 1: D = 0, so C_{t-1} = clamp(C_t + q_t u_t^T) -- a clamped running
+    sum computed here by hand -- and dH_0 is its last value, dq_t = H_t u_t
+    with H_t = 0 (no input reaches the state), df_t = <R_t, -Z_t>."""
+    q, k, v, f, W, w_r = _rand(B=1, N=1, T=6, K=3, V=4, seed=71)
+    f = np.ones_like(f)
+    rng = np.random.default_rng(17)
+    dy = 3.0 * rng.standard_normal(v.shape)
+    dH_T = rng.standard_normal((1, 1, 3, 4))
+    c = 0.7
+    g = backward(q, k, v, f, W, w_r, dy, dH_T, state_grad_clip=c)
+    C = dH_T[0, 0].copy()
+    for t in range(5, -1, -1):
+        R = C + np.outer(q[0, t, 0], dy[0, t, 0])
+        np.testing.assert_allclose(g["df"][0, t, 0], -np.sum(R * np.tanh(np.outer(k[0, t, 0], v[0, t, 0]))),
+                                   rtol=1e-12, atol=1e-13)
+        C = np.minimum(np.maximum(R, -c), c)
+    np.testing.assert_allclose(g["dH_0"][0, 0], C, rtol=1e-13)
+    assert np.all(np.abs(g["dH_0"]) <= c)
+
+
+def test_state_grad_clip_bounds_every_state_gradient():
+    """With clipping, every C_t handed to the next step lies in [-c, c]: the
+    dq it produces (H_t u_t uses no C) is unchanged, while dH_0 is bounded."""
+    args = _rand(B=2, N=2, T=9, K=4, V=3, seed=72)
+    dy = 5.0 * np.random.default_rng(18).standard_normal((2, 9, 2, 3))
+    g0 = backward(*args, dy)
+    g1 = backward(*args, dy, state_grad_clip=0.05)
+    np.testing.assert_array_equal(g0["dq"], g1["dq"])
+    assert np.all(np.abs(g1["dH_0"]) <= 0.05)
+    assert not np.allclose(g0["dk"], g1["dk"])
