@@ -162,6 +162,11 @@ size_t m2rnn_backward_state_workspace_size(int64_t B, int64_t T, int64_t N,
  *   H_0  [B,N,K,V] fp32 (may be NULL = zero): the forward's initial state;
  *   dH_0 [B,N,K,V] fp32 (may be NULL): receives dL/dH_0, the state gradient
  *        carried one step past t = 1 (C_0 in the recursion above);
+ *   state_grad_clip: c > 0 clamps every newly formed state gradient C_{t-1}
+ *        elementwise to [-c, c] (per-step clipping of the recurrent state
+ *        gradient in BPTT, notes section 2.3; the result is then no longer
+ *        the exact gradient); 0 = off; negative or NaN is
+ *        M2RNN_ERR_INVALID_ARG;
  *   qk_heads: as for m2rnn_forward_state.  With a shared q/k (1), dq and dk
  *        are [B,T,1,K]: the per-head gradients summed over the heads in a
  *        fixed order (notes section 2.7).
@@ -174,10 +179,11 @@ int m2rnn_backward_state(const void* q, const void* k, const void* v,
                          const float* H_0, const float* dy, const float* dH_T,
                          const float* ckpt, int ckpt_every, float* dq,
                          float* dk, float* dv, float* df, float* dW,
-                         float* dw_r, float* dH_0, int64_t B, int64_t T,
-                         int64_t N, int64_t qk_heads, int64_t K, int64_t V,
-                         m2rnn_dtype dtype, void* workspace,
-                         size_t workspace_bytes, void* cuda_stream);
+                         float* dw_r, float* dH_0, float state_grad_clip,
+                         int64_t B, int64_t T, int64_t N, int64_t qk_heads,
+                         int64_t K, int64_t V, m2rnn_dtype dtype,
+                         void* workspace, size_t workspace_bytes,
+                         void* cuda_stream);
 
 /*
  * One decoding step for a batch of states (serving: one new token per

@@ -74,7 +74,7 @@ def load() -> ctypes.CDLL:
     lib.m2rnn_forward_state.restype = ci
     lib.m2rnn_forward_state.argtypes = [vp] * 10 + [ci] + [i64] * 6 + [ci, vp, sz, vp]
     lib.m2rnn_backward_state.restype = ci
-    lib.m2rnn_backward_state.argtypes = [vp] * 10 + [ci] + [vp] * 7 + [i64] * 6 + [ci, vp, sz, vp]
+    lib.m2rnn_backward_state.argtypes = [vp] * 10 + [ci] + [vp] * 7 + [ctypes.c_float] + [i64] * 6 + [ci, vp, sz, vp]
     lib.m2rnn_backward_state_workspace_size.restype = sz
     lib.m2rnn_backward_state_workspace_size.argtypes = [i64] * 6 + [ci, ci, ci]
     lib.m2rnn_decode_step.restype = ci
@@ -138,11 +138,11 @@ def m2rnn_backward_state_workspace_size(B, T, N, qk_heads, K, V, dtype, ckpt_eve
 
 
 def m2rnn_backward_state(q, k, v, f, W, w_r, H_0, dy, dH_T, ckpt, ckpt_every, dq, dk, dv, df, dW,
-                         dw_r, dH_0, B, T, N, qk_heads, K, V, dtype, workspace, workspace_bytes,
-                         stream) -> int:
+                         dw_r, dH_0, state_grad_clip, B, T, N, qk_heads, K, V, dtype, workspace,
+                         workspace_bytes, stream) -> int:
     return load().m2rnn_backward_state(q, k, v, f, W, w_r, H_0, dy, dH_T, ckpt, ckpt_every, dq, dk,
-                                       dv, df, dW, dw_r, dH_0, B, T, N, qk_heads, K, V, dtype,
-                                       workspace, workspace_bytes, stream)
+                                       dv, df, dW, dw_r, dH_0, state_grad_clip, B, T, N, qk_heads, K,
+                                       V, dtype, workspace, workspace_bytes, stream)
 
 
 def m2rnn_decode_step(H, q, k, v, f, W, w_r, y, B, N, qk_heads, K, V, dtype, workspace,
@@ -232,11 +232,13 @@ def forward(q, k, v, f, W, w_r, *, H_0=None, want_state: bool = True, ckpt_every
 
 
 def backward(q, k, v, f, W, w_r, dy, *, dH_T=None, H_0=None, want_dH0: bool = False, ckpt=None,
-             ckpt_every: int = 14, out=None, workspace=None, stream=None):
+             ckpt_every: int = 14, state_grad_clip: float = 0.0, out=None, workspace=None,
+             stream=None):
     """Backward scan on the GPU.  Returns dict(dq, dk, dv, df, dW, dw_r[, dH_0]).
 
     ``H_0`` is the forward's initial state (None = zero); ``ckpt``, if given,
-    must come from a forward with the same ``H_0``."""
+    must come from a forward with the same ``H_0``; ``state_grad_clip`` > 0
+    clamps every new state gradient C_{t-1} to [-c, c]."""
     import torch
     B, T, N, K, V, NQ = _shapes(q, v)
     dt = _dtype_code(q)
@@ -261,8 +263,9 @@ def backward(q, k, v, f, W, w_r, dy, *, dH_T=None, H_0=None, want_dH0: bool = Fa
         workspace = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
     st = m2rnn_backward_state(_ptr(q), _ptr(k), _ptr(v), _ptr(f), _ptr(W), _ptr(w_r), _ptr(H_0),
                               _ptr(dy), _ptr(dH_T), _ptr(ckpt), ckpt_every, _ptr(dq), _ptr(dk),
-                              _ptr(dv), _ptr(df), _ptr(dW), _ptr(dw_r), _ptr(dH_0), B, T, N, NQ, K,
-                              V, dt, _ptr(workspace), workspace.numel(), _stream_handle(stream))
+                              _ptr(dv), _ptr(df), _ptr(dW), _ptr(dw_r), _ptr(dH_0), float(state_grad_clip),
+                              B, T, N, NQ, K, V, dt, _ptr(workspace), workspace.numel(),
+                              _stream_handle(stream))
     _check(st, "m2rnn_backward_state")
     res = dict(dq=dq, dk=dk, dv=dv, df=df, dW=dW, dw_r=dw_r, workspace=workspace)
     if dH_0 is not None:

@@ -240,8 +240,10 @@ int m2rnn_backward_state(const void* q, const void* k, const void* v, const void
                          const void* W, const void* w_r, const float* H_0, const float* dy,
                          const float* dH_T, const float* ckpt, int ckpt_every, float* dq,
                          float* dk, float* dv, float* df, float* dW, float* dw_r, float* dH_0,
-                         int64_t B, int64_t T, int64_t N, int64_t qk_heads, int64_t K, int64_t V,
-                         m2rnn_dtype dtype, void* workspace, size_t workspace_bytes, void* cuda_stream) {
+                         float state_grad_clip, int64_t B, int64_t T, int64_t N, int64_t qk_heads,
+                         int64_t K, int64_t V, m2rnn_dtype dtype, void* workspace, size_t workspace_bytes,
+                         void* cuda_stream) {
+  if (!(state_grad_clip >= 0.f)) return M2RNN_ERR_INVALID_ARG;  // also rejects NaN
   if (!dtype_ok(dtype) || !dims_ok(B, T, N, K, V)) return M2RNN_ERR_INVALID_ARG;
   if (qk_heads != 1 && qk_heads != N) return M2RNN_ERR_INVALID_ARG;
   const bool shared_qk = qk_heads == 1 && N > 1;
@@ -284,6 +286,7 @@ int m2rnn_backward_state(const void* q, const void* k, const void* v, const void
   a.q = q; a.k = k; a.v = v; a.f = f; a.W = W; a.w_r = w_r;
   a.dy = dy; a.dH_T = dH_T; a.H0 = H_0; a.ckpt = ck; a.ckpt_every = ckpt_every; a.n_ckpt = nck;
   a.dq = dq; a.dk = dk; a.dv = dv; a.df = df; a.dW = dW; a.dw_r = dw_r; a.dH0 = dH_0;
+  a.clip = state_grad_clip;
   a.qkN = static_cast<int>(qk_heads);
   float* dq_heads = reinterpret_cast<float*>(ws + l.qk_off);
   float* dk_heads = dq_heads + B * T * N * K;
@@ -318,7 +321,7 @@ int m2rnn_backward(const void* q, const void* k, const void* v, const void* f, c
                    float* dw_r, int64_t B, int64_t T, int64_t N, int64_t K, int64_t V,
                    m2rnn_dtype dtype, void* workspace, size_t workspace_bytes, void* cuda_stream) {
   return m2rnn_backward_state(q, k, v, f, W, w_r, nullptr, dy, dH_T, ckpt, ckpt_every, dq, dk, dv,
-                              df, dW, dw_r, nullptr, B, T, N, N, K, V, dtype, workspace,
+                              df, dW, dw_r, nullptr, 0.f, B, T, N, N, K, V, dtype, workspace,
                               workspace_bytes, cuda_stream);
 }
 

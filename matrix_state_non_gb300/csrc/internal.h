@@ -42,6 +42,7 @@ struct BwdArgs {
   const float* H0;    // initial state; null = zero
   float* dH0;         // gradient of the initial state; may be null
   int qkN;            // heads of q and k (1 = shared); dq/dk are per head here either way
+  float clip;         // > 0: every new C_{t-1} clamped to [-clip, clip]; else no clipping
   const float* ckpt;  // never null here (recomputed by the caller layer if needed)
   int ckpt_every;
   int64_t n_ckpt;

@@ -336,6 +336,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();  // the tiles are read by the tensor core
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&xfull[xs]));
+        if (A.clip > 0.f) {  // per-step clipping of the state gradient
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nt][e] = fminf(fmaxf(acc[nt][e], -A.clip), A.clip);
+        }
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll

@@ -295,6 +295,12 @@ __global__ void __launch_bounds__((kMaxRB + 1) * 32, 1)
           }
         }
         if (lane == 0) part_df[s * R + w] = pf;
+        if (A.clip > 0.f) {  // per-step clipping of the state gradient
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nt][e] = fminf(fmaxf(acc[nt][e], -A.clip), A.clip);
+        }
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll

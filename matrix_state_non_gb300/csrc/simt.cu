@@ -238,7 +238,8 @@ __global__ void __launch_bounds__(kThreads) simt_backward_kernel(BwdArgs a) {
         const int i = e / V, m = e % V;
         float s3 = 0.f;
         for (int j = 0; j < V; ++j) s3 = fmaf(Dm[i * V + j], Ws[m * V + j], s3);  // D W^T
-        Cm[e] = ft * Cm[e] + s3;
+        const float cn = ft * Cm[e] + s3;
+        Cm[e] = (a.clip > 0.f) ? fminf(fmaxf(cn, -a.clip), a.clip) : cn;  // per-step clipping
       }
       __syncthreads();
     }

@@ -113,8 +113,13 @@ def test_state_entry_points_reject_bad_arguments_without_a_device(lib):
     assert shared >= per_head + 2 * 4 * 2 * 8 * 4 * 64   # room for the per-head dq, dk
     common = dict(B=1, T=8, N=1, QK=1, K=64, V=64)
     st = binding.m2rnn_backward_state(P, P, P, P, P, P, None, P, None, None, 14, P, P, P, P, P, P,
-                                      P + 8, *common.values(), binding.M2RNN_BF16, P, 1 << 30, None)
+                                      P + 8, 0.0, *common.values(), binding.M2RNN_BF16, P, 1 << 30, None)
     assert st == binding.M2RNN_ERR_INVALID_ARG
+    for bad_clip in (-1.0, float("nan")):
+        st = binding.m2rnn_backward_state(P, P, P, P, P, P, None, P, None, None, 14, P, P, P, P, P, P,
+                                          None, bad_clip, *common.values(), binding.M2RNN_BF16, P,
+                                          1 << 30, None)
+        assert st == binding.M2RNN_ERR_INVALID_ARG
     st = binding.m2rnn_decode_step(None, P, P, P, P, P, P, P, 1, 1, 1, 64, 64, binding.M2RNN_BF16, P,
                                    1 << 20, None)
     assert st == binding.M2RNN_ERR_INVALID_ARG

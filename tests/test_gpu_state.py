@@ -142,3 +142,20 @@ def test_decode_steps_follow_the_scan(kernel_family, K):
     np.testing.assert_allclose(H.cpu().numpy(), full["H_T"], rtol=0, atol=tol)
     y_ref, H_ref = oracle_forward(*oracle_args(inp), H_0=H0.astype(np.float64))
     check_forward({"y": np.stack(ys, axis=1), "H_T": H.cpu().numpy()}, y_ref, H_ref, "bf16")
+
+
+@pytest.mark.parametrize("kernel_family", ["mma", "simt"], indirect=True)
+@pytest.mark.parametrize("B,N,T,K,V,C", [(2, 2, 45, 64, 64, 14), (1, 3, 40, 64, 16, 8)])
+def test_backward_state_gradient_clipping(kernel_family, B, N, T, K, V, C):
+    """Per-step clipping of the state gradient against the oracle (a clip
+    level that binds on a sizeable share of the elements)."""
+    inp = make_inputs(B, N, T, K, V, "bf16", seed=370 + T + V, with_dy=True)
+    H0 = _state(B, N, K, V, seed=7)
+    clip = 0.5
+    got = gpu_backward(inp, ckpt_every=C, H_0=H0, want_dH0=True, state_grad_clip=clip)
+    ref = oracle_backward(*oracle_args(inp), inp.exact["dy"], None, H_0=H0.astype(np.float64),
+                          state_grad_clip=clip)
+    full = oracle_backward(*oracle_args(inp), inp.exact["dy"], None, H_0=H0.astype(np.float64))
+    assert np.mean(np.abs(full["dH_0"]) > clip) > 0.05  # the clip does bind
+    assert np.all(np.abs(got["dH_0"]) <= clip)
+    check_grads(got, ref, "bf16", label=(kernel_family, B, N, T, K, V, C))
