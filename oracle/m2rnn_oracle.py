@@ -162,3 +162,70 @@ def loss(q, k, v, f, W, w_r, dy, dH_T=None, H_0=None):
     if dH_T is not None:
         val += float(np.sum(_as64(dH_T) * H_T))
     return val
+
+
+# ---------------------------------------------------------------------------
+# Input-dependent forget gate (section 2.2 of the notes, the paper's
+# Eq. 13 and 17): f_{t,n} = (1 + exp(a_{t,n} + beta_n))^(-alpha_n)
+#                         = exp(-alpha_n * softplus(a_{t,n} + beta_n)),
+# alpha_n >= 0 keeps f in [0, 1]; alpha_n = 1 gives sigmoid(-a - beta).
+# ---------------------------------------------------------------------------
+
+def _softplus(x):
+    return np.logaddexp(0.0, x)
+
+
+def gate(a, alpha, beta):
+    """f [B,T,N] from the gate pre-activation a [B,T,N] and per-head alpha, beta [N]."""
+    a, alpha, beta = _as64(a), _as64(alpha), _as64(beta)
+    return np.exp(-alpha * _softplus(a + beta))
+
+
+def gate_backward(a, alpha, beta, df):
+    """Chain rule through the gate: with s = softplus(a + beta) and
+    ds/da = sigmoid(a + beta),
+        da = df * f * (-alpha) * sigmoid(a + beta)
+        dalpha = sum over b, t of df * f * (-s)
+        dbeta  = sum over b, t of da
+    Returns (da [B,T,N], dalpha [N], dbeta [N])."""
+    a, alpha, beta, df = _as64(a), _as64(alpha), _as64(beta), _as64(df)
+    x = a + beta
+    f = np.exp(-alpha * _softplus(x))
+    sig = 0.5 * (1.0 + np.tanh(0.5 * x))  # logistic function, overflow-free
+    da = df * f * (-alpha) * sig
+    dalpha = np.sum(df * f * (-_softplus(x)), axis=(0, 1))
+    dbeta = np.sum(da, axis=(0, 1))
+    return da, dalpha, dbeta
+
+
+# ---------------------------------------------------------------------------
+# Output path (section 2.3 of the notes, step 4): the readout is multiplied
+# by the output gate g_t first, then RMS-normalised over the full width of a
+# token, all heads together (Appendix C: the statistic spans every head's
+# elements, d = N V), with a per-channel weight w [N,V]:
+#     x = y * g,   s = (sum(x^2) / d + eps)^(-1/2),   out = w * x * s.
+# The notes omit the stabilising epsilon; it is added inside the root here.
+# Backward (Appendix C), with p = w * dout and r = sum(p * x):
+#     dx = s p - r s^3 x / d,   dy = dx * g,   dg = dx * y,
+#     dw = sum over b, t of dout * x * s.
+# ---------------------------------------------------------------------------
+
+def output_norm(y, g, w, eps=1e-6):
+    """out [B,T,N,V] from y, g [B,T,N,V] and w [N,V]."""
+    y, g, w = _as64(y), _as64(g), _as64(w)
+    x = y * g
+    d = x.shape[2] * x.shape[3]
+    s = (np.sum(x * x, axis=(2, 3), keepdims=True) / d + eps) ** -0.5
+    return w[None, None] * x * s
+
+
+def output_norm_backward(y, g, w, dout, eps=1e-6):
+    """Returns (dy, dg [B,T,N,V], dw [N,V])."""
+    y, g, w, dout = _as64(y), _as64(g), _as64(w), _as64(dout)
+    x = y * g
+    d = x.shape[2] * x.shape[3]
+    s = (np.sum(x * x, axis=(2, 3), keepdims=True) / d + eps) ** -0.5
+    p = w[None, None] * dout
+    r = np.sum(p * x, axis=(2, 3), keepdims=True)
+    dx = s * p - r * s ** 3 * x / d
+    return dx * g, dx * y, np.sum(dout * x * s, axis=(0, 1))

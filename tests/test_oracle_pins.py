@@ -562,3 +562,92 @@ def test_state_grad_clip_bounds_every_state_gradient():
     np.testing.assert_array_equal(g0["dq"], g1["dq"])
     assert np.all(np.abs(g1["dH_0"]) <= 0.05)
     assert not np.allclose(g0["dk"], g1["dk"])
+
+
+# --------------------------------------------------------------------------
+# The forget gate f = exp(-alpha softplus(a + beta)) (section 2.2)
+# --------------------------------------------------------------------------
+
+from oracle import gate, gate_backward  # noqa: E402
+
+
+def _gate_args(B=2, T=5, N=3, seed=80):
+    rng = np.random.default_rng(seed)
+    return rng.standard_normal((B, T, N)) * 2.0, rng.uniform(0.1, 2.0, N), rng.standard_normal(N)
+
+
+def test_gate_alpha_one_is_a_sigmoid():
+    """alpha = 1: f = (1 + e^{a+beta})^{-1} = sigmoid(-a - beta) (section 2.2)."""
+    a, _, beta = _gate_args()
+    f = gate(a, np.ones_like(beta), beta)
+    np.testing.assert_allclose(f, 1.0 / (1.0 + np.exp(a + beta)), rtol=1e-13)
+    assert np.all((f >= 0) & (f <= 1))
+
+
+def test_gate_power_form():
+    """The two printed forms agree: (1 + e^{a+beta})^{-alpha}."""
+    a, alpha, beta = _gate_args(seed=81)
+    np.testing.assert_allclose(gate(a, alpha, beta), (1.0 + np.exp(a + beta)) ** (-alpha), rtol=1e-12)
+
+
+def test_gated_scan_gradient_matches_finite_differences():
+    """Through the gate and the scan: central differences of the loss with
+    f = gate(a, alpha, beta) with respect to a, alpha and beta."""
+    q, k, v, _, W, w_r = _rand(B=1, N=2, T=4, K=3, V=2, seed=82)
+    a, alpha, beta = _gate_args(B=1, T=4, N=2, seed=83)
+    dy = np.random.default_rng(19).standard_normal(v.shape)
+
+    def L(a_, al_, be_):
+        return loss(q, k, v, gate(a_, al_, be_), W, w_r, dy)
+
+    df = backward(q, k, v, gate(a, alpha, beta), W, w_r, dy)["df"]
+    da, dal, dbe = gate_backward(a, alpha, beta, df)
+    eps = 1e-6
+    for x, g_an, name in ((a, da, "a"), (alpha, dal, "alpha"), (beta, dbe, "beta")):
+        fd = np.zeros_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            mi = it.multi_index
+            xp, xm = x.copy(), x.copy()
+            xp[mi] += eps
+            xm[mi] -= eps
+            args_p = [xp if y is x else y for y in (a, alpha, beta)]
+            args_m = [xm if y is x else y for y in (a, alpha, beta)]
+            fd[mi] = (L(*args_p) - L(*args_m)) / (2 * eps)
+        np.testing.assert_allclose(g_an, fd, rtol=2e-7, atol=2e-8, err_msg=name)
+
+
+# --------------------------------------------------------------------------
+# Output gate and RMSNorm over the full width (section 2.3, Appendix C)
+# --------------------------------------------------------------------------
+
+from oracle import output_norm, output_norm_backward  # noqa: E402
+
+
+def test_output_norm_is_torch_rms_norm():
+    """Reduces to a library routine: torch's RMSNorm over the last N*V values
+    of y * g, with the per-channel weight, forward and autograd backward."""
+    rng = np.random.default_rng(90)
+    B, T, N, V = 2, 3, 4, 5
+    y, g = rng.standard_normal((B, T, N, V)), rng.standard_normal((B, T, N, V))
+    w, dout = rng.standard_normal((N, V)), rng.standard_normal((B, T, N, V))
+    eps = 1e-5
+    ty, tg, tw = (torch.tensor(x, requires_grad=True) for x in (y, g, w))
+    tout = torch.nn.functional.rms_norm((ty * tg).reshape(B, T, N * V), (N * V,), tw.reshape(N * V), eps)
+    np.testing.assert_allclose(output_norm(y, g, w, eps), tout.detach().numpy().reshape(B, T, N, V), rtol=1e-12)
+    (tout * torch.from_numpy(dout).reshape(B, T, N * V)).sum().backward()
+    dy, dg, dw = output_norm_backward(y, g, w, dout, eps)
+    np.testing.assert_allclose(dy, ty.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dg, tg.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dw, tw.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_output_norm_scale_invariance():
+    """With eps = 0 the output does not change when y is scaled (and is
+    unit-RMS before the weight)."""
+    rng = np.random.default_rng(91)
+    y, g = rng.standard_normal((1, 2, 3, 4)), rng.standard_normal((1, 2, 3, 4))
+    w = np.ones((3, 4))
+    o1 = output_norm(y, g, w, eps=0.0)
+    np.testing.assert_allclose(output_norm(7.5 * y, g, w, eps=0.0), o1, rtol=1e-13)
+    np.testing.assert_allclose(np.mean(o1 ** 2, axis=(2, 3)), 1.0, rtol=1e-13)
