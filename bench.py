@@ -40,7 +40,8 @@ import numpy as np  # noqa: E402
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from matrix_state_non_gb300.inputs import WORKLOADS, make_workload  # noqa: E402
+from matrix_state_non_gb300.inputs import (WORKLOADS, make_gate_inputs, make_norm_inputs,  # noqa: E402
+                                           make_workload)
 
 METRIC = "M²RNN scan tokens·heads/s (fwd, fwd+bwd) and % of tensor/HBM roofline, 1 GB300"
 UNIT = "tokens*heads/s"
@@ -425,6 +426,7 @@ def run_gpu(args, dist):
         fwd_extra["decode_bf16_k64"] = time_decode(binding, dev, stream, dist)
         fwd_extra["mv_bf16_k64v16@fwd+bwd"] = time_fwdbwd("mv_bf16_k64v16", binding, dev, stream, flush, pk,
                                                           dist)
+        fwd_extra["gated_block_bf16_k64"] = time_gated_block(binding, dev, stream, flush, pk, dist)
     cpu = cpu_baseline_sample() if (dist.rank == 0 and not args.no_cpu) else None
     launches_per_step = 4  # forward scan, backward scan, dv/df row sums, dW/dw_r partial sums
     line = {
@@ -528,6 +530,98 @@ def time_fwdbwd(name, binding, dev, stream, flush, pk, dist, reps=3):
             "ns_per_step_per_chain": t * 1e6 / w["T"],
             "roofline_ms": max(t_tensor, t_hbm) * 1e3, "roofline_frac": max(t_tensor, t_hbm) / (t * 1e-3),
             "bound": "tensor" if t_tensor >= t_hbm else "hbm"}
+
+
+def time_gated_block(binding, dev, stream, flush, pk, dist, reps=3):
+    """The fwd+bwd workload with the forget gate computed in the scan kernels
+    from (a, alpha, beta) and the gated RMSNorm output path around it: gated
+    forward, output norm, its backward (whose dy feeds the scan), gated
+    backward (da, dalpha, dbeta).  Each piece timed with events inside one
+    step; the two norm kernels also timed alone after an L2 flush, against
+    the HBM roofline of their algorithmic bytes."""
+    import torch
+    w = WORKLOADS[MAIN]
+    B, T, N, K, V = w["B"], w["T"], w["N"], w["K"], w["V"]
+    inp = make_workload(MAIN)
+    d = binding.to_device(inp, dev)
+    gs, _ = make_gate_inputs(B, T, N, "bf16", seed=w["seed"] + 100)
+    ns, _ = make_norm_inputs(B, T, N, V, "bf16", seed=w["seed"] + 101)
+    up = {n: binding.to_device(_Store(x), dev)["x"] for n, x in list(gs.items()) + list(ns.items())}
+    gate = (up["a"], up["alpha"], up["beta"])
+    args = (d["q"], d["k"], d["v"], None, d["W"], d["w_r"])
+    fo = binding.forward(*args, gate=gate, ckpt_every=CKPT_EVERY)
+    out = binding.output_norm(fo["y"], up["g"], up["w"])
+    nb = binding.output_norm_backward(fo["y"], up["g"], up["w"], up["dout"])
+    bo = binding.backward(*args, nb["dy"], gate=gate, ckpt=fo["ckpt"], ckpt_every=CKPT_EVERY)
+    nws = torch.empty(binding.m2rnn_output_norm_backward_workspace_size(B, T, N, V), device=dev,
+                      dtype=torch.uint8)
+
+    def norm_fwd():
+        binding.output_norm(fo["y"], up["g"], up["w"], out=out)
+
+    def norm_bwd():
+        binding.output_norm_backward(fo["y"], up["g"], up["w"], up["dout"], out=nb, workspace=nws)
+
+    def step(evs=None):
+        rec = (lambda i: evs[i].record(stream)) if evs else (lambda i: None)
+        rec(0)
+        binding.forward(*args, gate=gate, ckpt_every=CKPT_EVERY, out=fo, workspace=fo["workspace"])
+        rec(1)
+        norm_fwd()
+        rec(2)
+        norm_bwd()
+        rec(3)
+        binding.backward(*args, nb["dy"], gate=gate, ckpt=fo["ckpt"], ckpt_every=CKPT_EVERY, out=bo,
+                         workspace=bo["workspace"])
+        rec(4)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    runs = []
+    for _ in range(reps):
+        flush.zero_()
+        evs = [mk() for _ in range(5)]
+        step(evs)
+        runs.append(evs)
+    alone = {}
+    for name, fn in (("norm_fwd", norm_fwd), ("norm_bwd", norm_bwd)):
+        pairs = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = mk(), mk()
+            a.record(stream)
+            fn()
+            b.record(stream)
+            pairs.append((a, b))
+        alone[name] = pairs
+    torch.cuda.synchronize(dev)
+    for o in (fo, bo):
+        st, detail = binding.sync_status(o["workspace"])
+        if st != binding.M2RNN_OK:
+            raise RuntimeError(f"gated block: device status {binding.status_string(st)} at {detail}")
+    piece = lambda i: dist.max(sum(e[i].elapsed_time(e[i + 1]) for e in runs) / reps)  # noqa: E731
+    ms = {"gated_forward": piece(0), "norm_forward": piece(1), "norm_backward": piece(2),
+          "gated_backward": piece(3)}
+    total = sum(ms.values())
+    elems = B * T * N * V
+    nbytes = {"norm_fwd": elems * (4 + 2 + 4) + N * V * 4, "norm_bwd": elems * (4 + 2 + 4 + 4 + 4) + N * V * 4}
+    alone_ms = {k: dist.max(sum(a.elapsed_time(b) for a, b in v) / reps) for k, v in alone.items()}
+    norm = {k: {"ms": alone_ms[k], "bytes": nbytes[k],
+                "achieved_gbs": nbytes[k] / (alone_ms[k] * 1e-3) / 1e9,
+                "hbm_frac": nbytes[k] / (alone_ms[k] * 1e-3) / (pk["hbm_gbs"] * 1e9)} for k in alone_ms}
+    del d, fo, bo, out, nb
+    return {"workload": w["desc"] + ", gate from (a, alpha, beta) in-kernel, RMSNorm(y*g) over N*V",
+            "ms": total, "value": dist.world * units(w) / (total * 1e-3), "unit": UNIT, "pieces_ms": ms,
+            "norm_alone_after_l2_flush": norm}
+
+
+class _Store:
+    """Adapter so binding.to_device uploads one array."""
+
+    def __init__(self, x):
+        self.store = {"x": x}
 
 
 def time_decode(binding, dev, stream, dist, steps=64):

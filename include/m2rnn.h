@@ -32,9 +32,10 @@
  *  - Supported shapes: B, T, N >= 1; K, V in [1, 128].  bf16 inputs with
  *    K a multiple of 16 (and at most 128) run on tensor-core kernels: V = 64
  *    on the warp-MMA scans (the backward for ckpt_every <= 28, its dW on
- *    tcgen05), V = 128 (forward, K in {32, 64, 128}) on tcgen05.  Every
- *    other supported shape runs on the fp32 CUDA-core kernels.  Nothing runs
- *    on the host CPU.
+ *    tcgen05), V = 16 on register-resident warp-MMA scans (the backward for
+ *    ckpt_every <= 32, <= 16 with K > 64), V = 128 (forward, K in
+ *    {32, 64, 128}) on tcgen05.  Every other supported shape runs on the
+ *    fp32 CUDA-core kernels.  Nothing runs on the host CPU.
  */
 #ifndef M2RNN_H_
 #define M2RNN_H_
@@ -186,6 +187,83 @@ int m2rnn_backward_state(const void* q, const void* k, const void* v,
                          void* cuda_stream);
 
 /*
+ * Forward scan with the forget gate computed inside the scan kernels from its
+ * pre-activation (reading notes, section 2.2; the paper's Eq. 13 and 17):
+ *     f_t = (1 + exp(a_t + beta))^(-alpha) = exp(-alpha softplus(a_t + beta))
+ * per head, in fp32.  As m2rnn_forward_state with f replaced by
+ *   a     [B,T,N] in `dtype`: the gate pre-activation;
+ *   alpha [N] fp32 (alpha >= 0 keeps f in (0, 1]), beta [N] fp32.
+ * `ckpt` from this call serves m2rnn_backward_gated with the same a, alpha,
+ * beta.  Workspace: m2rnn_forward_workspace_size bytes.
+ */
+int m2rnn_forward_gated(const void* q, const void* k, const void* v,
+                        const void* a, const float* alpha, const float* beta,
+                        const void* W, const void* w_r, const float* H_0,
+                        float* y, float* H_T, float* ckpt, int ckpt_every,
+                        int64_t B, int64_t T, int64_t N, int64_t qk_heads,
+                        int64_t K, int64_t V, m2rnn_dtype dtype,
+                        void* workspace, size_t workspace_bytes,
+                        void* cuda_stream);
+
+/*
+ * Backward of m2rnn_forward_gated: as m2rnn_backward_state, with the gate
+ * gradient taken through to its parameters.  With x = a + beta and
+ * s = softplus(x):
+ *   da     [B,T,N] fp32 = df f (-alpha) sigmoid(x);
+ *   dalpha [N] fp32     = sum over b, t of df f (-s);
+ *   dbeta  [N] fp32     = sum over b, t of da;
+ * sums in a fixed order.  Workspace: m2rnn_backward_state_workspace_size
+ * bytes.
+ */
+int m2rnn_backward_gated(const void* q, const void* k, const void* v,
+                         const void* a, const float* alpha, const float* beta,
+                         const void* W, const void* w_r, const float* H_0,
+                         const float* dy, const float* dH_T, const float* ckpt,
+                         int ckpt_every, float* dq, float* dk, float* dv,
+                         float* da, float* dalpha, float* dbeta, float* dW,
+                         float* dw_r, float* dH_0, float state_grad_clip,
+                         int64_t B, int64_t T, int64_t N, int64_t qk_heads,
+                         int64_t K, int64_t V, m2rnn_dtype dtype,
+                         void* workspace, size_t workspace_bytes,
+                         void* cuda_stream);
+
+/*
+ * Output path of the block (reading notes, section 2.3, step 4): the readout
+ * y is multiplied by the output gate g first, then RMS-normalised over the
+ * full width of a token, all heads together (d = N V; the statistic spans
+ * every head, notes Appendix C), with a per-channel weight w:
+ *     x = y (*) g,   s = (sum_j x_j^2 / d + eps)^(-1/2),   out = w (*) x s.
+ *   y   [B,T,N,V] fp32 (the scan's output);  g [B,T,N,V] in `dtype`;
+ *   w   [N,V] fp32;  eps >= 0 (the notes omit it; it sits inside the root);
+ *   out [B,T,N,V] fp32;  rstd [B,T] fp32 (may be NULL): receives s.
+ * N V <= 16384.  No workspace; the status block is not used.
+ */
+int m2rnn_output_norm(const float* y, const void* g, const float* w, float eps,
+                      float* out, float* rstd, int64_t B, int64_t T,
+                      int64_t N, int64_t V, m2rnn_dtype dtype,
+                      void* cuda_stream);
+
+/* Bytes of device workspace m2rnn_output_norm_backward needs (per-block
+ * partial sums of dw), 0 for an unsupported shape. */
+size_t m2rnn_output_norm_backward_workspace_size(int64_t B, int64_t T,
+                                                 int64_t N, int64_t V);
+
+/*
+ * Backward of m2rnn_output_norm (notes Appendix C, with the epsilon kept):
+ * with p = w (*) dout and r = sum_j p_j x_j per token,
+ *     dx = s p - r s^3 x / d,   dy = dx (*) g,   dg = dx (*) y,
+ *     dw = sum over b, t of dout (*) x s   (fixed order).
+ * dout, dy, dg [B,T,N,V] fp32; dw [N,V] fp32; other arguments as for
+ * m2rnn_output_norm.  dy feeds m2rnn_backward_state / _gated as its dy.
+ */
+int m2rnn_output_norm_backward(const float* y, const void* g, const float* w,
+                               const float* dout, float eps, float* dy,
+                               float* dg, float* dw, int64_t B, int64_t T,
+                               int64_t N, int64_t V, m2rnn_dtype dtype,
+                               void* workspace, size_t workspace_bytes,
+                               void* cuda_stream);
+
+/*
  * One decoding step for a batch of states (serving: one new token per
  * (b, head)): H [B,N,K,V] fp32 is updated in place to H_t from H_{t-1}, and
  * y [B,N,V] fp32 receives y_t.  q, k [B,qk_heads,K]; v [B,N,V]; f [B,N];
@@ -245,9 +323,9 @@ int m2rnn_backward_noalloc(const void* q, const void* k, const void* v,
                            int64_t K, int64_t V, m2rnn_dtype dtype, int sync,
                            void* cuda_stream);
 
-/* Which kernel family a call with these arguments would run:
- * 1 = tensor-core (tcgen05) kernels, 0 = fp32 CUDA-core kernels,
- * negative = the status the call would return. */
+/* Which forward kernel family a call with these arguments would run:
+ * 2 = warp-MMA tensor-core kernels, 1 = tcgen05 tensor-core kernels,
+ * 0 = fp32 CUDA-core kernels, negative = the status the call would return. */
 int m2rnn_path(int64_t K, int64_t V, m2rnn_dtype dtype);
 
 #ifdef __cplusplus

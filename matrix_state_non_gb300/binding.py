@@ -30,7 +30,9 @@ EXPORTS = (
     "m2rnn_version", "m2rnn_status_string", "m2rnn_checkpoint_count", "m2rnn_path",
     "m2rnn_forward_workspace_size", "m2rnn_backward_workspace_size", "m2rnn_forward",
     "m2rnn_backward", "m2rnn_sync_status", "m2rnn_forward_state", "m2rnn_backward_state",
-    "m2rnn_decode_step", "m2rnn_backward_state_workspace_size",
+    "m2rnn_decode_step", "m2rnn_backward_state_workspace_size", "m2rnn_forward_gated",
+    "m2rnn_backward_gated", "m2rnn_output_norm", "m2rnn_output_norm_backward_workspace_size",
+    "m2rnn_output_norm_backward",
 )
 
 _lib = None
@@ -79,6 +81,17 @@ def load() -> ctypes.CDLL:
     lib.m2rnn_backward_state_workspace_size.argtypes = [i64] * 6 + [ci, ci, ci]
     lib.m2rnn_decode_step.restype = ci
     lib.m2rnn_decode_step.argtypes = [vp] * 8 + [i64] * 5 + [ci, vp, sz, vp]
+    fl = ctypes.c_float
+    lib.m2rnn_forward_gated.restype = ci
+    lib.m2rnn_forward_gated.argtypes = [vp] * 12 + [ci] + [i64] * 6 + [ci, vp, sz, vp]
+    lib.m2rnn_backward_gated.restype = ci
+    lib.m2rnn_backward_gated.argtypes = [vp] * 12 + [ci] + [vp] * 9 + [fl] + [i64] * 6 + [ci, vp, sz, vp]
+    lib.m2rnn_output_norm.restype = ci
+    lib.m2rnn_output_norm.argtypes = [vp] * 3 + [fl] + [vp] * 2 + [i64] * 4 + [ci, vp]
+    lib.m2rnn_output_norm_backward_workspace_size.restype = sz
+    lib.m2rnn_output_norm_backward_workspace_size.argtypes = [i64] * 4
+    lib.m2rnn_output_norm_backward.restype = ci
+    lib.m2rnn_output_norm_backward.argtypes = [vp] * 4 + [fl] + [vp] * 3 + [i64] * 4 + [ci, vp, sz, vp]
     _lib = lib
     return lib
 
@@ -151,6 +164,34 @@ def m2rnn_decode_step(H, q, k, v, f, W, w_r, y, B, N, qk_heads, K, V, dtype, wor
                                     workspace_bytes, stream)
 
 
+def m2rnn_forward_gated(q, k, v, a, alpha, beta, W, w_r, H_0, y, H_T, ckpt, ckpt_every, B, T, N, qk_heads,
+                        K, V, dtype, workspace, workspace_bytes, stream) -> int:
+    return load().m2rnn_forward_gated(q, k, v, a, alpha, beta, W, w_r, H_0, y, H_T, ckpt, ckpt_every, B, T,
+                                      N, qk_heads, K, V, dtype, workspace, workspace_bytes, stream)
+
+
+def m2rnn_backward_gated(q, k, v, a, alpha, beta, W, w_r, H_0, dy, dH_T, ckpt, ckpt_every, dq, dk, dv, da,
+                         dalpha, dbeta, dW, dw_r, dH_0, state_grad_clip, B, T, N, qk_heads, K, V, dtype,
+                         workspace, workspace_bytes, stream) -> int:
+    return load().m2rnn_backward_gated(q, k, v, a, alpha, beta, W, w_r, H_0, dy, dH_T, ckpt, ckpt_every, dq,
+                                       dk, dv, da, dalpha, dbeta, dW, dw_r, dH_0, state_grad_clip, B, T, N,
+                                       qk_heads, K, V, dtype, workspace, workspace_bytes, stream)
+
+
+def m2rnn_output_norm(y, g, w, eps, out, rstd, B, T, N, V, dtype, stream) -> int:
+    return load().m2rnn_output_norm(y, g, w, eps, out, rstd, B, T, N, V, dtype, stream)
+
+
+def m2rnn_output_norm_backward_workspace_size(B, T, N, V) -> int:
+    return load().m2rnn_output_norm_backward_workspace_size(B, T, N, V)
+
+
+def m2rnn_output_norm_backward(y, g, w, dout, eps, dy, dg, dw, B, T, N, V, dtype, workspace,
+                               workspace_bytes, stream) -> int:
+    return load().m2rnn_output_norm_backward(y, g, w, dout, eps, dy, dg, dw, B, T, N, V, dtype, workspace,
+                                             workspace_bytes, stream)
+
+
 def m2rnn_sync_status(workspace, stream):
     """Returns (status, detail)."""
     d = ctypes.c_uint32(0)
@@ -193,12 +234,14 @@ def _shapes(q, v):
 
 
 def forward(q, k, v, f, W, w_r, *, H_0=None, want_state: bool = True, ckpt_every: int = 0,
-            out=None, workspace=None, stream=None):
+            gate=None, out=None, workspace=None, stream=None):
     """Forward scan on the GPU from ``H_0`` (fp32 [B,N,K,V]; None = zero).
     Returns dict(y, H_T[, ckpt]).
 
     ``ckpt_every`` > 0 also writes the checkpoints the backward can reuse.
-    ``out`` may hold preallocated y / H_T / ckpt tensors.
+    ``gate`` = (a, alpha, beta) with ``f`` None computes the forget gate in
+    the kernels (m2rnn_forward_gated).  ``out`` may hold preallocated y /
+    H_T / ckpt tensors.
     """
     import torch
     B, T, N, K, V, NQ = _shapes(q, v)
@@ -220,11 +263,20 @@ def forward(q, k, v, f, W, w_r, *, H_0=None, want_state: bool = True, ckpt_every
         raise M2RNNError(M2RNN_ERR_INVALID_ARG, "m2rnn_forward_workspace_size")
     if workspace is None:
         workspace = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
-    st = m2rnn_forward_state(_ptr(q), _ptr(k), _ptr(v), _ptr(f), _ptr(W), _ptr(w_r), _ptr(H_0),
-                             _ptr(y), _ptr(H_T), _ptr(ckpt), ckpt_every if ckpt is not None else 0,
-                             B, T, N, NQ, K, V, dt, _ptr(workspace), workspace.numel(),
-                             _stream_handle(stream))
-    _check(st, "m2rnn_forward_state")
+    ce = ckpt_every if ckpt is not None else 0
+    if gate is not None:
+        if f is not None:
+            raise ValueError("give either f or gate=(a, alpha, beta), not both")
+        a, alpha, beta = gate
+        st = m2rnn_forward_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(alpha), _ptr(beta), _ptr(W),
+                                 _ptr(w_r), _ptr(H_0), _ptr(y), _ptr(H_T), _ptr(ckpt), ce, B, T, N, NQ, K,
+                                 V, dt, _ptr(workspace), workspace.numel(), _stream_handle(stream))
+        _check(st, "m2rnn_forward_gated")
+    else:
+        st = m2rnn_forward_state(_ptr(q), _ptr(k), _ptr(v), _ptr(f), _ptr(W), _ptr(w_r), _ptr(H_0),
+                                 _ptr(y), _ptr(H_T), _ptr(ckpt), ce, B, T, N, NQ, K, V, dt,
+                                 _ptr(workspace), workspace.numel(), _stream_handle(stream))
+        _check(st, "m2rnn_forward_state")
     res = dict(y=y, H_T=H_T, workspace=workspace)
     if ckpt is not None:
         res["ckpt"] = ckpt
@@ -232,13 +284,15 @@ def forward(q, k, v, f, W, w_r, *, H_0=None, want_state: bool = True, ckpt_every
 
 
 def backward(q, k, v, f, W, w_r, dy, *, dH_T=None, H_0=None, want_dH0: bool = False, ckpt=None,
-             ckpt_every: int = 14, state_grad_clip: float = 0.0, out=None, workspace=None,
+             ckpt_every: int = 14, state_grad_clip: float = 0.0, gate=None, out=None, workspace=None,
              stream=None):
-    """Backward scan on the GPU.  Returns dict(dq, dk, dv, df, dW, dw_r[, dH_0]).
+    """Backward scan on the GPU.  Returns dict(dq, dk, dv, df, dW, dw_r[, dH_0]);
+    with ``gate`` = (a, alpha, beta) (and ``f`` None) da, dalpha, dbeta
+    replace df.
 
     ``H_0`` is the forward's initial state (None = zero); ``ckpt``, if given,
-    must come from a forward with the same ``H_0``; ``state_grad_clip`` > 0
-    clamps every new state gradient C_{t-1} to [-c, c]."""
+    must come from a forward with the same ``H_0`` (and gate); ``state_grad_clip``
+    > 0 clamps every new state gradient C_{t-1} to [-c, c]."""
     import torch
     B, T, N, K, V, NQ = _shapes(q, v)
     dt = _dtype_code(q)
@@ -252,7 +306,7 @@ def backward(q, k, v, f, W, w_r, dy, *, dH_T=None, H_0=None, want_dH0: bool = Fa
     dq = _get("dq", (B, T, NQ, K))
     dk = _get("dk", (B, T, NQ, K))
     dv = _get("dv", (B, T, N, V))
-    df = _get("df", (B, T, N))
+    df = _get("df", (B, T, N)) if gate is None else None
     dW = _get("dW", (N, V, V))
     dw_r = _get("dw_r", (N, V))
     dH_0 = _get("dH_0", (B, N, K, V)) if want_dH0 else None
@@ -261,13 +315,29 @@ def backward(q, k, v, f, W, w_r, dy, *, dH_T=None, H_0=None, want_dH0: bool = Fa
         raise M2RNNError(M2RNN_ERR_INVALID_ARG, "m2rnn_backward_state_workspace_size")
     if workspace is None or workspace.numel() < ws_bytes:
         workspace = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
-    st = m2rnn_backward_state(_ptr(q), _ptr(k), _ptr(v), _ptr(f), _ptr(W), _ptr(w_r), _ptr(H_0),
-                              _ptr(dy), _ptr(dH_T), _ptr(ckpt), ckpt_every, _ptr(dq), _ptr(dk),
-                              _ptr(dv), _ptr(df), _ptr(dW), _ptr(dw_r), _ptr(dH_0), float(state_grad_clip),
-                              B, T, N, NQ, K, V, dt, _ptr(workspace), workspace.numel(),
-                              _stream_handle(stream))
-    _check(st, "m2rnn_backward_state")
-    res = dict(dq=dq, dk=dk, dv=dv, df=df, dW=dW, dw_r=dw_r, workspace=workspace)
+    if gate is not None:
+        if f is not None:
+            raise ValueError("give either f or gate=(a, alpha, beta), not both")
+        a, alpha, beta = gate
+        da = _get("da", (B, T, N))
+        dalpha = _get("dalpha", (N,))
+        dbeta = _get("dbeta", (N,))
+        st = m2rnn_backward_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(alpha), _ptr(beta), _ptr(W),
+                                  _ptr(w_r), _ptr(H_0), _ptr(dy), _ptr(dH_T), _ptr(ckpt), ckpt_every,
+                                  _ptr(dq), _ptr(dk), _ptr(dv), _ptr(da), _ptr(dalpha), _ptr(dbeta), _ptr(dW),
+                                  _ptr(dw_r), _ptr(dH_0), float(state_grad_clip), B, T, N, NQ, K, V, dt,
+                                  _ptr(workspace), workspace.numel(), _stream_handle(stream))
+        _check(st, "m2rnn_backward_gated")
+        res = dict(dq=dq, dk=dk, dv=dv, da=da, dalpha=dalpha, dbeta=dbeta, dW=dW, dw_r=dw_r,
+                   workspace=workspace)
+    else:
+        st = m2rnn_backward_state(_ptr(q), _ptr(k), _ptr(v), _ptr(f), _ptr(W), _ptr(w_r), _ptr(H_0),
+                                  _ptr(dy), _ptr(dH_T), _ptr(ckpt), ckpt_every, _ptr(dq), _ptr(dk),
+                                  _ptr(dv), _ptr(df), _ptr(dW), _ptr(dw_r), _ptr(dH_0),
+                                  float(state_grad_clip), B, T, N, NQ, K, V, dt, _ptr(workspace),
+                                  workspace.numel(), _stream_handle(stream))
+        _check(st, "m2rnn_backward_state")
+        res = dict(dq=dq, dk=dk, dv=dv, df=df, dW=dW, dw_r=dw_r, workspace=workspace)
     if dH_0 is not None:
         res["dH_0"] = dH_0
     return res
@@ -293,6 +363,48 @@ def decode_step(H, q, k, v, f, W, w_r, *, y=None, workspace=None, stream=None):
                            _stream_handle(stream))
     _check(st, "m2rnn_decode_step")
     return y
+
+
+def output_norm(y, g, w, *, eps: float = 1e-6, want_rstd: bool = False, out=None, stream=None):
+    """out = w * (y*g) * rms^-1 over each token's N*V elements; y fp32
+    [B,T,N,V], g [B,T,N,V] (bf16 or fp32), w fp32 [N,V].  Returns out, or
+    (out, rstd [B,T]) with ``want_rstd``."""
+    import torch
+    B, T, N, V = y.shape
+    if out is None:
+        out = torch.empty((B, T, N, V), device=y.device, dtype=torch.float32)
+    rstd = torch.empty((B, T), device=y.device, dtype=torch.float32) if want_rstd else None
+    st = m2rnn_output_norm(_ptr(y), _ptr(g), _ptr(w), float(eps), _ptr(out), _ptr(rstd), B, T, N, V,
+                           _dtype_code(g), _stream_handle(stream))
+    _check(st, "m2rnn_output_norm")
+    return (out, rstd) if want_rstd else out
+
+
+def output_norm_backward(y, g, w, dout, *, eps: float = 1e-6, out=None, workspace=None, stream=None):
+    """Returns dict(dy, dg [B,T,N,V], dw [N,V]) of ``output_norm``; ``out``
+    may hold preallocated dy / dg / dw."""
+    import torch
+    B, T, N, V = y.shape
+    dev = y.device
+    out = dict(out or {})
+
+    def _get(name, shape):
+        t = out.get(name)
+        return t if t is not None else torch.empty(shape, device=dev, dtype=torch.float32)
+
+    dy = _get("dy", (B, T, N, V))
+    dg = _get("dg", (B, T, N, V))
+    dw = _get("dw", (N, V))
+    ws_bytes = m2rnn_output_norm_backward_workspace_size(B, T, N, V)
+    if ws_bytes == 0:
+        raise M2RNNError(M2RNN_ERR_UNSUPPORTED, "m2rnn_output_norm_backward_workspace_size")
+    if workspace is None or workspace.numel() < ws_bytes:
+        workspace = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
+    st = m2rnn_output_norm_backward(_ptr(y), _ptr(g), _ptr(w), _ptr(dout), float(eps), _ptr(dy), _ptr(dg),
+                                    _ptr(dw), B, T, N, V, _dtype_code(g), _ptr(workspace), workspace.numel(),
+                                    _stream_handle(stream))
+    _check(st, "m2rnn_output_norm_backward")
+    return dict(dy=dy, dg=dg, dw=dw)
 
 
 def sync_status(workspace, stream=None):

@@ -8,6 +8,7 @@
 #include <cstdlib>
 #include <cstring>
 
+#include "gate.cuh"
 #include "internal.h"
 
 using namespace m2rnn;
@@ -171,18 +172,35 @@ size_t m2rnn_backward_state_workspace_size(int64_t B, int64_t T, int64_t N, int6
   return bwd_layout(B, T, N, K, V, dtype, ckpt_every, have_ckpt != 0, qk_heads == 1 && N > 1).total;
 }
 
-int m2rnn_forward_state(const void* q, const void* k, const void* v, const void* f, const void* W,
-                        const void* w_r, const float* H_0, float* y, float* H_T, float* ckpt,
-                        int ckpt_every, int64_t B, int64_t T, int64_t N, int64_t qk_heads, int64_t K,
-                        int64_t V, m2rnn_dtype dtype, void* workspace, size_t workspace_bytes,
-                        void* cuda_stream) {
+}  // extern "C"
+
+namespace {
+
+// The forget gate as the caller gives it: f itself, or (a, alpha, beta).
+struct GateIn {
+  const void* f;
+  const void* a;
+  const float* alpha;
+  const float* beta;
+  bool ok() const {
+    if (a == nullptr) return f != nullptr && aligned16(f);
+    return f == nullptr && aligned16(a) && alpha != nullptr && beta != nullptr && aligned16(alpha) &&
+           aligned16(beta);
+  }
+};
+
+int forward_impl(const void* q, const void* k, const void* v, const GateIn& gate, const void* W,
+                 const void* w_r, const float* H_0, float* y, float* H_T, float* ckpt, int ckpt_every,
+                 int64_t B, int64_t T, int64_t N, int64_t qk_heads, int64_t K, int64_t V, m2rnn_dtype dtype,
+                 void* workspace, size_t workspace_bytes, void* cuda_stream) {
   if (!dtype_ok(dtype) || !dims_ok(B, T, N, K, V)) return M2RNN_ERR_INVALID_ARG;
   if (qk_heads != 1 && qk_heads != N) return M2RNN_ERR_INVALID_ARG;
   const int path = choose_path(K, V, dtype);
   if (path < 0) return path;
-  const void* req[] = {q, k, v, f, W, w_r, y};
+  const void* req[] = {q, k, v, W, w_r, y};
   for (const void* p : req)
     if (p == nullptr || !aligned16(p)) return M2RNN_ERR_INVALID_ARG;
+  if (!gate.ok()) return M2RNN_ERR_INVALID_ARG;
   if ((H_T && !aligned16(H_T)) || (ckpt && !aligned16(ckpt)) || (H_0 && !aligned16(H_0)))
     return M2RNN_ERR_INVALID_ARG;
   if (ckpt && (ckpt_every < 1 || ckpt_every > kMaxCkptEvery)) return M2RNN_ERR_INVALID_ARG;
@@ -193,7 +211,8 @@ int m2rnn_forward_state(const void* q, const void* k, const void* v, const void*
   cudaError_t e = cudaMemsetAsync(status, 0, kStatusBytes, s);
   if (e != cudaSuccess) return M2RNN_ERR_CUDA;
   FwdArgs a{};
-  a.q = q; a.k = k; a.v = v; a.f = f; a.W = W; a.w_r = w_r;
+  a.q = q; a.k = k; a.v = v; a.f = gate.f; a.W = W; a.w_r = w_r;
+  a.gate_a = gate.a; a.gate_alpha = gate.alpha; a.gate_beta = gate.beta;
   a.H0 = H_0; a.qkN = static_cast<int>(qk_heads); a.y = y; a.H_T = H_T; a.ckpt = ckpt;
   a.ckpt_every = ckpt ? ckpt_every : 1;
   a.n_ckpt = ckpt ? (T - 1) / ckpt_every : 0;
@@ -203,6 +222,30 @@ int m2rnn_forward_state(const void* q, const void* k, const void* v, const void*
   a.status = status;
   e = launch_forward_path(path, a, s);
   return cuda_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int m2rnn_forward_state(const void* q, const void* k, const void* v, const void* f, const void* W,
+                        const void* w_r, const float* H_0, float* y, float* H_T, float* ckpt,
+                        int ckpt_every, int64_t B, int64_t T, int64_t N, int64_t qk_heads, int64_t K,
+                        int64_t V, m2rnn_dtype dtype, void* workspace, size_t workspace_bytes,
+                        void* cuda_stream) {
+  if (f == nullptr) return M2RNN_ERR_INVALID_ARG;
+  return forward_impl(q, k, v, GateIn{f, nullptr, nullptr, nullptr}, W, w_r, H_0, y, H_T, ckpt, ckpt_every, B, T,
+                      N, qk_heads, K, V, dtype, workspace, workspace_bytes, cuda_stream);
+}
+
+int m2rnn_forward_gated(const void* q, const void* k, const void* v, const void* a, const float* alpha,
+                        const float* beta, const void* W, const void* w_r, const float* H_0, float* y,
+                        float* H_T, float* ckpt, int ckpt_every, int64_t B, int64_t T, int64_t N,
+                        int64_t qk_heads, int64_t K, int64_t V, m2rnn_dtype dtype, void* workspace,
+                        size_t workspace_bytes, void* cuda_stream) {
+  if (a == nullptr) return M2RNN_ERR_INVALID_ARG;
+  return forward_impl(q, k, v, GateIn{nullptr, a, alpha, beta}, W, w_r, H_0, y, H_T, ckpt, ckpt_every, B, T, N,
+                      qk_heads, K, V, dtype, workspace, workspace_bytes, cuda_stream);
 }
 
 int m2rnn_forward(const void* q, const void* k, const void* v, const void* f, const void* W,
@@ -236,13 +279,18 @@ int m2rnn_decode_step(float* H, const void* q, const void* k, const void* v, con
                              workspace, workspace_bytes, cuda_stream);
 }
 
-int m2rnn_backward_state(const void* q, const void* k, const void* v, const void* f,
-                         const void* W, const void* w_r, const float* H_0, const float* dy,
-                         const float* dH_T, const float* ckpt, int ckpt_every, float* dq,
-                         float* dk, float* dv, float* df, float* dW, float* dw_r, float* dH_0,
-                         float state_grad_clip, int64_t B, int64_t T, int64_t N, int64_t qk_heads,
-                         int64_t K, int64_t V, m2rnn_dtype dtype, void* workspace, size_t workspace_bytes,
-                         void* cuda_stream) {
+}  // extern "C"
+
+namespace {
+
+// df receives the gradient of f; with a gate given as (a, alpha, beta) it
+// then becomes da in place, and dalpha, dbeta [N] are written.
+int backward_impl(const void* q, const void* k, const void* v, const GateIn& gate, const void* W,
+                  const void* w_r, const float* H_0, const float* dy, const float* dH_T, const float* ckpt,
+                  int ckpt_every, float* dq, float* dk, float* dv, float* df, float* dalpha, float* dbeta,
+                  float* dW, float* dw_r, float* dH_0, float state_grad_clip, int64_t B, int64_t T, int64_t N,
+                  int64_t qk_heads, int64_t K, int64_t V, m2rnn_dtype dtype, void* workspace,
+                  size_t workspace_bytes, void* cuda_stream) {
   if (!(state_grad_clip >= 0.f)) return M2RNN_ERR_INVALID_ARG;  // also rejects NaN
   if (!dtype_ok(dtype) || !dims_ok(B, T, N, K, V)) return M2RNN_ERR_INVALID_ARG;
   if (qk_heads != 1 && qk_heads != N) return M2RNN_ERR_INVALID_ARG;
@@ -251,9 +299,12 @@ int m2rnn_backward_state(const void* q, const void* k, const void* v, const void
   if (path < 0) return path;
   const int bpath = choose_bwd_path(K, V, dtype, ckpt_every);
   if (ckpt_every < 1 || ckpt_every > kMaxCkptEvery) return M2RNN_ERR_INVALID_ARG;
-  const void* req[] = {q, k, v, f, W, w_r, dy, dq, dk, dv, df, dW, dw_r};
+  const void* req[] = {q, k, v, W, w_r, dy, dq, dk, dv, df, dW, dw_r};
   for (const void* p : req)
     if (p == nullptr || !aligned16(p)) return M2RNN_ERR_INVALID_ARG;
+  if (!gate.ok()) return M2RNN_ERR_INVALID_ARG;
+  if (gate.a != nullptr && (dalpha == nullptr || dbeta == nullptr || !aligned16(dalpha) || !aligned16(dbeta)))
+    return M2RNN_ERR_INVALID_ARG;
   if ((dH_T && !aligned16(dH_T)) || (ckpt && !aligned16(ckpt)) || (H_0 && !aligned16(H_0)) ||
       (dH_0 && !aligned16(dH_0)))
     return M2RNN_ERR_INVALID_ARG;
@@ -272,7 +323,8 @@ int m2rnn_backward_state(const void* q, const void* k, const void* v, const void
     if (nck > 0) {
       // Checkpoint pass: the forward without the readout.
       FwdArgs fa{};
-      fa.q = q; fa.k = k; fa.v = v; fa.f = f; fa.W = W; fa.w_r = w_r;
+      fa.q = q; fa.k = k; fa.v = v; fa.f = gate.f; fa.W = W; fa.w_r = w_r;
+      fa.gate_a = gate.a; fa.gate_alpha = gate.alpha; fa.gate_beta = gate.beta;
       fa.H0 = H_0; fa.qkN = static_cast<int>(qk_heads); fa.y = nullptr; fa.H_T = nullptr; fa.ckpt = ck;
       fa.ckpt_every = ckpt_every; fa.n_ckpt = nck;
       fa.B = static_cast<int>(B); fa.T = static_cast<int>(T); fa.N = static_cast<int>(N);
@@ -283,7 +335,8 @@ int m2rnn_backward_state(const void* q, const void* k, const void* v, const void
     }
   }
   BwdArgs a{};
-  a.q = q; a.k = k; a.v = v; a.f = f; a.W = W; a.w_r = w_r;
+  a.q = q; a.k = k; a.v = v; a.f = gate.f; a.W = W; a.w_r = w_r;
+  a.gate_a = gate.a; a.gate_alpha = gate.alpha; a.gate_beta = gate.beta;
   a.dy = dy; a.dH_T = dH_T; a.H0 = H_0; a.ckpt = ck; a.ckpt_every = ckpt_every; a.n_ckpt = nck;
   a.dq = dq; a.dk = dk; a.dv = dv; a.df = df; a.dW = dW; a.dw_r = dw_r; a.dH0 = dH_0;
   a.clip = state_grad_clip;
@@ -312,7 +365,77 @@ int m2rnn_backward_state(const void* q, const void* k, const void* v, const void
     e = launch_sum_qk_heads(dq_heads, dk_heads, dq, dk, B * T, static_cast<int>(N), static_cast<int>(K), s);
     if (e != cudaSuccess) return M2RNN_ERR_CUDA;
   }
-  return cuda_status(launch_reduce_partials(a, s));
+  e = launch_reduce_partials(a, s);
+  if (e != cudaSuccess) return M2RNN_ERR_CUDA;
+  if (gate.a != nullptr) {
+    const GateSrc gs{nullptr, gate.a, gate.alpha, gate.beta, dtype == M2RNN_BF16};
+    e = launch_gate_backward(gs, df, dalpha, dbeta, B * T, static_cast<int>(N), s);
+  }
+  return cuda_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int m2rnn_backward_state(const void* q, const void* k, const void* v, const void* f,
+                         const void* W, const void* w_r, const float* H_0, const float* dy,
+                         const float* dH_T, const float* ckpt, int ckpt_every, float* dq,
+                         float* dk, float* dv, float* df, float* dW, float* dw_r, float* dH_0,
+                         float state_grad_clip, int64_t B, int64_t T, int64_t N, int64_t qk_heads,
+                         int64_t K, int64_t V, m2rnn_dtype dtype, void* workspace, size_t workspace_bytes,
+                         void* cuda_stream) {
+  if (f == nullptr) return M2RNN_ERR_INVALID_ARG;
+  return backward_impl(q, k, v, GateIn{f, nullptr, nullptr, nullptr}, W, w_r, H_0, dy, dH_T, ckpt, ckpt_every,
+                       dq, dk, dv, df, nullptr, nullptr, dW, dw_r, dH_0, state_grad_clip, B, T, N, qk_heads, K,
+                       V, dtype, workspace, workspace_bytes, cuda_stream);
+}
+
+int m2rnn_backward_gated(const void* q, const void* k, const void* v, const void* a, const float* alpha,
+                         const float* beta, const void* W, const void* w_r, const float* H_0, const float* dy,
+                         const float* dH_T, const float* ckpt, int ckpt_every, float* dq, float* dk, float* dv,
+                         float* da, float* dalpha, float* dbeta, float* dW, float* dw_r, float* dH_0,
+                         float state_grad_clip, int64_t B, int64_t T, int64_t N, int64_t qk_heads, int64_t K,
+                         int64_t V, m2rnn_dtype dtype, void* workspace, size_t workspace_bytes,
+                         void* cuda_stream) {
+  if (a == nullptr) return M2RNN_ERR_INVALID_ARG;
+  return backward_impl(q, k, v, GateIn{nullptr, a, alpha, beta}, W, w_r, H_0, dy, dH_T, ckpt, ckpt_every, dq, dk,
+                       dv, da, dalpha, dbeta, dW, dw_r, dH_0, state_grad_clip, B, T, N, qk_heads, K, V, dtype,
+                       workspace, workspace_bytes, cuda_stream);
+}
+
+size_t m2rnn_output_norm_backward_workspace_size(int64_t B, int64_t T, int64_t N, int64_t V) {
+  if (!dims_ok(B, T, N, 1, V) || N * V > output_norm_max_width()) return 0;
+  const int64_t rows = B * T;
+  const int d = static_cast<int>(N * V);
+  return align256(sizeof(float) * static_cast<size_t>(output_norm_backward_parts(rows, d)) * d);
+}
+
+int m2rnn_output_norm(const float* y, const void* g, const float* w, float eps, float* out, float* rstd,
+                      int64_t B, int64_t T, int64_t N, int64_t V, m2rnn_dtype dtype, void* cuda_stream) {
+  if (!dtype_ok(dtype) || !dims_ok(B, T, N, 1, V) || !(eps >= 0.f)) return M2RNN_ERR_INVALID_ARG;
+  if (N * V > output_norm_max_width()) return M2RNN_ERR_UNSUPPORTED;
+  const void* req[] = {y, g, w, out};
+  for (const void* p : req)
+    if (p == nullptr || !aligned16(p)) return M2RNN_ERR_INVALID_ARG;
+  if (rstd && !aligned16(rstd)) return M2RNN_ERR_INVALID_ARG;
+  return cuda_status(launch_output_norm(y, g, w, eps, out, rstd, B * T, static_cast<int>(N * V),
+                                        dtype == M2RNN_BF16, static_cast<cudaStream_t>(cuda_stream)));
+}
+
+int m2rnn_output_norm_backward(const float* y, const void* g, const float* w, const float* dout, float eps,
+                               float* dy, float* dg, float* dw, int64_t B, int64_t T, int64_t N, int64_t V,
+                               m2rnn_dtype dtype, void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  if (!dtype_ok(dtype) || !dims_ok(B, T, N, 1, V) || !(eps >= 0.f)) return M2RNN_ERR_INVALID_ARG;
+  if (N * V > output_norm_max_width()) return M2RNN_ERR_UNSUPPORTED;
+  const void* req[] = {y, g, w, dout, dy, dg, dw};
+  for (const void* p : req)
+    if (p == nullptr || !aligned16(p)) return M2RNN_ERR_INVALID_ARG;
+  const size_t need = m2rnn_output_norm_backward_workspace_size(B, T, N, V);
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need) return M2RNN_ERR_WORKSPACE;
+  return cuda_status(launch_output_norm_backward(y, g, w, dout, eps, dy, dg, dw, static_cast<float*>(workspace),
+                                                 B * T, static_cast<int>(N * V), dtype == M2RNN_BF16,
+                                                 static_cast<cudaStream_t>(cuda_stream)));
 }
 
 int m2rnn_backward(const void* q, const void* k, const void* v, const void* f, const void* W,

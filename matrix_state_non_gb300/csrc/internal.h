@@ -20,6 +20,9 @@ struct FwdArgs {
   const void* w_r;
   const float* H0;  // initial state [B,N,K,V] fp32; null = zero
   int qkN;          // heads of q and k: 1 = one q/k shared by every head, else N
+  const void* gate_a;        // non-null: f = exp(-alpha softplus(a + beta)) from a [B,T,N] (input dtype)
+  const float* gate_alpha;   // [N]
+  const float* gate_beta;    // [N]
   float* y;      // may be null (checkpoint-only pass)
   float* H_T;    // may be null
   float* ckpt;   // may be null
@@ -42,6 +45,9 @@ struct BwdArgs {
   const float* H0;    // initial state; null = zero
   float* dH0;         // gradient of the initial state; may be null
   int qkN;            // heads of q and k (1 = shared); dq/dk are per head here either way
+  const void* gate_a;        // as in FwdArgs
+  const float* gate_alpha;
+  const float* gate_beta;
   float clip;         // > 0: every new C_{t-1} clamped to [-clip, clip]; else no clipping
   const float* ckpt;  // never null here (recomputed by the caller layer if needed)
   int ckpt_every;
@@ -106,5 +112,18 @@ bool tc_backward_supported(int K, int V);
 int tc_backward_parts(int K, int V);
 size_t tc_backward_scratch_bytes(int B, int N, int K, int V, int ckpt_every);
 cudaError_t launch_tc_backward(const BwdArgs& a, cudaStream_t s);
+
+// Gate backward (one block per head): grad holds df on entry, da on exit.
+struct GateSrc;
+cudaError_t launch_gate_backward(const GateSrc& gs, float* grad, float* dalpha, float* dbeta, int64_t BT, int N,
+                                 cudaStream_t s);
+// Gated RMSNorm output path over rows of d elements.
+int output_norm_max_width();
+int output_norm_backward_parts(int64_t rows, int d);
+cudaError_t launch_output_norm(const float* y, const void* g, const float* w, float eps, float* out, float* rstd,
+                               int64_t rows, int d, bool bf16, cudaStream_t s);
+cudaError_t launch_output_norm_backward(const float* y, const void* g, const float* w, const float* dout, float eps,
+                                        float* dy, float* dg, float* dw, float* part, int64_t rows, int d,
+                                        bool bf16, cudaStream_t s);
 
 }  // namespace m2rnn

@@ -40,6 +40,7 @@
 #include <algorithm>
 
 #include "internal.h"
+#include "gate.cuh"
 #include "mma_common.cuh"
 
 namespace m2rnn {
@@ -412,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // q, k, v, dy by TMA, f gathered by the lanes (its global-load latency
     // hidden behind the chunk's recompute) and published at the chunk's end.
     const bool loader = (warp == 4);
-    const uint16_t* fg = static_cast<const uint16_t*>(A.f);
+    const GateSrc gs{A.f, A.gate_a, A.gate_alpha, A.gate_beta, true};
     auto issue_chunk = [&](int li) -> float {
       const int t0 = (p.nchunks - 1 - li) * CL;
       uint8_t* buf = smem + p.cbuf_off + (li % kCBufs) * p.cbuf_bytes;
@@ -425,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_4d(smem_u32(buf + p.cdy_off), &tm_dy, fb, 0, n, t0, b);
       }
       const int t = t0 + lane;
-      return (lane < CL && t < T) ? bf16_bits_to_f32(fg[(static_cast<int64_t>(b) * T + t) * N + n]) : 0.f;
+      return (lane < CL && t < T) ? gate_value(gs, (static_cast<int64_t>(b) * T + t) * N + n, n) : 0.f;
     };
     auto publish_chunk = [&](int li, float fv) {
       float* cfw = reinterpret_cast<float*>(smem + p.cbuf_off + (li % kCBufs) * p.cbuf_bytes + p.cf_off);

@@ -25,6 +25,7 @@
 #include <algorithm>
 
 #include "internal.h"
+#include "gate.cuh"
 #include "mma_common.cuh"
 
 namespace m2rnn {
@@ -359,7 +360,7 @@ __global__ void __launch_bounds__((kMaxRB + 1) * 32, 1)
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_dy);
     }
-    const uint16_t* fg = static_cast<const uint16_t*>(A.f);
+    const GateSrc gs{A.f, A.gate_a, A.gate_alpha, A.gate_beta, true};
     int issued = 0;
     bool ok = true;
     for (int ci = 0; ci < p.nchunks; ++ci) {
@@ -375,7 +376,7 @@ __global__ void __launch_bounds__((kMaxRB + 1) * 32, 1)
       const int t = t0 + lane;
       if (lane < CL)
         reinterpret_cast<float*>(buf + p.cf_off)[lane] =
-            (t < T) ? bf16_bits_to_f32(fg[(static_cast<int64_t>(b) * T + t) * N + n]) : 0.f;
+            (t < T) ? gate_value(gs, (static_cast<int64_t>(b) * T + t) * N + n, n) : 0.f;
       __syncwarp();
       const uint32_t fb = smem_u32(&cfull[cb]);
       if (lane == 0) {

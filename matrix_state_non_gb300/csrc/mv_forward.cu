@@ -25,6 +25,7 @@
 #include <algorithm>
 
 #include "internal.h"
+#include "gate.cuh"
 #include "mma_common.cuh"
 
 namespace m2rnn {
@@ -226,7 +227,7 @@ __global__ void __launch_bounds__((kMaxRB + 1) * 32, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
     }
-    const uint16_t* fg = static_cast<const uint16_t*>(A.f);
+    const GateSrc gs{A.f, A.gate_a, A.gate_alpha, A.gate_beta, true};
     int issued = 0;
     bool ok = true;
     for (int tile = 0; tile < p.ntiles; ++tile) {
@@ -239,7 +240,7 @@ __global__ void __launch_bounds__((kMaxRB + 1) * 32, 1)
       const int t0 = tile * kS;
       uint8_t* stage = sStage + st * p.stage_bytes;
       float fv = 0.f;
-      if (t0 + lane < T) fv = bf16_bits_to_f32(fg[(static_cast<int64_t>(b) * T + t0 + lane) * N + n]);
+      if (t0 + lane < T) fv = gate_value(gs, (static_cast<int64_t>(b) * T + t0 + lane) * N + n, n);
       reinterpret_cast<float*>(stage + p.f_off)[lane] = fv;
       __syncwarp();
       const uint32_t fb = smem_u32(&full[st]);

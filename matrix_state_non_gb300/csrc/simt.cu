@@ -10,6 +10,7 @@
 // scheme; here only one chunk of states is cached at a time).
 #include <cuda_runtime.h>
 
+#include "gate.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -46,7 +47,7 @@ __global__ void __launch_bounds__(kThreads) simt_forward_kernel(FwdArgs a) {
   const Tin* q = static_cast<const Tin*>(a.q);
   const Tin* k = static_cast<const Tin*>(a.k);
   const Tin* v = static_cast<const Tin*>(a.v);
-  const Tin* f = static_cast<const Tin*>(a.f);
+  const GateSrc gs{a.f, a.gate_a, a.gate_alpha, a.gate_beta, sizeof(Tin) == 2};
   const Tin* W = static_cast<const Tin*>(a.W) + static_cast<int64_t>(n) * V * V;
   const Tin* w_r = static_cast<const Tin*>(a.w_r) + static_cast<int64_t>(n) * V;
 
@@ -63,7 +64,7 @@ __global__ void __launch_bounds__(kThreads) simt_forward_kernel(FwdArgs a) {
       qs[i] = ld_in(q, rowqk * K + i);
     }
     for (int j = threadIdx.x; j < V; j += kThreads) vs[j] = ld_in(v, row * V + j);
-    if (threadIdx.x == 0) fs[0] = ld_in(f, row);
+    if (threadIdx.x == 0) fs[0] = gate_value(gs, row, n);
     __syncthreads();
     const float ft = fs[0];
     for (int e = threadIdx.x; e < KV; e += kThreads) {
@@ -132,7 +133,7 @@ __global__ void __launch_bounds__(kThreads) simt_backward_kernel(BwdArgs a) {
   const Tin* q = static_cast<const Tin*>(a.q);
   const Tin* k = static_cast<const Tin*>(a.k);
   const Tin* v = static_cast<const Tin*>(a.v);
-  const Tin* f = static_cast<const Tin*>(a.f);
+  const GateSrc gs{a.f, a.gate_a, a.gate_alpha, a.gate_beta, sizeof(Tin) == 2};
   const Tin* W = static_cast<const Tin*>(a.W) + static_cast<int64_t>(n) * V * V;
   const Tin* w_r = static_cast<const Tin*>(a.w_r) + static_cast<int64_t>(n) * V;
   float* Hs = a.scratch + static_cast<int64_t>(chain) * (2 * CL + 1) * KV;  // [CL+1][K][V]
@@ -167,7 +168,7 @@ __global__ void __launch_bounds__(kThreads) simt_backward_kernel(BwdArgs a) {
       const int64_t rowqk = (static_cast<int64_t>(b) * T + s0 + s) * qk_heads(a.qkN, N) + qk_head(a.qkN, n);
       for (int i = threadIdx.x; i < K; i += kThreads) ks[i] = ld_in(k, rowqk * K + i);
       for (int j = threadIdx.x; j < V; j += kThreads) vs[j] = ld_in(v, row * V + j);
-      if (threadIdx.x == 0) fs[0] = ld_in(f, row);
+      if (threadIdx.x == 0) fs[0] = gate_value(gs, row, n);
       __syncthreads();
       const float ft = fs[0];
       for (int e = threadIdx.x; e < KV; e += kThreads) {
@@ -195,7 +196,7 @@ __global__ void __launch_bounds__(kThreads) simt_backward_kernel(BwdArgs a) {
         vs[j] = ld_in(v, row * V + j);
         us[j] = a.dy[row * V + j];
       }
-      if (threadIdx.x == 0) fs[0] = ld_in(f, row);
+      if (threadIdx.x == 0) fs[0] = gate_value(gs, row, n);
       __syncthreads();
       const float ft = fs[0];
       const float* Hprev = Hs + static_cast<int64_t>(s) * KV;

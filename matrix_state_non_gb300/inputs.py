@@ -146,3 +146,36 @@ def from_exact(exact: dict, dtype: str) -> M2RNNInputs:
             raise ValueError(f"{name} is not exactly representable in {dt}")
         store[name], ex[name] = s, e
     return M2RNNInputs(B, N, T, K, V, dtype, store, ex)
+
+
+def make_gate_inputs(B: int, T: int, N: int, dtype: str = "bf16", seed: int = 0):
+    """Forget-gate parameters: the pre-activation a [B,T,N] ~ N(0, 1) in the
+    storage dtype, and per head alpha ~ U(0.5, 2), beta ~ N(-2, 0.5) in fp32
+    (so that a + beta centres where the f distribution above centres).
+    Returns (store, exact) dicts with keys a, alpha, beta."""
+    rng = np.random.default_rng(seed)
+    raw = {"a": rng.standard_normal((B, T, N)),
+           "alpha": rng.uniform(0.5, 2.0, N),
+           "beta": rng.standard_normal(N) * 0.5 - 2.0}
+    store, exact = {}, {}
+    store["a"], exact["a"] = round_to_dtype(raw["a"], dtype)
+    for name in ("alpha", "beta"):
+        store[name], exact[name] = round_to_dtype(raw[name], "f32")
+    return store, exact
+
+
+def make_norm_inputs(B: int, T: int, N: int, V: int, dtype: str = "bf16", seed: int = 0):
+    """Output-path inputs: a readout y [B,T,N,V] ~ N(0, 1/4) (fp32), the output
+    gate g [B,T,N,V] ~ N(0, 1) in the storage dtype, the per-channel weight
+    w [N,V] ~ 1 + N(0, 1/100) and the upstream gradient dout ~ N(0, 1) (fp32).
+    Returns (store, exact) dicts with keys y, g, w, dout."""
+    rng = np.random.default_rng(seed)
+    raw = {"y": rng.standard_normal((B, T, N, V)) * 0.5,
+           "g": rng.standard_normal((B, T, N, V)),
+           "w": 1.0 + rng.standard_normal((N, V)) * 0.1,
+           "dout": rng.standard_normal((B, T, N, V))}
+    store, exact = {}, {}
+    for name in ("y", "w", "dout"):
+        store[name], exact[name] = round_to_dtype(raw[name], "f32")
+    store["g"], exact["g"] = round_to_dtype(raw["g"], dtype)
+    return store, exact

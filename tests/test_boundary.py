@@ -128,6 +128,40 @@ def test_state_entry_points_reject_bad_arguments_without_a_device(lib):
     assert st == binding.M2RNN_ERR_UNSUPPORTED   # V above the supported 128
 
 
+def test_gate_and_output_norm_entry_points_reject_bad_arguments_without_a_device(lib):
+    bf = binding.M2RNN_BF16
+
+    def fg(a=P, alpha=P, beta=P, N=2):
+        return binding.m2rnn_forward_gated(P, P, P, a, alpha, beta, P, P, None, P, None, None, 0, 1, 8, N, N,
+                                           64, 64, bf, P, 1 << 20, None)
+    assert fg(a=None) == binding.M2RNN_ERR_INVALID_ARG
+    assert fg(alpha=None) == binding.M2RNN_ERR_INVALID_ARG
+    assert fg(beta=P + 4) == binding.M2RNN_ERR_INVALID_ARG
+
+    def bg(dalpha=P, dbeta=P, a=P):
+        return binding.m2rnn_backward_gated(P, P, P, a, P, P, P, P, None, P, None, None, 14, P, P, P, P, dalpha,
+                                            dbeta, P, P, None, 0.0, 1, 8, 2, 2, 64, 64, bf, P, 1 << 30, None)
+    assert bg(dalpha=None) == binding.M2RNN_ERR_INVALID_ARG
+    assert bg(dbeta=P + 8) == binding.M2RNN_ERR_INVALID_ARG
+    assert bg(a=None) == binding.M2RNN_ERR_INVALID_ARG
+
+    assert binding.m2rnn_output_norm_backward_workspace_size(4, 4096, 8, 64) > 0
+    assert binding.m2rnn_output_norm_backward_workspace_size(1, 8, 129, 128) == 0   # N V above 16384
+    assert binding.m2rnn_output_norm_backward_workspace_size(0, 8, 8, 64) == 0
+    assert binding.m2rnn_output_norm(P, P, P, -1.0, P, None, 1, 8, 8, 64, bf, None) == \
+        binding.M2RNN_ERR_INVALID_ARG
+    assert binding.m2rnn_output_norm(P, P, P, float("nan"), P, None, 1, 8, 8, 64, bf, None) == \
+        binding.M2RNN_ERR_INVALID_ARG
+    assert binding.m2rnn_output_norm(P, P + 2, P, 1e-6, P, None, 1, 8, 8, 64, bf, None) == \
+        binding.M2RNN_ERR_INVALID_ARG
+    assert binding.m2rnn_output_norm(P, P, P, 1e-6, P, None, 1, 8, 129, 128, bf, None) == \
+        binding.M2RNN_ERR_UNSUPPORTED
+    assert binding.m2rnn_output_norm_backward(P, P, P, P, 1e-6, P, P, P, 1, 8, 8, 64, bf, P, 16, None) == \
+        binding.M2RNN_ERR_WORKSPACE
+    assert binding.m2rnn_output_norm_backward(P, P, P, None, 1e-6, P, P, P, 1, 8, 8, 64, bf, P, 1 << 30,
+                                              None) == binding.M2RNN_ERR_INVALID_ARG
+
+
 def test_noalloc_backward_rejects_unsupported_shapes_without_a_device(lib):
     def call(**kw):
         a = dict(C=16, B=1, T=64, N=1, K=64, V=64, dt=binding.M2RNN_BF16, ckpt=P)
