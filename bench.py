@@ -586,10 +586,15 @@ def time_gated_block(binding, dev, stream, flush, pk, dist, reps=3):
         step(evs)
         runs.append(evs)
     alone = {}
+    # After the write flush, read another buffer larger than L2: that writes
+    # the flush's dirty lines back before the timed launch instead of during
+    # it (a kernel of ~20 us would otherwise pay for them).
+    evict = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     for name, fn in (("norm_fwd", norm_fwd), ("norm_bwd", norm_bwd)):
         pairs = []
         for _ in range(reps):
             flush.zero_()
+            evict.sum()
             a, b = mk(), mk()
             a.record(stream)
             fn()
@@ -611,7 +616,7 @@ def time_gated_block(binding, dev, stream, flush, pk, dist, reps=3):
     norm = {k: {"ms": alone_ms[k], "bytes": nbytes[k],
                 "achieved_gbs": nbytes[k] / (alone_ms[k] * 1e-3) / 1e9,
                 "hbm_frac": nbytes[k] / (alone_ms[k] * 1e-3) / (pk["hbm_gbs"] * 1e9)} for k in alone_ms}
-    del d, fo, bo, out, nb
+    del d, fo, bo, out, nb, evict
     return {"workload": w["desc"] + ", gate from (a, alpha, beta) in-kernel, RMSNorm(y*g) over N*V",
             "ms": total, "value": dist.world * units(w) / (total * 1e-3), "unit": UNIT, "pieces_ms": ms,
             "norm_alone_after_l2_flush": norm}

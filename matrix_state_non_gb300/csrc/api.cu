@@ -90,7 +90,7 @@ cudaError_t launch_forward_path(int path, const FwdArgs& a, cudaStream_t s) {
 }
 
 struct BwdLayout {
-  size_t ckpt_off, dwp_off, dwrp_off, scratch_off, qk_off, total;
+  size_t ckpt_off, dwp_off, dwrp_off, scratch_off, qk_off, gate_off, total;
 };
 
 // shared_qk: one q/k for every head; the per-head dq, dk go to the workspace
@@ -119,6 +119,8 @@ BwdLayout bwd_layout(int64_t B, int64_t T, int64_t N, int64_t K, int64_t V, int 
     off = align256(off + simt_backward_scratch_bytes(b, nn, k, v, C));
   l.qk_off = off;
   if (shared_qk) off = align256(off + 2 * sizeof(float) * static_cast<size_t>(B * T * N * K));
+  l.gate_off = off;  // gate-backward partials (used by the gated backward only)
+  off = align256(off + 2 * sizeof(float) * static_cast<size_t>(N) * gate_backward_parts(B * T));
   l.total = off;
   return l;
 }
@@ -305,6 +307,7 @@ int backward_impl(const void* q, const void* k, const void* v, const GateIn& gat
   if (!gate.ok()) return M2RNN_ERR_INVALID_ARG;
   if (gate.a != nullptr && (dalpha == nullptr || dbeta == nullptr || !aligned16(dalpha) || !aligned16(dbeta)))
     return M2RNN_ERR_INVALID_ARG;
+  if (gate.a != nullptr && N > 65535) return M2RNN_ERR_UNSUPPORTED;  // heads index the grid's y dimension
   if ((dH_T && !aligned16(dH_T)) || (ckpt && !aligned16(ckpt)) || (H_0 && !aligned16(H_0)) ||
       (dH_0 && !aligned16(dH_0)))
     return M2RNN_ERR_INVALID_ARG;
@@ -369,7 +372,8 @@ int backward_impl(const void* q, const void* k, const void* v, const GateIn& gat
   if (e != cudaSuccess) return M2RNN_ERR_CUDA;
   if (gate.a != nullptr) {
     const GateSrc gs{nullptr, gate.a, gate.alpha, gate.beta, dtype == M2RNN_BF16};
-    e = launch_gate_backward(gs, df, dalpha, dbeta, B * T, static_cast<int>(N), s);
+    e = launch_gate_backward(gs, df, dalpha, dbeta, reinterpret_cast<float*>(ws + l.gate_off), B * T,
+                             static_cast<int>(N), s);
   }
   return cuda_status(e);
 }

@@ -26,7 +26,7 @@
 namespace m2rnn {
 namespace {
 
-constexpr int kGateThreads = 512;
+constexpr int kGateThreads = 256;
 
 // Fixed-order block sum of two values; every thread gets the totals.
 template <int kThreads>
@@ -51,15 +51,18 @@ __device__ __forceinline__ float2 block_sum2(float a, float b, float2* red) {
   return t;
 }
 
-// One block per head n; grad holds df on entry and da on exit.
-__global__ void __launch_bounds__(kGateThreads) gate_backward_kernel(GateSrc gs, float* grad, float* dalpha,
-                                                                     float* dbeta, int64_t BT, int N) {
+// Grid (P, N): block (p, n) takes rows i = p * 256 + tid, stepping P * 256,
+// of head n; grad holds df on entry and da on exit.  Block partials of
+// dalpha, dbeta go to part[n][p]; gate_finish_kernel sums them in order.
+__global__ void __launch_bounds__(kGateThreads) gate_backward_kernel(GateSrc gs, float* grad, float2* part,
+                                                                     int64_t BT, int N) {
   __shared__ float2 red[kGateThreads / 32];
-  const int n = blockIdx.x;
+  const int n = blockIdx.y, P = gridDim.x;
   const float al = gs.alpha[n], be = gs.beta[n];
   float sa = 0.f, sb = 0.f;
 #pragma unroll 4
-  for (int64_t i = threadIdx.x; i < BT; i += kGateThreads) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kGateThreads + threadIdx.x; i < BT;
+       i += static_cast<int64_t>(P) * kGateThreads) {
     const int64_t idx = i * N + n;
     const float x = (gs.bf16 ? bf16_bits_to_f32(static_cast<const uint16_t*>(gs.a)[idx])
                              : static_cast<const float*>(gs.a)[idx]) + be;
@@ -73,10 +76,20 @@ __global__ void __launch_bounds__(kGateThreads) gate_backward_kernel(GateSrc gs,
     sb += d;
   }
   const float2 t = block_sum2<kGateThreads>(sa, sb, red);
-  if (threadIdx.x == 0) {
-    dalpha[n] = t.x;
-    dbeta[n] = t.y;
+  if (threadIdx.x == 0) part[static_cast<int64_t>(n) * P + blockIdx.x] = t;
+}
+
+__global__ void gate_finish_kernel(const float2* part, float* dalpha, float* dbeta, int P, int N) {
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (n >= N) return;
+  float2 t = part[static_cast<int64_t>(n) * P];
+  for (int p = 1; p < P; ++p) {
+    const float2 u = part[static_cast<int64_t>(n) * P + p];
+    t.x += u.x;
+    t.y += u.y;
   }
+  dalpha[n] = t.x;
+  dbeta[n] = t.y;
 }
 
 // ---------------------------------------------------------------------------
@@ -240,13 +253,146 @@ __global__ void __launch_bounds__(kThreads) output_norm_backward_kernel(NormArgs
   }
 }
 
-// dw[j] = sum over blocks p (in order) of part[p][j].
-__global__ void sum_columns_kernel(const float* part, float* out, int P, int d) {
-  const int j = blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= d) return;
+// Rows of up to 1024 elements: one warp per row, lane l owning groups
+// l, l + 32, ... (kPer of them), eight warps per block; only shuffles in the
+// row sums.  Warp w takes rows w, w + (total warps), ...
+constexpr int kRowWarps = 8;
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+template <int kPer>
+__global__ void __launch_bounds__(32 * kRowWarps) norm_rows_kernel(NormArgs A) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * kRowWarps;
+  const int d = A.d;
+  float4 wv[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int j = 4 * (lane + 32 * i);
+    wv[i] = j < d ? ld4_f32(A.w, 0, j, d, A.vec) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5); row < A.rows;
+       row += nw) {
+    const int64_t base = row * d;
+    float4 x[kPer];
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int j = 4 * (lane + 32 * i);
+      x[i] = j < d ? mul4(ld4_f32(A.y, base, j, d, A.vec), ld4_in(A, A.g, base, j))
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      ss += dot4(x[i], x[i]);
+    }
+    const float s = rsqrtf(warp_sum(ss) / static_cast<float>(d) + A.eps);
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int j = 4 * (lane + 32 * i);
+      if (j < d) {
+        const float4 o = mul4(wv[i], x[i]);
+        st4(A.out, base, j, d, A.vec, make_float4(o.x * s, o.y * s, o.z * s, o.w * s));
+      }
+    }
+    if (A.rstd != nullptr && lane == 0) A.rstd[row] = s;
+  }
+}
+
+// dw: each lane accumulates its columns over the warp's rows; the block's
+// eight warps are summed in warp order through shared memory, one partial
+// row per block.
+template <int kPer>
+__global__ void __launch_bounds__(32 * kRowWarps) norm_rows_backward_kernel(NormArgs A) {
+  __shared__ float dws[kRowWarps][128 * kPer];
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * kRowWarps;
+  const int d = A.d;
+  const float inv_d = 1.f / static_cast<float>(d);
+  float4 wv[kPer], dwa[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int j = 4 * (lane + 32 * i);
+    wv[i] = j < d ? ld4_f32(A.w, 0, j, d, A.vec) : make_float4(0.f, 0.f, 0.f, 0.f);
+    dwa[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * kRowWarps + wib; row < A.rows; row += nw) {
+    const int64_t base = row * d;
+    float4 yv[kPer], gv[kPer], ov[kPer];
+    float ss = 0.f, rr = 0.f;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int j = 4 * (lane + 32 * i);
+      if (j < d) {
+        yv[i] = ld4_f32(A.y, base, j, d, A.vec);
+        gv[i] = ld4_in(A, A.g, base, j);
+        ov[i] = ld4_f32(A.dout, base, j, d, A.vec);
+      } else {
+        yv[i] = gv[i] = ov[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      const float4 x = mul4(yv[i], gv[i]);
+      ss += dot4(x, x);
+      rr += dot4(mul4(wv[i], ov[i]), x);
+    }
+    ss = warp_sum(ss);
+    rr = warp_sum(rr);
+    const float s = rsqrtf(ss * inv_d + A.eps);
+    const float c = rr * s * s * s * inv_d;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int j = 4 * (lane + 32 * i);
+      if (j < d) {
+        const float4 x = mul4(yv[i], gv[i]);
+        const float4 p = mul4(wv[i], ov[i]);
+        const float4 dx = make_float4(s * p.x - c * x.x, s * p.y - c * x.y, s * p.z - c * x.z, s * p.w - c * x.w);
+        st4(A.dy, base, j, d, A.vec, mul4(dx, gv[i]));
+        st4(A.dg, base, j, d, A.vec, mul4(dx, yv[i]));
+        dwa[i].x += ov[i].x * x.x * s;
+        dwa[i].y += ov[i].y * x.y * s;
+        dwa[i].z += ov[i].z * x.z * s;
+        dwa[i].w += ov[i].w * x.w * s;
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int j = 4 * (lane + 32 * i);
+    *reinterpret_cast<float4*>(&dws[wib][j]) = dwa[i];
+  }
+  __syncthreads();
+  float* part = A.dw_part + static_cast<int64_t>(blockIdx.x) * d;
+  for (int j = threadIdx.x; j < d; j += 32 * kRowWarps) {
+    float t = dws[0][j];
+#pragma unroll
+    for (int w = 1; w < kRowWarps; ++w) t += dws[w][j];
+    part[j] = t;
+  }
+}
+
+// dw[j] = sum over the P block partials part[p][j]: block b takes columns
+// 32 b .. 32 b + 31 (one per lane); its 32 warps each sum a contiguous
+// 32nd of p in order, then the 32 are added in warp order.
+constexpr int kSumWarps = 32;
+
+__global__ void __launch_bounds__(32 * kSumWarps) sum_columns_kernel(const float* part, float* out, int P, int d) {
+  __shared__ float red[kSumWarps][33];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int j = blockIdx.x * 32 + lane;
+  const int per = (P + kSumWarps - 1) / kSumWarps, p0 = w * per, p1 = min(P, p0 + per);
   float acc = 0.f;
-  for (int p = 0; p < P; ++p) acc += part[static_cast<int64_t>(p) * d + j];
-  out[j] = acc;
+  if (j < d) {
+#pragma unroll 4
+    for (int p = p0; p < p1; ++p) acc += part[static_cast<int64_t>(p) * d + j];
+  }
+  red[w][lane] = acc;
+  __syncthreads();
+  if (w == 0 && j < d) {
+    float t = red[0][lane];
+#pragma unroll
+    for (int i = 1; i < kSumWarps; ++i) t += red[i][lane];
+    out[j] = t;
+  }
 }
 
 // Launch shape for a row width d: threads per block and register groups per
@@ -255,11 +401,14 @@ struct NormShape {
   int threads, per;
 };
 
+// threads == 0: one warp per row (norm_rows_*), per = groups per lane.
 NormShape norm_shape(int d) {
   const int groups = (d + 3) / 4;
-  if (groups <= 128) return {128, 1};
-  if (groups <= 256) return {128, 2};
-  if (groups <= 512) return {128, 4};
+  if (groups <= 32) return {0, 1};
+  if (groups <= 64) return {0, 2};
+  if (groups <= 128) return {0, 4};
+  if (groups <= 256) return {0, 8};
+  if (groups <= 512) return {256, 2};
   if (groups <= 1024) return {256, 4};
   if (groups <= 2048) return {256, 8};
   return {512, 8};
@@ -267,6 +416,19 @@ NormShape norm_shape(int d) {
 
 cudaError_t launch_norm(bool backward, const NormArgs& A, int grid, cudaStream_t s) {
   const NormShape sh = norm_shape(A.d);
+#define M2RNN_ROWS_CASE(PER)                                                            \
+  if (sh.threads == 0 && sh.per == PER) {                                               \
+    if (backward)                                                                       \
+      norm_rows_backward_kernel<PER><<<grid, 32 * kRowWarps, 0, s>>>(A);                \
+    else                                                                                \
+      norm_rows_kernel<PER><<<grid, 32 * kRowWarps, 0, s>>>(A);                         \
+    return cudaGetLastError();                                                          \
+  }
+  M2RNN_ROWS_CASE(1)
+  M2RNN_ROWS_CASE(2)
+  M2RNN_ROWS_CASE(4)
+  M2RNN_ROWS_CASE(8)
+#undef M2RNN_ROWS_CASE
 #define M2RNN_NORM_CASE(TH, PER)                                                   \
   if (sh.threads == TH && sh.per == PER) {                                         \
     if (backward)                                                                  \
@@ -275,9 +437,7 @@ cudaError_t launch_norm(bool backward, const NormArgs& A, int grid, cudaStream_t
       output_norm_kernel<TH, PER><<<grid, TH, 0, s>>>(A);                          \
     return cudaGetLastError();                                                     \
   }
-  M2RNN_NORM_CASE(128, 1)
-  M2RNN_NORM_CASE(128, 2)
-  M2RNN_NORM_CASE(128, 4)
+  M2RNN_NORM_CASE(256, 2)
   M2RNN_NORM_CASE(256, 4)
   M2RNN_NORM_CASE(256, 8)
   M2RNN_NORM_CASE(512, 8)
@@ -293,13 +453,23 @@ int output_norm_max_width() { return 4 * 512 * 8; }
 // cover every SM a few times over.
 int output_norm_backward_parts(int64_t rows, int d) {
   const NormShape sh = norm_shape(d);
-  const int64_t cap = (sh.threads <= 128) ? 1216 : (sh.threads <= 256 ? 608 : 304);
-  return static_cast<int>(rows < cap ? rows : cap);
+  const int64_t want = sh.threads == 0 ? (rows + kRowWarps - 1) / kRowWarps : rows;
+  const int64_t cap = sh.threads == 0 ? 608 : (sh.threads <= 256 ? 608 : 304);
+  return static_cast<int>(want < cap ? want : cap);
 }
 
-cudaError_t launch_gate_backward(const GateSrc& gs, float* grad, float* dalpha, float* dbeta, int64_t BT, int N,
-                                 cudaStream_t s) {
-  gate_backward_kernel<<<N, kGateThreads, 0, s>>>(gs, grad, dalpha, dbeta, BT, N);
+int gate_backward_parts(int64_t BT) {
+  const int64_t p = (BT + 4 * kGateThreads - 1) / (4 * kGateThreads);
+  return static_cast<int>(p < 128 ? p : 128);
+}
+
+cudaError_t launch_gate_backward(const GateSrc& gs, float* grad, float* dalpha, float* dbeta, float* part,
+                                 int64_t BT, int N, cudaStream_t s) {
+  const int P = gate_backward_parts(BT);
+  gate_backward_kernel<<<dim3(P, N), kGateThreads, 0, s>>>(gs, grad, reinterpret_cast<float2*>(part), BT, N);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  gate_finish_kernel<<<(N + 127) / 128, 128, 0, s>>>(reinterpret_cast<const float2*>(part), dalpha, dbeta, P, N);
   return cudaGetLastError();
 }
 
@@ -308,8 +478,10 @@ cudaError_t launch_output_norm(const float* y, const void* g, const float* w, fl
   NormArgs A{};
   A.y = y; A.g = g; A.w = w; A.out = out; A.rstd = rstd;
   A.rows = rows; A.d = d; A.eps = eps; A.bf16 = bf16; A.vec = (d % 4) == 0;
+  const NormShape sh = norm_shape(d);
+  const int64_t want = sh.threads == 0 ? (rows + kRowWarps - 1) / kRowWarps : rows;
   const int64_t cap = 152 * 16;
-  const int grid = static_cast<int>(rows < cap ? rows : cap);
+  const int grid = static_cast<int>(want < cap ? want : cap);
   return launch_norm(false, A, grid, s);
 }
 
@@ -322,7 +494,7 @@ cudaError_t launch_output_norm_backward(const float* y, const void* g, const flo
   const int P = output_norm_backward_parts(rows, d);
   cudaError_t e = launch_norm(true, A, P, s);
   if (e != cudaSuccess) return e;
-  sum_columns_kernel<<<(d + 255) / 256, 256, 0, s>>>(part, dw, P, d);
+  sum_columns_kernel<<<(d + 31) / 32, 32 * kSumWarps, 0, s>>>(part, dw, P, d);
   return cudaGetLastError();
 }
 

@@ -113,10 +113,12 @@ int tc_backward_parts(int K, int V);
 size_t tc_backward_scratch_bytes(int B, int N, int K, int V, int ckpt_every);
 cudaError_t launch_tc_backward(const BwdArgs& a, cudaStream_t s);
 
-// Gate backward (one block per head): grad holds df on entry, da on exit.
+// Gate backward: grad holds df on entry, da on exit; part holds
+// 2 * N * gate_backward_parts(BT) floats of scratch.
 struct GateSrc;
-cudaError_t launch_gate_backward(const GateSrc& gs, float* grad, float* dalpha, float* dbeta, int64_t BT, int N,
-                                 cudaStream_t s);
+int gate_backward_parts(int64_t BT);
+cudaError_t launch_gate_backward(const GateSrc& gs, float* grad, float* dalpha, float* dbeta, float* part,
+                                 int64_t BT, int N, cudaStream_t s);
 // Gated RMSNorm output path over rows of d elements.
 int output_norm_max_width();
 int output_norm_backward_parts(int64_t rows, int d);

@@ -165,12 +165,13 @@ def _run_norm(store, eps, backward=False):
     return {n: v.cpu().numpy() for n, v in res.items()}
 
 
-# widths d = N V: 512 (one group of 4 per thread at 128 threads), 256 (the
-# pages' 16 heads x 16), 15 (not a multiple of 4: scalar path), 4100 (256
-# threads x 5 of 8 register groups, ragged), 16384 (the widest, N = V = 128,
-# 512 threads), 4 (one head, one group).
-NORM_SHAPES = [(2, 33, 8, 64), (1, 17, 16, 16), (2, 5, 3, 5), (1, 3, 41, 100), (1, 2, 128, 128),
-               (1, 1, 1, 4)]
+# widths d = N V: 512 (a warp per row, 4 groups of 4 per lane), 256 (the
+# pages' 16 heads x 16), 15 (not a multiple of 4: scalar path), 960 (a warp
+# per row, 8 groups per lane, ragged), 1600 (a block per row, 256 threads x
+# 2 groups), 4100 (256 threads x 5 of 8 groups, ragged), 16384 (the widest,
+# N = V = 128, 512 threads), 4 (one head, one group).
+NORM_SHAPES = [(2, 33, 8, 64), (1, 17, 16, 16), (2, 5, 3, 5), (1, 9, 12, 80), (2, 7, 16, 100),
+               (1, 3, 41, 100), (1, 2, 128, 128), (1, 1, 1, 4)]
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
