@@ -97,6 +97,12 @@ def io_bytes_bwd(w, s_in=2, ckpt_every=CKPT_EVERY):
     return units(w) * per_unit + ck
 
 
+def stash_bytes(w):
+    """The forward's fp16 Z stash (written by the forward, read by the
+    backward of a training step): 2 K V bytes per unit."""
+    return 2.0 * w["K"] * w["V"] * units(w)
+
+
 def source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "matrix_state_non_gb300", "csrc")
@@ -301,10 +307,11 @@ def run_gpu(args, dist):
     d = binding.to_device(inp, dev)
     B, T, N, K, V = w["B"], w["T"], w["N"], w["K"], w["V"]
     stream = torch.cuda.current_stream(dev)
-    # Preallocated outputs and workspaces.
-    fwd_out = binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=CKPT_EVERY)
+    # Preallocated outputs and workspaces.  The forward leaves its Z stash
+    # (fp16 Z_t of every step) and checkpoints for the backward.
+    fwd_out = binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=CKPT_EVERY, stash=True)
     bwd_out = binding.backward(*(d[n] for n in IN_NAMES), d["dy"], ckpt=fwd_out["ckpt"],
-                               ckpt_every=CKPT_EVERY)
+                               ckpt_every=CKPT_EVERY, z_stash=fwd_out["z_stash"])
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
@@ -312,12 +319,13 @@ def run_gpu(args, dist):
     def step(timing=None):
         if timing is not None:
             timing[0].record(stream)
-        binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=CKPT_EVERY, out=fwd_out,
+        binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=CKPT_EVERY, stash=True, out=fwd_out,
                         workspace=fwd_out["workspace"])
         if timing is not None:
             timing[1].record(stream)
         binding.backward(*(d[n] for n in IN_NAMES), d["dy"], ckpt=fwd_out["ckpt"],
-                         ckpt_every=CKPT_EVERY, out=bwd_out, workspace=bwd_out["workspace"])
+                         ckpt_every=CKPT_EVERY, z_stash=fwd_out["z_stash"], out=bwd_out,
+                         workspace=bwd_out["workspace"])
         if timing is not None:
             timing[2].record(stream)
 
@@ -393,7 +401,7 @@ def run_gpu(args, dist):
                 "frac": achieved / peak, "traffic": profiled_traffic(kname, MAIN),
                 "kernel": kname, "peak_source": f"{pk['source']} bf16 sustained",
                 "kernel_ms": kms, "ns_per_step_per_chain": kms * 1e6 / T,
-                "hbm_frac": (io_bytes_bwd(w) if kname == "m2rnn_backward" else io_bytes_fwd(w))
+                "hbm_frac": ((io_bytes_bwd(w) if kname == "m2rnn_backward" else io_bytes_fwd(w)) + stash_bytes(w))
                 / (kms * 1e-3) / (pk["hbm_gbs"] * 1e9)}
 
     # Forward-only workloads.
@@ -435,6 +443,7 @@ def run_gpu(args, dist):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w["desc"], "B": B, "T": T, "heads": N, "K": K, "V": V,
                    "state": "fp32", "ckpt_every": CKPT_EVERY,
+                   "z_stash": "fp16 Z_t of every step, written by the forward, read by the backward",
                    "l2": "flushed between timed steps (256 MiB write outside the events)",
                    "parallelism": f"replicas x{dist.world} (independent chains, no collective)"},
         "roofline": roofline,
@@ -549,10 +558,11 @@ def time_gated_block(binding, dev, stream, flush, pk, dist, reps=3):
     up = {n: binding.to_device(_Store(x), dev)["x"] for n, x in list(gs.items()) + list(ns.items())}
     gate = (up["a"], up["alpha"], up["beta"])
     args = (d["q"], d["k"], d["v"], None, d["W"], d["w_r"])
-    fo = binding.forward(*args, gate=gate, ckpt_every=CKPT_EVERY)
+    fo = binding.forward(*args, gate=gate, ckpt_every=CKPT_EVERY, stash=True)
     out = binding.output_norm(fo["y"], up["g"], up["w"])
     nb = binding.output_norm_backward(fo["y"], up["g"], up["w"], up["dout"])
-    bo = binding.backward(*args, nb["dy"], gate=gate, ckpt=fo["ckpt"], ckpt_every=CKPT_EVERY)
+    bo = binding.backward(*args, nb["dy"], gate=gate, ckpt=fo["ckpt"], ckpt_every=CKPT_EVERY,
+                          z_stash=fo["z_stash"])
     nws = torch.empty(binding.m2rnn_output_norm_backward_workspace_size(B, T, N, V), device=dev,
                       dtype=torch.uint8)
 
@@ -565,14 +575,14 @@ def time_gated_block(binding, dev, stream, flush, pk, dist, reps=3):
     def step(evs=None):
         rec = (lambda i: evs[i].record(stream)) if evs else (lambda i: None)
         rec(0)
-        binding.forward(*args, gate=gate, ckpt_every=CKPT_EVERY, out=fo, workspace=fo["workspace"])
+        binding.forward(*args, gate=gate, ckpt_every=CKPT_EVERY, stash=True, out=fo, workspace=fo["workspace"])
         rec(1)
         norm_fwd()
         rec(2)
         norm_bwd()
         rec(3)
-        binding.backward(*args, nb["dy"], gate=gate, ckpt=fo["ckpt"], ckpt_every=CKPT_EVERY, out=bo,
-                         workspace=bo["workspace"])
+        binding.backward(*args, nb["dy"], gate=gate, ckpt=fo["ckpt"], ckpt_every=CKPT_EVERY,
+                         z_stash=fo["z_stash"], out=bo, workspace=bo["workspace"])
         rec(4)
 
     for _ in range(3):
@@ -696,16 +706,21 @@ def run_only(args, dist):
     inp = make_workload(args.only)
     d = binding.to_device(inp, dev)
     ck = CKPT_EVERY if w["backward"] else 0
-    out = binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=ck)
+    # Training workloads run as the benchmark step does: with the Z stash where the shape has one.
+    stash = w["backward"] and binding.m2rnn_z_stash_size(w["B"], w["T"], w["N"], w["K"], w["V"],
+                                                         binding.M2RNN_BF16 if w["dtype"] == "bf16"
+                                                         else binding.M2RNN_F32) > 0
+    out = binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=ck, stash=stash)
     bout = None
 
     def step():
         nonlocal bout
-        binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=ck, out=out, workspace=out["workspace"])
+        binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=ck, stash=stash, out=out,
+                        workspace=out["workspace"])
         if w["backward"]:
             bout = binding.backward(*(d[n] for n in IN_NAMES), d["dy"], ckpt=out["ckpt"],
-                                    ckpt_every=ck, out=bout, workspace=None if bout is None
-                                    else bout["workspace"])
+                                    ckpt_every=ck, z_stash=out.get("z_stash"), out=bout,
+                                    workspace=None if bout is None else bout["workspace"])
 
     for _ in range(args.warmup):
         step()

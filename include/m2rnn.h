@@ -142,14 +142,27 @@ int m2rnn_backward(const void* q, const void* k, const void* v, const void* f,
  * following steps continues the same sequence (the fixed-size recurrent
  * state of the reading notes, section 2.6): a sequence can run in pieces.
  * H_0 may equal H_T (each state element is read before it is overwritten).
+ *   z_stash (may be NULL): m2rnn_z_stash_size bytes that receive Z_t of
+ *        every step (fp16, an internal layout) for m2rnn_backward_state;
+ *        only for the shapes where that size is non-zero (else
+ *        M2RNN_ERR_UNSUPPORTED).  The backward then skips the rerun of the
+ *        recurrence's transform and tanh: it advances the state from each
+ *        checkpoint by the gate blend alone.  Pass `ckpt` too.
  */
 int m2rnn_forward_state(const void* q, const void* k, const void* v,
                         const void* f, const void* W, const void* w_r,
                         const float* H_0, float* y, float* H_T, float* ckpt,
-                        int ckpt_every, int64_t B, int64_t T, int64_t N,
+                        int ckpt_every, void* z_stash, int64_t B, int64_t T,
+                        int64_t N,
                         int64_t qk_heads, int64_t K, int64_t V,
                         m2rnn_dtype dtype, void* workspace,
                         size_t workspace_bytes, void* cuda_stream);
+
+/* Bytes of the Z stash of m2rnn_forward_state / m2rnn_backward_state
+ * (B T N K V fp16 values), or 0 where the stash is not supported (it is for
+ * bf16 inputs with V = 64 and K a multiple of 16, <= 128). */
+size_t m2rnn_z_stash_size(int64_t B, int64_t T, int64_t N, int64_t K,
+                          int64_t V, m2rnn_dtype dtype);
 
 /* Bytes of device workspace m2rnn_backward_state needs (a shared q/k,
  * qk_heads = 1 with N > 1, adds room for the per-head dq, dk). */
@@ -173,12 +186,16 @@ size_t m2rnn_backward_state_workspace_size(int64_t B, int64_t T, int64_t N,
  *        fixed order (notes section 2.7).
  * When a sequence runs in pieces, dH_0 of a later piece is the dH_T of the
  * piece before it.  `ckpt`, if given, must come from m2rnn_forward_state
- * with the same H_0.  workspace: m2rnn_backward_state_workspace_size bytes.
+ * with the same H_0.  z_stash (may be NULL): the stash that same forward
+ * call wrote, with its `ckpt` (required when T > ckpt_every), ckpt_every
+ * <= 28; Z_t then comes from the stash in fp16 instead of a rerun.
+ * workspace: m2rnn_backward_state_workspace_size bytes.
  */
 int m2rnn_backward_state(const void* q, const void* k, const void* v,
                          const void* f, const void* W, const void* w_r,
                          const float* H_0, const float* dy, const float* dH_T,
-                         const float* ckpt, int ckpt_every, float* dq,
+                         const float* ckpt, int ckpt_every,
+                         const void* z_stash, float* dq,
                          float* dk, float* dv, float* df, float* dW,
                          float* dw_r, float* dH_0, float state_grad_clip,
                          int64_t B, int64_t T, int64_t N, int64_t qk_heads,
@@ -200,7 +217,8 @@ int m2rnn_forward_gated(const void* q, const void* k, const void* v,
                         const void* a, const float* alpha, const float* beta,
                         const void* W, const void* w_r, const float* H_0,
                         float* y, float* H_T, float* ckpt, int ckpt_every,
-                        int64_t B, int64_t T, int64_t N, int64_t qk_heads,
+                        void* z_stash, int64_t B, int64_t T, int64_t N,
+                        int64_t qk_heads,
                         int64_t K, int64_t V, m2rnn_dtype dtype,
                         void* workspace, size_t workspace_bytes,
                         void* cuda_stream);
@@ -219,8 +237,8 @@ int m2rnn_backward_gated(const void* q, const void* k, const void* v,
                          const void* a, const float* alpha, const float* beta,
                          const void* W, const void* w_r, const float* H_0,
                          const float* dy, const float* dH_T, const float* ckpt,
-                         int ckpt_every, float* dq, float* dk, float* dv,
-                         float* da, float* dalpha, float* dbeta, float* dW,
+                         int ckpt_every, const void* z_stash, float* dq,
+                         float* dk, float* dv, float* da, float* dalpha, float* dbeta, float* dW,
                          float* dw_r, float* dH_0, float state_grad_clip,
                          int64_t B, int64_t T, int64_t N, int64_t qk_heads,
                          int64_t K, int64_t V, m2rnn_dtype dtype,

@@ -32,7 +32,7 @@ EXPORTS = (
     "m2rnn_backward", "m2rnn_sync_status", "m2rnn_forward_state", "m2rnn_backward_state",
     "m2rnn_decode_step", "m2rnn_backward_state_workspace_size", "m2rnn_forward_gated",
     "m2rnn_backward_gated", "m2rnn_output_norm", "m2rnn_output_norm_backward_workspace_size",
-    "m2rnn_output_norm_backward",
+    "m2rnn_output_norm_backward", "m2rnn_z_stash_size",
 )
 
 _lib = None
@@ -74,18 +74,20 @@ def load() -> ctypes.CDLL:
     lib.m2rnn_sync_status.restype = ci
     lib.m2rnn_sync_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.m2rnn_forward_state.restype = ci
-    lib.m2rnn_forward_state.argtypes = [vp] * 10 + [ci] + [i64] * 6 + [ci, vp, sz, vp]
+    lib.m2rnn_forward_state.argtypes = [vp] * 10 + [ci, vp] + [i64] * 6 + [ci, vp, sz, vp]
     lib.m2rnn_backward_state.restype = ci
-    lib.m2rnn_backward_state.argtypes = [vp] * 10 + [ci] + [vp] * 7 + [ctypes.c_float] + [i64] * 6 + [ci, vp, sz, vp]
+    lib.m2rnn_backward_state.argtypes = [vp] * 10 + [ci, vp] + [vp] * 7 + [ctypes.c_float] + [i64] * 6 + [ci, vp, sz, vp]
     lib.m2rnn_backward_state_workspace_size.restype = sz
     lib.m2rnn_backward_state_workspace_size.argtypes = [i64] * 6 + [ci, ci, ci]
     lib.m2rnn_decode_step.restype = ci
     lib.m2rnn_decode_step.argtypes = [vp] * 8 + [i64] * 5 + [ci, vp, sz, vp]
     fl = ctypes.c_float
     lib.m2rnn_forward_gated.restype = ci
-    lib.m2rnn_forward_gated.argtypes = [vp] * 12 + [ci] + [i64] * 6 + [ci, vp, sz, vp]
+    lib.m2rnn_forward_gated.argtypes = [vp] * 12 + [ci, vp] + [i64] * 6 + [ci, vp, sz, vp]
     lib.m2rnn_backward_gated.restype = ci
-    lib.m2rnn_backward_gated.argtypes = [vp] * 12 + [ci] + [vp] * 9 + [fl] + [i64] * 6 + [ci, vp, sz, vp]
+    lib.m2rnn_backward_gated.argtypes = [vp] * 12 + [ci, vp] + [vp] * 9 + [fl] + [i64] * 6 + [ci, vp, sz, vp]
+    lib.m2rnn_z_stash_size.restype = sz
+    lib.m2rnn_z_stash_size.argtypes = [i64] * 5 + [ci]
     lib.m2rnn_output_norm.restype = ci
     lib.m2rnn_output_norm.argtypes = [vp] * 3 + [fl] + [vp] * 2 + [i64] * 4 + [ci, vp]
     lib.m2rnn_output_norm_backward_workspace_size.restype = sz
@@ -139,10 +141,14 @@ def m2rnn_backward(q, k, v, f, W, w_r, dy, dH_T, ckpt, ckpt_every, dq, dk, dv, d
                                  workspace_bytes, stream)
 
 
-def m2rnn_forward_state(q, k, v, f, W, w_r, H_0, y, H_T, ckpt, ckpt_every, B, T, N, qk_heads, K, V,
+def m2rnn_forward_state(q, k, v, f, W, w_r, H_0, y, H_T, ckpt, ckpt_every, z_stash, B, T, N, qk_heads, K, V,
                         dtype, workspace, workspace_bytes, stream) -> int:
-    return load().m2rnn_forward_state(q, k, v, f, W, w_r, H_0, y, H_T, ckpt, ckpt_every, B, T, N,
+    return load().m2rnn_forward_state(q, k, v, f, W, w_r, H_0, y, H_T, ckpt, ckpt_every, z_stash, B, T, N,
                                       qk_heads, K, V, dtype, workspace, workspace_bytes, stream)
+
+
+def m2rnn_z_stash_size(B, T, N, K, V, dtype) -> int:
+    return load().m2rnn_z_stash_size(B, T, N, K, V, dtype)
 
 
 def m2rnn_backward_state_workspace_size(B, T, N, qk_heads, K, V, dtype, ckpt_every, have_ckpt) -> int:
@@ -150,10 +156,10 @@ def m2rnn_backward_state_workspace_size(B, T, N, qk_heads, K, V, dtype, ckpt_eve
                                                       int(bool(have_ckpt)))
 
 
-def m2rnn_backward_state(q, k, v, f, W, w_r, H_0, dy, dH_T, ckpt, ckpt_every, dq, dk, dv, df, dW,
+def m2rnn_backward_state(q, k, v, f, W, w_r, H_0, dy, dH_T, ckpt, ckpt_every, z_stash, dq, dk, dv, df, dW,
                          dw_r, dH_0, state_grad_clip, B, T, N, qk_heads, K, V, dtype, workspace,
                          workspace_bytes, stream) -> int:
-    return load().m2rnn_backward_state(q, k, v, f, W, w_r, H_0, dy, dH_T, ckpt, ckpt_every, dq, dk,
+    return load().m2rnn_backward_state(q, k, v, f, W, w_r, H_0, dy, dH_T, ckpt, ckpt_every, z_stash, dq, dk,
                                        dv, df, dW, dw_r, dH_0, state_grad_clip, B, T, N, qk_heads, K,
                                        V, dtype, workspace, workspace_bytes, stream)
 
@@ -164,17 +170,17 @@ def m2rnn_decode_step(H, q, k, v, f, W, w_r, y, B, N, qk_heads, K, V, dtype, wor
                                     workspace_bytes, stream)
 
 
-def m2rnn_forward_gated(q, k, v, a, alpha, beta, W, w_r, H_0, y, H_T, ckpt, ckpt_every, B, T, N, qk_heads,
-                        K, V, dtype, workspace, workspace_bytes, stream) -> int:
-    return load().m2rnn_forward_gated(q, k, v, a, alpha, beta, W, w_r, H_0, y, H_T, ckpt, ckpt_every, B, T,
+def m2rnn_forward_gated(q, k, v, a, alpha, beta, W, w_r, H_0, y, H_T, ckpt, ckpt_every, z_stash, B, T, N,
+                        qk_heads, K, V, dtype, workspace, workspace_bytes, stream) -> int:
+    return load().m2rnn_forward_gated(q, k, v, a, alpha, beta, W, w_r, H_0, y, H_T, ckpt, ckpt_every, z_stash, B, T,
                                       N, qk_heads, K, V, dtype, workspace, workspace_bytes, stream)
 
 
-def m2rnn_backward_gated(q, k, v, a, alpha, beta, W, w_r, H_0, dy, dH_T, ckpt, ckpt_every, dq, dk, dv, da,
-                         dalpha, dbeta, dW, dw_r, dH_0, state_grad_clip, B, T, N, qk_heads, K, V, dtype,
+def m2rnn_backward_gated(q, k, v, a, alpha, beta, W, w_r, H_0, dy, dH_T, ckpt, ckpt_every, z_stash, dq, dk, dv,
+                         da, dalpha, dbeta, dW, dw_r, dH_0, state_grad_clip, B, T, N, qk_heads, K, V, dtype,
                          workspace, workspace_bytes, stream) -> int:
-    return load().m2rnn_backward_gated(q, k, v, a, alpha, beta, W, w_r, H_0, dy, dH_T, ckpt, ckpt_every, dq,
-                                       dk, dv, da, dalpha, dbeta, dW, dw_r, dH_0, state_grad_clip, B, T, N,
+    return load().m2rnn_backward_gated(q, k, v, a, alpha, beta, W, w_r, H_0, dy, dH_T, ckpt, ckpt_every, z_stash,
+                                       dq, dk, dv, da, dalpha, dbeta, dW, dw_r, dH_0, state_grad_clip, B, T, N,
                                        qk_heads, K, V, dtype, workspace, workspace_bytes, stream)
 
 
@@ -234,14 +240,15 @@ def _shapes(q, v):
 
 
 def forward(q, k, v, f, W, w_r, *, H_0=None, want_state: bool = True, ckpt_every: int = 0,
-            gate=None, out=None, workspace=None, stream=None):
+            gate=None, stash: bool = False, out=None, workspace=None, stream=None):
     """Forward scan on the GPU from ``H_0`` (fp32 [B,N,K,V]; None = zero).
     Returns dict(y, H_T[, ckpt]).
 
     ``ckpt_every`` > 0 also writes the checkpoints the backward can reuse.
     ``gate`` = (a, alpha, beta) with ``f`` None computes the forget gate in
-    the kernels (m2rnn_forward_gated).  ``out`` may hold preallocated y /
-    H_T / ckpt tensors.
+    the kernels (m2rnn_forward_gated).  ``stash`` also returns "z_stash", the
+    fp16 Z_t of every step for ``backward`` (bf16, V = 64 only).  ``out`` may
+    hold preallocated y / H_T / ckpt / z_stash tensors.
     """
     import torch
     B, T, N, K, V, NQ = _shapes(q, v)
@@ -263,36 +270,45 @@ def forward(q, k, v, f, W, w_r, *, H_0=None, want_state: bool = True, ckpt_every
         raise M2RNNError(M2RNN_ERR_INVALID_ARG, "m2rnn_forward_workspace_size")
     if workspace is None:
         workspace = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
+    z_stash = out.get("z_stash")
+    if z_stash is None and stash:
+        zb = m2rnn_z_stash_size(B, T, N, K, V, dt)
+        if zb == 0:
+            raise M2RNNError(M2RNN_ERR_UNSUPPORTED, "m2rnn_z_stash_size")
+        z_stash = torch.empty(zb, device=dev, dtype=torch.uint8)
     ce = ckpt_every if ckpt is not None else 0
     if gate is not None:
         if f is not None:
             raise ValueError("give either f or gate=(a, alpha, beta), not both")
         a, alpha, beta = gate
         st = m2rnn_forward_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(alpha), _ptr(beta), _ptr(W),
-                                 _ptr(w_r), _ptr(H_0), _ptr(y), _ptr(H_T), _ptr(ckpt), ce, B, T, N, NQ, K,
-                                 V, dt, _ptr(workspace), workspace.numel(), _stream_handle(stream))
+                                 _ptr(w_r), _ptr(H_0), _ptr(y), _ptr(H_T), _ptr(ckpt), ce, _ptr(z_stash), B, T,
+                                 N, NQ, K, V, dt, _ptr(workspace), workspace.numel(), _stream_handle(stream))
         _check(st, "m2rnn_forward_gated")
     else:
         st = m2rnn_forward_state(_ptr(q), _ptr(k), _ptr(v), _ptr(f), _ptr(W), _ptr(w_r), _ptr(H_0),
-                                 _ptr(y), _ptr(H_T), _ptr(ckpt), ce, B, T, N, NQ, K, V, dt,
+                                 _ptr(y), _ptr(H_T), _ptr(ckpt), ce, _ptr(z_stash), B, T, N, NQ, K, V, dt,
                                  _ptr(workspace), workspace.numel(), _stream_handle(stream))
         _check(st, "m2rnn_forward_state")
     res = dict(y=y, H_T=H_T, workspace=workspace)
     if ckpt is not None:
         res["ckpt"] = ckpt
+    if z_stash is not None:
+        res["z_stash"] = z_stash
     return res
 
 
 def backward(q, k, v, f, W, w_r, dy, *, dH_T=None, H_0=None, want_dH0: bool = False, ckpt=None,
-             ckpt_every: int = 14, state_grad_clip: float = 0.0, gate=None, out=None, workspace=None,
-             stream=None):
+             ckpt_every: int = 14, state_grad_clip: float = 0.0, gate=None, z_stash=None, out=None,
+             workspace=None, stream=None):
     """Backward scan on the GPU.  Returns dict(dq, dk, dv, df, dW, dw_r[, dH_0]);
     with ``gate`` = (a, alpha, beta) (and ``f`` None) da, dalpha, dbeta
     replace df.
 
     ``H_0`` is the forward's initial state (None = zero); ``ckpt``, if given,
-    must come from a forward with the same ``H_0`` (and gate); ``state_grad_clip``
-    > 0 clamps every new state gradient C_{t-1} to [-c, c]."""
+    must come from a forward with the same ``H_0`` (and gate); ``z_stash``, with
+    that forward's ``ckpt``, replaces the rerun of the transform and tanh;
+    ``state_grad_clip`` > 0 clamps every new state gradient C_{t-1} to [-c, c]."""
     import torch
     B, T, N, K, V, NQ = _shapes(q, v)
     dt = _dtype_code(q)
@@ -324,7 +340,7 @@ def backward(q, k, v, f, W, w_r, dy, *, dH_T=None, H_0=None, want_dH0: bool = Fa
         dbeta = _get("dbeta", (N,))
         st = m2rnn_backward_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(alpha), _ptr(beta), _ptr(W),
                                   _ptr(w_r), _ptr(H_0), _ptr(dy), _ptr(dH_T), _ptr(ckpt), ckpt_every,
-                                  _ptr(dq), _ptr(dk), _ptr(dv), _ptr(da), _ptr(dalpha), _ptr(dbeta), _ptr(dW),
+                                  _ptr(z_stash), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(da), _ptr(dalpha), _ptr(dbeta), _ptr(dW),
                                   _ptr(dw_r), _ptr(dH_0), float(state_grad_clip), B, T, N, NQ, K, V, dt,
                                   _ptr(workspace), workspace.numel(), _stream_handle(stream))
         _check(st, "m2rnn_backward_gated")
@@ -332,8 +348,8 @@ def backward(q, k, v, f, W, w_r, dy, *, dH_T=None, H_0=None, want_dH0: bool = Fa
                    workspace=workspace)
     else:
         st = m2rnn_backward_state(_ptr(q), _ptr(k), _ptr(v), _ptr(f), _ptr(W), _ptr(w_r), _ptr(H_0),
-                                  _ptr(dy), _ptr(dH_T), _ptr(ckpt), ckpt_every, _ptr(dq), _ptr(dk),
-                                  _ptr(dv), _ptr(df), _ptr(dW), _ptr(dw_r), _ptr(dH_0),
+                                  _ptr(dy), _ptr(dH_T), _ptr(ckpt), ckpt_every, _ptr(z_stash), _ptr(dq),
+                                  _ptr(dk), _ptr(dv), _ptr(df), _ptr(dW), _ptr(dw_r), _ptr(dH_0),
                                   float(state_grad_clip), B, T, N, NQ, K, V, dt, _ptr(workspace),
                                   workspace.numel(), _stream_handle(stream))
         _check(st, "m2rnn_backward_state")

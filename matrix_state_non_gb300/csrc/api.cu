@@ -127,6 +127,11 @@ BwdLayout bwd_layout(int64_t B, int64_t T, int64_t N, int64_t K, int64_t V, int 
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA; }
 
+// Shapes whose forward can leave Z_t for the backward (the V = 64 warp-MMA pair).
+bool stash_ok(int64_t K, int64_t V, int dt) {
+  return dt == M2RNN_BF16 && V == 64 && K >= 16 && K <= kMaxDim && K % 16 == 0;
+}
+
 }  // namespace
 
 extern "C" {
@@ -193,12 +198,17 @@ struct GateIn {
 
 int forward_impl(const void* q, const void* k, const void* v, const GateIn& gate, const void* W,
                  const void* w_r, const float* H_0, float* y, float* H_T, float* ckpt, int ckpt_every,
-                 int64_t B, int64_t T, int64_t N, int64_t qk_heads, int64_t K, int64_t V, m2rnn_dtype dtype,
-                 void* workspace, size_t workspace_bytes, void* cuda_stream) {
+                 void* z_stash, int64_t B, int64_t T, int64_t N, int64_t qk_heads, int64_t K, int64_t V,
+                 m2rnn_dtype dtype, void* workspace, size_t workspace_bytes, void* cuda_stream) {
   if (!dtype_ok(dtype) || !dims_ok(B, T, N, K, V)) return M2RNN_ERR_INVALID_ARG;
   if (qk_heads != 1 && qk_heads != N) return M2RNN_ERR_INVALID_ARG;
-  const int path = choose_path(K, V, dtype);
+  int path = choose_path(K, V, dtype);
   if (path < 0) return path;
+  if (z_stash != nullptr) {
+    if (!stash_ok(K, V, dtype)) return M2RNN_ERR_UNSUPPORTED;
+    if (!aligned16(z_stash)) return M2RNN_ERR_INVALID_ARG;
+    path = kPathMma;  // the kernel that writes the stash
+  }
   const void* req[] = {q, k, v, W, w_r, y};
   for (const void* p : req)
     if (p == nullptr || !aligned16(p)) return M2RNN_ERR_INVALID_ARG;
@@ -216,6 +226,7 @@ int forward_impl(const void* q, const void* k, const void* v, const GateIn& gate
   a.q = q; a.k = k; a.v = v; a.f = gate.f; a.W = W; a.w_r = w_r;
   a.gate_a = gate.a; a.gate_alpha = gate.alpha; a.gate_beta = gate.beta;
   a.H0 = H_0; a.qkN = static_cast<int>(qk_heads); a.y = y; a.H_T = H_T; a.ckpt = ckpt;
+  a.zstash = static_cast<uint16_t*>(z_stash);
   a.ckpt_every = ckpt ? ckpt_every : 1;
   a.n_ckpt = ckpt ? (T - 1) / ckpt_every : 0;
   a.B = static_cast<int>(B); a.T = static_cast<int>(T); a.N = static_cast<int>(N);
@@ -232,29 +243,29 @@ extern "C" {
 
 int m2rnn_forward_state(const void* q, const void* k, const void* v, const void* f, const void* W,
                         const void* w_r, const float* H_0, float* y, float* H_T, float* ckpt,
-                        int ckpt_every, int64_t B, int64_t T, int64_t N, int64_t qk_heads, int64_t K,
+                        int ckpt_every, void* z_stash, int64_t B, int64_t T, int64_t N, int64_t qk_heads, int64_t K,
                         int64_t V, m2rnn_dtype dtype, void* workspace, size_t workspace_bytes,
                         void* cuda_stream) {
   if (f == nullptr) return M2RNN_ERR_INVALID_ARG;
-  return forward_impl(q, k, v, GateIn{f, nullptr, nullptr, nullptr}, W, w_r, H_0, y, H_T, ckpt, ckpt_every, B, T,
-                      N, qk_heads, K, V, dtype, workspace, workspace_bytes, cuda_stream);
+  return forward_impl(q, k, v, GateIn{f, nullptr, nullptr, nullptr}, W, w_r, H_0, y, H_T, ckpt, ckpt_every,
+                      z_stash, B, T, N, qk_heads, K, V, dtype, workspace, workspace_bytes, cuda_stream);
 }
 
 int m2rnn_forward_gated(const void* q, const void* k, const void* v, const void* a, const float* alpha,
                         const float* beta, const void* W, const void* w_r, const float* H_0, float* y,
-                        float* H_T, float* ckpt, int ckpt_every, int64_t B, int64_t T, int64_t N,
+                        float* H_T, float* ckpt, int ckpt_every, void* z_stash, int64_t B, int64_t T, int64_t N,
                         int64_t qk_heads, int64_t K, int64_t V, m2rnn_dtype dtype, void* workspace,
                         size_t workspace_bytes, void* cuda_stream) {
   if (a == nullptr) return M2RNN_ERR_INVALID_ARG;
-  return forward_impl(q, k, v, GateIn{nullptr, a, alpha, beta}, W, w_r, H_0, y, H_T, ckpt, ckpt_every, B, T, N,
-                      qk_heads, K, V, dtype, workspace, workspace_bytes, cuda_stream);
+  return forward_impl(q, k, v, GateIn{nullptr, a, alpha, beta}, W, w_r, H_0, y, H_T, ckpt, ckpt_every, z_stash,
+                      B, T, N, qk_heads, K, V, dtype, workspace, workspace_bytes, cuda_stream);
 }
 
 int m2rnn_forward(const void* q, const void* k, const void* v, const void* f, const void* W,
                   const void* w_r, float* y, float* H_T, float* ckpt, int ckpt_every, int64_t B,
                   int64_t T, int64_t N, int64_t K, int64_t V, m2rnn_dtype dtype, void* workspace,
                   size_t workspace_bytes, void* cuda_stream) {
-  return m2rnn_forward_state(q, k, v, f, W, w_r, nullptr, y, H_T, ckpt, ckpt_every, B, T, N, N, K, V,
+  return m2rnn_forward_state(q, k, v, f, W, w_r, nullptr, y, H_T, ckpt, ckpt_every, nullptr, B, T, N, N, K, V,
                              dtype, workspace, workspace_bytes, cuda_stream);
 }
 
@@ -277,7 +288,7 @@ int m2rnn_decode_step(float* H, const void* q, const void* k, const void* v, con
   }
   // Otherwise the scan kernels with T = 1, from H to H: every kernel reads a
   // state element before the same thread block overwrites it.
-  return m2rnn_forward_state(q, k, v, f, W, w_r, H, y, H, nullptr, 0, B, 1, N, qk_heads, K, V, dtype,
+  return m2rnn_forward_state(q, k, v, f, W, w_r, H, y, H, nullptr, 0, nullptr, B, 1, N, qk_heads, K, V, dtype,
                              workspace, workspace_bytes, cuda_stream);
 }
 
@@ -289,7 +300,7 @@ namespace {
 // then becomes da in place, and dalpha, dbeta [N] are written.
 int backward_impl(const void* q, const void* k, const void* v, const GateIn& gate, const void* W,
                   const void* w_r, const float* H_0, const float* dy, const float* dH_T, const float* ckpt,
-                  int ckpt_every, float* dq, float* dk, float* dv, float* df, float* dalpha, float* dbeta,
+                  int ckpt_every, const void* z_stash, float* dq, float* dk, float* dv, float* df, float* dalpha, float* dbeta,
                   float* dW, float* dw_r, float* dH_0, float state_grad_clip, int64_t B, int64_t T, int64_t N,
                   int64_t qk_heads, int64_t K, int64_t V, m2rnn_dtype dtype, void* workspace,
                   size_t workspace_bytes, void* cuda_stream) {
@@ -299,8 +310,14 @@ int backward_impl(const void* q, const void* k, const void* v, const GateIn& gat
   const bool shared_qk = qk_heads == 1 && N > 1;
   const int path = choose_path(K, V, dtype);
   if (path < 0) return path;
-  const int bpath = choose_bwd_path(K, V, dtype, ckpt_every);
+  int bpath = choose_bwd_path(K, V, dtype, ckpt_every);
   if (ckpt_every < 1 || ckpt_every > kMaxCkptEvery) return M2RNN_ERR_INVALID_ARG;
+  if (z_stash != nullptr) {
+    if (!stash_ok(K, V, dtype) || ckpt_every > mma_backward_max_chunk()) return M2RNN_ERR_UNSUPPORTED;
+    if (!aligned16(z_stash)) return M2RNN_ERR_INVALID_ARG;
+    if (ckpt == nullptr && (T - 1) / ckpt_every > 0) return M2RNN_ERR_INVALID_ARG;  // stash and checkpoints go together
+    bpath = kPathMma;  // the kernel that reads the stash
+  }
   const void* req[] = {q, k, v, W, w_r, dy, dq, dk, dv, df, dW, dw_r};
   for (const void* p : req)
     if (p == nullptr || !aligned16(p)) return M2RNN_ERR_INVALID_ARG;
@@ -341,6 +358,7 @@ int backward_impl(const void* q, const void* k, const void* v, const GateIn& gat
   a.q = q; a.k = k; a.v = v; a.f = gate.f; a.W = W; a.w_r = w_r;
   a.gate_a = gate.a; a.gate_alpha = gate.alpha; a.gate_beta = gate.beta;
   a.dy = dy; a.dH_T = dH_T; a.H0 = H_0; a.ckpt = ck; a.ckpt_every = ckpt_every; a.n_ckpt = nck;
+  a.zstash = static_cast<const uint16_t*>(z_stash);
   a.dq = dq; a.dk = dk; a.dv = dv; a.df = df; a.dW = dW; a.dw_r = dw_r; a.dH0 = dH_0;
   a.clip = state_grad_clip;
   a.qkN = static_cast<int>(qk_heads);
@@ -384,28 +402,34 @@ extern "C" {
 
 int m2rnn_backward_state(const void* q, const void* k, const void* v, const void* f,
                          const void* W, const void* w_r, const float* H_0, const float* dy,
-                         const float* dH_T, const float* ckpt, int ckpt_every, float* dq,
+                         const float* dH_T, const float* ckpt, int ckpt_every, const void* z_stash, float* dq,
                          float* dk, float* dv, float* df, float* dW, float* dw_r, float* dH_0,
                          float state_grad_clip, int64_t B, int64_t T, int64_t N, int64_t qk_heads,
                          int64_t K, int64_t V, m2rnn_dtype dtype, void* workspace, size_t workspace_bytes,
                          void* cuda_stream) {
   if (f == nullptr) return M2RNN_ERR_INVALID_ARG;
   return backward_impl(q, k, v, GateIn{f, nullptr, nullptr, nullptr}, W, w_r, H_0, dy, dH_T, ckpt, ckpt_every,
-                       dq, dk, dv, df, nullptr, nullptr, dW, dw_r, dH_0, state_grad_clip, B, T, N, qk_heads, K,
+                       z_stash, dq, dk, dv, df, nullptr, nullptr, dW, dw_r, dH_0, state_grad_clip, B, T, N, qk_heads, K,
                        V, dtype, workspace, workspace_bytes, cuda_stream);
 }
 
 int m2rnn_backward_gated(const void* q, const void* k, const void* v, const void* a, const float* alpha,
                          const float* beta, const void* W, const void* w_r, const float* H_0, const float* dy,
-                         const float* dH_T, const float* ckpt, int ckpt_every, float* dq, float* dk, float* dv,
+                         const float* dH_T, const float* ckpt, int ckpt_every, const void* z_stash, float* dq, float* dk, float* dv,
                          float* da, float* dalpha, float* dbeta, float* dW, float* dw_r, float* dH_0,
                          float state_grad_clip, int64_t B, int64_t T, int64_t N, int64_t qk_heads, int64_t K,
                          int64_t V, m2rnn_dtype dtype, void* workspace, size_t workspace_bytes,
                          void* cuda_stream) {
   if (a == nullptr) return M2RNN_ERR_INVALID_ARG;
-  return backward_impl(q, k, v, GateIn{nullptr, a, alpha, beta}, W, w_r, H_0, dy, dH_T, ckpt, ckpt_every, dq, dk,
+  return backward_impl(q, k, v, GateIn{nullptr, a, alpha, beta}, W, w_r, H_0, dy, dH_T, ckpt, ckpt_every, z_stash,
+                       dq, dk,
                        dv, da, dalpha, dbeta, dW, dw_r, dH_0, state_grad_clip, B, T, N, qk_heads, K, V, dtype,
                        workspace, workspace_bytes, cuda_stream);
+}
+
+size_t m2rnn_z_stash_size(int64_t B, int64_t T, int64_t N, int64_t K, int64_t V, m2rnn_dtype dtype) {
+  if (!dims_ok(B, T, N, K, V) || !stash_ok(K, V, dtype)) return 0;
+  return static_cast<size_t>(B) * T * N * K * V * 2;
 }
 
 size_t m2rnn_output_norm_backward_workspace_size(int64_t B, int64_t T, int64_t N, int64_t V) {
@@ -447,7 +471,7 @@ int m2rnn_backward(const void* q, const void* k, const void* v, const void* f, c
                    int ckpt_every, float* dq, float* dk, float* dv, float* df, float* dW,
                    float* dw_r, int64_t B, int64_t T, int64_t N, int64_t K, int64_t V,
                    m2rnn_dtype dtype, void* workspace, size_t workspace_bytes, void* cuda_stream) {
-  return m2rnn_backward_state(q, k, v, f, W, w_r, nullptr, dy, dH_T, ckpt, ckpt_every, dq, dk, dv,
+  return m2rnn_backward_state(q, k, v, f, W, w_r, nullptr, dy, dH_T, ckpt, ckpt_every, nullptr, dq, dk, dv,
                               df, dW, dw_r, nullptr, 0.f, B, T, N, N, K, V, dtype, workspace,
                               workspace_bytes, cuda_stream);
 }

@@ -37,7 +37,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) decode_step_kernel(
     status->detail = 0u;
   }
   __shared__ float ypart[kMaxWarps][kV];
-  __shared__ __align__(128) uint8_t wtile[4][2048];  // W as four 16 x 64 bf16 k-tiles (swizzled)
+  __shared__ __align__(128) uint8_t wtile[4][2048];  // W as four 16 x 64 fp16 k-tiles (swizzled)
   const int chain = blockIdx.x, n = chain % N;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int g = lane >> 2, qd = lane & 3;
@@ -62,8 +62,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32) decode_step_kernel(
   }
   for (int e = threadIdx.x; e < kV * kV / 8; e += blockDim.x) {  // 16-byte chunks of W
     const int row = e >> 3, col = (e & 7) * 8;
-    const uint4 x = *reinterpret_cast<const uint4*>(Wn + row * kV + col);
-    *reinterpret_cast<uint4*>(wtile[row >> 4] + tile_off(row & 15, col)) = x;
+    const uint4 x = *reinterpret_cast<const uint4*>(Wn + row * kV + col);  // bf16, re-encoded as fp16
+    *reinterpret_cast<uint4*>(wtile[row >> 4] + tile_off(row & 15, col)) =
+        make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z), bf16x2_to_f16x2(x.w));
   }
   __syncthreads();
   const float k0 = bf16_bits_to_f32(kc[16 * warp + g]), k1 = bf16_bits_to_f32(kc[16 * warp + g + 8]);
@@ -79,18 +80,20 @@ __global__ void __launch_bounds__(kMaxWarps * 32) decode_step_kernel(
   }
 #pragma unroll
   for (int kt = 0; kt < 4; ++kt) {
-    uint32_t a[4];  // bf16(H) k-tile kt = n-tiles 2kt, 2kt+1 of the accumulator layout
-    a[0] = pack2_bf16(h[2 * kt][0], h[2 * kt][1]);
-    a[1] = pack2_bf16(h[2 * kt][2], h[2 * kt][3]);
-    a[2] = pack2_bf16(h[2 * kt + 1][0], h[2 * kt + 1][1]);
-    a[3] = pack2_bf16(h[2 * kt + 1][2], h[2 * kt + 1][3]);
+    // fp16 k-tile kt of H = n-tiles 2kt, 2kt+1 of the accumulator layout
+    // (the scan kernels' operand precision).
+    uint32_t a[4];
+    a[0] = pack2_f16(h[2 * kt][0], h[2 * kt][1]);
+    a[1] = pack2_f16(h[2 * kt][2], h[2 * kt][3]);
+    a[2] = pack2_f16(h[2 * kt + 1][0], h[2 * kt + 1][1]);
+    a[3] = pack2_f16(h[2 * kt + 1][2], h[2 * kt + 1][3]);
     const uint32_t wt = smem_u32(wtile[kt]);
 #pragma unroll
     for (int nt2 = 0; nt2 < 4; ++nt2) {
       uint32_t bd[4];  // B fragments (k = W row, n = W column) of n-tiles 2nt2, 2nt2+1
       ldmatrix_x4_trans(bd, ldsm_addr_b_trans(wt, nt2, lane));
-      mma_bf16_16816(acc[2 * nt2], a, bd[0], bd[1]);
-      mma_bf16_16816(acc[2 * nt2 + 1], a, bd[2], bd[3]);
+      mma_f16_16816(acc[2 * nt2], a, bd[0], bd[1]);
+      mma_f16_16816(acc[2 * nt2 + 1], a, bd[2], bd[3]);
     }
   }
   const float q0 = bf16_bits_to_f32(qc[16 * warp + g]), q1 = bf16_bits_to_f32(qc[16 * warp + g + 8]);

@@ -23,6 +23,7 @@ struct FwdArgs {
   const void* gate_a;        // non-null: f = exp(-alpha softplus(a + beta)) from a [B,T,N] (input dtype)
   const float* gate_alpha;   // [N]
   const float* gate_beta;    // [N]
+  uint16_t* zstash;  // V = 64 warp-MMA forward: fp16 Z_t of every step for the backward, or null
   float* y;      // may be null (checkpoint-only pass)
   float* H_T;    // may be null
   float* ckpt;   // may be null
@@ -50,6 +51,7 @@ struct BwdArgs {
   const float* gate_beta;
   float clip;         // > 0: every new C_{t-1} clamped to [-clip, clip]; else no clipping
   const float* ckpt;  // never null here (recomputed by the caller layer if needed)
+  const uint16_t* zstash;  // the forward's Z stash (V = 64 warp-MMA backward), or null: rerun the forward
   int ckpt_every;
   int64_t n_ckpt;
   float* dq;

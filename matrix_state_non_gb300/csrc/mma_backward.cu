@@ -26,7 +26,11 @@
 //                   next chunk (Eq. 10-11), caching each thread's Z_t and
 //                   H_{t-1} values (fp32) in its own lane of tensor memory, so
 //                   the cache never touches DRAM; also dq_t = H_t u_t and the
-//                   chunk loads (TMA);
+//                   chunk loads (TMA).  When the forward left its Z_t in a
+//                   stash (fp16), the rerun is only H_t = H_{t-1} + (1-f_t)
+//                   (Z_t - H_{t-1}) from the chunk's checkpoint, with Z_t
+//                   bulk-copied a chunk at a time: no MMA, no tanh, no
+//                   exchange between the warps;
 //   gradient warps  dW += H_{t-1}^T D_t as one tcgen05 MMA per step into a
 //                   tensor-memory accumulator, and the fixed-order sums of
 //                   the dk, dv, df shares and dw_r.
@@ -90,7 +94,7 @@ struct MmaBwdParams {
   int nchunks;
   int nbuf;  // TMEM cache buffers: 2 if ckpt_every <= kTwoBufChunk, else 1
   uint32_t htile_off, cbuf_off, cbuf_bytes, cq_off, ck_off, cv_off, cdy_off, cf_off;
-  uint32_t xring_off, dqp_off, dwr_off, bar_off, misc_off;
+  uint32_t xring_off, dqp_off, dwr_off, bar_off, misc_off, zbuf_off;
   uint32_t tx_bytes;
   float* dvp;  // [B*T*N][R][V]: row-block partials of D^T k
   float* dfp;  // [B*T*N][R]:    row-block partials of df
@@ -118,6 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* xfull = tfree + 2;
   uint64_t* xempty = xfull + kNX;
   uint64_t* dwdone = xempty + kNX;
+  uint64_t* zfull = dwdone + 1;  // [2]: Z stash chunk buffers
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.misc_off);
   volatile int* vabort = reinterpret_cast<volatile int*>(smem + p.misc_off + 4);
   volatile int* rabort = reinterpret_cast<volatile int*>(smem + p.misc_off + 8);
@@ -140,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&xempty[i]), 2);    // the dW MMA's commit + the step's duty warp
     }
     mbar_init(smem_u32(dwdone), 1);          // every dW MMA complete
+    for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&zfull[i]), 1);  // the loading lane (+ bulk bytes)
     *abort_flag = 0;
     *vabort = 0;
     *rabort = 0;
@@ -369,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) *abort_flag = 1;
   } else if (warp < 8) {
     // ======================= recompute warps (Eq. 10-11) =======================
-    // Forward transform fragments: B[k][col] = W[k][16w + col], k-tiles in
+    // Forward transform fragments (fp16): B[k][col] = W[k][16w + col], k-tiles in
     // the order w, w+1, w+2, w+3 (mod 4): the first is this warp's own 16
     // columns of H, whose A fragments it holds in registers.
     uint32_t bw[2][4][2];
@@ -379,10 +385,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int kt = 0; kt < 4; ++kt) {
         const int k0 = 16 * ((w + kt) & 3) + 2 * qd;
-        bw[nt][kt][0] = static_cast<uint32_t>(Wg[k0 * kV + col]) |
-                        (static_cast<uint32_t>(Wg[(k0 + 1) * kV + col]) << 16);
-        bw[nt][kt][1] = static_cast<uint32_t>(Wg[(k0 + 8) * kV + col]) |
-                        (static_cast<uint32_t>(Wg[(k0 + 9) * kV + col]) << 16);
+        bw[nt][kt][0] = bf16x2_to_f16x2(static_cast<uint32_t>(Wg[k0 * kV + col]) |
+                                        (static_cast<uint32_t>(Wg[(k0 + 1) * kV + col]) << 16));
+        bw[nt][kt][1] = bf16x2_to_f16x2(static_cast<uint32_t>(Wg[(k0 + 8) * kV + col]) |
+                                        (static_cast<uint32_t>(Wg[(k0 + 9) * kV + col]) << 16));
+        if (!f16x2_finite(bw[nt][kt][0]) || !f16x2_finite(bw[nt][kt][1]))
+          report_device_error(status, kStatusCheck, kWhereWRange);
       }
     }
     const uint32_t htile0 = smem_u32(smem + p.htile_off);
@@ -433,12 +441,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane < CL) cfw[lane] = fv;
       mbar_arrive(smem_u32(&cfull[li % kCBufs]));  // all 32 lanes: the phase's arrival count
     };
+    // Z stash: chunk li's steps into buffer li % nbuf (one bulk copy).
+    const bool zs = A.zstash != nullptr;
+    const uint8_t* zsrc = reinterpret_cast<const uint8_t*>(A.zstash) + static_cast<int64_t>(blockIdx.x) * T * kZStepBytes;
+    auto issue_z = [&](int li) {
+      if (lane == 0) {
+        const int t0 = (p.nchunks - 1 - li) * CL;
+        const uint32_t bytes = static_cast<uint32_t>(min(CL, T - t0)) * kZStepBytes;
+        const uint32_t zb = smem_u32(&zfull[li % p.nbuf]);
+        mbar_arrive_expect_tx(zb, bytes);
+        bulk_load(smem_u32(smem + p.zbuf_off) + (li % p.nbuf) * CL * kZStepBytes, zsrc + static_cast<int64_t>(t0) * kZStepBytes,
+                  bytes, zb);
+      }
+    };
+    int zissued = 0;  // Z chunks whose copies have been issued
     if (loader) {
       if (lane == 0) {
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         tma_prefetch_desc(&tm_dy);
+      }
+      if (zs) {
+        for (; zissued < min(p.nbuf, p.nchunks); ++zissued) issue_z(zissued);
       }
       publish_chunk(0, issue_chunk(0));
     }
@@ -459,6 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (mine && ci >= 3 && ci + 1 < p.nchunks)
         mine = mbar_wait_timed(smem_u32(&cempty[(ci + 1) % kCBufs]), ((ci - 3) / kCBufs) & 1, status,
                                kWhereBwdCEmpty);
+      if (mine && zs)
+        mine = mbar_wait_timed(smem_u32(&zfull[ci % p.nbuf]), (ci / p.nbuf) & 1, status, kWhereBwdZFull);
       if (!mine) *rabort = 1;
       named_bar_sync(2, 128);
       if (*rabort) {
@@ -481,64 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) h[nt][e] = hnext[nt][e];
       if (c > 0) load_start(c - 1, hnext);
-      // Step s: acc = k_s v_s^T + H_{s-1} W with H_{s-1}'s own k-tile taken
-      // from registers (while the other three load from the bf16 tile).
-      uint32_t hown[4];
-      hown[0] = pack2_bf16(h[0][0], h[0][1]);
-      hown[1] = pack2_bf16(h[0][2], h[0][3]);
-      hown[2] = pack2_bf16(h[1][0], h[1][1]);
-      hown[3] = pack2_bf16(h[1][2], h[1][3]);
-      st_shared_b32(htile0 + tile_off(g, jcol0), hown[0]);
-      st_shared_b32(htile0 + tile_off(g + 8, jcol0), hown[1]);
-      st_shared_b32(htile0 + tile_off(g, jcol0 + 8), hown[2]);
-      st_shared_b32(htile0 + tile_off(g + 8, jcol0 + 8), hown[3]);
-      float acc[2][4];
-      auto start_step = [&](int s) {
-        const float k0 = bf16_bits_to_f32(ck[s * kRows + g]);
-        const float k1 = bf16_bits_to_f32(ck[s * kRows + g + 8]);
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const uint32_t vv = *reinterpret_cast<const uint32_t*>(cv + s * kV + jcol0 + 8 * nt);
-          const float v0 = bf16lo(vv), v1 = bf16hi(vv);
-          acc[nt][0] = k0 * v0;
-          acc[nt][1] = k0 * v1;
-          acc[nt][2] = k1 * v0;
-          acc[nt][3] = k1 * v1;
-          mma_bf16_16816(acc[nt], hown, bw[nt][0][0], bw[nt][0][1]);
-        }
-      };
-      named_bar_sync(2, 128);
-      for (int s = 0; s < L; ++s) {
-        const float omf = 1.f - cf[s];
-        const uint32_t atile = htile0 + (s & 1) * 2048;
-        uint32_t af[3][4];
-#pragma unroll
-        for (int i = 0; i < 3; ++i) ldmatrix_x4(af[i], ldsm_addr_a(atile, (w + 1 + i) & 3, lane));
-        start_step(s);
-#pragma unroll
-        for (int i = 0; i < 3; ++i)
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) mma_bf16_16816(acc[nt], af[i], bw[nt][i + 1][0], bw[nt][i + 1][1]);
-        const uint32_t otile = htile0 + ((s + 1) & 1) * 2048;
-        uint32_t cache[16];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float z = tanh_fast(acc[nt][e]);
-            cache[4 * nt + e] = __float_as_uint(z);
-            cache[8 + 4 * nt + e] = __float_as_uint(h[nt][e]);  // H_{s-1}
-            h[nt][e] = fmaf(omf, z - h[nt][e], h[nt][e]);
-          }
-        hown[0] = pack2_bf16(h[0][0], h[0][1]);
-        hown[1] = pack2_bf16(h[0][2], h[0][3]);
-        hown[2] = pack2_bf16(h[1][0], h[1][1]);
-        hown[3] = pack2_bf16(h[1][2], h[1][3]);
-        st_shared_b32(otile + tile_off(g, jcol0), hown[0]);
-        st_shared_b32(otile + tile_off(g + 8, jcol0), hown[1]);
-        st_shared_b32(otile + tile_off(g, jcol0 + 8), hown[2]);
-        st_shared_b32(otile + tile_off(g + 8, jcol0 + 8), hown[3]);
-        tmem_st_32x32b_x16(tbuf + 16 * s, cache);
+      auto dq_share = [&](int s, const float (&h)[2][4]) {
         // dq_t = H_t u_t: this thread's share (its four columns, rows g and
         // g + 8); the sixteen shares of a row are summed at the chunk's end.
         {
@@ -554,7 +524,91 @@ __global__ void __launch_bounds__(kThreads, 1)
           p1 = fmaf(h[1][3], u1.y, p1);
           *reinterpret_cast<float2*>(dqp + (s * 16 + w * 4 + qd) * kRows + 2 * g) = make_float2(p0, p1);
         }
+      };
+      if (zs) {
+        // Z_t from the stash; the state advances by the gate blend alone.
+        const uint32_t zb = smem_u32(smem + p.zbuf_off) + (ci % p.nbuf) * CL * kZStepBytes + (w * 32 + lane) * 16;
+        for (int s = 0; s < L; ++s) {
+          const float omf = 1.f - cf[s];
+          const uint4 zq = ld_shared_v4(zb + s * kZStepBytes);
+          const float z[2][4] = {{f16lo(zq.x), f16hi(zq.x), f16lo(zq.y), f16hi(zq.y)},
+                                 {f16lo(zq.z), f16hi(zq.z), f16lo(zq.w), f16hi(zq.w)}};
+          uint32_t cache[16];
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              cache[4 * nt + e] = __float_as_uint(z[nt][e]);
+              cache[8 + 4 * nt + e] = __float_as_uint(h[nt][e]);  // H_{s-1}
+              h[nt][e] = fmaf(omf, z[nt][e] - h[nt][e], h[nt][e]);
+            }
+          tmem_st_32x32b_x16(tbuf + 16 * s, cache);
+          dq_share(s, h);
+        }
+        // Every read of this Z buffer and every dq share of the chunk is done.
         named_bar_sync(2, 128);
+        if (loader && zissued < p.nchunks) issue_z(zissued++);
+      } else {
+        // Step s, as in the forward: acc = k_s v_s^T + fp16(H_{s-1}) W, the
+        // own k-tile from registers while the other three load from the tile.
+        uint32_t hh[4];
+        auto split = [&]() {
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            hh[2 * nt] = pack2_f16(h[nt][0], h[nt][1]);
+            hh[2 * nt + 1] = pack2_f16(h[nt][2], h[nt][3]);
+          }
+        };
+        auto store_tile = [&](uint32_t base) {
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            const int col = jcol0 + 8 * nt;
+            st_shared_b32(base + tile_off(g, col), hh[2 * nt]);
+            st_shared_b32(base + tile_off(g + 8, col), hh[2 * nt + 1]);
+          }
+        };
+        split();
+        store_tile(htile0);
+        named_bar_sync(2, 128);
+        for (int s = 0; s < L; ++s) {
+          const float omf = 1.f - cf[s];
+          const uint32_t atile = htile0 + (s & 1) * 2048;
+          uint32_t af[3][4];
+#pragma unroll
+          for (int i = 0; i < 3; ++i) ldmatrix_x4(af[i], ldsm_addr_a(atile, (w + 1 + i) & 3, lane));
+          float acc[2][4];
+          const float k0 = bf16_bits_to_f32(ck[s * kRows + g]);
+          const float k1 = bf16_bits_to_f32(ck[s * kRows + g + 8]);
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            const uint32_t vv = *reinterpret_cast<const uint32_t*>(cv + s * kV + jcol0 + 8 * nt);
+            const float v0 = bf16lo(vv), v1 = bf16hi(vv);
+            acc[nt][0] = k0 * v0;
+            acc[nt][1] = k0 * v1;
+            acc[nt][2] = k1 * v0;
+            acc[nt][3] = k1 * v1;
+            mma_f16_16816(acc[nt], hh, bw[nt][0][0], bw[nt][0][1]);
+          }
+#pragma unroll
+          for (int i = 0; i < 3; ++i)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) mma_f16_16816(acc[nt], af[i], bw[nt][i + 1][0], bw[nt][i + 1][1]);
+          uint32_t cache[16];
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float z = tanh_fast(acc[nt][e]);
+              cache[4 * nt + e] = __float_as_uint(z);
+              cache[8 + 4 * nt + e] = __float_as_uint(h[nt][e]);  // H_{s-1}
+              h[nt][e] = fmaf(omf, z - h[nt][e], h[nt][e]);
+            }
+          split();
+          store_tile(htile0 + ((s + 1) & 1) * 2048);
+          tmem_st_32x32b_x16(tbuf + 16 * s, cache);
+          dq_share(s, h);
+          named_bar_sync(2, 128);
+        }
       }
       tmem_st_wait();
       if (more) publish_chunk(ci + 1, fnext);
@@ -577,9 +631,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) {
       *abort_flag = 1;
       // No TMA copy may still be writing when the CTA exits.
-      if (loader)
+      if (loader) {
         for (int li = max(0, issued - 2); li < min(issued, p.nchunks); ++li)
           mbar_wait_timed(smem_u32(&cfull[li % kCBufs]), (li / kCBufs) & 1, nullptr, kWhereBwdDrain);
+        for (int li = max(0, zissued - p.nbuf); li < zissued; ++li)
+          mbar_wait_timed(smem_u32(&zfull[li % p.nbuf]), (li / p.nbuf) & 1, nullptr, kWhereBwdDrain);
+      }
     }
   } else {
     // ======================= gradient warps =======================
@@ -784,7 +841,7 @@ cudaError_t launch_mma_backward(const BwdArgs& a, cudaStream_t stream) {
   const int C = a.ckpt_every;
   p.nchunks = (a.T + C - 1) / C;
   p.nbuf = (C <= kTwoBufChunk) ? 2 : 1;
-  p.htile_off = 0;
+  p.htile_off = 0;  // two 2 KB fp16 tiles for the rerun
   p.cbuf_off = 4096;
   p.cq_off = 0;
   p.ck_off = align_up(C * kRows * 2, 128);
@@ -796,8 +853,10 @@ cudaError_t launch_mma_backward(const BwdArgs& a, cudaStream_t stream) {
   p.dqp_off = p.xring_off + kNX * kXSlotBytes;
   p.dwr_off = p.dqp_off + kMaxChunk * 16 * kRows * 4;
   p.bar_off = p.dwr_off + 4 * kV * 4;
-  p.misc_off = p.bar_off + (2 * kCBufs + 4 + 2 * kNX + 1) * 8;
-  const uint32_t smem = align_up(p.misc_off + 32, 128) + 1024;
+  p.misc_off = p.bar_off + (2 * kCBufs + 4 + 2 * kNX + 1 + 2) * 8;
+  p.zbuf_off = align_up(p.misc_off + 32, 128);
+  const uint32_t zbytes = a.zstash != nullptr ? static_cast<uint32_t>(p.nbuf * C) * kZStepBytes : 0u;
+  const uint32_t smem = p.zbuf_off + zbytes + 1024;
   p.tx_bytes = 2 * C * kRows * 2 + C * kV * 2 + C * kV * 4;
   const size_t rows = static_cast<size_t>(a.B) * a.T * a.N;
   p.dvp = a.scratch;

@@ -28,6 +28,16 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// The same with fp16 operands (A and B both fp16).
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -83,6 +93,58 @@ __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w &
 __device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// Streaming (evict-first) 16-byte global store: data read back much later.
+__device__ __forceinline__ void st_global_cs_v4(void* ptr, uint4 v) {
+  asm volatile("st.global.cs.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// fp16 pairs (IEEE binary16, round to nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t pack2_f16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float f16lo(uint32_t w) {
+  float f;
+  asm("{\n .reg .f16 l, h;\n mov.b32 {l, h}, %1;\n cvt.f32.f16 %0, l;\n}" : "=f"(f) : "r"(w));
+  return f;
+}
+__device__ __forceinline__ float f16hi(uint32_t w) {
+  float f;
+  asm("{\n .reg .f16 l, h;\n mov.b32 {l, h}, %1;\n cvt.f32.f16 %0, h;\n}" : "=f"(f) : "r"(w));
+  return f;
+}
+
+// A pair of bf16 inputs re-encoded as fp16 (exact for magnitudes in fp16's
+// normal range; |x| >= 65520 becomes infinite, see f16x2_finite).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) { return pack2_f16(bf16lo(w), bf16hi(w)); }
+__device__ __forceinline__ bool f16x2_finite(uint32_t x) {
+  return (x & 0x7C00u) != 0x7C00u && (x & 0x7C000000u) != 0x7C000000u;
+}
+
+// The recurrent state enters the state-transform MMAs as fp16 (|H| <= 1, 11
+// significant bits) with W re-encoded as fp16: a bf16 state operand (8 bits)
+// perturbs Z_t by ~2e-3 relative, and the backward chain can amplify that
+// over thousands of steps; fp16 cuts it eightfold at no extra cost.
+
+// The Z stash written by the V = 64 warp-MMA forward for its backward: for
+// each (chain, row block) and step, 2 KB = 4 warps x 32 lanes x 8 fp16, lane
+// order as the accumulator fragments (values Z[g][j], Z[g][j+1], Z[g+8][j],
+// Z[g+8][j+1] for j = 16w + 2qd and then j + 8).  One row block's steps are
+// contiguous, so a chunk of steps is one bulk copy.
+constexpr uint32_t kZStepBytes = 2048;
 
 // Bounded wait without the CTA-wide abort flag: used by the compute warps,
 // which then agree on the outcome through a flag read after a named barrier.

@@ -10,12 +10,13 @@
 // section 1.2), one CTA each; the CTAs of a chain form a cluster and sum the
 // readout through distributed shared memory, as in the tensor-memory kernel.
 // Inside a CTA four compute warps own 16 value columns each of the 16 x 64
-// state.  Per step a warp runs D = bf16(H_{t-1}) * W[:, its 16 columns] + k v^T
-// as eight m16n8k16 warp MMAs (W fragments live in registers for the whole
-// scan, the rank-1 write seeds the accumulator exactly), applies tanh and the
-// gate blend to its 8 fp32 state values per thread, and writes bf16(H_t) to a
-// swizzled shared tile that the four warps read back with ldmatrix after one
-// named barrier.  The readout of step t-1 runs on the tensor core too, while
+// state.  Per step a warp runs D = H_{t-1} * W[:, its 16 columns] + k v^T as
+// eight m16n8k16 warp MMAs with fp16 operands (H_{t-1} rounded to fp16, W
+// re-encoded as fp16 and held in registers for the whole scan; the rank-1
+// write seeds the accumulator exactly), applies tanh and the gate blend to
+// its 8 fp32 state values per thread, and writes fp16(H_t) to a swizzled
+// shared tile that the four warps read back with ldmatrix after one named
+// barrier.  The readout of step t-1 runs on the tensor core too, while
 // the step-t MMAs are in flight: y^T = q^T H_{t-1} as one m16n8k16 per column
 // tile with q replicated over the A rows and H_{t-1} (fp32, split into bf16
 // high and low parts, transposed into B fragments with movmatrix) as B, so the
@@ -55,7 +56,9 @@ struct MmaFwdParams {
   uint32_t tx_bytes;
 };
 
-template <int NT>
+// Compile-time modes (a per-step branch costs ~20-30 ns of a ~250 ns step,
+// measured): kY = readout y, kCk = checkpoints, kZ = the Z stash.
+template <int NT, bool kY, bool kCk, bool kZ>
 __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
     mma_forward_kernel(const __grid_constant__ MmaFwdParams p, const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
@@ -68,7 +71,7 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
   const int chain = static_cast<int>(blockIdx.x) / R;
   const int b = chain / N, n = chain % N;
   const int ntiles = p.ntiles;
-  const bool do_y = p.a.y != nullptr;
+  constexpr bool do_y = kY;
   StatusBlock* status = p.a.status;
   constexpr int CW = 8 / NT;        // compute warps
   constexpr int NCOL = 8 * NT;      // value columns per compute warp
@@ -84,7 +87,7 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
   uint64_t* yempty = ypeer + kYS;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.misc_off);
   volatile int* cabort = reinterpret_cast<volatile int*>(smem + p.misc_off + 4);
-  const uint32_t abuf0 = smem_u32(smem + p.abuf_off);  // two 2 KB bf16 tiles
+  const uint32_t abuf0 = smem_u32(smem + p.abuf_off);  // two 2 KB fp16 tiles
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNS; ++i) {
@@ -106,75 +109,95 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
 
   if (warp < CW) {
     // ---------------- compute warps ----------------
+    static_assert(NT == 2, "four compute warps of 16 value columns");
     const int g = lane >> 2, qd = lane & 3;
     const int w = warp;
-    // W fragments for this warp's output columns: B[k][n] = W[k][NCOL w + n].
-    // With NT = 2 a warp's 16 columns of H are one k-tile, whose A fragments
-    // it holds in registers: the k-tiles are stored in the order w, w+1,
-    // w+2, w+3 (mod 4) so that the first is its own.
+    // W fragments for this warp's output columns: B[k][n] = W[k][16 w + n].
+    // A warp's 16 columns of H are one k-tile, whose A fragments it holds in
+    // registers: the k-tiles are stored in the order w, w+1, w+2, w+3 (mod 4)
+    // so that the first is its own.
     const uint16_t* Wg = static_cast<const uint16_t*>(p.a.W) + static_cast<int64_t>(n) * kV * kV;
-    uint32_t bw[NT][4][2];
+    uint32_t bw[2][4][2];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
+    for (int nt = 0; nt < 2; ++nt) {
       const int col = NCOL * w + 8 * nt + g;
 #pragma unroll
       for (int kt = 0; kt < 4; ++kt) {
-        const int k0 = 16 * (NT == 2 ? ((w + kt) & 3) : kt) + 2 * qd;
-        bw[nt][kt][0] = static_cast<uint32_t>(Wg[k0 * kV + col]) |
-                        (static_cast<uint32_t>(Wg[(k0 + 1) * kV + col]) << 16);
-        bw[nt][kt][1] = static_cast<uint32_t>(Wg[(k0 + 8) * kV + col]) |
-                        (static_cast<uint32_t>(Wg[(k0 + 9) * kV + col]) << 16);
+        const int k0 = 16 * ((w + kt) & 3) + 2 * qd;
+        bw[nt][kt][0] = bf16x2_to_f16x2(static_cast<uint32_t>(Wg[k0 * kV + col]) |
+                                        (static_cast<uint32_t>(Wg[(k0 + 1) * kV + col]) << 16));
+        bw[nt][kt][1] = bf16x2_to_f16x2(static_cast<uint32_t>(Wg[(k0 + 8) * kV + col]) |
+                                        (static_cast<uint32_t>(Wg[(k0 + 9) * kV + col]) << 16));
+        if (!f16x2_finite(bw[nt][kt][0]) || !f16x2_finite(bw[nt][kt][1]))
+          report_device_error(status, kStatusCheck, kWhereWRange);
       }
     }
-    // State: h[nt][0..3] = H[g][j], H[g][j+1], H[g+8][j], H[g+8][j+1], j = NCOL w + 8nt + 2qd.
-    float h[NT][4];
+    // State: h[nt][0..3] = H[g][j], H[g][j+1], H[g+8][j], H[g+8][j+1], j = 16 w + 8nt + 2qd.
+    float h[2][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int c = 0; c < 4; ++c) h[nt][c] = 0.f;
     const int jcol0 = NCOL * w + 2 * qd;
     const int64_t row_g = static_cast<int64_t>(cta_rank) * kRows + g;
     float q_prev0 = 0.f, q_prev1 = 0.f;
     uint32_t q_prev_lo = 0u, q_prev_hi = 0u;
-    uint32_t hown[4] = {0u, 0u, 0u, 0u};  // bf16 H_{t-1} of the warp's own k-tile (NT = 2), A layout
+    // fp16 H_{t-1} as the MMA operand (see mma_common.cuh).  hh: this warp's
+    // own k-tile (accumulator layout = A layout); the exchange tile holds
+    // all four k-tiles.
+    uint32_t hh[4] = {0u, 0u, 0u, 0u};
+    auto split = [&]() {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        hh[2 * nt] = pack2_f16(h[nt][0], h[nt][1]);
+        hh[2 * nt + 1] = pack2_f16(h[nt][2], h[nt][3]);
+      }
+    };
+    auto store_tiles = [&](uint32_t base) {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int col = jcol0 + 8 * nt;
+        st_shared_b32(base + tile_off(g, col), hh[2 * nt]);
+        st_shared_b32(base + tile_off(g + 8, col), hh[2 * nt + 1]);
+      }
+    };
     if (p.a.H0 != nullptr) {
-      // Start from the given state: fp32 into the registers, bf16 into the
+      // Start from the given state: fp32 into the registers, fp16 into the
       // operand tile of step 0 (ordered by the first tile's barrier).
       const float* src = p.a.H0 + (static_cast<int64_t>(chain) * p.a.K + row_g) * kV + jcol0;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
+      for (int nt = 0; nt < 2; ++nt) {
         const float2 x0 = *reinterpret_cast<const float2*>(src + 8 * nt);
         const float2 x1 = *reinterpret_cast<const float2*>(src + 8 * kV + 8 * nt);
         h[nt][0] = x0.x; h[nt][1] = x0.y; h[nt][2] = x1.x; h[nt][3] = x1.y;
-        const uint32_t p0 = pack2_bf16(h[nt][0], h[nt][1]), p1 = pack2_bf16(h[nt][2], h[nt][3]);
-        st_shared_b32(abuf0 + tile_off(g, jcol0 + 8 * nt), p0);
-        st_shared_b32(abuf0 + tile_off(g + 8, jcol0 + 8 * nt), p1);
-        if constexpr (NT == 2) {
-          hown[2 * nt] = p0;
-          hown[2 * nt + 1] = p1;
-        }
       }
+      split();
+      store_tiles(abuf0);
     }
     int ck_left = p.a.ckpt_every, ck_idx = 0;  // countdown to the next checkpoint (no division per step)
+    // This thread's 16 bytes of the Z stash at step 0 (advancing 2 KB a step).
+    uint8_t* const zst = !kZ ? nullptr
+                             : reinterpret_cast<uint8_t*>(p.a.zstash) +
+                                   static_cast<int64_t>(chain * R + cta_rank) * T * kZStepBytes + (w * 32 + lane) * 16;
     int ys_prev = 0, s_prev = 0;
     bool have_prev = false;
 
     auto readout = [&](float q0, float q1, int ys, int s) {
       // y partial over this CTA's 16 rows for the warp's columns (last step only).
-      float part[2 * NT];
+      float part[4];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
+      for (int nt = 0; nt < 2; ++nt) {
         part[2 * nt + 0] = fmaf(q0, h[nt][0], q1 * h[nt][2]);
         part[2 * nt + 1] = fmaf(q0, h[nt][1], q1 * h[nt][3]);
       }
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1)
 #pragma unroll
-        for (int u = 0; u < 2 * NT; ++u) part[u] += __shfl_xor_sync(0xffffffffu, part[u], o);
+        for (int u = 0; u < 4; ++u) part[u] += __shfl_xor_sync(0xffffffffu, part[u], o);
       if (g == 0) {
         float* dst = sY + (ys * kS + s) * kV + jcol0;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
           *reinterpret_cast<float2*>(dst + 8 * nt) = make_float2(part[2 * nt], part[2 * nt + 1]);
       }
     };
@@ -198,114 +221,116 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
       const uint16_t* vs = reinterpret_cast<const uint16_t*>(stage + p.v_off);
       const float* fs = reinterpret_cast<const float*>(stage + p.f_off);
       const int nsteps = min(kS, T - tile * kS);
-      for (int s = 0; s < nsteps; ++s) {
-        const int t = tile * kS + s;
-        // Inputs of step t.
-        const float k0 = bf16_bits_to_f32(ks[s * kRows + g]);
-        const float k1 = bf16_bits_to_f32(ks[s * kRows + g + 8]);
-        const float omf = 1.f - fs[s];
-        float acc[NT][4];
+      // Steps run in segments that end where a checkpoint is due, so the
+      // step itself carries no checkpoint test.
+      for (int s = 0; s < nsteps;) {
+        const int seg_end = kCk ? min(nsteps, s + ck_left) : nsteps;
+        const int seg_len = seg_end - s;
+        for (; s < seg_end; ++s) {
+          const int t = tile * kS + s;
+          // Inputs of step t.
+          const float k0 = bf16_bits_to_f32(ks[s * kRows + g]);
+          const float k1 = bf16_bits_to_f32(ks[s * kRows + g + 8]);
+          const float omf = 1.f - fs[s];
+          float acc[2][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const uint32_t vv = *reinterpret_cast<const uint32_t*>(vs + s * kV + jcol0 + 8 * nt);
-          const float v0 = bf16lo(vv), v1 = bf16hi(vv);
-          acc[nt][0] = k0 * v0;  // exact: products of bf16 values fit in fp32
-          acc[nt][1] = k0 * v1;
-          acc[nt][2] = k1 * v0;
-          acc[nt][3] = k1 * v1;
+          for (int nt = 0; nt < 2; ++nt) {
+            const uint32_t vv = *reinterpret_cast<const uint32_t*>(vs + s * kV + jcol0 + 8 * nt);
+            const float v0 = bf16lo(vv), v1 = bf16hi(vv);
+            acc[nt][0] = k0 * v0;  // exact: products of bf16 values fit in fp32
+            acc[nt][1] = k0 * v1;
+            acc[nt][2] = k1 * v0;
+            acc[nt][3] = k1 * v1;
+          }
+          // H_{t-1} as the A operand: the own k-tile from registers, issued
+          // while the other three load from the tile.
+          const uint32_t atile = abuf0 + (t & 1) * 2048;
+          uint32_t af[3][4];
+#pragma unroll
+          for (int i = 0; i < 3; ++i) ldmatrix_x4(af[i], ldsm_addr_a(atile, (w + 1 + i) & 3, lane));
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) mma_f16_16816(acc[nt], hh, bw[nt][0][0], bw[nt][0][1]);
+          // Readout of step t-1 on the tensor core: y^T = q^T H_{t-1} as an
+          // m16n8k16 with q replicated over the 16 A rows and H_{t-1} (fp32,
+          // split into bf16 high and low parts, ~16 bits) as B, transposed from
+          // the accumulator layout with movmatrix.
+          uint32_t rb[2][2][2];
+          float yd[2][4];
+          if (do_y && have_prev) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+              const uint32_t hi0 = pack2_bf16(h[nt][0], h[nt][1]);
+              const uint32_t hi1 = pack2_bf16(h[nt][2], h[nt][3]);
+              const uint32_t lo0 = pack2_bf16(h[nt][0] - bf16lo(hi0), h[nt][1] - bf16hi(hi0));
+              const uint32_t lo1 = pack2_bf16(h[nt][2] - bf16lo(hi1), h[nt][3] - bf16hi(hi1));
+              rb[nt][0][0] = movmatrix_trans(hi0);
+              rb[nt][0][1] = movmatrix_trans(hi1);
+              rb[nt][1][0] = movmatrix_trans(lo0);
+              rb[nt][1][1] = movmatrix_trans(lo1);
+              yd[nt][0] = yd[nt][1] = yd[nt][2] = yd[nt][3] = 0.f;
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 3; ++i)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) mma_f16_16816(acc[nt], af[i], bw[nt][i + 1][0], bw[nt][i + 1][1]);
+          if (do_y && have_prev) {
+            uint32_t qa[4];
+            qa[0] = qa[1] = q_prev_lo;
+            qa[2] = qa[3] = q_prev_hi;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+              mma_bf16_16816(yd[nt], qa, rb[nt][0][0], rb[nt][0][1]);
+              mma_bf16_16816(yd[nt], qa, rb[nt][1][0], rb[nt][1][1]);
+            }
+          }
+          // Eq. 10-11 on this thread's 8 state values; fp16 H_t to the other tile.
+          float zv[2][4];
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const float z = tanh_fast(acc[nt][c]);
+              zv[nt][c] = z;
+              h[nt][c] = fmaf(omf, z - h[nt][c], h[nt][c]);
+            }
+          split();
+          store_tiles(abuf0 + ((t + 1) & 1) * 2048);
+          if constexpr (kZ)  // Z_t for the backward, off the chain (a streaming store)
+            st_global_cs_v4(zst + static_cast<int64_t>(t) * kZStepBytes,
+                            make_uint4(pack2_f16(zv[0][0], zv[0][1]), pack2_f16(zv[0][2], zv[0][3]),
+                                       pack2_f16(zv[1][0], zv[1][1]), pack2_f16(zv[1][2], zv[1][3])));
+          if (do_y && have_prev && g == 0) {
+            float* dst = sY + (ys_prev * kS + s_prev) * kV + jcol0;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+              *reinterpret_cast<float2*>(dst + 8 * nt) = make_float2(yd[nt][0], yd[nt][1]);
+          }
+          q_prev_lo = *reinterpret_cast<const uint32_t*>(qs + s * kRows + 2 * qd);
+          q_prev_hi = *reinterpret_cast<const uint32_t*>(qs + s * kRows + 2 * qd + 8);
+          const bool prev_was_tile_end = have_prev && s == 0;  // y of the last step of the previous tile
+          have_prev = true;
+          ys_prev = ys;
+          s_prev = s;
+          named_bar_sync(1, CT);
+          if (do_y && prev_was_tile_end && threadIdx.x == 0) mbar_arrive(smem_u32(&yfull[(tile + kYS - 1) % kYS]));
         }
-        // H_{t-1} (bf16) as the A operand (NT = 2: the own k-tile from
-        // registers, issued while the other three load).
-        const uint32_t atile = abuf0 + (t & 1) * 2048;
-        uint32_t af[4][4];
-        if constexpr (NT == 2) {
+        if constexpr (kCk) {
+          ck_left -= seg_len;
+          if (ck_left == 0) {  // H after step t = tile kS + s - 1 starts a chunk: checkpoint it
+            ck_left = p.a.ckpt_every;
+            ++ck_idx;
+            if (tile * kS + s < T) {
+              float* dst = p.a.ckpt +
+                           ((static_cast<int64_t>(chain) * p.a.n_ckpt + ck_idx - 1) * p.a.K + row_g) * kV + jcol0;
 #pragma unroll
-          for (int i = 1; i < 4; ++i) ldmatrix_x4(af[i], ldsm_addr_a(atile, (w + i) & 3, lane));
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[nt], hown, bw[nt][0][0], bw[nt][0][1]);
-        } else {
-#pragma unroll
-          for (int kt = 0; kt < 4; ++kt) ldmatrix_x4(af[kt], ldsm_addr_a(atile, kt, lane));
-        }
-        // Readout of step t-1 on the tensor core: y^T = q^T H_{t-1} as an
-        // m16n8k16 with q replicated over the 16 A rows and H_{t-1} (split
-        // into bf16 hi + lo parts) as B, transposed from the accumulator
-        // layout with movmatrix.
-        uint32_t rb[NT][2][2];
-        float yd[NT][4];
-        if (do_y && have_prev) {
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const uint32_t hi0 = pack2_bf16(h[nt][0], h[nt][1]);
-            const uint32_t hi1 = pack2_bf16(h[nt][2], h[nt][3]);
-            const uint32_t lo0 = pack2_bf16(h[nt][0] - bf16lo(hi0), h[nt][1] - bf16hi(hi0));
-            const uint32_t lo1 = pack2_bf16(h[nt][2] - bf16lo(hi1), h[nt][3] - bf16hi(hi1));
-            rb[nt][0][0] = movmatrix_trans(hi0);
-            rb[nt][0][1] = movmatrix_trans(hi1);
-            rb[nt][1][0] = movmatrix_trans(lo0);
-            rb[nt][1][1] = movmatrix_trans(lo1);
-            yd[nt][0] = yd[nt][1] = yd[nt][2] = yd[nt][3] = 0.f;
+              for (int nt = 0; nt < 2; ++nt) {
+                *reinterpret_cast<float2*>(dst + 8 * nt) = make_float2(h[nt][0], h[nt][1]);
+                *reinterpret_cast<float2*>(dst + 8 * kV + 8 * nt) = make_float2(h[nt][2], h[nt][3]);
+              }
+            }
           }
         }
-#pragma unroll
-        for (int kt = (NT == 2 ? 1 : 0); kt < 4; ++kt)
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[nt], af[kt], bw[nt][kt][0], bw[nt][kt][1]);
-        if (do_y && have_prev) {
-          uint32_t qa[4];
-          qa[0] = qa[1] = q_prev_lo;
-          qa[2] = qa[3] = q_prev_hi;
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            mma_bf16_16816(yd[nt], qa, rb[nt][0][0], rb[nt][0][1]);
-            mma_bf16_16816(yd[nt], qa, rb[nt][1][0], rb[nt][1][1]);
-          }
-        }
-        // Eq. 10-11 on this thread's 8 state values; bf16(H_t) to the other tile.
-        const uint32_t otile = abuf0 + ((t + 1) & 1) * 2048;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const float z = tanh_fast(acc[nt][c]);
-            h[nt][c] = fmaf(omf, z - h[nt][c], h[nt][c]);
-          }
-          const int col = jcol0 + 8 * nt;
-          const uint32_t p0 = pack2_bf16(h[nt][0], h[nt][1]), p1 = pack2_bf16(h[nt][2], h[nt][3]);
-          if constexpr (NT == 2) {
-            hown[2 * nt] = p0;
-            hown[2 * nt + 1] = p1;
-          }
-          st_shared_b32(otile + tile_off(g, col), p0);
-          st_shared_b32(otile + tile_off(g + 8, col), p1);
-        }
-        if (p.a.ckpt != nullptr && --ck_left == 0) {  // H_{t+1} starts a chunk: checkpoint it
-          ck_left = p.a.ckpt_every;
-          ++ck_idx;
-        }
-        if (p.a.ckpt != nullptr && ck_left == p.a.ckpt_every && t + 1 < T) {
-          float* dst = p.a.ckpt +
-                       ((static_cast<int64_t>(chain) * p.a.n_ckpt + ck_idx - 1) * p.a.K + row_g) * kV + jcol0;
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            *reinterpret_cast<float2*>(dst + 8 * nt) = make_float2(h[nt][0], h[nt][1]);
-            *reinterpret_cast<float2*>(dst + 8 * kV + 8 * nt) = make_float2(h[nt][2], h[nt][3]);
-          }
-        }
-        if (do_y && have_prev && g == 0) {
-          float* dst = sY + (ys_prev * kS + s_prev) * kV + jcol0;
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-            *reinterpret_cast<float2*>(dst + 8 * nt) = make_float2(yd[nt][0], yd[nt][1]);
-        }
-        q_prev_lo = *reinterpret_cast<const uint32_t*>(qs + s * kRows + 2 * qd);
-        q_prev_hi = *reinterpret_cast<const uint32_t*>(qs + s * kRows + 2 * qd + 8);
-        const bool prev_was_tile_end = have_prev && s == 0;  // y of the last step of the previous tile
-        have_prev = true;
-        ys_prev = ys;
-        s_prev = s;
-        named_bar_sync(1, CT);
-        if (do_y && prev_was_tile_end && threadIdx.x == 0) mbar_arrive(smem_u32(&yfull[(tile + kYS - 1) % kYS]));
       }
       // Every compute warp is past its last read of this stage.
       if (threadIdx.x == 0) mbar_arrive(smem_u32(&empty[st]));
@@ -326,7 +351,7 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
       if (p.a.H_T != nullptr) {
         float* dst = p.a.H_T + (static_cast<int64_t>(chain) * p.a.K + row_g) * kV + jcol0;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
+        for (int nt = 0; nt < 2; ++nt) {
           *reinterpret_cast<float2*>(dst + 8 * nt) = make_float2(h[nt][0], h[nt][1]);
           *reinterpret_cast<float2*>(dst + 8 * kV + 8 * nt) = make_float2(h[nt][2], h[nt][3]);
         }
@@ -419,7 +444,7 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
 
 inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-template <int NT>
+template <int NT, bool kY, bool kCk, bool kZ>
 cudaError_t launch_nt(const FwdArgs& a, cudaStream_t stream) {
   MmaFwdParams p{};
   p.a = a;
@@ -453,7 +478,7 @@ cudaError_t launch_nt(const FwdArgs& a, cudaStream_t stream) {
       !make_tensor_map_btnx(&mk, a.k, bf, 2, a.B, a.T, qN, a.K, kRows, kS) ||
       !make_tensor_map_btnx(&mv, a.v, bf, 2, a.B, a.T, a.N, kV, kV, kS))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(mma_forward_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(mma_forward_kernel<NT, kY, kCk, kZ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
@@ -468,7 +493,7 @@ cudaError_t launch_nt(const FwdArgs& a, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, mma_forward_kernel<NT>, p, mq, mk, mv);
+  e = cudaLaunchKernelEx(&cfg, mma_forward_kernel<NT, kY, kCk, kZ>, p, mq, mk, mv);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -480,13 +505,15 @@ bool mma_forward_supported(int K, int V) {
   return (V == kV && K % kRows == 0 && K >= kRows && K <= 128) || mv_forward_supported(K, V);
 }
 
-// Tuning knob M2RNN_MMA_NT = 1 | 2: value-column tiles per compute warp
-// (1: eight compute warps, two per SM sub-partition; 2: four compute warps).
 cudaError_t launch_mma_forward(const FwdArgs& a, cudaStream_t stream) {
   if (a.V != kV) return launch_mv_forward(a, stream);
-  const char* e = std::getenv("M2RNN_MMA_NT");
-  if (e != nullptr && e[0] == '1') return launch_nt<1>(a, stream);
-  return launch_nt<2>(a, stream);
+  const bool y = a.y != nullptr, ck = a.ckpt != nullptr, z = a.zstash != nullptr;
+  if (z) {
+    if (y) return ck ? launch_nt<2, true, true, true>(a, stream) : launch_nt<2, true, false, true>(a, stream);
+    return ck ? launch_nt<2, false, true, true>(a, stream) : launch_nt<2, false, false, true>(a, stream);
+  }
+  if (y) return ck ? launch_nt<2, true, true, false>(a, stream) : launch_nt<2, true, false, false>(a, stream);
+  return ck ? launch_nt<2, false, true, false>(a, stream) : launch_nt<2, false, false, false>(a, stream);
 }
 
 }  // namespace m2rnn

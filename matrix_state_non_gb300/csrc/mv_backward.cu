@@ -85,14 +85,16 @@ __global__ void __launch_bounds__((kMaxRB + 1) * 32, 1)
     const int g = lane >> 2, qd = lane & 3, w = warp;
     const int CT = 32 * R;
     const uint16_t* Wg = static_cast<const uint16_t*>(A.W) + static_cast<int64_t>(n) * kV * kV;
-    uint32_t bw[2][2], bt[2][2];  // B fragments of W (rerun) and of W^T (C_{t-1} = f R + D W^T)
+    uint32_t bw[2][2], bt[2][2];  // B fragments of W (rerun, fp16) and of W^T (C_{t-1} = f R + D W^T, bf16)
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       const int col = 8 * nt + g;
-      bw[nt][0] = static_cast<uint32_t>(Wg[(2 * qd) * kV + col]) |
-                  (static_cast<uint32_t>(Wg[(2 * qd + 1) * kV + col]) << 16);
-      bw[nt][1] = static_cast<uint32_t>(Wg[(2 * qd + 8) * kV + col]) |
-                  (static_cast<uint32_t>(Wg[(2 * qd + 9) * kV + col]) << 16);
+      bw[nt][0] = bf16x2_to_f16x2(static_cast<uint32_t>(Wg[(2 * qd) * kV + col]) |
+                                  (static_cast<uint32_t>(Wg[(2 * qd + 1) * kV + col]) << 16));
+      bw[nt][1] = bf16x2_to_f16x2(static_cast<uint32_t>(Wg[(2 * qd + 8) * kV + col]) |
+                                  (static_cast<uint32_t>(Wg[(2 * qd + 9) * kV + col]) << 16));
+      if (!f16x2_finite(bw[nt][0]) || !f16x2_finite(bw[nt][1]))
+        report_device_error(status, kStatusCheck, kWhereWRange);
       bt[nt][0] = *reinterpret_cast<const uint32_t*>(Wg + col * kV + 2 * qd);
       bt[nt][1] = *reinterpret_cast<const uint32_t*>(Wg + col * kV + 2 * qd + 8);
     }
@@ -150,11 +152,12 @@ __global__ void __launch_bounds__((kMaxRB + 1) * 32, 1)
         }
       }
       for (int s = 0; s < L; ++s) {
-        uint32_t a[4];
-        a[0] = pack2_bf16(h[0][0], h[0][1]);
-        a[1] = pack2_bf16(h[0][2], h[0][3]);
-        a[2] = pack2_bf16(h[1][0], h[1][1]);
-        a[3] = pack2_bf16(h[1][2], h[1][3]);
+        uint32_t a[4];  // fp16 H_{s-1}, as in the forward
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          a[2 * nt] = pack2_f16(h[nt][0], h[nt][1]);
+          a[2 * nt + 1] = pack2_f16(h[nt][2], h[nt][3]);
+        }
         const float k0 = bf16_bits_to_f32(ck[s * K + 16 * w + g]);
         const float k1 = bf16_bits_to_f32(ck[s * K + 16 * w + g + 8]);
         const float omf = 1.f - cf[s];
@@ -166,7 +169,7 @@ __global__ void __launch_bounds__((kMaxRB + 1) * 32, 1)
           acc[nt][1] = k0 * bf16hi(vv);
           acc[nt][2] = k1 * bf16lo(vv);
           acc[nt][3] = k1 * bf16hi(vv);
-          mma_bf16_16816(acc[nt], a, bw[nt][0], bw[nt][1]);
+          mma_f16_16816(acc[nt], a, bw[nt][0], bw[nt][1]);
         }
         uint32_t cache[16];
 #pragma unroll

@@ -77,14 +77,16 @@ __global__ void __launch_bounds__((kMaxRB + 1) * 32, 1)
     const int g = lane >> 2, qd = lane & 3, w = warp;
     const int CT = 32 * R;
     const uint16_t* Wg = static_cast<const uint16_t*>(A.W) + static_cast<int64_t>(n) * kV * kV;
-    uint32_t bw[2][2];  // B[k][col] = W[k][8nt + col], k = 2qd.. and 2qd+8..
+    uint32_t bw[2][2];  // fp16 B[k][col] = W[k][8nt + col], k = 2qd.. and 2qd+8..
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       const int col = 8 * nt + g;
-      bw[nt][0] = static_cast<uint32_t>(Wg[(2 * qd) * kV + col]) |
-                  (static_cast<uint32_t>(Wg[(2 * qd + 1) * kV + col]) << 16);
-      bw[nt][1] = static_cast<uint32_t>(Wg[(2 * qd + 8) * kV + col]) |
-                  (static_cast<uint32_t>(Wg[(2 * qd + 9) * kV + col]) << 16);
+      bw[nt][0] = bf16x2_to_f16x2(static_cast<uint32_t>(Wg[(2 * qd) * kV + col]) |
+                                  (static_cast<uint32_t>(Wg[(2 * qd + 1) * kV + col]) << 16));
+      bw[nt][1] = bf16x2_to_f16x2(static_cast<uint32_t>(Wg[(2 * qd + 8) * kV + col]) |
+                                  (static_cast<uint32_t>(Wg[(2 * qd + 9) * kV + col]) << 16));
+      if (!f16x2_finite(bw[nt][0]) || !f16x2_finite(bw[nt][1]))
+        report_device_error(status, kStatusCheck, kWhereWRange);
     }
     const int64_t row_g = static_cast<int64_t>(chain) * K + 16 * w + g;  // state row of lane g
     float h[2][4];
@@ -99,11 +101,16 @@ __global__ void __launch_bounds__((kMaxRB + 1) * 32, 1)
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) h[nt][0] = h[nt][1] = h[nt][2] = h[nt][3] = 0.f;
     }
-    uint32_t hown[4];  // bf16(H_{t-1}) of the warp's rows: its own A operand
-    hown[0] = pack2_bf16(h[0][0], h[0][1]);
-    hown[1] = pack2_bf16(h[0][2], h[0][3]);
-    hown[2] = pack2_bf16(h[1][0], h[1][1]);
-    hown[3] = pack2_bf16(h[1][2], h[1][3]);
+    // fp16 H_{t-1} of the warp's rows: its own A operand (see mma_common.cuh).
+    uint32_t hown[4];
+    auto split = [&]() {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        hown[2 * nt] = pack2_f16(h[nt][0], h[nt][1]);
+        hown[2 * nt + 1] = pack2_f16(h[nt][2], h[nt][3]);
+      }
+    };
+    split();
     const uint16_t* wr = static_cast<const uint16_t*>(A.w_r) + static_cast<int64_t>(n) * kV;
     int ck_left = A.ckpt_every, ck_idx = 0;
     bool ok = true;
@@ -131,8 +138,9 @@ __global__ void __launch_bounds__((kMaxRB + 1) * 32, 1)
         qa[0] = qa[1] = qlo;
         qa[2] = qa[3] = qhi;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const uint32_t hi0 = hown[2 * nt], hi1 = hown[2 * nt + 1];
+        for (int nt = 0; nt < 2; ++nt) {  // H_{t-1} as bf16 high and low parts (~16 bits)
+          const uint32_t hi0 = pack2_bf16(h[nt][0], h[nt][1]);
+          const uint32_t hi1 = pack2_bf16(h[nt][2], h[nt][3]);
           const uint32_t lo0 = pack2_bf16(h[nt][0] - bf16lo(hi0), h[nt][1] - bf16hi(hi0));
           const uint32_t lo1 = pack2_bf16(h[nt][2] - bf16lo(hi1), h[nt][3] - bf16hi(hi1));
           yd[nt][0] = yd[nt][1] = yd[nt][2] = yd[nt][3] = 0.f;
@@ -160,7 +168,7 @@ __global__ void __launch_bounds__((kMaxRB + 1) * 32, 1)
           acc[nt][1] = k0 * v1;
           acc[nt][2] = k1 * v0;
           acc[nt][3] = k1 * v1;
-          mma_bf16_16816(acc[nt], hown, bw[nt][0], bw[nt][1]);  // + H_{t-1} W (Eq. 10)
+          mma_f16_16816(acc[nt], hown, bw[nt][0], bw[nt][1]);  // + H_{t-1} W (Eq. 10)
         }
         float yd[2][4];
         if (do_y && s > 0) {
@@ -171,11 +179,9 @@ __global__ void __launch_bounds__((kMaxRB + 1) * 32, 1)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) h[nt][e] = fmaf(omf, tanh_fast(acc[nt][e]) - h[nt][e], h[nt][e]);  // Eq. 11
-        hown[0] = pack2_bf16(h[0][0], h[0][1]);
-        hown[1] = pack2_bf16(h[0][2], h[0][3]);
-        hown[2] = pack2_bf16(h[1][0], h[1][1]);
-        hown[3] = pack2_bf16(h[1][2], h[1][3]);
+          for (int e = 0; e < 4; ++e)
+            h[nt][e] = fmaf(omf, tanh_fast(acc[nt][e]) - h[nt][e], h[nt][e]);  // Eq. 11
+        split();
         if (A.ckpt != nullptr && --ck_left == 0) {  // H_{t+1} starts a chunk: checkpoint it
           ck_left = A.ckpt_every;
           ++ck_idx;

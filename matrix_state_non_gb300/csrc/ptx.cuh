@@ -151,6 +151,13 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Untiled bulk copy global -> shared (both 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int c0, int c1, int c2, int c3) {
   asm volatile(
@@ -332,6 +339,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
          | (1u << 7)                             // A format: bf16
          | (1u << 10)                            // B format: bf16
          | ((a_mn_major ? 1u : 0u) << 15)        // A major-ness
+         | ((b_mn_major ? 1u : 0u) << 16)        // B major-ness
+         | (static_cast<uint32_t>(N >> 3) << 17) // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
+}
+
+// The same for fp16 A and B (kind::f16 with both formats F16).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4)                               // D format: f32
+         | ((a_mn_major ? 1u : 0u) << 15)        // A major-ness (A, B format fields 0: f16)
          | ((b_mn_major ? 1u : 0u) << 16)        // B major-ness
          | (static_cast<uint32_t>(N >> 3) << 17) // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16

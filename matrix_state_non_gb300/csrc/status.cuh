@@ -24,7 +24,10 @@ constexpr uint32_t kWhereFwdFull = 101, kWhereFwdEmpty = 102, kWhereFwdD = 103,
                    kWhereFwdH = 109;
 constexpr uint32_t kWhereBwdFull = 201, kWhereBwdCEmpty = 202, kWhereBwdTReady = 203,
                    kWhereBwdTFree = 204, kWhereBwdXFull = 205, kWhereBwdXEmpty = 206,
-                   kWhereBwdDrain = 207, kWhereBwdDW = 208;
+                   kWhereBwdDrain = 207, kWhereBwdDW = 208, kWhereBwdZFull = 209;
+// Input checks: an entry of W outside the fp16 range (|W| >= 65520) that the
+// fp16 state-operand kernels cannot represent.
+constexpr uint32_t kWhereWRange = 301;
 
 __device__ __forceinline__ void report_device_error(StatusBlock* s, unsigned int code,
                                                     uint32_t where) {

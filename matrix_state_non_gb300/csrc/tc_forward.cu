@@ -16,10 +16,11 @@
 //     D^T [V x NR] = W^T [V x V] * H_{t-1}^T [V x NR]      (M = 128, N = NR, K = V)
 // with A = W^T written to tensor memory once (stacked 128/V times to fill
 // M = 128, so the V = 64 case keeps all four TMEM lane quadrants busy), B =
-// bf16(H_{t-1}) rewritten in shared memory every step, D in TMEM.  TMEM lane L holds value column j = L mod V, so each
+// fp16(H_{t-1}) rewritten in shared memory every step (W re-encoded as fp16
+// too: see mma_common.cuh), D in TMEM.  TMEM lane L holds value column j = L mod V, so each
 // thread owns a column j and ROWS rows of the state in fp32 registers: the
 // rank-1 add, tanh, gate blend and the readout over its rows are all
-// thread-local.  The bf16 copy of H_t goes back to shared memory as the next
+// thread-local.  The fp16 copy of H_t goes back to shared memory as the next
 // MMA's B operand (MN-major: the thread's ROWS values are 16-byte runs).
 //
 // Warp roles: warps 0..4G-1 = G epilogue warpgroups; warp 4G = the MMA warp,
@@ -145,7 +146,7 @@ __global__ void __launch_bounds__(352, 1)
     for (uint32_t e = threadIdx.x * 16; e < static_cast<uint32_t>(G) * C::B_BYTES; e += blockDim.x * 16)
       *reinterpret_cast<uint4*>(sB + e) = zero;  // H_0 = 0
   } else if (warp < 4 * G) {
-    // bf16(H_0) as step 0's B operand: each epilogue thread writes the rows
+    // fp16(H_0) as step 0's B operand: each epilogue thread writes the rows
     // and column it owns (the same mapping as below; together they cover
     // every element of each group's tile).
     const int g = warp / 4, L = 32 * (warp % 4) + lane;
@@ -156,10 +157,10 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
     for (int r0 = 0; r0 < ROWS; r0 += 8) {
       uint4 pk;
-      pk.x = pack_bf16x2(src[(r0 + 0) * V], src[(r0 + 1) * V]);
-      pk.y = pack_bf16x2(src[(r0 + 2) * V], src[(r0 + 3) * V]);
-      pk.z = pack_bf16x2(src[(r0 + 4) * V], src[(r0 + 5) * V]);
-      pk.w = pack_bf16x2(src[(r0 + 6) * V], src[(r0 + 7) * V]);
+      pk.x = pack2_f16(src[(r0 + 0) * V], src[(r0 + 1) * V]);
+      pk.y = pack2_f16(src[(r0 + 2) * V], src[(r0 + 3) * V]);
+      pk.z = pack2_f16(src[(r0 + 4) * V], src[(r0 + 5) * V]);
+      pk.w = pack2_f16(src[(r0 + 6) * V], src[(r0 + 7) * V]);
       *reinterpret_cast<uint4*>(bslot + (r0 / 8) * C::SBO) = pk;
     }
   }
@@ -168,11 +169,12 @@ __global__ void __launch_bounds__(352, 1)
   cluster_sync_all();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
-  const uint32_t idesc = idesc_bf16_f32(128, C::NR, /*a_mn_major=*/false, /*b_mn_major=*/true);
+  // fp16 operands: W^T re-encoded, H_{t-1} rounded (see mma_common.cuh).
+  const uint32_t idesc = idesc_f16_f32(128, C::NR, /*a_mn_major=*/false, /*b_mn_major=*/true);
   const uint32_t a_tmem = tmem_base + p.a_tcol;
   if (warp < 4) {
     // A = [W^T; W^T; ...] in tensor memory (M = 128 lanes, K = V): lane L holds
-    // row L, i.e. A[L][m] = W[m][L mod V], two bf16 per 32-bit column.  Warp w
+    // row L, i.e. A[L][m] = W[m][L mod V], two fp16 per 32-bit column.  Warp w
     // writes lanes 32w..32w+31.
     const uint16_t* Wg = static_cast<const uint16_t*>(p.a.W) + static_cast<int64_t>(n) * V * V;
     const int jr = (32 * warp + lane) % V;
@@ -182,7 +184,9 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
       for (int u = 0; u < 32; ++u) {
         const int m = 2 * (c0 + u);
-        regs[u] = static_cast<uint32_t>(Wg[m * V + jr]) | (static_cast<uint32_t>(Wg[(m + 1) * V + jr]) << 16);
+        regs[u] = bf16x2_to_f16x2(static_cast<uint32_t>(Wg[m * V + jr]) |
+                                  (static_cast<uint32_t>(Wg[(m + 1) * V + jr]) << 16));
+        if (!f16x2_finite(regs[u])) report_device_error(p.a.status, kStatusCheck, kWhereWRange);
       }
       tmem_st_32x32b_x32(a_tmem + (static_cast<uint32_t>(32 * warp) << 16) + c0, regs);
     }
@@ -255,13 +259,13 @@ __global__ void __launch_bounds__(352, 1)
             h[r0 + u] = fmaf(omf, z - h[r0 + u], h[r0 + u]);                // Eq. 11
           }
           uint4 pk;
-          pk.x = pack_bf16x2(h[r0 + 0], h[r0 + 1]);
-          pk.y = pack_bf16x2(h[r0 + 2], h[r0 + 3]);
-          pk.z = pack_bf16x2(h[r0 + 4], h[r0 + 5]);
-          pk.w = pack_bf16x2(h[r0 + 6], h[r0 + 7]);
+          pk.x = pack2_f16(h[r0 + 0], h[r0 + 1]);
+          pk.y = pack2_f16(h[r0 + 2], h[r0 + 3]);
+          pk.z = pack2_f16(h[r0 + 4], h[r0 + 5]);
+          pk.w = pack2_f16(h[r0 + 6], h[r0 + 7]);
           *reinterpret_cast<uint4*>(bslot + (r0 / 8) * C::SBO) = pk;
         }
-        // Hand bf16(H_t) to the tensor core: make the generic-proxy stores
+        // Hand fp16(H_t) to the tensor core: make the generic-proxy stores
         // visible to the async proxy, then one arrival per warp for the MMA warp.
         fence_proxy_async_smem();
         tc_fence_before_sync();
@@ -306,7 +310,7 @@ __global__ void __launch_bounds__(352, 1)
     if (!ok) *abort_flag = 1;
   } else if (warp == 4 * G) {
     // ---------------- MMA warp: one converged warp issues every group's MMAs ----------------
-    // Step t of group g needs bf16(H_{t-1}) from that group's epilogue (step
+    // Step t of group g needs fp16(H_{t-1}) from that group's epilogue (step
     // 0 multiplies H_0 = 0); the groups alternate, so one group's MMAs run
     // while the other group's epilogue uses the special-function units.
     // B descriptor of group g, K slice kk: the start-address field (bits 0-13,

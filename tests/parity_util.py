@@ -46,17 +46,20 @@ def gpu_forward(inp, ckpt_every=0, H_0=None):
 
 
 def gpu_backward(inp, dH_T=None, ckpt_every=16, use_fwd_ckpt=False, H_0=None, want_dH0=False,
-                 state_grad_clip=0.0):
+                 state_grad_clip=0.0, stash=False):
+    """stash: the forward also leaves its Z stash, which the backward reads
+    (implies the forward's checkpoints)."""
     import torch
     from matrix_state_non_gb300 import binding
     d = binding.to_device(inp)
     h0 = _cuda_f32(H_0)
-    ckpt = None
-    if use_fwd_ckpt:
-        ckpt = binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=ckpt_every, H_0=h0)["ckpt"]
+    ckpt = z = None
+    if use_fwd_ckpt or stash:
+        fo = binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=ckpt_every, H_0=h0, stash=stash)
+        ckpt, z = fo["ckpt"], fo.get("z_stash")
     out = binding.backward(*(d[n] for n in IN_NAMES), d["dy"], dH_T=_cuda_f32(dH_T), H_0=h0,
                            want_dH0=want_dH0, ckpt=ckpt, ckpt_every=ckpt_every,
-                           state_grad_clip=state_grad_clip)
+                           state_grad_clip=state_grad_clip, z_stash=z)
     st, detail = binding.sync_status(out["workspace"])
     assert st == binding.M2RNN_OK, (binding.status_string(st), detail)
     torch.cuda.synchronize()

@@ -101,10 +101,10 @@ def test_backward_rejects_bad_arguments_without_a_device(lib):
 
 def test_state_entry_points_reject_bad_arguments_without_a_device(lib):
     # Misaligned initial state / state gradient, and a decode step without a state.
-    st = binding.m2rnn_forward_state(P, P, P, P, P, P, P + 4, P, None, None, 0, 1, 8, 1, 1, 64, 64,
+    st = binding.m2rnn_forward_state(P, P, P, P, P, P, P + 4, P, None, None, 0, None, 1, 8, 1, 1, 64, 64,
                                      binding.M2RNN_BF16, P, 1 << 20, None)
     assert st == binding.M2RNN_ERR_INVALID_ARG
-    st = binding.m2rnn_forward_state(P, P, P, P, P, P, None, P, None, None, 0, 1, 8, 4, 2, 64, 64,
+    st = binding.m2rnn_forward_state(P, P, P, P, P, P, None, P, None, None, 0, None, 1, 8, 4, 2, 64, 64,
                                      binding.M2RNN_BF16, P, 1 << 20, None)
     assert st == binding.M2RNN_ERR_INVALID_ARG   # q/k heads must be 1 or N
     assert binding.m2rnn_backward_state_workspace_size(1, 8, 4, 3, 64, 64, binding.M2RNN_BF16, 14, 1) == 0
@@ -112,11 +112,11 @@ def test_state_entry_points_reject_bad_arguments_without_a_device(lib):
     per_head = binding.m2rnn_backward_state_workspace_size(2, 8, 4, 4, 64, 64, binding.M2RNN_BF16, 14, 1)
     assert shared >= per_head + 2 * 4 * 2 * 8 * 4 * 64   # room for the per-head dq, dk
     common = dict(B=1, T=8, N=1, QK=1, K=64, V=64)
-    st = binding.m2rnn_backward_state(P, P, P, P, P, P, None, P, None, None, 14, P, P, P, P, P, P,
+    st = binding.m2rnn_backward_state(P, P, P, P, P, P, None, P, None, None, 14, None, P, P, P, P, P, P,
                                       P + 8, 0.0, *common.values(), binding.M2RNN_BF16, P, 1 << 30, None)
     assert st == binding.M2RNN_ERR_INVALID_ARG
     for bad_clip in (-1.0, float("nan")):
-        st = binding.m2rnn_backward_state(P, P, P, P, P, P, None, P, None, None, 14, P, P, P, P, P, P,
+        st = binding.m2rnn_backward_state(P, P, P, P, P, P, None, P, None, None, 14, None, P, P, P, P, P, P,
                                           None, bad_clip, *common.values(), binding.M2RNN_BF16, P,
                                           1 << 30, None)
         assert st == binding.M2RNN_ERR_INVALID_ARG
@@ -132,14 +132,14 @@ def test_gate_and_output_norm_entry_points_reject_bad_arguments_without_a_device
     bf = binding.M2RNN_BF16
 
     def fg(a=P, alpha=P, beta=P, N=2):
-        return binding.m2rnn_forward_gated(P, P, P, a, alpha, beta, P, P, None, P, None, None, 0, 1, 8, N, N,
+        return binding.m2rnn_forward_gated(P, P, P, a, alpha, beta, P, P, None, P, None, None, 0, None, 1, 8, N, N,
                                            64, 64, bf, P, 1 << 20, None)
     assert fg(a=None) == binding.M2RNN_ERR_INVALID_ARG
     assert fg(alpha=None) == binding.M2RNN_ERR_INVALID_ARG
     assert fg(beta=P + 4) == binding.M2RNN_ERR_INVALID_ARG
 
     def bg(dalpha=P, dbeta=P, a=P):
-        return binding.m2rnn_backward_gated(P, P, P, a, P, P, P, P, None, P, None, None, 14, P, P, P, P, dalpha,
+        return binding.m2rnn_backward_gated(P, P, P, a, P, P, P, P, None, P, None, None, 14, None, P, P, P, P, dalpha,
                                             dbeta, P, P, None, 0.0, 1, 8, 2, 2, 64, 64, bf, P, 1 << 30, None)
     assert bg(dalpha=None) == binding.M2RNN_ERR_INVALID_ARG
     assert bg(dbeta=P + 8) == binding.M2RNN_ERR_INVALID_ARG
@@ -160,6 +160,28 @@ def test_gate_and_output_norm_entry_points_reject_bad_arguments_without_a_device
         binding.M2RNN_ERR_WORKSPACE
     assert binding.m2rnn_output_norm_backward(P, P, P, None, 1e-6, P, P, P, 1, 8, 8, 64, bf, P, 1 << 30,
                                               None) == binding.M2RNN_ERR_INVALID_ARG
+
+
+def test_z_stash_rules_without_a_device(lib):
+    bf = binding.M2RNN_BF16
+    assert binding.m2rnn_z_stash_size(4, 4096, 8, 64, 64, bf) == 4 * 4096 * 8 * 64 * 64 * 2
+    assert binding.m2rnn_z_stash_size(1, 8, 1, 128, 128, bf) == 0            # V = 128: no stash
+    assert binding.m2rnn_z_stash_size(1, 8, 1, 64, 64, binding.M2RNN_F32) == 0
+    assert binding.m2rnn_z_stash_size(1, 8, 1, 40, 64, bf) == 0              # K not a multiple of 16
+
+    def fs(V=64, z=P, K=64):
+        return binding.m2rnn_forward_state(P, P, P, P, P, P, None, P, None, None, 0, z, 1, 8, 1, 1, K, V, bf, P,
+                                           1 << 20, None)
+    assert fs(V=128) == binding.M2RNN_ERR_UNSUPPORTED
+    assert fs(K=48, V=16) == binding.M2RNN_ERR_UNSUPPORTED
+    assert fs(z=P + 8) == binding.M2RNN_ERR_INVALID_ARG
+
+    def bs(T=64, ckpt=None, C=14, z=P):
+        return binding.m2rnn_backward_state(P, P, P, P, P, P, None, P, None, ckpt, C, z, P, P, P, P, P, P, None,
+                                            0.0, 1, T, 1, 1, 64, 64, bf, P, 1 << 30, None)
+    assert bs() == binding.M2RNN_ERR_INVALID_ARG          # T > ckpt_every needs the forward's checkpoints
+    assert bs(C=29, ckpt=P) == binding.M2RNN_ERR_UNSUPPORTED   # longer than the backward's chunk cache
+    assert bs(z=P + 4, ckpt=P) == binding.M2RNN_ERR_INVALID_ARG
 
 
 def test_noalloc_backward_rejects_unsupported_shapes_without_a_device(lib):

@@ -133,8 +133,8 @@ def test_decode_steps_follow_the_scan(kernel_family, K):
         ys.append(y.cpu().numpy())
     torch.cuda.synchronize()
     # The dedicated kernel sums the MMA k-tiles in another order than the scan,
-    # which can flip a bf16 rounding of the state operand (one bf16 ulp of a
-    # state element in (0.5, 1) is 2^-8): 2e-3 between the two GPU kernels;
+    # which can flip an fp16 rounding of the state operand (one ulp of a state
+    # element in (0.5, 1) is 2^-11): 2e-3 between the two GPU kernels;
     # the same kernel with T = 1 agrees to 1e-5.  Correctness is the oracle
     # check below.
     tol = 2e-3 if kernel_family == "auto" else 1e-5
