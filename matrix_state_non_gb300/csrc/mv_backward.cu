@@ -45,6 +45,8 @@ struct MvBwdParams {
   uint32_t tx_bytes;
 };
 
+// kClip: the state-gradient clamp as a compile-time switch (no per-step branch).
+template <bool kClip>
 __global__ void __launch_bounds__((kMaxRB + 1) * 32, 1)
     mv_backward_kernel(const __grid_constant__ MvBwdParams p, const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -299,7 +301,7 @@ __global__ void __launch_bounds__((kMaxRB + 1) * 32, 1)
           }
         }
         if (lane == 0) part_df[s * R + w] = pf;
-        if (A.clip > 0.f) {  // per-step clipping of the state gradient
+        if constexpr (kClip) {  // per-step clipping of the state gradient
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -445,10 +447,10 @@ cudaError_t launch_mv_backward(const BwdArgs& a, cudaStream_t stream) {
       !make_tensor_map_btnx(&mv, a.v, bf, 2, a.B, a.T, a.N, kV, kV, C) ||
       !make_tensor_map_btnx(&mdy, a.dy, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.B, a.T, a.N, kV, kV, C))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(mv_backward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  auto kernel = a.clip > 0.f ? mv_backward_kernel<true> : mv_backward_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  mv_backward_kernel<<<a.B * a.N, (p.R + 1) * 32, smem, stream>>>(p, mq, mk, mv, mdy);
+  kernel<<<a.B * a.N, (p.R + 1) * 32, smem, stream>>>(p, mq, mk, mv, mdy);
   return cudaGetLastError();
 }
 

@@ -45,6 +45,8 @@ struct MvFwdParams {
   uint32_t tx_bytes;
 };
 
+// Compile-time modes: kY = readout y, kCk = checkpoints (no per-step branch on either).
+template <bool kY, bool kCk>
 __global__ void __launch_bounds__((kMaxRB + 1) * 32, 1)
     mv_forward_kernel(const __grid_constant__ MvFwdParams p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
@@ -60,7 +62,7 @@ __global__ void __launch_bounds__((kMaxRB + 1) * 32, 1)
   uint64_t* empty = full + kNS;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.misc_off);
   volatile int* cabort = reinterpret_cast<volatile int*>(smem + p.misc_off + 4);
-  const bool do_y = A.y != nullptr;
+  constexpr bool do_y = kY;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNS; ++i) {
       mbar_init(smem_u32(&full[i]), 32);  // producer lanes (+ TMA bytes)
@@ -155,46 +157,54 @@ __global__ void __launch_bounds__((kMaxRB + 1) * 32, 1)
           *reinterpret_cast<float2*>(dst + 8) = make_float2(yd[1][0], yd[1][1]);
         }
       };
-      for (int s = 0; s < nsteps; ++s) {
-        const float k0 = bf16_bits_to_f32(ks[s * K + 16 * w + g]);
-        const float k1 = bf16_bits_to_f32(ks[s * K + 16 * w + g + 8]);
-        const float omf = 1.f - fs[s];
-        float acc[2][4];
+      // Steps run in segments that end where a checkpoint is due.
+      for (int s = 0; s < nsteps;) {
+        const int seg_end = kCk ? min(nsteps, s + ck_left) : nsteps;
+        const int seg_len = seg_end - s;
+        for (; s < seg_end; ++s) {
+          const float k0 = bf16_bits_to_f32(ks[s * K + 16 * w + g]);
+          const float k1 = bf16_bits_to_f32(ks[s * K + 16 * w + g + 8]);
+          const float omf = 1.f - fs[s];
+          float acc[2][4];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const uint32_t vv = *reinterpret_cast<const uint32_t*>(vs + s * kV + 8 * nt + 2 * qd);
-          const float v0 = bf16lo(vv), v1 = bf16hi(vv);
-          acc[nt][0] = k0 * v0;  // exact: products of bf16 values fit in fp32
-          acc[nt][1] = k0 * v1;
-          acc[nt][2] = k1 * v0;
-          acc[nt][3] = k1 * v1;
-          mma_f16_16816(acc[nt], hown, bw[nt][0], bw[nt][1]);  // + H_{t-1} W (Eq. 10)
+          for (int nt = 0; nt < 2; ++nt) {
+            const uint32_t vv = *reinterpret_cast<const uint32_t*>(vs + s * kV + 8 * nt + 2 * qd);
+            const float v0 = bf16lo(vv), v1 = bf16hi(vv);
+            acc[nt][0] = k0 * v0;  // exact: products of bf16 values fit in fp32
+            acc[nt][1] = k0 * v1;
+            acc[nt][2] = k1 * v0;
+            acc[nt][3] = k1 * v1;
+            mma_f16_16816(acc[nt], hown, bw[nt][0], bw[nt][1]);  // + H_{t-1} W (Eq. 10)
+          }
+          float yd[2][4];
+          if (do_y && s > 0) {
+            const uint32_t qlo = *reinterpret_cast<const uint32_t*>(qs + (s - 1) * K + 16 * w + 2 * qd);
+            const uint32_t qhi = *reinterpret_cast<const uint32_t*>(qs + (s - 1) * K + 16 * w + 2 * qd + 8);
+            readout_mma(qlo, qhi, yd);
+          }
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              h[nt][e] = fmaf(omf, tanh_fast(acc[nt][e]) - h[nt][e], h[nt][e]);  // Eq. 11
+          split();
+          if (do_y && s > 0) store_y(yd, s - 1);
         }
-        float yd[2][4];
-        if (do_y && s > 0) {
-          const uint32_t qlo = *reinterpret_cast<const uint32_t*>(qs + (s - 1) * K + 16 * w + 2 * qd);
-          const uint32_t qhi = *reinterpret_cast<const uint32_t*>(qs + (s - 1) * K + 16 * w + 2 * qd + 8);
-          readout_mma(qlo, qhi, yd);
-        }
+        if constexpr (kCk) {
+          ck_left -= seg_len;
+          if (ck_left == 0) {  // H after step t0 + s - 1 starts a chunk: checkpoint it
+            ck_left = A.ckpt_every;
+            ++ck_idx;
+            if (t0 + s < T) {
+              float* dst = A.ckpt + ((static_cast<int64_t>(chain) * A.n_ckpt + ck_idx - 1) * K + 16 * w + g) * kV;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            h[nt][e] = fmaf(omf, tanh_fast(acc[nt][e]) - h[nt][e], h[nt][e]);  // Eq. 11
-        split();
-        if (A.ckpt != nullptr && --ck_left == 0) {  // H_{t+1} starts a chunk: checkpoint it
-          ck_left = A.ckpt_every;
-          ++ck_idx;
-          if (t0 + s + 1 < T) {
-            float* dst = A.ckpt + ((static_cast<int64_t>(chain) * A.n_ckpt + ck_idx - 1) * K + 16 * w + g) * kV;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-              *reinterpret_cast<float2*>(dst + 8 * nt + 2 * qd) = make_float2(h[nt][0], h[nt][1]);
-              *reinterpret_cast<float2*>(dst + 8 * kV + 8 * nt + 2 * qd) = make_float2(h[nt][2], h[nt][3]);
+              for (int nt = 0; nt < 2; ++nt) {
+                *reinterpret_cast<float2*>(dst + 8 * nt + 2 * qd) = make_float2(h[nt][0], h[nt][1]);
+                *reinterpret_cast<float2*>(dst + 8 * kV + 8 * nt + 2 * qd) = make_float2(h[nt][2], h[nt][3]);
+              }
             }
           }
         }
-        if (do_y && s > 0) store_y(yd, s - 1);
       }
       if (do_y && nsteps > 0) {  // the tile's last step
         const uint32_t qlo = *reinterpret_cast<const uint32_t*>(qs + (nsteps - 1) * K + 16 * w + 2 * qd);
@@ -298,10 +308,12 @@ cudaError_t launch_mv_forward(const FwdArgs& a, cudaStream_t stream) {
       !make_tensor_map_btnx(&mk, a.k, bf, 2, a.B, a.T, qN, a.K, a.K, kS) ||
       !make_tensor_map_btnx(&mv, a.v, bf, 2, a.B, a.T, a.N, kV, kV, kS))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(mv_forward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto kernel = a.y != nullptr ? (a.ckpt != nullptr ? mv_forward_kernel<true, true> : mv_forward_kernel<true, false>)
+                               : (a.ckpt != nullptr ? mv_forward_kernel<false, true> : mv_forward_kernel<false, false>);
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  mv_forward_kernel<<<a.B * a.N, (p.R + 1) * 32, smem, stream>>>(p, mq, mk, mv);
+  kernel<<<a.B * a.N, (p.R + 1) * 32, smem, stream>>>(p, mq, mk, mv);
   return cudaGetLastError();
 }
 

@@ -85,7 +85,8 @@ __device__ __forceinline__ void unpack8_bf16(const uint4 w, float (&o)[8]) {
   o[7] = __uint_as_float(w.w & 0xFFFF0000u);
 }
 
-template <int V, int ROWS>
+// kY = readout y, kCk = checkpoints: compile-time modes, no per-step test.
+template <int V, int ROWS, bool kY, bool kCk>
 __global__ void __launch_bounds__(352, 1)
     tc_forward_kernel(const __grid_constant__ TcFwdParams p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -101,7 +102,7 @@ __global__ void __launch_bounds__(352, 1)
   const int chain = static_cast<int>(blockIdx.x) / R;
   const int b = chain / N, n = chain % N;
   const int ntiles = p.ntiles;
-  const bool do_y = p.a.y != nullptr;
+  constexpr bool do_y = kY;
   const int slots = G * C::COPIES;
   StatusBlock* status = p.a.status;
 
@@ -212,6 +213,7 @@ __global__ void __launch_bounds__(352, 1)
     for (int r = 0; r < ROWS; ++r)
       h[r] = p.a.H0 ? p.a.H0[(static_cast<int64_t>(chain) * p.a.K + row_global + r) * V + j] : 0.f;
     uint32_t dphase = 0;
+    int ck_left = p.a.ckpt_every, ck_idx = 0;  // countdown to the next checkpoint
     bool ok = true;
     for (int tile = 0; tile < ntiles && ok; ++tile) {
       const int st = tile % C::NS;
@@ -284,15 +286,17 @@ __global__ void __launch_bounds__(352, 1)
           }
           yp[(s * slots + g * C::COPIES + c) * V + j] = ya;
         }
-        if (p.a.ckpt != nullptr && (t + 1) % p.a.ckpt_every == 0 && t + 1 < T) {
-          float* dst = p.a.ckpt +
-                       ((static_cast<int64_t>(chain) * p.a.n_ckpt + (t + 1) / p.a.ckpt_every - 1) *
-                            p.a.K +
-                        row_global) *
-                           V +
-                       j;
+        if constexpr (kCk) {
+          if (--ck_left == 0) {  // H after step t starts a chunk: checkpoint it
+            ck_left = p.a.ckpt_every;
+            ++ck_idx;
+            if (t + 1 < T) {
+              float* dst =
+                  p.a.ckpt + ((static_cast<int64_t>(chain) * p.a.n_ckpt + ck_idx - 1) * p.a.K + row_global) * V + j;
 #pragma unroll
-          for (int r = 0; r < ROWS; ++r) dst[static_cast<int64_t>(r) * V] = h[r];
+              for (int r = 0; r < ROWS; ++r) dst[static_cast<int64_t>(r) * V] = h[r];
+            }
+          }
         }
       }
       if (!ok) break;
@@ -445,8 +449,8 @@ __global__ void __launch_bounds__(352, 1)
 // ---------------------------------------------------------------------------
 inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-template <int V, int ROWS>
-cudaError_t launch_cfg(const FwdArgs& a, int G, int R, cudaStream_t stream) {
+template <int V, int ROWS, bool kY, bool kCk>
+cudaError_t launch_cfg_mode(const FwdArgs& a, int G, int R, cudaStream_t stream) {
   using C = FwdCfg<V, ROWS>;
   TcFwdParams p{};
   p.a = a;
@@ -484,7 +488,7 @@ cudaError_t launch_cfg(const FwdArgs& a, int G, int R, cudaStream_t stream) {
       !make_tensor_map_btnx(&mv, a.v, bf, 2, a.B, a.T, a.N, V, V, kS))
     return cudaErrorInvalidValue;
 
-  auto kern = tc_forward_kernel<V, ROWS>;
+  auto kern = tc_forward_kernel<V, ROWS, kY, kCk>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if (R > 8) {
@@ -506,6 +510,15 @@ cudaError_t launch_cfg(const FwdArgs& a, int G, int R, cudaStream_t stream) {
   e = cudaLaunchKernelEx(&cfg, kern, p, mq, mk, mv);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+template <int V, int ROWS>
+cudaError_t launch_cfg(const FwdArgs& a, int G, int R, cudaStream_t stream) {
+  const bool y = a.y != nullptr, ck = a.ckpt != nullptr;
+  if (y) return ck ? launch_cfg_mode<V, ROWS, true, true>(a, G, R, stream)
+                   : launch_cfg_mode<V, ROWS, true, false>(a, G, R, stream);
+  return ck ? launch_cfg_mode<V, ROWS, false, true>(a, G, R, stream)
+            : launch_cfg_mode<V, ROWS, false, false>(a, G, R, stream);
 }
 
 }  // namespace
