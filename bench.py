@@ -103,10 +103,20 @@ def stash_bytes(w):
     return 2.0 * w["K"] * w["V"] * units(w)
 
 
-def source_hash():
+# The sources each profiled kernel is built from: a recorded DRAM traffic
+# figure is used only while these files are unchanged.
+KERNEL_SOURCES = {
+    "m2rnn_backward": ("mma_backward.cu", "mma_common.cuh", "ptx.cuh", "gate.cuh", "internal.h", "status.cuh"),
+    "m2rnn_forward": ("mma_forward.cu", "tc_forward.cu", "mv_forward.cu", "mma_common.cuh", "ptx.cuh",
+                      "gate.cuh", "internal.h", "status.cuh"),
+}
+
+
+def source_hash(kernel: str = None):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "matrix_state_non_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    names = KERNEL_SOURCES.get(kernel) or sorted(os.listdir(csrc))
+    for name in sorted(names):
         with open(os.path.join(csrc, name), "rb") as fh:
             h.update(name.encode())
             h.update(fh.read())
@@ -123,7 +133,7 @@ def profiled_traffic(kernel: str, workload: str):
     except (OSError, ValueError):
         return None
     ent = rec.get(f"{kernel}@{workload}")
-    if not ent or ent.get("source_hash") != source_hash():
+    if not ent or ent.get("source_hash") != source_hash(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 
