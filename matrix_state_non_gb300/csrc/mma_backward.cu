@@ -216,6 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     bool ok = true;
+    bool xready = true;  // the slot of step rs is known to be free
     int rs = 0;          // reverse steps done (processing order)
     int xs = 0;          // exchange slot of step rs
     uint32_t xpar = 0;   // its phase parity, (rs / kNX) & 1
@@ -245,11 +246,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t slot_regs[16];
       tmem_ld_32x32b<16>(tbuf + 16 * (L - 1), slot_regs);
       for (int s = L - 1; s >= 0; --s, ++rs) {
-        // The slot is free once the gradient warps have consumed step rs - kNX.
-        // A give-up here is acted on at the next chunk boundary (the wait
-        // raised the CTA's abort flag, so the remaining waits end at once).
-        if (rs >= kNX &&
-            !mbar_wait(smem_u32(&xempty[xs]), xpar ^ 1u, abort_flag, status, kWhereBwdXEmpty))
+        // The slot is free once the gradient warps have consumed step rs - kNX
+        // (tested at the end of the previous step, so that the test's latency
+        // overlaps that step's tail; waited for here only if it failed).  A
+        // give-up is acted on at the next chunk boundary (the wait raised the
+        // CTA's abort flag, so the remaining waits end at once).
+        if (!xready && !mbar_wait(smem_u32(&xempty[xs]), xpar ^ 1u, abort_flag, status, kWhereBwdXEmpty))
           *vabort = 1;
         const uint32_t xb = xring0 + xs * kXSlotBytes;
         float* xg = reinterpret_cast<float*>(smem + p.xring_off + xs * kXSlotBytes);
@@ -360,6 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           xs = 0;
           xpar ^= 1u;
         }
+        xready = rs + 1 < kNX || mbar_test_wait(smem_u32(&xempty[xs]), xpar ^ 1u);
       }
       // Every slot of this cache buffer has been read (the last load was
       // waited for at s = 0): the recompute may refill it.
