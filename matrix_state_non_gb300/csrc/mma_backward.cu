@@ -35,9 +35,10 @@
 //                   tensor-memory accumulator, and the fixed-order sums of
 //                   the dk, dv, df shares and dw_r.
 // Warp w of each warpgroup runs on scheduler w, so the three interleave.  The
-// chunk caches take 16 TMEM columns per step and the dW accumulator 64: with
-// C <= 14 two caches fit and the recompute of chunk c-1 overlaps the reverse
-// walk of chunk c; with 14 < C <= 28 the two alternate.
+// chunk caches hold each thread's Z_t and H_{t-1} as fp16 pairs, 8 TMEM
+// columns per step; with the 64-column dW accumulator two caches of up to 28
+// steps fit, and the rebuild of chunk c-1 overlaps the reverse walk of chunk
+// c.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -53,11 +54,11 @@ namespace {
 constexpr int kV = 64;
 constexpr int kRows = 16;
 constexpr int kThreads = 384;     // reverse warps 0-3, recompute warps 4-7, gradient warps 8-11
-// Tensor memory: columns [0, 448) hold the chunk caches (16 columns per step),
-// columns [448, 512) the dW accumulator.
+// Tensor memory: columns [0, 448) hold two chunk caches (8 columns per step:
+// Z_t and H_{t-1} as fp16 pairs), columns [448, 512) the dW accumulator.
 constexpr int kDWCol = 448;
-constexpr int kMaxChunk = kDWCol / 16;     // 28: one chunk cache
-constexpr int kTwoBufChunk = kDWCol / 32;  // 14: two caches, the recompute runs a chunk ahead
+constexpr int kCacheCols = 8;
+constexpr int kMaxChunk = kDWCol / (2 * kCacheCols);  // 28: two caches, the recompute runs a chunk ahead
 constexpr int kCBufs = 4;         // chunk input buffers (reverse, gradient, recompute, loading)
 constexpr int kNX = 8;            // exchange ring slots, reverse -> gradient warps
 // Exchange slot (reverse -> gradient warps), one per time step:
@@ -92,7 +93,7 @@ struct MmaBwdParams {
   BwdArgs a;
   int R;
   int nchunks;
-  int nbuf;  // TMEM cache buffers: 2 if ckpt_every <= kTwoBufChunk, else 1
+  int nbuf;  // TMEM cache buffers (2)
   uint32_t htile_off, cbuf_off, cbuf_bytes, cq_off, ck_off, cv_off, cdy_off, cf_off;
   uint32_t xring_off, dqp_off, dwr_off, bar_off, misc_off, zbuf_off;
   uint32_t tx_bytes;
@@ -240,11 +241,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint16_t* cv = reinterpret_cast<const uint16_t*>(cbuf + p.cv_off);
       const float* cdy = reinterpret_cast<const float*>(cbuf + p.cdy_off);
       const float* cf = reinterpret_cast<const float*>(cbuf + p.cf_off);
-      const uint32_t tbuf = tcache + 16 * CL * tb;
+      const uint32_t tbuf = tcache + kCacheCols * CL * tb;
       // The next slot's TMEM load is issued one step ahead and waited for at
       // the top of the step.
-      uint32_t slot_regs[16];
-      tmem_ld_32x32b<16>(tbuf + 16 * (L - 1), slot_regs);
+      uint32_t slot_regs[kCacheCols];
+      tmem_ld_32x32b<kCacheCols>(tbuf + kCacheCols * (L - 1), slot_regs);
       for (int s = L - 1; s >= 0; --s, ++rs) {
         // The slot is free once the gradient warps have consumed step rs - kNX
         // (tested at the end of the previous step, so that the test's latency
@@ -272,11 +273,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            Z[nt][e] = __uint_as_float(slot_regs[4 * nt + e]);
-            Hp[nt][e] = __uint_as_float(slot_regs[8 + 4 * nt + e]);
+          for (int e = 0; e < 4; e += 2) {
+            const uint32_t zw = slot_regs[2 * nt + e / 2], hw = slot_regs[4 + 2 * nt + e / 2];
+            Z[nt][e] = f16lo(zw);
+            Z[nt][e + 1] = f16hi(zw);
+            Hp[nt][e] = f16lo(hw);
+            Hp[nt][e + 1] = f16hi(hw);
           }
-        if (s > 0) tmem_ld_32x32b<16>(tbuf + 16 * (s - 1), slot_regs);
+        if (s > 0) tmem_ld_32x32b<kCacheCols>(tbuf + kCacheCols * (s - 1), slot_regs);
         // R = C + q u^T ; D = (1-f) R (1 - Z^2)
         float Rv[2][4], Dv[2][4];
 #pragma unroll
@@ -450,14 +454,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Z stash: chunk li's steps into buffer li % nbuf (one bulk copy).
     const bool zs = A.zstash != nullptr;
     const uint8_t* zsrc = reinterpret_cast<const uint8_t*>(A.zstash) + static_cast<int64_t>(blockIdx.x) * T * kZStepBytes;
+    // One staging buffer: chunk li + 1 is copied in once chunk li is rebuilt,
+    // while the reverse warps still walk chunk li - 1.
     auto issue_z = [&](int li) {
       if (lane == 0) {
         const int t0 = (p.nchunks - 1 - li) * CL;
         const uint32_t bytes = static_cast<uint32_t>(min(CL, T - t0)) * kZStepBytes;
-        const uint32_t zb = smem_u32(&zfull[li % p.nbuf]);
+        const uint32_t zb = smem_u32(&zfull[0]);
         mbar_arrive_expect_tx(zb, bytes);
-        bulk_load(smem_u32(smem + p.zbuf_off) + (li % p.nbuf) * CL * kZStepBytes, zsrc + static_cast<int64_t>(t0) * kZStepBytes,
-                  bytes, zb);
+        bulk_load(smem_u32(smem + p.zbuf_off), zsrc + static_cast<int64_t>(t0) * kZStepBytes, bytes, zb);
       }
     };
     int zissued = 0;  // Z chunks whose copies have been issued
@@ -468,9 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tm_v);
         tma_prefetch_desc(&tm_dy);
       }
-      if (zs) {
-        for (; zissued < min(p.nbuf, p.nchunks); ++zissued) issue_z(zissued);
-      }
+      if (zs) issue_z(zissued++);
       publish_chunk(0, issue_chunk(0));
     }
     bool ok = true;
@@ -490,8 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (mine && ci >= 3 && ci + 1 < p.nchunks)
         mine = mbar_wait_timed(smem_u32(&cempty[(ci + 1) % kCBufs]), ((ci - 3) / kCBufs) & 1, status,
                                kWhereBwdCEmpty);
-      if (mine && zs)
-        mine = mbar_wait_timed(smem_u32(&zfull[ci % p.nbuf]), (ci / p.nbuf) & 1, status, kWhereBwdZFull);
+      if (mine && zs) mine = mbar_wait_timed(smem_u32(&zfull[0]), ci & 1, status, kWhereBwdZFull);
       if (!mine) *rabort = 1;
       named_bar_sync(2, 128);
       if (*rabort) {
@@ -507,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint16_t* cv = reinterpret_cast<const uint16_t*>(cbuf + p.cv_off);
       const float* cdy = reinterpret_cast<const float*>(cbuf + p.cdy_off);
       const float* cf = reinterpret_cast<const float*>(cbuf + p.cf_off);
-      const uint32_t tbuf = tcache + 16 * CL * tb;
+      const uint32_t tbuf = tcache + kCacheCols * CL * tb;
       float h[2][4];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
@@ -533,22 +535,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       if (zs) {
         // Z_t from the stash; the state advances by the gate blend alone.
-        const uint32_t zb = smem_u32(smem + p.zbuf_off) + (ci % p.nbuf) * CL * kZStepBytes + (w * 32 + lane) * 16;
+        const uint32_t zb = smem_u32(smem + p.zbuf_off) + (w * 32 + lane) * 16;
         for (int s = 0; s < L; ++s) {
           const float omf = 1.f - cf[s];
           const uint4 zq = ld_shared_v4(zb + s * kZStepBytes);
           const float z[2][4] = {{f16lo(zq.x), f16hi(zq.x), f16lo(zq.y), f16hi(zq.y)},
                                  {f16lo(zq.z), f16hi(zq.z), f16lo(zq.w), f16hi(zq.w)}};
-          uint32_t cache[16];
+          // The cache takes Z_s as stashed (already fp16 pairs) and H_{s-1}.
+          const uint32_t cache[kCacheCols] = {zq.x, zq.y, zq.z, zq.w,
+                                              pack2_f16(h[0][0], h[0][1]), pack2_f16(h[0][2], h[0][3]),
+                                              pack2_f16(h[1][0], h[1][1]), pack2_f16(h[1][2], h[1][3])};
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              cache[4 * nt + e] = __float_as_uint(z[nt][e]);
-              cache[8 + 4 * nt + e] = __float_as_uint(h[nt][e]);  // H_{s-1}
-              h[nt][e] = fmaf(omf, z[nt][e] - h[nt][e], h[nt][e]);
-            }
-          tmem_st_32x32b_x16(tbuf + 16 * s, cache);
+            for (int e = 0; e < 4; ++e) h[nt][e] = fmaf(omf, z[nt][e] - h[nt][e], h[nt][e]);
+          tmem_st_32x32b_x8(tbuf + kCacheCols * s, cache);
           dq_share(s, h);
         }
         // Every read of this Z buffer and every dq share of the chunk is done.
@@ -599,19 +600,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 3; ++i)
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) mma_f16_16816(acc[nt], af[i], bw[nt][i + 1][0], bw[nt][i + 1][1]);
-          uint32_t cache[16];
+          uint32_t cache[kCacheCols];  // Z_s and H_{s-1} as fp16 pairs
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
+          for (int nt = 0; nt < 2; ++nt) {
+            float z[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float z = tanh_fast(acc[nt][e]);
-              cache[4 * nt + e] = __float_as_uint(z);
-              cache[8 + 4 * nt + e] = __float_as_uint(h[nt][e]);  // H_{s-1}
-              h[nt][e] = fmaf(omf, z - h[nt][e], h[nt][e]);
-            }
+            for (int e = 0; e < 4; ++e) z[e] = tanh_fast(acc[nt][e]);
+            cache[2 * nt] = pack2_f16(z[0], z[1]);
+            cache[2 * nt + 1] = pack2_f16(z[2], z[3]);
+            cache[4 + 2 * nt] = pack2_f16(h[nt][0], h[nt][1]);
+            cache[4 + 2 * nt + 1] = pack2_f16(h[nt][2], h[nt][3]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) h[nt][e] = fmaf(omf, z[e] - h[nt][e], h[nt][e]);
+          }
           split();
           store_tile(htile0 + ((s + 1) & 1) * 2048);
-          tmem_st_32x32b_x16(tbuf + 16 * s, cache);
+          tmem_st_32x32b_x8(tbuf + kCacheCols * s, cache);
           dq_share(s, h);
           named_bar_sync(2, 128);
         }
@@ -640,8 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (loader) {
         for (int li = max(0, issued - 2); li < min(issued, p.nchunks); ++li)
           mbar_wait_timed(smem_u32(&cfull[li % kCBufs]), (li / kCBufs) & 1, nullptr, kWhereBwdDrain);
-        for (int li = max(0, zissued - p.nbuf); li < zissued; ++li)
-          mbar_wait_timed(smem_u32(&zfull[li % p.nbuf]), (li / p.nbuf) & 1, nullptr, kWhereBwdDrain);
+        if (zissued > 0) mbar_wait_timed(smem_u32(&zfull[0]), (zissued - 1) & 1, nullptr, kWhereBwdDrain);
       }
     }
   } else {
@@ -846,7 +849,7 @@ cudaError_t launch_mma_backward(const BwdArgs& a, cudaStream_t stream) {
   p.R = a.K / kRows;
   const int C = a.ckpt_every;
   p.nchunks = (a.T + C - 1) / C;
-  p.nbuf = (C <= kTwoBufChunk) ? 2 : 1;
+  p.nbuf = 2;
   p.htile_off = 0;  // two 2 KB fp16 tiles for the rerun
   p.cbuf_off = 4096;
   p.cq_off = 0;
@@ -861,7 +864,7 @@ cudaError_t launch_mma_backward(const BwdArgs& a, cudaStream_t stream) {
   p.bar_off = p.dwr_off + 4 * kV * 4;
   p.misc_off = p.bar_off + (2 * kCBufs + 4 + 2 * kNX + 1 + 2) * 8;
   p.zbuf_off = align_up(p.misc_off + 32, 128);
-  const uint32_t zbytes = a.zstash != nullptr ? static_cast<uint32_t>(p.nbuf * C) * kZStepBytes : 0u;
+  const uint32_t zbytes = a.zstash != nullptr ? static_cast<uint32_t>(C) * kZStepBytes : 0u;
   const uint32_t smem = p.zbuf_off + zbytes + 1024;
   p.tx_bytes = 2 * C * kRows * 2 + C * kV * 2 + C * kV * 4;
   const size_t rows = static_cast<size_t>(a.B) * a.T * a.N;
