@@ -515,13 +515,15 @@ def time_fwdbwd(name, binding, dev, stream, flush, pk, dist, reps=3):
     w = WORKLOADS[name]
     inp = make_workload(name)
     d = binding.to_device(inp, dev)
-    fo = binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=CKPT_EVERY)
-    bo = binding.backward(*(d[n] for n in IN_NAMES), d["dy"], ckpt=fo["ckpt"], ckpt_every=CKPT_EVERY)
+    fo = binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=CKPT_EVERY, stash=True)
+    bo = binding.backward(*(d[n] for n in IN_NAMES), d["dy"], ckpt=fo["ckpt"], ckpt_every=CKPT_EVERY,
+                          z_stash=fo["z_stash"])
 
     def step():
-        binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=CKPT_EVERY, out=fo, workspace=fo["workspace"])
-        binding.backward(*(d[n] for n in IN_NAMES), d["dy"], ckpt=fo["ckpt"], ckpt_every=CKPT_EVERY, out=bo,
-                         workspace=bo["workspace"])
+        binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=CKPT_EVERY, stash=True, out=fo,
+                        workspace=fo["workspace"])
+        binding.backward(*(d[n] for n in IN_NAMES), d["dy"], ckpt=fo["ckpt"], ckpt_every=CKPT_EVERY,
+                         z_stash=fo["z_stash"], out=bo, workspace=bo["workspace"])
 
     for _ in range(3):
         step()
@@ -542,9 +544,9 @@ def time_fwdbwd(name, binding, dev, stream, flush, pk, dist, reps=3):
     t = dist.max(sum(a.elapsed_time(b) for a, b in ev) / reps)
     fl = fwd_flops(w) + bwd_flops(w)
     t_tensor = fl / (pk["bf16_sustained"] * 1e12)
-    t_hbm = (io_bytes_fwd(w) + io_bytes_bwd(w)) / (pk["hbm_gbs"] * 1e9)
+    t_hbm = (io_bytes_fwd(w) + io_bytes_bwd(w) + 2 * stash_bytes(w)) / (pk["hbm_gbs"] * 1e9)
     del d, fo, bo
-    return {"workload": w["desc"], "kernel": "warp-mma (V = 16 register kernels)", "ms": t,
+    return {"workload": w["desc"] + ", Z stash", "kernel": "warp-mma (V = 16 register kernels)", "ms": t,
             "value": dist.world * units(w) / (t * 1e-3), "unit": UNIT,
             "ns_per_step_per_chain": t * 1e6 / w["T"],
             "roofline_ms": max(t_tensor, t_hbm) * 1e3, "roofline_frac": max(t_tensor, t_hbm) / (t * 1e-3),

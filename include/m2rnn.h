@@ -160,7 +160,7 @@ int m2rnn_forward_state(const void* q, const void* k, const void* v,
 
 /* Bytes of the Z stash of m2rnn_forward_state / m2rnn_backward_state
  * (B T N K V fp16 values), or 0 where the stash is not supported (it is for
- * bf16 inputs with V = 64 and K a multiple of 16, <= 128). */
+ * bf16 inputs with V = 64 or V = 16 and K a multiple of 16, <= 128). */
 size_t m2rnn_z_stash_size(int64_t B, int64_t T, int64_t N, int64_t K,
                           int64_t V, m2rnn_dtype dtype);
 
@@ -188,7 +188,8 @@ size_t m2rnn_backward_state_workspace_size(int64_t B, int64_t T, int64_t N,
  * piece before it.  `ckpt`, if given, must come from m2rnn_forward_state
  * with the same H_0.  z_stash (may be NULL): the stash that same forward
  * call wrote, with its `ckpt` (required when T > ckpt_every), ckpt_every
- * <= 28; Z_t then comes from the stash in fp16 instead of a rerun.
+ * <= 28 (V = 64) or within the V = 16 backward's chunk limit (32, or 16 for
+ * K > 64); Z_t then comes from the stash in fp16 instead of a rerun.
  * workspace: m2rnn_backward_state_workspace_size bytes.
  */
 int m2rnn_backward_state(const void* q, const void* k, const void* v,

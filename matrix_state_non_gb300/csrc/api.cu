@@ -127,9 +127,9 @@ BwdLayout bwd_layout(int64_t B, int64_t T, int64_t N, int64_t K, int64_t V, int 
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA; }
 
-// Shapes whose forward can leave Z_t for the backward (the V = 64 warp-MMA pair).
+// Shapes whose forward can leave Z_t for the backward (the warp-MMA kernels, V = 64 and V = 16).
 bool stash_ok(int64_t K, int64_t V, int dt) {
-  return dt == M2RNN_BF16 && V == 64 && K >= 16 && K <= kMaxDim && K % 16 == 0;
+  return dt == M2RNN_BF16 && (V == 64 || V == 16) && K >= 16 && K <= kMaxDim && K % 16 == 0;
 }
 
 }  // namespace
@@ -313,7 +313,9 @@ int backward_impl(const void* q, const void* k, const void* v, const GateIn& gat
   int bpath = choose_bwd_path(K, V, dtype, ckpt_every);
   if (ckpt_every < 1 || ckpt_every > kMaxCkptEvery) return M2RNN_ERR_INVALID_ARG;
   if (z_stash != nullptr) {
-    if (!stash_ok(K, V, dtype) || ckpt_every > mma_backward_max_chunk()) return M2RNN_ERR_UNSUPPORTED;
+    const bool chunk_ok = (V == 16) ? mv_backward_supported(static_cast<int>(K), 16, ckpt_every)
+                                    : ckpt_every <= mma_backward_max_chunk();
+    if (!stash_ok(K, V, dtype) || !chunk_ok) return M2RNN_ERR_UNSUPPORTED;
     if (!aligned16(z_stash)) return M2RNN_ERR_INVALID_ARG;
     if (ckpt == nullptr && (T - 1) / ckpt_every > 0) return M2RNN_ERR_INVALID_ARG;  // stash and checkpoints go together
     bpath = kPathMma;  // the kernel that reads the stash

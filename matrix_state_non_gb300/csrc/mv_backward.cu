@@ -41,12 +41,14 @@ struct MvBwdParams {
   BwdArgs a;
   int R, nchunks;
   uint32_t colset;  // TMEM column offset of warps 4..7 (they share lane quadrants with 0..3)
-  uint32_t cbuf_off, cbuf_bytes, cq_off, ck_off, cv_off, cdy_off, cf_off, part_off, bar_off, misc_off;
+  uint32_t cbuf_off, cbuf_bytes, cq_off, ck_off, cv_off, cdy_off, cf_off, cz_off, part_off, bar_off, misc_off;
   uint32_t tx_bytes;
 };
 
-// kClip: the state-gradient clamp as a compile-time switch (no per-step branch).
-template <bool kClip>
+// kClip: the state-gradient clamp as a compile-time switch (no per-step
+// branch).  kZ: Z_t comes from the forward's stash (copied with the chunk's
+// inputs), so the chunk rebuild is the gate blend alone.
+template <bool kClip, bool kZ>
 __global__ void __launch_bounds__((kMaxRB + 1) * 32, 1)
     mv_backward_kernel(const __grid_constant__ MvBwdParams p, const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -135,6 +137,7 @@ __global__ void __launch_bounds__((kMaxRB + 1) * 32, 1)
       const uint16_t* cv = reinterpret_cast<const uint16_t*>(cbuf + p.cv_off);
       const float* cdy = reinterpret_cast<const float*>(cbuf + p.cdy_off);
       const float* cf = reinterpret_cast<const float*>(cbuf + p.cf_off);
+      const uint32_t cz = smem_u32(cbuf + p.cz_off) + (w * 32 + lane) * 16;  // this thread's stashed Z, step 0
       // ---- rerun the chunk from its start state (Eq. 10-11), caching Z_s and H_{s-1} ----
       float h[2][4];
       {
@@ -153,6 +156,24 @@ __global__ void __launch_bounds__((kMaxRB + 1) * 32, 1)
           }
         }
       }
+      if constexpr (kZ) {
+        for (int s = 0; s < L; ++s) {
+          const float omf = 1.f - cf[s];
+          const uint4 zq = ld_shared_v4(cz + s * R * 512);
+          const float z[2][4] = {{f16lo(zq.x), f16hi(zq.x), f16lo(zq.y), f16hi(zq.y)},
+                                 {f16lo(zq.z), f16hi(zq.z), f16lo(zq.w), f16hi(zq.w)}};
+          uint32_t cache[16];
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              cache[4 * nt + e] = __float_as_uint(z[nt][e]);
+              cache[8 + 4 * nt + e] = __float_as_uint(h[nt][e]);  // H_{s-1}
+              h[nt][e] = fmaf(omf, z[nt][e] - h[nt][e], h[nt][e]);
+            }
+          tmem_st_32x32b_x16(tcache + 16 * s, cache);
+        }
+      } else {
       for (int s = 0; s < L; ++s) {
         uint32_t a[4];  // fp16 H_{s-1}, as in the forward
 #pragma unroll
@@ -184,6 +205,7 @@ __global__ void __launch_bounds__((kMaxRB + 1) * 32, 1)
             h[nt][e] = fmaf(omf, z - h[nt][e], h[nt][e]);
           }
         tmem_st_32x32b_x16(tcache + 16 * s, cache);
+      }
       }
       tmem_st_wait();
       // ---- reverse walk: h = H_t of the chunk's last step ----
@@ -385,7 +407,12 @@ __global__ void __launch_bounds__((kMaxRB + 1) * 32, 1)
       __syncwarp();
       const uint32_t fb = smem_u32(&cfull[cb]);
       if (lane == 0) {
-        mbar_arrive_expect_tx(fb, p.tx_bytes);
+        const uint32_t zbytes = kZ ? static_cast<uint32_t>(min(CL, T - t0) * R * 512) : 0u;
+        mbar_arrive_expect_tx(fb, p.tx_bytes + zbytes);
+        if constexpr (kZ)  // the chunk's stashed Z: one contiguous range
+          bulk_load(smem_u32(buf + p.cz_off),
+                    reinterpret_cast<const uint8_t*>(A.zstash) + (static_cast<int64_t>(chain) * T + t0) * R * 512,
+                    zbytes, fb);
         tma_load_4d(smem_u32(buf + p.cq_off), &tm_q, fb, 0, qk_head(A.qkN, n), t0, b);
         tma_load_4d(smem_u32(buf + p.ck_off), &tm_k, fb, 0, qk_head(A.qkN, n), t0, b);
         tma_load_4d(smem_u32(buf + p.cv_off), &tm_v, fb, 0, n, t0, b);
@@ -432,7 +459,8 @@ cudaError_t launch_mv_backward(const BwdArgs& a, cudaStream_t stream) {
   p.cv_off = p.ck_off + align_up(C * a.K * 2, 128);
   p.cdy_off = p.cv_off + align_up(C * kV * 2, 128);
   p.cf_off = p.cdy_off + align_up(C * kV * 4, 128);
-  p.cbuf_bytes = align_up(p.cf_off + kMaxChunkMv * 4, 128);
+  p.cz_off = align_up(p.cf_off + kMaxChunkMv * 4, 128);
+  p.cbuf_bytes = align_up(p.cz_off + (a.zstash != nullptr ? C * p.R * 512 : 0), 128);
   p.part_off = kCBufs * p.cbuf_bytes;
   p.bar_off = p.part_off + align_up(kMaxChunkMv * p.R * (kV + 1) * 4, 128);
   p.misc_off = p.bar_off + 2 * kCBufs * 8;
@@ -447,7 +475,8 @@ cudaError_t launch_mv_backward(const BwdArgs& a, cudaStream_t stream) {
       !make_tensor_map_btnx(&mv, a.v, bf, 2, a.B, a.T, a.N, kV, kV, C) ||
       !make_tensor_map_btnx(&mdy, a.dy, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.B, a.T, a.N, kV, kV, C))
     return cudaErrorInvalidValue;
-  auto kernel = a.clip > 0.f ? mv_backward_kernel<true> : mv_backward_kernel<false>;
+  auto kernel = a.zstash != nullptr ? (a.clip > 0.f ? mv_backward_kernel<true, true> : mv_backward_kernel<false, true>)
+                                    : (a.clip > 0.f ? mv_backward_kernel<true, false> : mv_backward_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   kernel<<<a.B * a.N, (p.R + 1) * 32, smem, stream>>>(p, mq, mk, mv, mdy);

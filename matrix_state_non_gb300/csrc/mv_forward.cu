@@ -23,6 +23,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "internal.h"
 #include "gate.cuh"
@@ -45,8 +46,12 @@ struct MvFwdParams {
   uint32_t tx_bytes;
 };
 
-// Compile-time modes: kY = readout y, kCk = checkpoints (no per-step branch on either).
-template <bool kY, bool kCk>
+// Compile-time modes: kY = readout y, kCk = checkpoints, kZ = the Z stash
+// (no per-step branch on any of them).  The stash layout for V = 16: per
+// (chain, step) the R row-block warps' 512 bytes each, lane l's 16 bytes
+// holding its fp16 Z values in accumulator-fragment order, so a chunk of
+// steps is one contiguous range.
+template <bool kY, bool kCk, bool kZ>
 __global__ void __launch_bounds__((kMaxRB + 1) * 32, 1)
     mv_forward_kernel(const __grid_constant__ MvFwdParams p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
@@ -91,6 +96,9 @@ __global__ void __launch_bounds__((kMaxRB + 1) * 32, 1)
         report_device_error(status, kStatusCheck, kWhereWRange);
     }
     const int64_t row_g = static_cast<int64_t>(chain) * K + 16 * w + g;  // state row of lane g
+    uint8_t* const zst = !kZ ? nullptr
+                             : reinterpret_cast<uint8_t*>(A.zstash) + static_cast<int64_t>(chain) * T * R * 512 +
+                                   w * 512 + lane * 16;
     float h[2][4];
     if (A.H0 != nullptr) {
 #pragma unroll
@@ -182,12 +190,19 @@ __global__ void __launch_bounds__((kMaxRB + 1) * 32, 1)
             const uint32_t qhi = *reinterpret_cast<const uint32_t*>(qs + (s - 1) * K + 16 * w + 2 * qd + 8);
             readout_mma(qlo, qhi, yd);
           }
+          float zv[2][4];
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              h[nt][e] = fmaf(omf, tanh_fast(acc[nt][e]) - h[nt][e], h[nt][e]);  // Eq. 11
+            for (int e = 0; e < 4; ++e) {
+              zv[nt][e] = tanh_fast(acc[nt][e]);
+              h[nt][e] = fmaf(omf, zv[nt][e] - h[nt][e], h[nt][e]);  // Eq. 11
+            }
           split();
+          if constexpr (kZ)  // Z_t for the backward (a streaming store, off the chain)
+            st_global_cs_v4(zst + static_cast<int64_t>(t0 + s) * R * 512,
+                            make_uint4(pack2_f16(zv[0][0], zv[0][1]), pack2_f16(zv[0][2], zv[0][3]),
+                                       pack2_f16(zv[1][0], zv[1][1]), pack2_f16(zv[1][2], zv[1][3])));
           if (do_y && s > 0) store_y(yd, s - 1);
         }
         if constexpr (kCk) {
@@ -308,8 +323,12 @@ cudaError_t launch_mv_forward(const FwdArgs& a, cudaStream_t stream) {
       !make_tensor_map_btnx(&mk, a.k, bf, 2, a.B, a.T, qN, a.K, a.K, kS) ||
       !make_tensor_map_btnx(&mv, a.v, bf, 2, a.B, a.T, a.N, kV, kV, kS))
     return cudaErrorInvalidValue;
-  auto kernel = a.y != nullptr ? (a.ckpt != nullptr ? mv_forward_kernel<true, true> : mv_forward_kernel<true, false>)
-                               : (a.ckpt != nullptr ? mv_forward_kernel<false, true> : mv_forward_kernel<false, false>);
+  auto pick = [&](auto z) {
+    constexpr bool Z = decltype(z)::value;
+    return a.y != nullptr ? (a.ckpt != nullptr ? mv_forward_kernel<true, true, Z> : mv_forward_kernel<true, false, Z>)
+                          : (a.ckpt != nullptr ? mv_forward_kernel<false, true, Z> : mv_forward_kernel<false, false, Z>);
+  };
+  auto kernel = a.zstash != nullptr ? pick(std::true_type{}) : pick(std::false_type{});
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;

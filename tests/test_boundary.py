@@ -169,11 +169,14 @@ def test_z_stash_rules_without_a_device(lib):
     assert binding.m2rnn_z_stash_size(1, 8, 1, 64, 64, binding.M2RNN_F32) == 0
     assert binding.m2rnn_z_stash_size(1, 8, 1, 40, 64, bf) == 0              # K not a multiple of 16
 
+    assert binding.m2rnn_z_stash_size(2, 8, 4, 64, 16, bf) == 2 * 8 * 4 * 64 * 16 * 2   # V = 16 too
+
     def fs(V=64, z=P, K=64):
         return binding.m2rnn_forward_state(P, P, P, P, P, P, None, P, None, None, 0, z, 1, 8, 1, 1, K, V, bf, P,
                                            1 << 20, None)
     assert fs(V=128) == binding.M2RNN_ERR_UNSUPPORTED
-    assert fs(K=48, V=16) == binding.M2RNN_ERR_UNSUPPORTED
+    assert fs(K=40, V=16) == binding.M2RNN_ERR_UNSUPPORTED   # K not a multiple of 16
+    assert fs(V=32) == binding.M2RNN_ERR_UNSUPPORTED
     assert fs(z=P + 8) == binding.M2RNN_ERR_INVALID_ARG
 
     def bs(T=64, ckpt=None, C=14, z=P):
@@ -182,6 +185,12 @@ def test_z_stash_rules_without_a_device(lib):
     assert bs() == binding.M2RNN_ERR_INVALID_ARG          # T > ckpt_every needs the forward's checkpoints
     assert bs(C=29, ckpt=P) == binding.M2RNN_ERR_UNSUPPORTED   # longer than the backward's chunk cache
     assert bs(z=P + 4, ckpt=P) == binding.M2RNN_ERR_INVALID_ARG
+
+    def bs16(K=64, C=14):
+        return binding.m2rnn_backward_state(P, P, P, P, P, P, None, P, None, P, C, P, P, P, P, P, P, P, None,
+                                            0.0, 1, 64, 1, 1, K, 16, bf, P, 1 << 30, None)
+    assert bs16(K=128, C=17) == binding.M2RNN_ERR_UNSUPPORTED   # over the V = 16 chunk limit for K > 64
+    assert bs16(K=64, C=33) == binding.M2RNN_ERR_UNSUPPORTED
 
 
 def test_noalloc_backward_rejects_unsupported_shapes_without_a_device(lib):

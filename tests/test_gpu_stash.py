@@ -109,3 +109,43 @@ def test_stash_backward_full_size_sampled_head():
            "df": got["df"][:, :, n:n + 1], "dW": got["dW"][n:n + 1], "dw_r": got["dw_r"][n:n + 1]}
     check_grads(sub, ref, "bf16", label=name)
     assert w["V"] == 64
+
+
+# V = 16 (the multi-value heads of the reading notes, section 2.4): the stash
+# is written by the register-resident V = 16 forward and read by its backward.
+@pytest.mark.parametrize("B,N,T,K,C,shared", [(2, 4, 50, 64, 14, True), (1, 3, 100, 64, 28, False),
+                                             (2, 2, 33, 128, 16, True), (1, 2, 1, 32, 14, False),
+                                             (1, 2, 64, 16, 32, True)])
+def test_stash_backward_v16_matches_oracle(B, N, T, K, C, shared):
+    inp = make_inputs(B, N, T, K, 16, "bf16", seed=620 + T + C, with_dy=True)
+    if shared:
+        for name in ("q", "k"):
+            inp.store[name] = np.ascontiguousarray(inp.store[name][:, :, :1])
+            inp.exact[name] = np.ascontiguousarray(inp.exact[name][:, :, :1])
+    H0 = np.random.default_rng(T).uniform(-0.9, 0.9, (B, N, K, 16)).astype(np.float32)
+    got = gpu_backward(inp, ckpt_every=C, stash=True, H_0=H0, want_dH0=True)
+    ref = oracle_backward(*oracle_args(inp), inp.exact["dy"], None, H_0=H0.astype(np.float64))
+    check_grads(got, ref, "bf16", label=(B, N, T, K, C, shared))
+
+
+def test_stash_v16_clipping_and_full_size():
+    """Clipped state gradients with the stash, then the V = 16 forward+backward
+    workload (B=4, 16 heads, T=4096, K=64, shared q/k) as the benchmark runs
+    it, one head against the oracle."""
+    inp = make_inputs(1, 2, 60, 64, 16, "bf16", seed=630, with_dy=True)
+    got = gpu_backward(inp, ckpt_every=28, stash=True, state_grad_clip=0.05)
+    ref = oracle_backward(*oracle_args(inp), inp.exact["dy"], None, state_grad_clip=0.05)
+    check_grads(got, ref, "bf16", label="clip")
+    name = "mv_bf16_k64v16"
+    inp = make_workload(name)
+    got = gpu_backward(inp, ckpt_every=28, stash=True)
+    e = inp.exact
+    n = WORKLOADS[name]["N"] - 1
+    ref = oracle_backward(e["q"], e["k"], e["v"][:, :, n:n + 1], e["f"][:, :, n:n + 1], e["W"][n:n + 1],
+                          e["w_r"][n:n + 1], e["dy"][:, :, n:n + 1])
+    # q, k are shared: their gradients sum over every head, so compare the
+    # per-head outputs of head n only.
+    sub = {"dv": got["dv"][:, :, n:n + 1], "df": got["df"][:, :, n:n + 1], "dW": got["dW"][n:n + 1],
+           "dw_r": got["dw_r"][n:n + 1]}
+    for k_, v_ in sub.items():
+        assert rel_fro(v_, ref[k_]) <= TOL_BF16_REL, (k_, rel_fro(v_, ref[k_]))
