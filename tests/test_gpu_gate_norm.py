@@ -49,7 +49,7 @@ def _oracle_gated_args(inp, ge):
     return [q, k, e["v"], gate(ge["a"], ge["alpha"], ge["beta"]), e["W"], e["w_r"]]
 
 
-def _run_gated(inp, gs, backward=False, ckpt_every=14, reuse=False):
+def _run_gated(inp, gs, backward=False, ckpt_every=14, reuse=False, stash=False):
     import torch
     from matrix_state_non_gb300 import binding
     d = {n: _dev(x) for n, x in inp.store.items()}
@@ -61,8 +61,11 @@ def _run_gated(inp, gs, backward=False, ckpt_every=14, reuse=False):
         assert st == binding.M2RNN_OK, (binding.status_string(st), detail)
         torch.cuda.synchronize()
         return {n: out[n].cpu().numpy() for n in ("y", "H_T")}
-    ckpt = binding.forward(*args, gate=g, ckpt_every=ckpt_every)["ckpt"] if reuse else None
-    out = binding.backward(*args, d["dy"], gate=g, ckpt=ckpt, ckpt_every=ckpt_every)
+    ckpt = z = None
+    if reuse or stash:
+        fo = binding.forward(*args, gate=g, ckpt_every=ckpt_every, stash=stash)
+        ckpt, z = fo["ckpt"], fo.get("z_stash")
+    out = binding.backward(*args, d["dy"], gate=g, ckpt=ckpt, ckpt_every=ckpt_every, z_stash=z)
     st, detail = binding.sync_status(out["workspace"])
     assert st == binding.M2RNN_OK, (binding.status_string(st), detail)
     torch.cuda.synchronize()
@@ -123,6 +126,14 @@ def test_gated_backward_other_families(B, N, T, K, V, dtype, shared, C):
     _check_gated_grads(got, inp, ge, TOL_F32 if dtype == "f32" else TOL_BF16_REL, (B, N, T, K, V, dtype))
 
 
+@pytest.mark.parametrize("B,N,T,K,V,C,shared", [(2, 2, 37, 64, 64, 14, False), (1, 3, 64, 32, 64, 28, False),
+                                               (2, 4, 50, 64, 16, 28, True)])
+def test_gated_backward_with_stash(B, N, T, K, V, C, shared):
+    inp, gs, ge = _gated_case(B, N, T, K, V, "bf16", seed=760 + T, shared_qk=shared)
+    got = _run_gated(inp, gs, backward=True, ckpt_every=C, stash=True)
+    _check_gated_grads(got, inp, ge, TOL_BF16_REL, (B, N, T, K, V, C, "stash"))
+
+
 def test_gated_backward_is_deterministic():
     inp, gs, _ = _gated_case(2, 4, 90, 64, 64, "bf16", seed=740)
     a = _run_gated(inp, gs, backward=True)
@@ -132,11 +143,13 @@ def test_gated_backward_is_deterministic():
 
 
 def test_gated_full_size_properties():
-    """The fwd+bwd workload's shape (B=4, heads=8, T=4096, K=V=64): dbeta is
+    """The fwd+bwd workload's shape (B=4, heads=8, T=4096, K=V=64), run as
+    the benchmark's gated block runs it (Z stash, 28-step chunks): dbeta is
     the (b, t)-sum of da, and dalpha the (b, t)-sum of da * s / (alpha
-    sigmoid(a + beta)), recomputed from the kernel's own da in float64."""
+    sigmoid(a + beta)), recomputed from the kernel's own da in float64; and
+    one head's gradients against the oracle."""
     inp, gs, ge = _gated_case(4, 8, 4096, 64, 64, "bf16", seed=750)
-    got = _run_gated(inp, gs, backward=True)
+    got = _run_gated(inp, gs, backward=True, ckpt_every=28, stash=True)
     da = got["da"].astype(np.float64)
     assert np.all(np.isfinite(da))
     # fp32 sums of 16384 terms: bound the error by the sum of magnitudes
@@ -146,6 +159,14 @@ def test_gated_full_size_properties():
     sig = 0.5 * (1.0 + np.tanh(0.5 * x))
     terms = da * s / (ge["alpha"] * sig)
     assert np.all(np.abs(got["dalpha"] - terms.sum(axis=(0, 1))) <= 1e-4 * np.abs(terms).sum(axis=(0, 1)))
+    n = 0
+    e = inp.exact
+    f = gate(ge["a"], ge["alpha"], ge["beta"])[:, :, n:n + 1]
+    ref = oracle_backward(e["q"][:, :, n:n + 1], e["k"][:, :, n:n + 1], e["v"][:, :, n:n + 1], f, e["W"][n:n + 1],
+                          e["w_r"][n:n + 1], e["dy"][:, :, n:n + 1])
+    da_ref, _, _ = gate_backward(ge["a"][:, :, n:n + 1], ge["alpha"][n:n + 1], ge["beta"][n:n + 1], ref["df"])
+    for name, r in (("dq", ref["dq"]), ("dk", ref["dk"]), ("dv", ref["dv"]), ("da", da_ref)):
+        assert rel_fro(got[name][:, :, n:n + 1], r) <= TOL_BF16_REL, (name, rel_fro(got[name][:, :, n:n + 1], r))
 
 
 # ---------------------------------------------------------------------------
