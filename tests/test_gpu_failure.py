@@ -34,3 +34,27 @@ def test_bounded_wait_reports_timeout_and_context_survives(monkeypatch):
     got = gpu_forward(inp)  # the same context keeps working
     y_ref, H_ref = oracle_forward(*oracle_args(inp))
     check_forward(got, y_ref, H_ref, "bf16")
+
+
+@pytest.mark.parametrize("K,V", [(64, 64), (64, 16), (128, 128)])
+def test_weight_outside_fp16_range_is_reported(K, V):
+    """The tensor-core kernels take W re-encoded as fp16; an entry of W that
+    fp16 cannot hold (|W| >= 65520) is reported through the status block
+    (M2RNN_ERR_DEVICE at the input-check site), not silently turned into
+    infinities.  The run itself completes; the next call is clean."""
+    import torch
+    from matrix_state_non_gb300 import binding
+    from matrix_state_non_gb300.inputs import f32_to_bf16_bits
+    inp = make_inputs(1, 2, 40, K, V, "bf16", seed=11)
+    inp.store["W"] = inp.store["W"].copy()
+    inp.store["W"][1, 3, 5] = f32_to_bf16_bits(np.array([70000.0], dtype=np.float32))[0]
+    d = binding.to_device(inp)
+    out = binding.forward(*(d[n] for n in NAMES))
+    st, detail = binding.sync_status(out["workspace"])
+    assert st == binding.M2RNN_ERR_DEVICE and detail == 301, (binding.status_string(st), detail)
+    # A W inside the range on the same context: no error, and the oracle agrees.
+    good = make_inputs(1, 2, 40, K, V, "bf16", seed=12)
+    got = gpu_forward(good)
+    y_ref, H_ref = oracle_forward(*oracle_args(good))
+    check_forward(got, y_ref, H_ref, "bf16", label=("after range error", K, V))
+    torch.cuda.synchronize()

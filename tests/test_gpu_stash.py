@@ -138,7 +138,7 @@ def test_stash_v16_clipping_and_full_size():
     check_grads(got, ref, "bf16", label="clip")
     name = "mv_bf16_k64v16"
     inp = make_workload(name)
-    got = gpu_backward(inp, ckpt_every=28, stash=True)
+    got = gpu_backward(inp, ckpt_every=32, stash=True)  # the benchmark's chunk length for V = 16
     e = inp.exact
     n = WORKLOADS[name]["N"] - 1
     ref = oracle_backward(e["q"], e["k"], e["v"][:, :, n:n + 1], e["f"][:, :, n:n + 1], e["W"][n:n + 1],
