@@ -410,24 +410,37 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
     for (int tile = 0; tile < ntiles; ++tile) {
       const int ys = tile % kYS;
       const uint32_t par = (tile / kYS) & 1;
+      const int t0 = tile * kS;
+      const int nsteps = min(kS, T - t0);
+      // v_t of this CTA's steps of the tile (s = cta_rank + i R), loaded
+      // before the waits so that their latency overlaps them.
+      uint32_t vr[kS];
+#pragma unroll
+      for (int i = 0; i < kS; ++i) {
+        const int s = cta_rank + i * R;
+        vr[i] = s < nsteps ? *reinterpret_cast<const uint32_t*>(
+                                 vg + ((static_cast<int64_t>(b) * T + t0 + s) * N + n) * kV + 2 * lane)
+                           : 0u;
+      }
       if (!mbar_wait(smem_u32(&yfull[ys]), par, abort_flag, status, kWhereFwdYFull)) break;
       fence_acq_rel_cluster();
       if (lane < R) mbar_arrive_cluster(mapa_shared(smem_u32(&ypeer[ys]), lane));
       if (!mbar_wait<true>(smem_u32(&ypeer[ys]), par, abort_flag, status, kWhereFwdYPeer)) break;
-      const int t0 = tile * kS;
-      const int nsteps = min(kS, T - t0);
       const uint32_t ybase = smem_u32(sY + ys * kS * kV);
-      for (int s = cta_rank; s < nsteps; s += R) {
-        const int64_t row = (static_cast<int64_t>(b) * T + t0 + s) * N + n;
-        float a0 = 0.f, a1 = 0.f;
-        for (int pr = 0; pr < R; ++pr) {  // fixed order over the chain's row blocks
-          const uint32_t ra = mapa_shared(ybase, pr) + static_cast<uint32_t>((s * kV + 2 * lane) * 4);
-          a0 += ld_shared_cluster_f32(ra);
-          a1 += ld_shared_cluster_f32(ra + 4);
+#pragma unroll
+      for (int i = 0; i < kS; ++i) {
+        const int s = cta_rank + i * R;
+        if (s < nsteps) {
+          const int64_t row = (static_cast<int64_t>(b) * T + t0 + s) * N + n;
+          float a0 = 0.f, a1 = 0.f;
+          for (int pr = 0; pr < R; ++pr) {  // fixed order over the chain's row blocks
+            const uint32_t ra = mapa_shared(ybase, pr) + static_cast<uint32_t>((s * kV + 2 * lane) * 4);
+            a0 += ld_shared_cluster_f32(ra);
+            a1 += ld_shared_cluster_f32(ra + 4);
+          }
+          *reinterpret_cast<float2*>(p.a.y + row * kV + 2 * lane) =
+              make_float2(fmaf(wr0, bf16lo(vr[i]), a0), fmaf(wr1, bf16hi(vr[i]), a1));
         }
-        const uint32_t vv = *reinterpret_cast<const uint32_t*>(vg + row * kV + 2 * lane);
-        *reinterpret_cast<float2*>(p.a.y + row * kV + 2 * lane) =
-            make_float2(fmaf(wr0, bf16lo(vv), a0), fmaf(wr1, bf16hi(vv), a1));
       }
       fence_acq_rel_cluster();
       __syncwarp();

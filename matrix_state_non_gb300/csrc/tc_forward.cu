@@ -29,8 +29,8 @@
 // group's tanh work (issuing a step's MMAs costs a few hundred cycles, so it
 // must not sit inside an epilogue warp); warp 4G+1 = TMA producer for q/k/v
 // tiles of S = 32 steps (f through plain loads); warp 4G+2 = readout reducer,
-// which sums the per-group/per-CTA partial readouts of a tile, adds w_r * v
-// and stores y.  Every wait is bounded (see ptx.cuh).
+// which sums the per-group/per-CTA partial readouts of a tile (one of them
+// carries w_r * v) and stores y.  Every wait is bounded (see ptx.cuh).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -65,7 +65,7 @@ struct FwdCfg {
 
 struct TcFwdParams {
   FwdArgs a;
-  int G, R, NRtot;
+  int R, NRtot;
   int ntiles;
   uint32_t tmem_cols;
   uint32_t a_tcol;  // TMEM column of the A operand (W^T stacked)
@@ -85,9 +85,12 @@ __device__ __forceinline__ void unpack8_bf16(const uint4 w, float (&o)[8]) {
   o[7] = __uint_as_float(w.w & 0xFFFF0000u);
 }
 
-// kY = readout y, kCk = checkpoints: compile-time modes, no per-step test.
-template <int V, int ROWS, bool kY, bool kCk>
-__global__ void __launch_bounds__(352, 1)
+// Compile-time modes, no per-step test: G epilogue warpgroups, kY = readout
+// y, kCk = checkpoints.  (G as a runtime value left the readout reducer's
+// loops unrolled too little to keep up: 5.72 against 4.88 ms on the
+// T = 4096, K = V = 128 workload, measured.)
+template <int V, int ROWS, int G, bool kY, bool kCk>
+__global__ void __launch_bounds__((4 * G + 3) * 32, 1)
     tc_forward_kernel(const __grid_constant__ TcFwdParams p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v) {
@@ -96,14 +99,14 @@ __global__ void __launch_bounds__(352, 1)
   // Align the working base to 1 KB (the launch reserves the slack).
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int G = p.G, R = p.R, NRtot = p.NRtot;
+  const int R = p.R, NRtot = p.NRtot;
   const int T = p.a.T, N = p.a.N;
   const int cta_rank = static_cast<int>(blockIdx.x) % R;
   const int chain = static_cast<int>(blockIdx.x) / R;
   const int b = chain / N, n = chain % N;
   const int ntiles = p.ntiles;
   constexpr bool do_y = kY;
-  const int slots = G * C::COPIES;
+  constexpr int slots = G * C::COPIES;
   StatusBlock* status = p.a.status;
 
   uint8_t* sB = smem + p.b_off;
@@ -212,6 +215,11 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
     for (int r = 0; r < ROWS; ++r)
       h[r] = p.a.H0 ? p.a.H0[(static_cast<int64_t>(chain) * p.a.K + row_global + r) * V + j] : 0.f;
+    // The residual w_r * v_t of column j rides on the partial of the chain's
+    // first rows (CTA 0, group 0, row run 0); the reducer only sums partials.
+    const float wrv = (cta_rank == 0 && g == 0 && c == 0)
+                          ? bf16_bits_to_f32(static_cast<const uint16_t*>(p.a.w_r)[static_cast<int64_t>(n) * V + j])
+                          : 0.f;
     uint32_t dphase = 0;
     int ck_left = p.a.ckpt_every, ck_idx = 0;  // countdown to the next checkpoint
     bool ok = true;
@@ -276,7 +284,7 @@ __global__ void __launch_bounds__(352, 1)
         // ---- off the serial chain ----
         if (do_y) {
           const uint16_t* qr = qs + s * NRtot + row_in_cta;
-          float ya = 0.f;
+          float ya = wrv * vj;  // w_r * v_t, carried by one partial of each column (wrv = 0 elsewhere)
 #pragma unroll
           for (int r0 = 0; r0 < ROWS; r0 += 8) {
             float qf[8];
@@ -386,11 +394,9 @@ __global__ void __launch_bounds__(352, 1)
     }
   } else if (warp == 4 * G + 2 && do_y) {
     // ---------------- readout reducer ----------------
-    const uint16_t* vg = static_cast<const uint16_t*>(p.a.v);
-    const uint16_t* wr = static_cast<const uint16_t*>(p.a.w_r) + static_cast<int64_t>(n) * V;
-    float wrl[V / 32];
-#pragma unroll
-    for (int u = 0; u < V / 32; ++u) wrl[u] = bf16_bits_to_f32(wr[lane + 32 * u]);
+    // The partials already carry w_r * v_t (see the epilogue): y_t is their
+    // sum in a fixed order (CTAs, then slots), every load of a step issued
+    // before the first add.
     bool ok = true;
     int done = 0;
     for (int tile = 0; tile < ntiles; ++tile) {
@@ -411,18 +417,23 @@ __global__ void __launch_bounds__(352, 1)
       const uint32_t ybase = smem_u32(sY + ys * (kS * slots * V));
       for (int s = cta_rank; s < nsteps; s += R) {
         const int64_t row = (static_cast<int64_t>(b) * T + t0 + s) * N + n;
+        float acc[V / 32];
 #pragma unroll
-        for (int u = 0; u < V / 32; ++u) {
-          const int jj = lane + 32 * u;
-          float acc = 0.f;
-          for (int pr = 0; pr < R; ++pr) {  // fixed order: CTAs, then slots
-            const uint32_t rb = mapa_shared(ybase, pr);
-            for (int sl = 0; sl < slots; ++sl)
-              acc += ld_shared_cluster_f32(rb + static_cast<uint32_t>(((s * slots + sl) * V + jj) * 4));
-          }
-          const float vv = bf16_bits_to_f32(vg[row * V + jj]);
-          p.a.y[row * V + jj] = fmaf(wrl[u], vv, acc);  // + w_r * v_t
+        for (int u = 0; u < V / 32; ++u) acc[u] = 0.f;
+        for (int pr = 0; pr < R; ++pr) {
+          const uint32_t rb = mapa_shared(ybase, pr) + static_cast<uint32_t>((s * slots * V + lane) * 4);
+          float x[slots][V / 32];
+#pragma unroll
+          for (int sl = 0; sl < slots; ++sl)
+#pragma unroll
+            for (int u = 0; u < V / 32; ++u) x[sl][u] = ld_shared_cluster_f32(rb + static_cast<uint32_t>((sl * V + 32 * u) * 4));
+#pragma unroll
+          for (int sl = 0; sl < slots; ++sl)
+#pragma unroll
+            for (int u = 0; u < V / 32; ++u) acc[u] += x[sl][u];
         }
+#pragma unroll
+        for (int u = 0; u < V / 32; ++u) p.a.y[row * V + lane + 32 * u] = acc[u];
       }
       fence_acq_rel_cluster();
       __syncwarp();
@@ -449,12 +460,11 @@ __global__ void __launch_bounds__(352, 1)
 // ---------------------------------------------------------------------------
 inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-template <int V, int ROWS, bool kY, bool kCk>
-cudaError_t launch_cfg_mode(const FwdArgs& a, int G, int R, cudaStream_t stream) {
+template <int V, int ROWS, int G, bool kY, bool kCk>
+cudaError_t launch_cfg_mode(const FwdArgs& a, int R, cudaStream_t stream) {
   using C = FwdCfg<V, ROWS>;
   TcFwdParams p{};
   p.a = a;
-  p.G = G;
   p.R = R;
   p.NRtot = G * C::NR;
   p.ntiles = (a.T + kS - 1) / kS;
@@ -488,7 +498,7 @@ cudaError_t launch_cfg_mode(const FwdArgs& a, int G, int R, cudaStream_t stream)
       !make_tensor_map_btnx(&mv, a.v, bf, 2, a.B, a.T, a.N, V, V, kS))
     return cudaErrorInvalidValue;
 
-  auto kern = tc_forward_kernel<V, ROWS, kY, kCk>;
+  auto kern = tc_forward_kernel<V, ROWS, G, kY, kCk>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if (R > 8) {
@@ -512,13 +522,13 @@ cudaError_t launch_cfg_mode(const FwdArgs& a, int G, int R, cudaStream_t stream)
   return cudaGetLastError();
 }
 
-template <int V, int ROWS>
-cudaError_t launch_cfg(const FwdArgs& a, int G, int R, cudaStream_t stream) {
+template <int V, int ROWS, int G>
+cudaError_t launch_cfg(const FwdArgs& a, int R, cudaStream_t stream) {
   const bool y = a.y != nullptr, ck = a.ckpt != nullptr;
-  if (y) return ck ? launch_cfg_mode<V, ROWS, true, true>(a, G, R, stream)
-                   : launch_cfg_mode<V, ROWS, true, false>(a, G, R, stream);
-  return ck ? launch_cfg_mode<V, ROWS, false, true>(a, G, R, stream)
-            : launch_cfg_mode<V, ROWS, false, false>(a, G, R, stream);
+  if (y) return ck ? launch_cfg_mode<V, ROWS, G, true, true>(a, R, stream)
+                   : launch_cfg_mode<V, ROWS, G, true, false>(a, R, stream);
+  return ck ? launch_cfg_mode<V, ROWS, G, false, true>(a, R, stream)
+            : launch_cfg_mode<V, ROWS, G, false, false>(a, R, stream);
 }
 
 }  // namespace
@@ -530,12 +540,12 @@ bool tc_forward_supported(int K, int V) {
 }
 
 cudaError_t launch_tc_forward(const FwdArgs& a, cudaStream_t s) {
-  if (a.V == 64) return launch_cfg<64, 8>(a, /*G=*/1, /*R=*/a.K / 16, s);
+  if (a.V == 64) return launch_cfg<64, 8, 1>(a, /*R=*/a.K / 16, s);
   if (a.V == 128) {
     // Two warpgroups ping-pong on the tensor core, each with half the rows.
-    if (a.K == 128) return launch_cfg<128, 64>(a, 2, 1, s);
-    if (a.K == 64) return launch_cfg<128, 32>(a, 2, 1, s);
-    if (a.K == 32) return launch_cfg<128, 16>(a, 2, 1, s);
+    if (a.K == 128) return launch_cfg<128, 64, 2>(a, 1, s);
+    if (a.K == 64) return launch_cfg<128, 32, 2>(a, 1, s);
+    if (a.K == 32) return launch_cfg<128, 16, 2>(a, 1, s);
   }
   return cudaErrorInvalidValue;
 }
