@@ -17,11 +17,14 @@
 // with A = W^T written to tensor memory once (stacked 128/V times to fill
 // M = 128, so the V = 64 case keeps all four TMEM lane quadrants busy), B =
 // fp16(H_{t-1}) rewritten in shared memory every step (W re-encoded as fp16
-// too: see mma_common.cuh), D in TMEM.  TMEM lane L holds value column j = L mod V, so each
-// thread owns a column j and ROWS rows of the state in fp32 registers: the
-// rank-1 add, tanh, gate blend and the readout over its rows are all
-// thread-local.  The fp16 copy of H_t goes back to shared memory as the next
-// MMA's B operand (MN-major: the thread's ROWS values are 16-byte runs).
+// too: see mma_common.cuh), D in TMEM.  For V = 128 the rank-1 write v_t k_t^T
+// is one more K slice of bf16 operands (A column [v_t, 0..], B row k_t: exact
+// products) issued as its own MMA; for V = 64 the epilogue adds it.  TMEM lane
+// L holds value column j = L mod V, so each thread owns a column j and ROWS
+// rows of the state in fp32 registers: tanh, the gate blend and the readout
+// over its rows are all thread-local.  The fp16 copy of H_t goes back to
+// shared memory as the next MMA's B operand (MN-major: the thread's ROWS
+// values are 16-byte runs).
 //
 // Warp roles: warps 0..4G-1 = G epilogue warpgroups; warp 4G = the MMA warp,
 // which issues every group's MMAs from one elected lane of a converged warp,
@@ -56,8 +59,17 @@ struct FwdCfg {
   static constexpr int NR = ROWS * COPIES;      // rows per group = MMA N
   static constexpr int NS = (V == 64) ? 4 : 3;  // input pipeline stages
   static constexpr int KSTEPS = V / 16;         // MMAs per step (K = 16 each)
-  static constexpr uint32_t B_BYTES = NR * V * 2u;
-  static constexpr uint32_t SBO = V * 16u;  // next 8 rows (A) / next 8 columns (B)
+  // V = 128: the rank-1 write runs on the tensor core as one more K slice
+  // (17 % faster on the T = 4096, K = V = 128 workload); at V = 64, with 8
+  // rows per thread, writing the slice costs more than the FMAs it saves
+  // (232 against 312 ns per step on the 16K workload), so it stays in the
+  // epilogue there.
+  static constexpr bool FOLD = (V == 128);
+  // B = [H_{t-1}^T ; X]: V (+ 16) K-rows; the slice X carries the rank-1
+  // write (first row k_t, the rest 0).
+  static constexpr int KB = V + (FOLD ? 16 : 0);
+  static constexpr uint32_t B_BYTES = NR * KB * 2u;
+  static constexpr uint32_t SBO = KB * 16u;  // next 8 columns (B)
   static constexpr uint32_t LBO = 128u;     // next 8 K-elements
   static_assert(ROWS % 8 == 0, "rows per thread come in 16-byte runs");
   static_assert(NR % 16 == 0 && NR <= 256, "MMA N for M = 128");
@@ -68,7 +80,7 @@ struct TcFwdParams {
   int R, NRtot;
   int ntiles;
   uint32_t tmem_cols;
-  uint32_t a_tcol;  // TMEM column of the A operand (W^T stacked)
+  uint32_t a_tcol;  // TMEM column of the A operand (W^T stacked), then (V = 128) G x 8 columns of [v_t, 0]
   uint32_t b_off, stage_off, stage_bytes, q_off, k_off, v_off, f_off;
   uint32_t y_off, bar_off, misc_off;
   uint32_t tx_bytes;
@@ -145,11 +157,13 @@ __global__ void __launch_bounds__((4 * G + 3) * 32, 1)
     tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
     tmem_relinquish();
   }
-  if (p.a.H0 == nullptr) {
+  {
     const uint4 zero = make_uint4(0, 0, 0, 0);
     for (uint32_t e = threadIdx.x * 16; e < static_cast<uint32_t>(G) * C::B_BYTES; e += blockDim.x * 16)
-      *reinterpret_cast<uint4*>(sB + e) = zero;  // H_0 = 0
-  } else if (warp < 4 * G) {
+      *reinterpret_cast<uint4*>(sB + e) = zero;  // H_0 = 0 and the rank-1 slice's zero rows
+  }
+  __syncthreads();
+  if (p.a.H0 != nullptr && warp < 4 * G) {
     // fp16(H_0) as step 0's B operand: each epilogue thread writes the rows
     // and column it owns (the same mapping as below; together they cover
     // every element of each group's tile).
@@ -175,6 +189,8 @@ __global__ void __launch_bounds__((4 * G + 3) * 32, 1)
   const uint32_t tmem_base = *tmem_slot;
   // fp16 operands: W^T re-encoded, H_{t-1} rounded (see mma_common.cuh).
   const uint32_t idesc = idesc_f16_f32(128, C::NR, /*a_mn_major=*/false, /*b_mn_major=*/true);
+  // The rank-1 slice multiplies the bf16 inputs as they are (exact products).
+  const uint32_t idesc_x = idesc_bf16_f32(128, C::NR, /*a_mn_major=*/false, /*b_mn_major=*/true);
   const uint32_t a_tmem = tmem_base + p.a_tcol;
   if (warp < 4) {
     // A = [W^T; W^T; ...] in tensor memory (M = 128 lanes, K = V): lane L holds
@@ -196,6 +212,13 @@ __global__ void __launch_bounds__((4 * G + 3) * 32, 1)
     }
     tmem_st_wait();
   }
+  if (C::FOLD && warp < 4 * G) {
+    // The rank-1 slice of group warp/4's A operand: [v_t, 0, ..., 0] per
+    // lane, 8 columns; all but the first element stay zero.
+    const uint32_t zeros[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    tmem_st_32x32b_x8(a_tmem + (static_cast<uint32_t>(32 * (warp % 4)) << 16) + V / 2 + 8 * (warp / 4), zeros);
+    tmem_st_wait();
+  }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -211,6 +234,21 @@ __global__ void __launch_bounds__((4 * G + 3) * 32, 1)
     const uint32_t hbar = smem_u32(&hready[g]);
     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * wq) << 16) + g * C::NR + c * ROWS;
     uint8_t* bslot = sB + g * C::B_BYTES + ((c * ROWS) / 8) * C::SBO + (j / 8) * C::LBO + (j % 8) * 16;
+    // V = 128: the rank-1 write of step x enters the MMA as one more K slice:
+    // A column [v_x, 0..] in this thread's TMEM lane, B row k_x (the group's
+    // rows, 16-byte runs copied by the first NR/8 threads).  Written once the
+    // group's previous MMA has completed, before the group's arrival.  (A
+    // second slice written while the MMA runs measured slower: 1094 against
+    // 984 ns per step.)
+    const uint32_t xaddr = a_tmem + (static_cast<uint32_t>(32 * wq) << 16) + V / 2 + 8 * g;
+    auto put_x = [&](const uint8_t* stg, int sx) {
+      const uint16_t* vx = reinterpret_cast<const uint16_t*>(stg + p.v_off);
+      const uint16_t* kx = reinterpret_cast<const uint16_t*>(stg + p.k_off);
+      tmem_st_32x32b_x1(xaddr, static_cast<uint32_t>(vx[sx * V + j]));
+      if (L < C::NR / 8)
+        *reinterpret_cast<uint4*>(sB + g * C::B_BYTES + L * C::SBO + V * 16) =
+            *reinterpret_cast<const uint4*>(kx + sx * NRtot + g * C::NR + 8 * L);
+    };
     float h[ROWS];
 #pragma unroll
     for (int r = 0; r < ROWS; ++r)
@@ -238,11 +276,19 @@ __global__ void __launch_bounds__((4 * G + 3) * 32, 1)
       }
       const uint8_t* stage = sStage + st * p.stage_bytes;
       const uint16_t* qs = reinterpret_cast<const uint16_t*>(stage + p.q_off);
-      const uint16_t* ks = reinterpret_cast<const uint16_t*>(stage + p.k_off);
       const uint16_t* vs = reinterpret_cast<const uint16_t*>(stage + p.v_off);
+      const uint16_t* ks = reinterpret_cast<const uint16_t*>(stage + p.k_off);
       const float* fs = reinterpret_cast<const float*>(stage + p.f_off);
       float* yp = sY + ys * (kS * slots * V);
       const int nsteps = min(kS, T - tile * kS);
+      if (C::FOLD && tile == 0) {  // step 0's rank-1 slice (its H_0 part is in place already)
+        put_x(stage, 0);
+        fence_proxy_async_smem();
+        tmem_st_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(hbar);
+      }
       for (int s = 0; s < nsteps; ++s) {
         const int t = tile * kS + s;
         const float vj = bf16_bits_to_f32(vs[s * V + j]);
@@ -261,12 +307,13 @@ __global__ void __launch_bounds__((4 * G + 3) * 32, 1)
 #pragma unroll
         for (int r0 = 0; r0 < ROWS; r0 += 8) {
           float kf[8];
-          unpack8_bf16(*reinterpret_cast<const uint4*>(kr + r0), kf);
+          if (!C::FOLD) unpack8_bf16(*reinterpret_cast<const uint4*>(kr + r0), kf);
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
-            const float x = fmaf(kf[u], vj, __uint_as_float(acc[r0 + u]));  // (H W)_ij + k_i v_j
-            const float z = tanh_fast(x);                                   // Eq. 10
-            h[r0 + u] = fmaf(omf, z - h[r0 + u], h[r0 + u]);                // Eq. 11
+            // (H W)_ij + k_i v_j: from the MMA alone (V = 128), or + the rank-1 term here.
+            const float x = C::FOLD ? __uint_as_float(acc[r0 + u]) : fmaf(kf[u], vj, __uint_as_float(acc[r0 + u]));
+            const float z = tanh_fast(x);                     // Eq. 10
+            h[r0 + u] = fmaf(omf, z - h[r0 + u], h[r0 + u]);  // Eq. 11
           }
           uint4 pk;
           pk.x = pack2_f16(h[r0 + 0], h[r0 + 1]);
@@ -275,9 +322,24 @@ __global__ void __launch_bounds__((4 * G + 3) * 32, 1)
           pk.w = pack2_f16(h[r0 + 6], h[r0 + 7]);
           *reinterpret_cast<uint4*>(bslot + (r0 / 8) * C::SBO) = pk;
         }
-        // Hand fp16(H_t) to the tensor core: make the generic-proxy stores
-        // visible to the async proxy, then one arrival per warp for the MMA warp.
+        // The next step's rank-1 slice (at a tile's end, from the next tile).
+        if (C::FOLD && t + 1 < T) {
+          if (s + 1 < nsteps) {
+            put_x(stage, s + 1);
+          } else {
+            const int tn = tile + 1;
+            if (!mbar_wait(smem_u32(&full[tn % C::NS]), (tn / C::NS) & 1, abort_flag, status, kWhereFwdFull)) {
+              ok = false;
+              break;
+            }
+            put_x(sStage + (tn % C::NS) * p.stage_bytes, 0);
+          }
+        }
+        // Hand the operands to the tensor core: make the generic-proxy stores
+        // visible to the async proxy, complete the tensor-memory store, then
+        // one arrival per warp for the MMA warp.
         fence_proxy_async_smem();
+        if (C::FOLD) tmem_st_wait();
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(hbar);
@@ -322,9 +384,9 @@ __global__ void __launch_bounds__((4 * G + 3) * 32, 1)
     if (!ok) *abort_flag = 1;
   } else if (warp == 4 * G) {
     // ---------------- MMA warp: one converged warp issues every group's MMAs ----------------
-    // Step t of group g needs fp16(H_{t-1}) from that group's epilogue (step
-    // 0 multiplies H_0 = 0); the groups alternate, so one group's MMAs run
-    // while the other group's epilogue uses the special-function units.
+    // Step t of group g needs fp16(H_{t-1}) and the rank-1 slice of step t
+    // from that group's epilogue; the groups alternate, so one group's MMAs
+    // run while the other group's epilogue uses the special-function units.
     // B descriptor of group g, K slice kk: the start-address field (bits 0-13,
     // in 16-byte units) advances by (g * B_BYTES + kk * 2 * LBO) / 16.
     const uint64_t bdesc0 = smem_desc_noswizzle(smem_u32(sB), C::LBO, C::SBO);
@@ -332,7 +394,7 @@ __global__ void __launch_bounds__((4 * G + 3) * 32, 1)
     bool ok = true;
     for (int t = 0; t < T && ok; ++t) {
       for (int g = 0; g < G; ++g) {
-        if (t > 0) {
+        if (C::FOLD || t > 0) {  // (without the fold, step 0 multiplies H_0 alone, in place at the start)
           if (!mbar_wait(smem_u32(&hready[g]), (hph >> g) & 1u, abort_flag, status, kWhereFwdH)) {
             ok = false;
             break;
@@ -342,10 +404,13 @@ __global__ void __launch_bounds__((4 * G + 3) * 32, 1)
         if (elect_one()) {
           tc_fence_after_sync();
           const uint64_t bg = bdesc0 + ((static_cast<uint32_t>(g) * C::B_BYTES) >> 4);
+          if (C::FOLD)  // v_t k_t^T first (it starts the accumulator)
+            tc_mma_f16_ts(tmem_base + g * C::NR, a_tmem + V / 2 + 8 * g, bg + ((C::KSTEPS * 2 * C::LBO) >> 4),
+                          idesc_x, 0u);
 #pragma unroll
           for (int kk = 0; kk < C::KSTEPS; ++kk)
             tc_mma_f16_ts(tmem_base + g * C::NR, a_tmem + kk * 8, bg + ((kk * 2 * C::LBO) >> 4), idesc,
-                          kk > 0 ? 1u : 0u);
+                          (C::FOLD || kk > 0) ? 1u : 0u);
           tc_commit(smem_u32(&dfull[g]));
         }
         __syncwarp();
@@ -471,7 +536,7 @@ cudaError_t launch_cfg_mode(const FwdArgs& a, int R, cudaStream_t stream) {
   // TMEM: D accumulators (G x NR columns) then A = W^T (V/2 columns).
   p.a_tcol = align_up(static_cast<uint32_t>(G * C::NR), 32);
   uint32_t cols = 32;
-  while (cols < p.a_tcol + V / 2) cols *= 2;
+  while (cols < p.a_tcol + V / 2 + (C::FOLD ? 8 * G : 0)) cols *= 2;
   p.tmem_cols = cols;
   p.b_off = 0;
   p.stage_off = align_up(p.b_off + G * C::B_BYTES, 128);
