@@ -86,6 +86,11 @@ struct TcFwdParams {
   uint32_t tx_bytes;
 };
 
+// Store 32 data-path lanes x 32 bits x 1 column (thread i writes lane base + i).
+__device__ __forceinline__ void tmem_st_32x32b_x1(uint32_t taddr, uint32_t r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(r) : "memory");
+}
+
 __device__ __forceinline__ void unpack8_bf16(const uint4 w, float (&o)[8]) {
   o[0] = __uint_as_float(w.x << 16);
   o[1] = __uint_as_float(w.x & 0xFFFF0000u);
