@@ -1,4 +1,7 @@
-// tcgen05 backward scan (placeholder until the tensor-core backward lands).
+// Entry points of a tensor-core backward for V = 128, not built: they report
+// "not supported", so the dispatcher runs the V = 128 backward on the fp32
+// SIMT kernel (simt.cu).  The V = 64 and V = 16 backwards are the warp-MMA
+// kernels (mma_backward.cu, mv_backward.cu).
 #include "internal.h"
 
 namespace m2rnn {
