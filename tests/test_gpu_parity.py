@@ -197,12 +197,31 @@ def test_backward_full_size_sampled_head(n):
     check_grads(sub, ref, "bf16", label=(name, n))
 
 
+@pytest.mark.parametrize("B,N,T,K,V,C,reuse", [
+    (2, 3, 50, 128, 128, 40, True),    # chunks longer than the 16 staged steps, ragged last chunk
+    (1, 2, 37, 16, 128, 7, False),     # one compute warp beside the idle warps of the dW read-back
+    (1, 1, 33, 96, 128, 16, True),     # six compute warps
+    (1, 1, 5, 64, 128, 1, False),      # one-step chunks
+    (8, 16, 24, 128, 128, 16, True),   # the wide-head workload's grid (B=8, 16 heads), short T
+])
+def test_backward_v128_tensor_core(B, N, T, K, V, C, reuse):
+    """The V = 128 backward (warp-MMA chain, tcgen05 dW) against the oracle."""
+    from matrix_state_non_gb300 import binding
+    assert binding.m2rnn_path(K, V, binding.M2RNN_BF16) == 1
+    inp = make_inputs(B, N, T, K, V, "bf16", seed=500 + T + K, with_dy=True)
+    dH = np.random.default_rng(9).standard_normal((B, N, K, V)).astype(np.float32)
+    got = gpu_backward(inp, dH_T=dH, ckpt_every=C, use_fwd_ckpt=reuse)
+    ref = oracle_backward(*oracle_args(inp), inp.exact["dy"], dH.astype(np.float64))
+    check_grads(got, ref, "bf16", label=(B, N, T, K, V, C))
+
+
 def test_backward_is_deterministic():
-    inp = make_inputs(2, 2, 80, 64, 64, "bf16", seed=12, with_dy=True)
-    a = gpu_backward(inp, ckpt_every=16)
-    b = gpu_backward(inp, ckpt_every=16)
-    for name in a:
-        assert np.array_equal(a[name], b[name]), name
+    for V in (64, 128):
+        inp = make_inputs(2, 2, 80, 64, V, "bf16", seed=12, with_dy=True)
+        a = gpu_backward(inp, ckpt_every=16)
+        b = gpu_backward(inp, ckpt_every=16)
+        for name in a:
+            assert np.array_equal(a[name], b[name]), (V, name)
 
 
 # ---------------------------------------------------------------------------

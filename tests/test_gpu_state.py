@@ -159,3 +159,19 @@ def test_backward_state_gradient_clipping(kernel_family, B, N, T, K, V, C):
     assert np.mean(np.abs(full["dH_0"]) > clip) > 0.05  # the clip does bind
     assert np.all(np.abs(got["dH_0"]) <= clip)
     check_grads(got, ref, "bf16", label=(kernel_family, B, N, T, K, V, C))
+
+
+@pytest.mark.parametrize("B,N,T,K,V,C,clip", [(1, 2, 33, 128, 128, 16, 0.3), (1, 1, 40, 32, 128, 12, 0.5)])
+def test_backward_state_gradient_clipping_v128(B, N, T, K, V, C, clip):
+    """The V = 128 tensor-core backward with an initial state and per-step
+    clipping of the state gradient, against the oracle (K = 32 runs two
+    compute warps beside the idle ones that read the dW accumulator back)."""
+    inp = make_inputs(B, N, T, K, V, "bf16", seed=370 + T + V, with_dy=True)
+    H0 = _state(B, N, K, V, seed=7)
+    got = gpu_backward(inp, ckpt_every=C, H_0=H0, want_dH0=True, state_grad_clip=clip)
+    ref = oracle_backward(*oracle_args(inp), inp.exact["dy"], None, H_0=H0.astype(np.float64),
+                          state_grad_clip=clip)
+    full = oracle_backward(*oracle_args(inp), inp.exact["dy"], None, H_0=H0.astype(np.float64))
+    assert np.mean(np.abs(full["dH_0"]) > clip) > 0.05  # the clip does bind
+    assert np.all(np.abs(got["dH_0"]) <= clip)
+    check_grads(got, ref, "bf16", label=(B, N, T, K, V, C))
