@@ -483,6 +483,7 @@ def run_gpu(args, dist):
         fwd_extra["mv_bf16_k64v16@fwd+bwd"] = time_fwdbwd("mv_bf16_k64v16", binding, dev, stream, flush, pk,
                                                           dist)
         fwd_extra["gated_block_bf16_k64"] = time_gated_block(binding, dev, stream, flush, pk, dist)
+        fwd_extra["fwdbwd_bf16_k128"] = time_fwdbwd("fwdbwd_bf16_k128", binding, dev, stream, flush, pk, dist)
     cpu = cpu_baseline_sample() if (dist.rank == 0 and not args.no_cpu) else None
     launches_per_step = 4  # forward scan, backward scan, dv/df row sums, dW/dw_r partial sums
     line = {
@@ -554,17 +555,19 @@ def time_fwdbwd(name, binding, dev, stream, flush, pk, dist, reps=3):
     import torch
     w = WORKLOADS[name]
     C = CKPT_EVERY_MV if w["V"] == 16 else CKPT_EVERY
+    # The Z stash where the shape has one (V = 64, V = 16).
+    stash = binding.m2rnn_z_stash_size(w["B"], w["T"], w["N"], w["K"], w["V"], binding.M2RNN_BF16) > 0
     inp = make_workload(name)
     d = binding.to_device(inp, dev)
-    fo = binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=C, stash=True)
+    fo = binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=C, stash=stash)
     bo = binding.backward(*(d[n] for n in IN_NAMES), d["dy"], ckpt=fo["ckpt"], ckpt_every=C,
-                          z_stash=fo["z_stash"])
+                          z_stash=fo.get("z_stash"))
 
     def step():
-        binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=C, stash=True, out=fo,
+        binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=C, stash=stash, out=fo,
                         workspace=fo["workspace"])
         binding.backward(*(d[n] for n in IN_NAMES), d["dy"], ckpt=fo["ckpt"], ckpt_every=C,
-                         z_stash=fo["z_stash"], out=bo, workspace=bo["workspace"])
+                         z_stash=fo.get("z_stash"), out=bo, workspace=bo["workspace"])
 
     for _ in range(3):
         step()
@@ -585,9 +588,13 @@ def time_fwdbwd(name, binding, dev, stream, flush, pk, dist, reps=3):
     t = dist.max(sum(a.elapsed_time(b) for a, b in ev) / reps)
     fl = fwd_flops(w) + bwd_flops(w)
     t_tensor = fl / (pk["bf16_sustained"] * 1e12)
-    t_hbm = (io_bytes_fwd(w) + io_bytes_bwd(w, ckpt_every=C) + 2 * stash_bytes(w)) / (pk["hbm_gbs"] * 1e9)
+    t_hbm = (io_bytes_fwd(w) + io_bytes_bwd(w, ckpt_every=C) + (2 * stash_bytes(w) if stash else 0)) / \
+        (pk["hbm_gbs"] * 1e9)
     del d, fo, bo
-    return {"workload": w["desc"] + ", Z stash", "kernel": "warp-mma (V = 16 register kernels)", "ms": t,
+    kern = {16: "warp-mma (V = 16 register kernels)", 64: "warp-mma (+ tcgen05 dW)",
+            128: "tcgen05 forward, warp-mma chain + tcgen05 dW backward"}.get(w["V"], "?")
+    return {"workload": w["desc"] + (", Z stash" if stash else "") + f", checkpoints every {C}",
+            "kernel": kern, "ms": t,
             "value": dist.world * units(w) / (t * 1e-3), "unit": UNIT,
             "ns_per_step_per_chain": t * 1e6 / w["T"],
             "roofline_ms": max(t_tensor, t_hbm) * 1e3, "roofline_frac": max(t_tensor, t_hbm) / (t * 1e-3),

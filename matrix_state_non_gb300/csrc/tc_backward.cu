@@ -69,6 +69,12 @@ __device__ __forceinline__ uint32_t cm16_off(int row, int col) {
 
 __device__ __forceinline__ uint32_t f16_to_bf16x2(uint32_t w) { return pack2_bf16(f16lo(w), f16hi(w)); }
 
+// Bring `bytes` (a multiple of 16) at a 16-byte aligned global address into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+               : "memory");
+}
+
 template <bool kClip>
 __global__ void __launch_bounds__(256, 1) tc_backward_kernel(const __grid_constant__ TcBwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -301,15 +307,23 @@ __global__ void __launch_bounds__(256, 1) tc_backward_kernel(const __grid_consta
         const float k1 = bf16_bits_to_f32(ks[s * K + 16 * w + g + 8]);
         const float ft = fs[s], omf = 1.f - ft;
         const uint4* const cst = cache + sl * cstride;
+        // The step's cached Z_t and H_{t-1}, all loads issued before the first
+        // use; the warp's 8 KB of the next step back are brought into L2.
+        uint4 zq[kKT], hq[kKT];
+#pragma unroll
+        for (int kt = 0; kt < kKT; ++kt) {
+          zq[kt] = cst[kt * 32];
+          hq[kt] = cst[(8 + kt) * 32];
+        }
+        if (sl > 0 && lane == 0) prefetch_l2(cst - cstride - lane, 16 * 32 * 16);
         const uint32_t tbh = smem_u32(smem + p.tile_off + bsel * p.tile_bytes + w * 8192), tbd = tbh + 4096;
         float* const dvw = dvp + (bsel * nw + w) * kV;
         uint32_t dA[kKT][4];  // bf16 D_t of the warp's rows (A fragments)
         float pk0 = 0.f, pk1 = 0.f, pf = 0.f;
 #pragma unroll
         for (int kt = 0; kt < kKT; ++kt) {
-          const uint4 zq = cst[kt * 32], hq = cst[(8 + kt) * 32];
-          const uint32_t zw[4] = {zq.x, zq.y, zq.z, zq.w};
-          const uint32_t hw[4] = {hq.x, hq.y, hq.z, hq.w};
+          const uint32_t zw[4] = {zq[kt].x, zq[kt].y, zq[kt].z, zq[kt].w};
+          const uint32_t hw[4] = {hq[kt].x, hq[kt].y, hq[kt].z, hq[kt].w};
           // bf16 H_{t-1} into the dW tile (word positions as in the cache).
           st_shared_b32(tbh + cm16_off(g, 16 * kt + 2 * qd), f16_to_bf16x2(hw[0]));
           st_shared_b32(tbh + cm16_off(g + 8, 16 * kt + 2 * qd), f16_to_bf16x2(hw[1]));

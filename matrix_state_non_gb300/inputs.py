@@ -33,6 +33,10 @@ WORKLOADS = {
                          desc="bf16 long-context forward B=2 heads=16 T=16384 K=64 V=64"),
     "fwdbwd_bf16_k64": dict(B=4, N=8, T=4096, K=64, V=64, dtype="bf16", backward=True, seed=4,
                             desc="bf16 forward+backward B=4 heads=8 T=4096 K=64 V=64"),
+    # The wide-head shape trained: forward + backward at B=8 heads=16 K=V=128
+    # (the forward-only wide-head workload's batch, a quarter of its length).
+    "fwdbwd_bf16_k128": dict(B=8, N=16, T=1024, K=128, V=128, dtype="bf16", backward=True, seed=6,
+                             desc="bf16 wide-head forward+backward B=8 heads=16 T=1024 K=128 V=128"),
     # Multi-value heads (the pages' K = 64, V = 16 per head, one q/k shared by
     # every head) at the forward+backward workload's batch and length.
     "mv_bf16_k64v16": dict(B=4, N=16, T=4096, K=64, V=16, dtype="bf16", backward=True, seed=5,
