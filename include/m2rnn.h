@@ -33,9 +33,10 @@
  *    K a multiple of 16 (and at most 128) run on tensor-core kernels: V = 64
  *    on the warp-MMA scans (the backward for ckpt_every <= 28, its dW on
  *    tcgen05), V = 16 on register-resident warp-MMA scans (the backward for
- *    ckpt_every <= 32, <= 16 with K > 64), V = 128 (forward, K in
- *    {32, 64, 128}) on tcgen05.  Every other supported shape runs on the
- *    fp32 CUDA-core kernels.  Nothing runs on the host CPU.
+ *    ckpt_every <= 32, <= 16 with K > 64), V = 128: the forward (K in
+ *    {32, 64, 128}) on tcgen05, the backward (any ckpt_every) on warp MMAs
+ *    with its dW on tcgen05.  Every other supported shape runs on the fp32
+ *    CUDA-core kernels.  Nothing runs on the host CPU.
  */
 #ifndef M2RNN_H_
 #define M2RNN_H_
