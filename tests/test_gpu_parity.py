@@ -197,21 +197,22 @@ def test_backward_full_size_sampled_head(n):
     check_grads(sub, ref, "bf16", label=(name, n))
 
 
-@pytest.mark.parametrize("B,N,T,K,V,C,reuse", [
-    (2, 3, 50, 128, 128, 40, True),    # chunks longer than the 16 staged steps, ragged last chunk
-    (1, 2, 37, 16, 128, 7, False),     # one compute warp beside the idle warps of the dW read-back
-    (1, 1, 33, 96, 128, 16, True),     # six compute warps
-    (1, 1, 5, 64, 128, 1, False),      # one-step chunks
-    (8, 16, 24, 128, 128, 16, True),   # the wide-head workload's grid (B=8, 16 heads), short T
+@pytest.mark.parametrize("B,N,T,K,V,C,reuse,with_dH", [
+    (2, 3, 50, 128, 128, 40, True, True),    # chunks longer than the 16 staged steps, ragged last chunk
+    (1, 2, 37, 16, 128, 7, False, True),     # one compute warp beside the idle warps of the dW read-back
+    (1, 1, 33, 96, 128, 16, True, False),    # six compute warps, no dH_T
+    (1, 1, 5, 64, 128, 1, False, True),      # one-step chunks
+    (1, 2, 1, 128, 128, 16, False, True),    # a single step
+    (8, 16, 24, 128, 128, 16, True, True),   # the wide-head workload's grid (B=8, 16 heads), short T
 ])
-def test_backward_v128_tensor_core(B, N, T, K, V, C, reuse):
+def test_backward_v128_tensor_core(B, N, T, K, V, C, reuse, with_dH):
     """The V = 128 backward (warp-MMA chain, tcgen05 dW) against the oracle
     (it takes every K % 16 == 0; the forward that writes the checkpoints is
     the tcgen05 kernel for K = 32, 64, 128 and the SIMT kernel otherwise)."""
     inp = make_inputs(B, N, T, K, V, "bf16", seed=500 + T + K, with_dy=True)
-    dH = np.random.default_rng(9).standard_normal((B, N, K, V)).astype(np.float32)
+    dH = np.random.default_rng(9).standard_normal((B, N, K, V)).astype(np.float32) if with_dH else None
     got = gpu_backward(inp, dH_T=dH, ckpt_every=C, use_fwd_ckpt=reuse)
-    ref = oracle_backward(*oracle_args(inp), inp.exact["dy"], dH.astype(np.float64))
+    ref = oracle_backward(*oracle_args(inp), inp.exact["dy"], None if dH is None else dH.astype(np.float64))
     check_grads(got, ref, "bf16", label=(B, N, T, K, V, C))
 
 
