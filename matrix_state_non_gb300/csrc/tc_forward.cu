@@ -298,6 +298,20 @@ __global__ void __launch_bounds__((4 * G + 3) * 32, 1)
         const int t = tile * kS + s;
         const float vj = bf16_bits_to_f32(vs[s * V + j]);
         const float omf = 1.f - fs[s];
+        // V = 64: the rank-1 term k_i v_j of this thread's rows, formed while
+        // the MMA is in flight (the product of two bf16 values is exact, so
+        // adding it later rounds as a fused multiply-add would).
+        float kv[C::FOLD ? 1 : ROWS];
+        if constexpr (!C::FOLD) {
+          const uint16_t* kr = ks + s * NRtot + row_in_cta;
+#pragma unroll
+          for (int r0 = 0; r0 < ROWS; r0 += 8) {
+            float kf[8];
+            unpack8_bf16(*reinterpret_cast<const uint4*>(kr + r0), kf);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) kv[r0 + u] = kf[u] * vj;
+          }
+        }
         if (!mbar_wait(dbar, dphase, abort_flag, status, kWhereFwdD)) {
           ok = false;
           break;
@@ -308,15 +322,13 @@ __global__ void __launch_bounds__((4 * G + 3) * 32, 1)
         tmem_ld_32x32b<ROWS>(taddr, acc);
         tmem_ld_wait();
         tmem_ld_fence_regs(acc);
-        const uint16_t* kr = ks + s * NRtot + row_in_cta;
 #pragma unroll
         for (int r0 = 0; r0 < ROWS; r0 += 8) {
-          float kf[8];
-          if (!C::FOLD) unpack8_bf16(*reinterpret_cast<const uint4*>(kr + r0), kf);
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             // (H W)_ij + k_i v_j: from the MMA alone (V = 128), or + the rank-1 term here.
-            const float x = C::FOLD ? __uint_as_float(acc[r0 + u]) : fmaf(kf[u], vj, __uint_as_float(acc[r0 + u]));
+            float x = __uint_as_float(acc[r0 + u]);
+            if constexpr (!C::FOLD) x += kv[r0 + u];
             const float z = tanh_fast(x);                     // Eq. 10
             h[r0 + u] = fmaf(omf, z - h[r0 + u], h[r0 + u]);  // Eq. 11
           }
