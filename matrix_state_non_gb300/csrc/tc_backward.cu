@@ -25,7 +25,8 @@
 // dW += H_{t-1}^T D_t (M = N = 128, K = 16 per warp) into a tensor-memory
 // accumulator; the tiles are double-buffered behind the MMAs' commit.
 // dk and dq are row sums (shuffles over the four lanes of a row), dv and df
-// are summed over the rows in a fixed order (shuffles, then the warps).
+// are summed over the rows in a fixed order (a reduce-scatter of shuffles for
+// dv, a shuffle tree for df, then over the warps).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -358,17 +359,19 @@ __global__ void __launch_bounds__(256, 1) tc_backward_kernel(const __grid_consta
           st_shared_b32(tbd + cm16_off(g + 8, 16 * kt + 2 * qd), dA[kt][1]);
           st_shared_b32(tbd + cm16_off(g, 16 * kt + 8 + 2 * qd), dA[kt][2]);
           st_shared_b32(tbd + cm16_off(g + 8, 16 * kt + 8 + 2 * qd), dA[kt][3]);
-          // dv shares summed over the warp's rows (lanes 4 apart), fixed tree.
-#pragma unroll
-          for (int o = 4; o < 32; o <<= 1)
-#pragma unroll
-            for (int m = 0; m < 2; ++m) {
-              pv[m][0] += __shfl_xor_sync(0xffffffffu, pv[m][0], o);
-              pv[m][1] += __shfl_xor_sync(0xffffffffu, pv[m][1], o);
-            }
-          if (g == 0) {
-            *reinterpret_cast<float2*>(dvw + 16 * kt + 2 * qd) = make_float2(pv[0][0], pv[0][1]);
-            *reinterpret_cast<float2*>(dvw + 16 * kt + 8 + 2 * qd) = make_float2(pv[1][0], pv[1][1]);
+          // dv shares summed over the warp's rows (the eight lanes g of a
+          // column), reduce-scatter in a fixed order: each exchange halves the
+          // values a lane carries, so lane g ends with the full sum of value
+          // (g >> 1) (column 16kt + 8 (g >> 2) + 2qd + ((g >> 1) & 1)).
+          {
+            const bool hi4 = (g & 4) != 0, hi2 = (g & 2) != 0;
+            float k0 = hi4 ? pv[1][0] : pv[0][0], k1 = hi4 ? pv[1][1] : pv[0][1];
+            k0 += __shfl_xor_sync(0xffffffffu, hi4 ? pv[0][0] : pv[1][0], 16);
+            k1 += __shfl_xor_sync(0xffffffffu, hi4 ? pv[0][1] : pv[1][1], 16);
+            float kk = hi2 ? k1 : k0;
+            kk += __shfl_xor_sync(0xffffffffu, hi2 ? k0 : k1, 8);
+            kk += __shfl_xor_sync(0xffffffffu, kk, 4);
+            if ((g & 1) == 0) dvw[16 * kt + 8 * (g >> 2) + 2 * qd + ((g >> 1) & 1)] = kk;
           }
         }
         // Serial chain: C_{t-1} = f R + D W^T.  B[k = m][n = j] = W[j][m]:
