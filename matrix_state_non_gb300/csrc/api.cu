@@ -60,7 +60,13 @@ int choose_path(int64_t K, int64_t V, int dt) {
     case kPathSimt: return kPathSimt;
     default: break;
   }
-  if (mma) return kPathMma;  // latency-bound small state: ~16 rows per SM
+  // V = 64: both tensor-core forwards hold ~16 state rows per SM and are
+  // bound by the step latency; the tcgen05 step measured ~2 % shorter
+  // (217 vs 222 ns on the T = 16384 workload).  The training forward, which
+  // writes the Z stash in the order the backward reads it, is the warp-MMA
+  // kernel whatever this returns.
+  if (tc && v == 64) return kPathTc;
+  if (mma) return kPathMma;  // V = 16: the register-resident warp-MMA scan
   if (tc) return kPathTc;    // wide heads: tensor throughput matters
   return kPathSimt;
 }

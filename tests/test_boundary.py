@@ -36,9 +36,10 @@ def test_host_helpers(lib):
     assert binding.m2rnn_checkpoint_count(4096, 32) == 127
     assert binding.m2rnn_checkpoint_count(64, 64) == 0
     assert binding.m2rnn_checkpoint_count(0, 4) == -1
-    # kernel families: warp MMA for V=64 bf16, tcgen05 for V=128 bf16, fp32 CUDA cores otherwise
-    assert binding.m2rnn_path(64, 64, binding.M2RNN_BF16) == 2
+    # forward families: tcgen05 for V=64 and V=128 bf16, warp MMA for V=16 bf16, fp32 CUDA cores otherwise
+    assert binding.m2rnn_path(64, 64, binding.M2RNN_BF16) == 1
     assert binding.m2rnn_path(128, 128, binding.M2RNN_BF16) == 1
+    assert binding.m2rnn_path(64, 16, binding.M2RNN_BF16) == 2
     assert binding.m2rnn_path(16, 16, binding.M2RNN_F32) == 0
     assert binding.m2rnn_path(200, 64, binding.M2RNN_BF16) == binding.M2RNN_ERR_UNSUPPORTED
     assert binding.m2rnn_path(64, 64, 7) == binding.M2RNN_ERR_INVALID_ARG

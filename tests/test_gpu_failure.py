@@ -19,9 +19,12 @@ def test_bounded_wait_reports_timeout_and_context_survives(monkeypatch):
     from matrix_state_non_gb300 import binding
     if not torch.cuda.is_available():
         pytest.fail("CUDA GPU required for -m gpu tests")
-    # K = 16 rows: one CTA per chain, no cluster peer left waiting.
+    # K = 16 rows: one CTA per chain, no cluster peer left waiting.  The hook
+    # lives in the warp-MMA forward (its waits use the same bounded helper as
+    # every other kernel's).
     inp = make_inputs(1, 1, 200, 16, 64, "bf16", seed=3)
     d = binding.to_device(inp)
+    monkeypatch.setenv("M2RNN_KERNEL", "mma")
     monkeypatch.setenv("M2RNN_TEST_STALL_TILE", "1")
     out = binding.forward(*(d[n] for n in NAMES))
     st, detail = binding.sync_status(out["workspace"])
