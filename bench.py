@@ -458,8 +458,7 @@ def run_gpu(args, dist):
         for name in FWD_EXTRA:
             fwd_extra[name] = time_forward(name, binding, dev, stream, flush, pk, dist,
                                            reps=max(3, args.steps // 2))
-        # The same long-context workload on the warp-MMA kernel (the one the
-        # training step's forward uses, as it writes the Z stash), for
+        # The same long-context workload on the warp-MMA kernel, for
         # comparison with the tcgen05 kernel the dispatcher picks.
         prev = os.environ.get("M2RNN_KERNEL")
         os.environ["M2RNN_KERNEL"] = "mma"
@@ -506,7 +505,7 @@ def run_gpu(args, dist):
         "gpu_launches": launches_per_step * args.steps,
         "step_breakdown_ms": {"forward": f_avg, "backward": b_avg},
         "forward": fwd_extra,
-        "kernels": {"forward": "warp-mma (the kernel that writes the Z stash)",
+        "kernels": {"forward": "tcgen05 (writes the Z stash)",
                     "backward": "warp-mma chain + tcgen05 dW"},
     }
     return line
@@ -592,7 +591,7 @@ def time_fwdbwd(name, binding, dev, stream, flush, pk, dist, reps=3):
     t_hbm = (io_bytes_fwd(w) + io_bytes_bwd(w, ckpt_every=C) + (2 * stash_bytes(w) if stash else 0)) / \
         (pk["hbm_gbs"] * 1e9)
     del d, fo, bo
-    kern = {16: "warp-mma (V = 16 register kernels)", 64: "warp-mma (+ tcgen05 dW)",
+    kern = {16: "warp-mma (V = 16 register kernels)", 64: "tcgen05 forward, warp-mma chain + tcgen05 dW backward",
             128: "tcgen05 forward, warp-mma chain + tcgen05 dW backward"}.get(w["V"], "?")
     return {"workload": w["desc"] + (", Z stash" if stash else "") + f", checkpoints every {C}",
             "kernel": kern, "ms": t,

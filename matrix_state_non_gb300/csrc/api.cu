@@ -62,9 +62,7 @@ int choose_path(int64_t K, int64_t V, int dt) {
   }
   // V = 64: both tensor-core forwards hold ~16 state rows per SM and are
   // bound by the step latency; the tcgen05 step measured ~2 % shorter
-  // (217 vs 222 ns on the T = 16384 workload).  The training forward, which
-  // writes the Z stash in the order the backward reads it, is the warp-MMA
-  // kernel whatever this returns.
+  // (216 vs 221 ns on the T = 16384 workload).  It also writes the Z stash.
   if (tc && v == 64) return kPathTc;
   if (mma) return kPathMma;  // V = 16: the register-resident warp-MMA scan
   if (tc) return kPathTc;    // wide heads: tensor throughput matters
@@ -133,7 +131,8 @@ BwdLayout bwd_layout(int64_t B, int64_t T, int64_t N, int64_t K, int64_t V, int 
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA; }
 
-// Shapes whose forward can leave Z_t for the backward (the warp-MMA kernels, V = 64 and V = 16).
+// Shapes whose forward can leave Z_t for the backward (the tcgen05 forward at V = 64, the
+// register-resident warp-MMA forward at V = 16).
 bool stash_ok(int64_t K, int64_t V, int dt) {
   return dt == M2RNN_BF16 && (V == 64 || V == 16) && K >= 16 && K <= kMaxDim && K % 16 == 0;
 }
@@ -213,7 +212,7 @@ int forward_impl(const void* q, const void* k, const void* v, const GateIn& gate
   if (z_stash != nullptr) {
     if (!stash_ok(K, V, dtype)) return M2RNN_ERR_UNSUPPORTED;
     if (!aligned16(z_stash)) return M2RNN_ERR_INVALID_ARG;
-    path = kPathMma;  // the kernel that writes the stash
+    path = (V == 64) ? kPathTc : kPathMma;  // the kernels that write the stash: tcgen05 (V = 64), warp MMA (V = 16)
   }
   const void* req[] = {q, k, v, W, w_r, y};
   for (const void* p : req)

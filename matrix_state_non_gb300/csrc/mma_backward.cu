@@ -534,11 +534,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       if (zs) {
-        // Z_t from the stash; the state advances by the gate blend alone.
-        const uint32_t zb = smem_u32(smem + p.zbuf_off) + (w * 32 + lane) * 16;
+        // Z_t from the stash (written by the tcgen05 forward: per step and
+        // row block, Z[8c .. 8c+7][j] as 16 bytes at (c, j)); the state
+        // advances by the gate blend alone.  This thread's pairs: rows g, g+8
+        // (row runs 0, 1) and columns m0, m0+1, m0+8, m0+9 (m0 = 16w + 2qd).
+        const uint16_t* zb = reinterpret_cast<const uint16_t*>(smem + p.zbuf_off) + (16 * w + 2 * qd) * 8 + g;
         for (int s = 0; s < L; ++s) {
           const float omf = 1.f - cf[s];
-          const uint4 zq = ld_shared_v4(zb + s * kZStepBytes);
+          const uint16_t* zs_ = zb + s * (kZStepBytes / 2);
+          auto pair = [&](int run, int dm) {  // {Z[8 run + g][m0 + dm], Z[8 run + g][m0 + dm + 1]}
+            const uint16_t* e = zs_ + (run * kV + dm) * 8;
+            return static_cast<uint32_t>(e[0]) | (static_cast<uint32_t>(e[8]) << 16);
+          };
+          const uint4 zq = make_uint4(pair(0, 0), pair(1, 0), pair(0, 8), pair(1, 8));
           const float z[2][4] = {{f16lo(zq.x), f16hi(zq.x), f16lo(zq.y), f16hi(zq.y)},
                                  {f16lo(zq.z), f16hi(zq.z), f16lo(zq.w), f16hi(zq.w)}};
           // The cache takes Z_s as stashed (already fp16 pairs) and H_{s-1}.

@@ -139,11 +139,12 @@ __device__ __forceinline__ bool f16x2_finite(uint32_t x) {
 // perturbs Z_t by ~2e-3 relative, and the backward chain can amplify that
 // over thousands of steps; fp16 cuts it eightfold at no extra cost.
 
-// The Z stash written by the V = 64 warp-MMA forward for its backward: for
-// each (chain, row block) and step, 2 KB = 4 warps x 32 lanes x 8 fp16, lane
-// order as the accumulator fragments (values Z[g][j], Z[g][j+1], Z[g+8][j],
-// Z[g+8][j+1] for j = 16w + 2qd and then j + 8).  One row block's steps are
-// contiguous, so a chunk of steps is one bulk copy.
+// The Z stash written by the V = 64 tcgen05 forward for the warp-MMA
+// backward: for each (chain, row block of 16 rows) and step, 2 KB = 2 row runs
+// x 64 columns x 8 fp16, the 16 bytes at (run c, column j) holding
+// Z[8c .. 8c+7][j] (the forward's thread for that column and run writes them
+// with one store).  One row block's steps are contiguous, so a chunk of steps
+// is one bulk copy.
 constexpr uint32_t kZStepBytes = 2048;
 
 // Bounded wait without the CTA-wide abort flag: used by the compute warps,

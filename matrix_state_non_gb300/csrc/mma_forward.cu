@@ -57,8 +57,8 @@ struct MmaFwdParams {
 };
 
 // Compile-time modes (a per-step branch costs ~20-30 ns of a ~250 ns step,
-// measured): kY = readout y, kCk = checkpoints, kZ = the Z stash.
-template <int NT, bool kY, bool kCk, bool kZ>
+// measured): kY = readout y, kCk = checkpoints.
+template <int NT, bool kY, bool kCk>
 __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
     mma_forward_kernel(const __grid_constant__ MmaFwdParams p, const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
@@ -175,10 +175,6 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
       store_tiles(abuf0);
     }
     int ck_left = p.a.ckpt_every, ck_idx = 0;  // countdown to the next checkpoint (no division per step)
-    // This thread's 16 bytes of the Z stash at step 0 (advancing 2 KB a step).
-    uint8_t* const zst = !kZ ? nullptr
-                             : reinterpret_cast<uint8_t*>(p.a.zstash) +
-                                   static_cast<int64_t>(chain * R + cta_rank) * T * kZStepBytes + (w * 32 + lane) * 16;
     int ys_prev = 0, s_prev = 0;
     bool have_prev = false;
 
@@ -285,21 +281,15 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
             }
           }
           // Eq. 10-11 on this thread's 8 state values; fp16 H_t to the other tile.
-          float zv[2][4];
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
               const float z = tanh_fast(acc[nt][c]);
-              zv[nt][c] = z;
               h[nt][c] = fmaf(omf, z - h[nt][c], h[nt][c]);
             }
           split();
           store_tiles(abuf0 + ((t + 1) & 1) * 2048);
-          if constexpr (kZ)  // Z_t for the backward, off the chain (a streaming store)
-            st_global_cs_v4(zst + static_cast<int64_t>(t) * kZStepBytes,
-                            make_uint4(pack2_f16(zv[0][0], zv[0][1]), pack2_f16(zv[0][2], zv[0][3]),
-                                       pack2_f16(zv[1][0], zv[1][1]), pack2_f16(zv[1][2], zv[1][3])));
           if (do_y && have_prev && g == 0) {
             float* dst = sY + (ys_prev * kS + s_prev) * kV + jcol0;
 #pragma unroll
@@ -457,7 +447,7 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
 
 inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-template <int NT, bool kY, bool kCk, bool kZ>
+template <int NT, bool kY, bool kCk>
 cudaError_t launch_nt(const FwdArgs& a, cudaStream_t stream) {
   MmaFwdParams p{};
   p.a = a;
@@ -491,7 +481,7 @@ cudaError_t launch_nt(const FwdArgs& a, cudaStream_t stream) {
       !make_tensor_map_btnx(&mk, a.k, bf, 2, a.B, a.T, qN, a.K, kRows, kS) ||
       !make_tensor_map_btnx(&mv, a.v, bf, 2, a.B, a.T, a.N, kV, kV, kS))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(mma_forward_kernel<NT, kY, kCk, kZ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(mma_forward_kernel<NT, kY, kCk>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
@@ -506,7 +496,7 @@ cudaError_t launch_nt(const FwdArgs& a, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, mma_forward_kernel<NT, kY, kCk, kZ>, p, mq, mk, mv);
+  e = cudaLaunchKernelEx(&cfg, mma_forward_kernel<NT, kY, kCk>, p, mq, mk, mv);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -520,13 +510,11 @@ bool mma_forward_supported(int K, int V) {
 
 cudaError_t launch_mma_forward(const FwdArgs& a, cudaStream_t stream) {
   if (a.V != kV) return launch_mv_forward(a, stream);
-  const bool y = a.y != nullptr, ck = a.ckpt != nullptr, z = a.zstash != nullptr;
-  if (z) {
-    if (y) return ck ? launch_nt<2, true, true, true>(a, stream) : launch_nt<2, true, false, true>(a, stream);
-    return ck ? launch_nt<2, false, true, true>(a, stream) : launch_nt<2, false, false, true>(a, stream);
-  }
-  if (y) return ck ? launch_nt<2, true, true, false>(a, stream) : launch_nt<2, true, false, false>(a, stream);
-  return ck ? launch_nt<2, false, true, false>(a, stream) : launch_nt<2, false, false, false>(a, stream);
+  // The V = 64 Z stash is the tcgen05 forward's (its layout is the one the backward reads).
+  if (a.zstash != nullptr) return cudaErrorInvalidValue;
+  const bool y = a.y != nullptr, ck = a.ckpt != nullptr;
+  if (y) return ck ? launch_nt<2, true, true>(a, stream) : launch_nt<2, true, false>(a, stream);
+  return ck ? launch_nt<2, false, true>(a, stream) : launch_nt<2, false, false>(a, stream);
 }
 
 }  // namespace m2rnn

@@ -103,10 +103,10 @@ __device__ __forceinline__ void unpack8_bf16(const uint4 w, float (&o)[8]) {
 }
 
 // Compile-time modes, no per-step test: G epilogue warpgroups, kY = readout
-// y, kCk = checkpoints.  (G as a runtime value left the readout reducer's
+// y, kCk = checkpoints, kZ = the Z stash (V = 64).  (G as a runtime value left the readout reducer's
 // loops unrolled too little to keep up: 5.72 against 4.88 ms on the
 // T = 4096, K = V = 128 workload, measured.)
-template <int V, int ROWS, int G, bool kY, bool kCk>
+template <int V, int ROWS, int G, bool kY, bool kCk, bool kZ>
 __global__ void __launch_bounds__((4 * G + 3) * 32, 1)
     tc_forward_kernel(const __grid_constant__ TcFwdParams p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -263,6 +263,12 @@ __global__ void __launch_bounds__((4 * G + 3) * 32, 1)
     const float wrv = (cta_rank == 0 && g == 0 && c == 0)
                           ? bf16_bits_to_f32(static_cast<const uint16_t*>(p.a.w_r)[static_cast<int64_t>(n) * V + j])
                           : 0.f;
+    // Z stash (V = 64): per (chain, row block) and step 2 KB, thread L's 16
+    // bytes at (row run c, column j): Z[8c .. 8c+7][j] as fp16.
+    static_assert(!kZ || (V == 64 && ROWS == 8 && G == 1), "the Z stash layout is the V = 64 one");
+    uint8_t* const zst = !kZ ? nullptr
+                             : reinterpret_cast<uint8_t*>(p.a.zstash) +
+                                   static_cast<int64_t>(chain * R + cta_rank) * T * kZStepBytes + (c * V + j) * 16;
     uint32_t dphase = 0;
     int ck_left = p.a.ckpt_every, ck_idx = 0;  // countdown to the next checkpoint
     bool ok = true;
@@ -294,93 +300,108 @@ __global__ void __launch_bounds__((4 * G + 3) * 32, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(hbar);
       }
-      for (int s = 0; s < nsteps; ++s) {
-        const int t = tile * kS + s;
-        const float vj = bf16_bits_to_f32(vs[s * V + j]);
-        const float omf = 1.f - fs[s];
-        // V = 64: the rank-1 term k_i v_j of this thread's rows, formed while
-        // the MMA is in flight (the product of two bf16 values is exact, so
-        // adding it later rounds as a fused multiply-add would).
-        float kv[C::FOLD ? 1 : ROWS];
-        if constexpr (!C::FOLD) {
-          const uint16_t* kr = ks + s * NRtot + row_in_cta;
-#pragma unroll
-          for (int r0 = 0; r0 < ROWS; r0 += 8) {
-            float kf[8];
-            unpack8_bf16(*reinterpret_cast<const uint4*>(kr + r0), kf);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) kv[r0 + u] = kf[u] * vj;
-          }
-        }
-        if (!mbar_wait(dbar, dphase, abort_flag, status, kWhereFwdD)) {
-          ok = false;
-          break;
-        }
-        dphase ^= 1u;
-        tc_fence_after_sync();
-        uint32_t acc[ROWS];
-        tmem_ld_32x32b<ROWS>(taddr, acc);
-        tmem_ld_wait();
-        tmem_ld_fence_regs(acc);
-#pragma unroll
-        for (int r0 = 0; r0 < ROWS; r0 += 8) {
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            // (H W)_ij + k_i v_j: from the MMA alone (V = 128), or + the rank-1 term here.
-            float x = __uint_as_float(acc[r0 + u]);
-            if constexpr (!C::FOLD) x += kv[r0 + u];
-            const float z = tanh_fast(x);                     // Eq. 10
-            h[r0 + u] = fmaf(omf, z - h[r0 + u], h[r0 + u]);  // Eq. 11
-          }
-          uint4 pk;
-          pk.x = pack2_f16(h[r0 + 0], h[r0 + 1]);
-          pk.y = pack2_f16(h[r0 + 2], h[r0 + 3]);
-          pk.z = pack2_f16(h[r0 + 4], h[r0 + 5]);
-          pk.w = pack2_f16(h[r0 + 6], h[r0 + 7]);
-          *reinterpret_cast<uint4*>(bslot + (r0 / 8) * C::SBO) = pk;
-        }
-        // The next step's rank-1 slice (at a tile's end, from the next tile).
-        if (C::FOLD && t + 1 < T) {
-          if (s + 1 < nsteps) {
-            put_x(stage, s + 1);
-          } else {
-            const int tn = tile + 1;
-            if (!mbar_wait(smem_u32(&full[tn % C::NS]), (tn / C::NS) & 1, abort_flag, status, kWhereFwdFull)) {
-              ok = false;
-              break;
+      // Steps run in segments that end where a checkpoint is due, so the step
+      // itself carries no checkpoint test (the countdown inside the step cost
+      // ~30 ns of a ~250 ns step, measured).
+      for (int s = 0; s < nsteps && ok;) {
+        const int seg_end = kCk ? min(nsteps, s + ck_left) : nsteps;
+        const int seg_len = seg_end - s;
+        for (; s < seg_end; ++s) {
+          const int t = tile * kS + s;
+          const float vj = bf16_bits_to_f32(vs[s * V + j]);
+          const float omf = 1.f - fs[s];
+          // V = 64: the rank-1 term k_i v_j of this thread's rows, formed while
+          // the MMA is in flight (the product of two bf16 values is exact, so
+          // adding it later rounds as a fused multiply-add would).
+          float kv[C::FOLD ? 1 : ROWS];
+          float zv[kZ ? ROWS : 1];
+          if constexpr (!C::FOLD) {
+            const uint16_t* kr = ks + s * NRtot + row_in_cta;
+  #pragma unroll
+            for (int r0 = 0; r0 < ROWS; r0 += 8) {
+              float kf[8];
+              unpack8_bf16(*reinterpret_cast<const uint4*>(kr + r0), kf);
+  #pragma unroll
+              for (int u = 0; u < 8; ++u) kv[r0 + u] = kf[u] * vj;
             }
-            put_x(sStage + (tn % C::NS) * p.stage_bytes, 0);
           }
-        }
-        // Hand the operands to the tensor core: make the generic-proxy stores
-        // visible to the async proxy, complete the tensor-memory store, then
-        // one arrival per warp for the MMA warp.
-        fence_proxy_async_smem();
-        if (C::FOLD) tmem_st_wait();
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(hbar);
-        // ---- off the serial chain ----
-        if (do_y) {
-          const uint16_t* qr = qs + s * NRtot + row_in_cta;
-          float ya = wrv * vj;  // w_r * v_t, carried by one partial of each column (wrv = 0 elsewhere)
-#pragma unroll
+          if (!mbar_wait(dbar, dphase, abort_flag, status, kWhereFwdD)) {
+            ok = false;
+            break;
+          }
+          dphase ^= 1u;
+          tc_fence_after_sync();
+          uint32_t acc[ROWS];
+          tmem_ld_32x32b<ROWS>(taddr, acc);
+          tmem_ld_wait();
+          tmem_ld_fence_regs(acc);
+  #pragma unroll
           for (int r0 = 0; r0 < ROWS; r0 += 8) {
-            float qf[8];
-            unpack8_bf16(*reinterpret_cast<const uint4*>(qr + r0), qf);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) ya = fmaf(qf[u], h[r0 + u], ya);  // Eq. 12, this thread's rows
+  #pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              // (H W)_ij + k_i v_j: from the MMA alone (V = 128), or + the rank-1 term here.
+              float x = __uint_as_float(acc[r0 + u]);
+              if constexpr (!C::FOLD) x += kv[r0 + u];
+              const float z = tanh_fast(x);                     // Eq. 10
+              if constexpr (kZ) zv[r0 + u] = z;
+              h[r0 + u] = fmaf(omf, z - h[r0 + u], h[r0 + u]);  // Eq. 11
+            }
+            uint4 pk;
+            pk.x = pack2_f16(h[r0 + 0], h[r0 + 1]);
+            pk.y = pack2_f16(h[r0 + 2], h[r0 + 3]);
+            pk.z = pack2_f16(h[r0 + 4], h[r0 + 5]);
+            pk.w = pack2_f16(h[r0 + 6], h[r0 + 7]);
+            *reinterpret_cast<uint4*>(bslot + (r0 / 8) * C::SBO) = pk;
           }
-          yp[(s * slots + g * C::COPIES + c) * V + j] = ya;
+          // The next step's rank-1 slice (at a tile's end, from the next tile).
+          if (C::FOLD && t + 1 < T) {
+            if (s + 1 < nsteps) {
+              put_x(stage, s + 1);
+            } else {
+              const int tn = tile + 1;
+              if (!mbar_wait(smem_u32(&full[tn % C::NS]), (tn / C::NS) & 1, abort_flag, status, kWhereFwdFull)) {
+                ok = false;
+                break;
+              }
+              put_x(sStage + (tn % C::NS) * p.stage_bytes, 0);
+            }
+          }
+          // Hand the operands to the tensor core: make the generic-proxy stores
+          // visible to the async proxy, complete the tensor-memory store, then
+          // one arrival per warp for the MMA warp.
+          fence_proxy_async_smem();
+          if (C::FOLD) tmem_st_wait();
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(hbar);
+          // ---- off the serial chain ----
+          if constexpr (kZ)  // Z_t of the thread's 8 rows for the backward (a streaming store)
+            st_global_cs_v4(zst + static_cast<int64_t>(t) * kZStepBytes,
+                            make_uint4(pack2_f16(zv[0], zv[1]), pack2_f16(zv[2], zv[3]), pack2_f16(zv[4], zv[5]),
+                                       pack2_f16(zv[6], zv[7])));
+          if (do_y) {
+            const uint16_t* qr = qs + s * NRtot + row_in_cta;
+            float ya = wrv * vj;  // w_r * v_t, carried by one partial of each column (wrv = 0 elsewhere)
+  #pragma unroll
+            for (int r0 = 0; r0 < ROWS; r0 += 8) {
+              float qf[8];
+              unpack8_bf16(*reinterpret_cast<const uint4*>(qr + r0), qf);
+  #pragma unroll
+              for (int u = 0; u < 8; ++u) ya = fmaf(qf[u], h[r0 + u], ya);  // Eq. 12, this thread's rows
+            }
+            yp[(s * slots + g * C::COPIES + c) * V + j] = ya;
+          }
         }
+        if (!ok) break;
         if constexpr (kCk) {
-          if (--ck_left == 0) {  // H after step t starts a chunk: checkpoint it
+          ck_left -= seg_len;
+          if (ck_left == 0) {  // H after step tile kS + s - 1 starts a chunk: checkpoint it
             ck_left = p.a.ckpt_every;
             ++ck_idx;
-            if (t + 1 < T) {
+            if (tile * kS + s < T) {
               float* dst =
                   p.a.ckpt + ((static_cast<int64_t>(chain) * p.a.n_ckpt + ck_idx - 1) * p.a.K + row_global) * V + j;
-#pragma unroll
+  #pragma unroll
               for (int r = 0; r < ROWS; ++r) dst[static_cast<int64_t>(r) * V] = h[r];
             }
           }
@@ -542,7 +563,7 @@ __global__ void __launch_bounds__((4 * G + 3) * 32, 1)
 // ---------------------------------------------------------------------------
 inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-template <int V, int ROWS, int G, bool kY, bool kCk>
+template <int V, int ROWS, int G, bool kY, bool kCk, bool kZ>
 cudaError_t launch_cfg_mode(const FwdArgs& a, int R, cudaStream_t stream) {
   using C = FwdCfg<V, ROWS>;
   TcFwdParams p{};
@@ -580,7 +601,7 @@ cudaError_t launch_cfg_mode(const FwdArgs& a, int R, cudaStream_t stream) {
       !make_tensor_map_btnx(&mv, a.v, bf, 2, a.B, a.T, a.N, V, V, kS))
     return cudaErrorInvalidValue;
 
-  auto kern = tc_forward_kernel<V, ROWS, G, kY, kCk>;
+  auto kern = tc_forward_kernel<V, ROWS, G, kY, kCk, kZ>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if (R > 8) {
@@ -607,10 +628,20 @@ cudaError_t launch_cfg_mode(const FwdArgs& a, int R, cudaStream_t stream) {
 template <int V, int ROWS, int G>
 cudaError_t launch_cfg(const FwdArgs& a, int R, cudaStream_t stream) {
   const bool y = a.y != nullptr, ck = a.ckpt != nullptr;
-  if (y) return ck ? launch_cfg_mode<V, ROWS, G, true, true>(a, R, stream)
-                   : launch_cfg_mode<V, ROWS, G, true, false>(a, R, stream);
-  return ck ? launch_cfg_mode<V, ROWS, G, false, true>(a, R, stream)
-            : launch_cfg_mode<V, ROWS, G, false, false>(a, R, stream);
+  if constexpr (V == 64) {  // the Z stash of the training step (V = 64 only)
+    if (a.zstash != nullptr) {
+      if (y) return ck ? launch_cfg_mode<V, ROWS, G, true, true, true>(a, R, stream)
+                       : launch_cfg_mode<V, ROWS, G, true, false, true>(a, R, stream);
+      return ck ? launch_cfg_mode<V, ROWS, G, false, true, true>(a, R, stream)
+                : launch_cfg_mode<V, ROWS, G, false, false, true>(a, R, stream);
+    }
+  } else {
+    if (a.zstash != nullptr) return cudaErrorInvalidValue;
+  }
+  if (y) return ck ? launch_cfg_mode<V, ROWS, G, true, true, false>(a, R, stream)
+                   : launch_cfg_mode<V, ROWS, G, true, false, false>(a, R, stream);
+  return ck ? launch_cfg_mode<V, ROWS, G, false, true, false>(a, R, stream)
+            : launch_cfg_mode<V, ROWS, G, false, false, false>(a, R, stream);
 }
 
 }  // namespace

@@ -72,14 +72,14 @@ def test_stash_shared_qk_and_gate():
         assert r <= TOL_BF16_REL, (name, r)
 
 
-def test_forward_outputs_unchanged_by_the_stash(monkeypatch):
+def test_forward_outputs_unchanged_by_the_stash():
     """The stash leaves the outputs of the kernel that writes it (the
-    warp-MMA forward; forward-only calls default to tcgen05) unchanged."""
+    tcgen05 forward at V = 64) unchanged."""
     import torch
     from matrix_state_non_gb300 import binding
     inp = make_inputs(2, 2, 90, 64, 64, "bf16", seed=614)
     d = binding.to_device(inp)
-    monkeypatch.setenv("M2RNN_KERNEL", "mma")
+    assert binding.m2rnn_path(64, 64, binding.M2RNN_BF16) == 1
     a = binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=14)
     b = binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=14, stash=True)
     torch.cuda.synchronize()
