@@ -31,9 +31,10 @@
  *    m2rnn_sync_status.
  *  - Supported shapes: B, T, N >= 1; K, V in [1, 128].  bf16 inputs with
  *    K a multiple of 16 (and at most 128) run on tensor-core kernels: V = 64
- *    on the warp-MMA scans (the backward for ckpt_every <= 28, its dW on
- *    tcgen05), V = 16 on register-resident warp-MMA scans (the backward for
- *    ckpt_every <= 32, <= 16 with K > 64), V = 128: the forward (K in
+ *    with the forward on tcgen05 and the backward on warp MMAs
+ *    (ckpt_every <= 28, its dW on tcgen05), V = 16 on register-resident
+ *    warp-MMA scans (the backward for ckpt_every <= 32, <= 16 with
+ *    K > 64), V = 128: the forward (K in
  *    {32, 64, 128}) on tcgen05, the backward (any ckpt_every) on warp MMAs
  *    with its dW on tcgen05.  Every other supported shape runs on the fp32
  *    CUDA-core kernels.  Nothing runs on the host CPU.
