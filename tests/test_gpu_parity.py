@@ -227,7 +227,7 @@ def test_backward_is_deterministic():
 
 # ---------------------------------------------------------------------------
 # Every kernel family on the shapes they share (V = 64): the dispatcher picks
-# the warp-MMA kernels; M2RNN_KERNEL selects the others explicitly.
+# the tcgen05 forward; M2RNN_KERNEL selects each family explicitly.
 # ---------------------------------------------------------------------------
 @pytest.fixture
 def kernel_family(request, monkeypatch):
