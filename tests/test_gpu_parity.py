@@ -216,6 +216,23 @@ def test_backward_v128_tensor_core(B, N, T, K, V, C, reuse, with_dH):
     check_grads(got, ref, "bf16", label=(B, N, T, K, V, C))
 
 
+def test_backward_v128_full_size_sampled_head():
+    """The wide-head training workload as the benchmark runs it (B=8, 16
+    heads, T=1024, K=V=128: tcgen05 forward writing checkpoints every 28
+    steps, then the V = 128 backward): one head's gradients over every batch
+    element against the oracle."""
+    name = "fwdbwd_bf16_k128"
+    inp = make_workload(name)
+    n = 5
+    got = gpu_backward(inp, ckpt_every=28, use_fwd_ckpt=True)
+    ref = oracle_backward(*oracle_args(inp, slice(None), slice(n, n + 1)),
+                          inp.exact["dy"][:, :, n:n + 1])
+    sub = {"dq": got["dq"][:, :, n:n + 1], "dk": got["dk"][:, :, n:n + 1],
+           "dv": got["dv"][:, :, n:n + 1], "df": got["df"][:, :, n:n + 1],
+           "dW": got["dW"][n:n + 1], "dw_r": got["dw_r"][n:n + 1]}
+    check_grads(sub, ref, "bf16", label=(name, n))
+
+
 def test_backward_is_deterministic():
     for V in (64, 128):
         inp = make_inputs(2, 2, 80, 64, V, "bf16", seed=12, with_dy=True)
