@@ -333,7 +333,10 @@ int m2rnn_sync_status(void* workspace, void* cuda_stream, uint32_t* detail);
  *
  * sync != 0: synchronise `cuda_stream` and return the device-side status
  * (M2RNN_ERR_TIMEOUT / M2RNN_ERR_DEVICE) of this call; sync == 0: return
- * after queuing the work.
+ * after queuing the work, and read the device-side status later with
+ * m2rnn_backward_noalloc_status -- before the next call on the device, which
+ * clears it.  The array's address is looked up again if the device's
+ * context has been replaced since (e.g. after cudaDeviceReset).
  */
 int m2rnn_backward_noalloc(const void* q, const void* k, const void* v,
                            const void* f, const void* W, const void* w_r,
@@ -344,10 +347,41 @@ int m2rnn_backward_noalloc(const void* q, const void* k, const void* v,
                            int64_t K, int64_t V, m2rnn_dtype dtype, int sync,
                            void* cuda_stream);
 
+/*
+ * Device-side status of the last m2rnn_backward_noalloc call on the current
+ * device (the status block inside the built-in array): synchronises
+ * `cuda_stream` (the stream that call used), then reads and clears the block.
+ * Returns M2RNN_OK, M2RNN_ERR_TIMEOUT (a bounded wait gave up) or
+ * M2RNN_ERR_DEVICE (a failed device-side check); `detail` (may be NULL)
+ * receives the location code of the first device error.  Allocates nothing.
+ */
+int m2rnn_backward_noalloc_status(void* cuda_stream, uint32_t* detail);
+
 /* Which forward kernel family a call with these arguments would run:
  * 2 = warp-MMA tensor-core kernels, 1 = tcgen05 tensor-core kernels,
  * 0 = fp32 CUDA-core kernels, negative = the status the call would return. */
 int m2rnn_path(int64_t K, int64_t V, m2rnn_dtype dtype);
+
+/*
+ * Process-wide switches for tests and measurements (normal use needs
+ * neither).  No counterpart in the paper.
+ *   M2RNN_OPT_KERNEL_FAMILY: the kernel family every later call uses, as
+ *     coded by m2rnn_path: -1 automatic (the default), 0 fp32 CUDA cores,
+ *     1 tcgen05, 2 warp MMA.  A family that cannot run a call's shape falls
+ *     back to the automatic choice for that call.
+ *   M2RNN_OPT_TEST_STALL_TILE: failure-detection test hook.  n >= 0 makes the
+ *     warp-MMA forward's input producer withhold input tile n of chains that
+ *     run on one CTA (K = 16), so that the consumers' bounded waits expire
+ *     and the status block reports M2RNN_ERR_TIMEOUT; -1 (the default) is off.
+ * Initial values come from the environment variables M2RNN_KERNEL (auto |
+ * tcgen05 | mma | simt) and M2RNN_TEST_STALL_TILE, read once, at the first
+ * call that needs them; later changes of the environment have no effect.
+ * `previous` (may be NULL) receives the old value.  Returns M2RNN_OK, or
+ * M2RNN_ERR_INVALID_ARG for an unknown option or an out-of-range value.
+ * Changing a switch while another host thread is inside a call is a race.
+ */
+enum { M2RNN_OPT_KERNEL_FAMILY = 0, M2RNN_OPT_TEST_STALL_TILE = 1 };
+int m2rnn_set_option(int option, int value, int* previous);
 
 #ifdef __cplusplus
 }

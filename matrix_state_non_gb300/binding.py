@@ -9,6 +9,7 @@ there is no CPU path.  Loading fails loudly when the library is missing.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from typing import Optional
@@ -25,6 +26,10 @@ M2RNN_ERR_TIMEOUT = -5
 M2RNN_ERR_DEVICE = -6
 M2RNN_F32 = 0
 M2RNN_BF16 = 1
+M2RNN_OPT_KERNEL_FAMILY = 0
+M2RNN_OPT_TEST_STALL_TILE = 1
+# Kernel family codes (as m2rnn_path returns them); -1 = automatic choice.
+FAMILIES = {"auto": -1, "simt": 0, "tcgen05": 1, "mma": 2}
 
 EXPORTS = (
     "m2rnn_version", "m2rnn_status_string", "m2rnn_checkpoint_count", "m2rnn_path",
@@ -32,7 +37,8 @@ EXPORTS = (
     "m2rnn_backward", "m2rnn_sync_status", "m2rnn_forward_state", "m2rnn_backward_state",
     "m2rnn_decode_step", "m2rnn_backward_state_workspace_size", "m2rnn_forward_gated",
     "m2rnn_backward_gated", "m2rnn_output_norm", "m2rnn_output_norm_backward_workspace_size",
-    "m2rnn_output_norm_backward", "m2rnn_z_stash_size",
+    "m2rnn_output_norm_backward", "m2rnn_z_stash_size", "m2rnn_set_option",
+    "m2rnn_backward_noalloc", "m2rnn_backward_noalloc_status",
 )
 
 _lib = None
@@ -63,6 +69,8 @@ def load() -> ctypes.CDLL:
     lib.m2rnn_checkpoint_count.argtypes = [i64, ci]
     lib.m2rnn_path.restype = ci
     lib.m2rnn_path.argtypes = [i64, i64, ci]
+    lib.m2rnn_set_option.restype = ci
+    lib.m2rnn_set_option.argtypes = [ci, ci, ctypes.POINTER(ci)]
     lib.m2rnn_forward_workspace_size.restype = sz
     lib.m2rnn_forward_workspace_size.argtypes = [i64, i64, i64, i64, i64, ci]
     lib.m2rnn_backward_workspace_size.restype = sz
@@ -118,6 +126,37 @@ def m2rnn_checkpoint_count(T: int, ckpt_every: int) -> int:
 
 def m2rnn_path(K: int, V: int, dtype: int) -> int:
     return load().m2rnn_path(K, V, dtype)
+
+
+def m2rnn_set_option(option: int, value: int):
+    """Returns (status, previous value)."""
+    prev = ctypes.c_int(0)
+    st = load().m2rnn_set_option(option, value, ctypes.byref(prev))
+    return st, prev.value
+
+
+@contextlib.contextmanager
+def kernel_family(name: str):
+    """Run the enclosed calls on one kernel family ("auto", "tcgen05", "mma",
+    "simt"); the previous choice is restored on exit."""
+    st, prev = m2rnn_set_option(M2RNN_OPT_KERNEL_FAMILY, FAMILIES[name])
+    _check(st, "m2rnn_set_option")
+    try:
+        yield
+    finally:
+        m2rnn_set_option(M2RNN_OPT_KERNEL_FAMILY, prev)
+
+
+@contextlib.contextmanager
+def stall_tile_hook(tile: int):
+    """Failure-detection test hook (see include/m2rnn.h): the warp-MMA forward
+    withholds input tile `tile` of single-CTA chains inside the block."""
+    st, prev = m2rnn_set_option(M2RNN_OPT_TEST_STALL_TILE, tile)
+    _check(st, "m2rnn_set_option")
+    try:
+        yield
+    finally:
+        m2rnn_set_option(M2RNN_OPT_TEST_STALL_TILE, prev)
 
 
 def m2rnn_forward_workspace_size(B, T, N, K, V, dtype) -> int:
@@ -456,3 +495,16 @@ def m2rnn_backward_noalloc(q, k, v, f, W, w_r, dy, dH_T, ckpt, ckpt_every, dq, d
         fn.argtypes = [vp] * 9 + [ci] + [vp] * 6 + [i64] * 5 + [ci, ci, vp]
     return fn(q, k, v, f, W, w_r, dy, dH_T, ckpt, ckpt_every, dq, dk, dv, df, dW, dw_r, B, T, N,
               K, V, dtype, sync, stream)
+
+
+def m2rnn_backward_noalloc_status(stream):
+    """Device-side status of the last allocation-free backward on the current
+    device: returns (status, detail); synchronises `stream` first."""
+    lib = load()
+    fn = lib.m2rnn_backward_noalloc_status
+    if fn.argtypes is None:
+        fn.restype = ctypes.c_int
+        fn.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]
+    detail = ctypes.c_uint32(0)
+    st = fn(stream, ctypes.byref(detail))
+    return st, detail.value

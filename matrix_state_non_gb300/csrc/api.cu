@@ -5,8 +5,6 @@
 
 #include <climits>
 #include <cstdint>
-#include <cstdlib>
-#include <cstring>
 
 #include "gate.cuh"
 #include "internal.h"
@@ -34,16 +32,16 @@ bool dtype_ok(int dt) { return dt == M2RNN_F32 || dt == M2RNN_BF16; }
 
 constexpr int kPathSimt = 0, kPathTc = 1, kPathMma = 2;
 
-// Kernel family override for tests and benchmarks: M2RNN_KERNEL = auto |
-// tcgen05 | mma | simt.  A family that does not support the shape falls back
-// to the automatic choice.
+// Kernel family override for tests and benchmarks (m2rnn_set_option; first
+// read from M2RNN_KERNEL = auto | tcgen05 | mma | simt).  A family that does
+// not support the shape falls back to the automatic choice.
 int kernel_override() {
-  const char* e = std::getenv("M2RNN_KERNEL");
-  if (e == nullptr || std::strcmp(e, "auto") == 0) return -1;
-  if (std::strcmp(e, "tcgen05") == 0) return kPathTc;
-  if (std::strcmp(e, "mma") == 0) return kPathMma;
-  if (std::strcmp(e, "simt") == 0) return kPathSimt;
-  return -1;
+  switch (option_kernel_family()) {
+    case 1: return kPathTc;
+    case 2: return kPathMma;
+    case 0: return kPathSimt;
+    default: return -1;
+  }
 }
 
 // Which family runs the forward: 2 = warp-MMA, 1 = tcgen05, 0 = SIMT fp32, <0 = error.
@@ -162,6 +160,8 @@ int64_t m2rnn_checkpoint_count(int64_t T, int ckpt_every) {
 }
 
 int m2rnn_path(int64_t K, int64_t V, m2rnn_dtype dtype) { return choose_path(K, V, dtype); }
+
+int m2rnn_set_option(int option, int value, int* previous) { return set_option(option, value, previous); }
 
 size_t m2rnn_forward_workspace_size(int64_t B, int64_t T, int64_t N, int64_t K, int64_t V,
                                     m2rnn_dtype dtype) {

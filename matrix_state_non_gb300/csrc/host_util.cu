@@ -1,11 +1,16 @@
 // Host-side helpers shared by the kernel launchers: TMA tensor-map encoding
-// through the driver entry point (no link-time dependency on libcuda).
+// through the driver entry point (no link-time dependency on libcuda), and the
+// process-wide switches for tests and measurements.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
+#include "internal.h"
 #include "mma_common.cuh"
 
 namespace m2rnn {
@@ -39,6 +44,57 @@ bool make_tensor_map_btnx(CUtensorMap* m, const void* base, CUtensorMapDataType 
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+namespace {
+// -2 = not yet read from the environment.
+std::atomic<int> g_kernel_family{-2};
+std::atomic<int> g_stall_tile{-2};
+std::once_flag g_env_once;
+
+void read_env_once() {
+  std::call_once(g_env_once, [] {
+    int fam = -1;
+    if (const char* e = std::getenv("M2RNN_KERNEL")) {
+      if (std::strcmp(e, "tcgen05") == 0) fam = 1;
+      else if (std::strcmp(e, "mma") == 0) fam = 2;
+      else if (std::strcmp(e, "simt") == 0) fam = 0;
+    }
+    int stall = -1;
+    if (const char* e = std::getenv("M2RNN_TEST_STALL_TILE")) stall = std::atoi(e);
+    int expect = -2;
+    g_kernel_family.compare_exchange_strong(expect, fam);
+    expect = -2;
+    g_stall_tile.compare_exchange_strong(expect, stall);
+  });
+}
+}  // namespace
+
+int option_kernel_family() {
+  read_env_once();
+  return g_kernel_family.load(std::memory_order_relaxed);
+}
+
+int option_test_stall_tile() {
+  read_env_once();
+  return g_stall_tile.load(std::memory_order_relaxed);
+}
+
+int set_option(int option, int value, int* previous) {
+  read_env_once();
+  if (option == M2RNN_OPT_KERNEL_FAMILY) {
+    if (value < -1 || value > 2) return M2RNN_ERR_INVALID_ARG;
+    const int old = g_kernel_family.exchange(value);
+    if (previous != nullptr) *previous = old;
+    return M2RNN_OK;
+  }
+  if (option == M2RNN_OPT_TEST_STALL_TILE) {
+    if (value < -1) return M2RNN_ERR_INVALID_ARG;
+    const int old = g_stall_tile.exchange(value);
+    if (previous != nullptr) *previous = old;
+    return M2RNN_OK;
+  }
+  return M2RNN_ERR_INVALID_ARG;
 }
 
 }  // namespace m2rnn

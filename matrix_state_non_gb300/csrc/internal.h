@@ -70,6 +70,13 @@ struct BwdArgs {
   int parts;         // dW partials per chain
 };
 
+// Process-wide switches (m2rnn_set_option), first read from the environment
+// variables M2RNN_KERNEL and M2RNN_TEST_STALL_TILE once.  Kernel family: -1
+// automatic, 0 fp32 CUDA cores, 1 tcgen05, 2 warp MMA.  Stall tile: -1 off.
+int option_kernel_family();
+int option_test_stall_tile();
+int set_option(int option, int value, int* previous);
+
 // fp32 CUDA-core kernels (any K, V in [1, 128]).
 cudaError_t launch_simt_forward(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_simt_backward(const BwdArgs& a, cudaStream_t s);

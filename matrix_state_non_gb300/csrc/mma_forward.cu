@@ -454,12 +454,9 @@ cudaError_t launch_nt(const FwdArgs& a, cudaStream_t stream) {
   p.R = a.K / kRows;
   p.ntiles = (a.T + kS - 1) / kS;
   // Test hook for failure detection (single-CTA chains only, so no cluster
-  // peer is left waiting): M2RNN_TEST_STALL_TILE=n makes tile n never arrive;
-  // the consumers' bounded waits expire and the status block reports it.
-  p.stall_tile = -1;
-  if (const char* st = std::getenv("M2RNN_TEST_STALL_TILE")) {
-    if (p.R == 1) p.stall_tile = std::atoi(st);
-  }
+  // peer is left waiting): the stall-tile option n >= 0 makes tile n never
+  // arrive; the consumers' bounded waits expire and the status block reports it.
+  p.stall_tile = p.R == 1 ? option_test_stall_tile() : -1;
   p.abuf_off = 0;
   p.stage_off = 4096;
   p.q_off = 0;

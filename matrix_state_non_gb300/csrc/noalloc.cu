@@ -11,14 +11,18 @@
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library holds it (kStaticScratchBytes) until the process exits.  In host
 // code its name is only a host-side handle, so the device address is looked
-// up with cudaGetSymbolAddress once per device (with that device current) on
-// the first call made on that device, and passed to the kernels.
+// up with cudaGetSymbolAddress (with the device current) on the first call
+// made on a device, and passed to the kernels.  The address is kept per
+// device together with the identity of the context it belongs to; if that
+// context is replaced (cudaDeviceReset, then a new primary context), the next
+// call looks the address up again instead of using a stale one.
 //
 // All calls share the one array and it keeps the previous call's contents:
 // the status block is cleared at the start of each call, everything else is
 // fully overwritten before it is read.  Calls that overlap on the GPU (on
 // different streams, or from different host threads without ordering) race
 // on the array and corrupt each other's results.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -34,22 +38,68 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kStaticScratchBytes];
 
+struct DeviceScratch {
+  void* addr = nullptr;
+  unsigned long long ctx_id = 0;
+};
 std::mutex g_addr_mu;
-void* g_addr[kMaxDevices] = {};
+DeviceScratch g_addr[kMaxDevices];
 
-// Device address of g_noalloc_scratch on the current device (looked up once).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Identity of the current context (0 if the driver cannot tell).
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of g_noalloc_scratch on the current device.
 int scratch_address(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return M2RNN_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return M2RNN_ERR_UNSUPPORTED;
+  // 0 while this thread has no current context yet: then the lookup below
+  // (which makes the device's primary context current) runs.
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(g_addr_mu);
-  if (g_addr[dev] == nullptr) {
+  DeviceScratch& e = g_addr[dev];
+  if (e.addr == nullptr || ctx == 0 || e.ctx_id != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return M2RNN_ERR_CUDA;
-    g_addr[dev] = p;
+    e.addr = p;
+    e.ctx_id = current_context_id();
   }
-  *out = g_addr[dev];
+  *out = e.addr;
   return M2RNN_OK;
+}
+
+// Stream-ordered read (and clear) of the array's status block.
+int read_status(StatusBlock* status, cudaStream_t s, uint32_t* detail) {
+  unsigned int host[2] = {0u, 0u};
+  if (cudaMemcpyAsync(host, status, sizeof(host), cudaMemcpyDeviceToHost, s) != cudaSuccess) return M2RNN_ERR_CUDA;
+  if (cudaMemsetAsync(status, 0, sizeof(host), s) != cudaSuccess) return M2RNN_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return M2RNN_ERR_CUDA;
+  if (detail != nullptr) *detail = host[1];
+  if (host[0] == 0u) return M2RNN_OK;
+  return host[0] == kStatusTimeout ? M2RNN_ERR_TIMEOUT : M2RNN_ERR_DEVICE;
 }
 
 inline size_t round256(size_t x) { return (x + 255) / 256 * 256; }
@@ -110,9 +160,12 @@ extern "C" int m2rnn_backward_noalloc(const void* q, const void* k, const void* 
   if (launch_mma_backward(a, s) != cudaSuccess) return M2RNN_ERR_CUDA;
   if (launch_reduce_partials(a, s) != cudaSuccess) return M2RNN_ERR_CUDA;
   if (!sync) return M2RNN_OK;
-  if (cudaStreamSynchronize(s) != cudaSuccess) return M2RNN_ERR_CUDA;
-  unsigned int host[2] = {0u, 0u};
-  if (cudaMemcpy(host, status, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess) return M2RNN_ERR_CUDA;
-  if (host[0] == 0u) return M2RNN_OK;
-  return host[0] == kStatusTimeout ? M2RNN_ERR_TIMEOUT : M2RNN_ERR_DEVICE;
+  return read_status(status, s, nullptr);
+}
+
+extern "C" int m2rnn_backward_noalloc_status(void* cuda_stream, uint32_t* detail) {
+  void* base = nullptr;
+  const int st = scratch_address(&base);
+  if (st != M2RNN_OK) return st;
+  return read_status(reinterpret_cast<StatusBlock*>(base), static_cast<cudaStream_t>(cuda_stream), detail);
 }

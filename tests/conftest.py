@@ -15,3 +15,12 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def root_dir():
     return ROOT
+
+
+@pytest.fixture
+def kernel_family(request):
+    """Indirect parameter: run the test on one kernel family ("tcgen05",
+    "mma", "simt"); the automatic choice is restored afterwards."""
+    from matrix_state_non_gb300 import binding
+    with binding.kernel_family(request.param):
+        yield request.param

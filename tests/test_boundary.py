@@ -207,10 +207,35 @@ def test_noalloc_backward_rejects_unsupported_shapes_without_a_device(lib):
     assert call(B=4096, N=1024) == binding.M2RNN_ERR_WORKSPACE   # exceeds the built-in scratch
 
 
-def test_kernel_override_env(lib, monkeypatch):
-    monkeypatch.setenv("M2RNN_KERNEL", "tcgen05")
-    assert binding.m2rnn_path(64, 64, binding.M2RNN_BF16) == 1
-    monkeypatch.setenv("M2RNN_KERNEL", "simt")
-    assert binding.m2rnn_path(64, 64, binding.M2RNN_BF16) == 0
-    monkeypatch.setenv("M2RNN_KERNEL", "mma")
-    assert binding.m2rnn_path(128, 128, binding.M2RNN_BF16) == 1  # no warp-MMA kernel for V=128
+def test_kernel_family_option(lib):
+    with binding.kernel_family("tcgen05"):
+        assert binding.m2rnn_path(64, 64, binding.M2RNN_BF16) == 1
+    with binding.kernel_family("simt"):
+        assert binding.m2rnn_path(64, 64, binding.M2RNN_BF16) == 0
+    with binding.kernel_family("mma"):
+        assert binding.m2rnn_path(64, 64, binding.M2RNN_BF16) == 2
+        assert binding.m2rnn_path(128, 128, binding.M2RNN_BF16) == 1  # no warp-MMA kernel for V=128
+    assert binding.m2rnn_path(64, 64, binding.M2RNN_BF16) == 1      # the automatic choice is back
+    st, _ = binding.m2rnn_set_option(binding.M2RNN_OPT_KERNEL_FAMILY, 3)
+    assert st == binding.M2RNN_ERR_INVALID_ARG
+    st, _ = binding.m2rnn_set_option(99, 0)
+    assert st == binding.M2RNN_ERR_INVALID_ARG
+    with binding.stall_tile_hook(4):
+        st, prev = binding.m2rnn_set_option(binding.M2RNN_OPT_TEST_STALL_TILE, 4)
+        assert st == binding.M2RNN_OK and prev == 4
+    st, prev = binding.m2rnn_set_option(binding.M2RNN_OPT_TEST_STALL_TILE, -1)
+    assert st == binding.M2RNN_OK and prev == -1
+
+
+def test_options_start_from_the_environment(root_dir):
+    """The switches take their first values from M2RNN_KERNEL and
+    M2RNN_TEST_STALL_TILE, read once (checked in a fresh process)."""
+    import subprocess
+    import sys
+    code = ("from matrix_state_non_gb300 import binding as b; "
+            "print(b.m2rnn_path(64, 64, b.M2RNN_BF16), b.m2rnn_set_option(b.M2RNN_OPT_TEST_STALL_TILE, -1)[1])")
+    env = dict(os.environ, M2RNN_KERNEL="simt", M2RNN_TEST_STALL_TILE="3")
+    out = subprocess.run([sys.executable, "-c", code], cwd=root_dir, env=env, capture_output=True, text=True,
+                         timeout=120)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.split() == ["0", "3"]

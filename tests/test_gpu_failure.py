@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 NAMES = ("q", "k", "v", "f", "W", "w_r")
 
 
-def test_bounded_wait_reports_timeout_and_context_survives(monkeypatch):
+def test_bounded_wait_reports_timeout_and_context_survives():
     import torch
     from matrix_state_non_gb300 import binding
     if not torch.cuda.is_available():
@@ -24,16 +24,14 @@ def test_bounded_wait_reports_timeout_and_context_survives(monkeypatch):
     # every other kernel's).
     inp = make_inputs(1, 1, 200, 16, 64, "bf16", seed=3)
     d = binding.to_device(inp)
-    monkeypatch.setenv("M2RNN_KERNEL", "mma")
-    monkeypatch.setenv("M2RNN_TEST_STALL_TILE", "1")
-    out = binding.forward(*(d[n] for n in NAMES))
-    st, detail = binding.sync_status(out["workspace"])
+    with binding.kernel_family("mma"), binding.stall_tile_hook(1):
+        out = binding.forward(*(d[n] for n in NAMES))
+        st, detail = binding.sync_status(out["workspace"])
     assert st == binding.M2RNN_ERR_TIMEOUT, binding.status_string(st)
     # The consumers (input tile), the producer (free stage) and the reducer
     # (readout tile) all wait on the withheld tile; whichever gives up first
     # is recorded: any forward-kernel wait site (codes 1xx).
     assert detail // 100 == 1, detail
-    monkeypatch.delenv("M2RNN_TEST_STALL_TILE")
     got = gpu_forward(inp)  # the same context keeps working
     y_ref, H_ref = oracle_forward(*oracle_args(inp))
     check_forward(got, y_ref, H_ref, "bf16")

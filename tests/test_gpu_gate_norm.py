@@ -27,12 +27,6 @@ def _dev(arr):
     return t.cuda().contiguous()
 
 
-@pytest.fixture
-def kernel_family(request, monkeypatch):
-    monkeypatch.setenv("M2RNN_KERNEL", request.param)
-    return request.param
-
-
 def _gated_case(B, N, T, K, V, dtype, seed, shared_qk=False):
     inp = make_inputs(B, N, T, K, V, dtype, seed=seed, with_dy=True)
     gs, ge = make_gate_inputs(B, T, N, dtype, seed=seed + 1)
@@ -147,7 +141,7 @@ def test_gated_full_size_properties():
     the benchmark's gated block runs it (Z stash, 28-step chunks): dbeta is
     the (b, t)-sum of da, and dalpha the (b, t)-sum of da * s / (alpha
     sigmoid(a + beta)), recomputed from the kernel's own da in float64; and
-    one head's gradients against the oracle."""
+    one head's gradients (dq, dk, dv, da, dalpha, dbeta) against the oracle."""
     inp, gs, ge = _gated_case(4, 8, 4096, 64, 64, "bf16", seed=750)
     got = _run_gated(inp, gs, backward=True, ckpt_every=28, stash=True)
     da = got["da"].astype(np.float64)
@@ -164,9 +158,13 @@ def test_gated_full_size_properties():
     f = gate(ge["a"], ge["alpha"], ge["beta"])[:, :, n:n + 1]
     ref = oracle_backward(e["q"][:, :, n:n + 1], e["k"][:, :, n:n + 1], e["v"][:, :, n:n + 1], f, e["W"][n:n + 1],
                           e["w_r"][n:n + 1], e["dy"][:, :, n:n + 1])
-    da_ref, _, _ = gate_backward(ge["a"][:, :, n:n + 1], ge["alpha"][n:n + 1], ge["beta"][n:n + 1], ref["df"])
+    da_ref, dalpha_ref, dbeta_ref = gate_backward(ge["a"][:, :, n:n + 1], ge["alpha"][n:n + 1],
+                                                  ge["beta"][n:n + 1], ref["df"])
     for name, r in (("dq", ref["dq"]), ("dk", ref["dk"]), ("dv", ref["dv"]), ("da", da_ref)):
         assert rel_fro(got[name][:, :, n:n + 1], r) <= TOL_BF16_REL, (name, rel_fro(got[name][:, :, n:n + 1], r))
+    # The head's gate-parameter gradients (sums over every b and t) against the oracle's.
+    for name, r in (("dalpha", dalpha_ref), ("dbeta", dbeta_ref)):
+        assert rel_fro(got[name][n:n + 1], r) <= TOL_BF16_REL, (name, rel_fro(got[name][n:n + 1], r))
 
 
 # ---------------------------------------------------------------------------

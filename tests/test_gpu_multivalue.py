@@ -27,12 +27,6 @@ def shared_inputs(B, N, T, K, V, dtype, seed, with_dy=False):
     return out
 
 
-@pytest.fixture
-def kernel_family(request, monkeypatch):
-    monkeypatch.setenv("M2RNN_KERNEL", request.param)
-    return request.param
-
-
 @pytest.mark.parametrize("kernel_family", ["mma", "tcgen05", "simt"], indirect=True)
 @pytest.mark.parametrize("B,N,T,K,V", [(2, 4, 37, 64, 64), (1, 3, 50, 32, 64)])
 def test_forward_shared_qk(kernel_family, B, N, T, K, V):

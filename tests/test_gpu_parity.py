@@ -246,12 +246,6 @@ def test_backward_is_deterministic():
 # Every kernel family on the shapes they share (V = 64): the dispatcher picks
 # the tcgen05 forward; M2RNN_KERNEL selects each family explicitly.
 # ---------------------------------------------------------------------------
-@pytest.fixture
-def kernel_family(request, monkeypatch):
-    monkeypatch.setenv("M2RNN_KERNEL", request.param)
-    return request.param
-
-
 @pytest.mark.parametrize("kernel_family", ["mma", "tcgen05", "simt"], indirect=True)
 @pytest.mark.parametrize("B,N,T,K,V", [(2, 3, 37, 64, 64), (1, 2, 70, 16, 64), (1, 1, 97, 128, 64),
                                        (2, 1, 33, 48, 64), (1, 1, 1, 64, 64)])

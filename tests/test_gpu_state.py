@@ -23,12 +23,6 @@ def _state(B, N, K, V, seed):
     return np.random.default_rng(seed).uniform(-0.9, 0.9, (B, N, K, V)).astype(np.float32)
 
 
-@pytest.fixture
-def kernel_family(request, monkeypatch):
-    monkeypatch.setenv("M2RNN_KERNEL", request.param)
-    return request.param
-
-
 @pytest.mark.parametrize("kernel_family", ["mma", "tcgen05", "simt"], indirect=True)
 @pytest.mark.parametrize("B,N,T,K,V", [(2, 3, 37, 64, 64), (1, 1, 1, 64, 64), (1, 2, 70, 32, 64)])
 def test_forward_from_initial_state(kernel_family, B, N, T, K, V):
