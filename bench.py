@@ -49,7 +49,7 @@ MAIN = "fwdbwd_bf16_k64"
 FWD_EXTRA = ("fwd_bf16_k64", "fwd_bf16_k128", "fwd_bf16_16k", "mv_bf16_k64v16")
 IN_NAMES = ("q", "k", "v", "f", "W", "w_r")
 GRADS = ("dq", "dk", "dv", "df", "dW", "dw_r")
-CKPT_EVERY = 28  # chunk length of the backward rebuild (two 28-step chunk caches fit in TMEM)
+CKPT_EVERY = 20  # chunk length of the V = 64 backward rebuild (its longest: shared-memory bound)
 CKPT_EVERY_MV = 32  # the V = 16 backward's longest chunk (fewest chunk hand-offs)
 FLUSH_BYTES = 256 << 20  # larger than the 129 MB L2
 

@@ -32,7 +32,7 @@
  *  - Supported shapes: B, T, N >= 1; K, V in [1, 128].  bf16 inputs with
  *    K a multiple of 16 (and at most 128) run on tensor-core kernels: V = 64
  *    with the forward on tcgen05 and the backward on warp MMAs
- *    (ckpt_every <= 28, its dW on tcgen05), V = 16 on register-resident
+ *    (ckpt_every <= 20, its dW and its dk, dv on tensor cores), V = 16 on register-resident
  *    warp-MMA scans (the backward for ckpt_every <= 32, <= 16 with
  *    K > 64), V = 128: the forward (K in
  *    {32, 64, 128}) on tcgen05, the backward (any ckpt_every) on warp MMAs
@@ -190,7 +190,7 @@ size_t m2rnn_backward_state_workspace_size(int64_t B, int64_t T, int64_t N,
  * piece before it.  `ckpt`, if given, must come from m2rnn_forward_state
  * with the same H_0.  z_stash (may be NULL): the stash that same forward
  * call wrote, with its `ckpt` (required when T > ckpt_every), ckpt_every
- * <= 28 (V = 64) or within the V = 16 backward's chunk limit (32, or 16 for
+ * <= 20 (V = 64) or within the V = 16 backward's chunk limit (32, or 16 for
  * K > 64); Z_t then comes from the stash in fp16 instead of a rerun.
  * workspace: m2rnn_backward_state_workspace_size bytes.
  */
@@ -319,7 +319,7 @@ int m2rnn_sync_status(void* workspace, void* cuda_stream, uint32_t* detail);
  * inputs and outputs.
  *
  * Limits: bf16 inputs, V = 64, K a multiple of 16 (<= 128), 1 <= ckpt_every
- * <= 28, and `ckpt` (the forward's checkpoints for this ckpt_every) is
+ * <= 20, and `ckpt` (the forward's checkpoints for this ckpt_every) is
  * required whenever T > ckpt_every.  A problem whose scratch would exceed the
  * built-in 32 MiB returns M2RNN_ERR_WORKSPACE; other shapes return
  * M2RNN_ERR_UNSUPPORTED.  Nothing is allocated, on the host or the device.

@@ -13,32 +13,43 @@
 // Work split as in the forward: a chain's K rows in blocks of 16, one CTA per
 // block (rows never mix; only dv_t, df_t, dW and dw_r sum over rows, and
 // those are written as row-block partials and summed afterwards in a fixed
-// order).  The time axis runs over chunks of C <= 28 steps, last chunk first;
-// for each chunk the forward is rerun from its checkpoint (section 2.6 of the
-// notes describes the paper's rerun-and-cache backward; here only one or two
-// chunks are cached) and then walked backwards.  Three warpgroups:
-//   reverse warps   (each owning 16 value columns) the serial chain only:
-//                   R -> D -> bf16(D) tile -> one named barrier -> 8 warp MMAs
-//                   seeded with f R -> C_{t-1}; then their shares of dk, dv,
-//                   df and the bf16 D and H_{t-1} tiles go to the gradient
-//                   warps through a ring of shared-memory slots;
-//   recompute warps (each owning 16 value columns) the forward rerun of the
-//                   next chunk (Eq. 10-11), caching each thread's Z_t and
-//                   H_{t-1} values (fp32) in its own lane of tensor memory, so
-//                   the cache never touches DRAM; also dq_t = H_t u_t and the
-//                   chunk loads (TMA).  When the forward left its Z_t in a
-//                   stash (fp16), the rerun is only H_t = H_{t-1} + (1-f_t)
-//                   (Z_t - H_{t-1}) from the chunk's checkpoint, with Z_t
-//                   bulk-copied a chunk at a time: no MMA, no tanh, no
-//                   exchange between the warps;
+// order).  The time axis runs over chunks of C <= 20 steps, last chunk first;
+// for each chunk the forward is rebuilt from its checkpoint (section 2.6 of
+// the notes describes the paper's rerun-and-cache backward; here only two
+// chunks are cached, on chip) and then walked backwards.  Three warpgroups:
+//   reverse warps   (each owning 16 value columns) the serial chain:
+//                   R -> D = R * G -> bf16(D) tile -> one named barrier -> 8
+//                   warp MMAs seeded with f R -> C_{t-1}; besides it only the
+//                   df share <R, E>, handed to the gradient warps with the D
+//                   tile through a ring of shared-memory slots;
+//   recompute warps (each owning 16 value columns) the rebuild of the next
+//                   chunk: Eq. 10-11 rerun, or, when the forward left its Z_t
+//                   in a stash (fp16), only H_t = H_{t-1} + (1-f_t)(Z_t -
+//                   H_{t-1}) from the chunk's checkpoint with Z_t bulk-copied
+//                   a chunk at a time.  Per step and thread they cache in
+//                   their own tensor-memory lanes what the reverse walk needs,
+//                   G = (1-f)(1-Z^2) and E = H_{t-1} - Z (fp16), and write
+//                   bf16 H_{t-1} tiles for the dW MMA into a chunk buffer in
+//                   shared memory; they also form dq_t = H_t u_t (per-thread
+//                   shares summed at the chunk's end) and issue the chunk
+//                   loads (TMA);
 //   gradient warps  dW += H_{t-1}^T D_t as one tcgen05 MMA per step into a
-//                   tensor-memory accumulator, and the fixed-order sums of
-//                   the dk, dv, df shares and dw_r.
+//                   tensor-memory accumulator; every fourth step each warp
+//                   forms dk_t = D_t v_t and the row block's D_t^T k_t as
+//                   warp MMAs on the step's bf16 D tile (ldmatrix, plain and
+//                   transposed), sums the df shares, and adds dw_r.
 // Warp w of each warpgroup runs on scheduler w, so the three interleave.  The
-// chunk caches hold each thread's Z_t and H_{t-1} as fp16 pairs, 8 TMEM
-// columns per step; with the 64-column dW accumulator two caches of up to 28
-// steps fit, and the rebuild of chunk c-1 overlaps the reverse walk of chunk
-// c.
+// elementwise work is in packed fp32x2 arithmetic.  Two chunk caches (8
+// tensor-memory columns per step) and two H tile buffers let the rebuild of
+// chunk c-1 overlap the reverse walk of chunk c.  Shared memory is what
+// bounds the chunk length (20 steps).
+//
+// Measured (timing-only copies, B=4 N=8 T=4096): the proxy fence before the
+// reverse warps' hand-off cost 7.5 % of the kernel while it had the H tile and
+// df stores of the same step to drain; with the H tiles written by the
+// recompute warps, and the fence placed after the chain MMAs (the D tile
+// stores completed before the barrier) and before the df store (read only by
+// the generic proxy), it has nothing left to wait for.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -54,29 +65,31 @@ namespace {
 constexpr int kV = 64;
 constexpr int kRows = 16;
 constexpr int kThreads = 384;     // reverse warps 0-3, recompute warps 4-7, gradient warps 8-11
-// Tensor memory: columns [0, 448) hold two chunk caches (8 columns per step:
-// Z_t and H_{t-1} as fp16 pairs), columns [448, 512) the dW accumulator.
+// Tensor memory: columns [0, 320) hold two chunk caches, columns [448, 512)
+// the dW accumulator.  Per step and thread, 8 columns: G = (1-f)(1-Z^2) as
+// four fp16 pairs, then E = H_{t-1} - Z as four fp16 pairs, each in the order
+// (column block 0, row g), (0, g+8), (1, g), (1, g+8).
 constexpr int kDWCol = 448;
 constexpr int kCacheCols = 8;
-constexpr int kMaxChunk = kDWCol / (2 * kCacheCols);  // 28: two caches, the recompute runs a chunk ahead
+constexpr int kMaxChunk = 20;  // bounded by shared memory (the H tile and Z stash chunk buffers)
+static_assert(2 * kMaxChunk * kCacheCols <= kDWCol, "chunk caches overlap the dW accumulator");
 constexpr int kCBufs = 4;         // chunk input buffers (reverse, gradient, recompute, loading)
 constexpr int kNX = 8;            // exchange ring slots, reverse -> gradient warps
 // Exchange slot (reverse -> gradient warps), one per time step:
-//   Dt  bf16 D tile: A operand of the reverse warps' chain MMAs (ldmatrix) and
-//       B operand of the dW MMA (tcgen05)
-//   Ht  bf16 H_{t-1} tile, followed by 2 KB of zeros: A operand of the dW MMA,
-//       H_{t-1}^T padded from 64 to 128 rows
-//   Dv  per-thread sums of D k over the thread's two rows: [g][64 columns], rows padded to 72 floats
-//   Dk  per-thread sums of D v over the thread's four columns: [warp][qd][g][row g, g+8], groups padded to 18
-//   Df  per-thread sums of R (H_{t-1} - Z) over the thread's eight values: [128]
-// (strides chosen so that both the writers' and the readers' accesses are free of bank conflicts).
+//   Dt  bf16 D tile: A operand of the reverse warps' chain MMAs (ldmatrix),
+//       B operand of the dW MMA (tcgen05), and the operand of the gradient
+//       warps' dk and dv MMAs (ldmatrix, plain and transposed)
+//   Df  per-thread shares of df = <R, H_{t-1} - Z> over the thread's eight values: [128]
+// The H tile buffer holds, per chunk and step, the bf16 H_{t-1} tile: the A
+// operand of the dW MMA, H_{t-1}^T, whose M = 128 rows run 2 KB past the tile
+// (rows 64..127 of the accumulator take whatever follows and are never read;
+// 2 KB of slack after the buffers keep those reads inside the allocation).
 // Both bf16 tiles use the canonical no-swizzle core-matrix layout: the 8 x 8
 // block (rows 8i.., columns 8j..) is 128 contiguous bytes at 256 j + 128 i, so
 // as tcgen05 operands (MN-major, the columns contiguous) the core matrices
 // advance by 128 bytes along K (the 16 rows) and 256 bytes along M / N.
-constexpr int kDvStride = 72, kDkGroup = 18;
-constexpr uint32_t kXDt = 0, kXHt = 2048, kXZero = 4096, kXDv = 6144, kXDk = kXDv + 8 * kDvStride * 4,
-                   kXDf = kXDk + 16 * kDkGroup * 4, kXSlotBytes = 10240;
+constexpr uint32_t kXDt = 0, kXDf = 2048, kXSlotBytes = 2560;
+constexpr uint32_t kHTileBytes = 2048;
 static_assert(kXDf + 128 * 4 <= kXSlotBytes, "exchange slot overflow");
 
 __device__ __forceinline__ uint32_t cm_off(int row, int col) {
@@ -88,6 +101,15 @@ __device__ __forceinline__ uint32_t cm_ldsm_a(uint32_t tile, int kt, int lane) {
   const int mi = lane >> 3;
   return tile + cm_off((lane & 7) + (mi & 1) * 8, 16 * kt + (mi >> 1) * 8);
 }
+// ldmatrix.x4.trans address for the A fragments of the transposed tile (rows =
+// tile columns 16mt..16mt+15, k = the 16 tile rows): matrices (tile rows 0-7 |
+// 8-15) x (columns 16mt.. | 16mt+8..), the column block varying fastest.
+__device__ __forceinline__ uint32_t cm_ldsm_at(uint32_t tile, int mt, int lane) {
+  const int mi = lane >> 3;
+  return tile + cm_off((lane & 7) + (mi >> 1) * 8, 16 * mt + (mi & 1) * 8);
+}
+
+__device__ __forceinline__ float2 splat2(float x) { return make_float2(x, x); }
 
 struct MmaBwdParams {
   BwdArgs a;
@@ -95,11 +117,40 @@ struct MmaBwdParams {
   int nchunks;
   int nbuf;  // TMEM cache buffers (2)
   uint32_t htile_off, cbuf_off, cbuf_bytes, cq_off, ck_off, cv_off, cdy_off, cf_off;
-  uint32_t xring_off, dqp_off, dwr_off, bar_off, misc_off, zbuf_off;
+  uint32_t xring_off, dqp_off, dwr_off, bar_off, misc_off, zbuf_off, hbuf_off;
   uint32_t tx_bytes;
   float* dvp;  // [B*T*N][R][V]: row-block partials of D^T k
   float* dfp;  // [B*T*N][R]:    row-block partials of df
 };
+
+// One rebuilt step for the reverse walk: from Z_s (fp32 pairs z), H_{s-1}
+// (fp32 pairs h, advanced in place to H_s) and 1 - f_s, the 8 cache words of
+// this thread and its four bf16 H_{s-1} pairs for the dW tile.  Pairs are
+// indexed [column block nt][row half: 0 = g, 1 = g + 8].
+__device__ __forceinline__ void rebuild_step(const float2 (&z)[2][2], float2 (&h)[2][2], float omf,
+                                             uint32_t (&cache)[kCacheCols], uint32_t (&hb)[4]) {
+  const float2 omf2 = splat2(omf), nomf2 = splat2(-omf), neg1 = splat2(-1.f);
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const float2 zz = __fmul2_rn(z[nt][hh], z[nt][hh]);
+      const float2 G = __ffma2_rn(nomf2, zz, omf2);                 // (1-f)(1 - Z^2)
+      const float2 E = __ffma2_rn(z[nt][hh], neg1, h[nt][hh]);      // H_{s-1} - Z_s
+      cache[2 * nt + hh] = pack2_f16(G.x, G.y);
+      cache[4 + 2 * nt + hh] = pack2_f16(E.x, E.y);
+      hb[2 * nt + hh] = pack_bf16x2(h[nt][hh].x, h[nt][hh].y);
+      h[nt][hh] = __ffma2_rn(nomf2, E, h[nt][hh]);                  // H_s = H_{s-1} + (1-f)(Z_s - H_{s-1})
+    }
+}
+
+__device__ __forceinline__ void tmem_st_cache(uint32_t taddr, const uint32_t (&c)[kCacheCols]) {
+  tmem_st_32x32b_x8(taddr, c);
+}
+
+__device__ __forceinline__ void tmem_ld_cache(uint32_t taddr, uint32_t (&c)[kCacheCols]) {
+  tmem_ld_32x32b<8>(taddr, c);
+}
 
 // kClip: the state-gradient clamp, a compile-time switch (a per-step branch
 // on it cost ~7% of the kernel, measured).
@@ -127,6 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* xempty = xfull + kNX;
   uint64_t* dwdone = xempty + kNX;
   uint64_t* zfull = dwdone + 1;  // [2]: Z stash chunk buffers
+  uint64_t* hfree = zfull + 2;   // [2]: every dW MMA reading an H tile buffer is complete
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.misc_off);
   volatile int* vabort = reinterpret_cast<volatile int*>(smem + p.misc_off + 4);
   volatile int* rabort = reinterpret_cast<volatile int*>(smem + p.misc_off + 8);
@@ -150,6 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(smem_u32(dwdone), 1);          // every dW MMA complete
     for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&zfull[i]), 1);  // the loading lane (+ bulk bytes)
+    for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&hfree[i]), 1);  // the dW MMAs' commit
     *abort_flag = 0;
     *vabort = 0;
     *rabort = 0;
@@ -160,24 +213,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
-  // The zero halves of the dW MMA's A operand, written once.
-  for (uint32_t i = threadIdx.x; i < kNX * 128u; i += kThreads) {
-    const uint32_t slot = i >> 7, part = i & 127u;
-    *reinterpret_cast<uint4*>(smem + p.xring_off + slot * kXSlotBytes + kXZero + part * 16) =
-        make_uint4(0u, 0u, 0u, 0u);
-  }
-  fence_proxy_async_smem();
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
 
-  // Warp w of every warpgroup owns value columns 16w..16w+15 (thread columns
-  // jcol0 + 8nt + {0,1}, rows g and g+8 of the CTA's block).  Reverse warp w
-  // and recompute warp w + 4 share TMEM lanes 32w.. and the same fragment
-  // positions, so each reverse thread reads exactly what its recompute
-  // partner cached: buffer tb, slot s = columns 16 (C tb + s) .. + 15 holding
-  // {Z_s (8 values), H_{s-1} (8 values)}.
+  // Warp w of the reverse and recompute warpgroups owns value columns
+  // 16w..16w+15 (thread columns jcol0 + 8nt + {0,1}, rows g and g+8 of the
+  // CTA's block).  Reverse warp w and recompute warp w + 4 share TMEM lanes
+  // 32w.. and the same fragment positions, so each reverse thread reads
+  // exactly what its recompute partner cached: buffer tb, slot s = columns
+  // 12 (C tb + s) .. + 11.
   const int w = warp & 3;
   const int g = lane >> 2, qd = lane & 3;
   const int ctid = threadIdx.x & 127;
@@ -186,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint16_t* Wg = static_cast<const uint16_t*>(A.W) + static_cast<int64_t>(n) * kV * kV;
   const uint32_t tcache = tmem_base + (static_cast<uint32_t>(32 * w) << 16);
   const uint32_t xring0 = smem_u32(smem + p.xring_off);
+  const uint32_t hbuf0 = smem_u32(smem + p.hbuf_off);  // two buffers of C H tiles
 
   if (warp < 4) {
     // ======================= reverse warps =======================
@@ -203,17 +250,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         bt[nt][i][1] = *reinterpret_cast<const uint32_t*>(Wg + col * kV + k0 + 8);
       }
     }
-    // State gradient C (C-fragment layout), initialised with dH_T.
-    float Cg[2][4];
+    // State gradient C as pairs [column block nt][row half], initialised with dH_T.
+    float2 Cg[2][2];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       if (A.dH_T != nullptr) {
         const float* src = A.dH_T + (static_cast<int64_t>(chain) * A.K + row_g) * kV + jcol0 + 8 * nt;
-        const float2 x0 = *reinterpret_cast<const float2*>(src);
-        const float2 x1 = *reinterpret_cast<const float2*>(src + 8 * kV);
-        Cg[nt][0] = x0.x; Cg[nt][1] = x0.y; Cg[nt][2] = x1.x; Cg[nt][3] = x1.y;
+        Cg[nt][0] = *reinterpret_cast<const float2*>(src);
+        Cg[nt][1] = *reinterpret_cast<const float2*>(src + 8 * kV);
       } else {
-        Cg[nt][0] = Cg[nt][1] = Cg[nt][2] = Cg[nt][3] = 0.f;
+        Cg[nt][0] = Cg[nt][1] = make_float2(0.f, 0.f);
       }
     }
     bool ok = true;
@@ -235,17 +281,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      const uint8_t* cbuf = smem + p.cbuf_off + cb * p.cbuf_bytes;
-      const uint16_t* cq = reinterpret_cast<const uint16_t*>(cbuf + p.cq_off);
-      const uint16_t* ck = reinterpret_cast<const uint16_t*>(cbuf + p.ck_off);
-      const uint16_t* cv = reinterpret_cast<const uint16_t*>(cbuf + p.cv_off);
-      const float* cdy = reinterpret_cast<const float*>(cbuf + p.cdy_off);
-      const float* cf = reinterpret_cast<const float*>(cbuf + p.cf_off);
+      const uint32_t cbuf = smem_u32(smem + p.cbuf_off + cb * p.cbuf_bytes);
+      const uint32_t sq = cbuf + p.cq_off, sdy = cbuf + p.cdy_off, sf = cbuf + p.cf_off;
       const uint32_t tbuf = tcache + kCacheCols * CL * tb;
       // The next slot's TMEM load is issued one step ahead and waited for at
       // the top of the step.
-      uint32_t slot_regs[kCacheCols];
-      tmem_ld_32x32b<kCacheCols>(tbuf + kCacheCols * (L - 1), slot_regs);
+      uint32_t sr[kCacheCols];
+      tmem_ld_cache(tbuf + kCacheCols * (L - 1), sr);
       for (int s = L - 1; s >= 0; --s, ++rs) {
         // The slot is free once the gradient warps have consumed step rs - kNX
         // (tested at the end of the previous step, so that the test's latency
@@ -255,43 +297,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!xready && !mbar_wait(smem_u32(&xempty[xs]), xpar ^ 1u, abort_flag, status, kWhereBwdXEmpty))
           *vabort = 1;
         const uint32_t xb = xring0 + xs * kXSlotBytes;
-        float* xg = reinterpret_cast<float*>(smem + p.xring_off + xs * kXSlotBytes);
-        const float q0 = bf16_bits_to_f32(cq[s * kRows + g]);
-        const float q1 = bf16_bits_to_f32(cq[s * kRows + g + 8]);
-        const float ft = cf[s];
-        const float omf = 1.f - ft;
-        float u[2][2];
+        const float2 q0 = splat2(__uint_as_float(ld_shared_u16(sq + 2 * (s * kRows + g)) << 16));
+        const float2 q1 = splat2(__uint_as_float(ld_shared_u16(sq + 2 * (s * kRows + g + 8)) << 16));
+        const float2 f2 = splat2(ld_shared_f32(sf + 4 * s));
+        float2 u[2];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const float2 uu = *reinterpret_cast<const float2*>(cdy + s * kV + jcol0 + 8 * nt);
-          u[nt][0] = uu.x;
-          u[nt][1] = uu.y;
-        }
+        for (int nt = 0; nt < 2; ++nt) u[nt] = ld_shared_f32x2(sdy + 4 * (s * kV + jcol0 + 8 * nt));
         tmem_ld_wait();
-        tmem_ld_fence_regs(slot_regs);
-        float Z[2][4], Hp[2][4];
+        tmem_ld_fence_regs(sr);
+        float2 G[2][2];
+        uint32_t ew[4];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; e += 2) {
-            const uint32_t zw = slot_regs[2 * nt + e / 2], hw = slot_regs[4 + 2 * nt + e / 2];
-            Z[nt][e] = f16lo(zw);
-            Z[nt][e + 1] = f16hi(zw);
-            Hp[nt][e] = f16lo(hw);
-            Hp[nt][e + 1] = f16hi(hw);
-          }
-        if (s > 0) tmem_ld_32x32b<kCacheCols>(tbuf + kCacheCols * (s - 1), slot_regs);
-        // R = C + q u^T ; D = (1-f) R (1 - Z^2)
-        float Rv[2][4], Dv[2][4];
+        for (int i = 0; i < 4; ++i) {
+          G[i >> 1][i & 1] = f16x2_to_float2(sr[i]);
+          ew[i] = sr[4 + i];
+        }
+        if (s > 0) tmem_ld_cache(tbuf + kCacheCols * (s - 1), sr);
+        // R = C + q u^T ; D = R * G with G = (1-f)(1 - Z^2)
+        float2 Rv[2][2], Dv[2][2];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float qq = (e < 2) ? q0 : q1;
-            Rv[nt][e] = fmaf(qq, u[nt][e & 1], Cg[nt][e]);
-            const float zz = Z[nt][e];
-            Dv[nt][e] = omf * Rv[nt][e] * fmaf(-zz, zz, 1.f);
-          }
+          Rv[nt][0] = __ffma2_rn(q0, u[nt], Cg[nt][0]);
+          Rv[nt][1] = __ffma2_rn(q1, u[nt], Cg[nt][1]);
+          Dv[nt][0] = __fmul2_rn(Rv[nt][0], G[nt][0]);
+          Dv[nt][1] = __fmul2_rn(Rv[nt][1], G[nt][1]);
         }
         // Serial chain: C_{t-1} = f R + D W^T on the warp MMAs.  bf16(D) of
         // this warp's columns is its own k-tile (the accumulator layout of
@@ -299,10 +328,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // while the other three k-tiles load from the tile.
         const uint32_t dt = xb + kXDt;
         uint32_t aown[4];
-        aown[0] = pack2_bf16(Dv[0][0], Dv[0][1]);
-        aown[1] = pack2_bf16(Dv[0][2], Dv[0][3]);
-        aown[2] = pack2_bf16(Dv[1][0], Dv[1][1]);
-        aown[3] = pack2_bf16(Dv[1][2], Dv[1][3]);
+        aown[0] = pack2_bf16(Dv[0][0].x, Dv[0][0].y);
+        aown[1] = pack2_bf16(Dv[0][1].x, Dv[0][1].y);
+        aown[2] = pack2_bf16(Dv[1][0].x, Dv[1][0].y);
+        aown[3] = pack2_bf16(Dv[1][1].x, Dv[1][1].y);
         st_shared_b32(dt + cm_off(g, jcol0), aown[0]);
         st_shared_b32(dt + cm_off(g + 8, jcol0), aown[1]);
         st_shared_b32(dt + cm_off(g, jcol0 + 8), aown[2]);
@@ -314,42 +343,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         float acc[2][4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[nt][e] = ft * Rv[nt][e];
+          const float2 a0 = __fmul2_rn(f2, Rv[nt][0]), a1 = __fmul2_rn(f2, Rv[nt][1]);
+          acc[nt][0] = a0.x; acc[nt][1] = a0.y; acc[nt][2] = a1.x; acc[nt][3] = a1.y;
           mma_bf16_16816(acc[nt], aown, bt[nt][0][0], bt[nt][0][1]);
         }
 #pragma unroll
         for (int i = 0; i < 3; ++i)
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) mma_bf16_16816(acc[nt], af[i], bt[nt][i + 1][0], bt[nt][i + 1][1]);
-        // Off the chain: this thread's shares of dk, dv, df, and bf16 H_{t-1}
-        // for dW, handed to the gradient warps.
+        // The D tile is read by the tensor core (dW): its stores completed
+        // before the barrier, so this proxy fence has nothing to wait for.
+        fence_proxy_async_smem();
+        // Off the chain: this thread's share of df = <R, H_{t-1} - Z>, read
+        // by the gradient warps through the generic proxy only.
         {
-          const float k0 = bf16_bits_to_f32(ck[s * kRows + g]);
-          const float k1 = bf16_bits_to_f32(ck[s * kRows + g + 8]);
-          float pk0 = 0.f, pk1 = 0.f, pe = 0.f;
-          float* xdv = xg + kXDv / 4;
-          const uint32_t ht = xb + kXHt;
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            const int col = jcol0 + 8 * nt;
-            const uint32_t vb = *reinterpret_cast<const uint32_t*>(cv + s * kV + col);
-            const float v0 = bf16lo(vb), v1 = bf16hi(vb);
-            pk0 = fmaf(Dv[nt][0], v0, pk0);
-            pk0 = fmaf(Dv[nt][1], v1, pk0);
-            pk1 = fmaf(Dv[nt][2], v0, pk1);
-            pk1 = fmaf(Dv[nt][3], v1, pk1);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) pe = fmaf(Rv[nt][e], Hp[nt][e] - Z[nt][e], pe);
-            *reinterpret_cast<float2*>(xdv + g * kDvStride + col) =
-                make_float2(fmaf(Dv[nt][0], k0, Dv[nt][2] * k1), fmaf(Dv[nt][1], k0, Dv[nt][3] * k1));
-            st_shared_b32(ht + cm_off(g, col), pack2_bf16(Hp[nt][0], Hp[nt][1]));
-            st_shared_b32(ht + cm_off(g + 8, col), pack2_bf16(Hp[nt][2], Hp[nt][3]));
-          }
-          *reinterpret_cast<float2*>(xg + kXDk / 4 + (w * 4 + qd) * kDkGroup + 2 * g) = make_float2(pk0, pk1);
-          xg[kXDf / 4 + ctid] = pe;
+          float2 pe2 = __fmul2_rn(Rv[0][0], f16x2_to_float2(ew[0]));
+          pe2 = __ffma2_rn(Rv[0][1], f16x2_to_float2(ew[1]), pe2);
+          pe2 = __ffma2_rn(Rv[1][0], f16x2_to_float2(ew[2]), pe2);
+          pe2 = __ffma2_rn(Rv[1][1], f16x2_to_float2(ew[3]), pe2);
+          st_shared_f32(xb + kXDf + 4 * ctid, pe2.x + pe2.y);
         }
-        fence_proxy_async_smem();  // the tiles are read by the tensor core
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&xfull[xs]));
         if constexpr (kClip) {  // per-step clipping of the state gradient
@@ -359,9 +372,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 4; ++e) acc[nt][e] = fminf(fmaxf(acc[nt][e], -A.clip), A.clip);
         }
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) Cg[nt][e] = acc[nt][e];
+        for (int nt = 0; nt < 2; ++nt) {
+          Cg[nt][0] = make_float2(acc[nt][0], acc[nt][1]);
+          Cg[nt][1] = make_float2(acc[nt][2], acc[nt][3]);
+        }
         if (++xs == kNX) {
           xs = 0;
           xpar ^= 1u;
@@ -378,8 +392,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* dst = A.dH0 + (static_cast<int64_t>(chain) * A.K + row_g) * kV + jcol0;
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        *reinterpret_cast<float2*>(dst + 8 * nt) = make_float2(Cg[nt][0], Cg[nt][1]);
-        *reinterpret_cast<float2*>(dst + 8 * kV + 8 * nt) = make_float2(Cg[nt][2], Cg[nt][3]);
+        *reinterpret_cast<float2*>(dst + 8 * nt) = Cg[nt][0];
+        *reinterpret_cast<float2*>(dst + 8 * kV + 8 * nt) = Cg[nt][1];
       }
     }
     if (!ok) *abort_flag = 1;
@@ -404,14 +418,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     const uint32_t htile0 = smem_u32(smem + p.htile_off);
-    float* dqp = reinterpret_cast<float*>(smem + p.dqp_off);  // [C][4 warps][4 qd][8 g][row g, g+8]
+    const uint32_t dqp = smem_u32(smem + p.dqp_off);  // fp32 [C][4 warps][4 qd][8 g][row g, g+8]
     // Start state of a chunk: the checkpoint (H_0, zero if not given, for
-    // chunk 0).  The next
-    // chunk's is loaded a chunk ahead, so its latency stays off the path.
-    auto load_start = [&](int cc, float (&hs)[2][4]) {
+    // chunk 0).  The next chunk's is loaded a chunk ahead, so its latency
+    // stays off the path.
+    auto load_start = [&](int cc, float2 (&hs)[2][2]) {
       if (cc == 0 && A.H0 == nullptr) {
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) hs[nt][0] = hs[nt][1] = hs[nt][2] = hs[nt][3] = 0.f;
+        for (int nt = 0; nt < 2; ++nt) hs[nt][0] = hs[nt][1] = make_float2(0.f, 0.f);
       } else {
         const float* src =
             (cc == 0 ? A.H0 + (static_cast<int64_t>(chain) * A.K + row_g) * kV
@@ -419,13 +433,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             jcol0;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-          const float2 x0 = *reinterpret_cast<const float2*>(src + 8 * nt);
-          const float2 x1 = *reinterpret_cast<const float2*>(src + 8 * kV + 8 * nt);
-          hs[nt][0] = x0.x; hs[nt][1] = x0.y; hs[nt][2] = x1.x; hs[nt][3] = x1.y;
+          hs[nt][0] = *reinterpret_cast<const float2*>(src + 8 * nt);
+          hs[nt][1] = *reinterpret_cast<const float2*>(src + 8 * kV + 8 * nt);
         }
       }
     };
-    float hnext[2][4];
+    float2 hnext[2][2];
     load_start(p.nchunks - 1, hnext);
     // Warp 4 also loads the chunk inputs, one chunk ahead of its own use:
     // q, k, v, dy by TMA, f gathered by the lanes (its global-load latency
@@ -451,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane < CL) cfw[lane] = fv;
       mbar_arrive(smem_u32(&cfull[li % kCBufs]));  // all 32 lanes: the phase's arrival count
     };
-    // Z stash: chunk li's steps into buffer li % nbuf (one bulk copy).
+    // Z stash: chunk li's steps into the staging buffer (one bulk copy).
     const bool zs = A.zstash != nullptr;
     const uint8_t* zsrc = reinterpret_cast<const uint8_t*>(A.zstash) + static_cast<int64_t>(blockIdx.x) * T * kZStepBytes;
     // One staging buffer: chunk li + 1 is copied in once chunk li is rebuilt,
@@ -476,6 +489,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (zs) issue_z(zissued++);
       publish_chunk(0, issue_chunk(0));
     }
+    // The stash step (2 KB: 16 bytes = Z[8c .. 8c+7][j] at (c * 64 + j) * 16)
+    // read with one ldmatrix.x4.trans: matrix i covers row run i & 1 and the
+    // columns 16w + 8 (i >> 1) .. + 7 (one 16-byte stash row per column), so
+    // thread (g, qd) receives {Z[8c + g][j], Z[8c + g][j + 1]}, j = 16w + 8nt
+    // + 2qd, in the order (nt 0, row g), (0, g+8), (1, g), (1, g+8).
+    const uint32_t zaddr = smem_u32(smem + p.zbuf_off) +
+                           static_cast<uint32_t>(((lane >> 3) & 1) * kV + 16 * w + 8 * (lane >> 4) + (lane & 7)) * 16;
     bool ok = true;
     int issued = 1;  // chunks whose loads have been issued
     for (int ci = 0; ci < p.nchunks; ++ci) {
@@ -494,6 +514,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mine = mbar_wait_timed(smem_u32(&cempty[(ci + 1) % kCBufs]), ((ci - 3) / kCBufs) & 1, status,
                                kWhereBwdCEmpty);
       if (mine && zs) mine = mbar_wait_timed(smem_u32(&zfull[0]), ci & 1, status, kWhereBwdZFull);
+      // The H tile buffer is free once every dW MMA of chunk ci - nbuf is done.
+      if (mine && ci >= p.nbuf)
+        mine = mbar_wait_timed(smem_u32(&hfree[tb]), ((ci / p.nbuf) - 1) & 1, status, kWhereBwdDW);
       if (!mine) *rabort = 1;
       named_bar_sync(2, 128);
       if (*rabort) {
@@ -504,61 +527,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool more = loader && ci + 1 < p.nchunks;
       float fnext = 0.f;
       if (more) fnext = issue_chunk(ci + 1);
-      const uint8_t* cbuf = smem + p.cbuf_off + cb * p.cbuf_bytes;
-      const uint16_t* ck = reinterpret_cast<const uint16_t*>(cbuf + p.ck_off);
-      const uint16_t* cv = reinterpret_cast<const uint16_t*>(cbuf + p.cv_off);
-      const float* cdy = reinterpret_cast<const float*>(cbuf + p.cdy_off);
-      const float* cf = reinterpret_cast<const float*>(cbuf + p.cf_off);
+      const uint32_t cbuf = smem_u32(smem + p.cbuf_off + cb * p.cbuf_bytes);
+      const uint32_t sk = cbuf + p.ck_off, sv = cbuf + p.cv_off, sdy = cbuf + p.cdy_off, sf = cbuf + p.cf_off;
       const uint32_t tbuf = tcache + kCacheCols * CL * tb;
-      float h[2][4];
+      const uint32_t hbase = hbuf0 + static_cast<uint32_t>(tb * CL) * kHTileBytes;
+      // This thread's four bf16 H_{s-1} pairs into step s's H tile.
+      auto store_htile = [&](int s, const uint32_t (&hb)[4]) {
+        const uint32_t ht = hbase + static_cast<uint32_t>(s) * kHTileBytes;
+        st_shared_b32(ht + cm_off(g, jcol0), hb[0]);
+        st_shared_b32(ht + cm_off(g + 8, jcol0), hb[1]);
+        st_shared_b32(ht + cm_off(g, jcol0 + 8), hb[2]);
+        st_shared_b32(ht + cm_off(g + 8, jcol0 + 8), hb[3]);
+      };
+      float2 h[2][2];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) h[nt][e] = hnext[nt][e];
+      for (int nt = 0; nt < 2; ++nt) {
+        h[nt][0] = hnext[nt][0];
+        h[nt][1] = hnext[nt][1];
+      }
       if (c > 0) load_start(c - 1, hnext);
-      auto dq_share = [&](int s, const float (&h)[2][4]) {
-        // dq_t = H_t u_t: this thread's share (its four columns, rows g and
-        // g + 8); the sixteen shares of a row are summed at the chunk's end.
-        {
-          const float2 u0 = *reinterpret_cast<const float2*>(cdy + s * kV + jcol0);
-          const float2 u1 = *reinterpret_cast<const float2*>(cdy + s * kV + jcol0 + 8);
-          float p0 = h[0][0] * u0.x;
-          p0 = fmaf(h[0][1], u0.y, p0);
-          p0 = fmaf(h[1][0], u1.x, p0);
-          p0 = fmaf(h[1][1], u1.y, p0);
-          float p1 = h[0][2] * u0.x;
-          p1 = fmaf(h[0][3], u0.y, p1);
-          p1 = fmaf(h[1][2], u1.x, p1);
-          p1 = fmaf(h[1][3], u1.y, p1);
-          *reinterpret_cast<float2*>(dqp + (s * 16 + w * 4 + qd) * kRows + 2 * g) = make_float2(p0, p1);
+      // dq_t = H_t u_t: this thread's share over its four columns (rows g
+      // and g + 8), in fp32; the sixteen shares of a row are summed at the
+      // chunk's end.
+      auto dq_share = [&](int s) {
+        const float2 u0 = ld_shared_f32x2(sdy + 4 * (s * kV + jcol0));
+        const float2 u1 = ld_shared_f32x2(sdy + 4 * (s * kV + jcol0 + 8));
+        const float2 pg = __ffma2_rn(h[1][0], u1, __fmul2_rn(h[0][0], u0));
+        const float2 pg8 = __ffma2_rn(h[1][1], u1, __fmul2_rn(h[0][1], u0));
+        st_shared_f32x2(dqp + 4 * ((s * 16 + w * 4 + qd) * kRows + 2 * g), make_float2(pg.x + pg.y, pg8.x + pg8.y));
+      };
+      auto pack_h = [&](uint32_t (&ha)[4]) {  // fp16 H as this warp's A fragment
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          ha[2 * nt] = pack2_f16(h[nt][0].x, h[nt][0].y);
+          ha[2 * nt + 1] = pack2_f16(h[nt][1].x, h[nt][1].y);
         }
       };
       if (zs) {
-        // Z_t from the stash (written by the tcgen05 forward: per step and
-        // row block, Z[8c .. 8c+7][j] as 16 bytes at (c, j)); the state
-        // advances by the gate blend alone.  This thread's pairs: rows g, g+8
-        // (row runs 0, 1) and columns m0, m0+1, m0+8, m0+9 (m0 = 16w + 2qd).
-        const uint16_t* zb = reinterpret_cast<const uint16_t*>(smem + p.zbuf_off) + (16 * w + 2 * qd) * 8 + g;
         for (int s = 0; s < L; ++s) {
-          const float omf = 1.f - cf[s];
-          const uint16_t* zs_ = zb + s * (kZStepBytes / 2);
-          auto pair = [&](int run, int dm) {  // {Z[8 run + g][m0 + dm], Z[8 run + g][m0 + dm + 1]}
-            const uint16_t* e = zs_ + (run * kV + dm) * 8;
-            return static_cast<uint32_t>(e[0]) | (static_cast<uint32_t>(e[8]) << 16);
-          };
-          const uint4 zq = make_uint4(pair(0, 0), pair(1, 0), pair(0, 8), pair(1, 8));
-          const float z[2][4] = {{f16lo(zq.x), f16hi(zq.x), f16lo(zq.y), f16hi(zq.y)},
-                                 {f16lo(zq.z), f16hi(zq.z), f16lo(zq.w), f16hi(zq.w)}};
-          // The cache takes Z_s as stashed (already fp16 pairs) and H_{s-1}.
-          const uint32_t cache[kCacheCols] = {zq.x, zq.y, zq.z, zq.w,
-                                              pack2_f16(h[0][0], h[0][1]), pack2_f16(h[0][2], h[0][3]),
-                                              pack2_f16(h[1][0], h[1][1]), pack2_f16(h[1][2], h[1][3])};
+          const float omf = 1.f - ld_shared_f32(sf + 4 * s);
+          uint32_t zq[4];
+          ldmatrix_x4_trans(zq, zaddr + s * kZStepBytes);
+          float2 z[2][2];
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) h[nt][e] = fmaf(omf, z[nt][e] - h[nt][e], h[nt][e]);
-          tmem_st_32x32b_x8(tbuf + kCacheCols * s, cache);
-          dq_share(s, h);
+          for (int i = 0; i < 4; ++i) z[i >> 1][i & 1] = f16x2_to_float2(zq[i]);
+          uint32_t cache[kCacheCols], hb[4];
+          rebuild_step(z, h, omf, cache, hb);
+          tmem_st_cache(tbuf + kCacheCols * s, cache);
+          store_htile(s, hb);
+          dq_share(s);
         }
         // Every read of this Z buffer and every dq share of the chunk is done.
         named_bar_sync(2, 128);
@@ -567,13 +584,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Step s, as in the forward: acc = k_s v_s^T + fp16(H_{s-1}) W, the
         // own k-tile from registers while the other three load from the tile.
         uint32_t hh[4];
-        auto split = [&]() {
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            hh[2 * nt] = pack2_f16(h[nt][0], h[nt][1]);
-            hh[2 * nt + 1] = pack2_f16(h[nt][2], h[nt][3]);
-          }
-        };
         auto store_tile = [&](uint32_t base) {
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
@@ -582,21 +592,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             st_shared_b32(base + tile_off(g + 8, col), hh[2 * nt + 1]);
           }
         };
-        split();
+        pack_h(hh);
         store_tile(htile0);
         named_bar_sync(2, 128);
         for (int s = 0; s < L; ++s) {
-          const float omf = 1.f - cf[s];
+          const float omf = 1.f - ld_shared_f32(sf + 4 * s);
           const uint32_t atile = htile0 + (s & 1) * 2048;
           uint32_t af[3][4];
 #pragma unroll
           for (int i = 0; i < 3; ++i) ldmatrix_x4(af[i], ldsm_addr_a(atile, (w + 1 + i) & 3, lane));
           float acc[2][4];
-          const float k0 = bf16_bits_to_f32(ck[s * kRows + g]);
-          const float k1 = bf16_bits_to_f32(ck[s * kRows + g + 8]);
+          const float k0 = __uint_as_float(ld_shared_u16(sk + 2 * (s * kRows + g)) << 16);
+          const float k1 = __uint_as_float(ld_shared_u16(sk + 2 * (s * kRows + g + 8)) << 16);
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
-            const uint32_t vv = *reinterpret_cast<const uint32_t*>(cv + s * kV + jcol0 + 8 * nt);
+            const uint32_t vv = ld_shared_b32(sv + 2 * (s * kV + jcol0 + 8 * nt));
             const float v0 = bf16lo(vv), v1 = bf16hi(vv);
             acc[nt][0] = k0 * v0;
             acc[nt][1] = k0 * v1;
@@ -608,27 +618,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 3; ++i)
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) mma_f16_16816(acc[nt], af[i], bw[nt][i + 1][0], bw[nt][i + 1][1]);
-          uint32_t cache[kCacheCols];  // Z_s and H_{s-1} as fp16 pairs
+          float2 z[2][2];
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
-            float z[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) z[e] = tanh_fast(acc[nt][e]);
-            cache[2 * nt] = pack2_f16(z[0], z[1]);
-            cache[2 * nt + 1] = pack2_f16(z[2], z[3]);
-            cache[4 + 2 * nt] = pack2_f16(h[nt][0], h[nt][1]);
-            cache[4 + 2 * nt + 1] = pack2_f16(h[nt][2], h[nt][3]);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) h[nt][e] = fmaf(omf, z[e] - h[nt][e], h[nt][e]);
+            z[nt][0] = make_float2(tanh_fast(acc[nt][0]), tanh_fast(acc[nt][1]));
+            z[nt][1] = make_float2(tanh_fast(acc[nt][2]), tanh_fast(acc[nt][3]));
           }
-          split();
+          uint32_t cache[kCacheCols], hb[4];
+          rebuild_step(z, h, omf, cache, hb);
+          pack_h(hh);
           store_tile(htile0 + ((s + 1) & 1) * 2048);
-          tmem_st_32x32b_x8(tbuf + kCacheCols * s, cache);
-          dq_share(s, h);
+          tmem_st_cache(tbuf + kCacheCols * s, cache);
+          store_htile(s, hb);
+          dq_share(s);
           named_bar_sync(2, 128);
         }
       }
       tmem_st_wait();
+      fence_proxy_async_smem();  // the chunk's H tiles are read by the tensor core
       if (more) publish_chunk(ci + 1, fnext);
       tc_fence_before_sync();
       __syncwarp();
@@ -638,10 +645,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the sixteen shares of row r = g + 8 hi, warp by warp, in a fixed order.
       for (int idx = ctid; idx < L * kRows; idx += 128) {
         const int sp = idx >> 4, r = idx & 15;
-        const float* pp = dqp + sp * 16 * kRows + 2 * (r & 7) + (r >> 3);
+        const uint32_t pp = dqp + 4 * (sp * 16 * kRows + 2 * (r & 7) + (r >> 3));
         float sum = 0.f;
 #pragma unroll
-        for (int sh = 0; sh < 16; ++sh) sum += pp[sh * kRows];
+        for (int sh = 0; sh < 16; ++sh) sum += ld_shared_f32(pp + 4 * sh * kRows);
         const int64_t rowt = (static_cast<int64_t>(b) * T + s0 + sp) * N + n;
         A.dq[rowt * A.K + cta_rank * kRows + r] = sum;
       }
@@ -659,11 +666,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ======================= gradient warps =======================
     // Warp 8 issues the step's dW MMA (one elected lane, tcgen05, the
     // accumulator in TMEM columns 448..511):
-    //   dW (+)= [H_{t-1}^T ; 0] (128 x 16) * D (16 x 64),
+    //   dW (+)= [H_{t-1}^T ; *] (128 x 16) * D (16 x 64)  (rows 64.. unused),
     // committed to the slot's empty barrier.  Every fourth step (rs % 4 == w)
-    // warp 8 + w also sums that step's dk, dv and df shares.
+    // warp 8 + w also forms that step's dk and dv partial on the tensor core
+    // from the slot's bf16 D tile, sums the df shares and adds dw_r.
     float dwr0 = 0.f, dwr1 = 0.f;  // dw_r columns 2 lane, 2 lane + 1 (row block 0 only)
-    const int r16 = lane & 15, hh = lane >> 4;
     const uint32_t idesc = idesc_bf16_f32(128, kV, /*a_mn_major=*/true, /*b_mn_major=*/true);
     const uint32_t dw_tmem = tmem_base + kDWCol;
     bool ok = true;
@@ -681,20 +688,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
         break;
       }
-      const uint8_t* cbuf = smem + p.cbuf_off + cb * p.cbuf_bytes;
-      const uint16_t* cv = reinterpret_cast<const uint16_t*>(cbuf + p.cv_off);
-      const float* cdy = reinterpret_cast<const float*>(cbuf + p.cdy_off);
+      const uint32_t cbuf = smem_u32(smem + p.cbuf_off + cb * p.cbuf_bytes);
+      const uint32_t sk = cbuf + p.ck_off, sv = cbuf + p.cv_off, sdy = cbuf + p.cdy_off;
+      const int tb = ci % p.nbuf;
+      const uint32_t hbase = hbuf0 + static_cast<uint32_t>(tb * CL) * kHTileBytes;
       for (int s = L - 1; s >= 0; --s, ++rs) {
         const bool duty = (rs & 3) == w;
         const uint32_t xb = xring0 + xs * kXSlotBytes;
-        const float* xg = reinterpret_cast<const float*>(smem + p.xring_off + xs * kXSlotBytes);
         // A give-up is acted on at the next chunk boundary.
         if ((w == 0 || duty) && !mbar_wait(smem_u32(&xfull[xs]), xpar, abort_flag, status, kWhereBwdXFull))
           *gabort = 1;
         if (w == 0) {
           tc_fence_after_sync();
           if (elect_one()) {
-            tc_mma_f16_ss(dw_tmem, smem_desc_noswizzle(xb + kXHt, 128, 256),
+            tc_mma_f16_ss(dw_tmem, smem_desc_noswizzle(hbase + static_cast<uint32_t>(s) * kHTileBytes, 128, 256),
                           smem_desc_noswizzle(xb + kXDt, 128, 256), idesc, rs > 0 ? 1u : 0u);
             tc_commit(smem_u32(&xempty[xs]));  // arrives once the MMA has read the slot
           }
@@ -702,42 +709,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (duty) {
           const int64_t rowt = (static_cast<int64_t>(b) * T + s0 + s) * N + n;
-          // dk_t = D_t v_t: lane -> row r16 = g + 8 hi; warps 2 hh, 2 hh + 1 and
-          // their four qd shares, then the two halves (fixed order).
+          const uint32_t dt = xb + kXDt;
+          // dk_t = D_t v_t: A = D (four k-tiles), B = v_t pairs in every
+          // column; row g's value is c0, row g + 8's c2 (in every lane).
           {
-            const int gg = r16 & 7, hi = r16 >> 3;
-            const float* xk = xg + kXDk / 4 + 2 * gg + hi;
-            float pk = 0.f;
+            float d4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int ww = 0; ww < 2; ++ww)
-#pragma unroll
-              for (int qq = 0; qq < 4; ++qq) pk += xk[((2 * hh + ww) * 4 + qq) * kDkGroup];
-            pk += __shfl_xor_sync(0xffffffffu, pk, 16);
-            if (lane < 16) A.dk[rowt * A.K + cta_rank * kRows + r16] = pk;
-          }
-          // Row-block partial of D_t^T k_t: lane -> columns 2 lane, 2 lane + 1.
-          {
-            const float* xdv = xg + kXDv / 4 + 2 * lane;
-            float2 a2 = *reinterpret_cast<const float2*>(xdv);
-#pragma unroll
-            for (int gg = 1; gg < 8; ++gg) {
-              const float2 x = *reinterpret_cast<const float2*>(xdv + gg * kDvStride);
-              a2.x += x.x;
-              a2.y += x.y;
+            for (int kt = 0; kt < 4; ++kt) {
+              uint32_t a[4];
+              ldmatrix_x4(a, cm_ldsm_a(dt, kt, lane));
+              const uint32_t b0 = ld_shared_b32(sv + 2 * (s * kV + 16 * kt + 2 * qd));
+              const uint32_t b1 = ld_shared_b32(sv + 2 * (s * kV + 16 * kt + 2 * qd + 8));
+              mma_bf16_16816(d4, a, b0, b1);
             }
-            *reinterpret_cast<float2*>(p.dvp + (rowt * R + cta_rank) * kV + 2 * lane) = a2;
+            if (qd == 0) {
+              A.dk[rowt * A.K + cta_rank * kRows + g] = d4[0];
+              A.dk[rowt * A.K + cta_rank * kRows + g + 8] = d4[2];
+            }
+          }
+          // Row-block partial of D_t^T k_t: A = D^T (ldmatrix.trans, four
+          // 16-column m-tiles), B = k_t pairs of the block's rows in every
+          // column; column 16 mt + g is c0 of m-tile mt, 16 mt + g + 8 its c2.
+          // Lane (g, qd) stores m-tile qd's two values.
+          {
+            const uint32_t b0 = ld_shared_b32(sk + 2 * (s * kRows + 2 * qd));
+            const uint32_t b1 = ld_shared_b32(sk + 2 * (s * kRows + 2 * qd + 8));
+            float lo = 0.f, hi = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) {
+              uint32_t a[4];
+              ldmatrix_x4_trans(a, cm_ldsm_at(dt, mt, lane));
+              float d4[4] = {0.f, 0.f, 0.f, 0.f};
+              mma_bf16_16816(d4, a, b0, b1);
+              lo = (qd == mt) ? d4[0] : lo;
+              hi = (qd == mt) ? d4[2] : hi;
+            }
+            float* dst = p.dvp + (rowt * R + cta_rank) * kV + 16 * qd + g;
+            dst[0] = lo;
+            dst[8] = hi;
           }
           // Row-block partial of df_t = <R_t, H_{t-1} - Z_t>.
           {
-            const float4 e4 = *reinterpret_cast<const float4*>(xg + kXDf / 4 + 4 * lane);
+            const float4 e4 = ld_shared_f32x4(xb + kXDf + 16 * lane);
             float pf = (e4.x + e4.y) + (e4.z + e4.w);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) pf += __shfl_xor_sync(0xffffffffu, pf, o);  // fixed tree
             if (lane == 0) p.dfp[rowt * R + cta_rank] = pf;
           }
           if (cta_rank == 0) {  // dw_r += u_t * v_t, once per chain
-            const float2 uu = *reinterpret_cast<const float2*>(cdy + s * kV + 2 * lane);
-            const uint32_t vb = *reinterpret_cast<const uint32_t*>(cv + s * kV + 2 * lane);
+            const float2 uu = ld_shared_f32x2(sdy + 4 * (s * kV + 2 * lane));
+            const uint32_t vb = ld_shared_b32(sv + 2 * (s * kV + 2 * lane));
             dwr0 = fmaf(uu.x, bf16lo(vb), dwr0);
             dwr1 = fmaf(uu.y, bf16hi(vb), dwr1);
           }
@@ -748,6 +769,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           xs = 0;
           xpar ^= 1u;
         }
+      }
+      // The chunk's H tile buffer is free once its last dW MMA completes.
+      if (w == 0) {
+        if (elect_one()) tc_commit(smem_u32(&hfree[tb]));
+        __syncwarp();
       }
       // The gradient warps are the last readers of the chunk's inputs.
       __syncwarp();
@@ -867,10 +893,11 @@ cudaError_t launch_mma_backward(const BwdArgs& a, cudaStream_t stream) {
   p.cf_off = p.cdy_off + align_up(C * kV * 4, 128);
   p.cbuf_bytes = align_up(p.cf_off + C * 4, 128);
   p.xring_off = align_up(p.cbuf_off + kCBufs * p.cbuf_bytes, 1024);
-  p.dqp_off = p.xring_off + kNX * kXSlotBytes;
-  p.dwr_off = p.dqp_off + kMaxChunk * 16 * kRows * 4;
+  p.hbuf_off = p.xring_off + kNX * kXSlotBytes;  // two buffers of C H tiles, then 2 KB of slack
+  p.dqp_off = p.hbuf_off + (2 * C + 1) * kHTileBytes;
+  p.dwr_off = p.dqp_off + C * 16 * kRows * 4;
   p.bar_off = p.dwr_off + 4 * kV * 4;
-  p.misc_off = p.bar_off + (2 * kCBufs + 4 + 2 * kNX + 1 + 2) * 8;
+  p.misc_off = p.bar_off + (2 * kCBufs + 4 + 2 * kNX + 1 + 2 + 2) * 8;
   p.zbuf_off = align_up(p.misc_off + 32, 128);
   const uint32_t zbytes = a.zstash != nullptr ? static_cast<uint32_t>(C) * kZStepBytes : 0u;
   const uint32_t smem = p.zbuf_off + zbytes + 1024;

@@ -184,7 +184,7 @@ def test_z_stash_rules_without_a_device(lib):
         return binding.m2rnn_backward_state(P, P, P, P, P, P, None, P, None, ckpt, C, z, P, P, P, P, P, P, None,
                                             0.0, 1, T, 1, 1, 64, 64, bf, P, 1 << 30, None)
     assert bs() == binding.M2RNN_ERR_INVALID_ARG          # T > ckpt_every needs the forward's checkpoints
-    assert bs(C=29, ckpt=P) == binding.M2RNN_ERR_UNSUPPORTED   # longer than the backward's chunk cache
+    assert bs(C=21, ckpt=P) == binding.M2RNN_ERR_UNSUPPORTED   # longer than the backward's chunk cache
     assert bs(z=P + 4, ckpt=P) == binding.M2RNN_ERR_INVALID_ARG
 
     def bs16(K=64, C=14):
@@ -202,7 +202,7 @@ def test_noalloc_backward_rejects_unsupported_shapes_without_a_device(lib):
                                               a["B"], a["T"], a["N"], a["K"], a["V"], a["dt"], 0, None)
     assert call(V=128) == binding.M2RNN_ERR_UNSUPPORTED
     assert call(dt=binding.M2RNN_F32) == binding.M2RNN_ERR_UNSUPPORTED
-    assert call(C=29) == binding.M2RNN_ERR_UNSUPPORTED            # longer than the TMEM chunk cache
+    assert call(C=21) == binding.M2RNN_ERR_UNSUPPORTED            # longer than the TMEM chunk cache
     assert call(ckpt=None) == binding.M2RNN_ERR_INVALID_ARG      # T > C needs the forward's checkpoints
     assert call(B=4096, N=1024) == binding.M2RNN_ERR_WORKSPACE   # exceeds the built-in scratch
 

@@ -103,7 +103,7 @@ def _check_gated_grads(got, inp, ge, tol, label):
 
 
 @pytest.mark.parametrize("kernel_family", ["mma", "simt"], indirect=True)
-@pytest.mark.parametrize("B,N,T,K,V,C,reuse", [(2, 2, 37, 64, 64, 14, False), (1, 3, 64, 32, 64, 28, True),
+@pytest.mark.parametrize("B,N,T,K,V,C,reuse", [(2, 2, 37, 64, 64, 14, False), (1, 3, 64, 32, 64, 18, True),
                                                (1, 1, 1, 64, 64, 14, False)])
 def test_gated_backward(kernel_family, B, N, T, K, V, C, reuse):
     inp, gs, ge = _gated_case(B, N, T, K, V, "bf16", seed=720 + T)
@@ -120,7 +120,7 @@ def test_gated_backward_other_families(B, N, T, K, V, dtype, shared, C):
     _check_gated_grads(got, inp, ge, TOL_F32 if dtype == "f32" else TOL_BF16_REL, (B, N, T, K, V, dtype))
 
 
-@pytest.mark.parametrize("B,N,T,K,V,C,shared", [(2, 2, 37, 64, 64, 14, False), (1, 3, 64, 32, 64, 28, False),
+@pytest.mark.parametrize("B,N,T,K,V,C,shared", [(2, 2, 37, 64, 64, 14, False), (1, 3, 64, 32, 64, 18, False),
                                                (2, 4, 50, 64, 16, 28, True)])
 def test_gated_backward_with_stash(B, N, T, K, V, C, shared):
     inp, gs, ge = _gated_case(B, N, T, K, V, "bf16", seed=760 + T, shared_qk=shared)
@@ -138,12 +138,12 @@ def test_gated_backward_is_deterministic():
 
 def test_gated_full_size_properties():
     """The fwd+bwd workload's shape (B=4, heads=8, T=4096, K=V=64), run as
-    the benchmark's gated block runs it (Z stash, 28-step chunks): dbeta is
+    the benchmark's gated block runs it (Z stash, 20-step chunks): dbeta is
     the (b, t)-sum of da, and dalpha the (b, t)-sum of da * s / (alpha
     sigmoid(a + beta)), recomputed from the kernel's own da in float64; and
     one head's gradients (dq, dk, dv, da, dalpha, dbeta) against the oracle."""
     inp, gs, ge = _gated_case(4, 8, 4096, 64, 64, "bf16", seed=750)
-    got = _run_gated(inp, gs, backward=True, ckpt_every=28, stash=True)
+    got = _run_gated(inp, gs, backward=True, ckpt_every=20, stash=True)
     da = got["da"].astype(np.float64)
     assert np.all(np.isfinite(da))
     # fp32 sums of 16384 terms: bound the error by the sum of magnitudes
