@@ -111,6 +111,30 @@ __device__ __forceinline__ uint32_t cm_ldsm_at(uint32_t tile, int mt, int lane) 
 
 __device__ __forceinline__ float2 splat2(float x) { return make_float2(x, x); }
 
+// x split into bf16 hi + lo (x - hi - lo is below 2^-16 |x|), as a bf16 pair
+// {hi, lo} (hi in the low half).
+__device__ __forceinline__ uint32_t bf16_hilo(float x) {
+  const uint32_t hb = pack_bf16x2(x, 0.f) & 0xFFFFu;
+  const float lo = x - __uint_as_float(hb << 16);
+  return hb | (pack_bf16x2(lo, 0.f) << 16);
+}
+
+// Sum over the 32 lanes of x, in every lane, on the tensor core (no shuffles):
+// with A = ones, a B fragment holding {hi, lo} of lane (g, q)'s x at rows 2q,
+// 2q + 1 of column g sums the four lanes of group g (result s_n in column n);
+// lane (g, q) then holds s_2q, s_2q+1, whose hi and lo parts form the B
+// fragment of a second MMA that sums the eight groups.  Products with one are
+// exact and the accumulation is fp32; the order is fixed.
+__device__ __forceinline__ float warp_sum_mma(float x) {
+  const uint32_t ones[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};
+  float d[4] = {0.f, 0.f, 0.f, 0.f};
+  mma_bf16_16816(d, ones, bf16_hilo(x), 0u);
+  const uint32_t h0 = bf16_hilo(d[0]), h1 = bf16_hilo(d[1]);
+  float e[4] = {0.f, 0.f, 0.f, 0.f};
+  mma_bf16_16816(e, ones, (h0 & 0xFFFFu) | (h1 << 16), (h0 >> 16) | (h1 & 0xFFFF0000u));
+  return e[0];
+}
+
 struct MmaBwdParams {
   BwdArgs a;
   int R;
@@ -669,8 +693,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     //   dW (+)= [H_{t-1}^T ; *] (128 x 16) * D (16 x 64)  (rows 64.. unused),
     // committed to the slot's empty barrier.  Every fourth step (rs % 4 == w)
     // warp 8 + w also forms that step's dk and dv partial on the tensor core
-    // from the slot's bf16 D tile, sums the df shares and adds dw_r.
-    float dwr0 = 0.f, dwr1 = 0.f;  // dw_r columns 2 lane, 2 lane + 1 (row block 0 only)
+    // from the slot's bf16 D tile, sums the df shares (also on the tensor
+    // core) and adds its columns' dw_r.  (Splitting that work over all four
+    // warps every step was measured 46 % slower: four warps then poll the
+    // step's barrier instead of two.)
+    // dw_r: the chain's R row-block CTAs each sum a slice of the 32 column
+    // pairs; this lane's pair is columns 2 dwr_pair, 2 dwr_pair + 1.
+    float dwr0 = 0.f, dwr1 = 0.f;
+    const int dwr_ppr = (kV / 2 + R - 1) / R;
+    const int dwr_pair = cta_rank * dwr_ppr + lane;
+    const bool dwr_lane = lane < dwr_ppr && dwr_pair < kV / 2;
     const uint32_t idesc = idesc_bf16_f32(128, kV, /*a_mn_major=*/true, /*b_mn_major=*/true);
     const uint32_t dw_tmem = tmem_base + kDWCol;
     bool ok = true;
@@ -712,15 +744,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t dt = xb + kXDt;
           // dk_t = D_t v_t: A = D (four k-tiles), B = v_t pairs in every
           // column; row g's value is c0, row g + 8's c2 (in every lane).
+          // The B fragments of all four k-tiles come from two ldmatrix.x4
+          // whose eight row addresses per matrix all point at the same 8
+          // values of v_t.
           {
+            uint32_t vb[2][4];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) ldmatrix_x4(vb[hf], sv + 2 * (s * kV + 32 * hf + 8 * (lane >> 3)));
             float d4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int kt = 0; kt < 4; ++kt) {
               uint32_t a[4];
               ldmatrix_x4(a, cm_ldsm_a(dt, kt, lane));
-              const uint32_t b0 = ld_shared_b32(sv + 2 * (s * kV + 16 * kt + 2 * qd));
-              const uint32_t b1 = ld_shared_b32(sv + 2 * (s * kV + 16 * kt + 2 * qd + 8));
-              mma_bf16_16816(d4, a, b0, b1);
+              mma_bf16_16816(d4, a, vb[kt >> 1][2 * (kt & 1)], vb[kt >> 1][2 * (kt & 1) + 1]);
             }
             if (qd == 0) {
               A.dk[rowt * A.K + cta_rank * kRows + g] = d4[0];
@@ -748,19 +784,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             dst[0] = lo;
             dst[8] = hi;
           }
-          // Row-block partial of df_t = <R_t, H_{t-1} - Z_t>.
+          // Row-block partial of df_t = <R_t, H_{t-1} - Z_t>: four shares
+          // per lane, then the 32 lanes summed on the tensor core.
           {
             const float4 e4 = ld_shared_f32x4(xb + kXDf + 16 * lane);
-            float pf = (e4.x + e4.y) + (e4.z + e4.w);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) pf += __shfl_xor_sync(0xffffffffu, pf, o);  // fixed tree
+            const float pf = warp_sum_mma((e4.x + e4.y) + (e4.z + e4.w));
             if (lane == 0) p.dfp[rowt * R + cta_rank] = pf;
           }
-          if (cta_rank == 0) {  // dw_r += u_t * v_t, once per chain
-            const float2 uu = ld_shared_f32x2(sdy + 4 * (s * kV + 2 * lane));
-            const uint32_t vb = ld_shared_b32(sv + 2 * (s * kV + 2 * lane));
-            dwr0 = fmaf(uu.x, bf16lo(vb), dwr0);
-            dwr1 = fmaf(uu.y, bf16hi(vb), dwr1);
+          if (dwr_lane) {  // dw_r += u_t * v_t over this CTA's columns
+            const float2 uu = ld_shared_f32x2(sdy + 4 * (s * kV + 2 * dwr_pair));
+            const uint32_t vv = ld_shared_b32(sv + 2 * (s * kV + 2 * dwr_pair));
+            dwr0 = fmaf(uu.x, bf16lo(vv), dwr0);
+            dwr1 = fmaf(uu.y, bf16hi(vv), dwr1);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&xempty[xs]));
@@ -808,7 +843,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* sd = reinterpret_cast<float*>(smem + p.dwr_off);
       *reinterpret_cast<float2*>(sd + w * kV + 2 * lane) = make_float2(dwr0, dwr1);
       named_bar_sync(3, 128);
-      if (cta_rank == 0 && w == 0) {
+      if (w == 0 && dwr_lane) {
         float2 acc2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int ww = 0; ww < 4; ++ww) {
@@ -816,7 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc2.x += x.x;
           acc2.y += x.y;
         }
-        *reinterpret_cast<float2*>(A.dwr_part + static_cast<int64_t>(chain) * kV + 2 * lane) = acc2;
+        *reinterpret_cast<float2*>(A.dwr_part + static_cast<int64_t>(chain) * kV + 2 * dwr_pair) = acc2;
       }
     } else {
       *abort_flag = 1;
@@ -832,13 +867,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // dv = sum over the chain's row blocks of D^T k (fixed order) + w_r * dy;
-// df = sum over the row blocks.  One warp per (b, t, n).
+// df = sum of the RF row-block partials, in order.  One warp per (b, t, n).
 __global__ void __launch_bounds__(256) mma_backward_rows_kernel(const float* __restrict__ dvp,
                                                                 const float* __restrict__ dfp,
                                                                 const float* __restrict__ dy,
                                                                 const uint16_t* __restrict__ w_r,
                                                                 float* __restrict__ dv, float* __restrict__ df,
-                                                                int64_t rows, int N, int R) {
+                                                                int64_t rows, int N, int R, int RF) {
   const int lane = threadIdx.x & 31;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
   for (int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; row < rows;
@@ -855,7 +890,7 @@ __global__ void __launch_bounds__(256) mma_backward_rows_kernel(const float* __r
     *reinterpret_cast<float2*>(dv + row * kV + 2 * lane) = make_float2(fmaf(bf16lo(wb), u.x, a0), fmaf(bf16hi(wb), u.y, a1));
     if (lane == 0) {
       float sf = 0.f;
-      for (int pr = 0; pr < R; ++pr) sf += dfp[row * R + pr];
+      for (int pr = 0; pr < RF; ++pr) sf += dfp[row * RF + pr];
       df[row] = sf;
     }
   }
@@ -923,7 +958,7 @@ cudaError_t launch_mma_backward(const BwdArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int blocks = static_cast<int>(std::min<size_t>((rows + 7) / 8, 152 * 16));
   mma_backward_rows_kernel<<<blocks, 256, 0, stream>>>(p.dvp, p.dfp, a.dy, static_cast<const uint16_t*>(a.w_r),
-                                                       a.dv, a.df, static_cast<int64_t>(rows), a.N, p.R);
+                                                       a.dv, a.df, static_cast<int64_t>(rows), a.N, p.R, p.R);
   return cudaGetLastError();
 }
 
