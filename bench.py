@@ -51,6 +51,7 @@ IN_NAMES = ("q", "k", "v", "f", "W", "w_r")
 GRADS = ("dq", "dk", "dv", "df", "dW", "dw_r")
 CKPT_EVERY = 20  # chunk length of the V = 64 backward rebuild (its longest: shared-memory bound)
 CKPT_EVERY_MV = 32  # the V = 16 backward's longest chunk (fewest chunk hand-offs)
+CKPT_EVERY_K128 = 8  # the K = V = 128 backward: its chunk cache (64 KB per step and chain) stays in L2
 FLUSH_BYTES = 256 << 20  # larger than the 129 MB L2
 
 
@@ -563,7 +564,7 @@ def time_fwdbwd(name, binding, dev, stream, flush, pk, dist, reps=3):
     step: the same protocol as the headline step, for another workload."""
     import torch
     w = WORKLOADS[name]
-    C = CKPT_EVERY_MV if w["V"] == 16 else CKPT_EVERY
+    C = CKPT_EVERY_MV if w["V"] == 16 else (CKPT_EVERY_K128 if w["V"] == 128 else CKPT_EVERY)
     # The Z stash where the shape has one (V = 64, V = 16).
     stash = binding.m2rnn_z_stash_size(w["B"], w["T"], w["N"], w["K"], w["V"], binding.M2RNN_BF16) > 0
     inp = make_workload(name)
@@ -774,7 +775,7 @@ def run_only(args, dist):
     w = WORKLOADS[args.only]
     inp = make_workload(args.only)
     d = binding.to_device(inp, dev)
-    ck = CKPT_EVERY if w["backward"] else 0
+    ck = (CKPT_EVERY_MV if w["V"] == 16 else (CKPT_EVERY_K128 if w["V"] == 128 else CKPT_EVERY)) if w["backward"] else 0
     # Training workloads run as the benchmark step does: with the Z stash where the shape has one.
     stash = w["backward"] and binding.m2rnn_z_stash_size(w["B"], w["T"], w["N"], w["K"], w["V"],
                                                          binding.M2RNN_BF16 if w["dtype"] == "bf16"

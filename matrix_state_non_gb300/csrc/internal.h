@@ -121,6 +121,11 @@ bool tc_backward_supported(int K, int V);
 int tc_backward_parts(int K, int V);
 size_t tc_backward_scratch_bytes(int B, int N, int K, int V, int ckpt_every);
 cudaError_t launch_tc_backward(const BwdArgs& a, cudaStream_t s);
+// K = V = 128 with chunks of at most 16 steps: every product on tcgen05
+// (launch_tc_backward routes there).
+bool tc_backward128_supported(int K, int V, int ckpt_every);
+size_t tc_backward128_scratch_bytes(int B, int N, int ckpt_every);
+cudaError_t launch_tc_backward128(const BwdArgs& a, cudaStream_t s);
 
 // Gate backward: grad holds df on entry, da on exit; part holds
 // 2 * N * gate_backward_parts(BT) floats of scratch.

@@ -530,12 +530,15 @@ int tc_backward_parts(int, int) { return 1; }
 // The chunk cache (fp16 Z_t and H_{t-1} of every step of a chunk) and the
 // state gradient kept aside during each rerun, per chain.
 size_t tc_backward_scratch_bytes(int B, int N, int K, int V, int ckpt_every) {
+  if (tc_backward128_supported(K, V, ckpt_every)) return tc_backward128_scratch_bytes(B, N, ckpt_every);
   const size_t chains = static_cast<size_t>(B) * N;
   return chains * static_cast<size_t>(ckpt_every) * K * V * 4 + chains * static_cast<size_t>(K) * V * 4;
 }
 
 cudaError_t launch_tc_backward(const BwdArgs& a, cudaStream_t s) {
   if (!tc_backward_supported(a.K, a.V) || a.dtype != M2RNN_BF16) return cudaErrorInvalidValue;
+  // K = 128 with chunks of at most 16 steps: the all-tcgen05 kernel.
+  if (tc_backward128_supported(a.K, a.V, a.ckpt_every)) return launch_tc_backward128(a, s);
   return a.clip > 0.f ? launch_t<true>(a, s) : launch_t<false>(a, s);
 }
 

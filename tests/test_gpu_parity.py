@@ -204,11 +204,17 @@ def test_backward_full_size_sampled_head(n):
     (1, 1, 5, 64, 128, 1, False, True),      # one-step chunks
     (1, 2, 1, 128, 128, 16, False, True),    # a single step
     (8, 16, 24, 128, 128, 16, True, True),   # the wide-head workload's grid (B=8, 16 heads), short T
+    (2, 2, 45, 128, 128, 8, True, True),     # K = 128, C <= 16: the all-tcgen05 kernel, ragged last chunk
+    (1, 3, 17, 128, 128, 1, True, True),     # one-step chunks (every step a rerun and a walk)
+    (2, 1, 64, 128, 128, 12, False, True),   # checkpoints recomputed by the caller layer, 12-step chunks
+    (1, 2, 96, 128, 128, 16, True, False),   # the longest chunks, no dH_T
 ])
 def test_backward_v128_tensor_core(B, N, T, K, V, C, reuse, with_dH):
-    """The V = 128 backward (warp-MMA chain, tcgen05 dW) against the oracle
-    (it takes every K % 16 == 0; the forward that writes the checkpoints is
-    the tcgen05 kernel for K = 32, 64, 128 and the SIMT kernel otherwise)."""
+    """The V = 128 backward against the oracle: K = 128 with chunks of at
+    most 16 steps runs every product on tcgen05; other K, or longer chunks,
+    run the warp-MMA chain with the tcgen05 dW (it takes every K % 16 == 0;
+    the forward that writes the checkpoints is the tcgen05 kernel for K =
+    32, 64, 128 and the SIMT kernel otherwise)."""
     inp = make_inputs(B, N, T, K, V, "bf16", seed=500 + T + K, with_dy=True)
     dH = np.random.default_rng(9).standard_normal((B, N, K, V)).astype(np.float32) if with_dH else None
     got = gpu_backward(inp, dH_T=dH, ckpt_every=C, use_fwd_ckpt=reuse)
@@ -218,13 +224,13 @@ def test_backward_v128_tensor_core(B, N, T, K, V, C, reuse, with_dH):
 
 def test_backward_v128_full_size_sampled_head():
     """The wide-head training workload as the benchmark runs it (B=8, 16
-    heads, T=1024, K=V=128: tcgen05 forward writing checkpoints every 28
-    steps, then the V = 128 backward): one head's gradients over every batch
-    element against the oracle."""
+    heads, T=1024, K=V=128: tcgen05 forward writing checkpoints every 8
+    steps, then the all-tcgen05 V = 128 backward): one head's gradients over
+    every batch element against the oracle."""
     name = "fwdbwd_bf16_k128"
     inp = make_workload(name)
     n = 5
-    got = gpu_backward(inp, ckpt_every=28, use_fwd_ckpt=True)
+    got = gpu_backward(inp, ckpt_every=8, use_fwd_ckpt=True)
     ref = oracle_backward(*oracle_args(inp, slice(None), slice(n, n + 1)),
                           inp.exact["dy"][:, :, n:n + 1])
     sub = {"dq": got["dq"][:, :, n:n + 1], "dk": got["dk"][:, :, n:n + 1],
