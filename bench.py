@@ -50,7 +50,7 @@ FWD_EXTRA = ("fwd_bf16_k64", "fwd_bf16_k128", "fwd_bf16_16k", "mv_bf16_k64v16")
 IN_NAMES = ("q", "k", "v", "f", "W", "w_r")
 GRADS = ("dq", "dk", "dv", "df", "dW", "dw_r")
 CKPT_EVERY = 20  # chunk length of the V = 64 backward rebuild (its longest: shared-memory bound)
-CKPT_EVERY_MV = 32  # the V = 16 backward's longest chunk (fewest chunk hand-offs)
+CKPT_EVERY_MV = 20  # the V = 16 pipelined backward's longest chunk (its TMEM chunk cache is double-buffered)
 CKPT_EVERY_K128 = 8  # the K = V = 128 backward: its chunk cache (64 KB per step and chain) stays in L2
 FLUSH_BYTES = 256 << 20  # larger than the 129 MB L2
 
@@ -602,7 +602,7 @@ def time_fwdbwd(name, binding, dev, stream, flush, pk, dist, reps=3):
         (pk["hbm_gbs"] * 1e9)
     del d, fo, bo
     kern = {16: "warp-mma (V = 16 register kernels)", 64: "tcgen05 forward, warp-mma chain + tcgen05 dW backward",
-            128: "tcgen05 forward, warp-mma chain + tcgen05 dW backward"}.get(w["V"], "?")
+            128: "tcgen05 forward, tcgen05 backward (chain, dW, dk, dv, dq)"}.get(w["V"], "?")
     return {"workload": w["desc"] + (", Z stash" if stash else "") + f", checkpoints every {C}",
             "kernel": kern, "ms": t,
             "value": dist.world * units(w) / (t * 1e-3), "unit": UNIT,

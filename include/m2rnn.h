@@ -34,10 +34,12 @@
  *    with the forward on tcgen05 and the backward on warp MMAs
  *    (ckpt_every <= 20, its dW and its dk, dv on tensor cores), V = 16 on register-resident
  *    warp-MMA scans (the backward for ckpt_every <= 32, <= 16 with
- *    K > 64), V = 128: the forward (K in
- *    {32, 64, 128}) on tcgen05, the backward (any ckpt_every) on warp MMAs
- *    with its dW on tcgen05.  Every other supported shape runs on the fp32
- *    CUDA-core kernels.  Nothing runs on the host CPU.
+ *    K > 64), V = 128: the forward (K in {32, 64, 128}) on tcgen05, the
+ *    backward with K = 128 and ckpt_every <= 16 on tcgen05 (every product:
+ *    the state-gradient chain, dW, dk, dv, dq), with other K or longer
+ *    chunks on warp MMAs with its dW on tcgen05.  Every other supported
+ *    shape runs on the fp32 CUDA-core kernels.  Nothing runs on the host
+ *    CPU.
  */
 #ifndef M2RNN_H_
 #define M2RNN_H_

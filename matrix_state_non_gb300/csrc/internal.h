@@ -108,6 +108,11 @@ cudaError_t launch_mv_forward(const FwdArgs& a, cudaStream_t s);
 // Register-resident backward for V = 16 (chunks of up to 32 steps, 16 with K > 64).
 bool mv_backward_supported(int K, int V, int ckpt_every);
 cudaError_t launch_mv_backward(const BwdArgs& a, cudaStream_t s);
+// The pipelined V = 16 backward (rebuild and chain warps per row block);
+// launch_mv_backward runs it where it applies (chunks of up to 20 steps for
+// K <= 64, 10 for K <= 128).
+bool mv_backward_pipe_supported(int K, int V, int ckpt_every);
+cudaError_t launch_mv_backward_pipe(const BwdArgs& a, cudaStream_t s);
 
 bool mma_backward_supported(int K, int V);
 size_t mma_backward_scratch_bytes(int B, int T, int N, int K, int V, int ckpt_every);

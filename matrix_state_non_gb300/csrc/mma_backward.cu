@@ -111,30 +111,6 @@ __device__ __forceinline__ uint32_t cm_ldsm_at(uint32_t tile, int mt, int lane) 
 
 __device__ __forceinline__ float2 splat2(float x) { return make_float2(x, x); }
 
-// x split into bf16 hi + lo (x - hi - lo is below 2^-16 |x|), as a bf16 pair
-// {hi, lo} (hi in the low half).
-__device__ __forceinline__ uint32_t bf16_hilo(float x) {
-  const uint32_t hb = pack_bf16x2(x, 0.f) & 0xFFFFu;
-  const float lo = x - __uint_as_float(hb << 16);
-  return hb | (pack_bf16x2(lo, 0.f) << 16);
-}
-
-// Sum over the 32 lanes of x, in every lane, on the tensor core (no shuffles):
-// with A = ones, a B fragment holding {hi, lo} of lane (g, q)'s x at rows 2q,
-// 2q + 1 of column g sums the four lanes of group g (result s_n in column n);
-// lane (g, q) then holds s_2q, s_2q+1, whose hi and lo parts form the B
-// fragment of a second MMA that sums the eight groups.  Products with one are
-// exact and the accumulation is fp32; the order is fixed.
-__device__ __forceinline__ float warp_sum_mma(float x) {
-  const uint32_t ones[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};
-  float d[4] = {0.f, 0.f, 0.f, 0.f};
-  mma_bf16_16816(d, ones, bf16_hilo(x), 0u);
-  const uint32_t h0 = bf16_hilo(d[0]), h1 = bf16_hilo(d[1]);
-  float e[4] = {0.f, 0.f, 0.f, 0.f};
-  mma_bf16_16816(e, ones, (h0 & 0xFFFFu) | (h1 << 16), (h0 >> 16) | (h1 & 0xFFFF0000u));
-  return e[0];
-}
-
 struct MmaBwdParams {
   BwdArgs a;
   int R;

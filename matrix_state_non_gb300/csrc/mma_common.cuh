@@ -28,6 +28,16 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// D = A * B with a zero accumulator input.
+__device__ __forceinline__ void mma_bf16_16816_zc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                                  uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
+}
+
 // The same with fp16 operands (A and B both fp16).
 __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                               uint32_t b1) {
@@ -36,6 +46,30 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// x split into bf16 hi + lo (x - hi - lo is below 2^-16 |x|), as a bf16 pair
+// {hi, lo} (hi in the low half).
+__device__ __forceinline__ uint32_t bf16_hilo(float x) {
+  const uint32_t hb = pack_bf16x2(x, 0.f) & 0xFFFFu;
+  const float lo = x - __uint_as_float(hb << 16);
+  return hb | (pack_bf16x2(lo, 0.f) << 16);
+}
+
+// Sum over the 32 lanes of x, in every lane, on the tensor core (no shuffles):
+// with A = ones, a B fragment holding {hi, lo} of lane (g, q)'s x at rows 2q,
+// 2q + 1 of column g sums the four lanes of group g (result s_n in column n);
+// lane (g, q) then holds s_2q, s_2q+1, whose hi and lo parts form the B
+// fragment of a second MMA that sums the eight groups.  Products with one are
+// exact and the accumulation is fp32; the order is fixed.
+__device__ __forceinline__ float warp_sum_mma(float x) {
+  const uint32_t ones[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};
+  float d[4] = {0.f, 0.f, 0.f, 0.f};
+  mma_bf16_16816(d, ones, bf16_hilo(x), 0u);
+  const uint32_t h0 = bf16_hilo(d[0]), h1 = bf16_hilo(d[1]);
+  float e[4] = {0.f, 0.f, 0.f, 0.f};
+  mma_bf16_16816(e, ones, (h0 & 0xFFFFu) | (h1 << 16), (h0 >> 16) | (h1 & 0xFFFF0000u));
+  return e[0];
 }
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
@@ -128,6 +162,10 @@ __device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
 }
 __device__ __forceinline__ void st_shared_f32x2(uint32_t addr, float2 v) {
   asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y) : "memory");
+}
+__device__ __forceinline__ void st_shared_f32x4(uint32_t addr, float4 v) {
+  asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
 }
 
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {

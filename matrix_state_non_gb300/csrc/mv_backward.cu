@@ -447,6 +447,7 @@ bool mv_backward_supported(int K, int V, int ckpt_every) {
 
 cudaError_t launch_mv_backward(const BwdArgs& a, cudaStream_t stream) {
   if (!mv_backward_supported(a.K, a.V, a.ckpt_every)) return cudaErrorInvalidValue;
+  if (mv_backward_pipe_supported(a.K, a.V, a.ckpt_every)) return launch_mv_backward_pipe(a, stream);
   MvBwdParams p{};
   p.a = a;
   p.R = a.K / kRows;

@@ -101,10 +101,15 @@ def test_forward_v16_register_kernel(shared, B, N, T, K):
 
 @pytest.mark.parametrize("shared", [True, False])
 @pytest.mark.parametrize("B,N,T,K,C", [(2, 4, 45, 64, 8), (1, 3, 70, 16, 32), (1, 2, 33, 128, 16),
-                                       (1, 2, 5, 64, 1), (2, 2, 64, 32, 13)])
+                                       (1, 2, 5, 64, 1), (2, 2, 64, 32, 13), (2, 2, 61, 64, 20),
+                                       (1, 2, 50, 48, 20), (1, 2, 40, 128, 10), (1, 2, 57, 96, 7),
+                                       (1, 2, 90, 64, 25)])
 def test_backward_v16_register_kernel(shared, B, N, T, K, C):
     """The V = 16 register-resident backward (bf16): every gradient and dH_0
-    from a non-zero initial state, several chunks and a ragged first chunk."""
+    from a non-zero initial state, several chunks and a ragged first chunk.
+    Chunks of up to 20 steps (10 with K > 64) run the pipelined kernel
+    (rebuild and chain warps per row block), longer ones the single-warp
+    kernel: both are covered."""
     V = 16
     maker = shared_inputs if shared else (lambda *a, **kw: make_inputs(*a, **kw))
     inp = maker(B, N, T, K, V, "bf16", seed=460 + T + K + C, with_dy=True)
