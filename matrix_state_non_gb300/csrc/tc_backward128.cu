@@ -349,7 +349,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_backward128_kernel(const __gri
       }
       if (!ok) break;
       // H_{L-1} (after the chunk's last step) as the bf16 H tile that the
-      // reverse walk's first dq product reads (parity L & 1).
+      // reverse walk's first dq product reads (parity L & 1).  That product
+      // is issued in group 0's turn, which no hand-over of group 1 precedes
+      // in this chunk: group 1 signals its tile on hready (one arrival more
+      // than its rerun steps) and the MMA warp waits for it.
       {
         uint8_t* ht = smem + kHT + ((L & 1) * 2 + g) * kTileBytes;
 #pragma unroll
@@ -358,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_backward128_kernel(const __gri
               make_uint4(pack2_bf16(h[8 * r8], h[8 * r8 + 1]), pack2_bf16(h[8 * r8 + 2], h[8 * r8 + 3]),
                          pack2_bf16(h[8 * r8 + 4], h[8 * r8 + 5]), pack2_bf16(h[8 * r8 + 6], h[8 * r8 + 7]));
       }
+      if (g == 1) hand_over(hbar);
 
       // ---------------- reverse walk over the chunk ----------------
       // The next chunk's start state (its group's 64 rows, 32 KB) into L2.
@@ -574,6 +578,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_backward128_kernel(const __gri
       }
       // reverse
       for (int s = L - 1; s >= 0 && ok; --s, ++rs) {
+        // Group 1's H_{L-1} tile is written (read by the first step's dq
+        // product in group 0's turn; group 0's own is ordered by its hand-over).
+        if (s == L - 1) {
+          if (!mbar_wait(smem_u32(&hready[1]), (hph >> 1) & 1u, abort_flag, status, kWhereBwdTReady)) {
+            ok = false;
+            break;
+          }
+          hph ^= 2u;
+        }
         const int par = s & 1;
         const uint32_t sb = tmem_base + kSmall + 48u * static_cast<uint32_t>(rs & 1);
         for (int g = 0; g < 2; ++g) {
