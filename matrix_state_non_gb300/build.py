@@ -19,7 +19,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libm2rnn.so")
 SOURCES = ["api.cu", "simt.cu", "tc_forward.cu", "tc_backward.cu", "tc_backward128.cu", "mma_forward.cu",
            "mma_backward.cu", "host_util.cu", "noalloc.cu", "decode.cu",
-           "mv_forward.cu", "mv_backward.cu", "mv_backward_pipe.cu", "gate_norm.cu"]
+           "mv_forward.cu", "mv_backward.cu", "mv_backward_pipe.cu", "mv_forward_pipe.cu", "gate_norm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include")]

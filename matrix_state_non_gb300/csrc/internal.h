@@ -103,6 +103,10 @@ cudaError_t launch_sum_qk_heads(const float* dq_heads, const float* dk_heads, fl
 
 // Register-resident forward for V = 16 (one warp per 16 key rows, no exchange).
 bool mv_forward_supported(int K, int V);
+// The pipelined V = 16 forward (compute and readout warps per row block), for
+// K <= 64 with the readout y requested; launch_mv_forward runs it there.
+bool mv_forward_pipe_supported(int K, int V, bool readout);
+cudaError_t launch_mv_forward_pipe(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_mv_forward(const FwdArgs& a, cudaStream_t s);
 
 // Register-resident backward for V = 16 (chunks of up to 32 steps, 16 with K > 64).

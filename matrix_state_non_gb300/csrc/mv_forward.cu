@@ -300,6 +300,7 @@ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 bool mv_forward_supported(int K, int V) { return V == kV && K % kRows == 0 && K >= kRows && K <= kRows * kMaxRB; }
 
 cudaError_t launch_mv_forward(const FwdArgs& a, cudaStream_t stream) {
+  if (mv_forward_pipe_supported(a.K, a.V, a.y != nullptr)) return launch_mv_forward_pipe(a, stream);
   MvFwdParams p{};
   p.a = a;
   p.R = a.K / kRows;

@@ -119,3 +119,20 @@ def test_backward_v16_register_kernel(shared, B, N, T, K, C):
     got = gpu_backward(inp, dH_T=dH, ckpt_every=C, use_fwd_ckpt=(C % 2 == 0), H_0=H0, want_dH0=True)
     ref = oracle_backward(*oracle_args(inp), inp.exact["dy"], dH.astype(np.float64), H_0=H0.astype(np.float64))
     check_grads(got, ref, "bf16", label=(shared, B, N, T, K, C))
+
+
+def test_forward_v16_full_size_sampled_heads():
+    """The V = 16 forward at the benchmark's size (B=4, 16 heads, T=4096,
+    K=64, one q/k shared by the heads; the pipelined compute/readout kernel):
+    y and H_T of sampled heads against the oracle."""
+    from matrix_state_non_gb300.inputs import WORKLOADS, make_workload
+    name = "mv_bf16_k64v16"
+    w = WORKLOADS[name]
+    inp = make_workload(name)
+    got = gpu_forward(inp, ckpt_every=20)
+    e = inp.exact
+    for b, n in [(0, 0), (w["B"] - 1, w["N"] - 1), (1, 7)]:
+        y_ref, H_ref = oracle_forward(e["q"][b:b + 1], e["k"][b:b + 1], e["v"][b:b + 1, :, n:n + 1],
+                                      e["f"][b:b + 1, :, n:n + 1], e["W"][n:n + 1], e["w_r"][n:n + 1])
+        sub = {"y": got["y"][b:b + 1, :, n:n + 1], "H_T": got["H_T"][b:b + 1, n:n + 1]}
+        check_forward(sub, y_ref, H_ref, "bf16", label=(name, b, n))
