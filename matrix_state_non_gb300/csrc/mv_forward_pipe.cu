@@ -143,19 +143,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tt = th + static_cast<uint32_t>(hb * kS * kHCols);
       const int t0 = tile * kS;
       const int nsteps = min(kS, T - t0);
+      // The step's k (rows g, g + 8), v (columns 2qd.., 8 + 2qd..) and f,
+      // loaded one step ahead (the tile's last step reloads itself).
+      uint32_t kr0, kr1, vq0, vq1;
+      float fo;
+#define MV_FWD_LOAD_OPS(s_, kr0_, kr1_, vq0_, vq1_, fo_)          \
+  {                                                               \
+    const uint32_t krow = ks + 2 * ((s_) * K + 16 * w + g);       \
+    kr0_ = ld_shared_u16(krow);                                   \
+    kr1_ = ld_shared_u16(krow + 16);                              \
+    vq0_ = ld_shared_b32(vs + 2 * ((s_) * kV + 2 * qd));          \
+    vq1_ = ld_shared_b32(vs + 2 * ((s_) * kV + 8 + 2 * qd));      \
+    fo_ = ld_shared_f32(fs + 4 * (s_));                           \
+  }
+      MV_FWD_LOAD_OPS(0, kr0, kr1, vq0, vq1, fo)
       // Steps run in segments that end where a checkpoint is due.
       for (int s = 0; s < nsteps;) {
         const int seg_end = kCk ? min(nsteps, s + ck_left) : nsteps;
         const int seg_len = seg_end - s;
+#pragma unroll 2
         for (; s < seg_end; ++s) {
-          const uint32_t krow = ks + 2 * (s * K + 16 * w + g);
-          const float k0 = bf16_bits_to_f32(ld_shared_u16(krow));
-          const float k1 = bf16_bits_to_f32(ld_shared_u16(krow + 16));
-          const float omf = 1.f - ld_shared_f32(fs + 4 * s);
+          const int sn = s + 1 < nsteps ? s + 1 : s;
+          uint32_t nkr0, nkr1, nvq0, nvq1;
+          float nfo;
+          MV_FWD_LOAD_OPS(sn, nkr0, nkr1, nvq0, nvq1, nfo)
+          const float k0 = bf16_bits_to_f32(static_cast<uint16_t>(kr0));
+          const float k1 = bf16_bits_to_f32(static_cast<uint16_t>(kr1));
+          const float omf = 1.f - fo;
           float acc[2][4];
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
-            const uint32_t vv = ld_shared_b32(vs + 2 * (s * kV + 8 * nt + 2 * qd));
+            const uint32_t vv = nt == 0 ? vq0 : vq1;
             const float v0 = bf16lo(vv), v1 = bf16hi(vv);
             acc[nt][0] = k0 * v0;  // exact: products of bf16 values fit in fp32
             acc[nt][1] = k0 * v1;
@@ -182,6 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             st_global_cs_v4(zst + static_cast<int64_t>(t0 + s) * R * 512,
                             make_uint4(pack2_f16(zv[0][0], zv[0][1]), pack2_f16(zv[0][2], zv[0][3]),
                                        pack2_f16(zv[1][0], zv[1][1]), pack2_f16(zv[1][2], zv[1][3])));
+          kr0 = nkr0; kr1 = nkr1; vq0 = nvq0; vq1 = nvq1; fo = nfo;
         }
         if constexpr (kCk) {
           ck_left -= seg_len;
@@ -199,6 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+#undef MV_FWD_LOAD_OPS
       tmem_st_wait();
       tc_fence_before_sync();
       __syncwarp();
@@ -238,10 +258,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t hr[8];
         tmem_ld_32x32b<8>(tt, hr);
         float yprev[4] = {0.f, 0.f, 0.f, 0.f};  // the previous step's share (stored one step late)
+        // q of the block's rows 2qd.. and 2qd+8.. as bf16 pairs (A[m][k] =
+        // q[k] for every m), loaded one step ahead.
+        uint32_t qlo = ld_shared_b32(qs + 2 * (16 * w + 2 * qd));
+        uint32_t qhi = ld_shared_b32(qs + 2 * (16 * w + 2 * qd + 8));
+#pragma unroll 2
         for (int s = 0; s < nsteps; ++s) {
-          // q of the block's rows 2qd.. and 2qd+8.. as bf16 pairs (A[m][k] = q[k] for every m).
-          const uint32_t qlo = ld_shared_b32(qs + 2 * (s * K + 16 * w + 2 * qd));
-          const uint32_t qhi = ld_shared_b32(qs + 2 * (s * K + 16 * w + 2 * qd + 8));
+          const int sn = s + 1 < nsteps ? s + 1 : s;
+          const uint32_t nqlo = ld_shared_b32(qs + 2 * (sn * K + 16 * w + 2 * qd));
+          const uint32_t nqhi = ld_shared_b32(qs + 2 * (sn * K + 16 * w + 2 * qd + 8));
           tmem_ld_wait();
           tmem_ld_fence_regs(hr);
           float hh[8];
@@ -271,6 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           yprev[1] = yd[0][1];
           yprev[2] = yd[1][0];
           yprev[3] = yd[1][1];
+          qlo = nqlo;
+          qhi = nqhi;
         }
         if (g == 0 && nsteps > 0) {
           float* dst = yp + ((nsteps - 1) * R + w) * kV + 2 * qd;
