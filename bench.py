@@ -601,7 +601,7 @@ def time_fwdbwd(name, binding, dev, stream, flush, pk, dist, reps=3):
     t_hbm = (io_bytes_fwd(w) + io_bytes_bwd(w, ckpt_every=C) + (2 * stash_bytes(w) if stash else 0)) / \
         (pk["hbm_gbs"] * 1e9)
     del d, fo, bo
-    kern = {16: "warp-mma (V = 16: register forward, pipelined rebuild/chain backward)", 64: "tcgen05 forward, warp-mma chain + tcgen05 dW backward",
+    kern = {16: "warp-mma (V = 16: compute/readout forward, rebuild/chain backward)", 64: "tcgen05 forward, warp-mma chain + tcgen05 dW backward",
             128: "tcgen05 forward, tcgen05 backward (chain, dW, dk, dv, dq)"}.get(w["V"], "?")
     return {"workload": w["desc"] + (", Z stash" if stash else "") + f", checkpoints every {C}",
             "kernel": kern, "ms": t,
