@@ -463,11 +463,11 @@ def run_gpu(args, dist):
         for name in FWD_EXTRA:
             fwd_extra[name] = time_forward(name, binding, dev, stream, flush, pk, dist,
                                            reps=max(3, args.steps // 2))
-        # The same long-context workload on the warp-MMA kernel, for
-        # comparison with the tcgen05 kernel the dispatcher picks.
-        with binding.kernel_family("mma"):
-            fwd_extra["fwd_bf16_16k@warp-mma"] = time_forward("fwd_bf16_16k", binding, dev, stream, flush,
-                                                              pk, dist, reps=3)
+        # The same long-context workload on the tcgen05 kernel, for
+        # comparison with the warp-MMA kernel the dispatcher picks.
+        with binding.kernel_family("tcgen05"):
+            fwd_extra["fwd_bf16_16k@tcgen05"] = time_forward("fwd_bf16_16k", binding, dev, stream, flush,
+                                                             pk, dist, reps=3)
         with binding.kernel_family("simt"):  # the multi-value workload on the fp32 kernel, for comparison
             fwd_extra["mv_bf16_k64v16@simt"] = time_forward("mv_bf16_k64v16", binding, dev, stream, flush,
                                                             pk, dist, reps=3)
@@ -508,7 +508,7 @@ def summary_block(w, step_ms, fwd_extra, pk):
     """Compact per-workload figures (ms, ns per step and chain, roofline
     fraction against the burst bf16 peak / HBM copy rate), first in the line."""
     out = {}
-    for name in ("fwd_bf16_k64", "fwd_bf16_k128", "fwd_bf16_16k", "fwd_bf16_16k@warp-mma"):
+    for name in ("fwd_bf16_k64", "fwd_bf16_k128", "fwd_bf16_16k", "fwd_bf16_16k@tcgen05"):
         r = fwd_extra.get(name)
         if r:
             out[name] = {"kernel": r["kernel"], "ms": round(r["ms"], 4),

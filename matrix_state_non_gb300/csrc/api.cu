@@ -59,10 +59,11 @@ int choose_path(int64_t K, int64_t V, int dt) {
     default: break;
   }
   // V = 64: both tensor-core forwards hold ~16 state rows per SM and are
-  // bound by the step latency; the tcgen05 step measured ~2 % shorter
-  // (216 vs 221 ns on the T = 16384 workload).  It also writes the Z stash.
-  if (tc && v == 64) return kPathTc;
-  if (mma) return kPathMma;  // V = 16: the register-resident warp-MMA scan
+  // bound by the step latency; the warp-MMA scan with its readout on
+  // separate warps measured ~9 % shorter (196 vs 216 ns per step on the
+  // T = 16384 workload).  The Z stash is written by the tcgen05 forward (the
+  // caller layer routes stash calls there).
+  if (mma) return kPathMma;  // V = 64 and V = 16: the register-resident warp-MMA scans
   if (tc) return kPathTc;    // wide heads: tensor throughput matters
   return kPathSimt;
 }

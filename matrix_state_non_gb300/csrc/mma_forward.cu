@@ -16,14 +16,16 @@
 // write seeds the accumulator exactly), applies tanh and the gate blend to
 // its 8 fp32 state values per thread, and writes fp16(H_t) to a swizzled
 // shared tile that the four warps read back with ldmatrix after one named
-// barrier.  The readout of step t-1 runs on the tensor core too, while
-// the step-t MMAs are in flight: y^T = q^T H_{t-1} as one m16n8k16 per column
-// tile with q replicated over the A rows and H_{t-1} (fp32, split into bf16
-// high and low parts, transposed into B fragments with movmatrix) as B, so the
-// sum over rows needs no shuffles.  This beats the
-// tcgen05 kernel when only ~16 rows share an SM: a dependent m16n8k16 takes
-// ~21 cycles, while a 4-instruction tcgen05 step costs several hundred cycles
-// from issue to completion (measured on GB300).
+// barrier.  The readout runs on four readout warps, one per compute warp on
+// the same scheduler and tensor-memory lane quadrant: the compute warp leaves
+// H_t (fp32, 8 columns per step) in a double-buffered tile of tensor memory,
+// and the readout warp, one tile of 32 steps behind, forms y^T = q^T H_t as
+// one m16n8k16 per column tile with q replicated over the A rows and H_t
+// (split into bf16 high and low parts, transposed into B fragments with
+// movmatrix) as B, so the sum over rows needs no shuffles; it stores each
+// step's share one step late, so that no step waits for its own MMAs.  A
+// dependent m16n8k16 takes ~21 cycles, while a 4-instruction tcgen05 step
+// costs several hundred cycles from issue to completion (measured on GB300).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -42,10 +44,12 @@ constexpr int kRows = 16;   // key rows per CTA
 constexpr int kS = 32;      // steps per input tile
 constexpr int kNS = 4;      // input stages
 constexpr int kYS = 2;      // readout partial stages
-// Compute warps per CTA: 8 / NT, each owning 8*NT of the 64 value columns
-// (NT n-tiles of 8).  Plus one TMA producer warp and one readout-reducer warp.
+// Warps: 0-3 compute (8 / NT of them, each owning 8*NT of the 64 value
+// columns), 4-7 readout, 8 the TMA producer, 9 the readout reducer.
 template <int NT>
-constexpr int kThreadsFor() { return (8 / NT + 2) * 32; }
+constexpr int kThreadsFor() { return 10 * 32; }
+constexpr int kReadoutWarp0 = 4, kProducerWarp = 8, kReducerWarp = 9;
+constexpr int kHCols = 8;  // tensor-memory columns per step of H_t (fp32, accumulator-fragment order)
 
 struct MmaFwdParams {
   FwdArgs a;
@@ -85,8 +89,12 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
   uint64_t* yfull = empty + kNS;
   uint64_t* ypeer = yfull + kYS;
   uint64_t* yempty = ypeer + kYS;
+  uint64_t* hfull = yempty + kYS;  // [4 compute warps][2 tiles]: a tile's H_t is in tensor memory
+  uint64_t* hempty = hfull + 8;    // [4][2]: it has been read out
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.misc_off);
   volatile int* cabort = reinterpret_cast<volatile int*>(smem + p.misc_off + 4);
+  volatile int* rabort = reinterpret_cast<volatile int*>(smem + p.misc_off + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + p.misc_off + 12);
   const uint32_t abuf0 = smem_u32(smem + p.abuf_off);  // two 2 KB fp16 tiles
 
   if (threadIdx.x == 0) {
@@ -99,13 +107,22 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
       mbar_init(smem_u32(&ypeer[i]), R);
       mbar_init(smem_u32(&yempty[i]), R);
     }
+    for (int i = 0; i < 16; ++i) mbar_init(smem_u32(&hfull[i]), 1);
     *abort_flag = 0;
     *cabort = 0;
+    *rabort = 0;
     fence_mbar_init_cluster();
+  }
+  if (do_y && warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
   }
   for (int e = threadIdx.x; e < 2 * 2048 / 16; e += static_cast<int>(blockDim.x))
     reinterpret_cast<uint4*>(smem + p.abuf_off)[e] = make_uint4(0, 0, 0, 0);  // H_0 = 0
+  tc_fence_before_sync();
   cluster_sync_all();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = do_y ? *tmem_slot : 0u;
 
   if (warp < CW) {
     // ---------------- compute warps ----------------
@@ -140,8 +157,6 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
       for (int c = 0; c < 4; ++c) h[nt][c] = 0.f;
     const int jcol0 = NCOL * w + 2 * qd;
     const int64_t row_g = static_cast<int64_t>(cta_rank) * kRows + g;
-    float q_prev0 = 0.f, q_prev1 = 0.f;
-    uint32_t q_prev_lo = 0u, q_prev_hi = 0u;
     // fp16 H_{t-1} as the MMA operand (see mma_common.cuh).  hh: this warp's
     // own k-tile (accumulator layout = A layout); the exchange tile holds
     // all four k-tiles.
@@ -175,47 +190,25 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
       store_tiles(abuf0);
     }
     int ck_left = p.a.ckpt_every, ck_idx = 0;  // countdown to the next checkpoint (no division per step)
-    int ys_prev = 0, s_prev = 0;
-    bool have_prev = false;
-
-    auto readout = [&](float q0, float q1, int ys, int s) {
-      // y partial over this CTA's 16 rows for the warp's columns (last step only).
-      float part[4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        part[2 * nt + 0] = fmaf(q0, h[nt][0], q1 * h[nt][2]);
-        part[2 * nt + 1] = fmaf(q0, h[nt][1], q1 * h[nt][3]);
-      }
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1)
-#pragma unroll
-        for (int u = 0; u < 4; ++u) part[u] += __shfl_xor_sync(0xffffffffu, part[u], o);
-      if (g == 0) {
-        float* dst = sY + (ys * kS + s) * kV + jcol0;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-          *reinterpret_cast<float2*>(dst + 8 * nt) = make_float2(part[2 * nt], part[2 * nt + 1]);
-      }
-    };
-
+    const uint32_t th = tmem_base + (static_cast<uint32_t>(32 * w) << 16);  // this warp's lane quadrant
     bool ok = true;
     for (int tile = 0; tile < ntiles; ++tile) {
-      const int st = tile % kNS;
-      const int ys = tile % kYS;
+      const int st = tile % kNS, hb = tile & 1;
       bool mine = mbar_wait_timed(smem_u32(&full[st]), (tile / kNS) & 1, status, kWhereFwdFull);
-      if (mine && do_y && tile >= kYS)
-        mine = mbar_wait_timed<true>(smem_u32(&yempty[ys]), ((tile / kYS) - 1) & 1, status, kWhereFwdYEmpty);
+      if (mine && do_y && tile >= 2)  // the tensor-memory tile has been read out
+        mine = mbar_wait(smem_u32(&hempty[2 * w + hb]), ((tile >> 1) - 1) & 1, abort_flag, status, kWhereFwdYEmpty);
       if (!mine) *cabort = 1;
       named_bar_sync(1, CT);
       if (*cabort) {  // every compute warp reads the flag after the same barrier
         ok = false;
         break;
       }
+      tc_fence_after_sync();
       const uint8_t* stage = sStage + st * p.stage_bytes;
-      const uint16_t* qs = reinterpret_cast<const uint16_t*>(stage + p.q_off);
       const uint16_t* ks = reinterpret_cast<const uint16_t*>(stage + p.k_off);
       const uint16_t* vs = reinterpret_cast<const uint16_t*>(stage + p.v_off);
       const float* fs = reinterpret_cast<const float*>(stage + p.f_off);
+      const uint32_t tt = th + static_cast<uint32_t>(hb * kS * kHCols);
       const int nsteps = min(kS, T - tile * kS);
       // Steps run in segments that end where a checkpoint is due, so the
       // step itself carries no checkpoint test.
@@ -246,40 +239,10 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
           for (int i = 0; i < 3; ++i) ldmatrix_x4(af[i], ldsm_addr_a(atile, (w + 1 + i) & 3, lane));
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) mma_f16_16816(acc[nt], hh, bw[nt][0][0], bw[nt][0][1]);
-          // Readout of step t-1 on the tensor core: y^T = q^T H_{t-1} as an
-          // m16n8k16 with q replicated over the 16 A rows and H_{t-1} (fp32,
-          // split into bf16 high and low parts, ~16 bits) as B, transposed from
-          // the accumulator layout with movmatrix.
-          uint32_t rb[2][2][2];
-          float yd[2][4];
-          if (do_y && have_prev) {
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-              const uint32_t hi0 = pack2_bf16(h[nt][0], h[nt][1]);
-              const uint32_t hi1 = pack2_bf16(h[nt][2], h[nt][3]);
-              const uint32_t lo0 = pack2_bf16(h[nt][0] - bf16lo(hi0), h[nt][1] - bf16hi(hi0));
-              const uint32_t lo1 = pack2_bf16(h[nt][2] - bf16lo(hi1), h[nt][3] - bf16hi(hi1));
-              rb[nt][0][0] = movmatrix_trans(hi0);
-              rb[nt][0][1] = movmatrix_trans(hi1);
-              rb[nt][1][0] = movmatrix_trans(lo0);
-              rb[nt][1][1] = movmatrix_trans(lo1);
-              yd[nt][0] = yd[nt][1] = yd[nt][2] = yd[nt][3] = 0.f;
-            }
-          }
 #pragma unroll
           for (int i = 0; i < 3; ++i)
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) mma_f16_16816(acc[nt], af[i], bw[nt][i + 1][0], bw[nt][i + 1][1]);
-          if (do_y && have_prev) {
-            uint32_t qa[4];
-            qa[0] = qa[1] = q_prev_lo;
-            qa[2] = qa[3] = q_prev_hi;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-              mma_bf16_16816(yd[nt], qa, rb[nt][0][0], rb[nt][0][1]);
-              mma_bf16_16816(yd[nt], qa, rb[nt][1][0], rb[nt][1][1]);
-            }
-          }
           // Eq. 10-11 on this thread's 8 state values; fp16 H_t to the other tile.
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
@@ -290,20 +253,13 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
             }
           split();
           store_tiles(abuf0 + ((t + 1) & 1) * 2048);
-          if (do_y && have_prev && g == 0) {
-            float* dst = sY + (ys_prev * kS + s_prev) * kV + jcol0;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-              *reinterpret_cast<float2*>(dst + 8 * nt) = make_float2(yd[nt][0], yd[nt][1]);
+          if constexpr (kY) {  // H_t for the readout warp
+            const uint32_t hv[8] = {__float_as_uint(h[0][0]), __float_as_uint(h[0][1]), __float_as_uint(h[0][2]),
+                                    __float_as_uint(h[0][3]), __float_as_uint(h[1][0]), __float_as_uint(h[1][1]),
+                                    __float_as_uint(h[1][2]), __float_as_uint(h[1][3])};
+            tmem_st_32x32b_x8(tt + kHCols * s, hv);
           }
-          q_prev_lo = *reinterpret_cast<const uint32_t*>(qs + s * kRows + 2 * qd);
-          q_prev_hi = *reinterpret_cast<const uint32_t*>(qs + s * kRows + 2 * qd + 8);
-          const bool prev_was_tile_end = have_prev && s == 0;  // y of the last step of the previous tile
-          have_prev = true;
-          ys_prev = ys;
-          s_prev = s;
           named_bar_sync(1, CT);
-          if (do_y && prev_was_tile_end && threadIdx.x == 0) mbar_arrive(smem_u32(&yfull[(tile + kYS - 1) % kYS]));
         }
         if constexpr (kCk) {
           ck_left -= seg_len;
@@ -322,22 +278,17 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
           }
         }
       }
-      // Every compute warp is past its last read of this stage.
-      if (threadIdx.x == 0) mbar_arrive(smem_u32(&empty[st]));
+      if constexpr (kY) {  // the tile's H_t for the readout warp, which also releases the stage
+        tmem_st_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&hfull[2 * w + hb]));
+      } else {
+        // Every compute warp is past its last read of this stage.
+        if (threadIdx.x == 0) mbar_arrive(smem_u32(&empty[st]));
+      }
     }
     if (ok) {
-      if (do_y && have_prev) {
-        {
-          // q rows g and g+8 from the packed pairs held by lanes with qd = g/2 (and +8).
-          const uint32_t lo = __shfl_sync(0xffffffffu, q_prev_lo, (g >> 1));
-          const uint32_t hi = __shfl_sync(0xffffffffu, q_prev_hi, (g >> 1));
-          q_prev0 = (g & 1) ? bf16hi(lo) : bf16lo(lo);
-          q_prev1 = (g & 1) ? bf16hi(hi) : bf16lo(hi);
-        }
-        readout(q_prev0, q_prev1, ys_prev, s_prev);
-        named_bar_sync(1, CT);
-        if (threadIdx.x == 0) mbar_arrive(smem_u32(&yfull[ys_prev]));
-      }
       if (p.a.H_T != nullptr) {
         float* dst = p.a.H_T + (static_cast<int64_t>(chain) * p.a.K + row_g) * kV + jcol0;
 #pragma unroll
@@ -349,7 +300,88 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
     } else {
       *abort_flag = 1;
     }
-  } else if (warp == CW) {
+  } else if (do_y && warp >= kReadoutWarp0 && warp < kReadoutWarp0 + CW) {
+    // ---------------- readout warps ----------------
+    // y_t share of this CTA's 16 rows for compute warp w's 16 columns, one
+    // tile behind: y^T = q^T H_t with q replicated over the A rows and H_t
+    // (bf16 high and low parts, transposed with movmatrix) as B.
+    const int g = lane >> 2, qd = lane & 3;
+    const int w = warp - kReadoutWarp0;
+    const int jcol0 = NCOL * w + 2 * qd;
+    const uint32_t th = tmem_base + (static_cast<uint32_t>(32 * w) << 16);
+    for (int tile = 0; tile < ntiles; ++tile) {
+      const int st = tile % kNS, ys = tile % kYS, hb = tile & 1;
+      bool mine = mbar_wait(smem_u32(&full[st]), (tile / kNS) & 1, abort_flag, status, kWhereFwdFull) &&
+                  mbar_wait(smem_u32(&hfull[2 * w + hb]), (tile >> 1) & 1, abort_flag, status, kWhereFwdYFull);
+      if (mine && tile >= kYS)
+        mine = mbar_wait<true>(smem_u32(&yempty[ys]), ((tile / kYS) - 1) & 1, abort_flag, status, kWhereFwdYEmpty);
+      if (!mine) *rabort = 1;
+      const uint8_t* stage = sStage + st * p.stage_bytes;
+      const uint32_t qs = smem_u32(stage + p.q_off);
+      const int nsteps = min(kS, T - tile * kS);
+      if (mine) {
+        tc_fence_after_sync();
+        const uint32_t tt = th + static_cast<uint32_t>(hb * kS * kHCols);
+        uint32_t hr[8];
+        tmem_ld_32x32b<8>(tt, hr);
+        float yprev[4] = {0.f, 0.f, 0.f, 0.f};  // the previous step's share (stored one step late)
+        uint32_t qlo = ld_shared_b32(qs + 4 * qd), qhi = ld_shared_b32(qs + 4 * qd + 16);
+#pragma unroll 2
+        for (int s = 0; s < nsteps; ++s) {
+          const int sn = s + 1 < nsteps ? s + 1 : s;
+          // q of the CTA's rows 2qd.. and 2qd+8.. of the next step, as bf16 pairs.
+          const uint32_t nqlo = ld_shared_b32(qs + 2 * (sn * kRows + 2 * qd));
+          const uint32_t nqhi = ld_shared_b32(qs + 2 * (sn * kRows + 2 * qd + 8));
+          tmem_ld_wait();
+          tmem_ld_fence_regs(hr);
+          float hv[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) hv[i] = __uint_as_float(hr[i]);
+          tmem_ld_32x32b<8>(tt + kHCols * sn, hr);
+          const uint32_t qa[4] = {qlo, qlo, qhi, qhi};
+          float yd[2][4];
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            const float* hn = hv + 4 * nt;
+            const uint32_t hi0 = pack2_bf16(hn[0], hn[1]);
+            const uint32_t hi1 = pack2_bf16(hn[2], hn[3]);
+            const uint32_t lo0 = pack2_bf16(hn[0] - bf16lo(hi0), hn[1] - bf16hi(hi0));
+            const uint32_t lo1 = pack2_bf16(hn[2] - bf16lo(hi1), hn[3] - bf16hi(hi1));
+            mma_bf16_16816_zc(yd[nt], qa, movmatrix_trans(hi0), movmatrix_trans(hi1));
+            mma_bf16_16816(yd[nt], qa, movmatrix_trans(lo0), movmatrix_trans(lo1));
+          }
+          if (g == 0 && s > 0) {  // row 0 of the row-replicated result: columns 8nt + 2qd (+1)
+            float* dst = sY + (ys * kS + s - 1) * kV + jcol0;
+            *reinterpret_cast<float2*>(dst) = make_float2(yprev[0], yprev[1]);
+            *reinterpret_cast<float2*>(dst + 8) = make_float2(yprev[2], yprev[3]);
+          }
+          yprev[0] = yd[0][0];
+          yprev[1] = yd[0][1];
+          yprev[2] = yd[1][0];
+          yprev[3] = yd[1][1];
+          qlo = nqlo;
+          qhi = nqhi;
+        }
+        if (g == 0 && nsteps > 0) {
+          float* dst = sY + (ys * kS + nsteps - 1) * kV + jcol0;
+          *reinterpret_cast<float2*>(dst) = make_float2(yprev[0], yprev[1]);
+          *reinterpret_cast<float2*>(dst + 8) = make_float2(yprev[2], yprev[3]);
+        }
+        // The tile's H has been read (the last, repeated load included).
+        tmem_ld_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&hempty[2 * w + hb]));
+      }
+      named_bar_sync(2, CT);  // every readout warp's shares of the tile are written
+      if (*rabort) break;
+      if (threadIdx.x == 32 * kReadoutWarp0) {
+        mbar_arrive(smem_u32(&yfull[ys]));
+        mbar_arrive(smem_u32(&empty[st]));  // compute and readout warps are past the stage
+      }
+    }
+    if (*rabort) *abort_flag = 1;
+  } else if (warp == kProducerWarp) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -391,7 +423,7 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
       for (int tile = std::max(0, issued - kNS); tile < issued; ++tile)
         mbar_wait_timed(smem_u32(&full[tile % kNS]), (tile / kNS) & 1, nullptr, kWhereFwdDrain);
     }
-  } else if (warp == CW + 1 && do_y) {
+  } else if (warp == kReducerWarp && do_y) {
     // ---------------- readout reducer (sum over the chain's row blocks) ----------------
     const uint16_t* vg = static_cast<const uint16_t*>(p.a.v);
     const uint16_t* wr = static_cast<const uint16_t*>(p.a.w_r) + static_cast<int64_t>(n) * kV;
@@ -442,7 +474,12 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
         break;
     }
   }
+  tc_fence_before_sync();
   __syncthreads();
+  if (do_y && warp == 0) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, 512);
+  }
 }
 
 inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
@@ -466,8 +503,8 @@ cudaError_t launch_nt(const FwdArgs& a, cudaStream_t stream) {
   p.stage_bytes = align_up(p.f_off + kS * 4, 128);
   p.y_off = p.stage_off + kNS * p.stage_bytes;
   p.bar_off = p.y_off + kYS * kS * kV * 4;
-  p.misc_off = p.bar_off + (2 * kNS + 3 * kYS) * 8;
-  uint32_t smem = align_up(p.misc_off + 16, 128) + 1024;
+  p.misc_off = p.bar_off + (2 * kNS + 3 * kYS + 16) * 8;
+  uint32_t smem = align_up(p.misc_off + 16, 128) + 1024;  // + the 1 KB alignment slack
   smem = std::max<uint32_t>(smem, 120 * 1024);  // one CTA per SM
   p.tx_bytes = 2 * kS * kRows * 2 + kS * kV * 2;
 

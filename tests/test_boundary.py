@@ -37,7 +37,7 @@ def test_host_helpers(lib):
     assert binding.m2rnn_checkpoint_count(64, 64) == 0
     assert binding.m2rnn_checkpoint_count(0, 4) == -1
     # forward families: tcgen05 for V=64 and V=128 bf16, warp MMA for V=16 bf16, fp32 CUDA cores otherwise
-    assert binding.m2rnn_path(64, 64, binding.M2RNN_BF16) == 1
+    assert binding.m2rnn_path(64, 64, binding.M2RNN_BF16) == 2   # V = 64 forward: the warp-MMA scan
     assert binding.m2rnn_path(128, 128, binding.M2RNN_BF16) == 1
     assert binding.m2rnn_path(64, 16, binding.M2RNN_BF16) == 2
     assert binding.m2rnn_path(16, 16, binding.M2RNN_F32) == 0
@@ -215,7 +215,7 @@ def test_kernel_family_option(lib):
     with binding.kernel_family("mma"):
         assert binding.m2rnn_path(64, 64, binding.M2RNN_BF16) == 2
         assert binding.m2rnn_path(128, 128, binding.M2RNN_BF16) == 1  # no warp-MMA kernel for V=128
-    assert binding.m2rnn_path(64, 64, binding.M2RNN_BF16) == 1      # the automatic choice is back
+    assert binding.m2rnn_path(64, 64, binding.M2RNN_BF16) == 2      # the automatic choice is back
     st, _ = binding.m2rnn_set_option(binding.M2RNN_OPT_KERNEL_FAMILY, 3)
     assert st == binding.M2RNN_ERR_INVALID_ARG
     st, _ = binding.m2rnn_set_option(99, 0)

@@ -250,7 +250,8 @@ def test_backward_is_deterministic():
 
 # ---------------------------------------------------------------------------
 # Every kernel family on the shapes they share (V = 64): the dispatcher picks
-# the tcgen05 forward; M2RNN_KERNEL selects each family explicitly.
+# the warp-MMA forward (the tcgen05 one where the Z stash is written);
+# M2RNN_KERNEL selects each family explicitly.
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("kernel_family", ["mma", "tcgen05", "simt"], indirect=True)
 @pytest.mark.parametrize("B,N,T,K,V", [(2, 3, 37, 64, 64), (1, 2, 70, 16, 64), (1, 1, 97, 128, 64),
