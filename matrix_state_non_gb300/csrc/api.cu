@@ -61,8 +61,7 @@ int choose_path(int64_t K, int64_t V, int dt) {
   // V = 64: both tensor-core forwards hold ~16 state rows per SM and are
   // bound by the step latency; the warp-MMA scan with its readout on
   // separate warps measured ~9 % shorter (196 vs 216 ns per step on the
-  // T = 16384 workload).  The Z stash is written by the tcgen05 forward (the
-  // caller layer routes stash calls there).
+  // T = 16384 workload).  It also writes the Z stash.
   if (mma) return kPathMma;  // V = 64 and V = 16: the register-resident warp-MMA scans
   if (tc) return kPathTc;    // wide heads: tensor throughput matters
   return kPathSimt;
@@ -213,7 +212,7 @@ int forward_impl(const void* q, const void* k, const void* v, const GateIn& gate
   if (z_stash != nullptr) {
     if (!stash_ok(K, V, dtype)) return M2RNN_ERR_UNSUPPORTED;
     if (!aligned16(z_stash)) return M2RNN_ERR_INVALID_ARG;
-    path = (V == 64) ? kPathTc : kPathMma;  // the kernels that write the stash: tcgen05 (V = 64), warp MMA (V = 16)
+    path = kPathMma;  // the kernels that write the stash: the warp-MMA forwards (V = 64, V = 16)
   }
   const void* req[] = {q, k, v, W, w_r, y};
   for (const void* p : req)

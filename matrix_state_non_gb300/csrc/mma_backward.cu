@@ -489,13 +489,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (zs) issue_z(zissued++);
       publish_chunk(0, issue_chunk(0));
     }
-    // The stash step (2 KB: 16 bytes = Z[8c .. 8c+7][j] at (c * 64 + j) * 16)
-    // read with one ldmatrix.x4.trans: matrix i covers row run i & 1 and the
-    // columns 16w + 8 (i >> 1) .. + 7 (one 16-byte stash row per column), so
-    // thread (g, qd) receives {Z[8c + g][j], Z[8c + g][j + 1]}, j = 16w + 8nt
-    // + 2qd, in the order (nt 0, row g), (0, g+8), (1, g), (1, g+8).
-    const uint32_t zaddr = smem_u32(smem + p.zbuf_off) +
-                           static_cast<uint32_t>(((lane >> 3) & 1) * kV + 16 * w + 8 * (lane >> 4) + (lane & 7)) * 16;
+    // The stash step (2 KB) holds, at (32 w + lane) * 16, the 16 bytes that
+    // the forward's compute warp w, lane `lane`, wrote: {Z[g][j], Z[g][j+1]},
+    // j = 16w + 8nt + 2qd, in the order (nt 0, row g), (0, g+8), (1, g),
+    // (1, g+8) -- exactly this thread's values.
+    const uint32_t zaddr = smem_u32(smem + p.zbuf_off) + static_cast<uint32_t>((32 * w + lane) * 16);
     bool ok = true;
     int issued = 1;  // chunks whose loads have been issued
     for (int ci = 0; ci < p.nchunks; ++ci) {
@@ -566,8 +564,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (zs) {
         for (int s = 0; s < L; ++s) {
           const float omf = 1.f - ld_shared_f32(sf + 4 * s);
-          uint32_t zq[4];
-          ldmatrix_x4_trans(zq, zaddr + s * kZStepBytes);
+          const uint4 zv4 = ld_shared_v4(zaddr + s * kZStepBytes);
+          const uint32_t zq[4] = {zv4.x, zv4.y, zv4.z, zv4.w};
           float2 z[2][2];
 #pragma unroll
           for (int i = 0; i < 4; ++i) z[i >> 1][i & 1] = f16x2_to_float2(zq[i]);

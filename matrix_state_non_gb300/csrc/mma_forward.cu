@@ -61,8 +61,13 @@ struct MmaFwdParams {
 };
 
 // Compile-time modes (a per-step branch costs ~20-30 ns of a ~250 ns step,
-// measured): kY = readout y, kCk = checkpoints.
-template <int NT, bool kY, bool kCk>
+// measured): kY = readout y, kCk = checkpoints, kZ = the Z stash for the
+// backward.  The V = 64 stash: per (chain, row block) and step 2 KB, compute
+// warp w's lane L writing its 16 bytes at (32 w + L) * 16, its fp16 Z values
+// in accumulator-fragment order (column block 0, row g), (0, g+8), (1, g),
+// (1, g+8) -- the order in which the backward's recompute warps hold them --
+// so a chunk of steps is one contiguous range.
+template <int NT, bool kY, bool kCk, bool kZ>
 __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
     mma_forward_kernel(const __grid_constant__ MmaFwdParams p, const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
@@ -191,6 +196,9 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
     }
     int ck_left = p.a.ckpt_every, ck_idx = 0;  // countdown to the next checkpoint (no division per step)
     const uint32_t th = tmem_base + (static_cast<uint32_t>(32 * w) << 16);  // this warp's lane quadrant
+    uint8_t* const zst = !kZ ? nullptr
+                             : reinterpret_cast<uint8_t*>(p.a.zstash) +
+                                   (static_cast<int64_t>(chain) * R + cta_rank) * T * kZStepBytes + (32 * w + lane) * 16;
     bool ok = true;
     for (int tile = 0; tile < ntiles; ++tile) {
       const int st = tile % kNS, hb = tile & 1;
@@ -239,20 +247,35 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
           for (int i = 0; i < 3; ++i) ldmatrix_x4(af[i], ldsm_addr_a(atile, (w + 1 + i) & 3, lane));
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) mma_f16_16816(acc[nt], hh, bw[nt][0][0], bw[nt][0][1]);
+          // Two accumulation chains (f16 products, fp32 sums) for the other
+          // three k-tiles: two dependent MMAs after the tile loads, not three.
+          float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-          for (int i = 0; i < 3; ++i)
+          for (int nt = 0; nt < 2; ++nt) {
+            mma_f16_16816(acc[nt], af[0], bw[nt][1][0], bw[nt][1][1]);
+            mma_f16_16816(acc2[nt], af[1], bw[nt][2][0], bw[nt][2][1]);
+          }
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) mma_f16_16816(acc[nt], af[i], bw[nt][i + 1][0], bw[nt][i + 1][1]);
+          for (int nt = 0; nt < 2; ++nt) {
+            mma_f16_16816(acc2[nt], af[2], bw[nt][3][0], bw[nt][3][1]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nt][e] += acc2[nt][e];
+          }
           // Eq. 10-11 on this thread's 8 state values; fp16 H_t to the other tile.
+          float zv[2][4];
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-              const float z = tanh_fast(acc[nt][c]);
-              h[nt][c] = fmaf(omf, z - h[nt][c], h[nt][c]);
+              zv[nt][c] = tanh_fast(acc[nt][c]);
+              h[nt][c] = fmaf(omf, zv[nt][c] - h[nt][c], h[nt][c]);
             }
           split();
           store_tiles(abuf0 + ((t + 1) & 1) * 2048);
+          if constexpr (kZ)  // Z_t for the backward (a streaming store, off the chain)
+            st_global_cs_v4(zst + static_cast<int64_t>(t) * kZStepBytes,
+                            make_uint4(pack2_f16(zv[0][0], zv[0][1]), pack2_f16(zv[0][2], zv[0][3]),
+                                       pack2_f16(zv[1][0], zv[1][1]), pack2_f16(zv[1][2], zv[1][3])));
           if constexpr (kY) {  // H_t for the readout warp
             const uint32_t hv[8] = {__float_as_uint(h[0][0]), __float_as_uint(h[0][1]), __float_as_uint(h[0][2]),
                                     __float_as_uint(h[0][3]), __float_as_uint(h[1][0]), __float_as_uint(h[1][1]),
@@ -484,7 +507,7 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
 
 inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-template <int NT, bool kY, bool kCk>
+template <int NT, bool kY, bool kCk, bool kZ>
 cudaError_t launch_nt(const FwdArgs& a, cudaStream_t stream) {
   MmaFwdParams p{};
   p.a = a;
@@ -515,7 +538,7 @@ cudaError_t launch_nt(const FwdArgs& a, cudaStream_t stream) {
       !make_tensor_map_btnx(&mk, a.k, bf, 2, a.B, a.T, qN, a.K, kRows, kS) ||
       !make_tensor_map_btnx(&mv, a.v, bf, 2, a.B, a.T, a.N, kV, kV, kS))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(mma_forward_kernel<NT, kY, kCk>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(mma_forward_kernel<NT, kY, kCk, kZ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
@@ -530,7 +553,7 @@ cudaError_t launch_nt(const FwdArgs& a, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, mma_forward_kernel<NT, kY, kCk>, p, mq, mk, mv);
+  e = cudaLaunchKernelEx(&cfg, mma_forward_kernel<NT, kY, kCk, kZ>, p, mq, mk, mv);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -544,11 +567,13 @@ bool mma_forward_supported(int K, int V) {
 
 cudaError_t launch_mma_forward(const FwdArgs& a, cudaStream_t stream) {
   if (a.V != kV) return launch_mv_forward(a, stream);
-  // The V = 64 Z stash is the tcgen05 forward's (its layout is the one the backward reads).
-  if (a.zstash != nullptr) return cudaErrorInvalidValue;
   const bool y = a.y != nullptr, ck = a.ckpt != nullptr;
-  if (y) return ck ? launch_nt<2, true, true>(a, stream) : launch_nt<2, true, false>(a, stream);
-  return ck ? launch_nt<2, false, true>(a, stream) : launch_nt<2, false, false>(a, stream);
+  if (a.zstash != nullptr) {  // the training forward: readout, checkpoints and the stash
+    if (y) return ck ? launch_nt<2, true, true, true>(a, stream) : launch_nt<2, true, false, true>(a, stream);
+    return ck ? launch_nt<2, false, true, true>(a, stream) : launch_nt<2, false, false, true>(a, stream);
+  }
+  if (y) return ck ? launch_nt<2, true, true, false>(a, stream) : launch_nt<2, true, false, false>(a, stream);
+  return ck ? launch_nt<2, false, true, false>(a, stream) : launch_nt<2, false, false, false>(a, stream);
 }
 
 }  // namespace m2rnn

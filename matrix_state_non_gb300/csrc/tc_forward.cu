@@ -34,8 +34,7 @@
 // V = 64, measured); warp 4G+1 = TMA producer for q/k/v tiles of S = 32
 // steps (f through plain loads); warp 4G+2 = readout reducer, which sums the
 // per-group/per-CTA partial readouts of a tile (one of them carries w_r * v)
-// and stores y.  Checkpoints are written between segments of steps; at V = 64
-// the kernel can also stream fp16 Z_t (the Z stash) for the backward.  Every
+// and stores y.  Checkpoints are written between segments of steps.  Every
 // wait is bounded (see ptx.cuh).
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -106,10 +105,10 @@ __device__ __forceinline__ void unpack8_bf16(const uint4 w, float (&o)[8]) {
 }
 
 // Compile-time modes, no per-step test: G epilogue warpgroups, kY = readout
-// y, kCk = checkpoints, kZ = the Z stash (V = 64).  (G as a runtime value left the readout reducer's
+// y, kCk = checkpoints.  (G as a runtime value left the readout reducer's
 // loops unrolled too little to keep up: 5.72 against 4.88 ms on the
 // T = 4096, K = V = 128 workload, measured.)
-template <int V, int ROWS, int G, bool kY, bool kCk, bool kZ>
+template <int V, int ROWS, int G, bool kY, bool kCk>
 __global__ void __launch_bounds__((4 * G + 3) * 32, 1)
     tc_forward_kernel(const __grid_constant__ TcFwdParams p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -266,12 +265,6 @@ __global__ void __launch_bounds__((4 * G + 3) * 32, 1)
     const float wrv = (cta_rank == 0 && g == 0 && c == 0)
                           ? bf16_bits_to_f32(static_cast<const uint16_t*>(p.a.w_r)[static_cast<int64_t>(n) * V + j])
                           : 0.f;
-    // Z stash (V = 64): per (chain, row block) and step 2 KB, thread L's 16
-    // bytes at (row run c, column j): Z[8c .. 8c+7][j] as fp16.
-    static_assert(!kZ || (V == 64 && ROWS == 8 && G == 1), "the Z stash layout is the V = 64 one");
-    uint8_t* const zst = !kZ ? nullptr
-                             : reinterpret_cast<uint8_t*>(p.a.zstash) +
-                                   static_cast<int64_t>(chain * R + cta_rank) * T * kZStepBytes + (c * V + j) * 16;
     uint32_t dphase = 0;
     int ck_left = p.a.ckpt_every, ck_idx = 0;  // countdown to the next checkpoint
     bool ok = true;
@@ -317,7 +310,6 @@ __global__ void __launch_bounds__((4 * G + 3) * 32, 1)
           // the MMA is in flight (the product of two bf16 values is exact, so
           // adding it later rounds as a fused multiply-add would).
           float kv[C::FOLD ? 1 : ROWS];
-          float zv[kZ ? ROWS : 1];
           if constexpr (!C::FOLD) {
             const uint16_t* kr = ks + s * NRtot + row_in_cta;
   #pragma unroll
@@ -346,7 +338,6 @@ __global__ void __launch_bounds__((4 * G + 3) * 32, 1)
               float x = __uint_as_float(acc[r0 + u]);
               if constexpr (!C::FOLD) x += kv[r0 + u];
               const float z = tanh_fast(x);                     // Eq. 10
-              if constexpr (kZ) zv[r0 + u] = z;
               h[r0 + u] = fmaf(omf, z - h[r0 + u], h[r0 + u]);  // Eq. 11
             }
             uint4 pk;
@@ -378,10 +369,6 @@ __global__ void __launch_bounds__((4 * G + 3) * 32, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(hbar);
           // ---- off the serial chain ----
-          if constexpr (kZ)  // Z_t of the thread's 8 rows for the backward (a streaming store)
-            st_global_cs_v4(zst + static_cast<int64_t>(t) * kZStepBytes,
-                            make_uint4(pack2_f16(zv[0], zv[1]), pack2_f16(zv[2], zv[3]), pack2_f16(zv[4], zv[5]),
-                                       pack2_f16(zv[6], zv[7])));
           if (do_y) {
             const uint16_t* qr = qs + s * NRtot + row_in_cta;
             float ya = wrv * vj;  // w_r * v_t, carried by one partial of each column (wrv = 0 elsewhere)
@@ -566,7 +553,7 @@ __global__ void __launch_bounds__((4 * G + 3) * 32, 1)
 // ---------------------------------------------------------------------------
 inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-template <int V, int ROWS, int G, bool kY, bool kCk, bool kZ>
+template <int V, int ROWS, int G, bool kY, bool kCk>
 cudaError_t launch_cfg_mode(const FwdArgs& a, int R, cudaStream_t stream) {
   using C = FwdCfg<V, ROWS>;
   TcFwdParams p{};
@@ -604,7 +591,7 @@ cudaError_t launch_cfg_mode(const FwdArgs& a, int R, cudaStream_t stream) {
       !make_tensor_map_btnx(&mv, a.v, bf, 2, a.B, a.T, a.N, V, V, kS))
     return cudaErrorInvalidValue;
 
-  auto kern = tc_forward_kernel<V, ROWS, G, kY, kCk, kZ>;
+  auto kern = tc_forward_kernel<V, ROWS, G, kY, kCk>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if (R > 8) {
@@ -630,21 +617,12 @@ cudaError_t launch_cfg_mode(const FwdArgs& a, int R, cudaStream_t stream) {
 
 template <int V, int ROWS, int G>
 cudaError_t launch_cfg(const FwdArgs& a, int R, cudaStream_t stream) {
+  if (a.zstash != nullptr) return cudaErrorInvalidValue;  // the Z stash is written by the warp-MMA forwards
   const bool y = a.y != nullptr, ck = a.ckpt != nullptr;
-  if constexpr (V == 64) {  // the Z stash of the training step (V = 64 only)
-    if (a.zstash != nullptr) {
-      if (y) return ck ? launch_cfg_mode<V, ROWS, G, true, true, true>(a, R, stream)
-                       : launch_cfg_mode<V, ROWS, G, true, false, true>(a, R, stream);
-      return ck ? launch_cfg_mode<V, ROWS, G, false, true, true>(a, R, stream)
-                : launch_cfg_mode<V, ROWS, G, false, false, true>(a, R, stream);
-    }
-  } else {
-    if (a.zstash != nullptr) return cudaErrorInvalidValue;
-  }
-  if (y) return ck ? launch_cfg_mode<V, ROWS, G, true, true, false>(a, R, stream)
-                   : launch_cfg_mode<V, ROWS, G, true, false, false>(a, R, stream);
-  return ck ? launch_cfg_mode<V, ROWS, G, false, true, false>(a, R, stream)
-            : launch_cfg_mode<V, ROWS, G, false, false, false>(a, R, stream);
+  if (y) return ck ? launch_cfg_mode<V, ROWS, G, true, true>(a, R, stream)
+                   : launch_cfg_mode<V, ROWS, G, true, false>(a, R, stream);
+  return ck ? launch_cfg_mode<V, ROWS, G, false, true>(a, R, stream)
+            : launch_cfg_mode<V, ROWS, G, false, false>(a, R, stream);
 }
 
 }  // namespace

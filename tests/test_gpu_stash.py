@@ -74,15 +74,14 @@ def test_stash_shared_qk_and_gate():
 
 def test_forward_outputs_unchanged_by_the_stash():
     """The stash leaves the outputs of the kernel that writes it (the
-    tcgen05 forward at V = 64) unchanged."""
+    warp-MMA forward at V = 64) unchanged."""
     import torch
     from matrix_state_non_gb300 import binding
     inp = make_inputs(2, 2, 90, 64, 64, "bf16", seed=614)
     d = binding.to_device(inp)
-    with binding.kernel_family("tcgen05"):  # the same kernel with and without the stash
-        assert binding.m2rnn_path(64, 64, binding.M2RNN_BF16) == 1
-        a = binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=14)
-        b = binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=14, stash=True)
+    assert binding.m2rnn_path(64, 64, binding.M2RNN_BF16) == 2  # the same kernel with and without the stash
+    a = binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=14)
+    b = binding.forward(*(d[n] for n in IN_NAMES), ckpt_every=14, stash=True)
     torch.cuda.synchronize()
     for name in ("y", "H_T", "ckpt"):
         assert torch.equal(a[name], b[name]), name
