@@ -498,7 +498,7 @@ def run_gpu(args, dist):
         "gpu_launches": launches_per_step * args.steps,
         "step_breakdown_ms": {"forward": f_avg, "backward": b_avg},
         "forward": fwd_extra,
-        "kernels": {"forward": "tcgen05 (writes the Z stash)",
+        "kernels": {"forward": "warp-mma with readout warps (writes the Z stash)",
                     "backward": "warp-mma chain + tcgen05 dW"},
     }
     return line
@@ -515,7 +515,7 @@ def summary_block(w, step_ms, fwd_extra, pk):
                          "ns_per_step_per_chain": round(r["ns_per_step_per_chain"], 1),
                          "roofline_frac": round(r["roofline_frac"], 4)}
     fl = fwd_flops(w) + bwd_flops(w)
-    out[MAIN] = {"kernel": "tcgen05 fwd + warp-mma/tcgen05 bwd", "ms": round(step_ms, 4),
+    out[MAIN] = {"kernel": "warp-mma fwd + warp-mma/tcgen05 bwd", "ms": round(step_ms, 4),
                  "ns_per_step_per_chain": round(step_ms * 1e6 / w["T"], 1),
                  "roofline_frac": round(fl / (pk["bf16"] * 1e12) / (step_ms * 1e-3), 4)}
     return out
@@ -601,7 +601,7 @@ def time_fwdbwd(name, binding, dev, stream, flush, pk, dist, reps=3):
     t_hbm = (io_bytes_fwd(w) + io_bytes_bwd(w, ckpt_every=C) + (2 * stash_bytes(w) if stash else 0)) / \
         (pk["hbm_gbs"] * 1e9)
     del d, fo, bo
-    kern = {16: "warp-mma (V = 16: compute/readout forward, rebuild/chain backward)", 64: "tcgen05 forward, warp-mma chain + tcgen05 dW backward",
+    kern = {16: "warp-mma (V = 16: compute/readout forward, rebuild/chain backward)", 64: "warp-mma forward (readout warps), warp-mma chain + tcgen05 dW backward",
             128: "tcgen05 forward, tcgen05 backward (chain, dW, dk, dv, dq)"}.get(w["V"], "?")
     return {"workload": w["desc"] + (", Z stash" if stash else "") + f", checkpoints every {C}",
             "kernel": kern, "ms": t,
