@@ -31,8 +31,9 @@
  *    m2rnn_sync_status.
  *  - Supported shapes: B, T, N >= 1; K, V in [1, 128].  bf16 inputs with
  *    K a multiple of 16 (and at most 128) run on tensor-core kernels: V = 64
- *    with the forward on tcgen05 and the backward on warp MMAs
- *    (ckpt_every <= 20, its dW and its dk, dv on tensor cores), V = 16 on register-resident
+ *    with the forward on warp MMAs (tcgen05 on request) and the backward on
+ *    warp MMAs (ckpt_every <= 20, its dW and its dk, dv on tensor cores),
+ *    V = 16 on register-resident
  *    warp-MMA scans (the backward for ckpt_every <= 32, <= 16 with
  *    K > 64), V = 128: the forward (K in {32, 64, 128}) on tcgen05, the
  *    backward with K = 128 and ckpt_every <= 16 on tcgen05 (every product:
