@@ -46,10 +46,12 @@
 //
 // Measured (timing-only copies, B=4 N=8 T=4096): the proxy fence before the
 // reverse warps' hand-off cost 7.5 % of the kernel while it had the H tile and
-// df stores of the same step to drain; with the H tiles written by the
-// recompute warps, and the fence placed after the chain MMAs (the D tile
-// stores completed before the barrier) and before the df store (read only by
-// the generic proxy), it has nothing left to wait for.
+// df stores of the same step to drain.  The H tiles are now written by the
+// recompute warps, and the fence sits right after the exchange barrier (the
+// D tile stores are complete, no ldmatrix or MMA is in flight yet) and
+// before the df store (read only by the generic proxy).  A latency probe of
+// the reverse step alone: fence after the chain MMAs 343 cycles per step,
+// after the barrier 294, none 281.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -81,9 +83,7 @@ constexpr int kNX = 8;            // exchange ring slots, reverse -> gradient wa
 //       warps' dk and dv MMAs (ldmatrix, plain and transposed)
 //   Df  per-thread shares of df = <R, H_{t-1} - Z> over the thread's eight values: [128]
 // The H tile buffer holds, per chunk and step, the bf16 H_{t-1} tile: the A
-// operand of the dW MMA, H_{t-1}^T, whose M = 128 rows run 2 KB past the tile
-// (rows 64..127 of the accumulator take whatever follows and are never read;
-// 2 KB of slack after the buffers keep those reads inside the allocation).
+// operand of the dW MMA, H_{t-1}^T (M = 64).
 // Both bf16 tiles use the canonical no-swizzle core-matrix layout: the 8 x 8
 // block (rows 8i.., columns 8j..) is 128 contiguous bytes at 256 j + 128 i, so
 // as tcgen05 operands (MN-major, the columns contiguous) the core matrices
@@ -337,6 +337,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         st_shared_b32(dt + cm_off(g, jcol0 + 8), aown[2]);
         st_shared_b32(dt + cm_off(g + 8, jcol0 + 8), aown[3]);
         named_bar_sync(1, 128);
+        // The D tile is also read by the tensor core (dW), through the async
+        // proxy: this thread's stores to it completed before the barrier, so
+        // the fence has nothing to wait for here; placed after the chain
+        // MMAs it stalled the step by ~50 cycles (measured).
+        fence_proxy_async_smem();
         uint32_t af[3][4];
 #pragma unroll
         for (int i = 0; i < 3; ++i) ldmatrix_x4(af[i], cm_ldsm_a(dt, (w + 1 + i) & 3, lane));
@@ -351,9 +356,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 3; ++i)
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) mma_bf16_16816(acc[nt], af[i], bt[nt][i + 1][0], bt[nt][i + 1][1]);
-        // The D tile is read by the tensor core (dW): its stores completed
-        // before the barrier, so this proxy fence has nothing to wait for.
-        fence_proxy_async_smem();
         // Off the chain: this thread's share of df = <R, H_{t-1} - Z>, read
         // by the gradient warps through the generic proxy only.
         {
@@ -663,8 +665,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ======================= gradient warps =======================
     // Warp 8 issues the step's dW MMA (one elected lane, tcgen05, the
-    // accumulator in TMEM columns 448..511):
-    //   dW (+)= [H_{t-1}^T ; *] (128 x 16) * D (16 x 64)  (rows 64.. unused),
+    // accumulator in TMEM columns 448..511; with M = 64, row 16q + r sits in
+    // lane 32q + r):
+    //   dW (+)= H_{t-1}^T (64 x 16) * D (16 x 64),
     // committed to the slot's empty barrier.  Every fourth step (rs % 4 == w)
     // warp 8 + w also forms that step's dk and dv partial on the tensor core
     // from the slot's bf16 D tile, sums the df shares (also on the tensor
@@ -677,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int dwr_ppr = (kV / 2 + R - 1) / R;
     const int dwr_pair = cta_rank * dwr_ppr + lane;
     const bool dwr_lane = lane < dwr_ppr && dwr_pair < kV / 2;
-    const uint32_t idesc = idesc_bf16_f32(128, kV, /*a_mn_major=*/true, /*b_mn_major=*/true);
+    const uint32_t idesc = idesc_bf16_f32(64, kV, /*a_mn_major=*/true, /*b_mn_major=*/true);
     const uint32_t dw_tmem = tmem_base + kDWCol;
     bool ok = true;
     int rs = 0, xs = 0;
@@ -794,12 +797,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     }
     if (ok) {
-      // dW partial of this row block from TMEM: accumulator row m = lane 32w + lane
-      // (rows 64..127 are the zero padding), column n = 448 + n.
-      if (w < 2) {
+      // dW partial of this row block from TMEM: accumulator row m = 16w + lane
+      // in lane 32w + lane (lanes 16..31 of each quadrant unused), column
+      // n = 448 + n.
+      {
         if (!mbar_wait_timed(smem_u32(dwdone), 0, status, kWhereBwdDW)) *gabort = 1;
         tc_fence_after_sync();
-        float* dwp = A.dW_part + static_cast<int64_t>(blockIdx.x) * kV * kV + (32 * w + lane) * kV;
+        float* dwp = A.dW_part + static_cast<int64_t>(blockIdx.x) * kV * kV + (16 * w + (lane & 15)) * kV;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t r[32];
@@ -808,7 +812,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_fence_regs(r);
 #pragma unroll
           for (int c4 = 0; c4 < 32; c4 += 4)
-            *reinterpret_cast<float4*>(dwp + 32 * half + c4) =
+            if (lane < 16) *reinterpret_cast<float4*>(dwp + 32 * half + c4) =
                 make_float4(__uint_as_float(r[c4]), __uint_as_float(r[c4 + 1]), __uint_as_float(r[c4 + 2]),
                             __uint_as_float(r[c4 + 3]));
         }
@@ -902,8 +906,8 @@ cudaError_t launch_mma_backward(const BwdArgs& a, cudaStream_t stream) {
   p.cf_off = p.cdy_off + align_up(C * kV * 4, 128);
   p.cbuf_bytes = align_up(p.cf_off + C * 4, 128);
   p.xring_off = align_up(p.cbuf_off + kCBufs * p.cbuf_bytes, 1024);
-  p.hbuf_off = p.xring_off + kNX * kXSlotBytes;  // two buffers of C H tiles, then 2 KB of slack
-  p.dqp_off = p.hbuf_off + (2 * C + 1) * kHTileBytes;
+  p.hbuf_off = p.xring_off + kNX * kXSlotBytes;  // two buffers of C H tiles
+  p.dqp_off = p.hbuf_off + 2 * C * kHTileBytes;
   p.dwr_off = p.dqp_off + C * 16 * kRows * 4;
   p.bar_off = p.dwr_off + 4 * kV * 4;
   p.misc_off = p.bar_off + (2 * kCBufs + 4 + 2 * kNX + 1 + 2 + 2) * 8;
