@@ -348,6 +348,7 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
         uint32_t hr[8];
         tmem_ld_32x32b<8>(tt, hr);
         float yprev[4] = {0.f, 0.f, 0.f, 0.f};  // the previous step's share (stored one step late)
+        uint32_t qmag = 0u;                     // per-halfword max of the tile's |q| bits (bf16)
         uint32_t qlo = ld_shared_b32(qs + 4 * qd), qhi = ld_shared_b32(qs + 4 * qd + 16);
 #pragma unroll 2
         for (int s = 0; s < nsteps; ++s) {
@@ -361,17 +362,19 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
 #pragma unroll
           for (int i = 0; i < 8; ++i) hv[i] = __uint_as_float(hr[i]);
           tmem_ld_32x32b<8>(tt + kHCols * sn, hr);
-          const uint32_t qa[4] = {qlo, qlo, qhi, qhi};
+          // y in fp16 operands: H_t (|H| <= 1) to fp16 as in the state
+          // transform, q re-encoded from bf16 (exact below 65536 in
+          // magnitude; the tile's largest |q| is checked after the loop).
+          qmag = __vmaxu2(qmag, __vmaxu2(qlo & 0x7FFF7FFFu, qhi & 0x7FFF7FFFu));
+          const uint32_t qf0 = bf16x2_to_f16x2(qlo), qf1 = bf16x2_to_f16x2(qhi);
+          const uint32_t qa[4] = {qf0, qf0, qf1, qf1};
           float yd[2][4];
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
             const float* hn = hv + 4 * nt;
-            const uint32_t hi0 = pack2_bf16(hn[0], hn[1]);
-            const uint32_t hi1 = pack2_bf16(hn[2], hn[3]);
-            const uint32_t lo0 = pack2_bf16(hn[0] - bf16lo(hi0), hn[1] - bf16hi(hi0));
-            const uint32_t lo1 = pack2_bf16(hn[2] - bf16lo(hi1), hn[3] - bf16hi(hi1));
-            mma_bf16_16816_zc(yd[nt], qa, movmatrix_trans(hi0), movmatrix_trans(hi1));
-            mma_bf16_16816(yd[nt], qa, movmatrix_trans(lo0), movmatrix_trans(lo1));
+            yd[nt][0] = yd[nt][1] = yd[nt][2] = yd[nt][3] = 0.f;
+            mma_f16_16816(yd[nt], qa, movmatrix_trans(pack2_f16(hn[0], hn[1])),
+                          movmatrix_trans(pack2_f16(hn[2], hn[3])));
           }
           if (g == 0 && s > 0) {  // row 0 of the row-replicated result: columns 8nt + 2qd (+1)
             float* dst = sY + (ys * kS + s - 1) * kV + jcol0;
@@ -385,6 +388,8 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
           qlo = nqlo;
           qhi = nqhi;
         }
+        if ((qmag & 0xFFFFu) >= 0x4780u || (qmag >> 16) >= 0x4780u)  // |q| >= 65536 (or not finite)
+          report_device_error(status, kStatusCheck, kWhereQRange);
         if (g == 0 && nsteps > 0) {
           float* dst = sY + (ys * kS + nsteps - 1) * kV + jcol0;
           *reinterpret_cast<float2*>(dst) = make_float2(yprev[0], yprev[1]);

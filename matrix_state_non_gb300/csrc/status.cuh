@@ -28,6 +28,9 @@ constexpr uint32_t kWhereBwdFull = 201, kWhereBwdCEmpty = 202, kWhereBwdTReady =
 // Input checks: an entry of W outside the fp16 range (|W| >= 65520) that the
 // fp16 state-operand kernels cannot represent.
 constexpr uint32_t kWhereWRange = 301;
+// An entry of q with |q| >= 65536 (or not finite) in a forward whose readout
+// takes q as an fp16 operand (V = 64 warp-MMA forward with y).
+constexpr uint32_t kWhereQRange = 302;
 
 __device__ __forceinline__ void report_device_error(StatusBlock* s, unsigned int code,
                                                     uint32_t where) {

@@ -7,7 +7,7 @@ import pytest
 
 from matrix_state_non_gb300.inputs import make_inputs
 from oracle import forward as oracle_forward
-from parity_util import check_forward, gpu_forward, oracle_args
+from parity_util import TOL_BF16_REL, check_forward, gpu_forward, oracle_args, rel_fro
 
 pytestmark = pytest.mark.gpu
 
@@ -35,6 +35,39 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     got = gpu_forward(inp)  # the same context keeps working
     y_ref, H_ref = oracle_forward(*oracle_args(inp))
     check_forward(got, y_ref, H_ref, "bf16")
+
+
+def test_query_outside_fp16_range_is_reported():
+    """The V = 64 warp-MMA forward reads out y with q re-encoded as fp16; a
+    q entry of magnitude 65536 or more is reported through the status block
+    (location 302), and the next call on the same context is clean."""
+    import torch
+    from matrix_state_non_gb300 import binding
+    from matrix_state_non_gb300.inputs import f32_to_bf16_bits
+    inp = make_inputs(1, 2, 40, 64, 64, "bf16", seed=13)
+    inp.store["q"] = inp.store["q"].copy()
+    inp.store["q"][0, 33, 1, 7] = f32_to_bf16_bits(np.array([-70000.0], dtype=np.float32))[0]
+    d = binding.to_device(inp)
+    out = binding.forward(*(d[n] for n in NAMES))
+    st, detail = binding.sync_status(out["workspace"])
+    assert st == binding.M2RNN_ERR_DEVICE and detail == 302, (binding.status_string(st), detail)
+    # 65280, the largest bf16 magnitude below the limit, is accepted: no
+    # error, finite y, and y within the relative tolerance (its absolute
+    # error scales with that q, so only the relative bar applies).
+    edge = make_inputs(1, 2, 40, 64, 64, "bf16", seed=14)
+    edge.store["q"] = edge.store["q"].copy()
+    edge.store["q"][0, 5, 0, 3] = f32_to_bf16_bits(np.array([65280.0], dtype=np.float32))[0]
+    edge.exact["q"] = edge.exact["q"].copy()
+    edge.exact["q"][0, 5, 0, 3] = 65280.0
+    d = binding.to_device(edge)
+    out = binding.forward(*(d[n] for n in NAMES))
+    st, detail = binding.sync_status(out["workspace"])
+    assert st == binding.M2RNN_OK, (binding.status_string(st), detail)
+    y = out["y"].cpu().numpy()
+    assert np.isfinite(y).all()
+    y_ref, _ = oracle_forward(*oracle_args(edge))
+    assert rel_fro(y, y_ref) <= TOL_BF16_REL, rel_fro(y, y_ref)
+    torch.cuda.synchronize()
 
 
 @pytest.mark.parametrize("K,V", [(64, 64), (64, 16), (128, 128)])
