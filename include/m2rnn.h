@@ -41,12 +41,12 @@
  *    chunks on warp MMAs with its dW on tcgen05.  Every other supported
  *    shape runs on the fp32 CUDA-core kernels.  Nothing runs on the host
  *    CPU.
- *  - The tensor-core kernels take W re-encoded as fp16, and the V = 64
- *    warp-MMA forward reads out y with q as an fp16 operand: with bf16
- *    inputs, an entry with |W| >= 65520, or (that forward, y requested)
- *    |q| >= 65536, is reported by m2rnn_sync_status as M2RNN_ERR_DEVICE
- *    with location 301 (W) or 302 (q); the call's results are then not
- *    valid.
+ *  - The tensor-core kernels take W re-encoded as fp16, and the warp-MMA
+ *    forwards with readout warps (V = 64; V = 16 with K <= 64) read out y
+ *    with q as an fp16 operand: with bf16 inputs, an entry with
+ *    |W| >= 65520, or (those forwards, y requested) |q| >= 65536, is
+ *    reported by m2rnn_sync_status as M2RNN_ERR_DEVICE with location 301
+ *    (W) or 302 (q); the call's results are then not valid.
  */
 #ifndef M2RNN_H_
 #define M2RNN_H_

@@ -258,6 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t hr[8];
         tmem_ld_32x32b<8>(tt, hr);
         float yprev[4] = {0.f, 0.f, 0.f, 0.f};  // the previous step's share (stored one step late)
+        uint32_t qmag = 0u;                     // per-halfword max of the tile's |q| bits (bf16)
         // q of the block's rows 2qd.. and 2qd+8.. as bf16 pairs (A[m][k] =
         // q[k] for every m), loaded one step ahead.
         uint32_t qlo = ld_shared_b32(qs + 2 * (16 * w + 2 * qd));
@@ -273,17 +274,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 8; ++i) hh[i] = __uint_as_float(hr[i]);
           tmem_ld_32x32b<8>(tt + kHCols * (s + 1 < nsteps ? s + 1 : s), hr);
-          const uint32_t qa[4] = {qlo, qlo, qhi, qhi};
+          // y in fp16 operands: H_t (|H| <= 1) to fp16 as in the state
+          // transform, q re-encoded from bf16 (exact below 65536 in
+          // magnitude; the tile's largest |q| is checked after the loop).
+          qmag = __vmaxu2(qmag, __vmaxu2(qlo & 0x7FFF7FFFu, qhi & 0x7FFF7FFFu));
+          const uint32_t qf0 = bf16x2_to_f16x2(qlo), qf1 = bf16x2_to_f16x2(qhi);
+          const uint32_t qa[4] = {qf0, qf0, qf1, qf1};
           float yd[2][4];
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {  // H_t as bf16 high and low parts (~16 bits)
+          for (int nt = 0; nt < 2; ++nt) {
             const float* hn = hh + 4 * nt;
-            const uint32_t hi0 = pack2_bf16(hn[0], hn[1]);
-            const uint32_t hi1 = pack2_bf16(hn[2], hn[3]);
-            const uint32_t lo0 = pack2_bf16(hn[0] - bf16lo(hi0), hn[1] - bf16hi(hi0));
-            const uint32_t lo1 = pack2_bf16(hn[2] - bf16lo(hi1), hn[3] - bf16hi(hi1));
-            mma_bf16_16816_zc(yd[nt], qa, movmatrix_trans(hi0), movmatrix_trans(hi1));
-            mma_bf16_16816(yd[nt], qa, movmatrix_trans(lo0), movmatrix_trans(lo1));
+            yd[nt][0] = yd[nt][1] = yd[nt][2] = yd[nt][3] = 0.f;
+            mma_f16_16816(yd[nt], qa, movmatrix_trans(pack2_f16(hn[0], hn[1])),
+                          movmatrix_trans(pack2_f16(hn[2], hn[3])));
           }
           // The previous step's share (row 0 of the row-replicated result:
           // columns 8nt + 2qd, +1); its MMAs completed during this step.
@@ -299,6 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           qlo = nqlo;
           qhi = nqhi;
         }
+        if ((qmag & 0xFFFFu) >= 0x4780u || (qmag >> 16) >= 0x4780u)  // |q| >= 65536 (or not finite)
+          report_device_error(status, kStatusCheck, kWhereQRange);
         if (g == 0 && nsteps > 0) {
           float* dst = yp + ((nsteps - 1) * R + w) * kV + 2 * qd;
           *reinterpret_cast<float2*>(dst) = make_float2(yprev[0], yprev[1]);

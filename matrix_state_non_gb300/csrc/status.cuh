@@ -29,7 +29,8 @@ constexpr uint32_t kWhereBwdFull = 201, kWhereBwdCEmpty = 202, kWhereBwdTReady =
 // fp16 state-operand kernels cannot represent.
 constexpr uint32_t kWhereWRange = 301;
 // An entry of q with |q| >= 65536 (or not finite) in a forward whose readout
-// takes q as an fp16 operand (V = 64 warp-MMA forward with y).
+// takes q as an fp16 operand (the V = 64 and V = 16 warp-MMA forwards with
+// readout warps).
 constexpr uint32_t kWhereQRange = 302;
 
 __device__ __forceinline__ void report_device_error(StatusBlock* s, unsigned int code,

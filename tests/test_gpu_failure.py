@@ -37,14 +37,16 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     check_forward(got, y_ref, H_ref, "bf16")
 
 
-def test_query_outside_fp16_range_is_reported():
-    """The V = 64 warp-MMA forward reads out y with q re-encoded as fp16; a
-    q entry of magnitude 65536 or more is reported through the status block
-    (location 302), and the next call on the same context is clean."""
+@pytest.mark.parametrize("V", [64, 16])
+def test_query_outside_fp16_range_is_reported(V):
+    """The warp-MMA forwards with readout warps (V = 64, and V = 16 with
+    K <= 64) read out y with q re-encoded as fp16; a q entry of magnitude
+    65536 or more is reported through the status block (location 302), and
+    the next call on the same context is clean."""
     import torch
     from matrix_state_non_gb300 import binding
     from matrix_state_non_gb300.inputs import f32_to_bf16_bits
-    inp = make_inputs(1, 2, 40, 64, 64, "bf16", seed=13)
+    inp = make_inputs(1, 2, 40, 64, V, "bf16", seed=13)
     inp.store["q"] = inp.store["q"].copy()
     inp.store["q"][0, 33, 1, 7] = f32_to_bf16_bits(np.array([-70000.0], dtype=np.float32))[0]
     d = binding.to_device(inp)
@@ -54,7 +56,7 @@ def test_query_outside_fp16_range_is_reported():
     # 65280, the largest bf16 magnitude below the limit, is accepted: no
     # error, finite y, and y within the relative tolerance (its absolute
     # error scales with that q, so only the relative bar applies).
-    edge = make_inputs(1, 2, 40, 64, 64, "bf16", seed=14)
+    edge = make_inputs(1, 2, 40, 64, V, "bf16", seed=14)
     edge.store["q"] = edge.store["q"].copy()
     edge.store["q"][0, 5, 0, 3] = f32_to_bf16_bits(np.array([65280.0], dtype=np.float32))[0]
     edge.exact["q"] = edge.exact["q"].copy()
