@@ -33,9 +33,8 @@
  *    K a multiple of 16 (and at most 128) run on tensor-core kernels: V = 64
  *    with the forward on warp MMAs (tcgen05 on request) and the backward on
  *    warp MMAs (ckpt_every <= 20, its dW and its dk, dv on tensor cores),
- *    V = 16 on register-resident
- *    warp-MMA scans (the backward for ckpt_every <= 32, <= 16 with
- *    K > 64), V = 128: the forward (K in {32, 64, 128}) on tcgen05, the
+ *    V = 16 on warp-MMA scans with the state in registers (the backward
+ *    for ckpt_every <= 32, <= 16 with K > 64), V = 128: the forward (K in {32, 64, 128}) on tcgen05, the
  *    backward with K = 128 and ckpt_every <= 16 on tcgen05 (every product:
  *    the state-gradient chain, dW, dk, dv, dq), with other K or longer
  *    chunks on warp MMAs with its dW on tcgen05.  Every other supported
