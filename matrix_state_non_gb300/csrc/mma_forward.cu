@@ -20,10 +20,11 @@
 // the same scheduler and tensor-memory lane quadrant: the compute warp leaves
 // H_t (fp32, 8 columns per step) in a double-buffered tile of tensor memory,
 // and the readout warp, one tile of 32 steps behind, forms y^T = q^T H_t as
-// one m16n8k16 per column tile with q replicated over the A rows and H_t
-// (split into bf16 high and low parts, transposed into B fragments with
-// movmatrix) as B, so the sum over rows needs no shuffles; it stores each
-// step's share one step late, so that no step waits for its own MMAs.  A
+// one m16n8k16 per column tile with fp16 operands: q replicated over the A
+// rows (staged in fp16 by the producer warp, which checks its range) and
+// fp16 H_t, transposed into B fragments with movmatrix, as B, so the sum
+// over rows needs no shuffles; it stores each step's share one step late,
+// so that no step waits for its own MMAs.  A
 // dependent m16n8k16 takes ~21 cycles, while a 4-instruction tcgen05 step
 // costs several hundred cycles from issue to completion (measured on GB300).
 #include <cuda.h>
@@ -45,7 +46,8 @@ constexpr int kS = 32;      // steps per input tile
 constexpr int kNS = 4;      // input stages
 constexpr int kYS = 2;      // readout partial stages
 // Warps: 0-3 compute (8 / NT of them, each owning 8*NT of the 64 value
-// columns), 4-7 readout, 8 the TMA producer, 9 the readout reducer.
+// columns), 4-7 readout, 8 the producer (k, v by TMA; q and f by its
+// lanes), 9 the readout reducer.
 template <int NT>
 constexpr int kThreadsFor() { return 10 * 32; }
 constexpr int kReadoutWarp0 = 4, kProducerWarp = 8, kReducerWarp = 9;
@@ -69,8 +71,8 @@ struct MmaFwdParams {
 // so a chunk of steps is one contiguous range.
 template <int NT, bool kY, bool kCk, bool kZ>
 __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
-    mma_forward_kernel(const __grid_constant__ MmaFwdParams p, const __grid_constant__ CUtensorMap tm_q,
-                       const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
+    mma_forward_kernel(const __grid_constant__ MmaFwdParams p, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -348,7 +350,6 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
         uint32_t hr[8];
         tmem_ld_32x32b<8>(tt, hr);
         float yprev[4] = {0.f, 0.f, 0.f, 0.f};  // the previous step's share (stored one step late)
-        uint32_t qmag = 0u;                     // per-halfword max of the tile's |q| bits (bf16)
         uint32_t qlo = ld_shared_b32(qs + 4 * qd), qhi = ld_shared_b32(qs + 4 * qd + 16);
 #pragma unroll 2
         for (int s = 0; s < nsteps; ++s) {
@@ -363,11 +364,8 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
           for (int i = 0; i < 8; ++i) hv[i] = __uint_as_float(hr[i]);
           tmem_ld_32x32b<8>(tt + kHCols * sn, hr);
           // y in fp16 operands: H_t (|H| <= 1) to fp16 as in the state
-          // transform, q re-encoded from bf16 (exact below 65536 in
-          // magnitude; the tile's largest |q| is checked after the loop).
-          qmag = __vmaxu2(qmag, __vmaxu2(qlo & 0x7FFF7FFFu, qhi & 0x7FFF7FFFu));
-          const uint32_t qf0 = bf16x2_to_f16x2(qlo), qf1 = bf16x2_to_f16x2(qhi);
-          const uint32_t qa[4] = {qf0, qf0, qf1, qf1};
+          // transform; q as staged in fp16 by the producer.
+          const uint32_t qa[4] = {qlo, qlo, qhi, qhi};
           float yd[2][4];
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
@@ -388,8 +386,6 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
           qlo = nqlo;
           qhi = nqhi;
         }
-        if ((qmag & 0xFFFFu) >= 0x4780u || (qmag >> 16) >= 0x4780u)  // |q| >= 65536 (or not finite)
-          report_device_error(status, kStatusCheck, kWhereQRange);
         if (g == 0 && nsteps > 0) {
           float* dst = sY + (ys * kS + nsteps - 1) * kV + jcol0;
           *reinterpret_cast<float2*>(dst) = make_float2(yprev[0], yprev[1]);
@@ -410,9 +406,8 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
     }
     if (*rabort) *abort_flag = 1;
   } else if (warp == kProducerWarp) {
-    // ---------------- TMA producer ----------------
+    // ---------------- producer ----------------
     if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
     }
@@ -435,11 +430,36 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
       float fv = 0.f;
       if (t0 + lane < T) fv = gate_value(gs, (static_cast<int64_t>(b) * T + t0 + lane) * N + n, n);
       reinterpret_cast<float*>(stage + p.f_off)[lane] = fv;
+      if constexpr (kY) {
+        // q of step t0 + lane (the CTA's 16 rows), re-encoded as fp16 for
+        // the readout's MMA once here instead of at every readout step; a
+        // magnitude the fp16 operand cannot hold is reported.
+        uint4 qv[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+        if (t0 + lane < T) {
+          const uint4* src = reinterpret_cast<const uint4*>(
+              static_cast<const uint16_t*>(p.a.q) +
+              ((static_cast<int64_t>(b) * T + t0 + lane) * qk_heads(p.a.qkN, N) + qk_head(p.a.qkN, n)) * p.a.K +
+              cta_rank * kRows);
+          qv[0] = src[0];
+          qv[1] = src[1];
+        }
+        uint32_t mag = 0u;
+        uint32_t* qw = reinterpret_cast<uint32_t*>(qv);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          mag = __vmaxu2(mag, qw[i] & 0x7FFF7FFFu);
+          qw[i] = bf16x2_to_f16x2(qw[i]);
+        }
+        if ((mag & 0xFFFFu) >= 0x4780u || (mag >> 16) >= 0x4780u)  // |q| >= 65536 (or not finite)
+          report_device_error(status, kStatusCheck, kWhereQRange);
+        uint4* dst = reinterpret_cast<uint4*>(stage + p.q_off + lane * kRows * 2);
+        dst[0] = qv[0];
+        dst[1] = qv[1];
+      }
       __syncwarp();
       const uint32_t fb = smem_u32(&full[st]);
       if (lane == 0) {
         mbar_arrive_expect_tx(fb, p.tx_bytes);
-        tma_load_4d(smem_u32(stage + p.q_off), &tm_q, fb, cta_rank * kRows, qk_head(p.a.qkN, n), t0, b);
         tma_load_4d(smem_u32(stage + p.k_off), &tm_k, fb, cta_rank * kRows, qk_head(p.a.qkN, n), t0, b);
         tma_load_4d(smem_u32(stage + p.v_off), &tm_v, fb, 0, n, t0, b);
       } else {
@@ -534,13 +554,12 @@ cudaError_t launch_nt(const FwdArgs& a, cudaStream_t stream) {
   p.misc_off = p.bar_off + (2 * kNS + 3 * kYS + 16) * 8;
   uint32_t smem = align_up(p.misc_off + 16, 128) + 1024;  // + the 1 KB alignment slack
   smem = std::max<uint32_t>(smem, 120 * 1024);  // one CTA per SM
-  p.tx_bytes = 2 * kS * kRows * 2 + kS * kV * 2;
+  p.tx_bytes = kS * kRows * 2 + kS * kV * 2;  // k and v by TMA (q is staged by the producer's lanes)
 
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mk, mv;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int qN = qk_heads(a.qkN, a.N);
-  if (!make_tensor_map_btnx(&mq, a.q, bf, 2, a.B, a.T, qN, a.K, kRows, kS) ||
-      !make_tensor_map_btnx(&mk, a.k, bf, 2, a.B, a.T, qN, a.K, kRows, kS) ||
+  if (!make_tensor_map_btnx(&mk, a.k, bf, 2, a.B, a.T, qN, a.K, kRows, kS) ||
       !make_tensor_map_btnx(&mv, a.v, bf, 2, a.B, a.T, a.N, kV, kV, kS))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(mma_forward_kernel<NT, kY, kCk, kZ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -558,7 +577,7 @@ cudaError_t launch_nt(const FwdArgs& a, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, mma_forward_kernel<NT, kY, kCk, kZ>, p, mq, mk, mv);
+  e = cudaLaunchKernelEx(&cfg, mma_forward_kernel<NT, kY, kCk, kZ>, p, mk, mv);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

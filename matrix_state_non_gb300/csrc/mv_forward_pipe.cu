@@ -11,14 +11,15 @@
 //     blend); it leaves H_t (fp32) in a double-buffered tile of tensor
 //     memory, 8 columns per step, and writes checkpoints and the Z stash;
 //   readout warp: one tile of 32 steps behind, the block's share of
-//     y_t = H_t^T q_t on the tensor core (q replicated over the A rows, H_t as
-//     B in bf16 high and low parts, transposed with movmatrix), stored one
+//     y_t = H_t^T q_t on the tensor core with fp16 operands (q replicated
+//     over the A rows, H_t as B, transposed with movmatrix), stored one
 //     step late so that no step waits for its own MMA; at the end of a tile
 //     the readout warps add the row blocks' shares in a fixed order, plus
 //     w_r * v_t, and write y.
 // The compute warps never stop for the readout or for each other.  A
-// producer warp streams q, k, v by TMA (f by plain loads) into a ring of
-// input stages that the readout warps release.  Every wait is bounded.
+// producer warp streams k, v by TMA into a ring of input stages that the
+// readout warps release; its lanes load f and q (q re-encoded as fp16, its
+// range checked).  Every wait is bounded.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -49,8 +50,8 @@ struct MvFwdPipeParams {
 
 template <bool kCk, bool kZ>
 __global__ void __launch_bounds__(kThreads, 1)
-    mv_forward_pipe_kernel(const __grid_constant__ MvFwdPipeParams p, const __grid_constant__ CUtensorMap tm_q,
-                           const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
+    mv_forward_pipe_kernel(const __grid_constant__ MvFwdPipeParams p, const __grid_constant__ CUtensorMap tm_k,
+                           const __grid_constant__ CUtensorMap tm_v) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const FwdArgs& A = p.a;
@@ -258,7 +259,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t hr[8];
         tmem_ld_32x32b<8>(tt, hr);
         float yprev[4] = {0.f, 0.f, 0.f, 0.f};  // the previous step's share (stored one step late)
-        uint32_t qmag = 0u;                     // per-halfword max of the tile's |q| bits (bf16)
         // q of the block's rows 2qd.. and 2qd+8.. as bf16 pairs (A[m][k] =
         // q[k] for every m), loaded one step ahead.
         uint32_t qlo = ld_shared_b32(qs + 2 * (16 * w + 2 * qd));
@@ -275,11 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 8; ++i) hh[i] = __uint_as_float(hr[i]);
           tmem_ld_32x32b<8>(tt + kHCols * (s + 1 < nsteps ? s + 1 : s), hr);
           // y in fp16 operands: H_t (|H| <= 1) to fp16 as in the state
-          // transform, q re-encoded from bf16 (exact below 65536 in
-          // magnitude; the tile's largest |q| is checked after the loop).
-          qmag = __vmaxu2(qmag, __vmaxu2(qlo & 0x7FFF7FFFu, qhi & 0x7FFF7FFFu));
-          const uint32_t qf0 = bf16x2_to_f16x2(qlo), qf1 = bf16x2_to_f16x2(qhi);
-          const uint32_t qa[4] = {qf0, qf0, qf1, qf1};
+          // transform; q as staged in fp16 by the producer.
+          const uint32_t qa[4] = {qlo, qlo, qhi, qhi};
           float yd[2][4];
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
@@ -302,8 +299,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           qlo = nqlo;
           qhi = nqhi;
         }
-        if ((qmag & 0xFFFFu) >= 0x4780u || (qmag >> 16) >= 0x4780u)  // |q| >= 65536 (or not finite)
-          report_device_error(status, kStatusCheck, kWhereQRange);
         if (g == 0 && nsteps > 0) {
           float* dst = yp + ((nsteps - 1) * R + w) * kV + 2 * qd;
           *reinterpret_cast<float2*>(dst) = make_float2(yprev[0], yprev[1]);
@@ -333,9 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (*rabort) *abort_flag = 1;
   } else if (warp == 8) {
-    // ---------------- TMA producer ----------------
+    // ---------------- producer (k, v by TMA; q and f by its lanes) ----------------
     if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
     }
@@ -354,11 +348,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       float fv = 0.f;
       if (t0 + lane < T) fv = gate_value(gs, (static_cast<int64_t>(b) * T + t0 + lane) * N + n, n);
       reinterpret_cast<float*>(stage + p.f_off)[lane] = fv;
+      {
+        // q of step t0 + lane (all K rows), re-encoded as fp16 for the
+        // readout's MMA once here instead of at every readout step; a
+        // magnitude the fp16 operand cannot hold is reported.
+        const uint4* src = reinterpret_cast<const uint4*>(
+            static_cast<const uint16_t*>(A.q) +
+            ((static_cast<int64_t>(b) * T + t0 + lane) * qk_heads(A.qkN, N) + qk_head(A.qkN, n)) * K);
+        uint4* dst = reinterpret_cast<uint4*>(stage + p.q_off + lane * K * 2);
+        uint32_t mag = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {  // K / 8 pieces of 16 bytes, K <= 64
+          if (i < K / 8) {
+            uint4 qv = t0 + lane < T ? src[i] : make_uint4(0u, 0u, 0u, 0u);
+            mag = __vmaxu2(mag, __vmaxu2(qv.x & 0x7FFF7FFFu, qv.y & 0x7FFF7FFFu));
+            mag = __vmaxu2(mag, __vmaxu2(qv.z & 0x7FFF7FFFu, qv.w & 0x7FFF7FFFu));
+            qv = make_uint4(bf16x2_to_f16x2(qv.x), bf16x2_to_f16x2(qv.y), bf16x2_to_f16x2(qv.z),
+                            bf16x2_to_f16x2(qv.w));
+            dst[i] = qv;
+          }
+        }
+        if ((mag & 0xFFFFu) >= 0x4780u || (mag >> 16) >= 0x4780u)  // |q| >= 65536 (or not finite)
+          report_device_error(status, kStatusCheck, kWhereQRange);
+      }
       __syncwarp();
       const uint32_t fb = smem_u32(&full[st]);
       if (lane == 0) {
         mbar_arrive_expect_tx(fb, p.tx_bytes);
-        tma_load_4d(smem_u32(stage + p.q_off), &tm_q, fb, 0, qk_head(A.qkN, n), t0, b);
         tma_load_4d(smem_u32(stage + p.k_off), &tm_k, fb, 0, qk_head(A.qkN, n), t0, b);
         tma_load_4d(smem_u32(stage + p.v_off), &tm_v, fb, 0, n, t0, b);
       } else {
@@ -382,12 +398,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
 template <bool kCk, bool kZ>
-cudaError_t launch_t(const MvFwdPipeParams& p, uint32_t smem, cudaStream_t stream, const CUtensorMap& mq,
-                     const CUtensorMap& mk, const CUtensorMap& mv) {
+cudaError_t launch_t(const MvFwdPipeParams& p, uint32_t smem, cudaStream_t stream, const CUtensorMap& mk,
+                     const CUtensorMap& mv) {
   auto kernel = mv_forward_pipe_kernel<kCk, kZ>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kernel<<<p.a.B * p.a.N, kThreads, smem, stream>>>(p, mq, mk, mv);
+  kernel<<<p.a.B * p.a.N, kThreads, smem, stream>>>(p, mk, mv);
   return cudaGetLastError();
 }
 
@@ -413,18 +429,17 @@ cudaError_t launch_mv_forward_pipe(const FwdArgs& a, cudaStream_t stream) {
   p.bar_off = p.y_off + 2 * kS * p.R * kV * 4;
   p.misc_off = p.bar_off + (2 * kNS + 16) * 8;
   const uint32_t smem = align_up(p.misc_off + 16, 128);
-  p.tx_bytes = 2 * kS * a.K * 2 + kS * kV * 2;
+  p.tx_bytes = kS * a.K * 2 + kS * kV * 2;  // k and v by TMA (q is staged by the producer's lanes)
 
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mk, mv;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int qN = qk_heads(a.qkN, a.N);
-  if (!make_tensor_map_btnx(&mq, a.q, bf, 2, a.B, a.T, qN, a.K, a.K, kS) ||
-      !make_tensor_map_btnx(&mk, a.k, bf, 2, a.B, a.T, qN, a.K, a.K, kS) ||
+  if (!make_tensor_map_btnx(&mk, a.k, bf, 2, a.B, a.T, qN, a.K, a.K, kS) ||
       !make_tensor_map_btnx(&mv, a.v, bf, 2, a.B, a.T, a.N, kV, kV, kS))
     return cudaErrorInvalidValue;
   const bool ck = a.ckpt != nullptr, z = a.zstash != nullptr;
-  if (z) return ck ? launch_t<true, true>(p, smem, stream, mq, mk, mv) : launch_t<false, true>(p, smem, stream, mq, mk, mv);
-  return ck ? launch_t<true, false>(p, smem, stream, mq, mk, mv) : launch_t<false, false>(p, smem, stream, mq, mk, mv);
+  if (z) return ck ? launch_t<true, true>(p, smem, stream, mk, mv) : launch_t<false, true>(p, smem, stream, mk, mv);
+  return ck ? launch_t<true, false>(p, smem, stream, mk, mv) : launch_t<false, false>(p, smem, stream, mk, mv);
 }
 
 }  // namespace m2rnn
