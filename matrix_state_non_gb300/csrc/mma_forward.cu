@@ -370,9 +370,8 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
             const float* hn = hv + 4 * nt;
-            yd[nt][0] = yd[nt][1] = yd[nt][2] = yd[nt][3] = 0.f;
-            mma_f16_16816(yd[nt], qa, movmatrix_trans(pack2_f16(hn[0], hn[1])),
-                          movmatrix_trans(pack2_f16(hn[2], hn[3])));
+            mma_f16_16816_zc(yd[nt], qa, movmatrix_trans(pack2_f16(hn[0], hn[1])),
+                             movmatrix_trans(pack2_f16(hn[2], hn[3])));
           }
           if (g == 0 && s > 0) {  // row 0 of the row-replicated result: columns 8nt + 2qd (+1)
             float* dst = sY + (ys * kS + s - 1) * kV + jcol0;

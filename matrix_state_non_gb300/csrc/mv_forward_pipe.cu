@@ -281,9 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
             const float* hn = hh + 4 * nt;
-            yd[nt][0] = yd[nt][1] = yd[nt][2] = yd[nt][3] = 0.f;
-            mma_f16_16816(yd[nt], qa, movmatrix_trans(pack2_f16(hn[0], hn[1])),
-                          movmatrix_trans(pack2_f16(hn[2], hn[3])));
+            mma_f16_16816_zc(yd[nt], qa, movmatrix_trans(pack2_f16(hn[0], hn[1])),
+                             movmatrix_trans(pack2_f16(hn[2], hn[3])));
           }
           // The previous step's share (row 0 of the row-replicated result:
           // columns 8nt + 2qd, +1); its MMAs completed during this step.
