@@ -18,11 +18,12 @@
 // shared tile that the four warps read back with ldmatrix after one named
 // barrier.  The readout runs on four readout warps, one per compute warp on
 // the same scheduler and tensor-memory lane quadrant: the compute warp leaves
-// H_t (fp32, 8 columns per step) in a double-buffered tile of tensor memory,
+// H_t (its fp16 A-operand pairs, 4 columns per step) in a double-buffered
+// tile of tensor memory,
 // and the readout warp, one tile of 32 steps behind, forms y^T = q^T H_t as
 // one m16n8k16 per column tile with fp16 operands: q replicated over the A
 // rows (staged in fp16 by the producer warp, which checks its range) and
-// fp16 H_t, transposed into B fragments with movmatrix, as B, so the sum
+// those H_t pairs, transposed into B fragments with movmatrix, as B, so the sum
 // over rows needs no shuffles; it stores each step's share one step late,
 // so that no step waits for its own MMAs.  A
 // dependent m16n8k16 takes ~21 cycles, while a 4-instruction tcgen05 step
@@ -51,7 +52,7 @@ constexpr int kYS = 2;      // readout partial stages
 template <int NT>
 constexpr int kThreadsFor() { return 10 * 32; }
 constexpr int kReadoutWarp0 = 4, kProducerWarp = 8, kReducerWarp = 9;
-constexpr int kHCols = 8;  // tensor-memory columns per step of H_t (fp32, accumulator-fragment order)
+constexpr int kHCols = 4;  // tensor-memory columns per step of H_t (fp16 pairs, the exchange's A-fragment order)
 
 struct MmaFwdParams {
   FwdArgs a;
@@ -278,12 +279,9 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
             st_global_cs_v4(zst + static_cast<int64_t>(t) * kZStepBytes,
                             make_uint4(pack2_f16(zv[0][0], zv[0][1]), pack2_f16(zv[0][2], zv[0][3]),
                                        pack2_f16(zv[1][0], zv[1][1]), pack2_f16(zv[1][2], zv[1][3])));
-          if constexpr (kY) {  // H_t for the readout warp
-            const uint32_t hv[8] = {__float_as_uint(h[0][0]), __float_as_uint(h[0][1]), __float_as_uint(h[0][2]),
-                                    __float_as_uint(h[0][3]), __float_as_uint(h[1][0]), __float_as_uint(h[1][1]),
-                                    __float_as_uint(h[1][2]), __float_as_uint(h[1][3])};
-            tmem_st_32x32b_x8(tt + kHCols * s, hv);
-          }
+          // H_t for the readout warp: the fp16 pairs just packed as the next
+          // step's A operand, which are also the readout's B operand.
+          if constexpr (kY) tmem_st_32x32b_x4(tt + kHCols * s, hh);
           named_bar_sync(1, CT);
         }
         if constexpr (kCk) {
@@ -347,8 +345,8 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
       if (mine) {
         tc_fence_after_sync();
         const uint32_t tt = th + static_cast<uint32_t>(hb * kS * kHCols);
-        uint32_t hr[8];
-        tmem_ld_32x32b<8>(tt, hr);
+        uint32_t hr[4];
+        tmem_ld_32x32b<4>(tt, hr);
         float yprev[4] = {0.f, 0.f, 0.f, 0.f};  // the previous step's share (stored one step late)
         uint32_t qlo = ld_shared_b32(qs + 4 * qd), qhi = ld_shared_b32(qs + 4 * qd + 16);
 #pragma unroll 2
@@ -359,20 +357,15 @@ __global__ void __launch_bounds__(kThreadsFor<NT>(), 1)
           const uint32_t nqhi = ld_shared_b32(qs + 2 * (sn * kRows + 2 * qd + 8));
           tmem_ld_wait();
           tmem_ld_fence_regs(hr);
-          float hv[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) hv[i] = __uint_as_float(hr[i]);
-          tmem_ld_32x32b<8>(tt + kHCols * sn, hr);
+          const uint32_t hc[4] = {hr[0], hr[1], hr[2], hr[3]};  // H_t, fp16 pairs
+          tmem_ld_32x32b<4>(tt + kHCols * sn, hr);
           // y in fp16 operands: H_t (|H| <= 1) to fp16 as in the state
           // transform; q as staged in fp16 by the producer.
           const uint32_t qa[4] = {qlo, qlo, qhi, qhi};
           float yd[2][4];
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            const float* hn = hv + 4 * nt;
-            mma_f16_16816_zc(yd[nt], qa, movmatrix_trans(pack2_f16(hn[0], hn[1])),
-                             movmatrix_trans(pack2_f16(hn[2], hn[3])));
-          }
+          for (int nt = 0; nt < 2; ++nt)
+            mma_f16_16816_zc(yd[nt], qa, movmatrix_trans(hc[2 * nt]), movmatrix_trans(hc[2 * nt + 1]));
           if (g == 0 && s > 0) {  // row 0 of the row-replicated result: columns 8nt + 2qd (+1)
             float* dst = sY + (ys * kS + s - 1) * kV + jcol0;
             *reinterpret_cast<float2*>(dst) = make_float2(yprev[0], yprev[1]);

@@ -8,8 +8,9 @@
 //   compute warp: the recurrence, as in the register-resident kernel (two
 //     m16n8k16 MMAs per step with W in registers and the warp's own fp16 H
 //     block as the A operand, seeded with k v^T, then tanh and the gate
-//     blend); it leaves H_t (fp32) in a double-buffered tile of tensor
-//     memory, 8 columns per step, and writes checkpoints and the Z stash;
+//     blend); it leaves H_t (its fp16 A-operand pairs) in a double-buffered
+//     tile of tensor memory, 4 columns per step, and writes checkpoints and
+//     the Z stash;
 //   readout warp: one tile of 32 steps behind, the block's share of
 //     y_t = H_t^T q_t on the tensor core with fp16 operands (q replicated
 //     over the A rows, H_t as B, transposed with movmatrix), stored one
@@ -37,7 +38,7 @@ constexpr int kV = 16;
 constexpr int kRows = 16;
 constexpr int kS = 32;       // steps per input tile
 constexpr int kNS = 4;       // input stages: read out, computed, loading, spare
-constexpr int kHCols = 8;    // TMEM columns per step (H_t, fp32, accumulator-fragment order)
+constexpr int kHCols = 4;    // TMEM columns per step (H_t as fp16 pairs, the A-fragment order)
 constexpr int kThreads = 9 * 32;
 
 struct MvFwdPipeParams {
@@ -191,12 +192,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               h[nt][e] = fmaf(omf, zv[nt][e] - h[nt][e], h[nt][e]);  // Eq. 11
             }
           split();
-          {  // H_t for the readout warp
-            const uint32_t hv[8] = {__float_as_uint(h[0][0]), __float_as_uint(h[0][1]), __float_as_uint(h[0][2]),
-                                    __float_as_uint(h[0][3]), __float_as_uint(h[1][0]), __float_as_uint(h[1][1]),
-                                    __float_as_uint(h[1][2]), __float_as_uint(h[1][3])};
-            tmem_st_32x32b_x8(tt + kHCols * s, hv);
-          }
+          // H_t for the readout warp: the fp16 pairs just packed as the next
+          // step's A operand, which are also the readout's B operand.
+          tmem_st_32x32b_x4(tt + kHCols * s, hown);
           if constexpr (kZ)  // Z_t for the backward (a streaming store, off the chain)
             st_global_cs_v4(zst + static_cast<int64_t>(t0 + s) * R * 512,
                             make_uint4(pack2_f16(zv[0][0], zv[0][1]), pack2_f16(zv[0][2], zv[0][3]),
@@ -256,8 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (mine) {
         tc_fence_after_sync();
         const uint32_t tt = th + static_cast<uint32_t>(hb * kS * kHCols);
-        uint32_t hr[8];
-        tmem_ld_32x32b<8>(tt, hr);
+        uint32_t hr[4];
+        tmem_ld_32x32b<4>(tt, hr);
         float yprev[4] = {0.f, 0.f, 0.f, 0.f};  // the previous step's share (stored one step late)
         // q of the block's rows 2qd.. and 2qd+8.. as bf16 pairs (A[m][k] =
         // q[k] for every m), loaded one step ahead.
@@ -270,20 +268,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t nqhi = ld_shared_b32(qs + 2 * (sn * K + 16 * w + 2 * qd + 8));
           tmem_ld_wait();
           tmem_ld_fence_regs(hr);
-          float hh[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) hh[i] = __uint_as_float(hr[i]);
-          tmem_ld_32x32b<8>(tt + kHCols * (s + 1 < nsteps ? s + 1 : s), hr);
+          const uint32_t hc[4] = {hr[0], hr[1], hr[2], hr[3]};  // H_t, fp16 pairs
+          tmem_ld_32x32b<4>(tt + kHCols * (s + 1 < nsteps ? s + 1 : s), hr);
           // y in fp16 operands: H_t (|H| <= 1) to fp16 as in the state
           // transform; q as staged in fp16 by the producer.
           const uint32_t qa[4] = {qlo, qlo, qhi, qhi};
           float yd[2][4];
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            const float* hn = hh + 4 * nt;
-            mma_f16_16816_zc(yd[nt], qa, movmatrix_trans(pack2_f16(hn[0], hn[1])),
-                             movmatrix_trans(pack2_f16(hn[2], hn[3])));
-          }
+          for (int nt = 0; nt < 2; ++nt)
+            mma_f16_16816_zc(yd[nt], qa, movmatrix_trans(hc[2 * nt]), movmatrix_trans(hc[2 * nt + 1]));
           // The previous step's share (row 0 of the row-replicated result:
           // columns 8nt + 2qd, +1); its MMAs completed during this step.
           if (g == 0 && s > 0) {
