@@ -239,3 +239,28 @@ def test_options_start_from_the_environment(root_dir):
                          timeout=120)
     assert out.returncode == 0, out.stderr
     assert out.stdout.split() == ["0", "3"]
+
+
+def test_fp16_operand_range_limits():
+    """The range limits the kernels check for their fp16 operands (W: the
+    location-301 check; q in the warp-MMA readouts: location 302, which
+    compares the bf16 magnitude bits with 0x4780) are where fp16 stops
+    holding the value: 0x4780 is bf16 65536, which fp16 rounds to infinity,
+    while 65280, the bf16 value just below, is exact in fp16; for W (any
+    real input) fp16 overflows from 65520 on."""
+    import numpy as np
+    bf16_bits_to_f32 = lambda b: np.array([b << 16], dtype=np.uint32).view(np.float32)[0]
+    assert bf16_bits_to_f32(0x4780) == 65536.0
+    assert bf16_bits_to_f32(0x477F) == 65280.0
+    with np.errstate(over="ignore"):
+        assert np.isinf(np.float16(np.float32(65536.0)))
+        assert np.float16(np.float32(65280.0)) == 65280.0
+        assert np.isinf(np.float16(np.float32(65520.0)))
+        assert np.isfinite(np.float16(np.float32(65519.0)))
+    # Every bf16 magnitude pattern below 0x4780 is finite in fp16, and none
+    # at or above it (0x7F80 and up are infinities and NaNs).
+    bits = np.arange(0x0000, 0x7F80, dtype=np.uint32)
+    vals = (bits << 16).view(np.float32)
+    with np.errstate(over="ignore"):
+        finite = np.isfinite(vals.astype(np.float16))
+    assert finite[bits < 0x4780].all() and not finite[bits >= 0x4780].any()
